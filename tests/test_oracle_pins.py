@@ -1,0 +1,419 @@
+"""Pins of the C oracle against values and properties that do not come from itself.
+
+Each test states what fixes the expected value: a hand-worked case, a closed form,
+an independent brute force, or an invariant of the definition. A plausible mistake
+in the oracle (a dropped term, a wrong sign or index, a transposed operand, a wrong
+tie rule) fails at least one of them.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+from routed_expert_ffn_grouped_b300 import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------- int4 unpacking
+def test_unpack_hand_bytes(orc):
+    # Hand-decoded bytes: low nibble is the even element, code = nibble - 8.
+    b = np.array([0x00, 0xFF, 0x8F, 0x08, 0x80, 0x7A], np.uint8)
+    want = [-8, -8, 7, 7, 7, 0, 0, -8, -8, 0, 2, -1]
+    assert orc.unpack_int4(b).tolist() == want
+
+
+def test_unpack_exhaustive_roundtrip(orc):
+    b = np.arange(256, dtype=np.uint8)
+    q = orc.unpack_int4(b).reshape(256, 2).astype(np.int64)
+    # Inverse map written as packing: byte = (lo + 8) + 16 * (hi + 8).
+    assert ((q[:, 0] + 8) + 16 * (q[:, 1] + 8)).tolist() == list(range(256))
+    # Every code in [-8, 7] appears 16 times in each position.
+    for pos in range(2):
+        vals, counts = np.unique(q[:, pos], return_counts=True)
+        assert vals.tolist() == list(range(-8, 8)) and set(counts.tolist()) == {16}
+
+
+# ---------------------------------------------------------------- q8 quantiser
+def test_q8_hand_cases(orc):
+    # amax = 127 gives d = 1 exactly, so the codes are roundf of the values themselves.
+    g = np.zeros(32, np.float32)
+    g[:8] = [127.0, -127.0, 2.5, -2.5, 0.49, -0.5, 3.5, 1.0]
+    q, s = orc.q8_quantize(g[None])
+    assert s[0, 0] == np.float32(1.0)
+    assert q[0, :8].tolist() == [127, -127, 3, -3, 0, -1, 4, 1]   # halves away from zero
+    assert q[0, 8:].tolist() == [0] * 24
+
+
+def test_q8_zero_group_and_scale(orc):
+    x = np.zeros((2, 64), np.float32)
+    x[1, 32:] = np.linspace(-3, 5, 32, dtype=np.float32)
+    q, s = orc.q8_quantize(x)
+    assert s[0].tolist() == [0.0, 0.0] and not q[0].any()
+    assert s[1, 0] == 0.0 and not q[1, :32].any()
+    assert s[1, 1] == np.float32(np.float32(5.0) / np.float32(127.0))
+    assert q[1, 63] == 127          # the group's absmax maps to the top code
+
+
+def test_q8_bound_bruteforce(orc):
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((64, 256)) * rng.uniform(0.01, 100, (64, 1))).astype(np.float32)
+    q, s = orc.q8_quantize(x)
+    assert q.min() >= -127 and q.max() <= 127
+    d = np.repeat(s.astype(np.float64), 32, axis=1)
+    err = np.abs(x.astype(np.float64) - q * d)
+    assert np.all(err <= d / 2 * (1 + 1e-6) + 1e-30)
+    # Each group's absmax element maps to +-127.
+    xg = np.abs(x.reshape(64, 8, 32))
+    qg = np.abs(q.reshape(64, 8, 32).astype(np.int32))
+    am = xg.argmax(-1)
+    assert np.all(np.take_along_axis(qg, am[..., None], -1) == 127)
+
+
+def test_q8_rejects_ragged(orc):
+    with pytest.raises(ValueError):
+        orc.q8_quantize(np.zeros((1, 33), np.float32))
+
+
+# ---------------------------------------------------------------- integer group dots
+def test_group_dots_closed_forms(orc):
+    qa = np.full(64, 127, np.int8)
+    assert orc.group_dots(np.full((1, 32), 0xFF, np.uint8), qa).tolist() == [[7 * 127 * 32] * 2]
+    qa = np.full(64, -127, np.int8)
+    assert orc.group_dots(np.zeros((1, 32), np.uint8), qa).tolist() == [[32512, 32512]]
+    # Only element 1 of group 1 set (high nibble of byte 16): w=+7 there, -8 elsewhere.
+    w = np.full((1, 32), 0x88, np.uint8)         # all codes 0
+    w[0, 16] = 0xF8                               # element 33 -> +7, element 32 -> 0
+    qa = np.arange(64, dtype=np.int8)
+    assert orc.group_dots(w, qa).tolist() == [[0, 7 * 33]]
+
+
+def test_group_dots_bruteforce(orc):
+    rng = np.random.default_rng(2)
+    w = rng.integers(0, 256, (7, 96), dtype=np.uint8)       # 7 rows x 192 columns
+    qa = rng.integers(-127, 128, 192).astype(np.int8)
+    # Independent unpack via bit slicing of the whole matrix.
+    lo = (w & 15).astype(np.int64) - 8
+    hi = (w >> 4).astype(np.int64) - 8
+    full = np.stack([lo, hi], -1).reshape(7, 192)
+    want = (full * qa.astype(np.int64)).reshape(7, 6, 32).sum(-1)
+    assert np.array_equal(orc.group_dots(w, qa), want)
+
+
+# ---------------------------------------------------------------- router logits
+def test_router_logits_error_bound(orc):
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((3, 2048)).astype(np.float32)
+    Wr = (rng.standard_normal((10, 2048)) * 0.05).astype(np.float32)
+    got = orc.router_logits(x, Wr).astype(np.float64)
+    exact = x.astype(np.float64) @ Wr.astype(np.float64).T
+    mag = np.abs(x.astype(np.float64)) @ np.abs(Wr.astype(np.float64)).T
+    # 64 fmaf steps per chain + 5 tree levels, each one rounding of at most 2^-24.
+    assert np.all(np.abs(got - exact) <= (2048 / 32 + 5) * 2.0 ** -24 * mag * 1.01)
+
+
+def test_router_logits_order_matters_and_is_fixed(orc):
+    # Terms chosen so that a naive left-to-right fp32 sum and the strided order differ;
+    # the fixed order's value is worked by hand: chain j=0 sums 2^24 then +1 (lost to
+    # rounding) then -2^24 = 0; chain 1 holds 1 -> tree total 1.
+    x = np.zeros((1, 96), np.float32)
+    Wr = np.zeros((1, 96), np.float32)
+    x[0, [0, 32, 64, 1]] = [2.0 ** 24, 1.0, -(2.0 ** 24), 1.0]
+    Wr[0, [0, 32, 64, 1]] = 1.0
+    assert orc.router_logits(x, Wr)[0, 0] == np.float32(1.0)
+
+
+# ---------------------------------------------------------------- router selection
+def _cfg(**kw):
+    base = dict(name="t", d=32, ffn=32, n_exp=8, top_k=2, n_group=4, topk_group=2,
+                router="sigmoid", norm_topk=True, routed_scale=2.5, has_shared=False, shared_ffn=0,
+                bias="none")
+    base.update(kw)
+    return synth.LayerSpec(**base)
+
+
+def test_router_group_top2_sum_hand_case(orc):
+    # Logits 0 give s = 0.5 for every expert, so c = 0.5 + bias. Group scores (top-2 sums):
+    # g0 = 0.9 + 0.1 = 1.0, g1 = 0.65 + 0.65 = 1.3, g2 = 0.6 + 0.5 = 1.1, g3 = 0.4.
+    # g0 holds the single largest c (0.9) but is dropped: the kept groups are g1, g2,
+    # and the top-2 experts inside them are 2 and 3 (tie -> lower index first).
+    spec = _cfg()
+    bias = np.array([0.4, -0.4, 0.15, 0.15, 0.1, 0.0, -0.3, -0.3], np.float32)
+    ids, w = orc.router_select(spec, np.zeros((1, 8), np.float32), bias)
+    assert ids.tolist() == [[2, 3]]
+    assert w.tolist() == [[1.25, 1.25]]          # 0.5 / (0.5 + 0.5) * 2.5
+
+
+def test_router_all_equal_picks_lowest_ids(orc):
+    spec = _cfg(n_exp=16, top_k=4, n_group=4, topk_group=2)
+    ids, w = orc.router_select(spec, np.zeros((1, 16), np.float32), None)
+    assert ids.tolist() == [[0, 1, 2, 3]]
+    assert np.allclose(w, 2.5 / 4)
+
+
+def test_router_bias_dominates_but_weights_unbiased(orc):
+    spec = _cfg(n_exp=8, top_k=2, n_group=1, topk_group=1)
+    logits = np.array([[2.0, 1.0, 0.0, -1.0, -2.0, 0.5, 0.2, 0.1]], np.float32)
+    bias = np.zeros(8, np.float32)
+    bias[4] = 10.0                                  # lowest logit, huge bias
+    ids, w = orc.router_select(spec, logits, bias)
+    assert ids.tolist() == [[4, 0]]
+    s4, s0 = 1 / (1 + math.exp(2.0)), 1 / (1 + math.exp(-2.0))
+    s4, s0 = float(np.float32(s4)), float(np.float32(s0))
+    assert np.allclose(w[0], [s4 / (s4 + s0) * 2.5, s0 / (s4 + s0) * 2.5], rtol=1e-6)
+
+
+def test_router_e_equals_k_selects_all(orc):
+    spec = _cfg(n_exp=4, top_k=4, n_group=2, topk_group=2)
+    rng = np.random.default_rng(4)
+    ids, w = orc.router_select(spec, rng.standard_normal((5, 4)).astype(np.float32), None)
+    assert all(sorted(r) == [0, 1, 2, 3] for r in ids.tolist())
+    assert np.allclose(w.sum(1), 2.5, rtol=1e-6)
+
+
+def _c_scores(logits, bias):
+    s = (1.0 / (1.0 + np.exp(-logits.astype(np.float64)))).astype(np.float32)
+    return s, (s + (bias if bias is not None else np.float32(0))).astype(np.float32)
+
+
+def test_router_single_group_is_plain_topk(orc):
+    spec = _cfg(n_exp=64, top_k=6, n_group=1, topk_group=1)
+    rng = np.random.default_rng(5)
+    logits = rng.standard_normal((20, 64)).astype(np.float32)
+    bias = (rng.standard_normal(64) * 0.01).astype(np.float32)
+    ids, _ = orc.router_select(spec, logits, bias)
+    _, c = _c_scores(logits, bias)
+    want = np.argsort(-c, axis=1, kind="stable")[:, :6]
+    assert np.array_equal(ids, want)
+
+
+def test_router_grouped_bruteforce_subsets(orc):
+    """Exhaustive search over group subsets and expert subsets (E=16, no ties)."""
+    spec = _cfg(n_exp=16, top_k=4, n_group=4, topk_group=2)
+    rng = np.random.default_rng(6)
+    logits = rng.standard_normal((40, 16)).astype(np.float32)
+    bias = (rng.standard_normal(16) * 0.01).astype(np.float32)
+    ids, _ = orc.router_select(spec, logits, bias)
+    _, c = _c_scores(logits, bias)
+    for t in range(40):
+        cg = c[t].astype(np.float64).reshape(4, 4)
+        best = None
+        for groups in itertools.combinations(range(4), 2):
+            # group score = sum of the two largest values of the group
+            sc = sum(sum(sorted(cg[g])[-2:]) for g in groups)
+            if best is None or sc > best[0]:
+                best = (sc, groups)
+        allowed = [e for g in best[1] for e in range(4 * g, 4 * g + 4)]
+        best_set = max(itertools.combinations(allowed, 4), key=lambda S: sum(c[t][list(S)]))
+        assert sorted(ids[t].tolist()) == sorted(best_set)
+        assert list(c[t][ids[t]]) == sorted(c[t][ids[t]], reverse=True)
+
+
+def test_router_softmax_matches_textbook(orc):
+    spec = _cfg(n_exp=64, top_k=8, router="softmax", norm_topk=False, routed_scale=1.0)
+    rng = np.random.default_rng(7)
+    logits = rng.standard_normal((10, 64)).astype(np.float32)
+    ids, w = orc.router_select(spec, logits, None)
+    l64 = logits.astype(np.float64)
+    p = np.exp(l64 - l64.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    assert np.array_equal(ids, np.argsort(-logits, axis=1, kind="stable")[:, :8])
+    assert np.allclose(w, np.take_along_axis(p, ids, 1), rtol=1e-6)
+    spec_n = spec.replace(norm_topk=True)
+    _, wn = orc.router_select(spec_n, logits, None)
+    assert np.allclose(wn.sum(1), 1.0, rtol=1e-6)
+
+
+def test_router_bad_config_rejected(orc):
+    with pytest.raises(ValueError):
+        orc.router_select(_cfg(n_exp=8, n_group=3), np.zeros((1, 8), np.float32), None)
+    with pytest.raises(ValueError):   # 1 group of 2 experts cannot supply top-4
+        orc.router_select(_cfg(n_exp=8, n_group=4, topk_group=1, top_k=4),
+                          np.zeros((1, 8), np.float32), None)
+
+
+# ---------------------------------------------------------------- bucketing
+def test_bucket_stable_sort(orc):
+    rng = np.random.default_rng(8)
+    ids = rng.integers(0, 16, (37, 4)).astype(np.int32)
+    off, pairs = orc.bucket(ids, 16)
+    flat = ids.ravel()
+    assert off[0] == 0 and off[-1] == flat.size
+    assert np.array_equal(np.diff(off), np.bincount(flat, minlength=16))
+    assert np.array_equal(pairs, np.argsort(flat, kind="stable"))
+
+
+def test_bucket_hand_case(orc):
+    ids = np.array([[2, 0], [0, 3], [2, 1]], np.int32)    # pairs p = 0..5
+    off, pairs = orc.bucket(ids, 4)
+    assert off.tolist() == [0, 2, 3, 5, 6]
+    assert pairs.tolist() == [1, 2, 5, 0, 4, 3]
+
+
+def test_bucket_rejects_out_of_range(orc):
+    with pytest.raises(ValueError):
+        orc.bucket(np.array([[0, 4]], np.int32), 4)
+
+
+# ---------------------------------------------------------------- expert MLP and layer
+def _dequant(wp, s):
+    lo = (wp & 15).astype(np.float64) - 8
+    hi = (wp >> 4).astype(np.float64) - 8
+    q = np.stack([lo, hi], -1).reshape(wp.shape[0], -1)
+    return q * np.repeat(s.astype(np.float64), 32, axis=1)
+
+
+def test_expert_matches_dequantised_fp64_matmul(orc):
+    """Brute-force fp64 dequantised matmuls agree with the integer-dot oracle to 1e-6."""
+    spec = synth.TINY
+    blob = synth.expert_blob(spec, 0, 0, 3)
+    v = synth.expert_views(blob, spec.d, spec.ffn)
+    x = synth.activations(spec, 0, 1)[0]
+    qx, sx = orc.q8_quantize(x)
+    y, qh, sh = orc.expert_token(v, qx, sx)
+    xh = qx.astype(np.float64) * np.repeat(sx.astype(np.float64), 32)
+    gate = _dequant(v["w1"], v["s1"]) @ xh
+    up = _dequant(v["w3"], v["s3"]) @ xh
+    h = gate / (1 + np.exp(-gate)) * up
+    # h codes from the oracle's own q8 of h: check they quantise this h
+    hh = qh.astype(np.float64) * np.repeat(sh.astype(np.float64), 32)
+    assert np.max(np.abs(hh - h)) <= np.max(sh) * 0.5 * (1 + 1e-5)
+    yref = _dequant(v["w2"], v["s2"]) @ hh
+    assert np.max(np.abs(y - yref)) <= 1e-6 * np.max(np.abs(yref))
+
+
+def test_single_expert_layer_is_dense_swiglu(orc):
+    """E = k = 1, scale 1, no shared expert: the layer is one dense SwiGLU FFN."""
+    spec = synth.TINY.replace(n_exp=1, top_k=1, n_group=1, topk_group=1, routed_scale=1.0,
+                              has_shared=False, shared_ffn=0, bias="none")
+    layer = synth.make_layer(spec, 1)
+    x = synth.activations(spec, 1, 3)
+    out, ids, w = orc.moe_layer(spec, x, layer.Wr, None, [layer.expert(0)])
+    assert ids.tolist() == [[0]] * 3 and np.all(w == 1.0)
+    v = layer.expert(0)
+    for t in range(3):
+        qx, sx = orc.q8_quantize(x[t])
+        xh = qx.astype(np.float64) * np.repeat(sx.astype(np.float64), 32)
+        g = _dequant(v["w1"], v["s1"]) @ xh
+        u = _dequant(v["w3"], v["s3"]) @ xh
+        h = (g / (1 + np.exp(-g)) * u).astype(np.float32)
+        qh, sh = orc.q8_quantize(h)
+        ref = _dequant(v["w2"], v["s2"]) @ (qh.astype(np.float64) * np.repeat(sh.astype(np.float64), 32))
+        assert np.max(np.abs(out[t] - ref)) <= 1e-6 * np.max(np.abs(ref))
+
+
+def test_layer_combine_and_linearity(orc):
+    spec = synth.TINY
+    layer = synth.make_layer(spec, 0)
+    x = synth.activations(spec, 0, 4)
+    experts = [layer.expert(e) for e in range(spec.n_exp)]
+    out, ids, w = orc.moe_layer(spec, x, layer.Wr, layer.bias, experts, layer.shared())
+    # Combine: y_shared + sum_i w_i y_i, from the per-expert outputs.
+    for t in range(4):
+        qx, sx = orc.q8_quantize(x[t])
+        acc = orc.expert_token(layer.shared(), qx, sx)[0].astype(np.float64)
+        for i in range(spec.top_k):
+            acc += float(w[t, i]) * orc.expert_token(experts[ids[t, i]], qx, sx)[0]
+        assert np.max(np.abs(out[t] - acc)) <= 1e-6 * np.max(np.abs(acc))
+    # Doubling routed_scale doubles the routed part and leaves the shared part.
+    out2, ids2, w2 = orc.moe_layer(spec.replace(routed_scale=5.0), x, layer.Wr, layer.bias,
+                                   experts, layer.shared())
+    assert np.array_equal(ids, ids2) and np.array_equal(w2, 2 * w)
+    ysh = np.stack([orc.expert_token(layer.shared(), *orc.q8_quantize(x[t]))[0] for t in range(4)])
+    assert np.allclose(out2 - ysh, 2 * (out - ysh), rtol=1e-5, atol=1e-6 * np.abs(out).max())
+    # routed_scale 0: only the shared expert remains.
+    out0, _, _ = orc.moe_layer(spec.replace(routed_scale=0.0), x, layer.Wr, layer.bias,
+                               experts, layer.shared())
+    assert np.allclose(out0, ysh, rtol=0, atol=1e-6 * np.abs(ysh).max())
+
+
+def test_layer_tokens_independent_and_permutation_invariant(orc):
+    spec = synth.TINY
+    layer = synth.make_layer(spec, 2)
+    x = synth.activations(spec, 2, 5)
+    experts = [layer.expert(e) for e in range(spec.n_exp)]
+    out, ids, w = orc.moe_layer(spec, x, layer.Wr, layer.bias, experts, layer.shared())
+    for t in (0, 3):
+        o1, _, _ = orc.moe_layer(spec, x[t:t + 1], layer.Wr, layer.bias, experts, layer.shared())
+        assert np.array_equal(o1[0], out[t])
+    # Relabel experts with a permutation, feeding the ids through ids_in.
+    perm = np.random.default_rng(9).permutation(spec.n_exp)
+    inv = np.argsort(perm)
+    exp_p = [experts[perm[e]] for e in range(spec.n_exp)]
+    outp, _, _ = orc.moe_layer(spec, x, None, None, exp_p, layer.shared(),
+                               ids=inv[ids].astype(np.int32), w=w)
+    assert np.array_equal(outp, out)
+
+
+def test_layer_empty_batch(orc):
+    spec = synth.TINY
+    layer = synth.make_layer(spec, 0, experts=[])
+    out, ids, w = orc.moe_layer(spec, np.zeros((0, spec.d), np.float32), layer.Wr, layer.bias,
+                                [layer.expert(e) for e in range(spec.n_exp)], layer.shared())
+    assert out.shape == (0, spec.d) and ids.shape == (0, spec.top_k)
+
+
+# ---------------------------------------------------------------- LRU trace
+def test_lru_hand_sequence(orc):
+    # capacity 2, every lookup in its own batch: A B A C B -> miss miss hit miss(evict B) miss(evict A)
+    kinds, keys = [], []
+    for k in [1, 2, 1, 3, 2]:
+        kinds += [0, 1]
+        keys += [0, k]
+    res = orc.lru_trace(2, kinds, keys)[1::2]
+    assert res.tolist() == [0, 0, 1, 0, 0]
+
+
+def test_lru_cyclic_thrash(orc):
+    C = 8
+    keys = [i % (C + 1) for i in range(10 * (C + 1))]
+    kinds = [1] * len(keys)
+    allk = []
+    allkey = []
+    for k in keys:
+        allk += [0, 1]
+        allkey += [0, k]
+    res = orc.lru_trace(C, allk, allkey)[1::2]
+    assert res.sum() == 0
+
+
+def test_lru_pins_block_eviction(orc):
+    # capacity 2, one batch looks up three keys: the third has nowhere to go.
+    res = orc.lru_trace(2, [0, 1, 1, 1], [0, 10, 11, 12])
+    assert res.tolist() == [0, 0, 0, 2]
+    # a prefetch cannot evict pinned keys either, but can after the next batch start.
+    res = orc.lru_trace(2, [0, 1, 1, 2, 0, 2], [0, 10, 11, 12, 0, 12])
+    assert res.tolist() == [0, 0, 0, 2, 0, 0]
+
+
+def test_lru_random_against_ordered_dict(orc):
+    from collections import OrderedDict
+    rng = np.random.default_rng(10)
+    C = 6
+    kinds = rng.choice([0, 1, 1, 1, 2, 2], size=3000).astype(np.int32)
+    keys = rng.integers(0, 14, 3000).astype(np.int64)
+    got = orc.lru_trace(C, kinds, keys)
+    lru, pinned, want = OrderedDict(), set(), []
+    for kd, k in zip(kinds.tolist(), keys.tolist()):
+        if kd == 0:
+            pinned.clear()
+            want.append(0)
+            continue
+        if k in lru:
+            lru.move_to_end(k)
+            if kd == 1:
+                pinned.add(k)
+            want.append(1)
+            continue
+        if len(lru) >= C:
+            victim = next((v for v in lru if v not in pinned), None)
+            if victim is None:
+                want.append(2)
+                continue
+            del lru[victim]
+        lru[k] = True
+        if kd == 1:
+            pinned.add(k)
+        want.append(0)
+    assert got.tolist() == want
