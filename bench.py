@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark of one routed MoE FFN layer on B300 (GLM-5.2-shaped decode by default).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl colibri|reference]
+                    [--workload glm52_decode_t1|glm52_decode_t4|olmoe_decode_t1|...]
+
+A step is one pass of the whole layer (q8, router, bucketing, gate/up, down, combine)
+over one batch of T synthetic tokens, with all experts resident in HBM. Each timed step
+is one CUDA-graph replay bracketed by CUDA events on the launching stream; between
+steps (outside the events) the next token's activations are copied in and a 256 MB
+buffer is written to flush the 126 MB L2. Prints one JSON line.
+
+--impl reference times the CPU oracle (plain C, one core) on the same workload: each
+step is one expert pass of one token (the router and the shared expert ride with the
+first of a token's passes), so the step count of the GPU arm stays affordable.
+
+Multi-GPU (torchrun): the layer does not shard here, so N ranks run N independent
+replicas (weak scaling); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from routed_expert_ffn_grouped_b300 import synth  # noqa: E402
+
+METRIC = "MoE-layer decode tokens/s; expert-weight HBM GB/s as % of B300 peak"
+WORKLOADS = {
+    "glm52_decode_t1": ("glm52", 1, False),
+    "glm52_decode_t4": ("glm52", 4, False),
+    "olmoe_decode_t1": ("olmoe", 1, False),
+    "olmoe_decode_t16": ("olmoe", 16, False),
+    "glm52_prefill_t2048": ("glm52", 2048, True),
+}
+DEFAULT_WORKLOAD = "glm52_decode_t1"
+N_X = 64                 # distinct activation batches cycled through
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6400.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="colibri", choices=["colibri", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def traffic_from_profiles(kernel_file: str, workload: str):
+    """dram bytes per launch recorded by ncu in profiles/, or None when the kernel source
+    changed since (the summary stores the sha256 of the source it measured)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_file}.md")
+    src = os.path.join(ROOT, "routed_expert_ffn_grouped_b300", "csrc", "kernels_gemv.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    m = re.search(rf"traffic_bytes_per_launch\[{workload}\]:\s*([0-9.e+]+)", text)
+    s = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != sha:
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks",
+               0x10: "sync_boost", 0x1: "gpu_idle"}
+
+    def __init__(self, torch, device_index: int, period_s: float = 0.005):
+        self.samples, self.reasons = [], 0
+        self.period = period_s
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            h = None
+            try:
+                bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+                h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
+            except Exception:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
+                h = pynvml.nvmlDeviceGetHandleByIndex(idx)
+            self.h = h
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+
+    def _reasons(self):
+        f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return f(self.h)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                self.reasons |= int(self._reasons())
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+def dist_setup(torch):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(torch, world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(torch, world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def blob_bytes(spec, f):
+    L = synth.blob_layout(spec.d, f)
+    gate_up = 2 * (f * spec.d // 2) + 2 * 4 * f * (spec.d // 32)
+    down = spec.d * f // 2 + 4 * spec.d * (f // 32)
+    return L.nbytes, gate_up, down
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_tokens_per_s(spec, host, xs, budget_s: float, max_tokens: int):
+    import oracle
+    oracle.lib()
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_tokens:
+        oracle.moe_layer(spec, xs[n % len(xs)], host.Wr, host.bias, host.expert, host.shared())
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt
+
+
+def run_reference(args):
+    """The oracle on the host cores, step = one expert pass of one token."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    name, T, row_scale = WORKLOADS[args.workload]
+    spec = synth.SPECS[name]
+    host = synth.make_layer(spec, args.seed)
+    xs = [synth.activations(spec, args.seed, 1, step=i, row_scale=row_scale)[0] for i in range(N_X)]
+    per_tok = spec.top_k + (1 if spec.has_shared else 0)
+    state = {"tok": -1}
+
+    def step(i):
+        t, slot = divmod(i, per_tok)
+        x = xs[t % N_X]
+        if slot == 0 or state["tok"] != t:
+            q, s = oracle.q8_quantize(x)
+            ids, w = oracle.router_topk(spec, x[None], host.Wr, host.bias)
+            state.update(tok=t, q=q, s=s, ids=ids[0], w=w[0], acc=np.zeros(spec.d))
+        if spec.has_shared and slot == per_tok - 1:
+            y, _, _ = oracle.expert_token(host.shared(), state["q"], state["s"])
+            state["acc"] += y
+        elif slot < spec.top_k:
+            y, _, _ = oracle.expert_token(host.expert(int(state["ids"][slot])), state["q"], state["s"])
+            state["acc"] += float(state["w"][slot]) * y
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = (args.steps / per_tok) / dt       # tokens/s: one token per per_tok steps
+    sample = (f"{args.steps} steps = {args.steps / per_tok:.1f} tokens of the {args.workload} layer, "
+              f"one expert pass of one token per step, single-threaded C oracle")
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8xi4->i32, f64",
+            "data": "synthetic", "config": workload_config(spec, args.workload, T),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(spec, workload, T):
+    return {"workload": workload, "d": spec.d, "ffn": spec.ffn, "n_exp": spec.n_exp, "top_k": spec.top_k,
+            "shared_ffn": spec.shared_ffn if spec.has_shared else 0, "router": spec.router, "T": T,
+            "experts_resident": "all in HBM", "l2": "256 MB buffer written between timed steps",
+            "timing": "CUDA events per step around one CUDA-graph replay"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_colibri(args):
+    import torch
+    from routed_expert_ffn_grouped_b300 import build as cbuild
+    from routed_expert_ffn_grouped_b300 import colibri as C
+
+    world, rank, local = dist_setup(torch)
+    if rank == 0 or not os.path.exists(C.LIB_PATH):
+        cbuild.build()
+    barrier(torch, world)
+    name, T, row_scale = WORKLOADS[args.workload]
+    spec = synth.SPECS[name]
+    host = synth.make_layer(spec, args.seed)
+    dl = C.DeviceLayer(host)
+    stream = torch.cuda.Stream()
+    xs_host = np.stack([synth.activations(spec, args.seed, T, step=i, row_scale=row_scale) for i in range(N_X)])
+    xs = torch.from_numpy(xs_host).cuda()
+    x = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    ws = torch.empty(C.colibri_moe_workspace_bytes(dl.cfg, T), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    K, W = args.steps, args.warmup
+    ids_log = torch.empty((W + K, T, spec.top_k), dtype=torch.int32, device="cuda")
+
+    def layer():
+        C.colibri_moe_layer(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws,
+                            stream=torch.cuda.current_stream())
+
+    with torch.cuda.stream(stream):
+        x.copy_(xs[0])
+        layer()                                   # eager warm call (also checks the status)
+        stream.synchronize()
+        st = C.colibri_workspace_status(dl.cfg, T, ws, stream=stream)
+        if st != C.OK:
+            raise RuntimeError(f"layer reported device error {st}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        layer()
+    C.colibri_moe_profile_enable(True)
+    graph_prof = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_prof, stream=stream):
+        layer()
+    C.colibri_moe_profile_enable(False)
+
+    def pre(i):
+        x.copy_(xs[i % N_X])
+        flush.fill_(float(i))
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            pre(i)
+            graph.replay()
+            ids_log[i].copy_(ids)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(torch, world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch, local)
+    with sampler, torch.cuda.stream(stream):
+        for i in range(K):
+            pre(W + i)
+            starts[i].record(stream)
+            graph.replay()
+            ends[i].record(stream)
+            ids_log[W + i].copy_(ids)
+        torch.cuda.synchronize()
+    barrier(torch, world)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = allreduce_max(torch, world, float(sum(step_ms)))
+    value = world * T * K / (total_ms / 1e3)
+
+    # expert bytes per step: distinct routed experts + the shared expert
+    nb, gu_b, dn_b = blob_bytes(spec, spec.ffn)
+    sh = blob_bytes(spec, spec.shared_ffn) if spec.has_shared else (0, 0, 0)
+    ids_np = ids_log[W:].cpu().numpy()
+    distinct = np.array([len(np.unique(ids_np[i])) for i in range(K)])
+    expert_bytes = distinct * nb + sh[0]
+    gu_bytes = distinct * gu_b + sh[1]
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    layer_gbs = float(np.sum(expert_bytes) / (sum(step_ms) / 1e3) / 1e9)
+
+    # per-kernel profiling pass (events between the kernels, recorded inside the graph)
+    P = min(K, 400)
+    prof = {k: [] for k in C.PROFILE_KERNELS}
+    prof_bytes = []
+    with torch.cuda.stream(stream):
+        for i in range(P):
+            pre(W + i)
+            graph_prof.replay()
+            ms = C.colibri_moe_profile_read()
+            for k, v in ms.items():
+                prof[k].append(v)
+            prof_bytes.append(len(np.unique(ids.cpu().numpy())) * gu_b + sh[1])
+    kern_ms = {k: float(np.mean(v)) for k, v in prof.items()}
+    gu_gbs = float(np.mean(np.array(prof_bytes) / (np.array(prof["gateup"]) / 1e3)) / 1e9)
+    traffic = traffic_from_profiles("k_gateup", args.workload)
+
+    # end to end through the public API: pinned host x in, out back to pinned host, per step
+    x_pin = torch.from_numpy(xs_host).pin_memory()
+    out_pin = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
+    KE = min(K, 500)
+    e2e_s = 0.0
+    with torch.cuda.stream(stream):
+        for i in range(KE):
+            flush.fill_(float(i))
+            stream.synchronize()
+            t0 = time.perf_counter()
+            x.copy_(x_pin[i % N_X], non_blocking=True)
+            C.colibri_moe_layer(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws,
+                                stream=stream)
+            out_pin.copy_(out, non_blocking=True)
+            stream.synchronize()
+            e2e_s += time.perf_counter() - t0
+    e2e_s = allreduce_max(torch, world, e2e_s)
+    e2e_value = world * T * KE / e2e_s
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, n, dt = oracle_tokens_per_s(spec, host, [xs_host[i] for i in range(N_X)], 15.0, 64)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} batches of T={T} tokens of {args.workload} through the C oracle "
+                         f"({dt:.1f} s, single-threaded)"}
+        cpu["value"] = rate * T
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "i8xi4->i32, f32", "data": "synthetic",
+            "config": workload_config(spec, args.workload, T),
+            "expert_hbm_gbs": layer_gbs, "expert_hbm_frac": layer_gbs / hbm_peak,
+            "expert_bytes_per_step": float(np.mean(expert_bytes)),
+            "roofline": {"bound": "hbm", "kernel": "k_gateup", "achieved": gu_gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": gu_gbs / hbm_peak, "traffic": traffic,
+                         "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                         "algorithmic_bytes_per_launch": float(np.mean(prof_bytes))},
+            "kernel_ms": kern_ms,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * spec.d * 4,
+                    "d2h_bytes_per_step": T * spec.d * 4, "steps": KE,
+                    "path": "colibri_moe_layer via the Python binding, eager launches"},
+            "gpu_launches": 7 * K,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_colibri(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,265 @@
+/*
+ * colibri.h -- C ABI of libcolibri.so: one routed Mixture-of-Experts FFN layer on a
+ * B300 GPU (sm_103a), with int4 group-scaled expert weights, int8 activations and a
+ * small HBM expert cache fed from pinned host memory.
+ *
+ * The layer is the hot path of the Colibri expert-streaming MoE engine described on
+ * the pages "Guide Complet de Colibri" (dashen-tech.com), "Colibri纯C引擎爆火"
+ * (kongchang.com) and "Run a 744B-parameter model on your own machine"
+ * (aifrontierpost.com). Each entry point below cites the passage that defines its
+ * operation.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named "device" are CUDA device pointers; "host" pointers are ordinary
+ *     host memory. The caller allocates and owns every buffer passed in (device
+ *     memory, pinned host memory, streams); the library never frees caller memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Compute entry points only enqueue work on it and return without synchronising.
+ *   - Layouts are row-major. A packed int4 weight matrix [out][in] stores row n as
+ *     in/2 bytes; byte j holds element 2j in its low nibble and 2j+1 in its high
+ *     nibble, each nibble the offset-binary code q+8 of q in [-8, 7]. Its scales are
+ *     fp32 [out][in/32], one per 32 consecutive elements of a row.
+ *   - Every function returns COLIBRI_OK (0) or a negative COLIBRI_E_* code. Argument
+ *     errors are detected on the host before anything is enqueued. Launch errors are
+ *     returned as COLIBRI_E_CUDA. Errors found on the device (an expert id out of
+ *     range, a wait that ran out) set a flag in the workspace that
+ *     colibri_workspace_status reports; the kernels then skip the bad work and return.
+ */
+#ifndef COLIBRI_H
+#define COLIBRI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define COLIBRI_OK 0
+#define COLIBRI_E_INVAL (-1)   /* bad argument or configuration */
+#define COLIBRI_E_CUDA (-2)    /* a CUDA runtime call or launch failed */
+#define COLIBRI_E_NOMEM (-3)   /* workspace or cache pool too small */
+#define COLIBRI_E_TIMEOUT (-4) /* a bounded wait ran out */
+#define COLIBRI_E_MISS (-5)    /* strict cache lookup found an expert not resident */
+#define COLIBRI_E_STAGE (-6)   /* staging an expert into the cache failed */
+#define COLIBRI_E_DEVICE (-7)  /* a kernel reported bad input through the error flag */
+
+#define COLIBRI_GROUP 32 /* quantisation group: elements per scale */
+
+enum { COLIBRI_ROUTER_SIGMOID_GROUPED = 0, COLIBRI_ROUTER_SOFTMAX = 1 };
+
+/* Shape and routing of one layer.
+ *   d            hidden size (multiple of 32)
+ *   ffn          routed expert intermediate size (multiple of 32)
+ *   n_exp        routed experts E (<= 1024), top_k experts per token (<= 32)
+ *   n_group, topk_group   sigmoid router: E/n_group contiguous experts per group,
+ *                topk_group groups kept
+ *   has_shared, shared_ffn   one shared expert applied to every token with weight 1
+ *   router       COLIBRI_ROUTER_*
+ *   norm_topk    1: the k selected weights are renormalised to sum 1 before scaling
+ *   routed_scale multiplies the routed weights
+ *   group        must be COLIBRI_GROUP */
+typedef struct {
+    int d, ffn, n_exp, top_k, n_group, topk_group, has_shared, shared_ffn, router, norm_topk;
+    float routed_scale;
+    int group;
+} colibri_layer_cfg;
+
+/* One expert's tensors (device pointers, 16-byte aligned): gate w1 [f][d/2], up w3
+ * [f][d/2], down w2 [d][f/2] packed int4; scales s1 [f][d/32], s3 [f][d/32],
+ * s2 [d][f/32] fp32. Group-scaled int4 container: aifrontierpost tutorial, "Step 3 --
+ * Get a model"; the layer uses 32-element groups. */
+typedef struct {
+    const uint8_t *w1, *w3, *w2;
+    const float *s1, *s3, *s2;
+} colibri_expert;
+
+/* Byte offsets of the six parts inside one contiguous expert blob (w1|w3|w2|s1|s3|s2,
+ * each 256-byte aligned) and the blob's size. The cache stages whole blobs. */
+typedef struct {
+    size_t w1, w3, w2, s1, s3, s2, nbytes;
+} colibri_blob_layout;
+
+/* Host only. Fills *out for an expert of hidden size d and intermediate size f.
+ * The GLM-5.2-shaped expert (d=6144, f=2048) has 18,874,368 bytes of nibbles, the
+ * "~19 MB" routed expert of the kongchang.com article (section 核心思路), and
+ * 23,592,960 bytes with its scales. Returns COLIBRI_E_INVAL unless d, f are positive
+ * multiples of 32. */
+int colibri_blob_layout_for(int d, int f, colibri_blob_layout *out);
+
+/* Host only. A static string naming a status code. */
+const char *colibri_strerror(int status);
+
+/* q8 activation quantiser (the int8 side of the int8 x packed-int4 dot kernel:
+ * dashen-tech guide, table "Points techniques cles", integer dot-product row).
+ * Per row and per 32 consecutive columns: d = amax/127 in fp32, q = clamp(roundf(x/d),
+ * -127, 127), rounding halves away from zero; an all-zero group gets d = 0 and zero
+ * codes.
+ *   x      device fp32 [rows][cols], cols % 32 == 0
+ *   q      device int8 [rows][cols] (out)
+ *   scale  device fp32 [rows][cols/32] (out)
+ * rows == 0 is a no-op. */
+int colibri_q8_quantize(const float *x, int rows, int cols, int8_t *q, float *scale, void *stream);
+
+/* Router: logits, selection and weights for T tokens (DeepSeek-V3-style sigmoid router
+ * with a selection bias: dashen-tech guide, table "Points techniques cles", row "Router
+ * style DeepSeek-V3"; softmax top-k for OLMoE-shaped layers).
+ *   logits l[t][e] = x[t] . Wr[e] in fp32 with a fixed summation order: 32 strided
+ *   fmaf chains (chain j takes k = j, j+32, ... ascending) joined by a halving pairwise
+ *   tree, so that the selection is reproducible bit for bit.
+ *   Sigmoid mode: s = fp32(sigmoid(l)) evaluated in fp64, c = s + bias (fp32); group
+ *   score = sum of the two largest c of each of n_group contiguous groups; keep the
+ *   topk_group best groups; select the top_k largest c inside them in descending order
+ *   (ties: lower index, for groups and experts); w_i = s_i / sum_j s_j * routed_scale
+ *   (or s_i * routed_scale when norm_topk = 0).
+ *   Softmax mode: top_k largest logits (ties: lower index); w_i = softmax over all E
+ *   logits at i (renormalised over the k when norm_topk = 1) * routed_scale.
+ *   x       device fp32 [T][d];  Wr device fp32 [E][d], 16-byte aligned
+ *   bias    device fp32 [E] or NULL (zero); ignored in softmax mode
+ *   logits  device fp32 [T][E] (out; also the kernel's scratch)
+ *   ids     device int32 [T][top_k] (out), w device fp32 [T][top_k] (out)
+ * T == 0 is a no-op. */
+int colibri_router_topk(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                        const float *bias, float *logits, int32_t *ids, float *w, void *stream);
+
+/* Bytes of device workspace colibri_moe_layer needs for up to T_max tokens
+ * (0 on a bad configuration). */
+size_t colibri_moe_workspace_bytes(const colibri_layer_cfg *cfg, int T_max);
+
+/* One routed MoE FFN layer for T tokens (the expert MLP the pages run on the integer
+ * dot kernel: dashen-tech guide, "Analyse approfondie" step 3; shared experts resident
+ * next to the routed ones: kongchang.com article, section 核心思路).
+ *   q8(x) -> router (unless ids_given) -> bucketing of (token, slot) pairs by expert ->
+ *   per expert: gate = W1 q8(x), up = W3 q8(x) as int32 group dots times the two
+ *   groups' scales; h = silu(gate) * up; down y = W2 q8(h) likewise ->
+ *   out[t] = y_shared[t] + sum_i w[t][i] * y_{ids[t][i]}[t] in slot order.
+ *   T <= 32 runs the decode GEMV kernels; larger T runs the grouped GEMM on tcgen05.
+ *   x        device fp32 [T][d]
+ *   Wr, bias as for colibri_router_topk (unused when ids_given)
+ *   experts  device array of E colibri_expert (only the selected ids are read)
+ *   shared   host pointer to one colibri_expert of intermediate size shared_ffn whose
+ *            members are device pointers; NULL when cfg->has_shared == 0
+ *   ids, w   device [T][top_k]: outputs of the router, or inputs when ids_given != 0
+ *   out      device fp32 [T][d]
+ *   workspace  device, >= colibri_moe_workspace_bytes(cfg, T) bytes, 256-byte aligned;
+ *            owned by the caller, must not be shared by calls that overlap on the GPU
+ * T == 0 is a no-op. */
+int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                      const float *bias, const colibri_expert *experts,
+                      const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
+                      float *out, void *workspace, size_t ws_bytes, void *stream);
+
+/* Reads the device error flag of a workspace after synchronising `stream`, and clears
+ * it. *status_out = COLIBRI_OK or COLIBRI_E_DEVICE. */
+int colibri_workspace_status(const colibri_layer_cfg *cfg, int T_max, void *workspace,
+                             int *status_out, void *stream);
+
+/* Byte offsets of the layer's intermediates inside its workspace, for inspection by
+ * tests (q8 codes of x, bucket lists, h codes, per-pair expert outputs). Valid after a
+ * colibri_moe_layer call with the same cfg and T_max. */
+typedef struct {
+    size_t qx;      /* int8 [T][d]          q8 codes of x */
+    size_t sx;      /* fp32 [T][d/32]       their scales */
+    size_t offsets; /* int32 [E+1]          bucket offsets (exclusive scan of counts) */
+    size_t pairs;   /* int32 [T*k]          pairs p = t*k+i sorted by (expert, p) */
+    size_t hq;      /* int8 [T*k+T][fmax]   q8 codes of h per pair (routed, then shared) */
+    size_t hs;      /* fp32 [T*k+T][fmax/32] */
+    size_t y;       /* fp32 [T*k+T][d]      per-pair expert outputs */
+    size_t fmax;    /* row stride of hq: max(ffn, shared_ffn) */
+} colibri_workspace_view;
+int colibri_moe_workspace_view(const colibri_layer_cfg *cfg, int T_max, colibri_workspace_view *out);
+
+/* Profiling hook (process-wide, not thread-safe, off by default). While enabled,
+ * colibri_moe_layer records a timing event on its stream before its first kernel and
+ * after each of its seven kernels (also under CUDA-graph capture, as external
+ * event-record nodes), on the device that was current when profiling was enabled. */
+#define COLIBRI_PROFILE_KERNELS 7
+int colibri_moe_profile_enable(int on);
+
+/* Milliseconds of each kernel of the most recent profiled call, after waiting for it:
+ * ms[0] q8 of x, [1] router logits, [2] router selection, [3] bucketing, [4] gate/up,
+ * [5] down, [6] combine. A kernel the call skipped (the router when ids are given)
+ * reads about 0. n must be >= COLIBRI_PROFILE_KERNELS. */
+int colibri_moe_profile_read(float *ms, int n);
+
+/* Test export: int32 group dots of a packed int4 matrix with one int8 vector, computed
+ * by the decode GEMV's integer dot code.
+ *   w device [rows][cols/2], qa device int8 [cols], dots device int32 [rows][cols/32]. */
+int colibri_debug_group_dots(const uint8_t *w, const int8_t *qa, int rows, int cols,
+                             int32_t *dots, void *stream);
+
+/* ---- HBM expert cache -------------------------------------------------------------
+ * Experts stream from a larger, slower tier into a small LRU cache of HBM slots
+ * (dashen-tech guide, bullet "Streaming d'experts" and section "Router-Lookahead
+ * prefetch"; kongchang.com article, section 三级存储分层). Here the slower tier is
+ * pinned host memory holding n_layers * n_exp blobs; a miss or a prefetch copies a blob
+ * into a slot with cudaMemcpyAsync on the cache's copy stream, and the compute stream
+ * waits on the slot's ready event. */
+typedef struct colibri_cache colibri_cache;
+
+typedef struct {
+    int64_t lookups;         /* ids looked up */
+    int64_t hits;            /* ... found resident or already in flight */
+    int64_t misses;          /* ... staged on demand */
+    int64_t prefetch_staged; /* blobs staged by colibri_expert_cache_stage */
+    int64_t prefetch_used;   /* prefetched blobs later hit by a lookup */
+    int64_t prefetch_skipped;/* prefetches dropped: every slot pinned */
+    int64_t evictions;
+    int64_t bytes_staged;    /* host -> HBM bytes enqueued */
+    int n_slots;
+} colibri_cache_stats;
+
+/* Creates a cache.
+ *   hbm_pool     device memory owned by the caller, 256-byte aligned; the cache keeps
+ *                its per-layer expert tables at its start and cuts the rest into
+ *                slots of colibri_blob_layout_for(d, ffn).nbytes
+ *   pinned_host  page-locked host memory holding blob (l, e) at offset
+ *                (l * n_exp + e) * nbytes
+ *   copy_stream  stream for the staging copies (cudaStream_t as void*)
+ * Returns COLIBRI_E_NOMEM when the pool holds fewer slots than top_k. */
+int colibri_expert_cache_init(colibri_cache **out, void *hbm_pool, size_t pool_bytes,
+                              const void *pinned_host, int n_layers, int n_exp, int d, int ffn,
+                              int top_k, void *copy_stream);
+
+/* Prefetch: stage the blobs of layer `layer` named by host ids [n] that are not
+ * resident (the router-lookahead prefetch of the dashen-tech guide). Resident ones
+ * become most recently used. Returns at once; the copies run on the copy stream. */
+int colibri_expert_cache_stage(colibri_cache *c, int layer, const int32_t *ids, int n);
+
+/* Makes the blobs of layer `layer` named by host ids [n] usable by work enqueued on
+ * `wait_on` after this call: misses are staged now (or COLIBRI_E_MISS in strict mode),
+ * and `wait_on` waits for each slot's ready event. The slots stay pinned until the
+ * next lookup, which also records when the previous batch's compute has finished
+ * using them. Afterwards colibri_expert_cache_table(c, layer)[id] holds the expert. */
+int colibri_expert_cache_lookup(colibri_cache *c, int layer, const int32_t *ids, int n,
+                                void *wait_on);
+
+/* Device table of n_exp colibri_expert for `layer` (entries valid for looked-up ids). */
+const colibri_expert *colibri_expert_cache_table(colibri_cache *c, int layer);
+
+/* 1: lookups of non-resident ids fail with COLIBRI_E_MISS instead of staging. */
+int colibri_expert_cache_set_strict(colibri_cache *c, int strict);
+
+int colibri_expert_cache_stats(colibri_cache *c, colibri_cache_stats *out);
+
+/* Waits (polling, at most timeout_ms) for every staging copy issued so far.
+ * COLIBRI_E_TIMEOUT if they are still running. */
+int colibri_expert_cache_sync(colibri_cache *c, int timeout_ms);
+
+void colibri_expert_cache_destroy(colibri_cache *c);
+
+/* Test hook: the next `count` staging copies fail on the host (no copy is issued) and
+ * report COLIBRI_E_STAGE. */
+int colibri_expert_cache_inject_stage_failure(colibri_cache *c, int count);
+
+/* Host-only test export of the cache's replacement policy, on abstract keys. ops:
+ * kind 0 = start of a lookup batch (unpins every key), 1 = lookup key (pins it),
+ * 2 = prefetch key. result: kind 1: 1 hit, 0 miss (inserted), 2 no unpinned slot;
+ * kind 2: 1 resident, 0 inserted, 2 no room (skipped); kind 0: 0. */
+int colibri_lru_trace(int capacity, int64_t n_ops, const int32_t *kind, const int64_t *key,
+                      int8_t *result);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

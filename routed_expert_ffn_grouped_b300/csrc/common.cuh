@@ -1,0 +1,173 @@
+// Device helpers shared by the kernels of libcolibri.so (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "colibri.h"
+
+namespace clb {
+
+constexpr int G = COLIBRI_GROUP;  // quantisation group
+constexpr unsigned FULL = 0xffffffffu;
+
+// Error bits written to the workspace flag.
+constexpr int ERR_BAD_ID = 1;       // an expert id outside [0, E)
+constexpr int ERR_WAIT_TIMEOUT = 2; // an mbarrier or flag wait ran out of iterations
+constexpr int ERR_BAD_SHAPE = 4;    // a kernel was handed a shape it does not cover
+
+// Bound on spin iterations of any wait in these kernels. try_wait suspends the thread
+// for a hardware-chosen interval per attempt, so this is far beyond any legal wait.
+constexpr uint32_t WAIT_LIMIT = 1u << 24;
+
+// One-use loads of weight bytes: bypass L1, they are read once per call.
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_nc(const void *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// sum of four unsigned bytes of a times four signed bytes of b, plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// int32 dot of one 32-element group: 16 bytes of offset-binary nibbles (low nibble =
+// even element) against activation codes stored as 8 words in "even/odd" order (word
+// 2j = elements 8j, 8j+2, 8j+4, 8j+6; word 2j+1 = elements 8j+1, ..., 8j+7) and
+// corr = 8 * (sum of the 32 codes), which removes the +8 offset of the nibbles.
+__device__ __forceinline__ int dot_group(uint4 w, uint4 a0, uint4 a1, int corr)
+{
+    constexpr uint32_t M = 0x0F0F0F0Fu;
+    int acc = -corr;
+    acc = dp4a_us(w.x & M, a0.x, acc);
+    acc = dp4a_us((w.x >> 4) & M, a0.y, acc);
+    acc = dp4a_us(w.y & M, a0.z, acc);
+    acc = dp4a_us((w.y >> 4) & M, a0.w, acc);
+    acc = dp4a_us(w.z & M, a1.x, acc);
+    acc = dp4a_us((w.z >> 4) & M, a1.y, acc);
+    acc = dp4a_us(w.w & M, a1.z, acc);
+    acc = dp4a_us((w.w >> 4) & M, a1.w, acc);
+    return acc;
+}
+
+// Byte position of element k (0..31) of a group in the even/odd word order.
+__device__ __forceinline__ int eo_pos(int k)
+{
+    return (k & ~7) + ((k & 1) ? 4 + ((k & 7) >> 1) : ((k & 7) >> 1));
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(FULL, v, o);
+    return v;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(FULL, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
+    return v;
+}
+
+// q8 of one element given its group's absmax (the rule of colibri_q8_quantize).
+__device__ __forceinline__ int q8_code(float x, float d)
+{
+    if (d == 0.0f)
+        return 0;
+    float v = roundf(__fdiv_rn(x, d));
+    v = fminf(fmaxf(v, -127.0f), 127.0f);
+    return (int)v;
+}
+
+// ---- mbarrier + 1-D bulk copy (cp.async.bulk) ---------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Returns true once the phase with the given parity has completed, false after
+// WAIT_LIMIT attempts.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t addr = smem_u32(bar);
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done)
+            return true;
+    }
+    return false;
+}
+
+// Global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Per-slot work description written by the bucketing kernel.
+struct Slot {
+    int expert;  // routed expert id, or -1 for the shared expert
+    int begin;   // first entry in the pair list (routed) / 0 (shared)
+    int count;   // tokens routed to this slot
+    int pad;
+};
+
+// Device counters written by the bucketing kernel.
+struct Counters {
+    int n_slots;
+    int n_items_gateup;
+    int n_items_down;
+    int n_routed;
+};
+
+}  // namespace clb

@@ -1,0 +1,20 @@
+// Host-side layout of the colibri_moe_layer workspace.
+#pragma once
+
+#include <stddef.h>
+
+#include "colibri.h"
+
+namespace clb {
+
+// Byte offsets (256-byte aligned) of the layer's intermediates in the workspace.
+struct WsLayout {
+    size_t err, counters, qx, qx_eo, sx, xc, logits, offsets, pairs, slots;
+    size_t hq, hq_eo, hs, hc, y;
+    size_t fmax, total;
+};
+
+bool cfg_valid(const colibri_layer_cfg *c);
+WsLayout ws_layout(const colibri_layer_cfg *c, int T);
+
+}  // namespace clb

@@ -1,0 +1,92 @@
+"""Host-side checks of libcolibri.so: it loads without a GPU, exports every symbol that
+include/colibri.h declares, and its host-only logic (blob layout, argument checks, the
+cache's LRU policy) agrees with the generator and the oracle. No kernel is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from routed_expert_ffn_grouped_b300 import build as cbuild
+from routed_expert_ffn_grouped_b300 import colibri as C
+from routed_expert_ffn_grouped_b300 import synth
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "colibri.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return C.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(colibri_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 18
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(C.SIGNATURES) == names
+
+
+def test_blob_layout_matches_generator(lib):
+    for spec in (synth.TINY, synth.OLMOE, synth.GLM52):
+        a = C.colibri_blob_layout_for(spec.d, spec.ffn)
+        b = synth.blob_layout(spec.d, spec.ffn)
+        assert (a.w1, a.w3, a.w2, a.s1, a.s3, a.s2, a.nbytes) == (b.w1, b.w3, b.w2, b.s1, b.s3, b.s2, b.nbytes)
+    with pytest.raises(C.ColibriError):
+        C.colibri_blob_layout_for(100, 64)
+
+
+def test_strerror(lib):
+    assert C.strerror(0) == "ok"
+    assert "invalid" in C.strerror(C.E_INVAL)
+
+
+def test_workspace_bytes_and_config_checks(lib):
+    for spec in (synth.TINY, synth.OLMOE, synth.GLM52):
+        cfg = C.layer_cfg(spec)
+        assert C.colibri_moe_workspace_bytes(cfg, 4) > 0
+        assert C.colibri_moe_workspace_bytes(cfg, 2048) > C.colibri_moe_workspace_bytes(cfg, 4)
+    bad = C.layer_cfg(synth.TINY.replace(n_group=3))
+    assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0
+    bad = C.layer_cfg(synth.TINY)
+    bad.group = 64
+    assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0
+
+
+def test_argument_errors_detected_on_host(lib):
+    # Rejected before anything is enqueued: no device is touched.
+    assert lib.colibri_q8_quantize(None, 1, 33, None, None, None) == C.E_INVAL
+    assert lib.colibri_q8_quantize(None, 0, 64, None, None, None) == C.OK   # empty is a no-op
+    cfg = C.layer_cfg(synth.TINY)
+    assert lib.colibri_moe_layer(ctypes.byref(cfg), None, 0, None, None, None, None, None, None, 0,
+                                 None, None, 0, None) == C.OK
+    assert lib.colibri_moe_layer(ctypes.byref(cfg), None, 4, None, None, None, None, None, None, 0,
+                                 None, None, 0, None) == C.E_INVAL
+    assert lib.colibri_debug_group_dots(None, None, 1, 31, None, None) == C.E_INVAL
+    assert lib.colibri_lru_trace(0, 0, None, None, None) == C.E_INVAL
+
+
+def test_cache_policy_matches_oracle(lib, orc):
+    rng = np.random.default_rng(11)
+    for cap in (1, 3, 8):
+        kinds = rng.choice([0, 1, 1, 2, 2], size=4000).astype(np.int32)
+        keys = rng.integers(0, 3 * cap + 2, 4000).astype(np.int64)
+        assert np.array_equal(C.colibri_lru_trace(cap, kinds, keys), orc.lru_trace(cap, kinds, keys))
+
+
+def test_cache_policy_thrash_and_reuse(lib):
+    C_ = 16
+    kinds = np.tile([0, 1], 20 * (C_ + 1)).astype(np.int32)
+    keys = np.repeat(np.arange(20 * (C_ + 1)) % (C_ + 1), 2).astype(np.int64)
+    assert C.colibri_lru_trace(C_, kinds, keys)[1::2].sum() == 0
+    keys = np.repeat(np.arange(20 * C_) % C_, 2).astype(np.int64)
+    kinds = np.tile([0, 1], 20 * C_).astype(np.int32)
+    assert C.colibri_lru_trace(C_, kinds, keys)[1::2].sum() == 19 * C_

@@ -1,0 +1,229 @@
+"""CUDA path (through the C ABI) against the C oracle, on the same seeded inputs.
+
+Bit-exact: q8 codes and scales, router logits, expert ids, int32 group dots, bucket
+offsets and pair lists. Within tolerance: routing weights (1e-6 relative; fp64 sums in
+another order) and layer outputs, max |out - oracle| <= 2e-3 * rms(oracle) in fp32.
+"""
+import numpy as np
+import pytest
+
+from routed_expert_ffn_grouped_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from routed_expert_ffn_grouped_b300 import build
+    build.build()
+    return torch
+
+
+@pytest.fixture(scope="module")
+def C(torch_cuda):
+    from routed_expert_ffn_grouped_b300 import colibri
+    colibri.lib()
+    return colibri
+
+
+_layers = {}
+
+
+def dev_layer(C, spec, seed=0):
+    key = (spec, seed)
+    if key not in _layers:
+        host = synth.make_layer(spec, seed)
+        _layers[key] = (host, C.DeviceLayer(host))
+    return _layers[key]
+
+
+def assert_rms_close(got, want, tol=TOL):
+    want = np.asarray(want, np.float64)
+    rms = np.sqrt(np.mean(want ** 2))
+    err = np.max(np.abs(np.asarray(got, np.float64) - want)) if want.size else 0.0
+    assert err <= tol * rms, f"max err {err:.3e} > {tol} * rms {rms:.3e}"
+
+
+def to_dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# ------------------------------------------------------------------ q8
+@pytest.mark.parametrize("rows,cols", [(1, 512), (4, 6144), (16, 2048), (2048, 6144), (3, 32)])
+def test_q8_bit_exact(torch_cuda, C, orc, rows, cols):
+    torch = torch_cuda
+    rng = np.random.default_rng(rows * 7 + cols)
+    x = (rng.standard_normal((rows, cols)) * rng.uniform(0.01, 50, (rows, 1))).astype(np.float32)
+    x[0, :32] = 0.0                                   # an all-zero group
+    x[-1, 32:64] = np.arange(32, dtype=np.float32) - 15.5   # exact half-points after scaling
+    q = torch.empty((rows, cols), dtype=torch.int8, device="cuda")
+    s = torch.empty((rows, cols // 32), dtype=torch.float32, device="cuda")
+    C.colibri_q8_quantize(to_dev(torch, x), q, s)
+    torch.cuda.synchronize()
+    qo, so = orc.q8_quantize(x)
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), so.view(np.uint32))
+
+
+# ------------------------------------------------------------------ router
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 37), ("olmoe", 1), ("olmoe", 16),
+                                    ("glm52", 1), ("glm52", 4), ("glm52", 64)])
+def test_router_bit_exact(torch_cuda, C, orc, name, T):
+    torch = torch_cuda
+    spec = synth.SPECS[name]
+    Wr, bias = synth.router_weights(spec, 0)
+    x = synth.activations(spec, 0, T, step=3)
+    cfg = C.layer_cfg(spec)
+    logits = torch.empty((T, spec.n_exp), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    C.colibri_router_topk(cfg, to_dev(torch, x), to_dev(torch, Wr),
+                          None if bias is None else to_dev(torch, bias), logits, ids, w)
+    torch.cuda.synchronize()
+    lo = orc.router_logits(x, Wr)
+    assert np.array_equal(logits.cpu().numpy().view(np.uint32), lo.view(np.uint32))
+    io, wo = orc.router_select(spec, lo, bias)
+    assert np.array_equal(ids.cpu().numpy(), io)
+    np.testing.assert_allclose(w.cpu().numpy(), wo, rtol=1e-6, atol=0)
+
+
+def test_router_ties_lowest_index(torch_cuda, C, orc):
+    """All-equal logits (x = 0): ids must be the lowest indices of the lowest groups."""
+    torch = torch_cuda
+    spec = synth.GLM52
+    Wr, _ = synth.router_weights(spec, 0)
+    x = np.zeros((2, spec.d), np.float32)
+    cfg = C.layer_cfg(spec)
+    logits = torch.empty((2, spec.n_exp), dtype=torch.float32, device="cuda")
+    ids = torch.empty((2, spec.top_k), dtype=torch.int32, device="cuda")
+    w = torch.empty((2, spec.top_k), dtype=torch.float32, device="cuda")
+    C.colibri_router_topk(cfg, to_dev(torch, x), to_dev(torch, Wr), None, logits, ids, w)
+    io, _ = orc.router_select(spec, orc.router_logits(x, Wr), None)
+    assert np.array_equal(ids.cpu().numpy(), io)
+    assert io[0].tolist() == list(range(8))
+
+
+# ------------------------------------------------------------------ integer group dots
+@pytest.mark.parametrize("rows,cols", [(64, 6144), (37, 2048), (8, 32)])
+def test_group_dots_bit_exact(torch_cuda, C, orc, rows, cols):
+    torch = torch_cuda
+    rng = np.random.default_rng(rows + cols)
+    w = rng.integers(0, 256, (rows, cols // 2), dtype=np.uint8)
+    qa = rng.integers(-127, 128, cols).astype(np.int8)
+    qa[:32] = -127
+    w[0, :16] = 0                                       # -8 x -127 in group 0: 32512
+    dots = torch.empty((rows, cols // 32), dtype=torch.int32, device="cuda")
+    C.colibri_debug_group_dots(to_dev(torch, w), to_dev(torch, qa), dots)
+    torch.cuda.synchronize()
+    want = orc.group_dots(w, qa)
+    assert want[0, 0] == 32512
+    assert np.array_equal(dots.cpu().numpy(), want)
+
+
+# ------------------------------------------------------------------ the layer
+def run_layer(torch, C, dl, x, ids=None, w=None):
+    spec = dl.spec
+    T = x.shape[0]
+    cfg = dl.cfg
+    ws = torch.empty(C.colibri_moe_workspace_bytes(cfg, max(T, 1)), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
+    given = ids is not None
+    ids_d = to_dev(torch, ids) if given else torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w_d = to_dev(torch, w) if given else torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    C.colibri_moe_layer(cfg, to_dev(torch, x), dl.Wr, dl.bias, dl.table, dl.shared, ids_d, w_d, given, out, ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), ids_d.cpu().numpy(), w_d.cpu().numpy(), ws
+
+
+def ws_slice(ws, off, nbytes, dtype):
+    return ws[off:off + nbytes].cpu().numpy().view(dtype)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 1), ("tiny", 13), ("olmoe", 1), ("olmoe", 16),
+                                    ("glm52", 1), ("glm52", 4)])
+def test_moe_layer_parity(torch_cuda, C, orc, name, T):
+    torch = torch_cuda
+    spec = synth.SPECS[name]
+    host, dl = dev_layer(C, spec)
+    x = synth.activations(spec, 0, T, step=11)
+    out, ids, w, ws = run_layer(torch, C, dl, x)
+    assert C.colibri_workspace_status(dl.cfg, T, ws) == C.OK
+    ref, ids_o, w_o = orc.moe_layer(spec, x, host.Wr, host.bias, host.expert, host.shared())
+    assert np.array_equal(ids, ids_o)
+    np.testing.assert_allclose(w, w_o, rtol=1e-6)
+    assert_rms_close(out, ref)
+    # intermediates inside the workspace: q8 codes of x and the bucket lists, bit-exact
+    v = C.colibri_moe_workspace_view(dl.cfg, T)
+    qx = ws_slice(ws, v.qx, T * spec.d, np.int8).reshape(T, spec.d)
+    sx = ws_slice(ws, v.sx, 4 * T * spec.d // 32, np.float32).reshape(T, -1)
+    qo, so = orc.q8_quantize(x)
+    assert np.array_equal(qx, qo) and np.array_equal(sx.view(np.uint32), so.view(np.uint32))
+    off = ws_slice(ws, v.offsets, 4 * (spec.n_exp + 1), np.int32)
+    pairs = ws_slice(ws, v.pairs, 4 * T * spec.top_k, np.int32)
+    off_o, pairs_o = orc.bucket(ids_o, spec.n_exp)
+    assert np.array_equal(off, off_o) and np.array_equal(pairs, pairs_o)
+    # h codes: equal except a rounding-boundary flip of at most 1
+    hq = ws_slice(ws, v.hq, (T * spec.top_k) * v.fmax, np.int8).reshape(-1, v.fmax)
+    t, i = 0, 0
+    _, qh_o, _ = orc.expert_token(host.expert(int(ids_o[t, i])), qo[t], so[t])
+    diff = np.abs(hq[t * spec.top_k + i, :spec.ffn].astype(np.int32) - qh_o)
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.95
+
+
+def test_moe_layer_ids_given(torch_cuda, C, orc):
+    torch = torch_cuda
+    spec = synth.GLM52
+    host, dl = dev_layer(C, spec)
+    ids, w = synth.streaming_ids(spec, 5, 1, 2)
+    ids, w = ids[:, 0], w[:, 0]          # 2 tokens
+    x = synth.activations(spec, 5, 2)
+    out, ids_d, w_d, ws = run_layer(torch, C, dl, x, ids, w)
+    assert np.array_equal(ids_d, ids)
+    ref, _, _ = orc.moe_layer(spec, x, None, None, host.expert, host.shared(), ids=ids, w=w)
+    assert_rms_close(out, ref)
+
+
+def test_moe_layer_bad_id_reports(torch_cuda, C):
+    torch = torch_cuda
+    spec = synth.TINY
+    _, dl = dev_layer(C, spec)
+    ids = np.array([[0, 1, 2, spec.n_exp]], np.int32)         # last id out of range
+    w = np.full((1, 4), 0.5, np.float32)
+    _, _, _, ws = run_layer(torch, C, dl, synth.activations(spec, 0, 1), ids, w)
+    assert C.colibri_workspace_status(dl.cfg, 1, ws) == C.E_DEVICE
+    assert C.colibri_workspace_status(dl.cfg, 1, ws) == C.OK    # read clears it
+
+
+def test_moe_layer_empty_and_deterministic(torch_cuda, C):
+    torch = torch_cuda
+    spec = synth.OLMOE
+    _, dl = dev_layer(C, spec)
+    out, _, _, _ = run_layer(torch, C, dl, np.zeros((0, spec.d), np.float32))
+    assert out.shape == (0, spec.d)
+    x = synth.activations(spec, 1, 16)
+    a, _, _, _ = run_layer(torch, C, dl, x)
+    b, _, _, _ = run_layer(torch, C, dl, x)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_glm_prefill_sampled(torch_cuda, C, orc):
+    """T = 2048 prefill; the oracle recomputes a sample of tokens (tokens are independent)."""
+    torch = torch_cuda
+    spec = synth.GLM52
+    host, dl = dev_layer(C, spec)
+    T = 2048
+    x = synth.activations(spec, 0, T, step=21, row_scale=True)
+    out, ids, w, ws = run_layer(torch, C, dl, x)
+    assert C.colibri_workspace_status(dl.cfg, T, ws) == C.OK
+    io_all, _ = orc.router_topk(spec, x, host.Wr, host.bias)
+    assert np.array_equal(ids, io_all)
+    counts = np.bincount(ids.ravel(), minlength=spec.n_exp)
+    assert counts.sum() == T * spec.top_k
+    for t in (0, 1, 777, 2047):
+        ref, _, _ = orc.moe_layer(spec, x[t:t + 1], host.Wr, host.bias, host.expert, host.shared())
+        assert_rms_close(out[t:t + 1], ref)
