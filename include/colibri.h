@@ -149,6 +149,33 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
                       const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
                       float *out, void *workspace, size_t ws_bytes, void *stream);
 
+/* colibri_moe_layer without a caller-supplied workspace. The pages have no counterpart
+ * to this entry point: it exists for callers that cannot allocate device memory when
+ * they run the layer (a host runtime that owns all device memory through its own pool
+ * and forbids other allocations after start-up, a plugin handed only its input and
+ * output buffers, a latency-critical loop that cannot afford cudaMalloc's implicit
+ * device synchronisation).
+ *   The workspace is a fixed array of COLIBRI_NOALLOC_SCRATCH_BYTES (16 MiB) that the
+ *   library holds in the memory of every device it is loaded on, until the process
+ *   exits. The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *   library routine. The first call made with a device current looks up the array's
+ *   device address on that device (cudaGetSymbolAddress); make that first call before
+ *   any stream capture.
+ *   Arguments, layouts and results are those of colibri_moe_layer. Returns
+ *   COLIBRI_E_NOMEM when colibri_moe_workspace_bytes(cfg, T) exceeds the array (the
+ *   GLM-5.2-shaped layer fits up to T = 32), COLIBRI_E_INVAL on a bad configuration.
+ *   Every call on a device shares the one array and leaves its contents behind for
+ *   the next call; each call rewrites what it reads (its first kernel clears the
+ *   error flag). Calls whose work overlaps on the GPU (other streams, other host
+ *   threads) race on the array and corrupt each other's results: serialise them.
+ *   Device-side errors (an id out of range) are skipped by the kernels as in
+ *   colibri_moe_layer; this variant offers no reader for the flag. */
+#define COLIBRI_NOALLOC_SCRATCH_BYTES (16u << 20)
+int colibri_moe_layer_noalloc(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                              const float *bias, const colibri_expert *experts,
+                              const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
+                              float *out, void *stream);
+
 /* Reads the device error flag of a workspace after synchronising `stream`, and clears
  * it. *status_out = COLIBRI_OK or COLIBRI_E_DEVICE. */
 int colibri_workspace_status(const colibri_layer_cfg *cfg, int T_max, void *workspace,

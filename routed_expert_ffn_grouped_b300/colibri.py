@@ -68,6 +68,8 @@ SIGNATURES = {
     "colibri_moe_workspace_bytes": (_SZ, [_PCFG, _I]),
     "colibri_moe_layer": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
                                _SZ, _P]),
+    "colibri_moe_layer_noalloc": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I,
+                                       _P, _P]),
     "colibri_workspace_status": (_I, [_PCFG, _I, _P, ctypes.POINTER(_I), _P]),
     "colibri_moe_workspace_view": (_I, [_PCFG, _I, ctypes.POINTER(WorkspaceView)]),
     "colibri_debug_group_dots": (_I, [_P, _P, _I, _I, _P, _P]),
@@ -177,6 +179,19 @@ def colibri_moe_layer(cfg: LayerCfg, x, Wr, bias, experts, shared: Expert | None
                                    ctypes.byref(shared) if shared is not None else None, _ptr(ids), _ptr(w),
                                    int(bool(ids_given)), _ptr(out), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def colibri_moe_layer_noalloc(cfg: LayerCfg, x, Wr, bias, experts, shared: Expert | None, ids, w,
+                              ids_given: bool, out, stream=None):
+    """colibri_moe_layer on the library's own fixed device scratch (no workspace argument)."""
+    T = x.shape[0]
+    _check("colibri_moe_layer_noalloc",
+           lib().colibri_moe_layer_noalloc(ctypes.byref(cfg), _ptr(x), T, _ptr(Wr), _ptr(bias), _ptr(experts),
+                                           ctypes.byref(shared) if shared is not None else None, _ptr(ids),
+                                           _ptr(w), int(bool(ids_given)), _ptr(out), _stream(stream)))
 
 
 def colibri_workspace_status(cfg: LayerCfg, T_max: int, workspace, stream=None) -> int:
