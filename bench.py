@@ -90,66 +90,69 @@ def traffic_from_profiles(kernel_file: str, workload: str):
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while running."""
+    """Samples SM clocks and clock-event reasons with `nvidia-smi -lms` while running."""
 
-    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
-               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks",
-               0x10: "sync_boost", 0x1: "gpu_idle"}
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, torch, device_index: int, period_s: float = 0.005):
-        self.samples, self.reasons = [], 0
-        self.period = period_s
-        self.ok = False
+    def __init__(self, torch, device_index: int, period_ms: int = 20):
+        import subprocess
+        self.subprocess = subprocess
+        self.period = period_ms
+        self.index = device_index
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            h = None
-            try:
-                bus = torch.cuda.get_device_properties(device_index).pci_bus_id
-                h = pynvml.nvmlDeviceGetHandleByPciBusId(bus)
-            except Exception:
-                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-                idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
-                h = pynvml.nvmlDeviceGetHandleByIndex(idx)
-            self.h = h
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+            self.sel = ["--id=" + bus] if bus else []
         except Exception:
-            self.max_mhz = None
-
-    def _reasons(self):
-        f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
-        return f(self.h)
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                self.reasons |= int(self._reasons())
-            except Exception:
-                pass
-            time.sleep(self.period)
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            first = vis.split(",")[device_index] if vis else str(device_index)
+            self.sel = ["--id=" + first]
+        self.lines = []
+        self.first = []
 
     def __enter__(self):
-        if self.ok:
-            self._stop = threading.Event()
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        try:
+            self.proc = self.subprocess.Popen(
+                ["nvidia-smi", *self.sel, "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 f"-lms={self.period}"], stdout=self.subprocess.PIPE, stderr=self.subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        # the first sample marks that the sampler runs before the timed region starts
+        first = self.proc.stdout.readline()
+        self.first = [first] if first.strip() else []
         return self
 
     def __exit__(self, *exc):
-        if self.ok:
-            self._stop.set()
-            self._t.join()
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = self.first + [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
-        names = [n for bit, n in self.REASONS.items() if self.reasons & bit and n != "gpu_idle"]
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": names, "samples": len(self.samples)}
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
 
 
 def dist_setup(torch):
@@ -247,6 +250,14 @@ def run_reference(args):
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def launches_per_step(T: int, ids_given: bool) -> int:
+    """Kernels colibri_moe_layer launches per call: q8 (+ router logits), selection and
+    bucketing (one kernel for T <= 32), gate/up, down, combine."""
+    if ids_given:
+        return 5
+    return 5 if T <= 32 else 6
 
 
 def workload_config(spec, workload, T):
@@ -402,7 +413,7 @@ def run_colibri(args):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * spec.d * 4,
                     "d2h_bytes_per_step": T * spec.d * 4, "steps": KE,
                     "path": "colibri_moe_layer via the Python binding, eager launches"},
-            "gpu_launches": 7 * K,
+            "gpu_launches": launches_per_step(T, False) * K,
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -114,7 +114,7 @@ int colibri_q8_quantize(const float *x, int rows, int cols, int8_t *q, float *sc
  *   (or s_i * routed_scale when norm_topk = 0).
  *   Softmax mode: top_k largest logits (ties: lower index); w_i = softmax over all E
  *   logits at i (renormalised over the k when norm_topk = 1) * routed_scale.
- *   x       device fp32 [T][d];  Wr device fp32 [E][d], 16-byte aligned
+ *   x       device fp32 [T][d], Wr device fp32 [E][d], both 16-byte aligned
  *   bias    device fp32 [E] or NULL (zero); ignored in softmax mode
  *   logits  device fp32 [T][E] (out; also the kernel's scratch)
  *   ids     device int32 [T][top_k] (out), w device fp32 [T][top_k] (out)
@@ -140,6 +140,8 @@ size_t colibri_moe_workspace_bytes(const colibri_layer_cfg *cfg, int T_max);
  *   shared   host pointer to one colibri_expert of intermediate size shared_ffn whose
  *            members are device pointers; NULL when cfg->has_shared == 0
  *   ids, w   device [T][top_k]: outputs of the router, or inputs when ids_given != 0
+ *            (then the k ids of a token must be distinct and in [0, E); others set the
+ *            device error flag)
  *   out      device fp32 [T][d]
  *   workspace  device, >= colibri_moe_workspace_bytes(cfg, T) bytes, 256-byte aligned;
  *            owned by the caller, must not be shared by calls that overlap on the GPU
@@ -203,10 +205,12 @@ int colibri_moe_workspace_view(const colibri_layer_cfg *cfg, int T_max, colibri_
 #define COLIBRI_PROFILE_KERNELS 7
 int colibri_moe_profile_enable(int on);
 
-/* Milliseconds of each kernel of the most recent profiled call, after waiting for it:
+/* Milliseconds of each step of the most recent profiled call, after waiting for it:
  * ms[0] q8 of x, [1] router logits, [2] router selection, [3] bucketing, [4] gate/up,
- * [5] down, [6] combine. A kernel the call skipped (the router when ids are given)
- * reads about 0. n must be >= COLIBRI_PROFILE_KERNELS. */
+ * [5] down, [6] combine. Steps fused into one kernel report their time in the first of
+ * their slots (with the router, q8 rides in the logits kernel; for T <= 32 bucketing
+ * rides in the selection kernel); skipped and fused-away slots read about 0.
+ * n must be >= COLIBRI_PROFILE_KERNELS. */
 int colibri_moe_profile_read(float *ms, int n);
 
 /* Test export: int32 group dots of a packed int4 matrix with one int8 vector, computed

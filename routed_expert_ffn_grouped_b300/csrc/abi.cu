@@ -2,6 +2,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "workspace.h"
 
@@ -86,6 +88,8 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     L.sx = take(4 * (size_t)T * (d / G));
     L.xc = take(4 * (size_t)T * (d / G));
     L.logits = take(4 * (size_t)T * E);
+    L.s = take(4 * (size_t)T * E);
+    L.c = take(4 * (size_t)T * E);
     L.offsets = take(4 * (E + 1));
     L.pairs = take(4 * (size_t)T * K);
     L.slots = take(sizeof(Slot) * nslots);
@@ -158,27 +162,92 @@ int colibri_q8_quantize(const float *x, int rows, int cols, int8_t *q, float *sc
     return cuda_status(cudaGetLastError());
 }
 
-static int launch_router(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
-                         const float *bias, float *logits, int32_t *ids, float *w, int *err,
-                         cudaStream_t s, int prof_at)
+// Raises a kernel's dynamic shared memory limit to `bytes` whenever a launch needs more
+// than the largest limit set so far (the limits only grow). The default limit covers
+// 48 KB of static plus dynamic shared memory together, so even a launch just under it
+// sets the attribute.
+// Tracked per device: the attribute belongs to the device's context.
+constexpr int kMaxDev = 64;
+struct SmemLimits {
+    size_t have[kMaxDev] = {};
+};
+
+static bool smem_attr(const void *fn, size_t bytes, SmemLimits &lim)
 {
-    RouterArgs ra{x, T, cfg->d, cfg->n_exp, Wr, logits, err};
-    k_router_logits<<<cfg->n_exp, 32, (size_t)cfg->d * 4, s>>>(ra);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
+        return false;
+    if (bytes <= lim.have[dev])
+        return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+        return false;
+    lim.have[dev] = bytes;
+    return true;
+}
+
+// Number of SMs of the current device (cached per device).
+static int sm_count(int *out)
+{
+    static int cache[kMaxDev] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
         return COLIBRI_E_CUDA;
-    if (prof_at >= 0 && prof_mark(prof_at, s))
+    if (!cache[dev] && cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return COLIBRI_E_CUDA;
-    SelectArgs sa{logits, cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : bias, T, cfg->n_exp,
-                  cfg->top_k, cfg->n_group, cfg->topk_group, cfg->router, cfg->norm_topk,
-                  cfg->routed_scale, ids, w};
-    constexpr int SEL_WARPS = 4;
-    k_router_select<<<(T + SEL_WARPS - 1) / SEL_WARPS, 32 * SEL_WARPS, 0, s>>>(sa);
-    if (cudaGetLastError() != cudaSuccess)
-        return COLIBRI_E_CUDA;
-    if (prof_at >= 0 && prof_mark(prof_at + 1, s))
-        return COLIBRI_E_CUDA;
+    *out = cache[dev];
     return COLIBRI_OK;
+}
+
+// Token rows of x that k_route_logits stages per pass: up to 96 KB of x, at least one row.
+static int route_xt(int d, int T)
+{
+    int xt = (96 * 1024) / (d * 4);
+    xt = xt < 1 ? 1 : xt;
+    xt = xt > 32 ? 32 : xt;
+    return xt > T ? T : xt;
+}
+
+// Router logits (+ s and c when s_arr is given, + q8 of x when q8.x is set).
+static int launch_route_logits(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                               const float *bias, float *logits, float *s_arr, float *c_arr,
+                               const Q8Args &q8, int *err, cudaStream_t s)
+{
+    static SmemLimits have;
+    const int xt = route_xt(cfg->d, T);
+    const size_t smem = (size_t)cfg->d * 4 * (size_t)(1 + xt);
+    if (!smem_attr((const void *)k_route_logits, smem, have))
+        return COLIBRI_E_CUDA;
+    const bool sig = cfg->router != COLIBRI_ROUTER_SOFTMAX;
+    RouterArgs ra{x, T, cfg->d, cfg->n_exp, xt, Wr, sig ? bias : nullptr, logits,
+                  sig ? s_arr : nullptr, sig ? c_arr : nullptr, q8, err};
+    k_route_logits<<<cfg->n_exp, 128, smem, s>>>(ra);
+    return cuda_status(cudaGetLastError());
+}
+
+static SelectArgs select_args(const colibri_layer_cfg *cfg, int T, const float *logits, const float *s_arr,
+                              const float *c_arr, const float *bias, int32_t *ids, float *w)
+{
+    const bool sig = cfg->router != COLIBRI_ROUTER_SOFTMAX;
+    return SelectArgs{logits, sig ? s_arr : nullptr, sig ? c_arr : nullptr, sig ? bias : nullptr, T,
+                      cfg->n_exp, cfg->top_k, cfg->n_group, cfg->topk_group, cfg->router, cfg->norm_topk,
+                      cfg->routed_scale, ids, w};
+}
+
+static int launch_select(const SelectArgs &sa, cudaStream_t s)
+{
+    constexpr int SEL_WARPS = 4;
+    k_router_select<<<(sa.T + SEL_WARPS - 1) / SEL_WARPS, 32 * SEL_WARPS, 0, s>>>(sa);
+    return cuda_status(cudaGetLastError());
+}
+
+static int launch_router(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                         const float *bias, float *logits, int32_t *ids, float *w, cudaStream_t s)
+{
+    const Q8Args none{};
+    int rc = launch_route_logits(cfg, x, T, Wr, bias, logits, nullptr, nullptr, none, nullptr, s);
+    if (rc)
+        return rc;
+    return launch_select(select_args(cfg, T, logits, nullptr, nullptr, bias, ids, w), s);
 }
 
 int colibri_router_topk(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
@@ -188,9 +257,9 @@ int colibri_router_topk(const colibri_layer_cfg *cfg, const float *x, int T, con
         return COLIBRI_E_INVAL;
     if (T == 0)
         return COLIBRI_OK;
-    if (!x || !Wr || !logits || !ids || !w || !aligned(Wr, 16))
+    if (!x || !Wr || !logits || !ids || !w || !aligned(Wr, 16) || !aligned(x, 16))
         return COLIBRI_E_INVAL;
-    return launch_router(cfg, x, T, Wr, bias, logits, ids, w, nullptr, (cudaStream_t)stream, -1);
+    return launch_router(cfg, x, T, Wr, bias, logits, ids, w, (cudaStream_t)stream);
 }
 
 size_t colibri_moe_workspace_bytes(const colibri_layer_cfg *cfg, int T_max)
@@ -262,62 +331,99 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
 
     if (prof_mark(0, s))
         return COLIBRI_E_CUDA;
-    // a1: q8 of x (plain codes + even/odd codes + corrections); clears the error flag
     Q8Args qa{x, T, d, reinterpret_cast<int8_t *>(ws + L.qx), reinterpret_cast<float *>(ws + L.sx),
               reinterpret_cast<int8_t *>(ws + L.qx_eo), reinterpret_cast<int *>(ws + L.xc), err};
-    const long groups = (long)T * (d / G);
-    k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
-    if (cudaGetLastError() != cudaSuccess || prof_mark(1, s))
-        return COLIBRI_E_CUDA;
-
-    // a2-a3: router
-    if (!ids_given) {
-        int rc = launch_router(cfg, x, T, Wr, bias, reinterpret_cast<float *>(ws + L.logits), ids, w,
-                               err, s, g_prof.on ? 2 : -1);
-        if (rc)
-            return rc;
-    } else if (prof_mark(2, s) || prof_mark(3, s)) {
-        return COLIBRI_E_CUDA;
-    }
-
-    // a4: bucketing and slot list
-    const int down_blocks = (d + DN_ROWS - 1) / DN_ROWS;
+    const int down_blocks = (d + DN_ITEM_ROWS - 1) / DN_ITEM_ROWS;
     BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks,
                   reinterpret_cast<int32_t *>(ws + L.offsets), reinterpret_cast<int32_t *>(ws + L.pairs),
                   reinterpret_cast<Slot *>(ws + L.slots), reinterpret_cast<Counters *>(ws + L.counters), err};
     const size_t bsm = (size_t)34 * E * sizeof(int);
-    static bool bucket_attr_set = false;
-    if (bsm > 48 * 1024 && !bucket_attr_set) {
-        if (cudaFuncSetAttribute(k_bucket, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bsm) !=
-            cudaSuccess)
+    if (ids_given) {
+        // a1: q8 of x (plain codes + even/odd codes + corrections); clears the error flag
+        const long groups = (long)T * (d / G);
+        k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
+        if (cudaGetLastError() != cudaSuccess || prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s))
             return COLIBRI_E_CUDA;
-        bucket_attr_set = true;
+    } else {
+        // a1-a2: router logits with sigmoid scores, q8 of x on the side; clears the error flag
+        float *lg = reinterpret_cast<float *>(ws + L.logits);
+        float *sv = reinterpret_cast<float *>(ws + L.s);
+        float *cv = reinterpret_cast<float *>(ws + L.c);
+        qa.err = nullptr;
+        if (prof_mark(1, s))
+            return COLIBRI_E_CUDA;
+        int rc = launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, qa, err, s);
+        if (rc || prof_mark(2, s))
+            return COLIBRI_E_CUDA;
+        const SelectArgs sa = select_args(cfg, T, lg, sv, cv, bias, ids, w);
+        if (T <= 32) {
+            // a3-a4 fused for decode: selection and bucketing in one CTA
+            static SmemLimits have;
+            const size_t sm = std::max(bsm, select_cta_smem_bytes(E));
+            if (!smem_attr((const void *)k_select_bucket, sm, have))
+                return COLIBRI_E_CUDA;
+            k_select_bucket<<<1, 1024, sm, s>>>(sa, ba);
+            if (cudaGetLastError() != cudaSuccess || prof_mark(3, s) || prof_mark(4, s))
+                return COLIBRI_E_CUDA;
+            goto experts;
+        }
+        if (launch_select(sa, s) || prof_mark(3, s))
+            return COLIBRI_E_CUDA;
     }
-    k_bucket<<<1, 1024, bsm, s>>>(ba);
-    if (cudaGetLastError() != cudaSuccess || prof_mark(4, s))
-        return COLIBRI_E_CUDA;
-
+    {
+        // a4: bucketing and slot list
+        static SmemLimits have;
+        if (!smem_attr((const void *)k_bucket, bsm, have))
+            return COLIBRI_E_CUDA;
+        k_bucket<<<1, 1024, bsm, s>>>(ba);
+        if (cudaGetLastError() != cudaSuccess || prof_mark(4, s))
+            return COLIBRI_E_CUDA;
+    }
+experts:
     // a6-a8: gate/up (+ SwiGLU + q8 h), then down, for every slot (shared expert first)
     colibri_expert sh{};
     if (cfg->has_shared)
         sh = *shared;
     const int routed_slots = T * K < E ? T * K : E;
+    int n_sm = 0;
+    if (sm_count(&n_sm))
+        return COLIBRI_E_CUDA;
     const int gu_items = (cfg->has_shared ? cfg->shared_ffn / G : 0) + routed_slots * (cfg->ffn / G);
-    GateUpArgs ga{experts, sh, d, cfg->ffn, cfg->shared_ffn, T, K, cfg->has_shared, (int)L.fmax,
-                  reinterpret_cast<const Slot *>(ws + L.slots), reinterpret_cast<const Counters *>(ws + L.counters),
-                  reinterpret_cast<const int32_t *>(ws + L.pairs), reinterpret_cast<const int8_t *>(ws + L.qx_eo),
-                  reinterpret_cast<const float *>(ws + L.sx), reinterpret_cast<const int *>(ws + L.xc),
-                  reinterpret_cast<int8_t *>(ws + L.hq), reinterpret_cast<int8_t *>(ws + L.hq_eo),
-                  reinterpret_cast<float *>(ws + L.hs), reinterpret_cast<int *>(ws + L.hc)};
-    if (launch_gateup(ga, gu_items, s) != cudaSuccess || prof_mark(5, s))
+    StreamArgs st{};
+    st.experts = experts;
+    st.shared = sh;
+    st.d = d;
+    st.ffn = cfg->ffn;
+    st.shared_ffn = cfg->shared_ffn;
+    st.T = T;
+    st.K = K;
+    st.has_shared = cfg->has_shared;
+    st.fmax = (int)L.fmax;
+    st.slots = reinterpret_cast<const Slot *>(ws + L.slots);
+    st.counters = reinterpret_cast<const Counters *>(ws + L.counters);
+    st.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
+    st.err = err;
+    StreamArgs ga = st;
+    ga.aq_eo = reinterpret_cast<const int8_t *>(ws + L.qx_eo);
+    ga.as = reinterpret_cast<const float *>(ws + L.sx);
+    ga.ac = reinterpret_cast<const int *>(ws + L.xc);
+    ga.act_stride = d;
+    ga.act_groups = d / G;
+    ga.hq = reinterpret_cast<int8_t *>(ws + L.hq);
+    ga.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
+    ga.hs = reinterpret_cast<float *>(ws + L.hs);
+    ga.hc = reinterpret_cast<int *>(ws + L.hc);
+    if (launch_stream(MODE_GATEUP, ga, gu_items, n_sm, s) != cudaSuccess || prof_mark(5, s))
         return COLIBRI_E_CUDA;
     const int dn_items = (routed_slots + (cfg->has_shared ? 1 : 0)) * down_blocks;
-    DownArgs da{experts, sh, d, cfg->ffn, cfg->shared_ffn, T, K, cfg->has_shared, (int)L.fmax,
-                reinterpret_cast<const Slot *>(ws + L.slots), reinterpret_cast<const Counters *>(ws + L.counters),
-                reinterpret_cast<const int32_t *>(ws + L.pairs), reinterpret_cast<const int8_t *>(ws + L.hq_eo),
-                reinterpret_cast<const float *>(ws + L.hs), reinterpret_cast<const int *>(ws + L.hc),
-                reinterpret_cast<float *>(ws + L.y)};
-    if (launch_down(da, dn_items, s) != cudaSuccess || prof_mark(6, s))
+    StreamArgs da = st;
+    da.aq_eo = reinterpret_cast<const int8_t *>(ws + L.hq_eo);
+    da.as = reinterpret_cast<const float *>(ws + L.hs);
+    da.ac = reinterpret_cast<const int *>(ws + L.hc);
+    da.act_stride = (long)L.fmax;
+    da.act_groups = (int)L.fmax / G;
+    da.y = reinterpret_cast<float *>(ws + L.y);
+    if (launch_stream(MODE_DOWN, da, dn_items, n_sm, s) != cudaSuccess || prof_mark(6, s))
         return COLIBRI_E_CUDA;
 
     // a9: combine

@@ -19,13 +19,18 @@ struct Q8Args {
 struct RouterArgs {
     const float *x;
     int T, d, E;
+    int xt;              // token rows of x staged in shared memory per pass
     const float *Wr;
-    float *logits;
+    const float *bias;   // sigmoid mode; may be null (zero bias)
+    float *logits;       // [T][E]
+    float *s, *c;        // [T][E] sigmoid and biased score, or null (softmax mode)
+    Q8Args q8;           // q8 of x as a side job when q8.x != null
     int *err;
 };
 
 struct SelectArgs {
     const float *logits;
+    const float *s, *c;  // [T][E] from k_route_logits, or null: computed from logits
     const float *bias;
     int T, E, K, n_group, topk_group, router, norm_topk;
     float routed_scale;
@@ -43,37 +48,37 @@ struct BucketArgs {
     int *err;
 };
 
-// Decode gate/up: one CTA per (slot, 32-row block of f). Activations: even/odd codes,
-// scales and corrections of x per token.
-struct GateUpArgs {
+// Streaming decode GEMVs (kernels_stream.cu).
+enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
+constexpr int DN_ITEM_ROWS = 64;  // rows of d per down item
+constexpr int STREAM_TC = 4;      // tokens per register chunk
+constexpr int STREAM_TPAD = 32;   // gate/up tokens per pass over an item's weights
+
+struct StreamArgs {
     const colibri_expert *experts;
     colibri_expert shared;
     int d, ffn, shared_ffn, T, K, has_shared, fmax;
     const Slot *slots;
     const Counters *counters;
     const int32_t *pairs;
-    const int8_t *xq_eo;
-    const float *xs;
-    const int *xc;
-    int8_t *hq;     // [pairs_total][fmax] plain codes
-    int8_t *hq_eo;  // [pairs_total][fmax] even/odd codes
-    float *hs;      // [pairs_total][fmax/32]
-    int *hc;        // [pairs_total][fmax/32]
+    // activation codes in even/odd order, their scales and +8 corrections: x for gate/up
+    // (row = token), q8(h) for down (row = pair)
+    const int8_t *aq_eo;
+    const float *as;
+    const int *ac;
+    long act_stride;   // bytes between activation rows of aq_eo
+    int act_groups;    // groups between activation rows of as / ac
+    int8_t *hq, *hq_eo;  // gate/up outputs
+    float *hs;
+    int *hc;
+    float *y;          // down output [pairs_total][d]
+    int *err;
+    // set by launch_stream
+    int stage_bytes, ring, tpad;
 };
 
-// Decode down: one CTA per (slot, 64-row block of d).
-struct DownArgs {
-    const colibri_expert *experts;
-    colibri_expert shared;
-    int d, ffn, shared_ffn, T, K, has_shared, fmax;
-    const Slot *slots;
-    const Counters *counters;
-    const int32_t *pairs;
-    const int8_t *hq_eo;
-    const float *hs;
-    const int *hc;
-    float *y;  // [pairs_total][d]
-};
+size_t stream_stage_bytes(int mode, int d, int fmax);
+cudaError_t launch_stream(int mode, StreamArgs a, int max_items, int n_sm, cudaStream_t s);
 
 struct CombineArgs {
     const float *y;
@@ -82,20 +87,15 @@ struct CombineArgs {
     float *out;
 };
 
-constexpr int GU_ROWS = 32;     // rows of f per gate/up item (one h group)
-constexpr int GU_WARPS = 8;
-constexpr int DN_ROWS = 64;     // rows of d per down item
-constexpr int DN_WARPS = 8;
-constexpr int TOK_CHUNK = 32;   // tokens held in shared memory per gate/up pass
 
 __global__ void k_q8(Q8Args a);
-__global__ void k_router_logits(RouterArgs a);
+__global__ void k_route_logits(RouterArgs a);
+__global__ void k_select_bucket(SelectArgs sa, BucketArgs ba);
+size_t select_cta_smem_bytes(int E);
 __global__ void k_router_select(SelectArgs a);
 __global__ void k_bucket(BucketArgs a);
 __global__ void k_combine(CombineArgs a);
 __global__ void k_debug_dots(const uint8_t *w, const int8_t *qa, int rows, int cols, int32_t *dots);
 
-cudaError_t launch_gateup(const GateUpArgs &a, int grid, cudaStream_t s);
-cudaError_t launch_down(const DownArgs &a, int grid, cudaStream_t s);
 
 }  // namespace clb

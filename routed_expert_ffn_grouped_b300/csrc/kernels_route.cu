@@ -34,63 +34,106 @@ __global__ void __launch_bounds__(256) k_q8(Q8Args a)
     }
 }
 
-// ---- router logits ----------------------------------------------------------------
-// One warp per expert row of Wr (staged in shared memory by a bulk copy), all T tokens.
-// Lane j runs the fmaf chain over k = j, j+32, ... ascending for each token, then the
-// warp joins the 32 chains with a butterfly (offsets 16, 8, 4, 2, 1); lane 0 holds the
-// same value as the halving tree (fp32 addition is commutative).
-__global__ void __launch_bounds__(32) k_router_logits(RouterArgs a)
+// ---- router logits (+ the fp64 sigmoid, + q8 of x as a side job) --------------------
+// One CTA per expert e, four warps. The CTA bulk-copies Wr[e] and a chunk of XT token
+// rows of x (contiguous in x) into shared memory, then warp w takes the chunk's tokens
+// w, w+4, ...: lane j runs the fmaf chain over k = j, j+32, ... ascending, and the warp
+// joins the 32 chains with a butterfly (offsets 16, 8, 4, 2, 1); lane 0 then holds the
+// value of the halving tree (fp32 addition is commutative). In sigmoid mode lane 0 also
+// evaluates s = fp32(1/(1+exp(-l))) in fp64 and c = s + bias[e], so that the fp64 work
+// is spread over all CTAs. Before that, the CTAs quantise x (one warp per 32-group) when
+// the layer asks for it.
+constexpr int RL_WARPS = 4;
+
+__device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane)
+{
+    const int ng = a.cols / G;
+    const long row = gw / ng;
+    const int g = (int)(gw % ng);
+    const long base = row * a.cols + (long)g * G;
+    const float x = a.x[base + lane];
+    const float amax = warp_max(fabsf(x));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const int q = q8_code(x, d);
+    a.q[base + lane] = (int8_t)q;
+    if (lane == 0)
+        a.scale[row * ng + g] = d;
+    if (a.q_eo) {
+        a.q_eo[base + eo_pos(lane)] = (int8_t)q;
+        const int s = warp_sum_i(q);
+        if (lane == 0)
+            a.corr[row * ng + g] = 8 * s;
+    }
+}
+
+__global__ void __launch_bounds__(32 * RL_WARPS) k_route_logits(RouterArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    float *wrow = reinterpret_cast<float *>(smem_raw);
     __shared__ __align__(8) uint64_t bar;
-    const int e = blockIdx.x;
-    const int lane = threadIdx.x;
-    const int d = a.d;
-    if (lane == 0) {
+    const int d = a.d, e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *wrow = reinterpret_cast<float *>(smem_raw);
+    float *xs = wrow + d;
+    if (a.err && blockIdx.x == 0 && threadIdx.x == 0)
+        *a.err = 0;  // the first kernel of a layer call clears the flag
+    if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
     }
-    __syncwarp();
-    const uint32_t bytes = (uint32_t)d * 4u;
-    if (lane == 0) {
-        mbar_arrive_expect_tx(&bar, bytes);
-        const char *src = reinterpret_cast<const char *>(a.Wr + (long)e * d);
-        for (uint32_t off = 0; off < bytes; off += 32768u) {
-            uint32_t n = bytes - off < 32768u ? bytes - off : 32768u;
-            bulk_g2s(reinterpret_cast<char *>(wrow) + off, src + off, n, &bar);
-        }
+    __syncthreads();
+    // q8 side job: warp-granular, grid-strided over the T*d/32 groups of x
+    if (a.q8.x) {
+        const long n = (long)a.T * (d / G);
+        for (long gw = (long)blockIdx.x * RL_WARPS + warp; gw < n; gw += (long)gridDim.x * RL_WARPS)
+            q8_group(a.q8, gw, lane);
     }
-    if (!mbar_wait(&bar, 0)) {
-        if (lane == 0 && a.err)
-            atomicOr(a.err, ERR_WAIT_TIMEOUT);
-        mbar_wait(&bar, 0);  // bounded second wait for the copy still in flight
-        return;
-    }
-    constexpr int TT = 8;
-    for (int t0 = 0; t0 < a.T; t0 += TT) {
-        float acc[TT];
-#pragma unroll
-        for (int i = 0; i < TT; ++i)
-            acc[i] = 0.0f;
-        const int nt = min(TT, a.T - t0);
-        for (int k = lane; k < d; k += 32) {
-            const float wv = wrow[k];
-#pragma unroll
-            for (int i = 0; i < TT; ++i)
-                if (i < nt)
-                    acc[i] = fmaf(__ldg(a.x + (long)(t0 + i) * d + k), wv, acc[i]);
+    const uint32_t row_bytes = (uint32_t)d * 4u;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t0 = 0; t0 < a.T; t0 += a.xt) {
+        const int nt = min(a.xt, a.T - t0);
+        if (threadIdx.x == 0) {
+            const uint32_t xbytes = row_bytes * (uint32_t)nt;
+            mbar_arrive_expect_tx(&bar, (t0 == 0 ? row_bytes : 0u) + xbytes);
+            if (t0 == 0) {
+                const char *src = reinterpret_cast<const char *>(a.Wr + (long)e * d);
+                for (uint32_t off = 0; off < row_bytes; off += 32768u)
+                    bulk_g2s(reinterpret_cast<char *>(wrow) + off, src + off, min(32768u, row_bytes - off), &bar);
+            }
+            const char *xsrc = reinterpret_cast<const char *>(a.x + (long)t0 * d);
+            for (uint32_t off = 0; off < xbytes; off += 32768u)
+                bulk_g2s(reinterpret_cast<char *>(xs) + off, xsrc + off, min(32768u, xbytes - off), &bar);
         }
-#pragma unroll
-        for (int i = 0; i < TT; ++i) {
-            float v = acc[i];
+        if (!mbar_wait(&bar, phase)) {
+            ok = false;
+            if (lane == 0 && a.err)
+                atomicOr(a.err, ERR_WAIT_TIMEOUT);
+            mbar_wait(&bar, phase);  // bounded second wait for the copies still in flight
+            break;
+        }
+        phase ^= 1u;
+        for (int i = warp; i < nt; i += RL_WARPS) {
+            const float *xr = xs + (long)i * d;
+            float acc = 0.0f;
+#pragma unroll 8
+            for (int k = lane; k < d; k += 32)
+                acc = fmaf(xr[k], wrow[k], acc);
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1)
-                v = v + __shfl_xor_sync(FULL, v, o);
-            if (lane == 0 && i < nt)
-                a.logits[(long)(t0 + i) * a.E + e] = v;
+                acc = acc + __shfl_xor_sync(FULL, acc, o);
+            if (lane == 0) {
+                const long o = (long)(t0 + i) * a.E + e;
+                a.logits[o] = acc;
+                if (a.s) {
+                    const float sv = (float)(1.0 / (1.0 + exp(-(double)acc)));
+                    a.s[o] = sv;
+                    a.c[o] = sv + (a.bias ? a.bias[e] : 0.0f);
+                }
+            }
         }
+        __syncthreads();  // the chunk buffer is refilled next
     }
+    (void)ok;
 }
 
 // (value, index) order of the selection: larger value first, then lower index.
@@ -112,21 +155,16 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i)
     }
 }
 
-// ---- router selection -------------------------------------------------------------
-// One warp per token. Lane j owns experts e = j + 32 r. Group scores are computed by
-// one lane per group over the group's contiguous experts (staged in shared memory);
-// group and expert top-k are warp-shuffle argmax rounds with the (value, index) order.
-constexpr int SEL_WARPS = 4;
-
-__global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
+// ---- router selection (one warp per token) ----------------------------------------
+// Lane j owns experts e = j + 32 r. Sigmoid mode reads s and c from the logits kernel
+// when it wrote them, else evaluates them here the same way;
+// group scores are computed by one lane per group over the group's contiguous experts
+// (staged in shared memory); group and expert top-k are warp-shuffle argmax rounds with
+// the (value, index) order. sc: this warp's shared row of at least E floats.
+__device__ void select_token(const SelectArgs &a, int t, int lane, float *sc)
 {
-    __shared__ float s_c[SEL_WARPS][1024];
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * SEL_WARPS + w;
-    if (t >= a.T)
-        return;
     const int E = a.E, R = (E + 31) / 32;
-    const float *l = a.logits + (long)t * E;
+    const long row = (long)t * E;
     float sv[32], cv[32];
     bool avail[32];
 #pragma unroll
@@ -136,16 +174,17 @@ __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
         avail[r] = false;
         const int e = lane + 32 * r;
         if (r < R && e < E) {
-            const float lv = l[e];
             if (a.router == COLIBRI_ROUTER_SOFTMAX) {
-                sv[r] = lv;
-                cv[r] = lv;
+                sv[r] = cv[r] = a.logits[row + e];
+            } else if (a.s) {
+                sv[r] = a.s[row + e];
+                cv[r] = a.c[row + e];
             } else {
-                sv[r] = (float)(1.0 / (1.0 + exp(-(double)lv)));
+                sv[r] = (float)(1.0 / (1.0 + exp(-(double)a.logits[row + e])));
                 cv[r] = sv[r] + (a.bias ? a.bias[e] : 0.0f);
             }
             avail[r] = true;
-            s_c[w][e] = cv[r];
+            sc[e] = cv[r];
         }
     }
     __syncwarp();
@@ -157,7 +196,7 @@ __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
         if (lane < a.n_group) {
             float m1 = -INFINITY, m2 = -INFINITY;
             for (int i = 0; i < gs; ++i) {
-                const float v = s_c[w][lane * gs + i];
+                const float v = sc[lane * gs + i];
                 if (v > m1) {
                     m2 = m1;
                     m1 = v;
@@ -184,11 +223,10 @@ __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
                 avail[r] = false;
         }
     }
-    // top-k: k rounds of warp argmax over the remaining candidates
+    // top-k: k rounds of warp argmax over the remaining candidates; lane i keeps pick i
     const int K = a.K;
-    double sel_sum = 0.0;
-    int picks[32];
-    float pick_s[32];
+    int my_pick = -1;
+    float my_s = 0.0f;
     for (int i = 0; i < K; ++i) {
         float bv = 0.0f;
         int bi = -1, br = -1;
@@ -213,13 +251,16 @@ __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
                     s_pick = sv[r];
                 }
         }
-        const int src = wi >= 0 ? (wi & 31) : 0;
-        s_pick = __shfl_sync(FULL, s_pick, src);
-        picks[i < 32 ? i : 31] = wi;
-        pick_s[i < 32 ? i : 31] = s_pick;
+        s_pick = __shfl_sync(FULL, s_pick, wi >= 0 ? (wi & 31) : 0);
+        if (lane == i) {
+            my_pick = wi;
+            my_s = s_pick;
+        }
     }
+    // weights: lane i < K holds pick i; sums in selection order (lane 0 first)
+    double p = (double)my_s, scale_sum = 0.0;
     if (a.router == COLIBRI_ROUTER_SOFTMAX) {
-        // softmax over all E logits in fp64
+        const float *l = a.logits + row;
         double m = -INFINITY;
         for (int e = lane; e < E; e += 32)
             m = fmax(m, (double)l[e]);
@@ -232,31 +273,28 @@ __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             z += __shfl_xor_sync(FULL, z, o);
-        double sel = 0.0;
-        for (int i = 0; i < K; ++i)
-            sel += exp((double)pick_s[i] - m) / z;
-        if (lane == 0) {
-            for (int i = 0; i < K; ++i) {
-                double p = exp((double)pick_s[i] - m) / z;
-                if (a.norm_topk)
-                    p = p / sel;
-                a.ids[(long)t * K + i] = picks[i];
-                a.w[(long)t * K + i] = (float)(p * (double)a.routed_scale);
-            }
-        }
-    } else {
-        for (int i = 0; i < K; ++i)
-            sel_sum += (double)pick_s[i];
-        if (lane == 0) {
-            for (int i = 0; i < K; ++i) {
-                double p = (double)pick_s[i];
-                if (a.norm_topk)
-                    p = p / sel_sum;
-                a.ids[(long)t * K + i] = picks[i];
-                a.w[(long)t * K + i] = (float)(p * (double)a.routed_scale);
-            }
-        }
+        p = lane < K ? exp(p - m) / z : 0.0;
     }
+    for (int i = 0; i < K; ++i)
+        scale_sum += __shfl_sync(FULL, lane < K ? p : 0.0, i);
+    if (lane < K) {
+        if (a.norm_topk)
+            p = p / scale_sum;
+        a.ids[(long)t * K + lane] = my_pick;
+        a.w[(long)t * K + lane] = (float)(p * (double)a.routed_scale);
+    }
+}
+
+constexpr int SEL_WARPS = 4;
+
+__global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
+{
+    __shared__ float s_c[SEL_WARPS][1024];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * SEL_WARPS + w;
+    if (t >= a.T)
+        return;
+    select_token(a, t, lane, s_c[w]);
 }
 
 // ---- bucketing --------------------------------------------------------------------
@@ -265,9 +303,8 @@ __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
 // running base + the count of the same expert in earlier warps of the chunk + its rank
 // among equal lanes of its warp (__match_any_sync). Finally the slot list (shared
 // expert first, then routed experts in ascending id) and the item counts.
-__global__ void __launch_bounds__(1024) k_bucket(BucketArgs a)
+__device__ void bucket_body(const BucketArgs &a, int *sm)
 {
-    extern __shared__ int sm[];
     const int E = a.E;
     int *cnt = sm;              // [E]
     int *run = sm + E;          // [E]
@@ -284,9 +321,14 @@ __global__ void __launch_bounds__(1024) k_bucket(BucketArgs a)
         if (e < 0 || e >= E) {
             if (a.err)
                 atomicOr(a.err, ERR_BAD_ID);
-        }
-        else
+        } else {
             atomicAdd(&cnt[e], 1);
+            // a token must not list an expert twice
+            const long t0 = p - p % a.K;
+            for (long q = t0; q < p; ++q)
+                if (a.ids[q] == e && a.err)
+                    atomicOr(a.err, ERR_BAD_ID);
+        }
     }
     __syncthreads();
     // exclusive scan of cnt over E <= 1024 (one element per thread)
@@ -407,6 +449,151 @@ __global__ void __launch_bounds__(1024) k_bucket(BucketArgs a)
         ct.n_items_down = ct.n_slots * a.down_blocks;
         *a.counters = ct;
     }
+}
+
+__global__ void __launch_bounds__(1024) k_bucket(BucketArgs a)
+{
+    extern __shared__ int sm[];
+    bucket_body(a, sm);
+}
+
+// ---- decode selection with the whole CTA -----------------------------------------
+// The k-th pick of the sequential selection (repeatedly take the best remaining
+// candidate in the (value desc, index asc) order) is the candidate that exactly k others
+// beat. So each candidate's thread counts the allowed candidates that beat it and, if
+// that rank is below top_k, writes itself to position rank. Groups are kept the same way
+// (rank of the group score below topk_group). The CTA (1024 threads) takes TPR tokens per
+// round, Epad = E rounded up to 32 threads per token.
+//   smem (floats): per token slot c[Epad] | gscore[32] | kept[32] (int) | pick_id[32] (int)
+//   | pick_s[32].
+constexpr int SEL_SLOT_EXTRA = 128;
+
+__device__ void select_cta(const SelectArgs &a, float *smf)
+{
+    const int E = a.E, K = a.K, Epad = (E + 31) & ~31;
+    const int TPR = max(1, 1024 / Epad), tid = threadIdx.x;
+    const int slot = tid / Epad, e = tid % Epad, lane = tid & 31;
+    const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
+    const int gs = sig ? E / a.n_group : E;
+    float *base = smf + (long)slot * (Epad + SEL_SLOT_EXTRA);
+    float *cs = base;
+    float *gsc = base + Epad;
+    int *kept = reinterpret_cast<int *>(base + Epad + 32);
+    int *pick = reinterpret_cast<int *>(base + Epad + 64);
+    float *pick_s = base + Epad + 96;
+    for (int t0 = 0; t0 < a.T; t0 += TPR) {
+        const int t = t0 + slot;
+        const bool act = slot < TPR && t < a.T && e < E;
+        const long row = (long)t * E;
+        float sv = 0.0f, cv = 0.0f;
+        if (act) {
+            if (!sig) {
+                sv = cv = a.logits[row + e];
+            } else if (a.s) {
+                sv = a.s[row + e];
+                cv = a.c[row + e];
+            } else {
+                sv = (float)(1.0 / (1.0 + exp(-(double)a.logits[row + e])));
+                cv = sv + (a.bias ? a.bias[e] : 0.0f);
+            }
+            cs[e] = cv;
+        }
+        __syncthreads();
+        if (sig) {
+            if (act && e < a.n_group) {
+                // the two largest c of group e (a multiset: equal values count twice)
+                float m1 = -INFINITY, m2 = -INFINITY;
+                for (int i = 0; i < gs; ++i) {
+                    const float v = cs[e * gs + i];
+                    if (v > m1) {
+                        m2 = m1;
+                        m1 = v;
+                    } else if (v > m2) {
+                        m2 = v;
+                    }
+                }
+                gsc[e] = gs == 1 ? m1 : m1 + m2;
+            }
+            __syncthreads();
+            if (act && e < a.n_group) {
+                const float v = gsc[e];
+                int rank = 0;
+                for (int g = 0; g < a.n_group; ++g)
+                    rank += better(gsc[g], g, v, e) && g != e;
+                kept[e] = rank < a.topk_group;
+            }
+            __syncthreads();
+        }
+        if (act && (!sig || kept[e / gs])) {
+            int rank = 0;
+            if (sig) {
+                for (int g = 0; g < a.n_group; ++g) {
+                    if (!kept[g])
+                        continue;
+                    for (int i = g * gs; i < (g + 1) * gs; ++i)
+                        rank += better(cs[i], i, cv, e) && i != e;
+                }
+            } else {
+                for (int i = 0; i < E; ++i)
+                    rank += better(cs[i], i, cv, e) && i != e;
+            }
+            if (rank < K) {
+                pick[rank] = e;
+                pick_s[rank] = sv;
+            }
+        }
+        __syncthreads();
+        // weights: the token slot's first warp (sums in selection order on lane 0)
+        if (slot < TPR && t < a.T && e < 32) {
+            double m = 0.0, z = 1.0;
+            if (!sig) {
+                const float *l = a.logits + row;
+                m = -INFINITY;
+                for (int i = lane; i < E; i += 32)
+                    m = fmax(m, (double)l[i]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    m = fmax(m, __shfl_xor_sync(FULL, m, o));
+                z = 0.0;
+                for (int i = lane; i < E; i += 32)
+                    z += exp((double)l[i] - m);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    z += __shfl_xor_sync(FULL, z, o);
+            }
+            double p = 0.0;
+            if (lane < K)
+                p = sig ? (double)pick_s[lane] : exp((double)pick_s[lane] - m) / z;
+            double sum = 0.0;
+            for (int i = 0; i < K; ++i)
+                sum += __shfl_sync(FULL, p, i);
+            if (lane < K) {
+                if (a.norm_topk)
+                    p = p / sum;
+                a.ids[(long)t * K + lane] = pick[lane];
+                a.w[(long)t * K + lane] = (float)(p * (double)a.routed_scale);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+size_t select_cta_smem_bytes(int E)
+{
+    const int Epad = (E + 31) & ~31;
+    const int TPR = 1024 / Epad > 0 ? 1024 / Epad : 1;
+    return (size_t)TPR * (Epad + SEL_SLOT_EXTRA) * sizeof(float);
+}
+
+// Decode (T <= 32): selection of every token with the whole CTA, then bucketing. The
+// selection's shared arrays and the bucketing's counters use the same dynamic shared
+// memory, one after the other.
+__global__ void __launch_bounds__(1024) k_select_bucket(SelectArgs sa, BucketArgs ba)
+{
+    extern __shared__ int sm[];
+    select_cta(sa, reinterpret_cast<float *>(sm));
+    __syncthreads();  // ids in global memory are visible to the whole block
+    bucket_body(ba, sm);
 }
 
 }  // namespace clb

@@ -9,7 +9,7 @@ namespace clb {
 
 // Byte offsets (256-byte aligned) of the layer's intermediates in the workspace.
 struct WsLayout {
-    size_t err, counters, qx, qx_eo, sx, xc, logits, offsets, pairs, slots;
+    size_t err, counters, qx, qx_eo, sx, xc, logits, s, c, offsets, pairs, slots;
     size_t hq, hq_eo, hs, hc, y;
     size_t fmax, total;
 };

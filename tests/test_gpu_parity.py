@@ -200,6 +200,17 @@ def test_moe_layer_bad_id_reports(torch_cuda, C):
     assert C.colibri_workspace_status(dl.cfg, 1, ws) == C.OK    # read clears it
 
 
+def test_moe_layer_duplicate_id_reports(torch_cuda, C):
+    """A token listing the same expert twice is bad input: the device flag reports it."""
+    torch = torch_cuda
+    spec = synth.TINY
+    _, dl = dev_layer(C, spec)
+    ids = np.array([[0, 1, 2, 3], [5, 6, 5, 7]], np.int32)
+    w = np.full((2, 4), 0.5, np.float32)
+    _, _, _, ws = run_layer(torch, C, dl, synth.activations(spec, 0, 2), ids, w)
+    assert C.colibri_workspace_status(dl.cfg, 2, ws) == C.E_DEVICE
+
+
 def test_moe_layer_empty_and_deterministic(torch_cuda, C):
     torch = torch_cuda
     spec = synth.OLMOE
