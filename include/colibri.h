@@ -15,10 +15,16 @@
  *     memory, pinned host memory, streams); the library never frees caller memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *     Compute entry points only enqueue work on it and return without synchronising.
- *   - Layouts are row-major. A packed int4 weight matrix [out][in] stores row n as
- *     in/2 bytes; byte j holds element 2j in its low nibble and 2j+1 in its high
- *     nibble, each nibble the offset-binary code q+8 of q in [-8, 7]. Its scales are
- *     fp32 [out][in/32], one per 32 consecutive elements of a row.
+ *   - Activations are row-major. A packed int4 weight matrix W [R][K] (R = out, K = in,
+ *     both multiples of 32) is stored in row blocks of 32 rows, group-major inside a
+ *     block: the 16 bytes of group g (columns 32g..32g+31) of row r are at byte
+ *         ((r / 32) * (K / 32) + g) * 512 + (r % 32) * 16,
+ *     and byte j of them holds column 32g+2j in its low nibble and 32g+2j+1 in its high
+ *     nibble, each nibble the offset-binary code q+8 of q in [-8, 7]. Its fp32 scales,
+ *     one per row and group, are stored alike: S[r][g] at float
+ *         ((r / 32) * (K / 32) + g) * 32 + r % 32.
+ *     A warp reading group g of a row block then loads 512 contiguous bytes. The layout
+ *     is this library's choice: the pages fix the group scaling, not the byte order.
  *   - Every function returns COLIBRI_OK (0) or a negative COLIBRI_E_* code. Argument
  *     errors are detected on the host before anything is enqueued. Launch errors are
  *     returned as COLIBRI_E_CUDA. Errors found on the device (an expert id out of
@@ -65,10 +71,10 @@ typedef struct {
     int group;
 } colibri_layer_cfg;
 
-/* One expert's tensors (device pointers, 16-byte aligned): gate w1 [f][d/2], up w3
- * [f][d/2], down w2 [d][f/2] packed int4; scales s1 [f][d/32], s3 [f][d/32],
- * s2 [d][f/32] fp32. Group-scaled int4 container: aifrontierpost tutorial, "Step 3 --
- * Get a model"; the layer uses 32-element groups. */
+/* One expert's tensors (device pointers, 16-byte aligned), in the stored layout above:
+ * gate w1 [f][d], up w3 [f][d], down w2 [d][f] packed int4; scales s1 [f][d/32],
+ * s3 [f][d/32], s2 [d][f/32] fp32. Group-scaled int4 container: aifrontierpost tutorial,
+ * "Step 3 -- Get a model"; the layer uses 32-element groups. */
 typedef struct {
     const uint8_t *w1, *w3, *w2;
     const float *s1, *s3, *s2;
@@ -214,8 +220,9 @@ int colibri_moe_profile_enable(int on);
 int colibri_moe_profile_read(float *ms, int n);
 
 /* Test export: int32 group dots of a packed int4 matrix with one int8 vector, computed
- * by the decode GEMV's integer dot code.
- *   w device [rows][cols/2], qa device int8 [cols], dots device int32 [rows][cols/32]. */
+ * by the decode GEMVs' integer dot code.
+ *   w device, [rows][cols] in the stored layout (rows % 32 == 0), qa device int8 [cols],
+ *   dots device int32 [rows][cols/32] (row-major). */
 int colibri_debug_group_dots(const uint8_t *w, const int8_t *qa, int rows, int cols,
                              int32_t *dots, void *stream);
 

@@ -208,10 +208,10 @@ def colibri_moe_workspace_view(cfg: LayerCfg, T_max: int) -> WorkspaceView:
     return v
 
 
-def colibri_debug_group_dots(w, qa, dots, stream=None):
-    rows, half = w.shape
+def colibri_debug_group_dots(w, qa, dots, rows: int, cols: int, stream=None):
+    """w: a [rows][cols] packed int4 matrix in the stored layout (flat bytes)."""
     _check("colibri_debug_group_dots",
-           lib().colibri_debug_group_dots(_ptr(w), _ptr(qa), rows, 2 * half, _ptr(dots), _stream(stream)))
+           lib().colibri_debug_group_dots(_ptr(w), _ptr(qa), rows, cols, _ptr(dots), _stream(stream)))
 
 
 PROFILE_KERNELS = ("q8", "router_logits", "router_select", "bucket", "gateup", "down", "combine")

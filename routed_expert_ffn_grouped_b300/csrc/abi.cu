@@ -185,19 +185,6 @@ static bool smem_attr(const void *fn, size_t bytes, SmemLimits &lim)
     return true;
 }
 
-// Number of SMs of the current device (cached per device).
-static int sm_count(int *out)
-{
-    static int cache[kMaxDev] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
-        return COLIBRI_E_CUDA;
-    if (!cache[dev] && cudaDeviceGetAttribute(&cache[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return COLIBRI_E_CUDA;
-    *out = cache[dev];
-    return COLIBRI_OK;
-}
-
 // Token rows of x that k_route_logits stages per pass: up to 96 KB of x, at least one row.
 static int route_xt(int d, int T)
 {
@@ -334,10 +321,13 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     Q8Args qa{x, T, d, reinterpret_cast<int8_t *>(ws + L.qx), reinterpret_cast<float *>(ws + L.sx),
               reinterpret_cast<int8_t *>(ws + L.qx_eo), reinterpret_cast<int *>(ws + L.xc), err};
     const int down_blocks = (d + DN_ITEM_ROWS - 1) / DN_ITEM_ROWS;
-    BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks,
+    // bucketing counters (34*E ints), plus the ids when they fit in 160 KB together
+    const size_t bsm0 = (size_t)34 * E * sizeof(int), pbytes = (size_t)T * K * sizeof(int);
+    const int stage_ids = bsm0 + pbytes <= 160 * 1024;
+    const size_t bsm = bsm0 + (stage_ids ? pbytes : 0);
+    BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks, stage_ids,
                   reinterpret_cast<int32_t *>(ws + L.offsets), reinterpret_cast<int32_t *>(ws + L.pairs),
                   reinterpret_cast<Slot *>(ws + L.slots), reinterpret_cast<Counters *>(ws + L.counters), err};
-    const size_t bsm = (size_t)34 * E * sizeof(int);
     if (ids_given) {
         // a1: q8 of x (plain codes + even/odd codes + corrections); clears the error flag
         const long groups = (long)T * (d / G);
@@ -385,11 +375,8 @@ experts:
     if (cfg->has_shared)
         sh = *shared;
     const int routed_slots = T * K < E ? T * K : E;
-    int n_sm = 0;
-    if (sm_count(&n_sm))
-        return COLIBRI_E_CUDA;
     const int gu_items = (cfg->has_shared ? cfg->shared_ffn / G : 0) + routed_slots * (cfg->ffn / G);
-    StreamArgs st{};
+    DecodeArgs st{};
     st.experts = experts;
     st.shared = sh;
     st.d = d;
@@ -403,7 +390,7 @@ experts:
     st.counters = reinterpret_cast<const Counters *>(ws + L.counters);
     st.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
     st.err = err;
-    StreamArgs ga = st;
+    DecodeArgs ga = st;
     ga.aq_eo = reinterpret_cast<const int8_t *>(ws + L.qx_eo);
     ga.as = reinterpret_cast<const float *>(ws + L.sx);
     ga.ac = reinterpret_cast<const int *>(ws + L.xc);
@@ -413,17 +400,17 @@ experts:
     ga.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
     ga.hs = reinterpret_cast<float *>(ws + L.hs);
     ga.hc = reinterpret_cast<int *>(ws + L.hc);
-    if (launch_stream(MODE_GATEUP, ga, gu_items, n_sm, s) != cudaSuccess || prof_mark(5, s))
+    if (launch_decode(MODE_GATEUP, ga, gu_items, s) != cudaSuccess || prof_mark(5, s))
         return COLIBRI_E_CUDA;
     const int dn_items = (routed_slots + (cfg->has_shared ? 1 : 0)) * down_blocks;
-    StreamArgs da = st;
+    DecodeArgs da = st;
     da.aq_eo = reinterpret_cast<const int8_t *>(ws + L.hq_eo);
     da.as = reinterpret_cast<const float *>(ws + L.hs);
     da.ac = reinterpret_cast<const int *>(ws + L.hc);
     da.act_stride = (long)L.fmax;
     da.act_groups = (int)L.fmax / G;
     da.y = reinterpret_cast<float *>(ws + L.y);
-    if (launch_stream(MODE_DOWN, da, dn_items, n_sm, s) != cudaSuccess || prof_mark(6, s))
+    if (launch_decode(MODE_DOWN, da, dn_items, s) != cudaSuccess || prof_mark(6, s))
         return COLIBRI_E_CUDA;
 
     // a9: combine
@@ -463,13 +450,14 @@ int colibri_moe_profile_read(float *ms, int n)
 int colibri_debug_group_dots(const uint8_t *w, const int8_t *qa, int rows, int cols, int32_t *dots,
                              void *stream)
 {
-    if (!w || !qa || !dots || rows < 0 || cols <= 0 || cols % G)
+    if (!w || !qa || !dots || rows < 0 || rows % 32 || cols <= 0 || cols % G)
         return COLIBRI_E_INVAL;
     if (rows == 0)
         return COLIBRI_OK;
     if (!aligned(w, 16) || !aligned(qa, 16))
         return COLIBRI_E_INVAL;
-    k_debug_dots<<<(rows + 7) / 8, 256, 0, (cudaStream_t)stream>>>(w, qa, rows, cols, dots);
+    const long n = (long)rows * (cols / G);
+    k_debug_dots<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(w, qa, rows, cols, dots);
     return cuda_status(cudaGetLastError());
 }
 

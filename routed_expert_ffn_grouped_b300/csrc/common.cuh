@@ -43,23 +43,41 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
     return d;
 }
 
-// int32 dot of one 32-element group: 16 bytes of offset-binary nibbles (low nibble =
-// even element) against activation codes stored as 8 words in "even/odd" order (word
-// 2j = elements 8j, 8j+2, 8j+4, 8j+6; word 2j+1 = elements 8j+1, ..., 8j+7) and
-// corr = 8 * (sum of the 32 codes), which removes the +8 offset of the nibbles.
-__device__ __forceinline__ int dot_group(uint4 w, uint4 a0, uint4 a1, int corr)
+// The 16 bytes of one 32-element group of offset-binary nibbles (byte j: element 2j in
+// the low nibble, 2j+1 in the high nibble), split without shifting: l[i] keeps the low
+// nibbles (elements 8i, 8i+2, 8i+4, 8i+6) as bytes, h[i] the high nibbles as 16x their
+// value (elements 8i+1, ..., 8i+7).
+struct NibbleSplit {
+    uint32_t l[4], h[4];
+};
+
+__device__ __forceinline__ NibbleSplit split_nibbles(uint4 w)
 {
-    constexpr uint32_t M = 0x0F0F0F0Fu;
-    int acc = -corr;
-    acc = dp4a_us(w.x & M, a0.x, acc);
-    acc = dp4a_us((w.x >> 4) & M, a0.y, acc);
-    acc = dp4a_us(w.y & M, a0.z, acc);
-    acc = dp4a_us((w.y >> 4) & M, a0.w, acc);
-    acc = dp4a_us(w.z & M, a1.x, acc);
-    acc = dp4a_us((w.z >> 4) & M, a1.y, acc);
-    acc = dp4a_us(w.w & M, a1.z, acc);
-    acc = dp4a_us((w.w >> 4) & M, a1.w, acc);
-    return acc;
+    constexpr uint32_t LO = 0x0F0F0F0Fu, HI = 0xF0F0F0F0u;
+    NibbleSplit n;
+    n.l[0] = w.x & LO, n.h[0] = w.x & HI;
+    n.l[1] = w.y & LO, n.h[1] = w.y & HI;
+    n.l[2] = w.z & LO, n.h[2] = w.z & HI;
+    n.l[3] = w.w & LO, n.h[3] = w.w & HI;
+    return n;
+}
+
+// int32 dot of one group against activation codes stored as 8 words in even/odd order
+// (word 2i = elements 8i, 8i+2, 8i+4, 8i+6; word 2i+1 = elements 8i+1, ..., 8i+7), given
+// corr = 8 * (sum of the 32 codes), which removes the +8 offset of the nibbles. The sum
+// over the high nibbles carries a factor 16 and is a multiple of 16, so the arithmetic
+// shift by 4 is exact.
+__device__ __forceinline__ int dot_split(const NibbleSplit &n, uint4 a0, uint4 a1, int corr)
+{
+    int lo = dp4a_us(n.l[0], a0.x, 0);
+    int hi = dp4a_us(n.h[0], a0.y, 0);
+    lo = dp4a_us(n.l[1], a0.z, lo);
+    hi = dp4a_us(n.h[1], a0.w, hi);
+    lo = dp4a_us(n.l[2], a1.x, lo);
+    hi = dp4a_us(n.h[2], a1.y, hi);
+    lo = dp4a_us(n.l[3], a1.z, lo);
+    hi = dp4a_us(n.h[3], a1.w, hi);
+    return lo + (hi >> 4) - corr;
 }
 
 // Byte position of element k (0..31) of a group in the even/odd word order.
@@ -142,6 +160,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
             return true;
     }
     return false;
+}
+
+// Hint: bring [src, src + bytes) into L2 (no completion to wait for). src 16-byte
+// aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.

@@ -41,6 +41,7 @@ struct SelectArgs {
 struct BucketArgs {
     const int32_t *ids;
     int T, K, E, has_shared, shared_ffn, ffn, down_blocks;
+    int stage_ids;  // 1: dynamic shared memory also holds the T*K ids after the 34*E counters
     int32_t *offsets;
     int32_t *pairs;
     Slot *slots;
@@ -48,13 +49,11 @@ struct BucketArgs {
     int *err;
 };
 
-// Streaming decode GEMVs (kernels_stream.cu).
+// Decode GEMVs (kernels_decode.cu).
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
-constexpr int DN_ITEM_ROWS = 64;  // rows of d per down item
-constexpr int STREAM_TC = 4;      // tokens per register chunk
-constexpr int STREAM_TPAD = 32;   // gate/up tokens per pass over an item's weights
+constexpr int DN_ITEM_ROWS = 32;  // rows of d per down item
 
-struct StreamArgs {
+struct DecodeArgs {
     const colibri_expert *experts;
     colibri_expert shared;
     int d, ffn, shared_ffn, T, K, has_shared, fmax;
@@ -73,12 +72,12 @@ struct StreamArgs {
     int *hc;
     float *y;          // down output [pairs_total][d]
     int *err;
-    // set by launch_stream
-    int stage_bytes, ring, tpad;
+    // set by launch_decode: K of the widest matrix, groups per ring stage, stage bytes,
+    // ring stages, tokens per chunk
+    int kmax, sg, stage_bytes, ring, tch;
 };
 
-size_t stream_stage_bytes(int mode, int d, int fmax);
-cudaError_t launch_stream(int mode, StreamArgs a, int max_items, int n_sm, cudaStream_t s);
+cudaError_t launch_decode(int mode, DecodeArgs a, int max_items, cudaStream_t s);
 
 struct CombineArgs {
     const float *y;

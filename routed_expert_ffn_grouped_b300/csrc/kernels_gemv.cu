@@ -25,37 +25,37 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a)
     *reinterpret_cast<float4 *>(a.out + (long)t * a.d + m) = acc;
 }
 
-// Test export: one warp per row, lanes over groups, through dot_group. The plain codes
-// are rearranged into even/odd words with byte permutes.
+// Test export: one thread per (row, group) of a matrix in the stored layout (row blocks of
+// 32 rows, group-major), through the decode kernels' split-nibble dot. The plain codes are
+// rearranged into even/odd words with byte permutes.
 __global__ void __launch_bounds__(256) k_debug_dots(const uint8_t *w, const int8_t *qa, int rows, int cols,
                                                     int32_t *dots)
 {
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows)
-        return;
     const int ng = cols / G;
-    for (int g = lane; g < ng; g += 32) {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(qa + g * G);
-        uint32_t P[8];
-        int sum = 0;
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)rows * ng)
+        return;
+    const int row = (int)(i / ng), g = (int)(i % ng);
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(qa + g * G);
+    uint32_t P[8];
+    int sum = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            P[j] = p[j];
-        for (int k = 0; k < G; ++k)
-            sum += qa[g * G + k];
-        uint4 A0, A1;
-        A0.x = __byte_perm(P[0], P[1], 0x6420);
-        A0.y = __byte_perm(P[0], P[1], 0x7531);
-        A0.z = __byte_perm(P[2], P[3], 0x6420);
-        A0.w = __byte_perm(P[2], P[3], 0x7531);
-        A1.x = __byte_perm(P[4], P[5], 0x6420);
-        A1.y = __byte_perm(P[4], P[5], 0x7531);
-        A1.z = __byte_perm(P[6], P[7], 0x6420);
-        A1.w = __byte_perm(P[6], P[7], 0x7531);
-        const uint4 wv = *reinterpret_cast<const uint4 *>(w + (long)row * (cols / 2) + g * 16);
-        dots[(long)row * ng + g] = dot_group(wv, A0, A1, 8 * sum);
-    }
+    for (int j = 0; j < 8; ++j)
+        P[j] = p[j];
+    for (int k = 0; k < G; ++k)
+        sum += qa[g * G + k];
+    uint4 A0, A1;
+    A0.x = __byte_perm(P[0], P[1], 0x6420);
+    A0.y = __byte_perm(P[0], P[1], 0x7531);
+    A0.z = __byte_perm(P[2], P[3], 0x6420);
+    A0.w = __byte_perm(P[2], P[3], 0x7531);
+    A1.x = __byte_perm(P[4], P[5], 0x6420);
+    A1.y = __byte_perm(P[4], P[5], 0x7531);
+    A1.z = __byte_perm(P[6], P[7], 0x6420);
+    A1.w = __byte_perm(P[6], P[7], 0x7531);
+    const size_t off = (((size_t)(row / 32) * ng + g) * 32 + row % 32) * 16;
+    const uint4 wv = *reinterpret_cast<const uint4 *>(w + off);
+    dots[(long)row * ng + g] = dot_split(split_nibbles(wv), A0, A1, 8 * sum);
 }
 
 }  // namespace clb

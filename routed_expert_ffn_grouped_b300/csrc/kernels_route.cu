@@ -313,11 +313,19 @@ __device__ void bucket_body(const BucketArgs &a, int *sm)
     __shared__ int s_total;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long P = (long)a.T * a.K;
+    // the ids, staged in shared memory when they fit (the launch sized it so)
+    const int32_t *sid = a.ids;
+    if (a.stage_ids) {
+        int *st = sm + 34 * E;
+        for (long p = tid; p < P; p += 1024)
+            st[p] = a.ids[p];
+        sid = st;
+    }
     for (int e = tid; e < E; e += 1024)
         cnt[e] = 0;
     __syncthreads();
     for (long p = tid; p < P; p += 1024) {
-        const int e = a.ids[p];
+        const int e = sid[p];
         if (e < 0 || e >= E) {
             if (a.err)
                 atomicOr(a.err, ERR_BAD_ID);
@@ -326,7 +334,7 @@ __device__ void bucket_body(const BucketArgs &a, int *sm)
             // a token must not list an expert twice
             const long t0 = p - p % a.K;
             for (long q = t0; q < p; ++q)
-                if (a.ids[q] == e && a.err)
+                if (sid[q] == e && a.err)
                     atomicOr(a.err, ERR_BAD_ID);
         }
     }
@@ -371,7 +379,7 @@ __device__ void bucket_body(const BucketArgs &a, int *sm)
             wcnt[i] = 0;
         __syncthreads();
         const long p = base + tid;
-        int e = p < P ? a.ids[p] : -1;
+        int e = p < P ? sid[p] : -1;
         if (e < 0 || e >= E)
             e = -1;
         const unsigned m = __match_any_sync(FULL, e);

@@ -70,8 +70,9 @@ SPECS = {s.name: s for s in (TINY, OLMOE, GLM52)}
 class BlobLayout:
     """Byte offsets of one expert inside its blob: w1 | w3 | w2 | s1 | s3 | s2.
 
-    w1, w3: [f][d/2] packed nibbles (gate, up); w2: [d][f/2] (down);
-    s1, s3: [f][d/32] fp32; s2: [d][f/32] fp32. Each part starts on a 256-byte boundary.
+    Logical tensors: w1, w3 [f][d/2] packed nibbles (gate, up); w2 [d][f/2] (down);
+    s1, s3 [f][d/32] fp32; s2 [d][f/32] fp32. Each part starts on a 256-byte boundary and
+    is stored in row blocks (see ``pack_nibbles`` / ``pack_scales``).
     """
     d: int
     f: int
@@ -104,37 +105,94 @@ def blob_layout(d: int, f: int) -> BlobLayout:
     return BlobLayout(d, f, *offs, o)
 
 
-def expert_views(blob: np.ndarray, d: int, f: int) -> dict:
-    """Named numpy views into one expert blob (uint8, length blob_layout(d, f).nbytes)."""
+# Storage order of one packed int4 matrix W [R][K] (R, K multiples of 32): row blocks of
+# ROW_BLOCK rows; inside a block, group-major: the 16 bytes of group g (columns 32g..32g+31)
+# of the block's 32 rows lie together, row after row. Byte (r, g, j) is at
+#     ((r // 32) * (K // 32) + g) * 512 + (r % 32) * 16 + j,
+# and byte j of a group holds column 32g+2j in its low nibble, 32g+2j+1 in its high nibble.
+# Scales S [R][K/32] follow the same order: S[r][g] at ((r // 32) * (K // 32) + g) * 32 + r % 32.
+ROW_BLOCK = 32
+
+
+def pack_nibbles(w: np.ndarray) -> np.ndarray:
+    """Logical packed matrix [R][K/2] (uint8, row-major) -> stored bytes (flat)."""
+    R, H = w.shape
+    assert R % ROW_BLOCK == 0 and H % 16 == 0
+    return np.ascontiguousarray(w.reshape(R // ROW_BLOCK, ROW_BLOCK, H // 16, 16).transpose(0, 2, 1, 3)).reshape(-1)
+
+
+def unpack_nibbles(flat: np.ndarray, R: int, K: int) -> np.ndarray:
+    """Stored bytes (flat) -> logical packed matrix [R][K/2]."""
+    H = K // 2
+    b = flat[:R * H].reshape(R // ROW_BLOCK, H // 16, ROW_BLOCK, 16)
+    return np.ascontiguousarray(b.transpose(0, 2, 1, 3)).reshape(R, H)
+
+
+def pack_scales(s: np.ndarray) -> np.ndarray:
+    """Logical scales [R][K/32] (fp32) -> stored order (flat fp32)."""
+    R, NG = s.shape
+    assert R % ROW_BLOCK == 0
+    return np.ascontiguousarray(s.reshape(R // ROW_BLOCK, ROW_BLOCK, NG).transpose(0, 2, 1)).reshape(-1)
+
+
+def unpack_scales(flat: np.ndarray, R: int, K: int) -> np.ndarray:
+    """Stored scales (flat fp32) -> logical [R][K/32]."""
+    NG = K // GROUP
+    b = flat[:R * NG].reshape(R // ROW_BLOCK, NG, ROW_BLOCK)
+    return np.ascontiguousarray(b.transpose(0, 2, 1)).reshape(R, NG)
+
+
+def _parts(d: int, f: int):
+    """(name, offset, rows R, columns K) of the six parts of a blob."""
     L = blob_layout(d, f)
+    return L, (("w1", L.w1, f, d), ("w3", L.w3, f, d), ("w2", L.w2, d, f),
+               ("s1", L.s1, f, d), ("s3", L.s3, f, d), ("s2", L.s2, d, f))
+
+
+def expert_views(blob: np.ndarray, d: int, f: int) -> dict:
+    """The logical tensors of one expert blob (uint8, length blob_layout(d, f).nbytes):
+    w1, w3 [f][d/2], w2 [d][f/2] uint8 and s1, s3 [f][d/32], s2 [d][f/32] fp32 (copies)."""
+    L, parts = _parts(d, f)
     b = blob.reshape(-1)
     assert b.dtype == np.uint8 and b.size >= L.nbytes
+    out = {}
+    for name, off, R, K in parts:
+        if name[0] == "w":
+            out[name] = unpack_nibbles(b[off:off + R * K // 2], R, K)
+        else:
+            out[name] = unpack_scales(b[off:off + 4 * R * (K // GROUP)].view(np.float32), R, K)
+    return out
 
-    def u8(off, rows, cols):
-        return b[off:off + rows * cols].reshape(rows, cols)
 
-    def f32(off, rows, cols):
-        return b[off:off + 4 * rows * cols].view(np.float32).reshape(rows, cols)
-
-    return {"w1": u8(L.w1, f, d // 2), "w3": u8(L.w3, f, d // 2), "w2": u8(L.w2, d, f // 2),
-            "s1": f32(L.s1, f, d // GROUP), "s3": f32(L.s3, f, d // GROUP),
-            "s2": f32(L.s2, d, f // GROUP)}
+def write_expert(out: np.ndarray, d: int, f: int, tensors: dict) -> np.ndarray:
+    """Store logical tensors (the keys of ``expert_views``) into a blob."""
+    L, parts = _parts(d, f)
+    b = out.reshape(-1)
+    b[:L.nbytes] = 0
+    for name, off, R, K in parts:
+        if name[0] == "w":
+            b[off:off + R * K // 2] = pack_nibbles(np.asarray(tensors[name], np.uint8))
+        else:
+            b[off:off + 4 * R * (K // GROUP)] = pack_scales(np.asarray(tensors[name], np.float32)).view(np.uint8)
+    return out
 
 
 def fill_expert_blob(out: np.ndarray, d: int, f: int, seed: int, layer: int, expert: int,
                      shared: bool = False) -> np.ndarray:
-    """Draw one expert (uniform int4 codes, |N(0, 0.02)| scales) into ``out`` (uint8 blob)."""
-    L = blob_layout(d, f)
+    """Draw one expert (uniform int4 codes, |N(0, 0.02)| scales) into ``out`` (uint8 blob).
+    Codes and scales are i.i.d., so they are drawn straight into storage order."""
+    L, parts = _parts(d, f)
     rng = np.random.default_rng([seed, layer, expert, _TAG_SHARED if shared else _TAG_EXPERT])
     b = out.reshape(-1)
     b[:L.nbytes] = 0
-    n = f * d // 2
-    for off in (L.w1, L.w3, L.w2):
-        b[off:off + n] = np.frombuffer(rng.bytes(n), np.uint8)
-    v = expert_views(b, d, f)
-    for k in ("s1", "s3", "s2"):
-        s = v[k]
-        s[...] = np.abs(rng.standard_normal(s.shape, dtype=np.float32)) * np.float32(0.02)
+    for name, off, R, K in parts:
+        if name[0] == "w":
+            n = R * K // 2
+            b[off:off + n] = np.frombuffer(rng.bytes(n), np.uint8)
+        else:
+            n = R * (K // GROUP)
+            s = np.abs(rng.standard_normal(n, dtype=np.float32)) * np.float32(0.02)
+            b[off:off + 4 * n] = s.view(np.uint8)
     return out
 
 
@@ -182,12 +240,19 @@ class Layer:
     shared_blob: np.ndarray | None
 
     def expert(self, e: int) -> dict:
-        return expert_views(self.blobs[e], self.spec.d, self.spec.ffn)
+        """Logical tensors of routed expert e (unpacked once, then kept)."""
+        memo = self.__dict__.setdefault("_views", {})
+        if e not in memo:
+            memo[e] = expert_views(self.blobs[e], self.spec.d, self.spec.ffn)
+        return memo[e]
 
     def shared(self) -> dict | None:
         if self.shared_blob is None:
             return None
-        return expert_views(self.shared_blob, self.spec.d, self.spec.shared_ffn)
+        memo = self.__dict__.setdefault("_views", {})
+        if "shared" not in memo:
+            memo["shared"] = expert_views(self.shared_blob, self.spec.d, self.spec.shared_ffn)
+        return memo["shared"]
 
 
 def make_layer(spec: LayerSpec, seed: int, layer: int = 0, experts=None) -> Layer:

@@ -110,7 +110,7 @@ def test_router_ties_lowest_index(torch_cuda, C, orc):
 
 
 # ------------------------------------------------------------------ integer group dots
-@pytest.mark.parametrize("rows,cols", [(64, 6144), (37, 2048), (8, 32)])
+@pytest.mark.parametrize("rows,cols", [(64, 6144), (96, 2048), (32, 32)])
 def test_group_dots_bit_exact(torch_cuda, C, orc, rows, cols):
     torch = torch_cuda
     rng = np.random.default_rng(rows + cols)
@@ -118,11 +118,13 @@ def test_group_dots_bit_exact(torch_cuda, C, orc, rows, cols):
     qa = rng.integers(-127, 128, cols).astype(np.int8)
     qa[:32] = -127
     w[0, :16] = 0                                       # -8 x -127 in group 0: 32512
+    w[1, :16] = 0xFF                                    # 7 x -127 in group 0: -28448
     dots = torch.empty((rows, cols // 32), dtype=torch.int32, device="cuda")
-    C.colibri_debug_group_dots(to_dev(torch, w), to_dev(torch, qa), dots)
+    C.colibri_debug_group_dots(to_dev(torch, synth.pack_nibbles(w)), to_dev(torch, qa), dots,
+                               rows=rows, cols=cols)
     torch.cuda.synchronize()
     want = orc.group_dots(w, qa)
-    assert want[0, 0] == 32512
+    assert want[0, 0] == 32512 and want[1, 0] == -28448
     assert np.array_equal(dots.cpu().numpy(), want)
 
 
