@@ -316,60 +316,66 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     int *err = reinterpret_cast<int *>(ws + L.err);
     const int d = cfg->d, E = cfg->n_exp, K = cfg->top_k;
 
+    // the control words (error flag, routing counter) and the work counters start every
+    // call at zero: if routing fails, the expert kernels find no work
+    if (cudaMemsetAsync(ws + L.err, 0, L.counters + sizeof(Counters) - L.err, s) != cudaSuccess)
+        return COLIBRI_E_CUDA;
     if (prof_mark(0, s))
         return COLIBRI_E_CUDA;
     Q8Args qa{x, T, d, reinterpret_cast<int8_t *>(ws + L.qx), reinterpret_cast<float *>(ws + L.sx),
-              reinterpret_cast<int8_t *>(ws + L.qx_eo), reinterpret_cast<int *>(ws + L.xc), err};
+              reinterpret_cast<int8_t *>(ws + L.qx_eo), reinterpret_cast<int *>(ws + L.xc), nullptr};
     const int down_blocks = (d + DN_ITEM_ROWS - 1) / DN_ITEM_ROWS;
-    // bucketing counters (34*E ints), plus the ids when they fit in 160 KB together
-    const size_t bsm0 = (size_t)34 * E * sizeof(int), pbytes = (size_t)T * K * sizeof(int);
-    const int stage_ids = bsm0 + pbytes <= 160 * 1024;
-    const size_t bsm = bsm0 + (stage_ids ? pbytes : 0);
-    BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks, stage_ids,
+    BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks, 0,
                   reinterpret_cast<int32_t *>(ws + L.offsets), reinterpret_cast<int32_t *>(ws + L.pairs),
                   reinterpret_cast<Slot *>(ws + L.slots), reinterpret_cast<Counters *>(ws + L.counters), err};
-    if (ids_given) {
-        // a1: q8 of x (plain codes + even/odd codes + corrections); clears the error flag
-        const long groups = (long)T * (d / G);
-        k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
-        if (cudaGetLastError() != cudaSuccess || prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s))
+    float *lg = reinterpret_cast<float *>(ws + L.logits);
+    float *sv = reinterpret_cast<float *>(ws + L.s);
+    float *cv = reinterpret_cast<float *>(ws + L.c);
+    const SelectArgs sa = select_args(cfg, T, lg, sv, cv, bias, ids, w);
+    if (!ids_given && T <= 32 && T * E <= 8192) {
+        // a1-a4 for decode in one kernel: q8 of x, logits and scores in every CTA, then
+        // selection and bucketing in the last CTA to finish
+        static SmemLimits have;
+        const int xt = route_xt(d, T);
+        const size_t smem = route_decode_smem_bytes(T, K, E, d, xt);
+        if (!smem_attr((const void *)k_route_decode, smem, have))
             return COLIBRI_E_CUDA;
-    } else {
-        // a1-a2: router logits with sigmoid scores, q8 of x on the side; clears the error flag
-        float *lg = reinterpret_cast<float *>(ws + L.logits);
-        float *sv = reinterpret_cast<float *>(ws + L.s);
-        float *cv = reinterpret_cast<float *>(ws + L.c);
-        qa.err = nullptr;
+        RouterArgs ra{x, T, d, E, xt, Wr, cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : bias, lg,
+                      cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : sv,
+                      cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : cv, qa, err};
         if (prof_mark(1, s))
             return COLIBRI_E_CUDA;
-        int rc = launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, qa, err, s);
-        if (rc || prof_mark(2, s))
+        k_route_decode<<<E, 256, smem, s>>>(ra, sa, ba, err + 4);
+        if (cudaGetLastError() != cudaSuccess || prof_mark(2, s) || prof_mark(3, s) || prof_mark(4, s))
             return COLIBRI_E_CUDA;
-        const SelectArgs sa = select_args(cfg, T, lg, sv, cv, bias, ids, w);
-        if (T <= 32) {
-            // a3-a4 fused for decode: selection and bucketing in one CTA
-            static SmemLimits have;
-            const size_t sm = std::max(bsm, select_cta_smem_bytes(E));
-            if (!smem_attr((const void *)k_select_bucket, sm, have))
+    } else {
+        if (ids_given) {
+            // a1: q8 of x (plain codes + even/odd codes + corrections)
+            const long groups = (long)T * (d / G);
+            k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
+            if (cudaGetLastError() != cudaSuccess || prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s))
                 return COLIBRI_E_CUDA;
-            k_select_bucket<<<1, 1024, sm, s>>>(sa, ba);
-            if (cudaGetLastError() != cudaSuccess || prof_mark(3, s) || prof_mark(4, s))
+        } else {
+            // a1-a3: router logits with sigmoid scores and q8 of x on the side, selection
+            if (prof_mark(1, s))
                 return COLIBRI_E_CUDA;
-            goto experts;
+            int rc = launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, qa, err, s);
+            if (rc || prof_mark(2, s))
+                return COLIBRI_E_CUDA;
+            if (launch_select(sa, s) || prof_mark(3, s))
+                return COLIBRI_E_CUDA;
         }
-        if (launch_select(sa, s) || prof_mark(3, s))
-            return COLIBRI_E_CUDA;
-    }
-    {
-        // a4: bucketing and slot list
+        // a4: bucketing and slot list (counters, plus the ids when they fit in 160 KB)
         static SmemLimits have;
+        const size_t bsm0 = bucket_smem_bytes(E, 1024), pbytes = (size_t)T * K * sizeof(int);
+        ba.stage_ids = bsm0 + pbytes <= 160 * 1024;
+        const size_t bsm = bsm0 + (ba.stage_ids ? pbytes : 0);
         if (!smem_attr((const void *)k_bucket, bsm, have))
             return COLIBRI_E_CUDA;
         k_bucket<<<1, 1024, bsm, s>>>(ba);
         if (cudaGetLastError() != cudaSuccess || prof_mark(4, s))
             return COLIBRI_E_CUDA;
     }
-experts:
     // a6-a8: gate/up (+ SwiGLU + q8 h), then down, for every slot (shared expert first)
     colibri_expert sh{};
     if (cfg->has_shared)

@@ -41,7 +41,7 @@ struct SelectArgs {
 struct BucketArgs {
     const int32_t *ids;
     int T, K, E, has_shared, shared_ffn, ffn, down_blocks;
-    int stage_ids;  // 1: dynamic shared memory also holds the T*K ids after the 34*E counters
+    int stage_ids;  // 1: k_bucket's shared memory also holds the T*K ids after its counters
     int32_t *offsets;
     int32_t *pairs;
     Slot *slots;
@@ -89,8 +89,9 @@ struct CombineArgs {
 
 __global__ void k_q8(Q8Args a);
 __global__ void k_route_logits(RouterArgs a);
-__global__ void k_select_bucket(SelectArgs sa, BucketArgs ba);
-size_t select_cta_smem_bytes(int E);
+__global__ void k_route_decode(RouterArgs ra, SelectArgs sa, BucketArgs ba, int *done);
+size_t route_decode_smem_bytes(int T, int K, int E, int d, int xt);
+size_t bucket_smem_bytes(int E, int nthreads);
 __global__ void k_router_select(SelectArgs a);
 __global__ void k_bucket(BucketArgs a);
 __global__ void k_combine(CombineArgs a);

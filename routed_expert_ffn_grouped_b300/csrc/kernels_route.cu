@@ -35,16 +35,14 @@ __global__ void __launch_bounds__(256) k_q8(Q8Args a)
 }
 
 // ---- router logits (+ the fp64 sigmoid, + q8 of x as a side job) --------------------
-// One CTA per expert e, four warps. The CTA bulk-copies Wr[e] and a chunk of XT token
-// rows of x (contiguous in x) into shared memory, then warp w takes the chunk's tokens
-// w, w+4, ...: lane j runs the fmaf chain over k = j, j+32, ... ascending, and the warp
-// joins the 32 chains with a butterfly (offsets 16, 8, 4, 2, 1); lane 0 then holds the
-// value of the halving tree (fp32 addition is commutative). In sigmoid mode lane 0 also
-// evaluates s = fp32(1/(1+exp(-l))) in fp64 and c = s + bias[e], so that the fp64 work
-// is spread over all CTAs. Before that, the CTAs quantise x (one warp per 32-group) when
-// the layer asks for it.
-constexpr int RL_WARPS = 4;
-
+// One CTA per expert e. The CTA bulk-copies Wr[e] and a chunk of xt token rows of x
+// (contiguous in x) into shared memory, then warp w takes the chunk's tokens w, w+nw,
+// ...: lane j runs the fmaf chain over k = j, j+32, ... ascending, and the warp joins the
+// 32 chains with a butterfly (offsets 16, 8, 4, 2, 1); lane 0 then holds the value of the
+// halving tree (fp32 addition is commutative). In sigmoid mode lane 0 also evaluates
+// s = fp32(1/(1+exp(-l))) in fp64 and c = s + bias[e], so that the fp64 work is spread
+// over all CTAs. Before that, the CTAs quantise x (one warp per 32-group) when the layer
+// asks for it.
 __device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane)
 {
     const int ng = a.cols / G;
@@ -66,53 +64,48 @@ __device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane)
     }
 }
 
-__global__ void __launch_bounds__(32 * RL_WARPS) k_route_logits(RouterArgs a)
+// Returns false if a bulk copy did not land within the wait limit (flagged in a.err).
+__device__ bool route_logits_part(const RouterArgs &a, unsigned char *smem_raw, uint64_t *bar)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bar;
-    const int d = a.d, e = blockIdx.x;
+    const int d = a.d, e = blockIdx.x, nw = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *wrow = reinterpret_cast<float *>(smem_raw);
     float *xs = wrow + d;
-    if (a.err && blockIdx.x == 0 && threadIdx.x == 0)
-        *a.err = 0;  // the first kernel of a layer call clears the flag
     if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
+        mbar_init(bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
     // q8 side job: warp-granular, grid-strided over the T*d/32 groups of x
     if (a.q8.x) {
         const long n = (long)a.T * (d / G);
-        for (long gw = (long)blockIdx.x * RL_WARPS + warp; gw < n; gw += (long)gridDim.x * RL_WARPS)
+        for (long gw = (long)blockIdx.x * nw + warp; gw < n; gw += (long)gridDim.x * nw)
             q8_group(a.q8, gw, lane);
     }
     const uint32_t row_bytes = (uint32_t)d * 4u;
     uint32_t phase = 0;
-    bool ok = true;
     for (int t0 = 0; t0 < a.T; t0 += a.xt) {
         const int nt = min(a.xt, a.T - t0);
         if (threadIdx.x == 0) {
             const uint32_t xbytes = row_bytes * (uint32_t)nt;
-            mbar_arrive_expect_tx(&bar, (t0 == 0 ? row_bytes : 0u) + xbytes);
+            mbar_arrive_expect_tx(bar, (t0 == 0 ? row_bytes : 0u) + xbytes);
             if (t0 == 0) {
                 const char *src = reinterpret_cast<const char *>(a.Wr + (long)e * d);
                 for (uint32_t off = 0; off < row_bytes; off += 32768u)
-                    bulk_g2s(reinterpret_cast<char *>(wrow) + off, src + off, min(32768u, row_bytes - off), &bar);
+                    bulk_g2s(reinterpret_cast<char *>(wrow) + off, src + off, min(32768u, row_bytes - off), bar);
             }
             const char *xsrc = reinterpret_cast<const char *>(a.x + (long)t0 * d);
             for (uint32_t off = 0; off < xbytes; off += 32768u)
-                bulk_g2s(reinterpret_cast<char *>(xs) + off, xsrc + off, min(32768u, xbytes - off), &bar);
+                bulk_g2s(reinterpret_cast<char *>(xs) + off, xsrc + off, min(32768u, xbytes - off), bar);
         }
-        if (!mbar_wait(&bar, phase)) {
-            ok = false;
+        if (!mbar_wait(bar, phase)) {
             if (lane == 0 && a.err)
                 atomicOr(a.err, ERR_WAIT_TIMEOUT);
-            mbar_wait(&bar, phase);  // bounded second wait for the copies still in flight
-            break;
+            mbar_wait(bar, phase);  // bounded second wait for the copies still in flight
+            return false;
         }
         phase ^= 1u;
-        for (int i = warp; i < nt; i += RL_WARPS) {
+        for (int i = warp; i < nt; i += nw) {
             const float *xr = xs + (long)i * d;
             float acc = 0.0f;
 #pragma unroll 8
@@ -133,7 +126,14 @@ __global__ void __launch_bounds__(32 * RL_WARPS) k_route_logits(RouterArgs a)
         }
         __syncthreads();  // the chunk buffer is refilled next
     }
-    (void)ok;
+    return true;
+}
+
+__global__ void __launch_bounds__(128) k_route_logits(RouterArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bar;
+    route_logits_part(a, smem_raw, &bar);
 }
 
 // (value, index) order of the selection: larger value first, then lower index.
@@ -303,28 +303,77 @@ __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
 // running base + the count of the same expert in earlier warps of the chunk + its rank
 // among equal lanes of its warp (__match_any_sync). Finally the slot list (shared
 // expert first, then routed experts in ascending id) and the item counts.
-__device__ void bucket_body(const BucketArgs &a, int *sm)
+// ---- block-wide helpers (any blockDim.x that is a multiple of 32, up to 1024) -------
+
+// In-place exclusive scan of the shared array v[0..n) by the whole block; returns the
+// total to every thread. Each thread scans a contiguous run of ceil(n / blockDim.x).
+__device__ int block_excl_scan(int *v, int n)
 {
-    const int E = a.E;
-    int *cnt = sm;              // [E]
-    int *run = sm + E;          // [E]
-    int *wcnt = sm + 2 * E;     // [32][E]
-    __shared__ int s_warp[32];
-    __shared__ int s_total;
+    __shared__ int s_w[32];
+    __shared__ int s_tot;
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (n + nt - 1) / nt;
+    const int b0 = min(n, tid * per), b1 = min(n, b0 + per);
+    int sum = 0;
+    for (int i = b0; i < b1; ++i)
+        sum += v[i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o)
+            incl += u;
+    }
+    if (lane == 31)
+        s_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nwarps = nt >> 5;
+        const int x = lane < nwarps ? s_w[lane] : 0;
+        int inc = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(FULL, inc, o);
+            if (lane >= o)
+                inc += u;
+        }
+        if (lane < nwarps)
+            s_w[lane] = inc - x;
+        if (lane == 31)
+            s_tot = inc;
+    }
+    __syncthreads();
+    int run = incl - sum + s_w[warp];
+    for (int i = b0; i < b1; ++i) {
+        const int x = v[i];
+        v[i] = run;
+        run += x;
+    }
+    const int tot = s_tot;
+    __syncthreads();
+    return tot;
+}
+
+// ---- bucketing --------------------------------------------------------------------
+// Counts per expert (shared-memory atomics), exclusive scan into offsets, then a stable
+// scatter in chunks of blockDim.x pairs: a pair's position is its expert's running base
+// + the count of the same expert in earlier warps of the chunk + its rank among equal
+// lanes of its warp (__match_any_sync). Finally the slot list (shared expert first, then
+// the routed experts in ascending id) and the work-item counts. sid: the T*K ids (shared
+// or global memory); sm: 3*E + nwarps*E ints of shared memory.
+__device__ void bucket_block(const BucketArgs &a, const int32_t *sid, int *sm)
+{
+    const int E = a.E, nt = blockDim.x, nwarps = nt >> 5;
+    int *cnt = sm;               // [E] counts, then offsets
+    int *run = sm + E;           // [E]
+    int *flag = sm + 2 * E;      // [E] nonzero-count flags, then their exclusive scan
+    int *wcnt = sm + 3 * E;      // [nwarps][E]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long P = (long)a.T * a.K;
-    // the ids, staged in shared memory when they fit (the launch sized it so)
-    const int32_t *sid = a.ids;
-    if (a.stage_ids) {
-        int *st = sm + 34 * E;
-        for (long p = tid; p < P; p += 1024)
-            st[p] = a.ids[p];
-        sid = st;
-    }
-    for (int e = tid; e < E; e += 1024)
+    for (int e = tid; e < E; e += nt)
         cnt[e] = 0;
     __syncthreads();
-    for (long p = tid; p < P; p += 1024) {
+    for (long p = tid; p < P; p += nt) {
         const int e = sid[p];
         if (e < 0 || e >= E) {
             if (a.err)
@@ -332,50 +381,28 @@ __device__ void bucket_body(const BucketArgs &a, int *sm)
         } else {
             atomicAdd(&cnt[e], 1);
             // a token must not list an expert twice
-            const long t0 = p - p % a.K;
-            for (long q = t0; q < p; ++q)
+            for (long q = p - p % a.K; q < p; ++q)
                 if (sid[q] == e && a.err)
                     atomicOr(a.err, ERR_BAD_ID);
         }
     }
     __syncthreads();
-    // exclusive scan of cnt over E <= 1024 (one element per thread)
-    const int c = tid < E ? cnt[tid] : 0;
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(FULL, incl, o);
-        if (lane >= o)
-            incl += v;
-    }
-    if (lane == 31)
-        s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int v = s_warp[lane];
-        int inc = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(FULL, inc, o);
-            if (lane >= o)
-                inc += u;
-        }
-        s_warp[lane] = inc - v;
-        if (lane == 31)
-            s_total = inc;
+    for (int e = tid; e < E; e += nt) {
+        flag[e] = cnt[e] > 0;
+        run[e] = cnt[e];
     }
     __syncthreads();
-    const int excl = incl - c + s_warp[warp];
-    if (tid < E) {
-        a.offsets[tid] = excl;
-        run[tid] = excl;
+    const int total = block_excl_scan(run, E);  // run = offsets
+    for (int e = tid; e < E; e += nt) {
+        a.offsets[e] = run[e];
+        cnt[e] = run[e];  // keep the offsets for the slot list
     }
     if (tid == 0)
-        a.offsets[E] = s_total;
+        a.offsets[E] = total;
     __syncthreads();
     // stable scatter
-    for (long base = 0; base < P; base += 1024) {
-        for (int i = tid; i < 32 * E; i += 1024)
+    for (long base = 0; base < P; base += nt) {
+        for (int i = tid; i < nwarps * E; i += nt)
             wcnt[i] = 0;
         __syncthreads();
         const long p = base + tid;
@@ -388,60 +415,40 @@ __device__ void bucket_body(const BucketArgs &a, int *sm)
         if (e >= 0 && lane == leader)
             wcnt[warp * E + e] = __popc(m);
         __syncthreads();
-        int tot = 0;
-        if (tid < E) {
-            for (int ww = 0; ww < 32; ++ww) {
-                const int v = wcnt[ww * E + tid];
-                wcnt[ww * E + tid] = tot;
+        for (int x = tid; x < E; x += nt) {
+            int tot = 0;
+            for (int ww = 0; ww < nwarps; ++ww) {
+                const int v = wcnt[ww * E + x];
+                wcnt[ww * E + x] = tot;
                 tot += v;
             }
+            flag[x] |= tot << 1;  // chunk total, consumed below
         }
         __syncthreads();
         if (e >= 0)
             a.pairs[run[e] + wcnt[warp * E + e] + rank] = (int)p;
         __syncthreads();
-        if (tid < E)
-            run[tid] += tot;
+        for (int x = tid; x < E; x += nt) {
+            run[x] += flag[x] >> 1;
+            flag[x] &= 1;
+        }
         __syncthreads();
     }
-    // slots: flags scan over experts with a non-zero count
-    const int flag = (tid < E && c > 0) ? 1 : 0;
-    int fin = flag;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(FULL, fin, o);
-        if (lane >= o)
-            fin += v;
-    }
-    __syncthreads();
-    if (lane == 31)
-        s_warp[warp] = fin;
-    __syncthreads();
-    if (warp == 0) {
-        int v = s_warp[lane];
-        int inc = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(FULL, inc, o);
-            if (lane >= o)
-                inc += u;
-        }
-        s_warp[lane] = inc - v;
-        if (lane == 31)
-            s_total = inc;
-    }
-    __syncthreads();
+    // slots: routed experts with a non-zero count, in ascending id after the shared one
+    const int n_routed = block_excl_scan(flag, E);
     const int sbase = a.has_shared ? 1 : 0;
-    if (flag) {
-        Slot s;
-        s.expert = tid;
-        s.begin = excl;
-        s.count = c;
-        s.pad = 0;
-        a.slots[sbase + fin - flag + s_warp[warp]] = s;
+    for (int e = tid; e < E; e += nt) {
+        const int c = (e + 1 < E ? cnt[e + 1] : total) - cnt[e];
+        if (c > 0) {
+            Slot s;
+            s.expert = e;
+            s.begin = cnt[e];
+            s.count = c;
+            s.pad = 0;
+            a.slots[sbase + flag[e]] = s;
+        }
     }
     if (tid == 0) {
-        const int n_routed = s_total;
         if (a.has_shared) {
             Slot s;
             s.expert = -1;
@@ -459,149 +466,291 @@ __device__ void bucket_body(const BucketArgs &a, int *sm)
     }
 }
 
+// Bucketing for few pairs (decode), with short loops only: every expert's thread counts
+// and lists its pairs by scanning all T*K ids in order, so the list is stable by
+// construction. O(E * T * K) work, trivial at decode sizes; sm: 2*E ints.
+__device__ void bucket_small(const BucketArgs &a, const int32_t *sid, int *sm)
+{
+    const int E = a.E, nt = blockDim.x, tid = threadIdx.x;
+    const int P = a.T * a.K;
+    int *off = sm, *flag = sm + E;
+    for (int p = tid; p < P; p += nt) {
+        const int e = sid[p];
+        bool bad = e < 0 || e >= E;
+        for (int q = p - p % a.K; q < p; ++q)
+            bad |= sid[q] == e;  // a token must not list an expert twice
+        if (bad && a.err)
+            atomicOr(a.err, ERR_BAD_ID);
+    }
+    for (int e = tid; e < E; e += nt) {
+        int c = 0;
+        for (int p = 0; p < P; ++p)
+            c += sid[p] == e;
+        off[e] = c;
+        flag[e] = c > 0;
+    }
+    __syncthreads();
+    const int total = block_excl_scan(off, E);
+    for (int e = tid; e < E; e += nt) {
+        a.offsets[e] = off[e];
+        int k = off[e];
+        for (int p = 0; p < P; ++p)
+            if (sid[p] == e)
+                a.pairs[k++] = p;
+    }
+    if (tid == 0)
+        a.offsets[E] = total;
+    const int n_routed = block_excl_scan(flag, E);
+    const int sbase = a.has_shared ? 1 : 0;
+    for (int e = tid; e < E; e += nt) {
+        const int c = (e + 1 < E ? off[e + 1] : total) - off[e];
+        if (c > 0) {
+            Slot sl;
+            sl.expert = e;
+            sl.begin = off[e];
+            sl.count = c;
+            sl.pad = 0;
+            a.slots[sbase + flag[e]] = sl;
+        }
+    }
+    if (tid == 0) {
+        if (a.has_shared) {
+            Slot sl;
+            sl.expert = -1;
+            sl.begin = 0;
+            sl.count = a.T;
+            sl.pad = 0;
+            a.slots[0] = sl;
+        }
+        Counters ct;
+        ct.n_slots = sbase + n_routed;
+        ct.n_routed = n_routed;
+        ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
+        ct.n_items_down = ct.n_slots * a.down_blocks;
+        *a.counters = ct;
+    }
+}
+
+size_t bucket_smem_bytes(int E, int nthreads)
+{
+    return (size_t)(3 + nthreads / 32) * E * sizeof(int);
+}
+
+// Prefill bucketing: one CTA of 1024 threads; the ids are staged in shared memory after
+// the counters when they fit (stage_ids).
 __global__ void __launch_bounds__(1024) k_bucket(BucketArgs a)
 {
     extern __shared__ int sm[];
-    bucket_body(a, sm);
+    const int32_t *sid = a.ids;
+    if (a.stage_ids) {
+        int *st = sm + (3 + 32) * a.E;
+        const long P = (long)a.T * a.K;
+        for (long p = threadIdx.x; p < P; p += blockDim.x)
+            st[p] = a.ids[p];
+        sid = st;
+        __syncthreads();
+    }
+    bucket_block(a, sid, sm);
 }
 
 // ---- decode selection with the whole CTA -----------------------------------------
 // The k-th pick of the sequential selection (repeatedly take the best remaining
 // candidate in the (value desc, index asc) order) is the candidate that exactly k others
-// beat. So each candidate's thread counts the allowed candidates that beat it and, if
-// that rank is below top_k, writes itself to position rank. Groups are kept the same way
-// (rank of the group score below topk_group). The CTA (1024 threads) takes TPR tokens per
-// round, Epad = E rounded up to 32 threads per token.
-//   smem (floats): per token slot c[Epad] | gscore[32] | kept[32] (int) | pick_id[32] (int)
-//   | pick_s[32].
-constexpr int SEL_SLOT_EXTRA = 128;
-
-__device__ void select_cta(const SelectArgs &a, float *smf)
+// beat. So each candidate counts the allowed candidates that beat it and, if that rank is
+// below top_k, writes itself to position rank. Groups are kept the same way (rank of the
+// group score below topk_group). Work is strided over (token, candidate) pairs, so any
+// block size serves. sm (floats): c [T][E] | group scores [T][32] | kept [T][32] (int) |
+// pick ids [T][32] (int) | pick s [T][32]. sids gets the T*K picked ids.
+__device__ __forceinline__ void top2_merge(float &m1, float &m2, float o1, float o2)
 {
-    const int E = a.E, K = a.K, Epad = (E + 31) & ~31;
-    const int TPR = max(1, 1024 / Epad), tid = threadIdx.x;
-    const int slot = tid / Epad, e = tid % Epad, lane = tid & 31;
-    const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
-    const int gs = sig ? E / a.n_group : E;
-    float *base = smf + (long)slot * (Epad + SEL_SLOT_EXTRA);
-    float *cs = base;
-    float *gsc = base + Epad;
-    int *kept = reinterpret_cast<int *>(base + Epad + 32);
-    int *pick = reinterpret_cast<int *>(base + Epad + 64);
-    float *pick_s = base + Epad + 96;
-    for (int t0 = 0; t0 < a.T; t0 += TPR) {
-        const int t = t0 + slot;
-        const bool act = slot < TPR && t < a.T && e < E;
-        const long row = (long)t * E;
-        float sv = 0.0f, cv = 0.0f;
-        if (act) {
-            if (!sig) {
-                sv = cv = a.logits[row + e];
-            } else if (a.s) {
-                sv = a.s[row + e];
-                cv = a.c[row + e];
-            } else {
-                sv = (float)(1.0 / (1.0 + exp(-(double)a.logits[row + e])));
-                cv = sv + (a.bias ? a.bias[e] : 0.0f);
-            }
-            cs[e] = cv;
-        }
-        __syncthreads();
-        if (sig) {
-            if (act && e < a.n_group) {
-                // the two largest c of group e (a multiset: equal values count twice)
-                float m1 = -INFINITY, m2 = -INFINITY;
-                for (int i = 0; i < gs; ++i) {
-                    const float v = cs[e * gs + i];
-                    if (v > m1) {
-                        m2 = m1;
-                        m1 = v;
-                    } else if (v > m2) {
-                        m2 = v;
-                    }
-                }
-                gsc[e] = gs == 1 ? m1 : m1 + m2;
-            }
-            __syncthreads();
-            if (act && e < a.n_group) {
-                const float v = gsc[e];
-                int rank = 0;
-                for (int g = 0; g < a.n_group; ++g)
-                    rank += better(gsc[g], g, v, e) && g != e;
-                kept[e] = rank < a.topk_group;
-            }
-            __syncthreads();
-        }
-        if (act && (!sig || kept[e / gs])) {
-            int rank = 0;
-            if (sig) {
-                for (int g = 0; g < a.n_group; ++g) {
-                    if (!kept[g])
-                        continue;
-                    for (int i = g * gs; i < (g + 1) * gs; ++i)
-                        rank += better(cs[i], i, cv, e) && i != e;
-                }
-            } else {
-                for (int i = 0; i < E; ++i)
-                    rank += better(cs[i], i, cv, e) && i != e;
-            }
-            if (rank < K) {
-                pick[rank] = e;
-                pick_s[rank] = sv;
-            }
-        }
-        __syncthreads();
-        // weights: the token slot's first warp (sums in selection order on lane 0)
-        if (slot < TPR && t < a.T && e < 32) {
-            double m = 0.0, z = 1.0;
-            if (!sig) {
-                const float *l = a.logits + row;
-                m = -INFINITY;
-                for (int i = lane; i < E; i += 32)
-                    m = fmax(m, (double)l[i]);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    m = fmax(m, __shfl_xor_sync(FULL, m, o));
-                z = 0.0;
-                for (int i = lane; i < E; i += 32)
-                    z += exp((double)l[i] - m);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    z += __shfl_xor_sync(FULL, z, o);
-            }
-            double p = 0.0;
-            if (lane < K)
-                p = sig ? (double)pick_s[lane] : exp((double)pick_s[lane] - m) / z;
-            double sum = 0.0;
-            for (int i = 0; i < K; ++i)
-                sum += __shfl_sync(FULL, p, i);
-            if (lane < K) {
-                if (a.norm_topk)
-                    p = p / sum;
-                a.ids[(long)t * K + lane] = pick[lane];
-                a.w[(long)t * K + lane] = (float)(p * (double)a.routed_scale);
-            }
-        }
-        __syncthreads();
+    // the two largest of the multiset {m1, m2, o1, o2}, given m1 >= m2 and o1 >= o2
+    if (o1 > m1) {
+        m2 = fmaxf(m1, o2);
+        m1 = o1;
+    } else {
+        m2 = fmaxf(m2, o1);
     }
 }
 
-size_t select_cta_smem_bytes(int E)
+// rank of (v, e) among row[b0..b1) in the (value desc, index asc) order; b0, b1 and the
+// row start are multiples of 4 (float4 reads, four at a time)
+__device__ __forceinline__ int rank_in(const float *row, int b0, int b1, float v, int e)
 {
-    const int Epad = (E + 31) & ~31;
-    const int TPR = 1024 / Epad > 0 ? 1024 / Epad : 1;
-    return (size_t)TPR * (Epad + SEL_SLOT_EXTRA) * sizeof(float);
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+    const float4 *q = reinterpret_cast<const float4 *>(row);
+    for (int j = b0; j < b1; j += 4) {
+        const float4 x = q[j >> 2];
+        r0 += better(x.x, j, v, e);
+        r1 += better(x.y, j + 1, v, e);
+        r2 += better(x.z, j + 2, v, e);
+        r3 += better(x.w, j + 3, v, e);
+    }
+    return r0 + r1 + r2 + r3;
 }
 
-// Decode (T <= 32): selection of every token with the whole CTA, then bucketing. The
-// selection's shared arrays and the bucketing's counters use the same dynamic shared
-// memory, one after the other.
-__global__ void __launch_bounds__(1024) k_select_bucket(SelectArgs sa, BucketArgs ba)
+__device__ void select_block(const SelectArgs &a, float *sm, int32_t *sids)
 {
-    extern __shared__ int sm[];
-    select_cta(sa, reinterpret_cast<float *>(sm));
-    __syncthreads();  // ids in global memory are visible to the whole block
-    bucket_body(ba, sm);
+    const int E = a.E, K = a.K, T = a.T, nt = blockDim.x, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+    const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
+    const int NG = sig ? a.n_group : 1, gs = E / NG;
+    const int Ep = (E + 3) & ~3;  // row stride (float4 aligned)
+    float *cs = sm;
+    float *gsc = cs + (size_t)T * Ep;
+    int *kept = reinterpret_cast<int *>(gsc + (size_t)T * 32);
+    int *pick = kept + (size_t)T * 32;
+    float *ps = reinterpret_cast<float *>(pick + (size_t)T * 32);
+    // written by other CTAs of this kernel: read at L2 (ld.global.cg), past this SM's L1
+    for (int i = tid; i < T * E; i += nt) {
+        const int t = i / E, e = i - t * E;
+        cs[t * Ep + e] = sig ? __ldcg(a.c + i) : __ldcg(a.logits + i);
+    }
+    __syncthreads();
+    if (sig) {
+        // group score = sum of the group's two largest c: one warp per (token, group)
+        for (int i = warp; i < T * NG; i += nwarps) {
+            const int t = i / NG, g = i - t * NG;
+            const float *row = cs + (size_t)t * Ep + g * gs;
+            float m1 = -INFINITY, m2 = -INFINITY;
+            for (int j = lane; j < gs; j += 32)
+                top2_merge(m1, m2, row[j], -INFINITY);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float o1 = __shfl_xor_sync(FULL, m1, o), o2 = __shfl_xor_sync(FULL, m2, o);
+                top2_merge(m1, m2, o1, o2);
+            }
+            if (lane == 0)
+                gsc[t * 32 + g] = gs == 1 ? m1 : m1 + m2;
+        }
+        __syncthreads();
+        for (int i = tid; i < T * NG; i += nt) {
+            const int t = i / NG, g = i - t * NG;
+            const float v = gsc[t * 32 + g];
+            int rank = 0;
+            for (int h = 0; h < NG; ++h)
+                rank += better(gsc[t * 32 + h], h, v, g);
+            kept[t * 32 + g] = rank < a.topk_group;
+        }
+        __syncthreads();
+    }
+    const bool vec = (gs & 3) == 0;
+    for (int i = tid; i < T * E; i += nt) {
+        const int t = i / E, e = i - t * E;
+        if (sig && !kept[t * 32 + e / gs])
+            continue;
+        const float *row = cs + (size_t)t * Ep;
+        const float v = row[e];
+        int rank = 0;
+        for (int g = 0; g < NG; ++g) {
+            if (sig && !kept[t * 32 + g])
+                continue;
+            if (vec) {
+                rank += rank_in(row, g * gs, (g + 1) * gs, v, e);
+            } else {
+                for (int j = g * gs; j < (g + 1) * gs; ++j)
+                    rank += better(row[j], j, v, e);
+            }
+        }
+        if (rank < K) {
+            pick[t * 32 + rank] = e;
+            ps[t * 32 + rank] = sig ? __ldcg(a.s + i) : v;
+        }
+    }
+    __syncthreads();
+    // weights: one warp per token, sums in selection order
+    for (int t = warp; t < T; t += nwarps) {
+        double m = 0.0, z = 1.0;
+        if (!sig) {
+            const float *l = cs + (size_t)t * Ep;
+            m = -INFINITY;
+            for (int i = lane; i < E; i += 32)
+                m = fmax(m, (double)l[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                m = fmax(m, __shfl_xor_sync(FULL, m, o));
+            z = 0.0;
+            for (int i = lane; i < E; i += 32)
+                z += exp((double)l[i] - m);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                z += __shfl_xor_sync(FULL, z, o);
+        }
+        float wt = 0.0f;
+        if (sig) {
+            // sigmoid weights in fp32: a compensated (TwoSum) sum of the k scores in
+            // selection order, then one division and the scale; within a few 1e-7 of the
+            // value computed in fp64 (fp64 is a slow, long-latency pipe here)
+            const float sv = lane < K ? ps[t * 32 + lane] : 0.0f;
+            float hi = 0.0f, lo = 0.0f;
+            for (int i = 0; i < K; ++i) {
+                const float x = __shfl_sync(FULL, sv, i);
+                const float u = hi + x, bb = u - hi;
+                lo += (hi - (u - bb)) + (x - bb);
+                hi = u;
+            }
+            const float sum = hi + lo;
+            wt = (a.norm_topk ? __fdiv_rn(sv, sum) : sv) * a.routed_scale;
+        } else {
+            double p = 0.0;
+            if (lane < K)
+                p = exp((double)ps[t * 32 + lane] - m) / z;
+            double sum = 0.0;
+            for (int i = 0; i < K; ++i)
+                sum += __shfl_sync(FULL, p, i);
+            if (a.norm_topk)
+                p = p / sum;
+            wt = (float)(p * (double)a.routed_scale);
+        }
+        if (lane < K) {
+            const int id = pick[t * 32 + lane];
+            a.ids[(long)t * K + lane] = id;
+            a.w[(long)t * K + lane] = wt;
+            sids[t * K + lane] = id;
+        }
+    }
+    __syncthreads();
+}
+
+__host__ __device__ size_t select_block_smem_bytes(int T, int E)
+{
+    return (size_t)T * ((E + 3) & ~3) * 4 + (size_t)T * 32 * 16;
+}
+
+// ---- decode routing in one kernel ---------------------------------------------------
+// Every CTA computes the logits (and sigmoid scores) of one expert for all T tokens and
+// quantises its share of x; the last CTA to finish (counted on a zeroed device counter)
+// selects the experts of every token and buckets the pairs, reading what the other CTAs
+// wrote from L2.
+__global__ void __launch_bounds__(256) k_route_decode(RouterArgs ra, SelectArgs sa, BucketArgs ba, int *done)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_last;
+    const bool ok = route_logits_part(ra, smem_raw, &bar);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();  // this CTA's logits, scores and codes are visible device-wide
+        s_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last || !ok)
+        return;
+    __threadfence();  // and the other CTAs' are visible to this one
+    // selection scratch, then the ids, then the bucketing counters (one after the other)
+    float *sel = reinterpret_cast<float *>(smem_raw);
+    int32_t *sids = reinterpret_cast<int32_t *>(sel + select_block_smem_bytes(sa.T, sa.E) / 4);
+    select_block(sa, sel, sids);
+    int *bsm = sids + ((sa.T * sa.K + 3) & ~3);
+    bucket_small(ba, sids, bsm);
+    if (threadIdx.x == 0)
+        *done = 0;  // ready for the next call
+}
+
+size_t route_decode_smem_bytes(int T, int K, int E, int d, int xt)
+{
+    const size_t logits = (size_t)d * 4 * (1 + xt);
+    const size_t last = select_block_smem_bytes(T, E) + 4 * (size_t)((T * K + 3) & ~3) + 8 * (size_t)E;
+    return logits > last ? logits : last;
 }
 
 }  // namespace clb
