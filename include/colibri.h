@@ -226,6 +226,13 @@ int colibri_moe_profile_read(float *ms, int n);
 int colibri_debug_group_dots(const uint8_t *w, const int8_t *qa, int rows, int cols,
                              int32_t *dots, void *stream);
 
+/* Test export: D = A B^T for one tile of integer codes on the tcgen05 tensor core, as the
+ * prefill grouped GEMM computes its per-group dots (codes as bf16, fp32 accumulation in
+ * tensor memory, exact for these ranges).
+ *   a device int8 [128][k] (values in [-128, 127]), b device int8 [n][k], row-major;
+ *   d device int32 [128][n] (out). n % 16 == 0, n <= 256; k % 16 == 0, k <= 256. */
+int colibri_debug_umma_i8(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, void *stream);
+
 /* ---- HBM expert cache -------------------------------------------------------------
  * Experts stream from a larger, slower tier into a small LRU cache of HBM slots
  * (dashen-tech guide, bullet "Streaming d'experts" and section "Router-Lookahead

@@ -63,6 +63,14 @@ bool cfg_valid(const colibri_layer_cfg *c)
     return true;
 }
 
+// Batches above DECODE_T_MAX tokens take the tensor-core grouped GEMMs, whose row tiles
+// are 128 rows; other shapes stay on the decode kernels (which chunk any token count).
+bool uses_gemm(const colibri_layer_cfg *c, int T)
+{
+    return T > DECODE_T_MAX && c->d % 128 == 0 && c->ffn % 128 == 0 &&
+           (!c->has_shared || c->shared_ffn % 128 == 0);
+}
+
 static size_t up256(size_t n)
 {
     return (n + 255) & ~size_t(255);
@@ -98,6 +106,9 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     L.hs = take(4 * PT * (fmax / G));
     L.hc = take(4 * PT * (fmax / G));
     L.y = take(4 * PT * d);
+    const bool prefill = uses_gemm(c, T);
+    L.xbf = take(prefill ? 2 * (size_t)T * d : 0);
+    L.hbf = take(prefill ? 2 * PT * fmax : 0);
     L.fmax = fmax;
     L.total = o;
     return L;
@@ -153,7 +164,7 @@ int colibri_q8_quantize(const float *x, int rows, int cols, int8_t *q, float *sc
         return COLIBRI_OK;
     if (!x || !q || !scale)
         return COLIBRI_E_INVAL;
-    Q8Args a{x, rows, cols, q, scale, nullptr, nullptr, nullptr};
+    Q8Args a{x, rows, cols, q, scale, nullptr, nullptr, nullptr};  // codes and scales only
     const long groups = (long)rows * (cols / G);
     const long blocks = (groups + 7) / 8;
     if (blocks > 0x7fffffffL)
@@ -322,8 +333,13 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
         return COLIBRI_E_CUDA;
     if (prof_mark(0, s))
         return COLIBRI_E_CUDA;
+    const bool prefill = uses_gemm(cfg, T);
+    // q8 of x: plain codes and scales; decode also wants the even/odd codes and their
+    // corrections, prefill the bf16 codes in the tensor-core order
     Q8Args qa{x, T, d, reinterpret_cast<int8_t *>(ws + L.qx), reinterpret_cast<float *>(ws + L.sx),
-              reinterpret_cast<int8_t *>(ws + L.qx_eo), reinterpret_cast<int *>(ws + L.xc), nullptr};
+              prefill ? nullptr : reinterpret_cast<int8_t *>(ws + L.qx_eo),
+              prefill ? nullptr : reinterpret_cast<int *>(ws + L.xc),
+              prefill ? reinterpret_cast<uint16_t *>(ws + L.xbf) : nullptr};
     const int down_blocks = (d + DN_ITEM_ROWS - 1) / DN_ITEM_ROWS;
     BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks, 0,
                   reinterpret_cast<int32_t *>(ws + L.offsets), reinterpret_cast<int32_t *>(ws + L.pairs),
@@ -332,7 +348,7 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     float *sv = reinterpret_cast<float *>(ws + L.s);
     float *cv = reinterpret_cast<float *>(ws + L.c);
     const SelectArgs sa = select_args(cfg, T, lg, sv, cv, bias, ids, w);
-    if (!ids_given && T <= 32 && T * E <= 8192) {
+    if (!ids_given && !prefill && T * E <= 8192) {
         // a1-a4 for decode in one kernel: q8 of x, logits and scores in every CTA, then
         // selection and bucketing in the last CTA to finish
         static SmemLimits have;
@@ -381,43 +397,78 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     if (cfg->has_shared)
         sh = *shared;
     const int routed_slots = T * K < E ? T * K : E;
-    const int gu_items = (cfg->has_shared ? cfg->shared_ffn / G : 0) + routed_slots * (cfg->ffn / G);
-    DecodeArgs st{};
-    st.experts = experts;
-    st.shared = sh;
-    st.d = d;
-    st.ffn = cfg->ffn;
-    st.shared_ffn = cfg->shared_ffn;
-    st.T = T;
-    st.K = K;
-    st.has_shared = cfg->has_shared;
-    st.fmax = (int)L.fmax;
-    st.slots = reinterpret_cast<const Slot *>(ws + L.slots);
-    st.counters = reinterpret_cast<const Counters *>(ws + L.counters);
-    st.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
-    st.err = err;
-    DecodeArgs ga = st;
-    ga.aq_eo = reinterpret_cast<const int8_t *>(ws + L.qx_eo);
-    ga.as = reinterpret_cast<const float *>(ws + L.sx);
-    ga.ac = reinterpret_cast<const int *>(ws + L.xc);
-    ga.act_stride = d;
-    ga.act_groups = d / G;
-    ga.hq = reinterpret_cast<int8_t *>(ws + L.hq);
-    ga.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
-    ga.hs = reinterpret_cast<float *>(ws + L.hs);
-    ga.hc = reinterpret_cast<int *>(ws + L.hc);
-    if (launch_decode(MODE_GATEUP, ga, gu_items, s) != cudaSuccess || prof_mark(5, s))
-        return COLIBRI_E_CUDA;
-    const int dn_items = (routed_slots + (cfg->has_shared ? 1 : 0)) * down_blocks;
-    DecodeArgs da = st;
-    da.aq_eo = reinterpret_cast<const int8_t *>(ws + L.hq_eo);
-    da.as = reinterpret_cast<const float *>(ws + L.hs);
-    da.ac = reinterpret_cast<const int *>(ws + L.hc);
-    da.act_stride = (long)L.fmax;
-    da.act_groups = (int)L.fmax / G;
-    da.y = reinterpret_cast<float *>(ws + L.y);
-    if (launch_decode(MODE_DOWN, da, dn_items, s) != cudaSuccess || prof_mark(6, s))
-        return COLIBRI_E_CUDA;
+    if (prefill) {
+        // a10-a11: grouped GEMMs on the tensor cores
+        GemmArgs gm{};
+        gm.experts = experts;
+        gm.shared = sh;
+        gm.d = d;
+        gm.ffn = cfg->ffn;
+        gm.shared_ffn = cfg->shared_ffn;
+        gm.T = T;
+        gm.K = K;
+        gm.has_shared = cfg->has_shared;
+        gm.fmax = (int)L.fmax;
+        gm.slots = reinterpret_cast<const Slot *>(ws + L.slots);
+        gm.counters = reinterpret_cast<const Counters *>(ws + L.counters);
+        gm.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
+        gm.err = err;
+        GemmArgs gg = gm;
+        gg.abf = reinterpret_cast<const uint16_t *>(ws + L.xbf);
+        gg.as = reinterpret_cast<const float *>(ws + L.sx);
+        gg.act_stride = d;
+        gg.act_groups = d / G;
+        gg.hbf = reinterpret_cast<uint16_t *>(ws + L.hbf);
+        gg.hs = reinterpret_cast<float *>(ws + L.hs);
+        if (launch_gemm(MODE_GATEUP, gg, s) != cudaSuccess || prof_mark(5, s))
+            return COLIBRI_E_CUDA;
+        GemmArgs gd = gm;
+        gd.abf = reinterpret_cast<const uint16_t *>(ws + L.hbf);
+        gd.as = reinterpret_cast<const float *>(ws + L.hs);
+        gd.act_stride = (long)L.fmax;
+        gd.act_groups = (int)L.fmax / G;
+        gd.y = reinterpret_cast<float *>(ws + L.y);
+        if (launch_gemm(MODE_DOWN, gd, s) != cudaSuccess || prof_mark(6, s))
+            return COLIBRI_E_CUDA;
+    } else {
+        const int gu_items = (cfg->has_shared ? cfg->shared_ffn / G : 0) + routed_slots * (cfg->ffn / G);
+        DecodeArgs st{};
+        st.experts = experts;
+        st.shared = sh;
+        st.d = d;
+        st.ffn = cfg->ffn;
+        st.shared_ffn = cfg->shared_ffn;
+        st.T = T;
+        st.K = K;
+        st.has_shared = cfg->has_shared;
+        st.fmax = (int)L.fmax;
+        st.slots = reinterpret_cast<const Slot *>(ws + L.slots);
+        st.counters = reinterpret_cast<const Counters *>(ws + L.counters);
+        st.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
+        st.err = err;
+        DecodeArgs ga = st;
+        ga.aq_eo = reinterpret_cast<const int8_t *>(ws + L.qx_eo);
+        ga.as = reinterpret_cast<const float *>(ws + L.sx);
+        ga.ac = reinterpret_cast<const int *>(ws + L.xc);
+        ga.act_stride = d;
+        ga.act_groups = d / G;
+        ga.hq = reinterpret_cast<int8_t *>(ws + L.hq);
+        ga.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
+        ga.hs = reinterpret_cast<float *>(ws + L.hs);
+        ga.hc = reinterpret_cast<int *>(ws + L.hc);
+        if (launch_decode(MODE_GATEUP, ga, gu_items, s) != cudaSuccess || prof_mark(5, s))
+            return COLIBRI_E_CUDA;
+        const int dn_items = (routed_slots + (cfg->has_shared ? 1 : 0)) * down_blocks;
+        DecodeArgs da = st;
+        da.aq_eo = reinterpret_cast<const int8_t *>(ws + L.hq_eo);
+        da.as = reinterpret_cast<const float *>(ws + L.hs);
+        da.ac = reinterpret_cast<const int *>(ws + L.hc);
+        da.act_stride = (long)L.fmax;
+        da.act_groups = (int)L.fmax / G;
+        da.y = reinterpret_cast<float *>(ws + L.y);
+        if (launch_decode(MODE_DOWN, da, dn_items, s) != cudaSuccess || prof_mark(6, s))
+            return COLIBRI_E_CUDA;
+    }
 
     // a9: combine
     CombineArgs ca{reinterpret_cast<const float *>(ws + L.y), w, T, K, d, cfg->has_shared, out};
@@ -451,6 +502,18 @@ int colibri_moe_profile_read(float *ms, int n)
         if (cudaEventElapsedTime(&ms[i], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess)
             return COLIBRI_E_CUDA;
     return COLIBRI_OK;
+}
+
+int colibri_debug_umma_i8(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, void *stream)
+{
+    if (!a || !b || !d || n <= 0 || n % 16 || n > 256 || k <= 0 || k % 16 || k > 256)
+        return COLIBRI_E_INVAL;
+    static SmemLimits have;
+    const size_t smem = debug_umma_smem(n, k);
+    if (!smem_attr((const void *)k_debug_umma, smem, have))
+        return COLIBRI_E_CUDA;
+    k_debug_umma<<<1, 128, smem, (cudaStream_t)stream>>>(a, b, n, k, d, nullptr);
+    return cuda_status(cudaGetLastError());
 }
 
 int colibri_debug_group_dots(const uint8_t *w, const int8_t *qa, int rows, int cols, int32_t *dots,

@@ -86,6 +86,21 @@ __device__ __forceinline__ int eo_pos(int k)
     return (k & ~7) + ((k & 1) ? 4 + ((k & 7) >> 1) : ((k & 7) >> 1));
 }
 
+// Position of element k (0..31) of a group in the tensor-core k order: inside each run of
+// 8 elements, slot s holds element (0, 4, 1, 5, 2, 6, 3, 7)[s], the order in which the
+// prefill converters unpack a 32-bit word of eight nibbles into four bf16 pairs.
+__host__ __device__ __forceinline__ int bf16_pos(int k)
+{
+    return (k & ~7) + ((k & 3) << 1) + ((k >> 2) & 1);
+}
+
+// bf16 bit pattern of a small integer (exact for |q| <= 256): the upper half of the fp32
+// pattern of (float)q.
+__device__ __forceinline__ uint16_t bf16_of_int(int q)
+{
+    return (uint16_t)(__float_as_uint((float)q) >> 16);
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -140,6 +155,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among `threads` threads (a multiple of 32) of the CTA on hardware barrier `id`.
+__device__ __forceinline__ void named_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Returns true once the phase with the given parity has completed, false after

@@ -13,7 +13,7 @@ struct Q8Args {
     float *scale;
     int8_t *q_eo;  // optional: codes in even/odd word order
     int *corr;     // optional: 8 * sum(codes) per group
-    int *err;      // optional: cleared by block 0
+    uint16_t *q_bf;  // optional: codes as bf16 in the tensor-core k order (bf16_pos)
 };
 
 struct RouterArgs {
@@ -78,6 +78,32 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode(int mode, DecodeArgs a, int max_items, cudaStream_t s);
+
+// Prefill grouped GEMMs on tcgen05 (kernels_gemm.cu).
+struct GemmArgs {
+    const colibri_expert *experts;
+    colibri_expert shared;
+    int d, ffn, shared_ffn, T, K, has_shared, fmax;
+    const Slot *slots;
+    const Counters *counters;
+    const int32_t *pairs;
+    // activations: codes as bf16 in the tensor-core k order, and their group scales; x
+    // for gate/up (row = token), q8(h) for down (row = pair)
+    const uint16_t *abf;
+    const float *as;
+    long act_stride;   // elements between activation rows of abf
+    int act_groups;    // groups between activation rows of as
+    uint16_t *hbf;     // gate/up output: q8(h) codes as bf16 [pairs_total][fmax]
+    float *hs;         // gate/up output: their scales [pairs_total][fmax/32]
+    float *y;          // down output [pairs_total][d]
+    int *err;
+};
+
+cudaError_t launch_gemm(int mode, const GemmArgs &a, cudaStream_t s);
+
+// tcgen05 test export (kernels_gemm.cu)
+__global__ void k_debug_umma(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, int *err);
+size_t debug_umma_smem(int n, int k);
 
 struct CombineArgs {
     const float *y;

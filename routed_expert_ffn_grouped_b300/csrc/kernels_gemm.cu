@@ -1,0 +1,521 @@
+// Prefill: grouped GEMMs of the routed experts on the tcgen05 tensor cores.
+//
+// The int4 weight codes and int8 activation codes are fed to kind::f16 MMAs as bf16,
+// which holds every integer in [-128, 127] exactly; the products (|q_w * q_a| <= 1016)
+// and their sums over one 32-element quantisation group (<= 32,512 in magnitude) are
+// exact in the fp32 accumulator in tensor memory. So each K-tile is one group: two MMAs
+// (K = 16 each) write a fresh accumulator, which then holds the exact int32 group dots
+// D[m][n]; the epilogue threads read it back (one TMEM lane = one weight row per thread)
+// and apply the group's scales, acc[m][n] += D[m][n] * s_w[m][g] * s_a[n][g], in fp32.
+#include "kernels.cuh"
+#include "umma.cuh"
+
+#include <cuda_bf16.h>
+
+namespace clb {
+
+// ---- test export: one 128 x N x K tile of integer codes through the tensor core ------
+// a int8 [128][k], b int8 [n][k] (row-major), d int32 [128][n]; n % 16 == 0, n <= 256,
+// k % 16 == 0, k <= 256. One CTA of 128 threads; thread m owns row m of D.
+__global__ void __launch_bounds__(128) k_debug_umma(const int8_t *a, const int8_t *b, int n, int k, int32_t *d,
+                                                    int *err)
+{
+    extern __shared__ __align__(1024) unsigned char sm[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t s_tmem;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    unsigned char *As = sm;
+    unsigned char *Bs = sm + (size_t)UMMA_M * k * 2;
+    const uint32_t ncols = n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256;
+    if (warp == 0)
+        tmem_alloc(&s_tmem, ncols);
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    // operands in the canonical layout, two codes (one bf16x2 word) at a time
+    for (int i = tid; i < UMMA_M * k / 2; i += blockDim.x) {
+        const int r = i / (k / 2), c = (i % (k / 2)) * 2;
+        *reinterpret_cast<uint32_t *>(As + umma_off(r, c, k)) = bf16x2_of(a[r * k + c], a[r * k + c + 1]);
+    }
+    for (int i = tid; i < n * k / 2; i += blockDim.x) {
+        const int r = i / (k / 2), c = (i % (k / 2)) * 2;
+        *reinterpret_cast<uint32_t *>(Bs + umma_off(r, c, k)) = bf16x2_of(b[r * k + c], b[r * k + c + 1]);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    if (tid == 0) {
+        const uint32_t idesc = umma_idesc_bf16(UMMA_M, n);
+        for (int ks = 0; ks < k / UMMA_K; ++ks) {
+            const uint64_t ad = umma_desc(smem_u32(As) + ks * 256, 128, k * 16);
+            const uint64_t bd = umma_desc(smem_u32(Bs) + ks * 256, 128, k * 16);
+            umma_bf16(tmem, ad, bd, idesc, ks > 0);
+        }
+        umma_commit(&bar);
+    }
+    const bool ok = mbar_wait(&bar, 0);
+    tc_fence_after();
+    if (ok) {
+        for (int c0 = 0; c0 < n; c0 += 16) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                d[(long)tid * n + c0 + j] = (int32_t)v[j];
+        }
+    } else if (tid == 0 && err) {
+        atomicOr(err, ERR_WAIT_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0)
+        tmem_dealloc(tmem, ncols);
+}
+
+size_t debug_umma_smem(int n, int k)
+{
+    return (size_t)(UMMA_M + n) * k * 2;
+}
+
+// ---- prefill grouped GEMM -------------------------------------------------------------
+// Work item = (slot, 128-row tile of the weight matrix, tile of up to GT_N of the slot's
+// tokens); items are ordered slot by slot, row tile by row tile, token tile innermost, so
+// that CTAs working at the same time share weight tiles through L2. Persistent CTAs take
+// items round robin. Warp roles in a CTA:
+//   warp 0      loader: bulk-copies GS-group chunks of the weight tiles and their scales
+//               (four 32-row blocks per matrix, contiguous runs) into a raw ring;
+//   warp 1      MMA issuer (one thread): per group, two K = 16 MMAs per matrix into a
+//               fresh TMEM accumulator (double-buffered), then commits;
+//   warps 2-5   converters: per group, nibbles -> bf16 A tiles (magic-number trick, k in
+//               the tensor-core order), the token tile's bf16 codes -> B tile, and the
+//               group's weight and activation scales, into a converted ring;
+//   warps 6-13  epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
+//               32*((w-6)/4).. (its tokens) of each group's D and accumulates
+//               D * s_w * s_a in registers; at the end of an item it forms the output.
+constexpr int GT_N = 64;       // tokens per item
+constexpr int GT_GS = 4;       // groups per raw (bulk-copied) stage
+constexpr int GT_RR = 4;       // raw ring stages
+constexpr int GT_CQ = 4;       // converted ring stages
+constexpr int GT_THREADS = 14 * 32;
+constexpr int GT_EPI0 = 6;     // first epilogue warp
+constexpr int GT_NEPI = 8;
+
+struct GemmItem {
+    colibri_expert ex;
+    int is_shared, mt, begin, count, n0, nt, kdim, slot;
+};
+
+// Item -> (slot, row tile, token tile). Per slot: row tiles * token tiles items.
+template <int MODE>
+__device__ __forceinline__ bool gemm_item(const GemmArgs &a, const int *pre, int n_slots, int item, GemmItem &it)
+{
+    int lo = 0, hi = n_slots;  // pre: inclusive prefix of items per slot
+    if (item >= pre[n_slots - 1])
+        return false;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (pre[mid] > item)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    const int slot = lo;
+    const int local = item - (slot ? pre[slot - 1] : 0);
+    const Slot sd = a.slots[slot];
+    it.slot = slot;
+    it.is_shared = sd.expert < 0;
+    it.ex = it.is_shared ? a.shared : a.experts[sd.expert];
+    const int ntiles = (sd.count + GT_N - 1) / GT_N;
+    it.mt = local / ntiles;
+    const int tt = local % ntiles;
+    it.n0 = tt * GT_N;
+    it.nt = min(GT_N, sd.count - it.n0);
+    it.begin = sd.begin;
+    it.count = sd.count;
+    it.kdim = MODE == MODE_GATEUP ? a.d : (it.is_shared ? a.shared_ffn : a.ffn);
+    return true;
+}
+
+template <int MODE>
+__device__ __forceinline__ int gemm_rows(const GemmArgs &a, int is_shared)
+{
+    return MODE == MODE_GATEUP ? (is_shared ? a.shared_ffn : a.ffn) : a.d;
+}
+
+// Shared memory: raw ring [GT_RR][M][ (4 blocks * GS tiles * 512) + (4 * GS * 128) ] |
+// converted ring [GT_CQ][ M * 8 KB A tiles | 4 KB B tile | M * 128 sw | GT_N sa ] |
+// barriers | item prefix [n_slots <= 1025].
+template <int MODE>
+struct GemmSmem {
+    static constexpr int M = MODE == MODE_GATEUP ? 2 : 1;
+    static constexpr int RAW_W = 4 * GT_GS * 512;      // one matrix's nibbles per stage
+    static constexpr int RAW_S = 4 * GT_GS * 128;      // one matrix's scales per stage
+    static constexpr int RAW = M * (RAW_W + RAW_S);
+    static constexpr int CA = UMMA_M * 32 * 2;         // one bf16 A tile (128 x 32)
+    static constexpr int CB = GT_N * 32 * 2;           // bf16 B tile (GT_N x 32)
+    static constexpr int CONV = M * CA + CB + M * UMMA_M * 4 + GT_N * 4;
+    static constexpr int BARS = 8 * (2 * GT_RR + 2 * GT_CQ + 4) + 16;
+    static constexpr int PRE = 4 * 1040;  // item prefix over at most 1025 slots
+    static constexpr int TOTAL = GT_RR * RAW + GT_CQ * CONV + BARS + PRE;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
+{
+    using L = GemmSmem<MODE>;
+    constexpr int M = L::M;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    unsigned char *raw = sm;
+    unsigned char *conv = sm + GT_RR * L::RAW;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(conv + GT_CQ * L::CONV);
+    uint64_t *raw_full = bars, *raw_empty = bars + GT_RR;
+    uint64_t *conv_full = bars + 2 * GT_RR, *conv_empty = conv_full + GT_CQ;
+    uint64_t *tm_full = conv_empty + GT_CQ, *tm_empty = tm_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + 2);
+    int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+    int *pre = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(bars) + L::BARS);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const Counters ct = *a.counters;
+    const int n_slots = ct.n_slots;
+
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, 256);
+        if (lane == 0) {
+            for (int i = 0; i < GT_RR; ++i) {
+                mbar_init(&raw_full[i], 1);
+                mbar_init(&raw_empty[i], 4);
+            }
+            for (int i = 0; i < GT_CQ; ++i) {
+                mbar_init(&conv_full[i], 4);
+                mbar_init(&conv_empty[i], 1 + GT_NEPI);
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&tm_full[i], 1);
+                mbar_init(&tm_empty[i], GT_NEPI);
+            }
+            *abort_flag = 0;
+            fence_mbar_init();
+        }
+    }
+    if (warp == 1) {
+        // items per slot, inclusive prefix (n_slots <= 1025)
+        int run = 0;
+        for (int s0 = 0; s0 < n_slots; s0 += 32) {
+            const int sl = s0 + lane;
+            int v = 0;
+            if (sl < n_slots) {
+                const Slot sd = a.slots[sl];
+                v = (gemm_rows<MODE>(a, sd.expert < 0) / UMMA_M) * ((sd.count + GT_N - 1) / GT_N);
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(FULL, v, o);
+                if (lane >= o)
+                    v += u;
+            }
+            if (sl < n_slots)
+                pre[sl] = run + v;
+            run += __shfl_sync(FULL, v, 31);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int n_items = n_slots > 0 ? pre[n_slots - 1] : 0;
+    auto fail = [&]() {
+        atomicOr(a.err, ERR_WAIT_TIMEOUT);
+        *reinterpret_cast<volatile int *>(abort_flag) = 1;
+    };
+    auto aborted = [&]() { return *reinterpret_cast<volatile int *>(abort_flag) != 0; };
+
+    if (warp == 0) {
+        // ---------------- loader ----------------
+        if (lane == 0) {
+            uint32_t st = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                GemmItem it;
+                gemm_item<MODE>(a, pre, n_slots, item, it);
+                const int ng = it.kdim / G;
+                for (int g0 = 0; ok && g0 < ng; g0 += GT_GS, ++st) {
+                    const int slot = st % GT_RR;
+                    if (st >= GT_RR && !mbar_wait(&raw_empty[slot], ((st / GT_RR) - 1) & 1)) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    if (aborted()) {
+                        ok = false;
+                        break;
+                    }
+                    const int n = min(GT_GS, ng - g0);
+                    unsigned char *dst = raw + (size_t)slot * L::RAW;
+                    mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)(M * 4 * n * (512 + 128)));
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        const uint8_t *W = m == 0 ? (MODE == MODE_GATEUP ? it.ex.w1 : it.ex.w2) : it.ex.w3;
+                        const float *S = m == 0 ? (MODE == MODE_GATEUP ? it.ex.s1 : it.ex.s2) : it.ex.s3;
+                        for (int b = 0; b < 4; ++b) {
+                            const size_t tile = (size_t)(it.mt * 4 + b) * ng + g0;  // group tile index
+                            bulk_g2s(dst + m * L::RAW_W + b * GT_GS * 512, W + tile * 512, n * 512, &raw_full[slot]);
+                            bulk_g2s(dst + M * L::RAW_W + m * L::RAW_S + b * GT_GS * 128, S + tile * 32, n * 128,
+                                     &raw_full[slot]);
+                        }
+                    }
+                }
+            }
+            // bounded wait for the copies issued, so that none lands after the CTA exits
+            const uint32_t nwait = st < GT_RR ? st : GT_RR;
+            for (uint32_t k = 1; k <= nwait; ++k)
+                mbar_wait(&raw_full[(st - k) % GT_RR], ((st - k) / GT_RR) & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            uint32_t cs = 0, gcount = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                GemmItem it;
+                gemm_item<MODE>(a, pre, n_slots, item, it);
+                const int ng = it.kdim / G;
+                const int nn = max(16, (it.nt + 15) & ~15);
+                const uint32_t idesc = umma_idesc_bf16(UMMA_M, nn);
+                for (int g = 0; g < ng; ++g, ++cs, ++gcount) {
+                    const int slot = cs % GT_CQ, tb = gcount & 1;
+                    if (!mbar_wait(&conv_full[slot], (cs / GT_CQ) & 1) ||
+                        (gcount >= 2 && !mbar_wait(&tm_empty[tb], ((gcount >> 1) - 1) & 1))) {
+                        fail();
+                        ok = false;
+                        break;
+                    }
+                    if (aborted()) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t cb = smem_u32(conv + (size_t)slot * L::CONV);
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            const uint64_t ad = umma_desc(cb + m * L::CA + ks * 256, 128, 32 * 16);
+                            const uint64_t bd = umma_desc(cb + M * L::CA + ks * 256, 128, 32 * 16);
+                            umma_bf16(tmem + tb * 128 + m * 64, ad, bd, idesc, ks);
+                        }
+                    }
+                    umma_commit(&conv_empty[slot]);
+                    umma_commit(&tm_full[tb]);
+                }
+            }
+        }
+    } else if (warp < GT_EPI0) {
+        // ---------------- converters (128 threads) ----------------
+        const int c = threadIdx.x - 64;  // 0..127: weight row of the tile / token chunk worker
+        uint32_t rs = 0, cs = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            GemmItem it;
+            gemm_item<MODE>(a, pre, n_slots, item, it);
+            const int ng = it.kdim / G;
+            // this thread's token (two threads per token: chunks 0-1 and 2-3)
+            const int tn = c >> 1, half = c & 1;
+            long arow = -1;
+            if (tn < it.nt) {
+                const int cidx = it.n0 + tn;
+                if (MODE == MODE_GATEUP)
+                    arow = it.is_shared ? cidx : a.pairs[it.begin + cidx] / a.K;
+                else
+                    arow = it.is_shared ? (long)a.T * a.K + cidx : a.pairs[it.begin + cidx];
+            }
+            for (int g0 = 0; ok && g0 < ng; g0 += GT_GS, ++rs) {
+                const int rslot = rs % GT_RR;
+                if (!mbar_wait(&raw_full[rslot], (rs / GT_RR) & 1)) {
+                    if (lane == 0)
+                        fail();
+                    ok = false;
+                    break;
+                }
+                const unsigned char *rb = raw + (size_t)rslot * L::RAW;
+                const int n = min(GT_GS, ng - g0);
+                for (int gi = 0; gi < n; ++gi, ++cs) {
+                    const int slot = cs % GT_CQ;
+                    if (cs >= GT_CQ && !mbar_wait(&conv_empty[slot], ((cs / GT_CQ) - 1) & 1)) {
+                        if (lane == 0)
+                            fail();
+                        ok = false;
+                        break;
+                    }
+                    unsigned char *cb = conv + (size_t)slot * L::CONV;
+                    const int blk = c >> 5, r = c & 31;
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        // row c's 32 nibbles of this group -> 32 bf16 in four 16-byte chunks
+                        const uint4 w = *reinterpret_cast<const uint4 *>(rb + m * L::RAW_W + (blk * GT_GS + gi) * 512 + r * 16);
+                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                        const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t p[4];
+#pragma unroll
+                            for (int s = 0; s < 4; ++s) {
+                                const uint32_t u = ((wv[j] >> (4 * s)) & 0x000F000Fu) | 0x43004300u;
+                                const __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&u), off);
+                                p[s] = *reinterpret_cast<const uint32_t *>(&h);
+                            }
+                            *reinterpret_cast<uint4 *>(cb + m * L::CA + umma_off(c, 8 * j, 32)) =
+                                make_uint4(p[0], p[1], p[2], p[3]);
+                        }
+                        // the row's weight scale of this group
+                        reinterpret_cast<float *>(cb + M * L::CA + L::CB)[m * UMMA_M + c] =
+                            *reinterpret_cast<const float *>(rb + M * L::RAW_W + m * L::RAW_S + (blk * GT_GS + gi) * 128 + r * 4);
+                    }
+                    // the token tile: two 16-byte chunks of this thread's token, or zeros
+                    const int g = g0 + gi;
+                    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+                    if (arow >= 0) {
+                        const uint16_t *src = a.abf + arow * a.act_stride + (long)g * G + half * 16;
+                        v0 = ld_nc(src);
+                        v1 = ld_nc(src + 8);
+                        if (half == 0)
+                            reinterpret_cast<float *>(cb + M * L::CA + L::CB + M * UMMA_M * 4)[tn] =
+                                a.as[arow * a.act_groups + g];
+                    }
+                    if (tn < GT_N) {
+                        *reinterpret_cast<uint4 *>(cb + M * L::CA + umma_off(tn, half * 16, 32)) = v0;
+                        *reinterpret_cast<uint4 *>(cb + M * L::CA + umma_off(tn, half * 16 + 8, 32)) = v1;
+                    }
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&conv_full[slot]);
+                }
+                if (!ok)
+                    break;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&raw_empty[rslot]);
+            }
+        }
+    } else {
+        // ---------------- epilogue (256 threads) ----------------
+        const int e = warp - GT_EPI0;
+        const int q = warp & 3, chalf = e >> 2;  // TMEM lane quarter (rows), token half
+        const int row = q * 32 + lane;             // row within the 128-row tile
+        uint32_t cs = 0, gcount = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            GemmItem it;
+            gemm_item<MODE>(a, pre, n_slots, item, it);
+            const int ng = it.kdim / G;
+            float acc[M][32];
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    acc[m][j] = 0.0f;
+            for (int g = 0; g < ng; ++g, ++cs, ++gcount) {
+                const int slot = cs % GT_CQ, tb = gcount & 1;
+                if (!mbar_wait(&tm_full[tb], (gcount >> 1) & 1)) {
+                    if (lane == 0)
+                        fail();
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const unsigned char *cb = conv + (size_t)slot * L::CONV;
+                const float *sw = reinterpret_cast<const float *>(cb + M * L::CA + L::CB);
+                const float *sa = sw + M * UMMA_M + chalf * 32;
+                // 16 columns at a time: TMEM -> registers -> fma into the accumulators
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const float swm = sw[m * UMMA_M + row];
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * 128 + m * 64 + chalf * 32;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float dv[16];
+                        tmem_ld16(ta + 16 * h, dv);
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 v = *reinterpret_cast<const float4 *>(sa + 16 * h + j);
+                            acc[m][16 * h + j] = fmaf(dv[j], swm * v.x, acc[m][16 * h + j]);
+                            acc[m][16 * h + j + 1] = fmaf(dv[j + 1], swm * v.y, acc[m][16 * h + j + 1]);
+                            acc[m][16 * h + j + 2] = fmaf(dv[j + 2], swm * v.z, acc[m][16 * h + j + 2]);
+                            acc[m][16 * h + j + 3] = fmaf(dv[j + 3], swm * v.w, acc[m][16 * h + j + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&tm_empty[tb]);
+                    mbar_arrive(&conv_empty[slot]);
+                }
+            }
+            if (!ok)
+                break;
+            // item output: columns chalf*32 + j < nt are tokens n0 + that of the slot
+            const int orow = it.mt * UMMA_M + row;  // output row (h row or d row)
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int col = chalf * 32 + j;
+                const bool valid = col < it.nt;
+                long pr = 0;
+                if (valid) {
+                    const int cidx = it.n0 + col;
+                    pr = it.is_shared ? (long)a.T * a.K + cidx : a.pairs[it.begin + cidx];
+                }
+                if (MODE == MODE_GATEUP) {
+                    const float gt = acc[0][j], up = acc[M - 1][j];
+                    const float h = gt / (1.0f + expf(-gt)) * up;
+                    const float amax = warp_max(fabsf(h));  // the 32 rows of one h group
+                    const float dd = __fdiv_rn(amax, 127.0f);
+                    const int qv = q8_code(h, dd);
+                    if (valid) {
+                        const long hb = pr * a.fmax + (long)(orow & ~31);
+                        a.hbf[hb + bf16_pos(lane)] = bf16_of_int(qv);
+                        if (lane == 0)
+                            a.hs[pr * (a.fmax / G) + orow / G] = dd;
+                    }
+                } else if (valid) {
+                    a.y[pr * a.d + orow] = acc[0][j];
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+cudaError_t launch_gemm(int mode, const GemmArgs &a, cudaStream_t s)
+{
+    int dev = 0, n_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    if (mode == MODE_GATEUP) {
+        const int smem = GemmSmem<MODE_GATEUP>::TOTAL;
+        e = cudaFuncSetAttribute(k_gemm<MODE_GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        k_gemm<MODE_GATEUP><<<n_sm, GT_THREADS, smem, s>>>(a);
+    } else {
+        const int smem = GemmSmem<MODE_DOWN>::TOTAL;
+        e = cudaFuncSetAttribute(k_gemm<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        k_gemm<MODE_DOWN><<<n_sm, GT_THREADS, smem, s>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace clb

@@ -7,31 +7,15 @@ namespace clb {
 // One warp per 32-element group, lane k holds element k. Writes the plain codes and
 // scales; optionally also the even/odd-ordered codes and the offset correction
 // 8 * sum(codes) the decode GEMV consumes.
+__device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane);
+
 __global__ void __launch_bounds__(256) k_q8(Q8Args a)
 {
     const int lane = threadIdx.x & 31;
     const long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int ng = a.cols / G;
-    if (a.err && blockIdx.x == 0 && threadIdx.x == 0)
-        *a.err = 0;  // the first kernel of a layer call clears the flag
-    if (gw >= (long)a.rows * ng)
+    if (gw >= a.rows * (a.cols / G))
         return;
-    const long row = gw / ng;
-    const int g = (int)(gw % ng);
-    const long base = row * a.cols + (long)g * G;
-    const float x = a.x[base + lane];
-    const float amax = warp_max(fabsf(x));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const int q = q8_code(x, d);
-    a.q[base + lane] = (int8_t)q;
-    if (lane == 0)
-        a.scale[row * ng + g] = d;
-    if (a.q_eo) {
-        a.q_eo[base + eo_pos(lane)] = (int8_t)q;
-        const int s = warp_sum_i(q);
-        if (lane == 0)
-            a.corr[row * ng + g] = 8 * s;
-    }
+    q8_group(a, gw, lane);
 }
 
 // ---- router logits (+ the fp64 sigmoid, + q8 of x as a side job) --------------------
@@ -56,6 +40,8 @@ __device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane)
     a.q[base + lane] = (int8_t)q;
     if (lane == 0)
         a.scale[row * ng + g] = d;
+    if (a.q_bf)
+        a.q_bf[base + bf16_pos(lane)] = bf16_of_int(q);
     if (a.q_eo) {
         a.q_eo[base + eo_pos(lane)] = (int8_t)q;
         const int s = warp_sum_i(q);

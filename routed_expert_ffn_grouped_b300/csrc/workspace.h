@@ -11,10 +11,14 @@ namespace clb {
 struct WsLayout {
     size_t err, counters, qx, qx_eo, sx, xc, logits, s, c, offsets, pairs, slots;
     size_t hq, hq_eo, hs, hc, y;
+    size_t xbf, hbf;  // prefill (T > DECODE_T_MAX): bf16 codes of x and of q8(h)
     size_t fmax, total;
 };
 
+constexpr int DECODE_T_MAX = 32;  // larger batches take the tensor-core prefill path
+
 bool cfg_valid(const colibri_layer_cfg *c);
+bool uses_gemm(const colibri_layer_cfg *c, int T);
 WsLayout ws_layout(const colibri_layer_cfg *c, int T);
 
 }  // namespace clb

@@ -128,6 +128,24 @@ def test_group_dots_bit_exact(torch_cuda, C, orc, rows, cols):
     assert np.array_equal(dots.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("n,k", [(16, 16), (16, 32), (64, 32), (128, 64), (256, 256)])
+def test_umma_tile_integer_dots_exact(torch_cuda, C, n, k):
+    """One tcgen05 tile of int4-range weight codes against int8 activation codes: the
+    int32 result must equal the integer matmul exactly (brute force in int64)."""
+    torch = torch_cuda
+    rng = np.random.default_rng(n * 1000 + k)
+    a = rng.integers(-8, 8, (128, k)).astype(np.int8)
+    b = rng.integers(-127, 128, (n, k)).astype(np.int8)
+    a[0, :32 if k >= 32 else k] = -8                  # the extreme group: -8 x -127 per element
+    b[0, :32 if k >= 32 else k] = -127
+    d = torch.empty((128, n), dtype=torch.int32, device="cuda")
+    C.colibri_debug_umma_i8(to_dev(torch, a), to_dev(torch, b), d)
+    torch.cuda.synchronize()
+    want = a.astype(np.int64) @ b.astype(np.int64).T
+    assert want[0, 0] == 1016 * min(k, 32) + (int(a[0, 32:].astype(np.int64) @ b[0, 32:].astype(np.int64)) if k > 32 else 0)
+    assert np.array_equal(d.cpu().numpy().astype(np.int64), want)
+
+
 # ------------------------------------------------------------------ the layer
 def run_layer(torch, C, dl, x, ids=None, w=None):
     spec = dl.spec
@@ -223,6 +241,22 @@ def test_moe_layer_empty_and_deterministic(torch_cuda, C):
     a, _, _, _ = run_layer(torch, C, dl, x)
     b, _, _, _ = run_layer(torch, C, dl, x)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 33), ("tiny", 100), ("olmoe", 48)])
+def test_prefill_gemm_parity(torch_cuda, C, orc, name, T):
+    """Batches above 32 tokens run the tcgen05 grouped GEMMs: every token against the
+    oracle, ragged token tiles (counts not multiples of the 64-token tile) included."""
+    torch = torch_cuda
+    spec = synth.SPECS[name]
+    host, dl = dev_layer(C, spec)
+    x = synth.activations(spec, 0, T, step=31, row_scale=True)
+    out, ids, w, ws = run_layer(torch, C, dl, x)
+    assert C.colibri_workspace_status(dl.cfg, T, ws) == C.OK
+    ref, ids_o, w_o = orc.moe_layer(spec, x, host.Wr, host.bias, host.expert, host.shared())
+    assert np.array_equal(ids, ids_o)
+    np.testing.assert_allclose(w, w_o, rtol=1e-6)
+    assert_rms_close(out, ref)
 
 
 def test_glm_prefill_sampled(torch_cuda, C, orc):
