@@ -213,11 +213,24 @@ static int launch_route_logits(const colibri_layer_cfg *cfg, const float *x, int
     static SmemLimits have;
     const int xt = route_xt(cfg->d, T);
     const size_t smem = (size_t)cfg->d * 4 * (size_t)(1 + xt);
-    if (!smem_attr((const void *)k_route_logits, smem, have))
-        return COLIBRI_E_CUDA;
     const bool sig = cfg->router != COLIBRI_ROUTER_SOFTMAX;
     RouterArgs ra{x, T, cfg->d, cfg->n_exp, xt, Wr, sig ? bias : nullptr, logits,
                   sig ? s_arr : nullptr, sig ? c_arr : nullptr, q8, err};
+    if (T > DECODE_T_MAX) {
+        // many tokens: (token x expert) tiles; q8 of x runs as its own kernel
+        if (q8.x) {
+            const long groups = (long)T * (cfg->d / G);
+            k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(q8);
+            if (cudaGetLastError() != cudaSuccess)
+                return COLIBRI_E_CUDA;
+        }
+        ra.q8.x = nullptr;
+        dim3 grid((T + 15) / 16, (cfg->n_exp + 31) / 32);
+        k_route_logits_tiled<<<grid, 256, 0, s>>>(ra);
+        return cuda_status(cudaGetLastError());
+    }
+    if (!smem_attr((const void *)k_route_logits, smem, have))
+        return COLIBRI_E_CUDA;
     k_route_logits<<<cfg->n_exp, 128, smem, s>>>(ra);
     return cuda_status(cudaGetLastError());
 }

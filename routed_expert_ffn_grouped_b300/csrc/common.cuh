@@ -16,9 +16,19 @@ constexpr int ERR_BAD_ID = 1;       // an expert id outside [0, E)
 constexpr int ERR_WAIT_TIMEOUT = 2; // an mbarrier or flag wait ran out of iterations
 constexpr int ERR_BAD_SHAPE = 4;    // a kernel was handed a shape it does not cover
 
-// Bound on spin iterations of any wait in these kernels. try_wait suspends the thread
-// for a hardware-chosen interval per attempt, so this is far beyond any legal wait.
-constexpr uint32_t WAIT_LIMIT = 1u << 24;
+// Bound on any wait in these kernels: a wait gives up (and its kernel reports
+// ERR_WAIT_TIMEOUT) after WAIT_LIMIT_NS of global time, far beyond any legal wait.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+// Suspend-time hint of one mbarrier try_wait: the thread sleeps until the phase completes
+// or this much time passes, instead of spinning on the issue slots.
+constexpr uint32_t WAIT_HINT_NS = 1000000u;
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 // One-use loads of weight bytes: bypass L1, they are read once per call.
 __device__ __forceinline__ uint4 ld_stream(const void *p)
@@ -169,23 +179,29 @@ __device__ __forceinline__ void named_sync(int id, int threads)
 }
 
 // Returns true once the phase with the given parity has completed, false after
-// WAIT_LIMIT attempts.
+// WAIT_LIMIT_NS. Each try_wait suspends the thread (up to WAIT_HINT_NS) until the phase
+// completes.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
-    uint32_t addr = smem_u32(bar);
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    const uint32_t addr = smem_u32(bar);
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(addr), "r"(parity)
+            : "r"(addr), "r"(parity), "r"(WAIT_HINT_NS)
             : "memory");
         if (done)
             return true;
+        const uint64_t now = global_ns();
+        if (i == 0)
+            t0 = now;
+        else if (now - t0 > WAIT_LIMIT_NS)
+            return false;
     }
-    return false;
 }
 
 // Hint: bring [src, src + bytes) into L2 (no completion to wait for). src 16-byte

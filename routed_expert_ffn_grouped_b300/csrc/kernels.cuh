@@ -115,6 +115,7 @@ struct CombineArgs {
 
 __global__ void k_q8(Q8Args a);
 __global__ void k_route_logits(RouterArgs a);
+__global__ void k_route_logits_tiled(RouterArgs a);
 __global__ void k_route_decode(RouterArgs ra, SelectArgs sa, BucketArgs ba, int *done);
 size_t route_decode_smem_bytes(int T, int K, int E, int d, int xt);
 size_t bucket_smem_bytes(int E, int nthreads);

@@ -88,20 +88,21 @@ size_t debug_umma_smem(int n, int k)
 //   warp 0      loader: bulk-copies GS-group chunks of the weight tiles and their scales
 //               (four 32-row blocks per matrix, contiguous runs) into a raw ring;
 //   warp 1      MMA issuer (one thread): per group, two K = 16 MMAs per matrix into a
-//               fresh TMEM accumulator (double-buffered), then commits;
-//   warps 2-5   converters: per group, nibbles -> bf16 A tiles (magic-number trick, k in
-//               the tensor-core order), the token tile's bf16 codes -> B tile, and the
-//               group's weight and activation scales, into a converted ring;
+//               fresh TMEM accumulator (GT_TB buffers), then commits;
+//   warps 2-5   converters, one group each: nibbles -> bf16 A tiles (magic-number
+//               trick, k in the tensor-core order), the token tile's bf16 codes -> B
+//               tile, and the group's weight and activation scales, into a converted ring;
 //   warps 6-13  epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
 //               32*((w-6)/4).. (its tokens) of each group's D and accumulates
 //               D * s_w * s_a in registers; at the end of an item it forms the output.
 constexpr int GT_N = 64;       // tokens per item
 constexpr int GT_GS = 4;       // groups per raw (bulk-copied) stage
 constexpr int GT_RR = 4;       // raw ring stages
-constexpr int GT_CQ = 4;       // converted ring stages
+constexpr int GT_CQ = 6;       // converted ring stages
 constexpr int GT_THREADS = 14 * 32;
 constexpr int GT_EPI0 = 6;     // first epilogue warp
 constexpr int GT_NEPI = 8;
+constexpr int GT_TB = 4;       // TMEM accumulator buffers (128 columns each)
 
 struct GemmItem {
     colibri_expert ex;
@@ -157,7 +158,7 @@ struct GemmSmem {
     static constexpr int CA = UMMA_M * 32 * 2;         // one bf16 A tile (128 x 32)
     static constexpr int CB = GT_N * 32 * 2;           // bf16 B tile (GT_N x 32)
     static constexpr int CONV = M * CA + CB + M * UMMA_M * 4 + GT_N * 4;
-    static constexpr int BARS = 8 * (2 * GT_RR + 2 * GT_CQ + 4) + 16;
+    static constexpr int BARS = 8 * (2 * GT_RR + 2 * GT_CQ + 2 * GT_TB) + 16;
     static constexpr int PRE = 4 * 1040;  // item prefix over at most 1025 slots
     static constexpr int TOTAL = GT_RR * RAW + GT_CQ * CONV + BARS + PRE;
 };
@@ -173,8 +174,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
     uint64_t *bars = reinterpret_cast<uint64_t *>(conv + GT_CQ * L::CONV);
     uint64_t *raw_full = bars, *raw_empty = bars + GT_RR;
     uint64_t *conv_full = bars + 2 * GT_RR, *conv_empty = conv_full + GT_CQ;
-    uint64_t *tm_full = conv_empty + GT_CQ, *tm_empty = tm_full + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + 2);
+    uint64_t *tm_full = conv_empty + GT_CQ, *tm_empty = tm_full + GT_TB;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + GT_TB);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
     int *pre = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(bars) + L::BARS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,17 +183,17 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
     const int n_slots = ct.n_slots;
 
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 256);
+        tmem_alloc(tmem_slot, 128 * GT_TB);
         if (lane == 0) {
             for (int i = 0; i < GT_RR; ++i) {
                 mbar_init(&raw_full[i], 1);
                 mbar_init(&raw_empty[i], 4);
             }
             for (int i = 0; i < GT_CQ; ++i) {
-                mbar_init(&conv_full[i], 4);
+                mbar_init(&conv_full[i], 1);
                 mbar_init(&conv_empty[i], 1 + GT_NEPI);
             }
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < GT_TB; ++i) {
                 mbar_init(&tm_full[i], 1);
                 mbar_init(&tm_empty[i], GT_NEPI);
             }
@@ -285,9 +286,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 const int nn = max(16, (it.nt + 15) & ~15);
                 const uint32_t idesc = umma_idesc_bf16(UMMA_M, nn);
                 for (int g = 0; g < ng; ++g, ++cs, ++gcount) {
-                    const int slot = cs % GT_CQ, tb = gcount & 1;
+                    const int slot = cs % GT_CQ, tb = gcount % GT_TB;
                     if (!mbar_wait(&conv_full[slot], (cs / GT_CQ) & 1) ||
-                        (gcount >= 2 && !mbar_wait(&tm_empty[tb], ((gcount >> 1) - 1) & 1))) {
+                        (gcount >= GT_TB && !mbar_wait(&tm_empty[tb], ((gcount / GT_TB) - 1) & 1))) {
                         fail();
                         ok = false;
                         break;
@@ -313,91 +314,157 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
             }
         }
     } else if (warp < GT_EPI0) {
-        // ---------------- converters (128 threads) ----------------
-        const int c = threadIdx.x - 64;  // 0..127: weight row of the tile / token chunk worker
-        uint32_t rs = 0, cs = 0;
+        // ---------------- converters (4 warps) ----------------
+        // Converter warp cw takes group cw of each raw chunk (GS = 4 groups), so four
+        // groups convert at once. Lane l handles rows l, l+32, l+64, l+96 of the 128-row
+        // weight tile (512 contiguous bytes per row block and group) and tokens l, l+32
+        // of the token tile. Nibbles become bf16 by a mask and the magic exponent 0x4300
+        // (128 + nibble) minus 136, in the tensor-core k order. The activations of the
+        // warp's next group are loaded one chunk ahead, so their L2 latency hides behind
+        // the current chunk.
+        const int cw = warp - 2;
+        uint32_t rs = 0, cb0 = 0;  // raw chunks seen, conversion stages of earlier chunks
         bool ok = true;
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        struct Chunk {
+            int item, g0, ng;
+            long arow[2];
             GemmItem it;
-            gemm_item<MODE>(a, pre, n_slots, item, it);
-            const int ng = it.kdim / G;
-            // this thread's token (two threads per token: chunks 0-1 and 2-3)
-            const int tn = c >> 1, half = c & 1;
-            long arow = -1;
-            if (tn < it.nt) {
-                const int cidx = it.n0 + tn;
-                if (MODE == MODE_GATEUP)
-                    arow = it.is_shared ? cidx : a.pairs[it.begin + cidx] / a.K;
-                else
-                    arow = it.is_shared ? (long)a.T * a.K + cidx : a.pairs[it.begin + cidx];
+        };
+        auto chunk_at = [&](int item, int g0, Chunk &ck) -> bool {
+            if (item >= n_items)
+                return false;
+            ck.item = item;
+            ck.g0 = g0;
+            gemm_item<MODE>(a, pre, n_slots, item, ck.it);
+            ck.ng = ck.it.kdim / G;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int tn = lane + 32 * h;
+                ck.arow[h] = -1;
+                if (tn < ck.it.nt) {
+                    const int cidx = ck.it.n0 + tn;
+                    if (MODE == MODE_GATEUP)
+                        ck.arow[h] = ck.it.is_shared ? cidx : a.pairs[ck.it.begin + cidx] / a.K;
+                    else
+                        ck.arow[h] = ck.it.is_shared ? (long)a.T * a.K + cidx : a.pairs[ck.it.begin + cidx];
+                }
             }
-            for (int g0 = 0; ok && g0 < ng; g0 += GT_GS, ++rs) {
-                const int rslot = rs % GT_RR;
-                if (!mbar_wait(&raw_full[rslot], (rs / GT_RR) & 1)) {
+            return true;
+        };
+        auto next_of = [&](const Chunk &ck, Chunk &nx) -> bool {
+            if (ck.g0 + GT_GS < ck.ng) {
+                nx = ck;
+                nx.g0 = ck.g0 + GT_GS;
+                return true;
+            }
+            return chunk_at(ck.item + gridDim.x, 0, nx);
+        };
+        // this warp's group of a chunk: tokens lane, lane+32, four 16-byte chunks each
+        uint4 vc[2][4], vn[2][4];
+        float sc[2], sn[2];
+        auto load_acts = [&](const Chunk &ck, uint4 (&v)[2][4], float (&sv)[2]) {
+            const int g = ck.g0 + cw;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sv[h] = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    v[h][q] = make_uint4(0, 0, 0, 0);
+                if (ck.arow[h] >= 0 && g < ck.ng) {
+                    const uint16_t *src = a.abf + ck.arow[h] * a.act_stride + (long)g * G;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        v[h][q] = ld_nc(src + 8 * q);
+                    sv[h] = a.as[ck.arow[h] * a.act_groups + g];
+                }
+            }
+        };
+        Chunk cur, nxt;
+        bool have = chunk_at(blockIdx.x, 0, cur);
+        if (have)
+            load_acts(cur, vc, sc);
+        while (ok && have) {
+            const bool more = next_of(cur, nxt);
+            if (more)
+                load_acts(nxt, vn, sn);
+            const int rslot = rs % GT_RR;
+            if (!mbar_wait(&raw_full[rslot], (rs / GT_RR) & 1)) {
+                if (lane == 0)
+                    fail();
+                ok = false;
+                break;
+            }
+            const unsigned char *rb = raw + (size_t)rslot * L::RAW;
+            const int n = min(GT_GS, cur.ng - cur.g0);
+            if (cw < n) {
+                const uint32_t cs = cb0 + cw;
+                const int slot = cs % GT_CQ;
+                if (cs >= GT_CQ && !mbar_wait(&conv_empty[slot], ((cs / GT_CQ) - 1) & 1)) {
                     if (lane == 0)
                         fail();
                     ok = false;
-                    break;
                 }
-                const unsigned char *rb = raw + (size_t)rslot * L::RAW;
-                const int n = min(GT_GS, ng - g0);
-                for (int gi = 0; gi < n; ++gi, ++cs) {
-                    const int slot = cs % GT_CQ;
-                    if (cs >= GT_CQ && !mbar_wait(&conv_empty[slot], ((cs / GT_CQ) - 1) & 1)) {
-                        if (lane == 0)
-                            fail();
-                        ok = false;
-                        break;
-                    }
+                if (ok) {
                     unsigned char *cb = conv + (size_t)slot * L::CONV;
-                    const int blk = c >> 5, r = c & 31;
+                    const __nv_bfloat162 off136 = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
                     for (int m = 0; m < M; ++m) {
-                        // row c's 32 nibbles of this group -> 32 bf16 in four 16-byte chunks
-                        const uint4 w = *reinterpret_cast<const uint4 *>(rb + m * L::RAW_W + (blk * GT_GS + gi) * 512 + r * 16);
-                        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-                        const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint32_t p[4];
+                        for (int blk = 0; blk < 4; ++blk) {
+                            const int r = blk * 32 + lane;
+                            const uint4 w =
+                                *reinterpret_cast<const uint4 *>(rb + m * L::RAW_W + (blk * GT_GS + cw) * 512 + lane * 16);
+                            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                            for (int s = 0; s < 4; ++s) {
-                                const uint32_t u = ((wv[j] >> (4 * s)) & 0x000F000Fu) | 0x43004300u;
-                                const __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&u), off);
-                                p[s] = *reinterpret_cast<const uint32_t *>(&h);
+                            for (int j = 0; j < 4; ++j) {
+                                // bf16 pairs (q_k, q_k+4) for k = 8j + s, s = 0..3: the mask and
+                                // the magic exponent make 128 + nibble, minus 136 is q
+                                uint32_t o[4];
+#pragma unroll
+                                for (int s2 = 0; s2 < 4; ++s2) {
+                                    const uint32_t u = ((wv[j] >> (4 * s2)) & 0x000F000Fu) | 0x43004300u;
+                                    const __nv_bfloat162 h =
+                                        __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&u), off136);
+                                    o[s2] = *reinterpret_cast<const uint32_t *>(&h);
+                                }
+                                *reinterpret_cast<uint4 *>(cb + m * L::CA + umma_off(r, 8 * j, 32)) =
+                                    make_uint4(o[0], o[1], o[2], o[3]);
                             }
-                            *reinterpret_cast<uint4 *>(cb + m * L::CA + umma_off(c, 8 * j, 32)) =
-                                make_uint4(p[0], p[1], p[2], p[3]);
+                            reinterpret_cast<float *>(cb + M * L::CA + L::CB)[m * UMMA_M + r] =
+                                *reinterpret_cast<const float *>(rb + M * L::RAW_W + m * L::RAW_S +
+                                                                 (blk * GT_GS + cw) * 128 + lane * 4);
                         }
-                        // the row's weight scale of this group
-                        reinterpret_cast<float *>(cb + M * L::CA + L::CB)[m * UMMA_M + c] =
-                            *reinterpret_cast<const float *>(rb + M * L::RAW_W + m * L::RAW_S + (blk * GT_GS + gi) * 128 + r * 4);
                     }
-                    // the token tile: two 16-byte chunks of this thread's token, or zeros
-                    const int g = g0 + gi;
-                    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-                    if (arow >= 0) {
-                        const uint16_t *src = a.abf + arow * a.act_stride + (long)g * G + half * 16;
-                        v0 = ld_nc(src);
-                        v1 = ld_nc(src + 8);
-                        if (half == 0)
-                            reinterpret_cast<float *>(cb + M * L::CA + L::CB + M * UMMA_M * 4)[tn] =
-                                a.as[arow * a.act_groups + g];
-                    }
-                    if (tn < GT_N) {
-                        *reinterpret_cast<uint4 *>(cb + M * L::CA + umma_off(tn, half * 16, 32)) = v0;
-                        *reinterpret_cast<uint4 *>(cb + M * L::CA + umma_off(tn, half * 16 + 8, 32)) = v1;
+                    // the token tile (zeros past the tile's tokens) and the tokens' scales
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int tn = lane + 32 * h;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            *reinterpret_cast<uint4 *>(cb + M * L::CA + umma_off(tn, 8 * q, 32)) = vc[h][q];
+                        reinterpret_cast<float *>(cb + M * L::CA + L::CB + M * UMMA_M * 4)[tn] = sc[h];
                     }
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&conv_full[slot]);
                 }
-                if (!ok)
-                    break;
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&raw_empty[rslot]);
+            }
+            if (!ok)
+                break;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&raw_empty[rslot]);
+            ++rs;
+            cb0 += n;
+            cur = nxt;
+            have = more;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sc[h] = sn[h];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    vc[h][q] = vn[h][q];
             }
         }
     } else {
@@ -418,8 +485,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 for (int j = 0; j < 32; ++j)
                     acc[m][j] = 0.0f;
             for (int g = 0; g < ng; ++g, ++cs, ++gcount) {
-                const int slot = cs % GT_CQ, tb = gcount & 1;
-                if (!mbar_wait(&tm_full[tb], (gcount >> 1) & 1)) {
+                const int slot = cs % GT_CQ, tb = gcount % GT_TB;
+                if (!mbar_wait(&tm_full[tb], (gcount / GT_TB) & 1)) {
                     if (lane == 0)
                         fail();
                     ok = false;
@@ -434,17 +501,25 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 for (int m = 0; m < M; ++m) {
                     const float swm = sw[m * UMMA_M + row];
                     const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * 128 + m * 64 + chalf * 32;
+                    uint32_t dv[2][16];
+                    tmem_ld16_async(ta, dv[0]);
+                    tmem_ld16_async(ta + 16, dv[1]);
+                    tmem_wait_ld();
+                    const float2 sw2 = make_float2(swm, swm);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        float dv[16];
-                        tmem_ld16(ta + 16 * h, dv);
 #pragma unroll
                         for (int j = 0; j < 16; j += 4) {
                             const float4 v = *reinterpret_cast<const float4 *>(sa + 16 * h + j);
-                            acc[m][16 * h + j] = fmaf(dv[j], swm * v.x, acc[m][16 * h + j]);
-                            acc[m][16 * h + j + 1] = fmaf(dv[j + 1], swm * v.y, acc[m][16 * h + j + 1]);
-                            acc[m][16 * h + j + 2] = fmaf(dv[j + 2], swm * v.z, acc[m][16 * h + j + 2]);
-                            acc[m][16 * h + j + 3] = fmaf(dv[j + 3], swm * v.w, acc[m][16 * h + j + 3]);
+                            // acc += D * (s_w * s_a), two columns per packed instruction
+                            const float2 q0 = ffma2(sw2, make_float2(v.x, v.y), make_float2(0.f, 0.f));
+                            const float2 q1 = ffma2(sw2, make_float2(v.z, v.w), make_float2(0.f, 0.f));
+                            float *ac = &acc[m][16 * h + j];
+                            const float2 r0 = ffma2(make_float2(__uint_as_float(dv[h][j]), __uint_as_float(dv[h][j + 1])),
+                                                    q0, make_float2(ac[0], ac[1]));
+                            const float2 r1 = ffma2(make_float2(__uint_as_float(dv[h][j + 2]), __uint_as_float(dv[h][j + 3])),
+                                                    q1, make_float2(ac[2], ac[3]));
+                            ac[0] = r0.x, ac[1] = r0.y, ac[2] = r1.x, ac[3] = r1.y;
                         }
                     }
                 }
@@ -490,7 +565,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, 128 * GT_TB);
     }
 }
 

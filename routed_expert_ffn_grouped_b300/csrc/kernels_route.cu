@@ -115,6 +115,103 @@ __device__ bool route_logits_part(const RouterArgs &a, unsigned char *smem_raw, 
     return true;
 }
 
+// ---- router logits for many tokens: (16 tokens x 32 experts) tiles --------------------
+// The same fixed summation order as route_logits_part: lane j of a warp keeps chain j
+// (k = j, j+32, ... ascending, fmaf) for each of its (token, expert) pairs; a K-chunk of x
+// and of Wr is staged in shared memory for the whole CTA. Warp w owns experts 4w..4w+3
+// of the tile and all 16 tokens: 64 chains a lane. The chains of each pair are then
+// added in the halving-tree pairs (16, 8, 4, 2, 1) by a transpose reduction: each step
+// adds the same two partial sums as the tree, only in another lane, so the result is the
+// tree's bit for bit; lane l ends with pair l and pair 32 + l, and evaluates their
+// sigmoid scores (fp64) in parallel.
+constexpr int RT_T = 16, RT_E = 32, RT_KC = 256;
+
+template <int N>
+__device__ __forceinline__ float tree_reduce_lanes(float (&v)[N], int lane)
+{
+    int o = 16;
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            v[i] = keep + __shfl_xor_sync(FULL, send, o);
+        }
+        o >>= 1;
+    }
+    return v[0];
+}
+
+__global__ void __launch_bounds__(256, 2) k_route_logits_tiled(RouterArgs a)
+{
+    __shared__ __align__(16) float xs[RT_T][RT_KC];
+    __shared__ __align__(16) float ws[RT_E][RT_KC];
+    const int d = a.d, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
+    const int nt = min(RT_T, a.T - t0), ne = min(RT_E, a.E - e0);
+    float acc[RT_T * 4];  // [expert 4w+i][token t]: index i * 16 + t
+#pragma unroll
+    for (int i = 0; i < RT_T * 4; ++i)
+        acc[i] = 0.0f;
+    for (int k0 = 0; k0 < d; k0 += RT_KC) {
+        const int kc = min(RT_KC, d - k0);  // a multiple of 32
+        __syncthreads();
+        for (int i = threadIdx.x; i < RT_T * (kc / 4); i += blockDim.x) {
+            const int t = i / (kc / 4), c = (i % (kc / 4)) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < nt)
+                v = *reinterpret_cast<const float4 *>(a.x + (long)(t0 + t) * d + k0 + c);
+            *reinterpret_cast<float4 *>(&xs[t][c]) = v;
+        }
+        for (int i = threadIdx.x; i < RT_E * (kc / 4); i += blockDim.x) {
+            const int e = i / (kc / 4), c = (i % (kc / 4)) * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e < ne)
+                v = *reinterpret_cast<const float4 *>(a.Wr + (long)(e0 + e) * d + k0 + c);
+            *reinterpret_cast<float4 *>(&ws[e][c]) = v;
+        }
+        __syncthreads();
+        for (int k = lane; k < kc; k += 32) {
+            float xv[RT_T];
+#pragma unroll
+            for (int t = 0; t < RT_T; ++t)
+                xv[t] = xs[t][k];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float wv = ws[warp * 4 + i][k];
+#pragma unroll
+                for (int t = 0; t < RT_T; ++t)
+                    acc[i * RT_T + t] = fmaf(xv[t], wv, acc[i * RT_T + t]);
+            }
+        }
+    }
+    float lo[32], hi[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        lo[i] = acc[i];
+        hi[i] = acc[32 + i];
+    }
+    const float r0 = tree_reduce_lanes<32>(lo, lane);  // pair index lane
+    const float r1 = tree_reduce_lanes<32>(hi, lane);  // pair index 32 + lane
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int idx = h * 32 + lane;
+        const int t = idx % RT_T, e = warp * 4 + idx / RT_T;
+        if (t < nt && e < ne) {
+            const float l = h ? r1 : r0;
+            const long o = (long)(t0 + t) * a.E + e0 + e;
+            a.logits[o] = l;
+            if (a.s) {
+                const float sv = (float)(1.0 / (1.0 + exp(-(double)l)));
+                a.s[o] = sv;
+                a.c[o] = sv + (a.bias ? a.bias[e0 + e] : 0.0f);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(128) k_route_logits(RouterArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
