@@ -119,9 +119,10 @@ def _check(fn: str, status: int):
 
 
 def _ptr(t) -> int | None:
-    """Address of a torch tensor or numpy array (None stays None)."""
-    if t is None:
-        return None
+    """Address of a torch tensor or numpy array; an int is taken as a raw address (the
+    expert cache's device table); None stays None."""
+    if t is None or isinstance(t, int):
+        return t
     if isinstance(t, np.ndarray):
         return t.ctypes.data
     return t.data_ptr()
