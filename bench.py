@@ -43,6 +43,7 @@ WORKLOADS = {
     "olmoe_decode_t1": ("olmoe", 1, False),
     "olmoe_decode_t16": ("olmoe", 16, False),
     "glm52_prefill_t2048": ("glm52", 2048, True),
+    "glm52_stream_8l": ("glm52", 1, False),
 }
 DEFAULT_WORKLOAD = "glm52_decode_t1"
 N_X = 64                 # distinct activation batches cycled through
@@ -59,6 +60,9 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--predictor", default="previous", choices=["previous", "lookahead"],
+                   help="expert streaming: next-layer prefetch from an emulated router lookahead "
+                        "that names each true id with probability 0.716, or the previous step's ids")
     return p.parse_args()
 
 
@@ -267,6 +271,123 @@ def workload_config(spec, workload, T):
             "timing": "CUDA events per step around one CUDA-graph replay"}
 
 
+# ---------------------------------------------------------------- expert streaming
+STREAM_LAYERS = 8
+STREAM_SLOTS = 512
+LOOKAHEAD_ACCURACY = 0.716   # next-layer routing predictability stated by the pages
+
+
+def run_stream(args):
+    """Decode T=1 through a stack of GLM-5.2-shaped layers whose routed experts live in
+    pinned host memory (2048 blobs, ~48 GB) behind an HBM LRU cache of 512 slots
+    (~12 GB); routing keeps each id from the previous step with probability 0.7; before
+    each layer the next layer's experts are prefetched as predicted by the previous
+    step's ids. The shared experts stay resident. A step is one token through all
+    layers; the timed region includes the host's cache decisions."""
+    import ctypes
+    import torch
+    from routed_expert_ffn_grouped_b300 import build as cbuild
+    from routed_expert_ffn_grouped_b300 import colibri as C
+
+    world, rank, local = dist_setup(torch)
+    if rank == 0 or not os.path.exists(C.LIB_PATH):
+        cbuild.build()
+    barrier(torch, world)
+    spec, T, L_ = synth.GLM52, 1, STREAM_LAYERS
+    E = spec.n_exp
+    K, W = args.steps, args.warmup
+    nb = synth.blob_layout(spec.d, spec.ffn).nbytes
+    t_gen = time.perf_counter()
+    pinned = torch.empty((L_ * E, nb), dtype=torch.uint8, pin_memory=True)
+    pn = pinned.numpy()
+    # layer 0's experts are drawn; the other layers hold copies (content does not change
+    # what is streamed or timed)
+    for e in range(E):
+        synth.fill_expert_blob(pn[e], spec.d, spec.ffn, args.seed, 0, e)
+    for l in range(1, L_):
+        pn[l * E:(l + 1) * E] = pn[:E]
+    gen_s = time.perf_counter() - t_gen
+    shared_blob = torch.from_numpy(synth.expert_blob(spec, args.seed, 0, 0, shared=True))
+    shared_dev = [shared_blob.cuda() for _ in range(L_)]
+    sl = C.colibri_blob_layout_for(spec.d, spec.shared_ffn)
+    shared = [C.Expert(b.data_ptr() + sl.w1, b.data_ptr() + sl.w3, b.data_ptr() + sl.w2,
+                       b.data_ptr() + sl.s1, b.data_ptr() + sl.s3, b.data_ptr() + sl.s2) for b in shared_dev]
+    tables = (L_ * E * ctypes.sizeof(C.Expert) + 255) // 256 * 256
+    pool = torch.empty(tables + STREAM_SLOTS * nb, dtype=torch.uint8, device="cuda")
+    copy = torch.cuda.Stream()
+    stream = torch.cuda.Stream()
+    cache = C.ExpertCache(pool, pinned, L_, E, spec.d, spec.ffn, spec.top_k, copy)
+    ids_np, w_np = synth.streaming_ids(spec, args.seed, L_, W + K + 1)
+    # emulated router lookahead: each id of the next layer is named correctly with the
+    # pages' stated predictability (71.6%), else replaced by a popular-looking wrong id
+    prng = np.random.default_rng([args.seed, 99])
+    guess = ids_np.copy()
+    wrong = prng.random(ids_np.shape) >= LOOKAHEAD_ACCURACY
+    guess[wrong] = prng.integers(0, E, int(wrong.sum()))
+    ids = torch.from_numpy(ids_np).cuda()          # [steps][layer][k]
+    w = torch.from_numpy(w_np).cuda()
+    cfg = C.layer_cfg(spec)
+    xs = torch.from_numpy(np.stack([synth.activations(spec, args.seed, T, step=i) for i in range(16)])).cuda()
+    out = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
+    ws = torch.empty(C.colibri_moe_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+
+    def step(s):
+        for l in range(L_):
+            cache.lookup(l, ids_np[s, l], wait_on=stream)
+            nl, ns = (l + 1, s) if l + 1 < L_ else (0, s + 1)
+            if args.predictor == "lookahead":
+                cache.stage(nl, np.unique(guess[ns, nl]))   # next-layer prefetch, predicted
+            elif ns - 1 >= 0:
+                cache.stage(nl, ids_np[ns - 1, nl])         # the previous step's ids
+            C.colibri_moe_layer(cfg, xs[(s * L_ + l) % 16], None, None, cache.table(l), shared[l],
+                                ids[s, l].view(1, -1), w[s, l].view(1, -1), True, out, ws, stream=stream)
+
+    for s in range(W):
+        step(s)
+    stream.synchronize()
+    cache.sync(60000)
+    st0 = cache.stats()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(torch, world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch, local)
+    t0 = time.perf_counter()
+    with sampler:
+        ev0.record(stream)
+        for s in range(W, W + K):
+            step(s)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    ms = allreduce_max(torch, world, ev0.elapsed_time(ev1))
+    st1 = cache.stats()
+    d = {k: st1[k] - st0[k] for k in st1 if k != "n_slots"}
+    value = world * T * K / (ms / 1e3)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "i8xi4->i32, f32", "data": "synthetic",
+            "config": {"workload": args.workload, "layers": L_, "d": spec.d, "ffn": spec.ffn, "n_exp": E,
+                       "top_k": spec.top_k, "T": T, "host_blobs": L_ * E, "host_bytes": L_ * E * nb,
+                       "hbm_slots": STREAM_SLOTS, "reuse": 0.7,
+                       "prefetch": ("next layer's ids from an emulated lookahead, 71.6% correct"
+                                    if args.predictor == "lookahead" else "previous step's ids of the next layer"),
+                       "timing": "CUDA events around K steps on the compute stream; host cache decisions inside"},
+            "cache": {"hit_rate": d["hits"] / max(1, d["lookups"]), "lookups": d["lookups"],
+                      "misses": d["misses"], "prefetch_staged": d["prefetch_staged"],
+                      "prefetch_used": d["prefetch_used"],
+                      "prefetch_accuracy": d["prefetch_used"] / max(1, d["prefetch_staged"]),
+                      "bytes_staged": d["bytes_staged"],
+                      "pcie_gbs": d["bytes_staged"] / (ms / 1e3) / 1e9},
+            "wall_s": wall, "generate_s": gen_s,
+            "gpu_launches": None,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    cache.close()
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_colibri(args):
     import torch
@@ -442,6 +563,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "glm52_stream_8l":
+        run_stream(args)
     else:
         run_colibri(args)
 
