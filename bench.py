@@ -49,6 +49,7 @@ DEFAULT_WORKLOAD = "glm52_decode_t1"
 N_X = 64                 # distinct activation batches cycled through
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
 
 
 def parse():
@@ -76,11 +77,12 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
-def traffic_from_profiles(kernel_file: str, workload: str):
-    """dram bytes per launch recorded by ncu in profiles/, or None when the kernel source
-    changed since (the summary stores the sha256 of the source it measured)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_file}.md")
-    src = os.path.join(ROOT, "routed_expert_ffn_grouped_b300", "csrc", "kernels_gemv.cu")
+def traffic_from_profiles(summary: str, source: str, workload: str):
+    """dram bytes per launch recorded by ncu in profiles/<summary>.md for `workload`, or
+    None when there is none or the kernel source changed since (the summary stores the
+    sha256 of the source file it measured)."""
+    path = os.path.join(ROOT, "profiles", f"{summary}.md")
+    src = os.path.join(ROOT, "routed_expert_ffn_grouped_b300", "csrc", source)
     try:
         text = open(path).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
@@ -256,12 +258,21 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def launches_per_step(T: int, ids_given: bool) -> int:
-    """Kernels colibri_moe_layer launches per call: q8 (+ router logits), selection and
-    bucketing (one kernel for T <= 32), gate/up, down, combine."""
+DECODE_T_MAX = 32   # largest T on the decode (GEMV) path; larger T takes the tcgen05 GEMMs
+
+
+def launches_per_step(T: int, n_exp: int, ids_given: bool) -> int:
+    """Kernels one colibri_moe_layer call launches: routing, gate/up, down, combine.
+    Routing is one fused kernel for decode (T <= 32, T x E <= 8192); with the ids given
+    it is q8 + bucketing; otherwise router logits (q8 on the side for T <= 32, its own
+    kernel above), selection and bucketing."""
     if ids_given:
-        return 5
-    return 5 if T <= 32 else 6
+        routing = 2
+    elif T <= DECODE_T_MAX and T * n_exp <= 8192:
+        routing = 1
+    else:
+        routing = (1 if T <= DECODE_T_MAX else 2) + 2
+    return routing + 3
 
 
 def workload_config(spec, workload, T):
@@ -381,7 +392,8 @@ def run_stream(args):
                       "bytes_staged": d["bytes_staged"],
                       "pcie_gbs": d["bytes_staged"] / (ms / 1e3) / 1e9},
             "wall_s": wall, "generate_s": gen_s,
-            "gpu_launches": None,
+            # 5 per layer call (ids given) + one table-entry write per staged blob
+            "gpu_launches": K * L_ * launches_per_step(T, E, True) + d["misses"] + d["prefetch_staged"],
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -502,7 +514,19 @@ def run_colibri(args):
             prof_bytes.append(len(np.unique(ids.cpu().numpy())) * gu_b + sh[1])
     kern_ms = {k: float(np.mean(v)) for k, v in prof.items()}
     gu_gbs = float(np.mean(np.array(prof_bytes) / (np.array(prof["gateup"]) / 1e3)) / 1e9)
-    traffic = traffic_from_profiles("k_gateup", args.workload)
+    prefill = T > DECODE_T_MAX
+    gu_kernel = "k_gemm<0> (tcgen05 gate/up)" if prefill else "k_ring<0> (gate/up GEMV)"
+    traffic = traffic_from_profiles("k_ring_gateup_glm52_decode_t1", "kernels_decode.cu", args.workload)
+    roof_tensor = None
+    if prefill:
+        # the same kernel against the tensor peak: algorithmic MACs of gate/up, routed
+        # pairs and the shared expert, x 2 flops
+        flops = 2.0 * T * spec.d * 2 * (spec.top_k * spec.ffn + (spec.shared_ffn if spec.has_shared else 0))
+        tf = flops / (float(np.mean(prof["gateup"])) / 1e3) / 1e12
+        tpeak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+        roof_tensor = {"bound": "tensor", "kernel": gu_kernel, "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
+                       "frac": tf / tpeak, "algorithmic_flops_per_launch": flops,
+                       "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind})"}
 
     # end to end through the public API: pinned host x in, out back to pinned host, per step
     x_pin = torch.from_numpy(xs_host).pin_memory()
@@ -535,14 +559,16 @@ def run_colibri(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "i8xi4->i32, f32", "data": "synthetic",
+            "dtype": ("bf16xbf16->f32 (int4 and q8 codes, exact in bf16)" if prefill else "i8xi4->i32, f32"),
+            "data": "synthetic",
             "config": workload_config(spec, args.workload, T),
             "expert_hbm_gbs": layer_gbs, "expert_hbm_frac": layer_gbs / hbm_peak,
             "expert_bytes_per_step": float(np.mean(expert_bytes)),
-            "roofline": {"bound": "hbm", "kernel": "k_gateup", "achieved": gu_gbs, "peak": hbm_peak,
+            "roofline": {"bound": "hbm", "kernel": gu_kernel, "achieved": gu_gbs, "peak": hbm_peak,
                          "unit": "GB/s", "frac": gu_gbs / hbm_peak, "traffic": traffic,
                          "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
                          "algorithmic_bytes_per_launch": float(np.mean(prof_bytes))},
+            "roofline_tensor": roof_tensor,
             "kernel_ms": kern_ms,
             "no_l2_flush": {"value": world * T / (nf_ms / 1e3), "ms_per_step": nf_ms, "steps": KB,
                             "note": "informational; the headline value flushes L2 between steps"},
@@ -550,7 +576,7 @@ def run_colibri(args):
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * spec.d * 4,
                     "d2h_bytes_per_step": T * spec.d * 4, "steps": KE,
                     "path": "colibri_moe_layer via the Python binding, eager launches"},
-            "gpu_launches": launches_per_step(T, False) * K,
+            "gpu_launches": launches_per_step(T, spec.n_exp, False) * K,
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)
