@@ -7,8 +7,12 @@
 A step is one pass of the whole layer (q8, router, bucketing, gate/up, down, combine)
 over one batch of T synthetic tokens, with all experts resident in HBM. Each timed step
 is one CUDA-graph replay bracketed by CUDA events on the launching stream; between
-steps (outside the events) the next token's activations are copied in and a 256 MB
-buffer is written to flush the 126 MB L2. Prints one JSON line.
+steps (outside the events) the next token's activations are copied in, a 256 MB buffer
+is written to flush the 126 MB L2, a second 256 MB buffer is read (no dirty lines left to
+write back), and the layer before runs once: a layer of the same shape with its own
+weights at other addresses, as in a model where layers run back to back. So the timed
+step starts with none of its own data in L2 but with the kernels' code warm. Prints one
+JSON line.
 
 --impl reference times the CPU oracle (plain C, one core) on the same workload: each
 step is one expert pass of one token (the router and the shared expert ride with the
@@ -262,23 +266,25 @@ DECODE_T_MAX = 32   # largest T on the decode (GEMV) path; larger T takes the tc
 
 
 def launches_per_step(T: int, n_exp: int, ids_given: bool) -> int:
-    """Kernels one colibri_moe_layer call launches: routing, gate/up, down, combine.
-    Routing is one fused kernel for decode (T <= 32, T x E <= 8192); with the ids given
-    it is q8 + bucketing; otherwise router logits (q8 on the side for T <= 32, its own
-    kernel above), selection and bucketing."""
-    if ids_given:
-        routing = 2
-    elif T <= DECODE_T_MAX and T * n_exp <= 8192:
-        routing = 1
-    else:
-        routing = (1 if T <= DECODE_T_MAX else 2) + 2
-    return routing + 3
+    """Kernels one colibri_moe_layer call launches. Decode (T <= 32): routing, then one
+    kernel for gate/up, down and combine; routing is one fused kernel (T x E <= 8192),
+    q8 + bucketing with the ids given, else router logits + selection + bucketing.
+    Prefill: q8, router logits, selection, bucketing (the first three replaced by q8 when
+    the ids are given), the two tcgen05 GEMMs and the combine."""
+    if T <= DECODE_T_MAX:
+        if ids_given:
+            return 3
+        return 2 if T * n_exp <= 8192 else 4
+    return 5 if ids_given else 7
 
 
 def workload_config(spec, workload, T):
     return {"workload": workload, "d": spec.d, "ffn": spec.ffn, "n_exp": spec.n_exp, "top_k": spec.top_k,
             "shared_ffn": spec.shared_ffn if spec.has_shared else 0, "router": spec.router, "T": T,
-            "experts_resident": "all in HBM", "l2": "256 MB buffer written between timed steps",
+            "experts_resident": "all in HBM",
+            "l2": ("between timed steps a 256 MB buffer is written and another 256 MB buffer read, then "
+                   "one call of the layer before (same shape, its own weights at other addresses): "
+                   "code and small tables warm, none of this layer's weights, router or shared expert in L2"),
             "timing": "CUDA events per step around one CUDA-graph replay"}
 
 
@@ -392,7 +398,7 @@ def run_stream(args):
                       "bytes_staged": d["bytes_staged"],
                       "pcie_gbs": d["bytes_staged"] / (ms / 1e3) / 1e9},
             "wall_s": wall, "generate_s": gen_s,
-            # 5 per layer call (ids given) + one table-entry write per staged blob
+            # per layer call (ids given) + one table-entry write per staged blob
             "gpu_launches": K * L_ * launches_per_step(T, E, True) + d["misses"] + d["prefetch_staged"],
             "clocks": sampler.summary(),
         }
@@ -423,6 +429,14 @@ def run_colibri(args):
     w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
     ws = torch.empty(C.colibri_moe_workspace_bytes(dl.cfg, T), dtype=torch.uint8, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    scrub = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    # the layer before: same shape, its own weights (as in a model, where the previous
+    # layer's call leaves code and small tables warm but none of this layer's data)
+    prev = C.DeviceLayer.twin(dl, shift=spec.n_exp // 3)
+    x_prev = torch.from_numpy(synth.activations(spec, args.seed + 1, T, row_scale=row_scale)).cuda()
+    out_prev = torch.empty_like(out)
+    ids_prev, w_prev = torch.empty_like(ids), torch.empty_like(w)
+    ws_prev = torch.empty_like(ws)
     K, W = args.steps, args.warmup
     ids_log = torch.empty((W + K, T, spec.top_k), dtype=torch.int32, device="cuda")
 
@@ -437,9 +451,16 @@ def run_colibri(args):
         st = C.colibri_workspace_status(dl.cfg, T, ws, stream=stream)
         if st != C.OK:
             raise RuntimeError(f"layer reported device error {st}")
+    def layer_prev():
+        C.colibri_moe_layer(prev.cfg, x_prev, prev.Wr, prev.bias, prev.table, prev.shared, ids_prev, w_prev, False,
+                            out_prev, ws_prev, stream=torch.cuda.current_stream())
+
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         layer()
+    graph_prev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_prev, stream=stream):
+        layer_prev()
     C.colibri_moe_profile_enable(True)
     graph_prof = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_prof, stream=stream):
@@ -449,6 +470,8 @@ def run_colibri(args):
     def pre(i):
         x.copy_(xs[i % N_X])
         flush.fill_(float(i))
+        scrub.sum()
+        graph_prev.replay()
 
     # warm-up
     with torch.cuda.stream(stream):
@@ -504,6 +527,7 @@ def run_colibri(args):
     P = min(K, 400)
     prof = {k: [] for k in C.PROFILE_KERNELS}
     prof_bytes = []
+    prefill = T > DECODE_T_MAX
     with torch.cuda.stream(stream):
         for i in range(P):
             pre(W + i)
@@ -511,12 +535,21 @@ def run_colibri(args):
             ms = C.colibri_moe_profile_read()
             for k, v in ms.items():
                 prof[k].append(v)
-            prof_bytes.append(len(np.unique(ids.cpu().numpy())) * gu_b + sh[1])
+            u = len(np.unique(ids.cpu().numpy()))
+            # algorithmic bytes of the roofline kernel: gate/up weights for the prefill
+            # GEMM, all expert weights for the fused decode kernel
+            prof_bytes.append(u * gu_b + sh[1] if prefill else u * nb + sh[0])
     kern_ms = {k: float(np.mean(v)) for k, v in prof.items()}
-    gu_gbs = float(np.mean(np.array(prof_bytes) / (np.array(prof["gateup"]) / 1e3)) / 1e9)
-    prefill = T > DECODE_T_MAX
-    gu_kernel = "k_gemm<0> (tcgen05 gate/up)" if prefill else "k_ring<0> (gate/up GEMV)"
-    traffic = traffic_from_profiles("k_ring_gateup_glm52_decode_t1", "kernels_decode.cu", args.workload)
+    if prefill:
+        roof_ms = np.array(prof["gateup"])
+        gu_kernel = "k_gemm<0> (tcgen05 gate/up + SwiGLU + q8)"
+        traffic = None
+    else:
+        # one kernel runs gate/up, down and combine; its profiling marks are back to back
+        roof_ms = np.array(prof["gateup"]) + np.array(prof["down"]) + np.array(prof["combine"])
+        gu_kernel = "k_decode (gate/up + down + combine)"
+        traffic = traffic_from_profiles("k_decode_glm52_decode_t1", "kernels_decode.cu", args.workload)
+    gu_gbs = float(np.mean(np.array(prof_bytes) / (roof_ms / 1e3)) / 1e9)
     roof_tensor = None
     if prefill:
         # the same kernel against the tensor peak: algorithmic MACs of gate/up, routed
@@ -536,6 +569,8 @@ def run_colibri(args):
     with torch.cuda.stream(stream):
         for i in range(KE):
             flush.fill_(float(i))
+            scrub.sum()
+            graph_prev.replay()
             stream.synchronize()
             t0 = time.perf_counter()
             x.copy_(x_pin[i % N_X], non_blocking=True)

@@ -326,6 +326,31 @@ class DeviceLayer:
             sl = colibri_blob_layout_for(spec.d, spec.shared_ffn)
             self.shared = self._expert_at(self.shared_blob.data_ptr(), sl)
 
+    @classmethod
+    def twin(cls, other: "DeviceLayer", shift: int = 1) -> "DeviceLayer":
+        """Another layer of the same shape at other device addresses: the same expert blobs
+        and shared expert copied on the device, router rows and bias rolled by `shift`
+        experts (so the twin routes elsewhere). For runs that need a second layer without
+        generating one on the host."""
+        import torch
+        t = cls.__new__(cls)
+        t.spec, t.cfg, t.lay = other.spec, other.cfg, other.lay
+        t.blobs = other.blobs.clone()
+        t.Wr = torch.roll(other.Wr, shifts=shift, dims=0).contiguous()
+        t.bias = torch.roll(other.bias, shifts=shift, dims=0).contiguous() if other.bias is not None else None
+        base, nb = t.blobs.data_ptr(), t.lay.nbytes
+        table = (Expert * t.spec.n_exp)()
+        for e in range(t.spec.n_exp):
+            table[e] = cls._expert_at(base + e * nb, t.lay)
+        t.table = torch.frombuffer(bytearray(bytes(table)), dtype=torch.uint8).to(other.blobs.device)
+        t.shared = None
+        t.shared_blob = None
+        if t.spec.has_shared:
+            t.shared_blob = other.shared_blob.clone()
+            sl = colibri_blob_layout_for(t.spec.d, t.spec.shared_ffn)
+            t.shared = cls._expert_at(t.shared_blob.data_ptr(), sl)
+        return t
+
     @staticmethod
     def _expert_at(base: int, lay: BlobLayout) -> Expert:
         return Expert(base + lay.w1, base + lay.w3, base + lay.w2, base + lay.s1, base + lay.s3, base + lay.s2)

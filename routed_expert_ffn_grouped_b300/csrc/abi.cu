@@ -91,6 +91,9 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     };
     L.err = take(256);
     L.counters = take(sizeof(Counters));
+    L.nslots = nslots;
+    L.sync_bytes = 4 * (4 + nslots + d / G);
+    L.sync = take(L.sync_bytes);
     L.qx = take((size_t)T * d);
     L.qx_eo = take((size_t)T * d);
     L.sx = take(4 * (size_t)T * (d / G));
@@ -103,8 +106,9 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     L.slots = take(sizeof(Slot) * nslots);
     L.hq = take(PT * fmax);
     L.hq_eo = take(PT * fmax);
-    L.hs = take(4 * PT * (fmax / G));
-    L.hc = take(4 * PT * (fmax / G));
+    const size_t hgs = (size_t)decode_hgs((int)fmax);  // >= fmax / G
+    L.hs = take(4 * PT * hgs);
+    L.hc = take(4 * PT * hgs);
     L.y = take(4 * PT * d);
     const bool prefill = uses_gemm(c, T);
     L.xbf = take(prefill ? 2 * (size_t)T * d : 0);
@@ -340,9 +344,10 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     int *err = reinterpret_cast<int *>(ws + L.err);
     const int d = cfg->d, E = cfg->n_exp, K = cfg->top_k;
 
-    // the control words (error flag, routing counter) and the work counters start every
-    // call at zero: if routing fails, the expert kernels find no work
-    if (cudaMemsetAsync(ws + L.err, 0, L.counters + sizeof(Counters) - L.err, s) != cudaSuccess)
+    // the control words (error flag, routing counter), the work counters and the decode
+    // kernel's claim and completion counters start every call at zero: if routing fails,
+    // the expert kernels find no work
+    if (cudaMemsetAsync(ws + L.err, 0, L.sync + L.sync_bytes - L.err, s) != cudaSuccess)
         return COLIBRI_E_CUDA;
     if (prof_mark(0, s))
         return COLIBRI_E_CUDA;
@@ -361,39 +366,92 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     float *sv = reinterpret_cast<float *>(ws + L.s);
     float *cv = reinterpret_cast<float *>(ws + L.c);
     const SelectArgs sa = select_args(cfg, T, lg, sv, cv, bias, ids, w);
-    if (!ids_given && !prefill && T * E <= 8192) {
-        // a1-a4 for decode in one kernel: q8 of x, logits and scores in every CTA, then
-        // selection and bucketing in the last CTA to finish
-        static SmemLimits have;
-        const int xt = route_xt(d, T);
-        const size_t smem = route_decode_smem_bytes(T, K, E, d, xt);
-        if (!smem_attr((const void *)k_route_decode, smem, have))
-            return COLIBRI_E_CUDA;
-        RouterArgs ra{x, T, d, E, xt, Wr, cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : bias, lg,
-                      cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : sv,
-                      cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : cv, qa, err};
+    colibri_expert sh{};
+    if (cfg->has_shared)
+        sh = *shared;
+    if (!prefill) {
+        // decode: routing inputs (router logits and scores with q8 of x on the side, or q8
+        // of x alone for given ids), then one kernel that selects, buckets and runs a6-a9
+        const bool select = !ids_given && decode_selects_in_kernel(T, E);
         if (prof_mark(1, s))
             return COLIBRI_E_CUDA;
-        k_route_decode<<<E, 256, smem, s>>>(ra, sa, ba, err + 4);
-        if (cudaGetLastError() != cudaSuccess || prof_mark(2, s) || prof_mark(3, s) || prof_mark(4, s))
-            return COLIBRI_E_CUDA;
-    } else {
         if (ids_given) {
-            // a1: q8 of x (plain codes + even/odd codes + corrections)
             const long groups = (long)T * (d / G);
             k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
-            if (cudaGetLastError() != cudaSuccess || prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s))
+            if (cudaGetLastError() != cudaSuccess)
                 return COLIBRI_E_CUDA;
-        } else {
-            // a1-a3: router logits with sigmoid scores and q8 of x on the side, selection
-            if (prof_mark(1, s))
-                return COLIBRI_E_CUDA;
-            int rc = launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, qa, err, s);
-            if (rc || prof_mark(2, s))
-                return COLIBRI_E_CUDA;
-            if (launch_select(sa, s) || prof_mark(3, s))
-                return COLIBRI_E_CUDA;
+        } else if (launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, qa, err, s)) {
+            return COLIBRI_E_CUDA;
         }
+        if (prof_mark(2, s))
+            return COLIBRI_E_CUDA;
+        if (!ids_given && !select && launch_select(sa, s))  // many experts: selection kernel
+            return COLIBRI_E_CUDA;
+        if (prof_mark(3, s) || prof_mark(4, s))
+            return COLIBRI_E_CUDA;
+        DecodeArgs da{};
+        da.experts = experts;
+        da.shared = sh;
+        da.d = d;
+        da.ffn = cfg->ffn;
+        da.shared_ffn = cfg->shared_ffn;
+        da.T = T;
+        da.K = K;
+        da.has_shared = cfg->has_shared;
+        da.fmax = (int)L.fmax;
+        da.ids_given = !select;
+        da.E = E;
+        da.n_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->n_group;
+        da.topk_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->topk_group;
+        da.router = cfg->router;
+        da.norm_topk = cfg->norm_topk;
+        da.routed_scale = cfg->routed_scale;
+        da.logits = lg;
+        da.rs = sv;
+        da.rc = cv;
+        da.ids = ids;
+        da.w_in = w;
+        da.w_out = w;
+        da.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+        da.pairs = reinterpret_cast<int32_t *>(ws + L.pairs);
+        da.slots = reinterpret_cast<Slot *>(ws + L.slots);
+        da.counters = reinterpret_cast<Counters *>(ws + L.counters);
+        da.xq_eo = reinterpret_cast<const int8_t *>(ws + L.qx_eo);
+        da.xs = reinterpret_cast<const float *>(ws + L.sx);
+        da.xc = reinterpret_cast<const int *>(ws + L.xc);
+        da.hq = reinterpret_cast<int8_t *>(ws + L.hq);
+        da.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
+        da.hs = reinterpret_cast<float *>(ws + L.hs);
+        da.hc = reinterpret_cast<int *>(ws + L.hc);
+        da.y = reinterpret_cast<float *>(ws + L.y);
+        da.out = out;
+        int *sync = reinterpret_cast<int *>(ws + L.sync);
+        da.claim = sync;
+        da.done_gu = sync + 4;
+        da.done_rb = sync + 4 + L.nslots;
+        da.err = err;
+        da.max_slots = (int)L.nslots;
+        if (launch_decode(da, s) != cudaSuccess || prof_mark(5, s) || prof_mark(6, s) || prof_mark(7, s))
+            return COLIBRI_E_CUDA;
+        return COLIBRI_OK;
+    }
+    if (ids_given) {
+        // a1: q8 of x
+        const long groups = (long)T * (d / G);
+        k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
+        if (cudaGetLastError() != cudaSuccess || prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s))
+            return COLIBRI_E_CUDA;
+    } else {
+        // a1-a3: router logits with sigmoid scores, q8 of x, selection
+        if (prof_mark(1, s))
+            return COLIBRI_E_CUDA;
+        int rc = launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, qa, err, s);
+        if (rc || prof_mark(2, s))
+            return COLIBRI_E_CUDA;
+        if (launch_select(sa, s) || prof_mark(3, s))
+            return COLIBRI_E_CUDA;
+    }
+    {
         // a4: bucketing and slot list (counters, plus the ids when they fit in 160 KB)
         static SmemLimits have;
         const size_t bsm0 = bucket_smem_bytes(E, 1024), pbytes = (size_t)T * K * sizeof(int);
@@ -405,83 +463,38 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
         if (cudaGetLastError() != cudaSuccess || prof_mark(4, s))
             return COLIBRI_E_CUDA;
     }
-    // a6-a8: gate/up (+ SwiGLU + q8 h), then down, for every slot (shared expert first)
-    colibri_expert sh{};
-    if (cfg->has_shared)
-        sh = *shared;
-    const int routed_slots = T * K < E ? T * K : E;
-    if (prefill) {
-        // a10-a11: grouped GEMMs on the tensor cores
-        GemmArgs gm{};
-        gm.experts = experts;
-        gm.shared = sh;
-        gm.d = d;
-        gm.ffn = cfg->ffn;
-        gm.shared_ffn = cfg->shared_ffn;
-        gm.T = T;
-        gm.K = K;
-        gm.has_shared = cfg->has_shared;
-        gm.fmax = (int)L.fmax;
-        gm.slots = reinterpret_cast<const Slot *>(ws + L.slots);
-        gm.counters = reinterpret_cast<const Counters *>(ws + L.counters);
-        gm.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
-        gm.err = err;
-        GemmArgs gg = gm;
-        gg.abf = reinterpret_cast<const uint16_t *>(ws + L.xbf);
-        gg.as = reinterpret_cast<const float *>(ws + L.sx);
-        gg.act_stride = d;
-        gg.act_groups = d / G;
-        gg.hbf = reinterpret_cast<uint16_t *>(ws + L.hbf);
-        gg.hs = reinterpret_cast<float *>(ws + L.hs);
-        if (launch_gemm(MODE_GATEUP, gg, s) != cudaSuccess || prof_mark(5, s))
-            return COLIBRI_E_CUDA;
-        GemmArgs gd = gm;
-        gd.abf = reinterpret_cast<const uint16_t *>(ws + L.hbf);
-        gd.as = reinterpret_cast<const float *>(ws + L.hs);
-        gd.act_stride = (long)L.fmax;
-        gd.act_groups = (int)L.fmax / G;
-        gd.y = reinterpret_cast<float *>(ws + L.y);
-        if (launch_gemm(MODE_DOWN, gd, s) != cudaSuccess || prof_mark(6, s))
-            return COLIBRI_E_CUDA;
-    } else {
-        const int gu_items = (cfg->has_shared ? cfg->shared_ffn / G : 0) + routed_slots * (cfg->ffn / G);
-        DecodeArgs st{};
-        st.experts = experts;
-        st.shared = sh;
-        st.d = d;
-        st.ffn = cfg->ffn;
-        st.shared_ffn = cfg->shared_ffn;
-        st.T = T;
-        st.K = K;
-        st.has_shared = cfg->has_shared;
-        st.fmax = (int)L.fmax;
-        st.slots = reinterpret_cast<const Slot *>(ws + L.slots);
-        st.counters = reinterpret_cast<const Counters *>(ws + L.counters);
-        st.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
-        st.err = err;
-        DecodeArgs ga = st;
-        ga.aq_eo = reinterpret_cast<const int8_t *>(ws + L.qx_eo);
-        ga.as = reinterpret_cast<const float *>(ws + L.sx);
-        ga.ac = reinterpret_cast<const int *>(ws + L.xc);
-        ga.act_stride = d;
-        ga.act_groups = d / G;
-        ga.hq = reinterpret_cast<int8_t *>(ws + L.hq);
-        ga.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
-        ga.hs = reinterpret_cast<float *>(ws + L.hs);
-        ga.hc = reinterpret_cast<int *>(ws + L.hc);
-        if (launch_decode(MODE_GATEUP, ga, gu_items, s) != cudaSuccess || prof_mark(5, s))
-            return COLIBRI_E_CUDA;
-        const int dn_items = (routed_slots + (cfg->has_shared ? 1 : 0)) * down_blocks;
-        DecodeArgs da = st;
-        da.aq_eo = reinterpret_cast<const int8_t *>(ws + L.hq_eo);
-        da.as = reinterpret_cast<const float *>(ws + L.hs);
-        da.ac = reinterpret_cast<const int *>(ws + L.hc);
-        da.act_stride = (long)L.fmax;
-        da.act_groups = (int)L.fmax / G;
-        da.y = reinterpret_cast<float *>(ws + L.y);
-        if (launch_decode(MODE_DOWN, da, dn_items, s) != cudaSuccess || prof_mark(6, s))
-            return COLIBRI_E_CUDA;
-    }
+    // a10-a11: grouped GEMMs on the tensor cores
+    GemmArgs gm{};
+    gm.experts = experts;
+    gm.shared = sh;
+    gm.d = d;
+    gm.ffn = cfg->ffn;
+    gm.shared_ffn = cfg->shared_ffn;
+    gm.T = T;
+    gm.K = K;
+    gm.has_shared = cfg->has_shared;
+    gm.fmax = (int)L.fmax;
+    gm.slots = reinterpret_cast<const Slot *>(ws + L.slots);
+    gm.counters = reinterpret_cast<const Counters *>(ws + L.counters);
+    gm.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
+    gm.err = err;
+    GemmArgs gg = gm;
+    gg.abf = reinterpret_cast<const uint16_t *>(ws + L.xbf);
+    gg.as = reinterpret_cast<const float *>(ws + L.sx);
+    gg.act_stride = d;
+    gg.act_groups = d / G;
+    gg.hbf = reinterpret_cast<uint16_t *>(ws + L.hbf);
+    gg.hs = reinterpret_cast<float *>(ws + L.hs);
+    if (launch_gemm(MODE_GATEUP, gg, s) != cudaSuccess || prof_mark(5, s))
+        return COLIBRI_E_CUDA;
+    GemmArgs gd = gm;
+    gd.abf = reinterpret_cast<const uint16_t *>(ws + L.hbf);
+    gd.as = reinterpret_cast<const float *>(ws + L.hs);
+    gd.act_stride = (long)L.fmax;
+    gd.act_groups = (int)L.fmax / G;
+    gd.y = reinterpret_cast<float *>(ws + L.y);
+    if (launch_gemm(MODE_DOWN, gd, s) != cudaSuccess || prof_mark(6, s))
+        return COLIBRI_E_CUDA;
 
     // a9: combine
     CombineArgs ca{reinterpret_cast<const float *>(ws + L.y), w, T, K, d, cfg->has_shared, out};

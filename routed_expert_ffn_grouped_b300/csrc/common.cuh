@@ -178,30 +178,39 @@ __device__ __forceinline__ void named_sync(int id, int threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity), "r"(WAIT_HINT_NS)
+        : "memory");
+    return done != 0;
+}
+
+// The rest of a wait that did not end at the first try (one copy of this code for all
+// call sites): false after WAIT_LIMIT_NS.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t addr = smem_u32(bar);
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait(addr, parity))
+            return true;
+        if (global_ns() - t0 > WAIT_LIMIT_NS)
+            return false;
+    }
+}
+
 // Returns true once the phase with the given parity has completed, false after
 // WAIT_LIMIT_NS. Each try_wait suspends the thread (up to WAIT_HINT_NS) until the phase
 // completes.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
-    const uint32_t addr = smem_u32(bar);
-    uint64_t t0 = 0;
-    for (uint32_t i = 0;; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(addr), "r"(parity), "r"(WAIT_HINT_NS)
-            : "memory");
-        if (done)
-            return true;
-        const uint64_t now = global_ns();
-        if (i == 0)
-            t0 = now;
-        else if (now - t0 > WAIT_LIMIT_NS)
-            return false;
-    }
+    return mbar_try_wait(smem_u32(bar), parity) || mbar_wait_slow(bar, parity);
 }
 
 // Hint: bring [src, src + bytes) into L2 (no completion to wait for). src 16-byte
@@ -209,6 +218,63 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
 {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// L2 policy for bytes read once per call: evicted first, so they do not push out lines
+// that are still to be used (a prefetched shared expert, small tables).
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the kernel before it still runs; grid_dep_wait() blocks
+// the calling thread until that kernel has completed and its writes are visible.
+// grid_dep_launch() lets the dependent kernel be scheduled before this one ends.
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *p >= target (a counter other CTAs raise); false after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool wait_count_geq(const int *p, int target)
+{
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (ld_acquire_gpu(p) >= target)
+            return true;
+        const uint64_t now = global_ns();
+        if (i == 0)
+            t0 = now;
+        else if (now - t0 > WAIT_LIMIT_NS)
+            return false;
+        __nanosleep(64);
+    }
 }
 
 // Global -> shared bulk copy; dst, src 16-byte aligned, bytes a multiple of 16.
@@ -235,6 +301,8 @@ struct Counters {
     int n_items_gateup;
     int n_items_down;
     int n_routed;
+    int n_rows;  // rows of h and y: the pairs listed in slots + the shared expert's T
+    int pad[3];
 };
 
 }  // namespace clb

@@ -57,27 +57,47 @@ struct DecodeArgs {
     const colibri_expert *experts;
     colibri_expert shared;
     int d, ffn, shared_ffn, T, K, has_shared, fmax;
-    const Slot *slots;
-    const Counters *counters;
-    const int32_t *pairs;
-    // activation codes in even/odd order, their scales and +8 corrections: x for gate/up
-    // (row = token), q8(h) for down (row = pair)
-    const int8_t *aq_eo;
-    const float *as;
-    const int *ac;
-    long act_stride;   // bytes between activation rows of aq_eo
-    int act_groups;    // groups between activation rows of as / ac
-    int8_t *hq, *hq_eo;  // gate/up outputs
+    // routing, done by every CTA: selection from the router scores (sigmoid: s, c;
+    // softmax: logits; [T][E]) unless ids_given, then bucketing
+    int ids_given, E, n_group, topk_group, router, norm_topk;
+    float routed_scale;
+    const float *logits, *rs, *rc;
+    int32_t *ids;       // [T][K]: given, or the selection (written by CTA 0)
+    const float *w_in;  // [T][K] given weights
+    float *w_out;       // [T][K] selected weights (CTA 0)
+    // bucketing results, written to the workspace by CTA 0
+    int32_t *offsets, *pairs;
+    Slot *slots;
+    Counters *counters;
+    // q8 of x in even/odd order, its scales and +8 corrections (row = token)
+    const int8_t *xq_eo;
+    const float *xs;
+    const int *xc;
+    // q8(h) (row = pair; the shared expert's rows follow the T*K routed pairs; scales and
+    // corrections hgs to a row), written by the gate/up items and read by the down items
+    int8_t *hq, *hq_eo;
     float *hs;
     int *hc;
-    float *y;          // down output [pairs_total][d]
+    float *y;    // down outputs [pairs][d]
+    float *out;  // layer output [T][d]
+    // zeroed per call: the work-claim counter, finished rows of h per slot, finished rows
+    // of y per row block of d
+    int *claim, *done_gu, *done_rb;
     int *err;
-    // set by launch_decode: K of the widest matrix, groups per ring stage, stage bytes,
-    // ring stages, tokens per chunk
-    int kmax, sg, stage_bytes, ring, tch;
+    int max_slots;  // the shared expert + min(E, T*K) routed slots
+    // set by launch_decode: ring stages, h buffers, tokens per chunk, groups per h row
+    int ring, nh, tch, hgs;
 };
 
-cudaError_t launch_decode(int mode, DecodeArgs a, int max_items, cudaStream_t s);
+// One persistent launch for a decode step's routing (selection unless ids_given, and
+// bucketing) and experts (gate/up, down, combine), started as a programmatic dependent of
+// the kernel before it.
+cudaError_t launch_decode(DecodeArgs a, cudaStream_t s);
+// Scales (and corrections) a row of q8(h) holds on the decode path: fmax/32 rounded up to
+// 16 bytes.
+int decode_hgs(int fmax);
+// Whether the decode kernel selects the experts itself (else a selection kernel does).
+bool decode_selects_in_kernel(int T, int E);
 
 // Prefill grouped GEMMs on tcgen05 (kernels_gemm.cu).
 struct GemmArgs {
@@ -116,8 +136,6 @@ struct CombineArgs {
 __global__ void k_q8(Q8Args a);
 __global__ void k_route_logits(RouterArgs a);
 __global__ void k_route_logits_tiled(RouterArgs a);
-__global__ void k_route_decode(RouterArgs ra, SelectArgs sa, BucketArgs ba, int *done);
-size_t route_decode_smem_bytes(int T, int K, int E, int d, int xt);
 size_t bucket_smem_bytes(int E, int nthreads);
 __global__ void k_router_select(SelectArgs a);
 __global__ void k_bucket(BucketArgs a);

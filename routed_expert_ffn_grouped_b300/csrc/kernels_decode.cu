@@ -1,309 +1,1130 @@
-// Decode GEMVs: fused gate/up + SwiGLU + q8(h), and down.
+// Decode (T <= 32 tokens): the experts of a layer in one persistent kernel. Each CTA
+// routes (expert selection from the router scores, or the given ids, and bucketing into
+// slots) in shared memory, then runs fused gate/up + SwiGLU + q8(h), down, and the
+// weighted combine with the shared expert.
 //
 // Expert matrices are stored in row blocks of 32 rows, group-major inside a block: the 16
 // bytes of one 32-column group of the block's 32 rows lie together (512 bytes), and the
-// whole block is one contiguous run. A work item is one row block of one expert slot (32
-// rows of W1 and W3 for gate/up: one group of h; 32 rows of W2 for down).
+// whole block is one contiguous run. A work item is one row block of one expert slot: 32
+// rows of W1 and W3 for gate/up (one 32-group of h), or 32 rows of W2 for down.
 //
-// One persistent CTA per SM takes a contiguous range of items. Its producer warp streams
-// each item's run through a ring of NS shared-memory stages with 1-D bulk copies (a stage
-// is SG group tiles of every matrix plus their scales, a few large copies), completion
-// counted on a "full" mbarrier per stage. So the bytes in flight per SM are set by the
-// ring (well over 100 KB), not by registers. The consumer warps split each stage's
-// groups; lane l owns row l of the block and reads its 16 bytes of a group tile from
-// shared memory (512 contiguous bytes per warp, no bank conflicts), so a lane accumulates
-// whole row dots over its groups in registers without any cross-lane reduction. At the
-// end of an item the consumers' partial sums meet in shared memory in a fixed order.
+// Items are claimed from a device counter, in the order: the shared expert's gate/up
+// items, the routed slots' gate/up items, then the down items slot by slot. A CTA
+// processes its items in claim order, so no down item precedes a gate/up item in any CTA
+// and every wait below ends (a down item waits for the gate/up items of its slot, all of
+// which were claimed earlier by running CTAs).
 //
-// The activation codes (even/odd word order, with scales and +8 corrections) of the
-// item's tokens are staged in shared memory when the slot (or token chunk) changes and
-// read as broadcasts. A slot with more tokens than a chunk holds is processed chunk by
-// chunk, its weights streamed once per chunk.
+// One CTA per SM, three roles. The producer warp claims items (two ahead, so a claim's
+// latency hides behind the copies of the items before) and streams each item through a
+// ring of shared-memory stages with 1-D bulk copies (a stage holds 32 group tiles of W1
+// and W3 or 64 of W2, with their scales: 40 KB), tagging each stage with the item and its
+// position; completion is counted on a "full" mbarrier per stage. For a down item it
+// also copies the item's rows of q8(h) into one of a few h buffers, once the gate/up
+// items of its slot are done, ahead of the consumers. The consumer warps split each
+// stage's groups; lane l owns row l of the block and reads its 16 bytes of a group tile
+// from shared memory, so a lane accumulates whole row dots over its groups in registers.
+// At the end of a chunk the consumers leave their partial sums in one of several buffers
+// and go on; an epilogue warp per buffer adds them in a fixed order, writes h (SwiGLU +
+// q8) or y, and publishes the result with a device-scope fence and a counter: rows of h
+// finished per slot, rows of y finished per row block of d. The epilogue warp that
+// completes a row block of d adds the slots' outputs for it in slot order:
+// out = y_shared + sum_i w_i * y_i.
+//
+// The kernel is launched as a programmatic dependent of the routing kernel before it
+// (router logits and scores, q8 of x): before waiting for that kernel, each CTA sends its
+// share of the shared expert's weights towards L2 and the producer streams the shared
+// expert's gate/up items, which need no routing.
 #include "kernels.cuh"
 
 namespace clb {
 
 namespace {
 
+constexpr int NC = 16;                       // consumer warps
+constexpr int NT = NC * 32;                  // consumer threads
+constexpr int GPW_GU = 2, GPW_DN = 4;        // groups per consumer warp and stage
+constexpr int SG_GU = NC * GPW_GU;           // group tiles per matrix and stage, gate/up
+constexpr int SG_DN = NC * GPW_DN;           // ... down
+constexpr int STAGE_BYTES = 2 * SG_GU * 640; // 2 matrices x 32 groups x (512 + 128) bytes
+static_assert(STAGE_BYTES == SG_DN * 640, "gate/up and down stages have one size");
+constexpr int MAX_RING = 16;
+constexpr size_t SMEM_BUDGET = 227 * 1024;  // the largest opt-in dynamic shared memory of a CTA
+constexpr int NE_MAX = 4;                    // epilogue warps launched
+constexpr int NH_MAX = 3;                    // h buffers at most
+constexpr int TAG_NEW_H = 1 << 20;           // stage tag: this chunk starts a new h buffer
+
+// Partial-sum buffers (and epilogue warps, one per buffer) by tokens per chunk.
+__host__ __device__ constexpr int nbuf_for(int tch)
+{
+    return tch <= 2 ? 4 : 2;
+}
+
+__host__ __device__ constexpr int round_up(int v, int m)
+{
+    return (v + m - 1) / m * m;
+}
+
 struct DecItem {
     colibri_expert ex;
-    int slot, is_shared, rb, begin, count, kdim;
+    int mode, slot, is_shared, rb, begin, count, kdim;
 };
 
-template <int MODE>
-__device__ __forceinline__ DecItem item_info(const DecodeArgs &a, int item)
+// One slot as the kernel keeps it in shared memory: its expert's matrices and its run of
+// the pair list.
+struct SlotInfo {
+    colibri_expert ex;
+    int begin, count, pad[2];
+};
+
+// What an epilogue warp needs about a finished chunk.
+struct ChunkDesc {
+    int mode, slot, rb, nt, pad[4];
+    int orow[8];
+};
+
+// Shared memory beside the ring: see ring_layout().
+struct RingLayout {
+    size_t full, empty, hfull, hempty, cbar, tbar, pfull, pempty, tag, flags, ctab, desc, stab, ptab, wtab, act,
+        hbuf, part, total;
+    size_t hb;  // bytes of one h buffer
+};
+
+// Bytes of the routing scratch (selection and bucketing), laid over the x staging area.
+__host__ __device__ __forceinline__ size_t route_scratch_bytes(int T, int E, int K, bool select)
+{
+    const size_t P = (size_t)T * K;
+    size_t b = 8 * P + 16;  // picked ids, first-occurrence flags (+ alignment)
+    if (select)
+        b += (size_t)T * ((E + 3) & ~3) * 4 + (size_t)T * 32 * 16;
+    return b;
+}
+
+// ring [ns][STAGE_BYTES] | full [ns] | empty [ns] | hfull [NH_MAX] | hempty [NH_MAX] |
+// consumer barrier | table barrier | pfull [NE_MAX] | pempty [NE_MAX] | stage tags [ns]
+// (int2) | flags (16 B) | counters | chunk descriptors [NE_MAX] | slot table [max_slots]
+// | pair list [T*K] | weights [T*K] | x staging area (codes [TCH][d] | scales [TCH][d/32]
+// | corrections [TCH][d/32]; routing scratch before the first gate/up item) | h buffers
+// [nh] (codes [TCH][fmax] | scales [TCH][hgs] | corrections [TCH][hgs]) | partial sums
+// [NBUF][NC][2][TCH][32].
+__host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, int ns, int nh, int tch)
+{
+    RingLayout L;
+    const int P = a.T * a.K;
+    size_t o = (size_t)ns * STAGE_BYTES;
+    auto take = [&](size_t bytes, size_t align) {
+        o = (o + align - 1) / align * align;
+        const size_t at = o;
+        o += bytes;
+        return at;
+    };
+    L.full = take(8 * (size_t)ns, 8);
+    L.empty = take(8 * (size_t)ns, 8);
+    L.hfull = take(8 * NH_MAX, 8);
+    L.hempty = take(8 * NH_MAX, 8);
+    L.cbar = take(8, 8);
+    L.tbar = take(8, 8);
+    L.pfull = take(8 * NE_MAX, 8);
+    L.pempty = take(8 * NE_MAX, 8);
+    L.tag = take(8 * (size_t)ns, 8);
+    L.flags = take(16, 16);
+    L.ctab = take(sizeof(Counters), 16);
+    L.desc = take(sizeof(ChunkDesc) * NE_MAX, 16);
+    L.stab = take(sizeof(SlotInfo) * (size_t)a.max_slots, 16);
+    L.ptab = take(4 * (size_t)P, 16);
+    L.wtab = take(4 * (size_t)P, 16);
+    const size_t xbytes = (size_t)tch * a.d + 8 * (size_t)tch * (a.d / G);
+    const size_t rbytes = route_scratch_bytes(a.T, a.E, a.K, !a.ids_given);
+    L.act = take(xbytes > rbytes ? xbytes : rbytes, 16);
+    L.hb = round_up(tch * a.fmax + 8 * tch * a.hgs, 16);
+    L.hbuf = take(L.hb * nh, 16);
+    L.part = take(4 * (size_t)nbuf_for(tch) * NC * 2 * tch * 32, 16);
+    L.total = o;
+    return L;
+}
+
+struct RingSmem {
+    unsigned char *ring;
+    uint64_t *full, *empty, *hfull, *hempty, *cbar, *tbar, *pfull, *pempty;
+    int2 *tag;
+    int *flags;  // [0] abort, [1] valid pairs, [2] distinct experts
+    Counters *ctab;
+    ChunkDesc *desc;
+    SlotInfo *stab;
+    int *ptab;
+    float *wtab;
+    unsigned char *act, *hbuf;
+    size_t hb;
+    float *part;
+};
+
+__device__ __forceinline__ RingSmem carve(unsigned char *sm, const DecodeArgs &a, int tch)
+{
+    const RingLayout L = ring_layout(a, a.ring, a.nh, tch);
+    RingSmem s;
+    s.ring = sm;
+    s.full = reinterpret_cast<uint64_t *>(sm + L.full);
+    s.empty = reinterpret_cast<uint64_t *>(sm + L.empty);
+    s.hfull = reinterpret_cast<uint64_t *>(sm + L.hfull);
+    s.hempty = reinterpret_cast<uint64_t *>(sm + L.hempty);
+    s.cbar = reinterpret_cast<uint64_t *>(sm + L.cbar);
+    s.tbar = reinterpret_cast<uint64_t *>(sm + L.tbar);
+    s.pfull = reinterpret_cast<uint64_t *>(sm + L.pfull);
+    s.pempty = reinterpret_cast<uint64_t *>(sm + L.pempty);
+    s.tag = reinterpret_cast<int2 *>(sm + L.tag);
+    s.flags = reinterpret_cast<int *>(sm + L.flags);
+    s.ctab = reinterpret_cast<Counters *>(sm + L.ctab);
+    s.desc = reinterpret_cast<ChunkDesc *>(sm + L.desc);
+    s.stab = reinterpret_cast<SlotInfo *>(sm + L.stab);
+    s.ptab = reinterpret_cast<int *>(sm + L.ptab);
+    s.wtab = reinterpret_cast<float *>(sm + L.wtab);
+    s.act = sm + L.act;
+    s.hbuf = sm + L.hbuf;
+    s.hb = L.hb;
+    s.part = reinterpret_cast<float *>(sm + L.part);
+    return s;
+}
+
+__device__ __forceinline__ void set_abort(const DecodeArgs &a, const RingSmem &s)
+{
+    atomicOr(a.err, ERR_WAIT_TIMEOUT);
+    *reinterpret_cast<volatile int *>(s.flags) = 1;
+}
+
+__device__ __forceinline__ bool aborted(const RingSmem &s)
+{
+    return *reinterpret_cast<volatile int *>(s.flags) != 0;
+}
+
+// Barrier of the consumer warps on an mbarrier (count NC): bounded, unlike bar.sync, so a
+// warp that gave up on a wait cannot strand the others.
+__device__ __noinline__ bool consumers_sync(const RingSmem &s, uint32_t &phase, int lane)
+{
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(s.cbar);
+    const bool ok = mbar_wait(s.cbar, phase);
+    phase ^= 1u;
+    return ok;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Work item idx of the claim order, given n_gu gate/up items. The shared expert's items
+// (slot 0) need nothing written by routing; the routed slots come from the table.
+__device__ __forceinline__ DecItem work_item(const DecodeArgs &a, const SlotInfo *stab, int n_gu, int idx)
 {
     DecItem it;
-    if (MODE == MODE_GATEUP) {
-        const int sh_items = a.has_shared ? a.shared_ffn / G : 0;
-        if (item < sh_items) {
+    const int sh_items = a.has_shared ? a.shared_ffn / G : 0;
+    if (idx < n_gu) {
+        it.mode = MODE_GATEUP;
+        if (idx < sh_items) {
             it.slot = 0;
-            it.rb = item;
+            it.rb = idx;
         } else {
-            const int r = item - sh_items, nrb = a.ffn / G;
+            const int r = idx - sh_items, nrb = a.ffn / G;
             it.slot = (a.has_shared ? 1 : 0) + r / nrb;
             it.rb = r % nrb;
         }
     } else {
-        const int nmb = a.d / G;
-        it.slot = item / nmb;
-        it.rb = item % nmb;
+        const int r = idx - n_gu, nmb = a.d / G;
+        it.mode = MODE_DOWN;
+        it.slot = r / nmb;
+        it.rb = r % nmb;
     }
-    const Slot sd = a.slots[it.slot];
-    it.is_shared = sd.expert < 0;
-    it.ex = it.is_shared ? a.shared : a.experts[sd.expert];
-    it.begin = sd.begin;
-    it.count = sd.count;
-    it.kdim = MODE == MODE_GATEUP ? a.d : (it.is_shared ? a.shared_ffn : a.ffn);
+    if (a.has_shared && it.slot == 0) {
+        it.is_shared = 1;
+        it.ex = a.shared;
+        it.begin = 0;
+        it.count = a.T;
+    } else {
+        const SlotInfo &si = stab[it.slot];
+        it.is_shared = 0;
+        it.ex = si.ex;
+        it.begin = si.begin;
+        it.count = si.count;
+    }
+    it.kdim = it.mode == MODE_GATEUP ? a.d : (it.is_shared ? a.shared_ffn : a.ffn);
     return it;
 }
 
-// Dynamic shared memory: ring [NS][stage] | full [NS] | empty [NS] | abort flag (16 B) |
-// activation codes [TCH][Kmax] | scales [TCH][Kmax/32] | corrections [TCH][Kmax/32] |
-// partial sums [2][NC][M][TCH][32] | activation rows [TCH] | output rows [TCH].
-struct RingSmem {
-    unsigned char *ring;
-    uint64_t *full, *empty;
-    int *abort_flag;
-    int8_t *codes;
-    float *sc;
-    int *corr;
-    float *part;
-    int *arow, *orow;
-};
-
-__device__ __forceinline__ RingSmem carve(unsigned char *sm, const DecodeArgs &a, int nc, int m, int tch)
+// Pair row of token c of an item's slot (the shared expert's rows follow the T*K pairs).
+__device__ __forceinline__ int item_row(const DecodeArgs &a, const RingSmem &s, const DecItem &it, int c)
 {
-    RingSmem s;
-    const int ngm = a.kmax / G;
-    s.ring = sm;
-    s.full = reinterpret_cast<uint64_t *>(sm + (size_t)a.ring * a.stage_bytes);
-    s.empty = s.full + a.ring;
-    s.abort_flag = reinterpret_cast<int *>(s.empty + a.ring);
-    s.codes = reinterpret_cast<int8_t *>(s.abort_flag + 4);
-    s.sc = reinterpret_cast<float *>(s.codes + (size_t)tch * a.kmax);
-    s.corr = reinterpret_cast<int *>(s.sc + (size_t)tch * ngm);
-    s.part = reinterpret_cast<float *>(s.corr + (size_t)tch * ngm);
-    s.arow = reinterpret_cast<int *>(s.part + (size_t)2 * nc * m * tch * 32);
-    s.orow = s.arow + tch;
-    return s;
+    return it.is_shared ? a.T * a.K + c : s.ptab[it.begin + c];
+}
+
+// This CTA's share of the shared expert's six parts, sent towards L2.
+__device__ void prefetch_shared(const DecodeArgs &a)
+{
+    const size_t nib1 = (size_t)a.shared_ffn * a.d / 2, sc1 = 4 * (size_t)a.shared_ffn * (a.d / G);
+    const size_t nib2 = (size_t)a.d * a.shared_ffn / 2, sc2 = 4 * (size_t)a.d * (a.shared_ffn / G);
+    const void *part[6] = {a.shared.w1, a.shared.w3, a.shared.s1, a.shared.s3, a.shared.w2, a.shared.s2};
+    const size_t bytes[6] = {nib1, nib1, sc1, sc1, nib2, sc2};
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+        const size_t share = ((bytes[i] + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
+        const size_t b0 = share * blockIdx.x;
+        if (b0 >= bytes[i])
+            continue;
+        const size_t n = min(share, bytes[i] - b0);
+        prefetch_l2(static_cast<const char *>(part[i]) + b0, (uint32_t)n);
+    }
+}
+
+// (value, index) order of the selection: larger value first, then lower index.
+__device__ __forceinline__ bool beats(float v, int i, float bv, int bi)
+{
+    return v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ void top2_merge(float &m1, float &m2, float o1, float o2)
+{
+    // the two largest of the multiset {m1, m2, o1, o2}, given m1 >= m2 and o1 >= o2
+    if (o1 > m1) {
+        m2 = fmaxf(m1, o2);
+        m1 = o1;
+    } else {
+        m2 = fmaxf(m2, o1);
+    }
+}
+
+// Expert selection for the T tokens by the consumer warps, in shared memory (every CTA
+// the same way). The k-th pick of the sequential selection (repeatedly take the best
+// remaining candidate) is the candidate that exactly k others beat, so each candidate
+// counts the allowed candidates that beat it and, if that rank is below top_k, takes
+// position rank; groups are kept the same way. Sigmoid mode: group score = sum of the
+// group's two largest biased scores c, top topk_group groups, top_k by c inside them,
+// w = s / sum(s) * routed_scale with a compensated fp32 sum in selection order. Softmax
+// mode: top_k by logit, w = softmax over all experts in fp64. Writes the ids and weights
+// to sids and s.wtab; CTA 0 also to the caller's ids and w.
+__device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, int *sids, uint32_t &cph, int tid,
+                           int warp, int lane)
+{
+    const int E = a.E, K = a.K, T = a.T;
+    const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
+    const int NG = sig ? a.n_group : 1, gs = E / NG;
+    const int Ep = (E + 3) & ~3;
+    float *cs = scr;
+    float *gsc = cs + (size_t)T * Ep;
+    int *kept = reinterpret_cast<int *>(gsc + (size_t)T * 32);
+    int *pick = kept + (size_t)T * 32;
+    float *ps = reinterpret_cast<float *>(pick + (size_t)T * 32);
+    for (int i = tid; i < T * E; i += NT) {
+        const int t = i / E, e = i - t * E;
+        cs[t * Ep + e] = sig ? __ldcg(a.rc + i) : __ldcg(a.logits + i);
+    }
+    if (!consumers_sync(s, cph, lane))
+        return false;
+    if (sig) {
+        for (int i = warp; i < T * NG; i += NC) {
+            const int t = i / NG, g = i - t * NG;
+            const float *row = cs + (size_t)t * Ep + g * gs;
+            float m1 = -INFINITY, m2 = -INFINITY;
+            for (int j = lane; j < gs; j += 32)
+                top2_merge(m1, m2, row[j], -INFINITY);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float o1 = __shfl_xor_sync(FULL, m1, o), o2 = __shfl_xor_sync(FULL, m2, o);
+                top2_merge(m1, m2, o1, o2);
+            }
+            if (lane == 0)
+                gsc[t * 32 + g] = gs == 1 ? m1 : m1 + m2;
+        }
+        if (!consumers_sync(s, cph, lane))
+            return false;
+        for (int i = tid; i < T * NG; i += NT) {
+            const int t = i / NG, g = i - t * NG;
+            const float v = gsc[t * 32 + g];
+            int rank = 0;
+            for (int h = 0; h < NG; ++h)
+                rank += beats(gsc[t * 32 + h], h, v, g);
+            kept[t * 32 + g] = rank < a.topk_group;
+        }
+        if (!consumers_sync(s, cph, lane))
+            return false;
+    }
+    const bool vec = (gs & 3) == 0;
+    for (int i = tid; i < T * E; i += NT) {
+        const int t = i / E, e = i - t * E;
+        if (sig && !kept[t * 32 + e / gs])
+            continue;
+        const float *row = cs + (size_t)t * Ep;
+        const float v = row[e];
+        int rank = 0;
+        for (int g = 0; g < NG; ++g) {
+            if (sig && !kept[t * 32 + g])
+                continue;
+            if (vec) {
+                // four independent counts over float4 reads (rows start 16-byte aligned)
+                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+                const float4 *q4 = reinterpret_cast<const float4 *>(row);
+#pragma unroll 4
+                for (int j = g * gs; j < (g + 1) * gs; j += 4) {
+                    const float4 x = q4[j >> 2];
+                    r0 += beats(x.x, j, v, e);
+                    r1 += beats(x.y, j + 1, v, e);
+                    r2 += beats(x.z, j + 2, v, e);
+                    r3 += beats(x.w, j + 3, v, e);
+                }
+                rank += r0 + r1 + r2 + r3;
+            } else {
+                for (int j = g * gs; j < (g + 1) * gs; ++j)
+                    rank += beats(row[j], j, v, e);
+            }
+        }
+        if (rank < K) {
+            pick[t * 32 + rank] = e;
+            ps[t * 32 + rank] = sig ? __ldcg(a.rs + i) : v;
+        }
+    }
+    if (!consumers_sync(s, cph, lane))
+        return false;
+    // weights: one warp per token; with at most 32 pairs warp 0 takes every token, and
+    // the bucketing that follows stays in that warp
+    const bool one_warp = T * K <= 32;
+    for (int t = one_warp ? (warp == 0 ? 0 : T) : warp; t < T; t += one_warp ? 1 : NC) {
+        double m = 0.0, z = 1.0;
+        if (!sig) {
+            const float *l = cs + (size_t)t * Ep;
+            m = -INFINITY;
+            for (int i = lane; i < E; i += 32)
+                m = fmax(m, (double)l[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                m = fmax(m, __shfl_xor_sync(FULL, m, o));
+            z = 0.0;
+            for (int i = lane; i < E; i += 32)
+                z += exp((double)l[i] - m);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                z += __shfl_xor_sync(FULL, z, o);
+        }
+        float wt = 0.0f;
+        if (sig) {
+            // compensated (TwoSum) sum of the k scores in selection order, one division
+            const float sv = lane < K ? ps[t * 32 + lane] : 0.0f;
+            float hi = 0.0f, lo = 0.0f;
+            for (int i = 0; i < K; ++i) {
+                const float x = __shfl_sync(FULL, sv, i);
+                const float u = hi + x, bb = u - hi;
+                lo += (hi - (u - bb)) + (x - bb);
+                hi = u;
+            }
+            const float sum = hi + lo;
+            wt = (a.norm_topk ? __fdiv_rn(sv, sum) : sv) * a.routed_scale;
+        } else {
+            double p = 0.0;
+            if (lane < K)
+                p = exp((double)ps[t * 32 + lane] - m) / z;
+            double sum = 0.0;
+            for (int i = 0; i < K; ++i)
+                sum += __shfl_sync(FULL, p, i);
+            if (a.norm_topk)
+                p = p / sum;
+            wt = (float)(p * (double)a.routed_scale);
+        }
+        if (lane < K) {
+            const int id = pick[t * 32 + lane];
+            sids[t * K + lane] = id;
+            s.wtab[t * K + lane] = wt;
+            if (blockIdx.x == 0) {
+                a.ids[(long)t * K + lane] = id;
+                a.w_out[(long)t * K + lane] = wt;
+            }
+        }
+    }
+    return one_warp || consumers_sync(s, cph, lane);
+}
+
+// Slot table, counters and (CTA 0) the workspace copies from the pair ids, for at most 32
+// pairs, by one warp: lane p holds pair p. Same results as the general bucketing below.
+__device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *sids, int lane)
+{
+    const int T = a.T, K = a.K, E = a.E, P = T * K;
+    const int sbase = a.has_shared ? 1 : 0;
+    __syncwarp();
+    const bool live = lane < P;
+    const int e = live ? sids[lane] : -1;
+    const bool valid = live && e >= 0 && e < E;
+    // lanes holding the same id (lanes past P get keys of their own)
+    const unsigned same = __match_any_sync(FULL, live ? e : -2 - lane);
+    const unsigned below = (1u << lane) - 1u;
+    const int tok0 = live ? lane - lane % K : 0;
+    const unsigned in_tok = below & ~((1u << tok0) - 1u);
+    const bool dup = live && (same & in_tok) != 0;
+    const bool fst = valid && (same & below) == 0;
+    if (blockIdx.x == 0 && live && (!valid || dup))
+        atomicOr(a.err, ERR_BAD_ID);
+    const unsigned fmask = __ballot_sync(FULL, fst);
+    const int n_valid = __popc(__ballot_sync(FULL, valid)), n_routed = __popc(fmask);
+    int less = 0, dless = 0;
+    for (int j = 0; j < P; ++j) {
+        const int ej = __shfl_sync(FULL, e, j);
+        const bool vj = ej >= 0 && ej < E;
+        less += vj && ej < e;
+        dless += ((fmask >> j) & 1) && ej < e;
+    }
+    if (valid) {
+        const int pos = __popc(same & below);
+        s.ptab[less + pos] = lane;
+        if (blockIdx.x == 0)
+            a.pairs[less + pos] = lane;
+        if (fst) {
+            SlotInfo si;
+            si.ex = a.experts[e];
+            si.begin = less;
+            si.count = __popc(same);
+            si.pad[0] = si.pad[1] = 0;
+            s.stab[sbase + dless] = si;
+            if (blockIdx.x == 0) {
+                Slot sl;
+                sl.expert = e;
+                sl.begin = less;
+                sl.count = si.count;
+                sl.pad = 0;
+                a.slots[sbase + dless] = sl;
+            }
+        }
+    }
+    if (blockIdx.x == 0) {
+        for (int x = lane; x <= E; x += 32) {
+            int c = 0;
+            for (int q = 0; q < P; ++q)
+                c += sids[q] >= 0 && sids[q] < x;
+            a.offsets[x] = c;
+        }
+    }
+    if (lane == 0) {
+        if (a.has_shared) {
+            SlotInfo si;
+            si.ex = a.shared;
+            si.begin = 0;
+            si.count = T;
+            si.pad[0] = si.pad[1] = 0;
+            s.stab[0] = si;
+        }
+        Counters ct;
+        ct.n_slots = sbase + n_routed;
+        ct.n_routed = n_routed;
+        ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
+        ct.n_items_down = ct.n_slots * (a.d / G);
+        ct.n_rows = n_valid + (a.has_shared ? T : 0);
+        ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
+        *s.ctab = ct;
+        if (blockIdx.x == 0) {
+            if (a.has_shared) {
+                Slot sl;
+                sl.expert = -1;
+                sl.begin = 0;
+                sl.count = T;
+                sl.pad = 0;
+                a.slots[0] = sl;
+            }
+            *a.counters = ct;
+        }
+    }
+}
+
+// Routing of this CTA: ids and weights (selected, or given), then bucketing in shared
+// memory: pair list stable by expert, slots = the shared expert then the distinct valid
+// experts in ascending id, counters. CTA 0 also writes the pair offsets, pair list, slots
+// and counters to the workspace and flags bad ids (outside [0, E), or twice in a token).
+__device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph, int tid, int warp, int lane)
+{
+    const int T = a.T, K = a.K, E = a.E, P = T * K;
+    int *sids = reinterpret_cast<int *>(s.act);
+    int *first = sids + P;
+    float *scr = reinterpret_cast<float *>(s.act + ((8 * (size_t)P + 15) & ~size_t(15)));
+    if (tid == 0)
+        s.flags[1] = s.flags[2] = 0;
+    if (a.ids_given) {
+        for (int i = tid; i < P; i += NT) {
+            sids[i] = __ldcg(a.ids + i);
+            s.wtab[i] = __ldcg(a.w_in + i);
+        }
+        if (P > 32 && !consumers_sync(s, cph, lane))
+            return false;
+    } else if (!select_cta(a, s, scr, sids, cph, tid, warp, lane)) {
+        return false;
+    }
+    if (P <= 32) {
+        if (warp == 0)
+            bucket_warp(a, s, sids, lane);
+        return consumers_sync(s, cph, lane);
+    }
+    for (int p = tid; p < P; p += NT) {
+        const int e = sids[p];
+        const bool valid = e >= 0 && e < E;
+        bool dup = false, fst = valid;
+        for (int q = 0; q < p; ++q) {
+            const bool same = sids[q] == e;
+            dup |= same && q >= p - p % K;
+            fst &= !same;
+        }
+        if (blockIdx.x == 0 && (!valid || dup))
+            atomicOr(a.err, ERR_BAD_ID);
+        first[p] = fst;
+        if (valid)
+            atomicAdd(&s.flags[1], 1);
+        if (fst)
+            atomicAdd(&s.flags[2], 1);
+    }
+    if (!consumers_sync(s, cph, lane))
+        return false;
+    const int sbase = a.has_shared ? 1 : 0;
+    for (int p = tid; p < P; p += NT) {
+        const int e = sids[p];
+        if (e < 0 || e >= E)
+            continue;
+        int less = 0, pos = 0, cnt = 0, dless = 0;
+        for (int q = 0; q < P; ++q) {
+            const int eq = sids[q];
+            const bool v = eq >= 0 && eq < E;
+            less += v && eq < e;
+            pos += q < p && eq == e;
+            cnt += eq == e;
+            dless += first[q] && eq < e;
+        }
+        s.ptab[less + pos] = p;
+        if (blockIdx.x == 0)
+            a.pairs[less + pos] = p;
+        if (first[p]) {
+            SlotInfo si;
+            si.ex = a.experts[e];
+            si.begin = less;
+            si.count = cnt;
+            si.pad[0] = si.pad[1] = 0;
+            s.stab[sbase + dless] = si;
+            if (blockIdx.x == 0) {
+                Slot sl;
+                sl.expert = e;
+                sl.begin = less;
+                sl.count = cnt;
+                sl.pad = 0;
+                a.slots[sbase + dless] = sl;
+            }
+        }
+    }
+    if (blockIdx.x == 0) {
+        for (int e = tid; e <= E; e += NT) {
+            int less = 0;
+            for (int q = 0; q < P; ++q)
+                less += sids[q] >= 0 && sids[q] < e;
+            a.offsets[e] = less;
+        }
+    }
+    if (tid == 0) {
+        if (a.has_shared) {
+            SlotInfo si;
+            si.ex = a.shared;
+            si.begin = 0;
+            si.count = T;
+            si.pad[0] = si.pad[1] = 0;
+            s.stab[0] = si;
+        }
+        const int n_routed = s.flags[2];
+        Counters ct;
+        ct.n_slots = sbase + n_routed;
+        ct.n_routed = n_routed;
+        ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
+        ct.n_items_down = ct.n_slots * (a.d / G);
+        ct.n_rows = s.flags[1] + (a.has_shared ? T : 0);
+        ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
+        *s.ctab = ct;
+        if (blockIdx.x == 0) {
+            if (a.has_shared) {
+                Slot sl;
+                sl.expert = -1;
+                sl.begin = 0;
+                sl.count = T;
+                sl.pad = 0;
+                a.slots[0] = sl;
+            }
+            *a.counters = ct;
+        }
+    }
+    return consumers_sync(s, cph, lane);
+}
+
+// Partial dots of one stage: consumer warp w takes groups w, w + NC, ... of the stage.
+// Activation row t of the chunk sits at row rows[t] of the staged codes (row stride
+// cstride bytes), scales and corrections (gstride groups a row).
+template <int MODE, int TCH>
+__device__ __forceinline__ void consume(const unsigned char *stg, const int8_t *codes, const float *sc,
+                                        const int *corr, int cstride, int gstride, const int (&rows)[TCH], int ng,
+                                        int g0, int nt, int warp, int lane, float (&acc)[2][TCH])
+{
+    constexpr int M = MODE == MODE_GATEUP ? 2 : 1;
+    constexpr int SG = MODE == MODE_GATEUP ? SG_GU : SG_DN;
+    constexpr int GPW = MODE == MODE_GATEUP ? GPW_GU : GPW_DN;
+    constexpr int scale_off = M * SG * 512;
+    const int n = min(SG, ng - g0);
+#pragma unroll
+    for (int u = 0; u < GPW; ++u) {
+        const int j = warp + u * NC;
+        if (j < n) {
+            const int g = g0 + j;
+            NibbleSplit nsp[M];
+            float sw[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                nsp[m] = split_nibbles(*reinterpret_cast<const uint4 *>(stg + (m * SG + j) * 512 + lane * 16));
+                sw[m] = *reinterpret_cast<const float *>(stg + scale_off + (m * SG + j) * 128 + lane * 4);
+            }
+#pragma unroll
+            for (int t = 0; t < TCH; ++t) {
+                if (t < nt) {
+                    const int r = rows[t];
+                    const uint4 *xa = reinterpret_cast<const uint4 *>(codes + (size_t)r * cstride + g * G);
+                    const uint4 A0 = xa[0], A1 = xa[1];
+                    const int cr = corr[r * gstride + g];
+                    const float sa = sc[r * gstride + g];
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        const int D = dot_split(nsp[m], A0, A1, cr);
+                        acc[m][t] = fmaf((float)D, sw[m] * sa, acc[m][t]);
+                    }
+                }
+            }
+        }
+    }
+}
+
+// ---------------- producer (one thread) ----------------
+template <int TCH>
+__device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
+{
+    const int NS = a.ring, NH = a.nh;
+    const int sh_items = a.has_shared ? a.shared_ffn / G : 0;
+    if (a.has_shared)
+        prefetch_shared(a);
+    if (blockIdx.x == 0)
+        prefetch_l2(a.experts, (uint32_t)(((size_t)a.E * sizeof(colibri_expert) + 15) & ~size_t(15)));
+    const uint64_t pol = policy_evict_first();
+    int n_gu = sh_items + 1, total = 0x7fffffff;  // until the table is in
+    bool have_table = false;
+    uint32_t st = 0, hsw = 0;  // stages posted, h buffers filled
+    int hslot = -1, hch = -1;  // rows in the newest h buffer
+    uint64_t h_ready = 0;      // slots (below 64) whose rows of h are all published
+    // the ring slot of stage st, once the consumers have released it
+    auto acquire = [&](uint32_t &slot) -> bool {
+        slot = st % NS;
+        if (st >= (uint32_t)NS && !mbar_wait(&s.empty[slot], ((st / NS) - 1) & 1)) {
+            set_abort(a, s);
+            return false;
+        }
+        return !aborted(s);
+    };
+    // claims run two items ahead of the item being streamed
+    int idx = atomicAdd(a.claim, 1), ahead = atomicAdd(a.claim, 1);
+    for (bool run = true; run;) {
+        if (!have_table && idx >= sh_items) {
+            // past the shared expert: wait for the consumers' routing (slot table)
+            if (!mbar_wait(s.tbar, 0)) {
+                set_abort(a, s);
+                break;
+            }
+            have_table = true;
+            n_gu = s.ctab->n_items_gateup;
+            total = n_gu + s.ctab->n_items_down;
+        }
+        if (idx >= total) {
+            uint32_t slot;
+            if (acquire(slot)) {
+                s.tag[slot] = make_int2(-1, 0);  // end of work
+                mbar_arrive(&s.full[slot]);
+                ++st;
+            }
+            break;
+        }
+        const int next = ahead;
+        ahead = atomicAdd(a.claim, 1);  // used two items from now
+        const DecItem it = work_item(a, s.stab, n_gu, idx);
+        const bool gu = it.mode == MODE_GATEUP;
+        const int SG = gu ? SG_GU : SG_DN;
+        const int ng = it.kdim / G, spi = (ng + SG - 1) / SG;
+        const int nq = spi * ((it.count + TCH - 1) / TCH);
+        const size_t blk = (size_t)it.rb * ng;  // first group tile of the row block
+        for (int q = 0; q < nq && run; ++q) {
+            const int ch = q / spi, k = q % spi;
+            int flag = 0;
+            if (!gu && k == 0 && (it.slot != hslot || ch != hch)) {
+                // the chunk's rows of q8(h) into the next h buffer, once all rows of h of
+                // its slot are published
+                const int b = hsw % NH;
+                if (hsw >= (uint32_t)NH && !mbar_wait(&s.hempty[b], ((hsw / NH) - 1) & 1)) {
+                    set_abort(a, s);
+                    run = false;
+                    break;
+                }
+                if (!(it.slot < 64 && ((h_ready >> it.slot) & 1))) {
+                    const int need = (it.is_shared ? a.shared_ffn : a.ffn) / G * it.count;
+                    if (!wait_count_geq(a.done_gu + it.slot, need)) {
+                        set_abort(a, s);
+                        run = false;
+                        break;
+                    }
+                    if (it.slot < 64)
+                        h_ready |= 1ull << it.slot;
+                }
+                fence_proxy_async_global();  // h was written through the generic proxy
+                const int nt = min(TCH, it.count - ch * TCH);
+                unsigned char *hb = s.hbuf + (size_t)b * s.hb;
+                int8_t *hcodes = reinterpret_cast<int8_t *>(hb);
+                float *hsc = reinterpret_cast<float *>(hb + (size_t)TCH * a.fmax);
+                int *hcr = reinterpret_cast<int *>(hsc + (size_t)TCH * a.hgs);
+                mbar_arrive_expect_tx(&s.hfull[b], (uint32_t)(nt * (it.kdim + 8 * a.hgs)));
+                for (int t = 0; t < nt; ++t) {
+                    const long p = item_row(a, s, it, ch * TCH + t);
+                    bulk_g2s(hcodes + (size_t)t * a.fmax, a.hq_eo + p * a.fmax, (uint32_t)it.kdim, &s.hfull[b]);
+                    bulk_g2s(hsc + (size_t)t * a.hgs, a.hs + p * a.hgs, (uint32_t)(4 * a.hgs), &s.hfull[b]);
+                    bulk_g2s(hcr + (size_t)t * a.hgs, a.hc + p * a.hgs, (uint32_t)(4 * a.hgs), &s.hfull[b]);
+                }
+                ++hsw;
+                hslot = it.slot;
+                hch = ch;
+                flag = TAG_NEW_H;
+            }
+            uint32_t slot;
+            if (!acquire(slot)) {
+                run = false;
+                break;
+            }
+            const int g0 = k * SG, n = min(SG, ng - g0);
+            unsigned char *dst = s.ring + (size_t)slot * STAGE_BYTES;
+            s.tag[slot] = make_int2(idx, q | flag);
+            if (gu) {
+                mbar_arrive_expect_tx(&s.full[slot], (uint32_t)(2 * n * 640));
+                bulk_g2s_hint(dst, it.ex.w1 + (blk + g0) * 512, n * 512, &s.full[slot], pol);
+                bulk_g2s_hint(dst + SG_GU * 512, it.ex.w3 + (blk + g0) * 512, n * 512, &s.full[slot], pol);
+                bulk_g2s_hint(dst + 2 * SG_GU * 512, it.ex.s1 + (blk + g0) * 32, n * 128, &s.full[slot], pol);
+                bulk_g2s_hint(dst + 2 * SG_GU * 512 + SG_GU * 128, it.ex.s3 + (blk + g0) * 32, n * 128,
+                              &s.full[slot], pol);
+            } else {
+                mbar_arrive_expect_tx(&s.full[slot], (uint32_t)(n * 640));
+                bulk_g2s_hint(dst, it.ex.w2 + (blk + g0) * 512, n * 512, &s.full[slot], pol);
+                bulk_g2s_hint(dst + SG_DN * 512, it.ex.s2 + (blk + g0) * 32, n * 128, &s.full[slot], pol);
+            }
+            ++st;
+        }
+        idx = next;
+    }
+    // bounded waits for the copies issued, before the CTA exits
+    const uint32_t n = st < (uint32_t)NS ? st : (uint32_t)NS;
+    for (uint32_t k = 1; k <= n; ++k) {
+        const uint32_t q = st - k;
+        mbar_wait(&s.full[q % NS], (q / NS) & 1);
+    }
+    if (hsw > 0)
+        mbar_wait(&s.hfull[(hsw - 1) % NH], ((hsw - 1) / NH) & 1);
+}
+
+// ---------------- epilogue warp e: the chunks that used partial-sum buffer e ----------------
+template <int TCH>
+__device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int lane)
+{
+    constexpr int PART = NC * 2 * TCH * 32;
+    const float *pb = s.part + (size_t)e * PART;
+    for (uint32_t k = 0;; ++k) {
+        if (!mbar_wait(&s.pfull[e], k & 1)) {
+            if (lane == 0)
+                set_abort(a, s);
+            return;
+        }
+        const ChunkDesc *dp = s.desc + e;
+        const int mode = dp->mode;
+        if (mode < 0)
+            return;  // end of work
+        const int slot = dp->slot, rb = dp->rb, nt = dp->nt;
+        for (int t = 0; t < nt; ++t) {
+            const long r = dp->orow[t];
+            if (mode == MODE_GATEUP) {
+                float gt = 0.0f, up = 0.0f;
+                for (int w = 0; w < NC; ++w) {
+                    gt += pb[((w * 2 + 0) * TCH + t) * 32 + lane];
+                    up += pb[((w * 2 + 1) * TCH + t) * 32 + lane];
+                }
+                const float h = gt / (1.0f + expf(-gt)) * up;
+                const float amax = warp_max(fabsf(h));
+                const float dd = __fdiv_rn(amax, 127.0f);
+                const int q = q8_code(h, dd);
+                const long hb = r * a.fmax + (long)rb * G;
+                a.hq[hb + lane] = (int8_t)q;
+                a.hq_eo[hb + eo_pos(lane)] = (int8_t)q;
+                const int sq = warp_sum_i(q);
+                if (lane == 0) {
+                    a.hs[r * a.hgs + rb] = dd;
+                    a.hc[r * a.hgs + rb] = 8 * sq;
+                }
+            } else {
+                float y = 0.0f;
+                for (int w = 0; w < NC; ++w)
+                    y += pb[(w * 2 * TCH + t) * 32 + lane];
+                a.y[r * a.d + (long)rb * G + lane] = y;
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&s.pempty[e]);  // the consumers may refill the buffer
+        __threadfence();                // this chunk's rows are visible device-wide
+        __syncwarp();
+        if (mode == MODE_GATEUP) {
+            if (lane == 0)
+                atomicAdd(a.done_gu + slot, nt);
+            continue;
+        }
+        int last = 0;
+        if (lane == 0) {
+            last = atomicAdd(a.done_rb + rb, nt) + nt == s.ctab->n_rows;
+            if (last)
+                __threadfence();
+        }
+        if (__shfl_sync(FULL, last, 0)) {
+            // every row of this block of d is in: combine it for all tokens
+            const long col = (long)rb * G + lane;
+            for (int t = 0; t < a.T; ++t) {
+                float o = a.has_shared ? __ldcg(a.y + ((long)a.T * a.K + t) * a.d + col) : 0.0f;
+                for (int i = 0; i < a.K; ++i)
+                    o = fmaf(s.wtab[t * a.K + i], __ldcg(a.y + ((long)t * a.K + i) * a.d + col), o);
+                a.out[(long)t * a.d + col] = o;
+            }
+        }
+    }
+}
+
+// ---------------- consumer warps ----------------
+template <int TCH>
+__device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, int lane)
+{
+    constexpr int NBUF = nbuf_for(TCH);
+    constexpr int PART = NC * 2 * TCH * 32;
+    const int NS = a.ring, NH = a.nh;
+    const int tid = threadIdx.x;
+    uint32_t cph = 0;  // consumer barrier phase
+    grid_dep_wait();   // router scores and q8 of x (or the given ids) are in
+    if (!route_cta(a, s, cph, tid, warp, lane))
+        return;
+    if (tid == 0)
+        mbar_arrive(s.tbar);  // the producer may read the table now
+    const int n_gu = s.ctab->n_items_gateup;
+    // the x staging area: all T tokens at once when they fit a chunk, else the chunk's
+    int8_t *xcodes = reinterpret_cast<int8_t *>(s.act);
+    float *xsc = reinterpret_cast<float *>(s.act + (size_t)TCH * a.d);
+    int *xcr = reinterpret_cast<int *>(xsc + (size_t)TCH * (a.d / G));
+    const bool x_all = a.T <= TCH;
+    bool x_staged = false;
+    int xrows[TCH];  // token of each staged x row
+#pragma unroll
+    for (int t = 0; t < TCH; ++t)
+        xrows[t] = -1;
+    uint32_t chunk = 0;  // chunks handed to the epilogue (buffer chunk % NBUF)
+    uint32_t hsw = 0;    // h buffers entered
+    int cur_h = 0;
+    int cur = -1, spi = 1, ng = 1;
+    DecItem it{};
+    int rows[TCH];
+    int orow = -1;  // lane t < nt: pair row of the chunk's t-th token
+    float acc[2][TCH];
+    // a buffer's previous chunk must have been read before it is written again
+    auto buffer_free = [&](int b) -> bool {
+        if (chunk >= (uint32_t)NBUF && !mbar_wait(&s.pempty[b], ((chunk / NBUF) - 1) & 1)) {
+            if (lane == 0)
+                set_abort(a, s);
+            return false;
+        }
+        return true;
+    };
+    for (uint32_t st = 0;; ++st) {
+        const int slot = st % NS;
+        if (!mbar_wait(&s.full[slot], (st / NS) & 1)) {
+            if (lane == 0)
+                set_abort(a, s);
+            return;
+        }
+        const int2 tag = s.tag[slot];
+        if (tag.x < 0) {
+            // end of work: one end descriptor into every buffer, in buffer order
+            for (int j = 0; j < NBUF; ++j, ++chunk) {
+                const int b = chunk % NBUF;
+                if (!buffer_free(b))
+                    return;
+                if (tid == 0)
+                    s.desc[b].mode = -1;
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&s.pfull[b]);
+            }
+            return;
+        }
+        if (tag.x != cur) {
+            cur = tag.x;
+            it = work_item(a, s.stab, n_gu, cur);
+            const int SG = it.mode == MODE_GATEUP ? SG_GU : SG_DN;
+            ng = it.kdim / G;
+            spi = (ng + SG - 1) / SG;
+        }
+        const int q = tag.y & (TAG_NEW_H - 1);
+        const int ch = q / spi, k = q % spi;
+        const int c0 = ch * TCH, nt = min(TCH, it.count - c0);
+        if (k == 0) {
+            orow = lane < nt ? item_row(a, s, it, c0 + lane) : -1;
+            if (it.mode == MODE_GATEUP) {
+                int tok[TCH];
+#pragma unroll
+                for (int t = 0; t < TCH; ++t) {
+                    const int p = __shfl_sync(FULL, orow, t);
+                    tok[t] = t < nt ? (it.is_shared ? c0 + t : p / a.K) : -1;
+                }
+                bool same = x_staged;
+                if (!x_all) {
+#pragma unroll
+                    for (int t = 0; t < TCH; ++t)
+                        same &= xrows[t] == tok[t];
+                }
+                if (!same) {
+                    // stage the x rows (all T tokens, or this chunk's), every warp alike
+                    if (!consumers_sync(s, cph, lane))
+                        return;
+                    const int nrow = x_all ? a.T : nt;
+#pragma unroll
+                    for (int t = 0; t < TCH; ++t)
+                        xrows[t] = x_all ? (t < a.T ? t : -1) : tok[t];
+                    const int v16 = a.d / 16, gx = a.d / G;
+                    for (int i = tid; i < nrow * v16; i += NT) {
+                        const int tt = i / v16, o = i % v16;
+                        int xr = 0;
+#pragma unroll
+                        for (int t = 0; t < TCH; ++t)
+                            xr = t == tt ? xrows[t] : xr;
+                        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.xq_eo + (long)xr * a.d) + o);
+                        reinterpret_cast<uint4 *>(xcodes + (size_t)tt * a.d)[o] = v;
+                    }
+                    for (int i = tid; i < nrow * gx; i += NT) {
+                        const int tt = i / gx, g = i % gx;
+                        int xr = 0;
+#pragma unroll
+                        for (int t = 0; t < TCH; ++t)
+                            xr = t == tt ? xrows[t] : xr;
+                        xsc[i] = __ldcg(a.xs + (long)xr * gx + g);
+                        xcr[i] = __ldcg(a.xc + (long)xr * gx + g);
+                    }
+                    if (!consumers_sync(s, cph, lane))
+                        return;
+                    x_staged = true;
+                }
+#pragma unroll
+                for (int t = 0; t < TCH; ++t)
+                    rows[t] = x_all ? (tok[t] < 0 ? 0 : tok[t]) : t;
+            } else {
+                if (tag.y & TAG_NEW_H) {
+                    // leave the previous h buffer, enter the next one
+                    __syncwarp();
+                    if (hsw > 0 && lane == 0)
+                        mbar_arrive(&s.hempty[(hsw - 1) % NH]);
+                    if (!mbar_wait(&s.hfull[hsw % NH], (hsw / NH) & 1)) {
+                        if (lane == 0)
+                            set_abort(a, s);
+                        return;
+                    }
+                    cur_h = hsw % NH;
+                    ++hsw;
+                }
+#pragma unroll
+                for (int t = 0; t < TCH; ++t)
+                    rows[t] = t;
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m)
+#pragma unroll
+                for (int t = 0; t < TCH; ++t)
+                    acc[m][t] = 0.0f;
+        }
+        const unsigned char *stg = s.ring + (size_t)slot * STAGE_BYTES;
+        if (it.mode == MODE_GATEUP) {
+            consume<MODE_GATEUP, TCH>(stg, xcodes, xsc, xcr, a.d, a.d / G, rows, ng, k * SG_GU, nt, warp, lane, acc);
+        } else {
+            const unsigned char *hb = s.hbuf + (size_t)cur_h * s.hb;
+            const int8_t *hcodes = reinterpret_cast<const int8_t *>(hb);
+            const float *hsc = reinterpret_cast<const float *>(hb + (size_t)TCH * a.fmax);
+            const int *hcr = reinterpret_cast<const int *>(hsc + (size_t)TCH * a.hgs);
+            consume<MODE_DOWN, TCH>(stg, hcodes, hsc, hcr, a.fmax, a.hgs, rows, ng, k * SG_DN, nt, warp, lane, acc);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&s.empty[slot]);
+        if (k != spi - 1)
+            continue;
+
+        // ---- end of a chunk: hand the partial sums to the epilogue warp of the buffer ----
+        const int b = chunk % NBUF;
+        if (!buffer_free(b))
+            return;
+        const int M = it.mode == MODE_GATEUP ? 2 : 1;
+        float *pb = s.part + (size_t)b * PART;
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int t = 0; t < TCH; ++t)
+                if (m < M && t < nt)
+                    pb[((warp * 2 + m) * TCH + t) * 32 + lane] = acc[m][t];
+        if (warp == 0) {
+            ChunkDesc *dp = s.desc + b;
+            if (lane < nt)
+                dp->orow[lane] = orow;
+            if (lane == 0) {
+                dp->mode = it.mode;
+                dp->slot = it.slot;
+                dp->rb = it.rb;
+                dp->nt = nt;
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&s.pfull[b]);
+        ++chunk;
+    }
 }
 
 }  // namespace
 
-// Bytes of dynamic shared memory besides the ring (host side mirror of carve()).
-static size_t ring_fixed_bytes(int kmax, int nc, int m, int tch, int ns)
+template <int TCH>
+__global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs a)
 {
-    const size_t ngm = kmax / G;
-    return 16 * (size_t)ns + 16 + (size_t)tch * kmax + 8 * (size_t)tch * ngm +
-           4 * (size_t)2 * nc * m * tch * 32 + 8 * (size_t)tch;
-}
-
-// MODE_GATEUP: M = 2 matrices (W1, W3), output h codes; MODE_DOWN: M = 1 (W2), output y.
-// NC consumer warps + 1 producer warp; TCH tokens per chunk; a stage holds SG = NC * GPW
-// groups and consumer warp w takes groups w, w + NC, ... of it.
-template <int MODE, int NC, int TCH, int GPW>
-__global__ void __launch_bounds__((NC + 1) * 32, 1) k_ring(DecodeArgs a)
-{
-    constexpr int M = MODE == MODE_GATEUP ? 2 : 1;
-    constexpr int SG = NC * GPW;
+    constexpr int NBUF = nbuf_for(TCH);
+    static_assert(TCH <= 8, "chunk descriptors hold 8 rows");
     extern __shared__ __align__(128) unsigned char sm[];
-    const RingSmem s = carve(sm, a, NC, M, TCH);
-    const int NS = a.ring;
+    const RingSmem s = carve(sm, a, TCH);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = MODE == MODE_GATEUP ? a.counters->n_items_gateup : a.counters->n_items_down;
-    const int i0 = (int)((long)blockIdx.x * n_items / gridDim.x);
-    const int i1 = (int)((long)(blockIdx.x + 1) * n_items / gridDim.x);
-    // stage layout: M group-tile runs of SG*512 bytes, then M scale runs of SG*128 bytes
-    constexpr int scale_off = M * SG * 512;
-
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < a.ring; ++i) {
             mbar_init(&s.full[i], 1);
             mbar_init(&s.empty[i], NC);
         }
-        *s.abort_flag = 0;
+        for (int i = 0; i < a.nh; ++i) {
+            mbar_init(&s.hfull[i], 1);
+            mbar_init(&s.hempty[i], NC);
+        }
+        mbar_init(s.cbar, NC);
+        mbar_init(s.tbar, 1);
+        for (int i = 0; i < NBUF; ++i) {
+            mbar_init(&s.pfull[i], NC);
+            mbar_init(&s.pempty[i], 1);
+        }
+        s.flags[0] = 0;
         fence_mbar_init();
     }
     __syncthreads();
-
     if (warp == NC) {
-        // ---------------- producer ----------------
-        if (lane != 0)
-            return;
-        uint32_t st = 0;
-        auto drain = [&]() {  // bounded wait for the copies issued, before the CTA exits
-            const uint32_t n = st < (uint32_t)NS ? st : (uint32_t)NS;
-            for (uint32_t k = 1; k <= n; ++k) {
-                const uint32_t q = st - k;
-                mbar_wait(&s.full[q % NS], (q / NS) & 1);
-            }
-        };
-        for (int item = i0; item < i1; ++item) {
-            const DecItem it = item_info<MODE>(a, item);
-            const int ng = it.kdim / G, spi = (ng + SG - 1) / SG;
-            const int nch = (it.count + TCH - 1) / TCH;
-            const size_t blk = (size_t)it.rb * ng;  // first group tile of the row block
-            for (int ch = 0; ch < nch; ++ch) {
-                for (int k = 0; k < spi; ++k, ++st) {
-                    const int slot = st % NS;
-                    if (st >= (uint32_t)NS && !mbar_wait(&s.empty[slot], ((st / NS) - 1) & 1)) {
-                        atomicOr(a.err, ERR_WAIT_TIMEOUT);
-                        *reinterpret_cast<volatile int *>(s.abort_flag) = 1;
-                        drain();
-                        return;
-                    }
-                    if (*reinterpret_cast<volatile int *>(s.abort_flag)) {
-                        drain();
-                        return;
-                    }
-                    const int g0 = k * SG, n = min(SG, ng - g0);
-                    unsigned char *dst = s.ring + (size_t)slot * a.stage_bytes;
-                    mbar_arrive_expect_tx(&s.full[slot], (uint32_t)(M * n * (512 + 128)));
-                    if (MODE == MODE_GATEUP) {
-                        bulk_g2s(dst, it.ex.w1 + (blk + g0) * 512, n * 512, &s.full[slot]);
-                        bulk_g2s(dst + SG * 512, it.ex.w3 + (blk + g0) * 512, n * 512, &s.full[slot]);
-                        bulk_g2s(dst + scale_off, it.ex.s1 + (blk + g0) * 32, n * 128, &s.full[slot]);
-                        bulk_g2s(dst + scale_off + SG * 128, it.ex.s3 + (blk + g0) * 32, n * 128, &s.full[slot]);
-                    } else {
-                        bulk_g2s(dst, it.ex.w2 + (blk + g0) * 512, n * 512, &s.full[slot]);
-                        bulk_g2s(dst + scale_off, it.ex.s2 + (blk + g0) * 32, n * 128, &s.full[slot]);
-                    }
-                }
-            }
-        }
-        return;
-    }
-
-    // ---------------- consumers ----------------
-    constexpr int NT = NC * 32;
-    uint32_t st = 0;
-    int buf = 0;
-    int staged_slot = -1, staged_ch = -1;
-    for (int item = i0; item < i1; ++item) {
-        const DecItem it = item_info<MODE>(a, item);
-        const int K = it.kdim, ng = K / G, spi = (ng + SG - 1) / SG;
-        const int nch = (it.count + TCH - 1) / TCH;
-        for (int ch = 0; ch < nch; ++ch) {
-            const int c0 = ch * TCH, nt = min(TCH, it.count - c0);
-            if (it.slot != staged_slot || ch != staged_ch) {
-                // stage this chunk's activation rows (all consumers)
-                named_sync(1, NT);
-                if ((int)threadIdx.x < nt) {
-                    const int c = c0 + threadIdx.x;
-                    const int p = it.is_shared ? a.T * a.K + c : a.pairs[it.begin + c];
-                    s.arow[threadIdx.x] = MODE == MODE_GATEUP ? (it.is_shared ? c : p / a.K) : p;
-                    s.orow[threadIdx.x] = p;
-                }
-                named_sync(1, NT);
-                const int v16 = K / 16;
-                for (int i = threadIdx.x; i < nt * v16; i += NT) {
-                    const int tt = i / v16, o = i % v16;
-                    const uint4 v = ld_nc(a.aq_eo + (long)s.arow[tt] * a.act_stride + o * 16);
-                    reinterpret_cast<uint4 *>(s.codes + (size_t)tt * K)[o] = v;
-                }
-                for (int i = threadIdx.x; i < nt * ng; i += NT) {
-                    const int tt = i / ng, g = i % ng;
-                    s.sc[i] = a.as[(long)s.arow[tt] * a.act_groups + g];
-                    s.corr[i] = a.ac[(long)s.arow[tt] * a.act_groups + g];
-                }
-                named_sync(1, NT);
-                staged_slot = it.slot;
-                staged_ch = ch;
-            }
-            float acc[M][TCH];
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-#pragma unroll
-                for (int t = 0; t < TCH; ++t)
-                    acc[m][t] = 0.0f;
-            bool aborted = false;
-            for (int k = 0; k < spi; ++k, ++st) {
-                const int slot = st % NS;
-                if (!mbar_wait(&s.full[slot], (st / NS) & 1)) {
-                    if (lane == 0)
-                        atomicOr(a.err, ERR_WAIT_TIMEOUT);
-                    *reinterpret_cast<volatile int *>(s.abort_flag) = 1;
-                    aborted = true;
-                    break;
-                }
-                const unsigned char *stg = s.ring + (size_t)slot * a.stage_bytes;
-                const int g0 = k * SG, n = min(SG, ng - g0);
-#pragma unroll
-                for (int u = 0; u < GPW; ++u) {
-                    const int j = warp + u * NC;
-                    if (j < n) {
-                        const int g = g0 + j;
-                        NibbleSplit ns[M];
-                        float sw[M];
-#pragma unroll
-                        for (int m = 0; m < M; ++m) {
-                            ns[m] = split_nibbles(*reinterpret_cast<const uint4 *>(stg + (m * SG + j) * 512 + lane * 16));
-                            sw[m] = *reinterpret_cast<const float *>(stg + scale_off + (m * SG + j) * 128 + lane * 4);
-                        }
-#pragma unroll
-                        for (int t = 0; t < TCH; ++t) {
-                            if (t < nt) {
-                                const uint4 *xa = reinterpret_cast<const uint4 *>(s.codes + (size_t)t * K + g * G);
-                                const uint4 A0 = xa[0], A1 = xa[1];
-                                const int corr = s.corr[t * ng + g];
-                                const float sa = s.sc[t * ng + g];
-#pragma unroll
-                                for (int m = 0; m < M; ++m) {
-                                    const int D = dot_split(ns[m], A0, A1, corr);
-                                    acc[m][t] = fmaf((float)D, sw[m] * sa, acc[m][t]);
-                                }
-                            }
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&s.empty[slot]);
-            }
-            // this warp's partial sums for the block's 32 rows
-            float *pb = s.part + (size_t)buf * (NC * M * TCH * 32);
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-#pragma unroll
-                for (int t = 0; t < TCH; ++t)
-                    if (t < nt)
-                        pb[((warp * M + m) * TCH + t) * 32 + lane] = acc[m][t];
-            // every consumer reaches this barrier once per chunk, aborted or not; a warp
-            // that aborts sets the flag first, so all of them leave together
-            named_sync(1, NT);
-            if (aborted || *reinterpret_cast<volatile int *>(s.abort_flag))
-                return;
-            for (int t = warp; t < nt; t += NC) {
-                if (MODE == MODE_GATEUP) {
-                    float gt = 0.0f, up = 0.0f;
-                    for (int w = 0; w < NC; ++w) {
-                        gt += pb[((w * 2 + 0) * TCH + t) * 32 + lane];
-                        up += pb[((w * 2 + 1) * TCH + t) * 32 + lane];
-                    }
-                    const float h = gt / (1.0f + expf(-gt)) * up;
-                    const float amax = warp_max(fabsf(h));
-                    const float dd = __fdiv_rn(amax, 127.0f);
-                    const int q = q8_code(h, dd);
-                    const long r = s.orow[t];
-                    const long hb = r * a.fmax + (long)it.rb * G;
-                    a.hq[hb + lane] = (int8_t)q;
-                    a.hq_eo[hb + eo_pos(lane)] = (int8_t)q;
-                    const int sq = warp_sum_i(q);
-                    if (lane == 0) {
-                        const int fsg = a.fmax / G;
-                        a.hs[r * fsg + it.rb] = dd;
-                        a.hc[r * fsg + it.rb] = 8 * sq;
-                    }
-                } else {
-                    float y = 0.0f;
-                    for (int w = 0; w < NC; ++w)
-                        y += pb[(w * TCH + t) * 32 + lane];
-                    a.y[(long)s.orow[t] * a.d + (long)it.rb * G + lane] = y;
-                }
-            }
-            buf ^= 1;
-        }
+        if (lane == 0)
+            run_producer<TCH>(a, s);
+    } else if (warp > NC) {
+        if (warp - NC - 1 < NBUF)
+            run_epilogue<TCH>(a, s, warp - NC - 1, lane);
+    } else {
+        run_consumers<TCH>(a, s, warp, lane);
     }
 }
 
@@ -311,29 +1132,29 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1) k_ring(DecodeArgs a)
 
 namespace {
 
-constexpr int RING_NC = 16;             // consumer warps
-constexpr size_t RING_BUDGET = 220 * 1024;
-
-// Groups per consumer warp and stage: stages of about 40 KB.
-template <int MODE>
-constexpr int ring_gpw()
+template <int TCH>
+cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
 {
-    return MODE == MODE_GATEUP ? 2 : 4;
-}
-
-template <int MODE, int TCH>
-cudaError_t launch_ring(DecodeArgs a, int max_items, cudaStream_t s)
-{
-    constexpr int M = MODE == MODE_GATEUP ? 2 : 1;
-    auto fn = k_ring<MODE, RING_NC, TCH, ring_gpw<MODE>()>;
-    a.sg = RING_NC * ring_gpw<MODE>();
-    a.stage_bytes = M * a.sg * (512 + 128);
-    const size_t fixed = ring_fixed_bytes(a.kmax, RING_NC, M, TCH, 16);
-    if (fixed + 2 * (size_t)a.stage_bytes > RING_BUDGET)
+    auto fn = k_decode<TCH>;
+    // the most 40 KB ring stages beside the rest, with 3 h buffers if that leaves 5
+    // stages, else 2
+    int best_ns = 0, best_nh = 2;
+    for (int nh = NH_MAX; nh >= 2; --nh) {
+        int ns = MAX_RING;
+        while (ns >= 2 && ring_layout(a, ns, nh, TCH).total > SMEM_BUDGET)
+            --ns;
+        if (ns > best_ns) {
+            best_ns = ns;
+            best_nh = nh;
+        }
+        if (ns >= 5)
+            break;
+    }
+    if (best_ns < 2)
         return cudaErrorInvalidValue;
-    int ns = (int)((RING_BUDGET - fixed) / a.stage_bytes);
-    a.ring = ns > 16 ? 16 : ns;
-    const size_t smem = (size_t)a.ring * a.stage_bytes + ring_fixed_bytes(a.kmax, RING_NC, M, TCH, a.ring);
+    a.ring = best_ns;
+    a.nh = best_nh;
+    const size_t smem = ring_layout(a, a.ring, a.nh, TCH).total;
     int dev = 0, n_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
@@ -342,33 +1163,51 @@ cudaError_t launch_ring(DecodeArgs a, int max_items, cudaStream_t s)
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    const int grid = max_items < n_sm ? max_items : n_sm;
-    fn<<<grid, (RING_NC + 1) * 32, smem, s>>>(a);
-    return cudaGetLastError();
-}
-
-template <int MODE>
-cudaError_t launch_mode(const DecodeArgs &a, int max_items, cudaStream_t s)
-{
-    switch (a.tch) {
-    case 1: return launch_ring<MODE, 1>(a, max_items, s);
-    case 2: return launch_ring<MODE, 2>(a, max_items, s);
-    case 4: return launch_ring<MODE, 4>(a, max_items, s);
-    default: return launch_ring<MODE, 8>(a, max_items, s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_sm);
+    cfg.blockDim = dim3((NC + 1 + NE_MAX) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, a);
+    if (e != cudaSuccess) {
+        // a stream that cannot take a programmatic dependency: plain stream order
+        (void)cudaGetLastError();
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelEx(&cfg, fn, a);
     }
+    return e;
 }
 
 }  // namespace
 
-cudaError_t launch_decode(int mode, DecodeArgs a, int max_items, cudaStream_t s)
+int decode_hgs(int fmax)
 {
-    if (max_items <= 0)
+    return round_up(fmax / G, 4);
+}
+
+bool decode_selects_in_kernel(int T, int E)
+{
+    return T * E <= 8192;
+}
+
+cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
+{
+    if (a.T <= 0)
         return cudaSuccess;
-    a.kmax = mode == MODE_GATEUP ? a.d : a.fmax;
+    a.hgs = decode_hgs(a.fmax);
     const int tmax = a.T < 8 ? a.T : 8;
     a.tch = tmax <= 1 ? 1 : tmax <= 2 ? 2 : tmax <= 4 ? 4 : 8;
-    return mode == MODE_GATEUP ? launch_mode<MODE_GATEUP>(a, max_items, s)
-                               : launch_mode<MODE_DOWN>(a, max_items, s);
+    switch (a.tch) {
+    case 1: return launch_tch<1>(a, s);
+    case 2: return launch_tch<2>(a, s);
+    case 4: return launch_tch<4>(a, s);
+    default: return launch_tch<8>(a, s);
+    }
 }
 
 }  // namespace clb

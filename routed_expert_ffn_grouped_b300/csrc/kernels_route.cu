@@ -11,6 +11,7 @@ __device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane);
 
 __global__ void __launch_bounds__(256) k_q8(Q8Args a)
 {
+    grid_dep_launch();  // a decode expert kernel after this one may be scheduled now
     const int lane = threadIdx.x & 31;
     const long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (gw >= a.rows * (a.cols / G))
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(256, 2) k_route_logits_tiled(RouterArgs a)
 
 __global__ void __launch_bounds__(128) k_route_logits(RouterArgs a)
 {
+    grid_dep_launch();  // a decode expert kernel after this one may be scheduled now
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar;
     route_logits_part(a, smem_raw, &bar);
@@ -372,6 +374,7 @@ constexpr int SEL_WARPS = 4;
 
 __global__ void __launch_bounds__(32 * SEL_WARPS) k_router_select(SelectArgs a)
 {
+    grid_dep_launch();  // a decode expert kernel after this one may be scheduled now
     __shared__ float s_c[SEL_WARPS][1024];
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x * SEL_WARPS + w;
@@ -545,71 +548,8 @@ __device__ void bucket_block(const BucketArgs &a, const int32_t *sid, int *sm)
         ct.n_routed = n_routed;
         ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
         ct.n_items_down = ct.n_slots * a.down_blocks;
-        *a.counters = ct;
-    }
-}
-
-// Bucketing for few pairs (decode), with short loops only: every expert's thread counts
-// and lists its pairs by scanning all T*K ids in order, so the list is stable by
-// construction. O(E * T * K) work, trivial at decode sizes; sm: 2*E ints.
-__device__ void bucket_small(const BucketArgs &a, const int32_t *sid, int *sm)
-{
-    const int E = a.E, nt = blockDim.x, tid = threadIdx.x;
-    const int P = a.T * a.K;
-    int *off = sm, *flag = sm + E;
-    for (int p = tid; p < P; p += nt) {
-        const int e = sid[p];
-        bool bad = e < 0 || e >= E;
-        for (int q = p - p % a.K; q < p; ++q)
-            bad |= sid[q] == e;  // a token must not list an expert twice
-        if (bad && a.err)
-            atomicOr(a.err, ERR_BAD_ID);
-    }
-    for (int e = tid; e < E; e += nt) {
-        int c = 0;
-        for (int p = 0; p < P; ++p)
-            c += sid[p] == e;
-        off[e] = c;
-        flag[e] = c > 0;
-    }
-    __syncthreads();
-    const int total = block_excl_scan(off, E);
-    for (int e = tid; e < E; e += nt) {
-        a.offsets[e] = off[e];
-        int k = off[e];
-        for (int p = 0; p < P; ++p)
-            if (sid[p] == e)
-                a.pairs[k++] = p;
-    }
-    if (tid == 0)
-        a.offsets[E] = total;
-    const int n_routed = block_excl_scan(flag, E);
-    const int sbase = a.has_shared ? 1 : 0;
-    for (int e = tid; e < E; e += nt) {
-        const int c = (e + 1 < E ? off[e + 1] : total) - off[e];
-        if (c > 0) {
-            Slot sl;
-            sl.expert = e;
-            sl.begin = off[e];
-            sl.count = c;
-            sl.pad = 0;
-            a.slots[sbase + flag[e]] = sl;
-        }
-    }
-    if (tid == 0) {
-        if (a.has_shared) {
-            Slot sl;
-            sl.expert = -1;
-            sl.begin = 0;
-            sl.count = a.T;
-            sl.pad = 0;
-            a.slots[0] = sl;
-        }
-        Counters ct;
-        ct.n_slots = sbase + n_routed;
-        ct.n_routed = n_routed;
-        ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
-        ct.n_items_down = ct.n_slots * a.down_blocks;
+        ct.n_rows = total + (a.has_shared ? a.T : 0);
+        ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
         *a.counters = ct;
     }
 }
@@ -634,206 +574,6 @@ __global__ void __launch_bounds__(1024) k_bucket(BucketArgs a)
         __syncthreads();
     }
     bucket_block(a, sid, sm);
-}
-
-// ---- decode selection with the whole CTA -----------------------------------------
-// The k-th pick of the sequential selection (repeatedly take the best remaining
-// candidate in the (value desc, index asc) order) is the candidate that exactly k others
-// beat. So each candidate counts the allowed candidates that beat it and, if that rank is
-// below top_k, writes itself to position rank. Groups are kept the same way (rank of the
-// group score below topk_group). Work is strided over (token, candidate) pairs, so any
-// block size serves. sm (floats): c [T][E] | group scores [T][32] | kept [T][32] (int) |
-// pick ids [T][32] (int) | pick s [T][32]. sids gets the T*K picked ids.
-__device__ __forceinline__ void top2_merge(float &m1, float &m2, float o1, float o2)
-{
-    // the two largest of the multiset {m1, m2, o1, o2}, given m1 >= m2 and o1 >= o2
-    if (o1 > m1) {
-        m2 = fmaxf(m1, o2);
-        m1 = o1;
-    } else {
-        m2 = fmaxf(m2, o1);
-    }
-}
-
-// rank of (v, e) among row[b0..b1) in the (value desc, index asc) order; b0, b1 and the
-// row start are multiples of 4 (float4 reads, four at a time)
-__device__ __forceinline__ int rank_in(const float *row, int b0, int b1, float v, int e)
-{
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-    const float4 *q = reinterpret_cast<const float4 *>(row);
-    for (int j = b0; j < b1; j += 4) {
-        const float4 x = q[j >> 2];
-        r0 += better(x.x, j, v, e);
-        r1 += better(x.y, j + 1, v, e);
-        r2 += better(x.z, j + 2, v, e);
-        r3 += better(x.w, j + 3, v, e);
-    }
-    return r0 + r1 + r2 + r3;
-}
-
-__device__ void select_block(const SelectArgs &a, float *sm, int32_t *sids)
-{
-    const int E = a.E, K = a.K, T = a.T, nt = blockDim.x, tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
-    const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
-    const int NG = sig ? a.n_group : 1, gs = E / NG;
-    const int Ep = (E + 3) & ~3;  // row stride (float4 aligned)
-    float *cs = sm;
-    float *gsc = cs + (size_t)T * Ep;
-    int *kept = reinterpret_cast<int *>(gsc + (size_t)T * 32);
-    int *pick = kept + (size_t)T * 32;
-    float *ps = reinterpret_cast<float *>(pick + (size_t)T * 32);
-    // written by other CTAs of this kernel: read at L2 (ld.global.cg), past this SM's L1
-    for (int i = tid; i < T * E; i += nt) {
-        const int t = i / E, e = i - t * E;
-        cs[t * Ep + e] = sig ? __ldcg(a.c + i) : __ldcg(a.logits + i);
-    }
-    __syncthreads();
-    if (sig) {
-        // group score = sum of the group's two largest c: one warp per (token, group)
-        for (int i = warp; i < T * NG; i += nwarps) {
-            const int t = i / NG, g = i - t * NG;
-            const float *row = cs + (size_t)t * Ep + g * gs;
-            float m1 = -INFINITY, m2 = -INFINITY;
-            for (int j = lane; j < gs; j += 32)
-                top2_merge(m1, m2, row[j], -INFINITY);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float o1 = __shfl_xor_sync(FULL, m1, o), o2 = __shfl_xor_sync(FULL, m2, o);
-                top2_merge(m1, m2, o1, o2);
-            }
-            if (lane == 0)
-                gsc[t * 32 + g] = gs == 1 ? m1 : m1 + m2;
-        }
-        __syncthreads();
-        for (int i = tid; i < T * NG; i += nt) {
-            const int t = i / NG, g = i - t * NG;
-            const float v = gsc[t * 32 + g];
-            int rank = 0;
-            for (int h = 0; h < NG; ++h)
-                rank += better(gsc[t * 32 + h], h, v, g);
-            kept[t * 32 + g] = rank < a.topk_group;
-        }
-        __syncthreads();
-    }
-    const bool vec = (gs & 3) == 0;
-    for (int i = tid; i < T * E; i += nt) {
-        const int t = i / E, e = i - t * E;
-        if (sig && !kept[t * 32 + e / gs])
-            continue;
-        const float *row = cs + (size_t)t * Ep;
-        const float v = row[e];
-        int rank = 0;
-        for (int g = 0; g < NG; ++g) {
-            if (sig && !kept[t * 32 + g])
-                continue;
-            if (vec) {
-                rank += rank_in(row, g * gs, (g + 1) * gs, v, e);
-            } else {
-                for (int j = g * gs; j < (g + 1) * gs; ++j)
-                    rank += better(row[j], j, v, e);
-            }
-        }
-        if (rank < K) {
-            pick[t * 32 + rank] = e;
-            ps[t * 32 + rank] = sig ? __ldcg(a.s + i) : v;
-        }
-    }
-    __syncthreads();
-    // weights: one warp per token, sums in selection order
-    for (int t = warp; t < T; t += nwarps) {
-        double m = 0.0, z = 1.0;
-        if (!sig) {
-            const float *l = cs + (size_t)t * Ep;
-            m = -INFINITY;
-            for (int i = lane; i < E; i += 32)
-                m = fmax(m, (double)l[i]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                m = fmax(m, __shfl_xor_sync(FULL, m, o));
-            z = 0.0;
-            for (int i = lane; i < E; i += 32)
-                z += exp((double)l[i] - m);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                z += __shfl_xor_sync(FULL, z, o);
-        }
-        float wt = 0.0f;
-        if (sig) {
-            // sigmoid weights in fp32: a compensated (TwoSum) sum of the k scores in
-            // selection order, then one division and the scale; within a few 1e-7 of the
-            // value computed in fp64 (fp64 is a slow, long-latency pipe here)
-            const float sv = lane < K ? ps[t * 32 + lane] : 0.0f;
-            float hi = 0.0f, lo = 0.0f;
-            for (int i = 0; i < K; ++i) {
-                const float x = __shfl_sync(FULL, sv, i);
-                const float u = hi + x, bb = u - hi;
-                lo += (hi - (u - bb)) + (x - bb);
-                hi = u;
-            }
-            const float sum = hi + lo;
-            wt = (a.norm_topk ? __fdiv_rn(sv, sum) : sv) * a.routed_scale;
-        } else {
-            double p = 0.0;
-            if (lane < K)
-                p = exp((double)ps[t * 32 + lane] - m) / z;
-            double sum = 0.0;
-            for (int i = 0; i < K; ++i)
-                sum += __shfl_sync(FULL, p, i);
-            if (a.norm_topk)
-                p = p / sum;
-            wt = (float)(p * (double)a.routed_scale);
-        }
-        if (lane < K) {
-            const int id = pick[t * 32 + lane];
-            a.ids[(long)t * K + lane] = id;
-            a.w[(long)t * K + lane] = wt;
-            sids[t * K + lane] = id;
-        }
-    }
-    __syncthreads();
-}
-
-__host__ __device__ size_t select_block_smem_bytes(int T, int E)
-{
-    return (size_t)T * ((E + 3) & ~3) * 4 + (size_t)T * 32 * 16;
-}
-
-// ---- decode routing in one kernel ---------------------------------------------------
-// Every CTA computes the logits (and sigmoid scores) of one expert for all T tokens and
-// quantises its share of x; the last CTA to finish (counted on a zeroed device counter)
-// selects the experts of every token and buckets the pairs, reading what the other CTAs
-// wrote from L2.
-__global__ void __launch_bounds__(256) k_route_decode(RouterArgs ra, SelectArgs sa, BucketArgs ba, int *done)
-{
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ int s_last;
-    const bool ok = route_logits_part(ra, smem_raw, &bar);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();  // this CTA's logits, scores and codes are visible device-wide
-        s_last = atomicAdd(done, 1) == (int)gridDim.x - 1;
-    }
-    __syncthreads();
-    if (!s_last || !ok)
-        return;
-    __threadfence();  // and the other CTAs' are visible to this one
-    // selection scratch, then the ids, then the bucketing counters (one after the other)
-    float *sel = reinterpret_cast<float *>(smem_raw);
-    int32_t *sids = reinterpret_cast<int32_t *>(sel + select_block_smem_bytes(sa.T, sa.E) / 4);
-    select_block(sa, sel, sids);
-    int *bsm = sids + ((sa.T * sa.K + 3) & ~3);
-    bucket_small(ba, sids, bsm);
-    if (threadIdx.x == 0)
-        *done = 0;  // ready for the next call
-}
-
-size_t route_decode_smem_bytes(int T, int K, int E, int d, int xt)
-{
-    const size_t logits = (size_t)d * 4 * (1 + xt);
-    const size_t last = select_block_smem_bytes(T, E) + 4 * (size_t)((T * K + 3) & ~3) + 8 * (size_t)E;
-    return logits > last ? logits : last;
 }
 
 }  // namespace clb

@@ -9,9 +9,11 @@ namespace clb {
 
 // Byte offsets (256-byte aligned) of the layer's intermediates in the workspace.
 struct WsLayout {
-    size_t err, counters, qx, qx_eo, sx, xc, logits, s, c, offsets, pairs, slots;
+    size_t err, counters, sync, qx, qx_eo, sx, xc, logits, s, c, offsets, pairs, slots;
     size_t hq, hq_eo, hs, hc, y;
     size_t xbf, hbf;  // prefill (T > DECODE_T_MAX): bf16 codes of x and of q8(h)
+    size_t nslots;      // slots at most: the shared expert + min(E, T*K) routed experts
+    size_t sync_bytes;  // decode kernel's claim counter | done_gu [nslots] | done_rb [d/32]
     size_t fmax, total;
 };
 
