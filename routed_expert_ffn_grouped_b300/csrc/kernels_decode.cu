@@ -5,8 +5,10 @@
 //
 // Expert matrices are stored in row blocks of 32 rows, group-major inside a block: the 16
 // bytes of one 32-column group of the block's 32 rows lie together (512 bytes), and the
-// whole block is one contiguous run. A work item is one row block of one expert slot: 32
-// rows of W1 and W3 for gate/up (one 32-group of h), or 32 rows of W2 for down.
+// whole block is one contiguous run. A work item of an expert slot is one row block of W1
+// and the same one of W3 for gate/up (one 32-group of h), or two neighbouring row blocks of
+// W2 for down (64 rows of y); either way a stage holds the same group range of two 32-row
+// blocks, so one code path computes both.
 //
 // Items are claimed from a device counter, in the order: the shared expert's gate/up
 // items, the routed slots' gate/up items, then the down items slot by slot. A CTA
@@ -16,8 +18,8 @@
 //
 // One CTA per SM, three roles. The producer warp claims items (two ahead, so a claim's
 // latency hides behind the copies of the items before) and streams each item through a
-// ring of shared-memory stages with 1-D bulk copies (a stage holds 32 group tiles of W1
-// and W3 or 64 of W2, with their scales: 40 KB), tagging each stage with the item and its
+// ring of shared-memory stages with 1-D bulk copies (a stage holds 32 group tiles of each
+// of the two row blocks, with their scales: 40 KB), tagging each stage with the item and its
 // position; completion is counted on a "full" mbarrier per stage. For a down item it
 // also copies the item's rows of q8(h) into one of a few h buffers, once the gate/up
 // items of its slot are done, ahead of the consumers. The consumer warps split each
@@ -42,11 +44,9 @@ namespace {
 
 constexpr int NC = 16;                       // consumer warps
 constexpr int NT = NC * 32;                  // consumer threads
-constexpr int GPW_GU = 2, GPW_DN = 4;        // groups per consumer warp and stage
-constexpr int SG_GU = NC * GPW_GU;           // group tiles per matrix and stage, gate/up
-constexpr int SG_DN = NC * GPW_DN;           // ... down
-constexpr int STAGE_BYTES = 2 * SG_GU * 640; // 2 matrices x 32 groups x (512 + 128) bytes
-static_assert(STAGE_BYTES == SG_DN * 640, "gate/up and down stages have one size");
+constexpr int GPW = 2;                       // groups per consumer warp and stage
+constexpr int SG = NC * GPW;                 // group tiles per matrix and stage
+constexpr int STAGE_BYTES = 2 * SG * 640;    // 2 matrices x 32 groups x (512 + 128) bytes
 constexpr int MAX_RING = 16;
 constexpr size_t SMEM_BUDGET = 227 * 1024;  // the largest opt-in dynamic shared memory of a CTA
 constexpr int NE_MAX = 4;                    // epilogue warps launched
@@ -84,8 +84,8 @@ struct ChunkDesc {
 
 // Shared memory beside the ring: see ring_layout().
 struct RingLayout {
-    size_t full, empty, hfull, hempty, cbar, tbar, pfull, pempty, tag, flags, ctab, desc, stab, ptab, wtab, act,
-        hbuf, part, total;
+    size_t full, empty, hfull, hempty, cbar, tbar, xbar, pfull, pempty, tag, flags, ctab, desc, stab, ptab, wtab,
+        act, hbuf, part, total;
     size_t hb;  // bytes of one h buffer
 };
 
@@ -95,17 +95,31 @@ __host__ __device__ __forceinline__ size_t route_scratch_bytes(int T, int E, int
     const size_t P = (size_t)T * K;
     size_t b = 8 * P + 16;  // picked ids, first-occurrence flags (+ alignment)
     if (select)
-        b += (size_t)T * ((E + 3) & ~3) * 4 + (size_t)T * 32 * 16;
+        b += 2 * (size_t)T * ((E + 3) & ~3) * 4 + (size_t)T * 32 * 16;
     return b;
 }
 
+// The x staging area: codes [TCH][d] | scales [TCH][d/32] | corrections [TCH][d/32], each
+// part starting on 16 bytes.
+__host__ __device__ __forceinline__ size_t x_sc_off(int d, int tch)
+{
+    return ((size_t)tch * d + 15) & ~size_t(15);
+}
+__host__ __device__ __forceinline__ size_t x_cr_off(int d, int tch)
+{
+    return x_sc_off(d, tch) + ((4 * (size_t)tch * (d / G) + 15) & ~size_t(15));
+}
+__host__ __device__ __forceinline__ size_t x_area_bytes(int d, int tch)
+{
+    return x_cr_off(d, tch) + ((4 * (size_t)tch * (d / G) + 15) & ~size_t(15));
+}
+
 // ring [ns][STAGE_BYTES] | full [ns] | empty [ns] | hfull [NH_MAX] | hempty [NH_MAX] |
-// consumer barrier | table barrier | pfull [NE_MAX] | pempty [NE_MAX] | stage tags [ns]
-// (int2) | flags (16 B) | counters | chunk descriptors [NE_MAX] | slot table [max_slots]
-// | pair list [T*K] | weights [T*K] | x staging area (codes [TCH][d] | scales [TCH][d/32]
-// | corrections [TCH][d/32]; routing scratch before the first gate/up item) | h buffers
-// [nh] (codes [TCH][fmax] | scales [TCH][hgs] | corrections [TCH][hgs]) | partial sums
-// [NBUF][NC][2][TCH][32].
+// consumer barrier | table barrier | x barrier | pfull [NE_MAX] | pempty [NE_MAX] | stage
+// tags [ns] (int2) | flags (16 B) | counters | chunk descriptors [NE_MAX] | slot table
+// [max_slots] | pair list [T*K] | weights [T*K] | x staging area | h buffers [nh] (codes
+// [TCH][fmax] | scales [TCH][hgs] | corrections [TCH][hgs]) | partial sums
+// [NBUF][NC][2][TCH][32] (before the first chunk: the routing scratch).
 __host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, int ns, int nh, int tch)
 {
     RingLayout L;
@@ -123,6 +137,7 @@ __host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, 
     L.hempty = take(8 * NH_MAX, 8);
     L.cbar = take(8, 8);
     L.tbar = take(8, 8);
+    L.xbar = take(8, 8);
     L.pfull = take(8 * NE_MAX, 8);
     L.pempty = take(8 * NE_MAX, 8);
     L.tag = take(8 * (size_t)ns, 8);
@@ -132,19 +147,19 @@ __host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, 
     L.stab = take(sizeof(SlotInfo) * (size_t)a.max_slots, 16);
     L.ptab = take(4 * (size_t)P, 16);
     L.wtab = take(4 * (size_t)P, 16);
-    const size_t xbytes = (size_t)tch * a.d + 8 * (size_t)tch * (a.d / G);
-    const size_t rbytes = route_scratch_bytes(a.T, a.E, a.K, !a.ids_given);
-    L.act = take(xbytes > rbytes ? xbytes : rbytes, 16);
+    L.act = take(x_area_bytes(a.d, tch), 16);
     L.hb = round_up(tch * a.fmax + 8 * tch * a.hgs, 16);
     L.hbuf = take(L.hb * nh, 16);
-    L.part = take(4 * (size_t)nbuf_for(tch) * NC * 2 * tch * 32, 16);
+    const size_t pbytes = 4 * (size_t)nbuf_for(tch) * NC * 2 * tch * 32;
+    const size_t rbytes = route_scratch_bytes(a.T, a.E, a.K, !a.ids_given);
+    L.part = take(pbytes > rbytes ? pbytes : rbytes, 16);  // routing scratch before the first chunk
     L.total = o;
     return L;
 }
 
 struct RingSmem {
     unsigned char *ring;
-    uint64_t *full, *empty, *hfull, *hempty, *cbar, *tbar, *pfull, *pempty;
+    uint64_t *full, *empty, *hfull, *hempty, *cbar, *tbar, *xbar, *pfull, *pempty;
     int2 *tag;
     int *flags;  // [0] abort, [1] valid pairs, [2] distinct experts
     Counters *ctab;
@@ -168,6 +183,7 @@ __device__ __forceinline__ RingSmem carve(unsigned char *sm, const DecodeArgs &a
     s.hempty = reinterpret_cast<uint64_t *>(sm + L.hempty);
     s.cbar = reinterpret_cast<uint64_t *>(sm + L.cbar);
     s.tbar = reinterpret_cast<uint64_t *>(sm + L.tbar);
+    s.xbar = reinterpret_cast<uint64_t *>(sm + L.xbar);
     s.pfull = reinterpret_cast<uint64_t *>(sm + L.pfull);
     s.pempty = reinterpret_cast<uint64_t *>(sm + L.pempty);
     s.tag = reinterpret_cast<int2 *>(sm + L.tag);
@@ -229,10 +245,10 @@ __device__ __forceinline__ DecItem work_item(const DecodeArgs &a, const SlotInfo
             it.rb = r % nrb;
         }
     } else {
-        const int r = idx - n_gu, nmb = a.d / G;
+        const int r = idx - n_gu, npairs = (a.d / G + 1) / 2;
         it.mode = MODE_DOWN;
-        it.slot = r / nmb;
-        it.rb = r % nmb;
+        it.slot = r / npairs;
+        it.rb = 2 * (r % npairs);  // first of the two row blocks
     }
     if (a.has_shared && it.slot == 0) {
         it.is_shared = 1;
@@ -307,14 +323,17 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
     const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
     const int NG = sig ? a.n_group : 1, gs = E / NG;
     const int Ep = (E + 3) & ~3;
-    float *cs = scr;
-    float *gsc = cs + (size_t)T * Ep;
+    float *cs = scr;                   // c (sigmoid) or logits [T][Ep]
+    float *ss = cs + (size_t)T * Ep;   // s [T][Ep] (sigmoid)
+    float *gsc = ss + (size_t)T * Ep;  // group scores [T][32]
     int *kept = reinterpret_cast<int *>(gsc + (size_t)T * 32);
     int *pick = kept + (size_t)T * 32;
     float *ps = reinterpret_cast<float *>(pick + (size_t)T * 32);
     for (int i = tid; i < T * E; i += NT) {
         const int t = i / E, e = i - t * E;
         cs[t * Ep + e] = sig ? __ldcg(a.rc + i) : __ldcg(a.logits + i);
+        if (sig)
+            ss[t * Ep + e] = __ldcg(a.rs + i);
     }
     if (!consumers_sync(s, cph, lane))
         return false;
@@ -346,46 +365,48 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
         if (!consumers_sync(s, cph, lane))
             return false;
     }
+    // rank of each allowed candidate, two adjacent threads a candidate (each counts over
+    // every other allowed group), added with one shuffle
     const bool vec = (gs & 3) == 0;
-    for (int i = tid; i < T * E; i += NT) {
-        const int t = i / E, e = i - t * E;
-        if (sig && !kept[t * 32 + e / gs])
-            continue;
-        const float *row = cs + (size_t)t * Ep;
-        const float v = row[e];
+    const int half = tid & 1;
+    for (int base = 0; base < T * E; base += NT / 2) {
+        const int i = base + (tid >> 1);
+        const bool live = i < T * E;
+        const int t = live ? i / E : 0, e = live ? i - t * E : 0;
+        const bool allowed = live && (!sig || kept[t * 32 + e / gs]);
         int rank = 0;
-        for (int g = 0; g < NG; ++g) {
-            if (sig && !kept[t * 32 + g])
-                continue;
-            if (vec) {
-                // four independent counts over float4 reads (rows start 16-byte aligned)
-                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-                const float4 *q4 = reinterpret_cast<const float4 *>(row);
-#pragma unroll 4
-                for (int j = g * gs; j < (g + 1) * gs; j += 4) {
-                    const float4 x = q4[j >> 2];
-                    r0 += beats(x.x, j, v, e);
-                    r1 += beats(x.y, j + 1, v, e);
-                    r2 += beats(x.z, j + 2, v, e);
-                    r3 += beats(x.w, j + 3, v, e);
+        if (allowed) {
+            const float *row = cs + (size_t)t * Ep;
+            const float v = row[e];
+            for (int g = half; g < NG; g += 2) {
+                if (sig && !kept[t * 32 + g])
+                    continue;
+                if (vec) {
+                    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+                    const float4 *q4 = reinterpret_cast<const float4 *>(row);
+                    for (int j = g * gs; j < (g + 1) * gs; j += 4) {
+                        const float4 x = q4[j >> 2];
+                        r0 += beats(x.x, j, v, e);
+                        r1 += beats(x.y, j + 1, v, e);
+                        r2 += beats(x.z, j + 2, v, e);
+                        r3 += beats(x.w, j + 3, v, e);
+                    }
+                    rank += r0 + r1 + r2 + r3;
+                } else {
+                    for (int j = g * gs; j < (g + 1) * gs; ++j)
+                        rank += beats(row[j], j, v, e);
                 }
-                rank += r0 + r1 + r2 + r3;
-            } else {
-                for (int j = g * gs; j < (g + 1) * gs; ++j)
-                    rank += beats(row[j], j, v, e);
             }
         }
-        if (rank < K) {
+        rank += __shfl_xor_sync(FULL, rank, 1);
+        if (allowed && half == 0 && rank < K) {
             pick[t * 32 + rank] = e;
-            ps[t * 32 + rank] = sig ? __ldcg(a.rs + i) : v;
+            ps[t * 32 + rank] = sig ? ss[t * Ep + e] : cs[t * Ep + e];
         }
     }
     if (!consumers_sync(s, cph, lane))
         return false;
-    // weights: one warp per token; with at most 32 pairs warp 0 takes every token, and
-    // the bucketing that follows stays in that warp
-    const bool one_warp = T * K <= 32;
-    for (int t = one_warp ? (warp == 0 ? 0 : T) : warp; t < T; t += one_warp ? 1 : NC) {
+    for (int t = warp; t < T; t += NC) {
         double m = 0.0, z = 1.0;
         if (!sig) {
             const float *l = cs + (size_t)t * Ep;
@@ -436,7 +457,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             }
         }
     }
-    return one_warp || consumers_sync(s, cph, lane);
+    return consumers_sync(s, cph, lane);
 }
 
 // Slot table, counters and (CTA 0) the workspace copies from the pair ids, for at most 32
@@ -510,7 +531,7 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
         ct.n_slots = sbase + n_routed;
         ct.n_routed = n_routed;
         ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
-        ct.n_items_down = ct.n_slots * (a.d / G);
+        ct.n_items_down = ct.n_slots * ((a.d / G + 1) / 2);
         ct.n_rows = n_valid + (a.has_shared ? T : 0);
         ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
         *s.ctab = ct;
@@ -535,9 +556,10 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
 __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph, int tid, int warp, int lane)
 {
     const int T = a.T, K = a.K, E = a.E, P = T * K;
-    int *sids = reinterpret_cast<int *>(s.act);
+    int *sids = reinterpret_cast<int *>(s.part);
     int *first = sids + P;
-    float *scr = reinterpret_cast<float *>(s.act + ((8 * (size_t)P + 15) & ~size_t(15)));
+    float *scr = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(s.part) +
+                                           ((8 * (size_t)P + 15) & ~size_t(15)));
     if (tid == 0)
         s.flags[1] = s.flags[2] = 0;
     if (a.ids_given) {
@@ -630,7 +652,7 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
         ct.n_slots = sbase + n_routed;
         ct.n_routed = n_routed;
         ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
-        ct.n_items_down = ct.n_slots * (a.d / G);
+        ct.n_items_down = ct.n_slots * ((a.d / G + 1) / 2);
         ct.n_rows = s.flags[1] + (a.has_shared ? T : 0);
         ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
         *s.ctab = ct;
@@ -652,14 +674,12 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
 // Partial dots of one stage: consumer warp w takes groups w, w + NC, ... of the stage.
 // Activation row t of the chunk sits at row rows[t] of the staged codes (row stride
 // cstride bytes), scales and corrections (gstride groups a row).
-template <int MODE, int TCH>
+template <int TCH>
 __device__ __forceinline__ void consume(const unsigned char *stg, const int8_t *codes, const float *sc,
                                         const int *corr, int cstride, int gstride, const int (&rows)[TCH], int ng,
                                         int g0, int nt, int warp, int lane, float (&acc)[2][TCH])
 {
-    constexpr int M = MODE == MODE_GATEUP ? 2 : 1;
-    constexpr int SG = MODE == MODE_GATEUP ? SG_GU : SG_DN;
-    constexpr int GPW = MODE == MODE_GATEUP ? GPW_GU : GPW_DN;
+    constexpr int M = 2;
     constexpr int scale_off = M * SG * 512;
     const int n = min(SG, ng - g0);
 #pragma unroll
@@ -744,10 +764,25 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
         ahead = atomicAdd(a.claim, 1);  // used two items from now
         const DecItem it = work_item(a, s.stab, n_gu, idx);
         const bool gu = it.mode == MODE_GATEUP;
-        const int SG = gu ? SG_GU : SG_DN;
         const int ng = it.kdim / G, spi = (ng + SG - 1) / SG;
         const int nq = spi * ((it.count + TCH - 1) / TCH);
-        const size_t blk = (size_t)it.rb * ng;  // first group tile of the row block
+        // the two row blocks: W1 and W3 at rb (gate/up), or W2 at rb and rb + 1 (down; the
+        // second absent past the last row block)
+        const unsigned char *wa, *wb;
+        const float *sa_, *sb_;
+        bool two = true;
+        if (gu) {
+            wa = it.ex.w1 + (size_t)it.rb * ng * 512;
+            wb = it.ex.w3 + (size_t)it.rb * ng * 512;
+            sa_ = it.ex.s1 + (size_t)it.rb * ng * 32;
+            sb_ = it.ex.s3 + (size_t)it.rb * ng * 32;
+        } else {
+            two = it.rb + 1 < a.d / G;
+            wa = it.ex.w2 + (size_t)it.rb * ng * 512;
+            wb = wa + (size_t)ng * 512;
+            sa_ = it.ex.s2 + (size_t)it.rb * ng * 32;
+            sb_ = sa_ + (size_t)ng * 32;
+        }
         for (int q = 0; q < nq && run; ++q) {
             const int ch = q / spi, k = q % spi;
             int flag = 0;
@@ -796,17 +831,12 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
             const int g0 = k * SG, n = min(SG, ng - g0);
             unsigned char *dst = s.ring + (size_t)slot * STAGE_BYTES;
             s.tag[slot] = make_int2(idx, q | flag);
-            if (gu) {
-                mbar_arrive_expect_tx(&s.full[slot], (uint32_t)(2 * n * 640));
-                bulk_g2s_hint(dst, it.ex.w1 + (blk + g0) * 512, n * 512, &s.full[slot], pol);
-                bulk_g2s_hint(dst + SG_GU * 512, it.ex.w3 + (blk + g0) * 512, n * 512, &s.full[slot], pol);
-                bulk_g2s_hint(dst + 2 * SG_GU * 512, it.ex.s1 + (blk + g0) * 32, n * 128, &s.full[slot], pol);
-                bulk_g2s_hint(dst + 2 * SG_GU * 512 + SG_GU * 128, it.ex.s3 + (blk + g0) * 32, n * 128,
-                              &s.full[slot], pol);
-            } else {
-                mbar_arrive_expect_tx(&s.full[slot], (uint32_t)(n * 640));
-                bulk_g2s_hint(dst, it.ex.w2 + (blk + g0) * 512, n * 512, &s.full[slot], pol);
-                bulk_g2s_hint(dst + SG_DN * 512, it.ex.s2 + (blk + g0) * 32, n * 128, &s.full[slot], pol);
+            mbar_arrive_expect_tx(&s.full[slot], (uint32_t)((two ? 2 : 1) * n * 640));
+            bulk_g2s_hint(dst, wa + (size_t)g0 * 512, n * 512, &s.full[slot], pol);
+            bulk_g2s_hint(dst + 2 * SG * 512, sa_ + (size_t)g0 * 32, n * 128, &s.full[slot], pol);
+            if (two) {
+                bulk_g2s_hint(dst + SG * 512, wb + (size_t)g0 * 512, n * 512, &s.full[slot], pol);
+                bulk_g2s_hint(dst + 2 * SG * 512 + SG * 128, sb_ + (size_t)g0 * 32, n * 128, &s.full[slot], pol);
             }
             ++st;
         }
@@ -860,10 +890,14 @@ __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int 
                     a.hc[r * a.hgs + rb] = 8 * sq;
                 }
             } else {
-                float y = 0.0f;
-                for (int w = 0; w < NC; ++w)
-                    y += pb[(w * 2 * TCH + t) * 32 + lane];
-                a.y[r * a.d + (long)rb * G + lane] = y;
+                float y0 = 0.0f, y1 = 0.0f;
+                for (int w = 0; w < NC; ++w) {
+                    y0 += pb[((w * 2 + 0) * TCH + t) * 32 + lane];
+                    y1 += pb[((w * 2 + 1) * TCH + t) * 32 + lane];
+                }
+                a.y[r * a.d + (long)rb * G + lane] = y0;
+                if (rb + 1 < a.d / G)
+                    a.y[r * a.d + (long)(rb + 1) * G + lane] = y1;
             }
         }
         __syncwarp();
@@ -876,20 +910,22 @@ __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int 
                 atomicAdd(a.done_gu + slot, nt);
             continue;
         }
-        int last = 0;
-        if (lane == 0) {
-            last = atomicAdd(a.done_rb + rb, nt) + nt == s.ctab->n_rows;
-            if (last)
-                __threadfence();
-        }
-        if (__shfl_sync(FULL, last, 0)) {
-            // every row of this block of d is in: combine it for all tokens
-            const long col = (long)rb * G + lane;
-            for (int t = 0; t < a.T; ++t) {
-                float o = a.has_shared ? __ldcg(a.y + ((long)a.T * a.K + t) * a.d + col) : 0.0f;
-                for (int i = 0; i < a.K; ++i)
-                    o = fmaf(s.wtab[t * a.K + i], __ldcg(a.y + ((long)t * a.K + i) * a.d + col), o);
-                a.out[(long)t * a.d + col] = o;
+        // each of the item's row blocks of d: the epilogue that completes it combines it
+        for (int b = rb; b < rb + 2 && b < a.d / G; ++b) {
+            int last = 0;
+            if (lane == 0) {
+                last = atomicAdd(a.done_rb + b, nt) + nt == s.ctab->n_rows;
+                if (last)
+                    __threadfence();
+            }
+            if (__shfl_sync(FULL, last, 0)) {
+                const long col = (long)b * G + lane;
+                for (int t = 0; t < a.T; ++t) {
+                    float o = a.has_shared ? __ldcg(a.y + ((long)a.T * a.K + t) * a.d + col) : 0.0f;
+                    for (int i = 0; i < a.K; ++i)
+                        o = fmaf(s.wtab[t * a.K + i], __ldcg(a.y + ((long)t * a.K + i) * a.d + col), o);
+                    a.out[(long)t * a.d + col] = o;
+                }
             }
         }
     }
@@ -905,16 +941,27 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
     const int tid = threadIdx.x;
     uint32_t cph = 0;  // consumer barrier phase
     grid_dep_wait();   // router scores and q8 of x (or the given ids) are in
+    // x codes of all T tokens, when one chunk holds them, come in with bulk copies while
+    // the CTA routes
+    const bool x_all = a.T <= TCH;
+    const bool x_bulk = x_all && ((long)a.T * a.d) % 128 == 0;
+    int8_t *xcodes = reinterpret_cast<int8_t *>(s.act);
+    float *xsc = reinterpret_cast<float *>(s.act + x_sc_off(a.d, TCH));
+    int *xcr = reinterpret_cast<int *>(s.act + x_cr_off(a.d, TCH));
+    if (x_bulk && tid == 0) {
+        fence_proxy_async_global();
+        const uint32_t nc = (uint32_t)(a.T * a.d), ns = (uint32_t)(4 * a.T * (a.d / G));
+        mbar_arrive_expect_tx(s.xbar, nc + 2 * ns);
+        bulk_g2s(xcodes, a.xq_eo, nc, s.xbar);
+        bulk_g2s(xsc, a.xs, ns, s.xbar);
+        bulk_g2s(xcr, a.xc, ns, s.xbar);
+    }
     if (!route_cta(a, s, cph, tid, warp, lane))
         return;
     if (tid == 0)
         mbar_arrive(s.tbar);  // the producer may read the table now
     const int n_gu = s.ctab->n_items_gateup;
     // the x staging area: all T tokens at once when they fit a chunk, else the chunk's
-    int8_t *xcodes = reinterpret_cast<int8_t *>(s.act);
-    float *xsc = reinterpret_cast<float *>(s.act + (size_t)TCH * a.d);
-    int *xcr = reinterpret_cast<int *>(xsc + (size_t)TCH * (a.d / G));
-    const bool x_all = a.T <= TCH;
     bool x_staged = false;
     int xrows[TCH];  // token of each staged x row
 #pragma unroll
@@ -962,7 +1009,6 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
         if (tag.x != cur) {
             cur = tag.x;
             it = work_item(a, s.stab, n_gu, cur);
-            const int SG = it.mode == MODE_GATEUP ? SG_GU : SG_DN;
             ng = it.kdim / G;
             spi = (ng + SG - 1) / SG;
         }
@@ -977,6 +1023,17 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
                 for (int t = 0; t < TCH; ++t) {
                     const int p = __shfl_sync(FULL, orow, t);
                     tok[t] = t < nt ? (it.is_shared ? c0 + t : p / a.K) : -1;
+                }
+                if (x_bulk && !x_staged) {
+                    if (!mbar_wait(s.xbar, 0)) {
+                        if (lane == 0)
+                            set_abort(a, s);
+                        return;
+                    }
+                    x_staged = true;
+#pragma unroll
+                    for (int t = 0; t < TCH; ++t)
+                        xrows[t] = t < a.T ? t : -1;
                 }
                 bool same = x_staged;
                 if (!x_all) {
@@ -1044,13 +1101,13 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
         }
         const unsigned char *stg = s.ring + (size_t)slot * STAGE_BYTES;
         if (it.mode == MODE_GATEUP) {
-            consume<MODE_GATEUP, TCH>(stg, xcodes, xsc, xcr, a.d, a.d / G, rows, ng, k * SG_GU, nt, warp, lane, acc);
+            consume<TCH>(stg, xcodes, xsc, xcr, a.d, a.d / G, rows, ng, k * SG, nt, warp, lane, acc);
         } else {
             const unsigned char *hb = s.hbuf + (size_t)cur_h * s.hb;
             const int8_t *hcodes = reinterpret_cast<const int8_t *>(hb);
             const float *hsc = reinterpret_cast<const float *>(hb + (size_t)TCH * a.fmax);
             const int *hcr = reinterpret_cast<const int *>(hsc + (size_t)TCH * a.hgs);
-            consume<MODE_DOWN, TCH>(stg, hcodes, hsc, hcr, a.fmax, a.hgs, rows, ng, k * SG_DN, nt, warp, lane, acc);
+            consume<TCH>(stg, hcodes, hsc, hcr, a.fmax, a.hgs, rows, ng, k * SG, nt, warp, lane, acc);
         }
         __syncwarp();
         if (lane == 0)
@@ -1062,13 +1119,12 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
         const int b = chunk % NBUF;
         if (!buffer_free(b))
             return;
-        const int M = it.mode == MODE_GATEUP ? 2 : 1;
         float *pb = s.part + (size_t)b * PART;
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
             for (int t = 0; t < TCH; ++t)
-                if (m < M && t < nt)
+                if (t < nt)
                     pb[((warp * 2 + m) * TCH + t) * 32 + lane] = acc[m][t];
         if (warp == 0) {
             ChunkDesc *dp = s.desc + b;
@@ -1109,6 +1165,7 @@ __global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs
         }
         mbar_init(s.cbar, NC);
         mbar_init(s.tbar, 1);
+        mbar_init(s.xbar, 1);
         for (int i = 0; i < NBUF; ++i) {
             mbar_init(&s.pfull[i], NC);
             mbar_init(&s.pempty[i], 1);
