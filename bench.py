@@ -166,14 +166,18 @@ class ClockSampler:
 
 
 def dist_setup(torch):
+    """World, rank and local rank from the launcher's environment; for N > 1 one process
+    group over all ranks (NCCL with GPUs, gloo without)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    gpu = torch.cuda.is_available()
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
+        if gpu:
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if gpu else "gloo")
+    elif gpu:
         torch.cuda.set_device(0)
     return world, rank, local
 
@@ -185,12 +189,20 @@ def barrier(torch, world):
 
 
 def allreduce_max(torch, world, v: float) -> float:
+    """The largest v over the ranks (every rank gets it)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank runs its own replica of the layer on its own tokens,
+    so the job processes world x tokens_per_rank x steps tokens in the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_ms / 1e3)
 
 
 def blob_bytes(spec, f):
@@ -496,7 +508,7 @@ def run_colibri(args):
     barrier(torch, world)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = allreduce_max(torch, world, float(sum(step_ms)))
-    value = world * T * K / (total_ms / 1e3)
+    value = weak_scaling_value(world, T, K, total_ms)
 
     # informational: the same replays without the L2 flush between them (what back-to-back
     # layers of a model see: weights still stream from HBM, code and small tables stay warm)

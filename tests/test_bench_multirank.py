@@ -1,0 +1,69 @@
+"""The multi-rank harness of bench.py on CPU: two gloo ranks set up the process group from
+the launcher's environment, meet at the barrier, agree on the slowest rank's time, and
+report the whole-job (weak-scaling) throughput; the reference arm runs on rank 0 only."""
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank: int, world: int, port: int, out):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    w, r, _ = bench.dist_setup(torch)
+    bench.barrier(torch, w)
+    my_ms = 10.0 + 5.0 * r                      # rank 1 is the slow one
+    mx = bench.allreduce_max(torch, w, my_ms)
+    val = bench.weak_scaling_value(w, 4, 20, mx)
+    out.put((r, w, mx, val))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_agree_on_the_slowest_time():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    got.sort()
+    assert [g[0] for g in got] == [0, 1] and all(g[1] == 2 for g in got)
+    assert all(g[2] == pytest.approx(15.0) for g in got)          # max over ranks
+    # 2 ranks x 4 tokens x 20 steps in the slowest rank's 15 ms
+    assert all(g[3] == pytest.approx(2 * 4 * 20 / 0.015) for g in got)
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.allreduce_max(None, 1, 3.5) == 3.5
+    assert bench.weak_scaling_value(1, 1, 10, 1.0) == pytest.approx(10_000.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
+    """Under torchrun the oracle arm is rank 0's alone: rank 1 returns at once (no output)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("RANK", "1")
+    class Args:  # what run_reference would read after its rank check
+        workload, steps, warmup, seed = "glm52_decode_t1", 1, 0, 0
+    assert bench.run_reference(Args()) is None
