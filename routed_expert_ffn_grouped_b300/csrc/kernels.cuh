@@ -85,8 +85,9 @@ struct DecodeArgs {
     int *claim, *done_gu, *done_rb;
     int *err;
     int max_slots;  // the shared expert + min(E, T*K) routed slots
-    // set by launch_decode: ring stages, h buffers, tokens per chunk, groups per h row
-    int ring, nh, tch, hgs;
+    // set by launch_decode: ring stages, h buffers, partial-sum buffers (= epilogue warps),
+    // tokens per chunk, groups per h row
+    int ring, nh, nbuf, tch, hgs;
 };
 
 // One persistent launch for a decode step's routing (selection unless ids_given, and

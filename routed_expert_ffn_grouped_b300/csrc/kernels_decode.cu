@@ -53,11 +53,6 @@ constexpr int NE_MAX = 4;                    // epilogue warps launched
 constexpr int NH_MAX = 3;                    // h buffers at most
 constexpr int TAG_NEW_H = 1 << 20;           // stage tag: this chunk starts a new h buffer
 
-// Partial-sum buffers (and epilogue warps, one per buffer) by tokens per chunk.
-__host__ __device__ constexpr int nbuf_for(int tch)
-{
-    return tch <= 2 ? 4 : 2;
-}
 
 __host__ __device__ constexpr int round_up(int v, int m)
 {
@@ -120,7 +115,7 @@ __host__ __device__ __forceinline__ size_t x_area_bytes(int d, int tch)
 // [max_slots] | pair list [T*K] | weights [T*K] | x staging area | h buffers [nh] (codes
 // [TCH][fmax] | scales [TCH][hgs] | corrections [TCH][hgs]) | partial sums
 // [NBUF][NC][2][TCH][32] (before the first chunk: the routing scratch).
-__host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, int ns, int nh, int tch)
+__host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, int ns, int nh, int nbuf, int tch)
 {
     RingLayout L;
     const int P = a.T * a.K;
@@ -150,7 +145,7 @@ __host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, 
     L.act = take(x_area_bytes(a.d, tch), 16);
     L.hb = round_up(tch * a.fmax + 8 * tch * a.hgs, 16);
     L.hbuf = take(L.hb * nh, 16);
-    const size_t pbytes = 4 * (size_t)nbuf_for(tch) * NC * 2 * tch * 32;
+    const size_t pbytes = 4 * (size_t)nbuf * NC * 2 * tch * 32;
     const size_t rbytes = route_scratch_bytes(a.T, a.E, a.K, !a.ids_given);
     L.part = take(pbytes > rbytes ? pbytes : rbytes, 16);  // routing scratch before the first chunk
     L.total = o;
@@ -174,7 +169,7 @@ struct RingSmem {
 
 __device__ __forceinline__ RingSmem carve(unsigned char *sm, const DecodeArgs &a, int tch)
 {
-    const RingLayout L = ring_layout(a, a.ring, a.nh, tch);
+    const RingLayout L = ring_layout(a, a.ring, a.nh, a.nbuf, tch);
     RingSmem s;
     s.ring = sm;
     s.full = reinterpret_cast<uint64_t *>(sm + L.full);
@@ -457,7 +452,8 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             }
         }
     }
-    return consumers_sync(s, cph, lane);
+    // one token: warp 0 wrote every pick and goes on to bucket them itself
+    return (T == 1 && T * K <= 32) || consumers_sync(s, cph, lane);
 }
 
 // Slot table, counters and (CTA 0) the workspace copies from the pair ids, for at most 32
@@ -935,7 +931,7 @@ __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int 
 template <int TCH>
 __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, int lane)
 {
-    constexpr int NBUF = nbuf_for(TCH);
+    const int NBUF = a.nbuf;
     constexpr int PART = NC * 2 * TCH * 32;
     const int NS = a.ring, NH = a.nh;
     const int tid = threadIdx.x;
@@ -1149,7 +1145,7 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
 template <int TCH>
 __global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs a)
 {
-    constexpr int NBUF = nbuf_for(TCH);
+    const int NBUF = a.nbuf;
     static_assert(TCH <= 8, "chunk descriptors hold 8 rows");
     extern __shared__ __align__(128) unsigned char sm[];
     const RingSmem s = carve(sm, a, TCH);
@@ -1193,25 +1189,28 @@ template <int TCH>
 cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
 {
     auto fn = k_decode<TCH>;
-    // the most 40 KB ring stages beside the rest, with 3 h buffers if that leaves 5
-    // stages, else 2
+    // partial-sum buffers (= epilogue warps): 4 for chunks of at most 2 tokens, else 2;
+    // then the most 40 KB ring stages beside the rest, with 3 h buffers if that still
+    // leaves 4 stages, else 2 (measured: more buffers beat a fifth stage)
+    const int best_nb = TCH <= 2 ? 4 : 2;
     int best_ns = 0, best_nh = 2;
     for (int nh = NH_MAX; nh >= 2; --nh) {
         int ns = MAX_RING;
-        while (ns >= 2 && ring_layout(a, ns, nh, TCH).total > SMEM_BUDGET)
+        while (ns >= 2 && ring_layout(a, ns, nh, best_nb, TCH).total > SMEM_BUDGET)
             --ns;
         if (ns > best_ns) {
             best_ns = ns;
             best_nh = nh;
         }
-        if (ns >= 5)
+        if (ns >= 4)
             break;
     }
     if (best_ns < 2)
         return cudaErrorInvalidValue;
     a.ring = best_ns;
     a.nh = best_nh;
-    const size_t smem = ring_layout(a, a.ring, a.nh, TCH).total;
+    a.nbuf = best_nb;
+    const size_t smem = ring_layout(a, a.ring, a.nh, a.nbuf, TCH).total;
     int dev = 0, n_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
@@ -1257,8 +1256,9 @@ cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
     if (a.T <= 0)
         return cudaSuccess;
     a.hgs = decode_hgs(a.fmax);
-    const int tmax = a.T < 8 ? a.T : 8;
-    a.tch = tmax <= 1 ? 1 : tmax <= 2 ? 2 : tmax <= 4 ? 4 : 8;
+    // tokens per chunk: up to 4 (a slot with more tokens streams its weights once per
+    // chunk, but the smaller x, h and partial-sum areas leave room for a deeper ring)
+    a.tch = a.T <= 1 ? 1 : a.T <= 2 ? 2 : 4;
     switch (a.tch) {
     case 1: return launch_tch<1>(a, s);
     case 2: return launch_tch<2>(a, s);
