@@ -1146,7 +1146,7 @@ template <int TCH>
 __global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs a)
 {
     const int NBUF = a.nbuf;
-    static_assert(TCH <= 8, "chunk descriptors hold 8 rows");
+    static_assert(TCH <= 8, "chunk descriptors hold 8 rows");  // launched with 1, 2 or 4
     extern __shared__ __align__(128) unsigned char sm[];
     const RingSmem s = carve(sm, a, TCH);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1262,8 +1262,7 @@ cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
     switch (a.tch) {
     case 1: return launch_tch<1>(a, s);
     case 2: return launch_tch<2>(a, s);
-    case 4: return launch_tch<4>(a, s);
-    default: return launch_tch<8>(a, s);
+    default: return launch_tch<4>(a, s);
     }
 }
 
