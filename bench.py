@@ -65,6 +65,11 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--hot-slots", type=int, default=0,
+                   help="glm52_stream_8l: cache slots held by the most used experts (0: plain LRU)")
+    p.add_argument("--cache-sim", action="store_true",
+                   help="glm52_stream_8l: hit rates of the cache policy for several hot-set sizes, "
+                        "simulated on the host (no GPU)")
     p.add_argument("--predictor", default="previous", choices=["previous", "lookahead"],
                    help="expert streaming: next-layer prefetch from an emulated router lookahead "
                         "that names each true id with probability 0.716, or the previous step's ids")
@@ -306,6 +311,55 @@ STREAM_SLOTS = 512
 LOOKAHEAD_ACCURACY = 0.716   # next-layer routing predictability stated by the pages
 
 
+def stream_ops(ids_np, guess, predictor: str, n_exp: int, steps: int):
+    """The cache operations of the streaming run, as colibri_lru_trace ops: per step and
+    layer a lookup batch (kind 0, then kind 1 per id) and the next layer's prefetch
+    (kind 2). Returns kinds, keys and the step of each op."""
+    L_ = ids_np.shape[1]
+    kinds, keys, step = [], [], []
+    for s in range(steps):
+        for l in range(L_):
+            kinds.append(0); keys.append(0); step.append(s)
+            for e in ids_np[s, l]:
+                kinds.append(1); keys.append(l * n_exp + int(e)); step.append(s)
+            nl, ns = (l + 1, s) if l + 1 < L_ else (0, s + 1)
+            if predictor == "lookahead":
+                pre = np.unique(guess[ns, nl])
+            elif ns - 1 >= 0:
+                pre = ids_np[ns - 1, nl]
+            else:
+                pre = []
+            for e in pre:
+                kinds.append(2); keys.append(nl * n_exp + int(e)); step.append(s)
+    return np.array(kinds, np.int32), np.array(keys, np.int64), np.array(step)
+
+
+def run_cache_sim(args):
+    """Hit rates of the expert cache's policy on the streaming workload's ids, for several
+    hot-set sizes, through the library's host-only trace of the policy."""
+    from routed_expert_ffn_grouped_b300 import colibri as C
+    spec, L_ = synth.GLM52, STREAM_LAYERS
+    K, W = args.steps, args.warmup
+    ids_np, _ = synth.streaming_ids(spec, args.seed, L_, W + K + 1)
+    prng = np.random.default_rng([args.seed, 99])
+    guess = ids_np.copy()
+    wrong = prng.random(ids_np.shape) >= LOOKAHEAD_ACCURACY
+    guess[wrong] = prng.integers(0, spec.n_exp, int(wrong.sum()))
+    kinds, keys, step = stream_ops(ids_np, guess, args.predictor, spec.n_exp, W + K)
+    timed = (kinds == 1) & (step >= W)
+    rates = {}
+    for n_hot in (0, 64, 128, 256, 384, STREAM_SLOTS - spec.top_k):
+        res = C.colibri_lru_trace_hot(STREAM_SLOTS, n_hot, kinds, keys)
+        rates[str(n_hot)] = float((res[timed] == 1).mean())
+    line = {"metric": "expert cache hit rate (host simulation of the policy)", "unit": "fraction",
+            "higher_is_better": True, "data": "synthetic",
+            "config": {"workload": args.workload, "layers": L_, "n_exp": spec.n_exp, "top_k": spec.top_k,
+                       "hbm_slots": STREAM_SLOTS, "hot_slots": args.hot_slots, "reuse": 0.7, "steps": K, "warmup": W,
+                       "predictor": args.predictor},
+            "hit_rate_by_hot_slots": rates}
+    print(json.dumps(line), flush=True)
+
+
 def run_stream(args):
     """Decode T=1 through a stack of GLM-5.2-shaped layers whose routed experts live in
     pinned host memory (2048 blobs, ~48 GB) behind an HBM LRU cache of 512 slots
@@ -346,6 +400,8 @@ def run_stream(args):
     copy = torch.cuda.Stream()
     stream = torch.cuda.Stream()
     cache = C.ExpertCache(pool, pinned, L_, E, spec.d, spec.ffn, spec.top_k, copy)
+    if args.hot_slots:
+        cache.set_hot(args.hot_slots)
     ids_np, w_np = synth.streaming_ids(spec, args.seed, L_, W + K + 1)
     # emulated router lookahead: each id of the next layer is named correctly with the
     # pages' stated predictability (71.6%), else replaced by a popular-looking wrong id
@@ -399,7 +455,7 @@ def run_stream(args):
             "dtype": "i8xi4->i32, f32", "data": "synthetic",
             "config": {"workload": args.workload, "layers": L_, "d": spec.d, "ffn": spec.ffn, "n_exp": E,
                        "top_k": spec.top_k, "T": T, "host_blobs": L_ * E, "host_bytes": L_ * E * nb,
-                       "hbm_slots": STREAM_SLOTS, "reuse": 0.7,
+                       "hbm_slots": STREAM_SLOTS, "hot_slots": args.hot_slots, "reuse": 0.7,
                        "prefetch": ("next layer's ids from an emulated lookahead, 71.6% correct"
                                     if args.predictor == "lookahead" else "previous step's ids of the next layer"),
                        "timing": "CUDA events around K steps on the compute stream; host cache decisions inside"},
@@ -639,7 +695,7 @@ def main():
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "glm52_stream_8l":
-        run_stream(args)
+        run_cache_sim(args) if args.cache_sim else run_stream(args)
     else:
         run_colibri(args)
 

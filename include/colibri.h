@@ -282,6 +282,15 @@ int colibri_expert_cache_lookup(colibri_cache *c, int layer, const int32_t *ids,
 /* Device table of n_exp colibri_expert for `layer` (entries valid for looked-up ids). */
 const colibri_expert *colibri_expert_cache_table(colibri_cache *c, int layer);
 
+/* Usage-pinned hot set (the "self-learning" cache of the kongchang.com article, section
+ * 三级存储分层, where learned-hot experts stay in the fast tier): every lookup counts a
+ * use of its (layer, id); up to n_hot slots hold the keys with the most uses and are never
+ * evicted. A key enters the hot set when there is room or when it has strictly more uses
+ * than the weakest hot key (fewest uses, then least recently used), which leaves the set
+ * but stays resident. Prefetches do not count as uses. 0 (the default) is plain LRU.
+ * COLIBRI_E_INVAL unless 0 <= n_hot <= slots - top_k (a lookup batch must always fit). */
+int colibri_expert_cache_set_hot(colibri_cache *c, int n_hot);
+
 /* 1: lookups of non-resident ids fail with COLIBRI_E_MISS instead of staging. */
 int colibri_expert_cache_set_strict(colibri_cache *c, int strict);
 
@@ -303,6 +312,11 @@ int colibri_expert_cache_inject_stage_failure(colibri_cache *c, int count);
  * kind 2: 1 resident, 0 inserted, 2 no room (skipped); kind 0: 0. */
 int colibri_lru_trace(int capacity, int64_t n_ops, const int32_t *kind, const int64_t *key,
                       int8_t *result);
+
+/* colibri_lru_trace with n_hot usage-pinned slots (colibri_expert_cache_set_hot); lookups
+ * (kind 1) count as uses, prefetches (kind 2) do not. 0 <= n_hot <= capacity. */
+int colibri_lru_trace_hot(int capacity, int n_hot, int64_t n_ops, const int32_t *kind, const int64_t *key,
+                          int8_t *result);
 
 #ifdef __cplusplus
 }

@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(Expert), ctypes.POINTER(Expert),
                                        _P, _P, _P, _P, _P]),
                 "orc_lru_trace": (_I, [_I, _I64, _P, _P, _P]),
+                "orc_lru_hot_trace": (_I, [_I, _I, _I64, _P, _P, _P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -242,6 +243,17 @@ def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None):
     if rc:
         raise ValueError("orc_moe_layer: bad input")
     return out, ids_r, w_r
+
+
+def lru_hot_trace(capacity: int, n_hot: int, kinds, keys) -> np.ndarray:
+    """The cache policy with n_hot usage-pinned slots (results as lru_trace)."""
+    kinds = _c(kinds, np.int32)
+    keys = _c(keys, np.int64)
+    res = np.empty(len(kinds), np.int8)
+    rc = lib().orc_lru_hot_trace(capacity, n_hot, len(kinds), _ptr(kinds), _ptr(keys), _ptr(res))
+    if rc:
+        raise ValueError("orc_lru_hot_trace: bad capacity or n_hot")
+    return res
 
 
 def lru_trace(capacity: int, kinds, keys) -> np.ndarray:

@@ -471,3 +471,109 @@ int orc_lru_trace(int capacity, int64_t n_ops, const int32_t *kind, const int64_
     free(keys); free(stamp); free(valid); free(pinned);
     return 0;
 }
+
+/* The expert cache's replacement policy with a usage-pinned hot set, on abstract keys
+ * (kongchang.com article, section 三级存储分层: learned-hot experts stay in the fast tier;
+ * the pages give no algorithm, so this is the reading the library implements): every
+ * lookup adds one use of its key; up to n_hot resident keys are hot and never evicted; a
+ * key with a new use enters the hot set when there is room or when it has strictly more
+ * uses than the weakest hot key (fewest uses, then least recently accessed), which leaves
+ * the set but stays resident. Victims are the least recently accessed slots that are
+ * neither pinned by the current lookup batch nor hot. n_hot = 0 is orc_lru_trace. Plain
+ * arrays and linear scans. */
+int orc_lru_hot_trace(int capacity, int n_hot, int64_t n_ops, const int32_t *kind, const int64_t *key,
+                      int8_t *result)
+{
+    if (capacity <= 0 || n_hot < 0 || n_hot > capacity)
+        return -1;
+    int64_t *keys = (int64_t *)calloc((size_t)capacity, sizeof(int64_t));
+    int64_t *stamp = (int64_t *)calloc((size_t)capacity, sizeof(int64_t));
+    unsigned char *valid = (unsigned char *)calloc((size_t)capacity, 1);
+    unsigned char *pinned = (unsigned char *)calloc((size_t)capacity, 1);
+    unsigned char *hot = (unsigned char *)calloc((size_t)capacity, 1);
+    int64_t *ukey = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_ops > 0 ? n_ops : 1));
+    int64_t *ucnt = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n_ops > 0 ? n_ops : 1));
+    if (!keys || !stamp || !valid || !pinned || !hot || !ukey || !ucnt) {
+        free(keys); free(stamp); free(valid); free(pinned); free(hot); free(ukey); free(ucnt);
+        return -1;
+    }
+    int64_t n_keys = 0, clock = 0;
+    for (int64_t o = 0; o < n_ops; ++o) {
+        if (kind[o] == 0) {
+            memset(pinned, 0, (size_t)capacity);
+            result[o] = 0;
+            continue;
+        }
+        const int lookup = kind[o] == 1;
+        if (lookup) {
+            int64_t u = -1;
+            for (int64_t i = 0; i < n_keys; ++i)
+                if (ukey[i] == key[o])
+                    u = i;
+            if (u < 0) {
+                u = n_keys++;
+                ukey[u] = key[o];
+                ucnt[u] = 0;
+            }
+            ucnt[u] += 1;
+        }
+        int slot = -1;
+        for (int i = 0; i < capacity; ++i)
+            if (valid[i] && keys[i] == key[o])
+                slot = i;
+        if (slot >= 0) {
+            result[o] = 1;
+        } else {
+            for (int i = 0; i < capacity && slot < 0; ++i)
+                if (!valid[i])
+                    slot = i;
+            if (slot < 0) {
+                for (int i = 0; i < capacity; ++i)
+                    if (!pinned[i] && !hot[i] && (slot < 0 || stamp[i] < stamp[slot]))
+                        slot = i;
+            }
+            if (slot < 0) {
+                result[o] = 2;
+                continue;
+            }
+            keys[slot] = key[o];
+            valid[slot] = 1;
+            hot[slot] = 0;
+            pinned[slot] = 0;
+            result[o] = 0;
+        }
+        stamp[slot] = ++clock;
+        if (lookup)
+            pinned[slot] = 1;
+        if (!lookup || n_hot == 0 || hot[slot])
+            continue;
+        /* the hot-set rule, counting uses by scanning the key list */
+        int n_in = 0, weakest = -1;
+        int64_t wu = 0, su = 0;
+        for (int i = 0; i < capacity; ++i) {
+            if (!valid[i])
+                continue;
+            int64_t ui = 0;
+            for (int64_t j = 0; j < n_keys; ++j)
+                if (ukey[j] == keys[i])
+                    ui = ucnt[j];
+            if (i == slot)
+                su = ui;
+            if (!hot[i])
+                continue;
+            ++n_in;
+            if (weakest < 0 || ui < wu || (ui == wu && stamp[i] < stamp[weakest])) {
+                weakest = i;
+                wu = ui;
+            }
+        }
+        if (n_in < n_hot) {
+            hot[slot] = 1;
+        } else if (su > wu) {
+            hot[weakest] = 0;
+            hot[slot] = 1;
+        }
+    }
+    free(keys); free(stamp); free(valid); free(pinned); free(hot); free(ukey); free(ucnt);
+    return 0;
+}

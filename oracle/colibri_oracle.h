@@ -120,6 +120,8 @@ int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr
  * Every lookup or stage of a key, hit or not, makes it the most recently used. */
 int orc_lru_trace(int capacity, int64_t n_ops, const int32_t *kind, const int64_t *key,
                   int8_t *result);
+int orc_lru_hot_trace(int capacity, int n_hot, int64_t n_ops, const int32_t *kind, const int64_t *key,
+                      int8_t *result);
 
 #ifdef __cplusplus
 }

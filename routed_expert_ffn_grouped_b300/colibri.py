@@ -86,6 +86,8 @@ SIGNATURES = {
     "colibri_expert_cache_destroy": (None, [_P]),
     "colibri_expert_cache_inject_stage_failure": (_I, [_P, _I]),
     "colibri_lru_trace": (_I, [_I, _I64, _P, _P, _P]),
+    "colibri_lru_trace_hot": (_I, [_I, _I, _I64, _P, _P, _P]),
+    "colibri_expert_cache_set_hot": (_I, [_P, _I]),
 }
 
 _lock = threading.Lock()
@@ -244,6 +246,15 @@ def colibri_lru_trace(capacity: int, kinds, keys) -> np.ndarray:
     return res
 
 
+def colibri_lru_trace_hot(capacity: int, n_hot: int, kinds, keys) -> np.ndarray:
+    kinds = np.ascontiguousarray(kinds, np.int32)
+    keys = np.ascontiguousarray(keys, np.int64)
+    res = np.empty(len(kinds), np.int8)
+    _check("colibri_lru_trace_hot",
+           lib().colibri_lru_trace_hot(capacity, n_hot, len(kinds), _ptr(kinds), _ptr(keys), _ptr(res)))
+    return res
+
+
 class ExpertCache:
     """colibri_expert_cache_* over a caller-owned HBM pool and pinned host blobs."""
 
@@ -271,6 +282,9 @@ class ExpertCache:
         if not p:
             raise ColibriError("colibri_expert_cache_table", E_INVAL, "bad layer")
         return p
+
+    def set_hot(self, n_hot: int):
+        _check("colibri_expert_cache_set_hot", lib().colibri_expert_cache_set_hot(self.handle, int(n_hot)))
 
     def set_strict(self, strict: bool):
         _check("colibri_expert_cache_set_strict", lib().colibri_expert_cache_set_strict(self.handle, int(strict)))

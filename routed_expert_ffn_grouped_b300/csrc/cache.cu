@@ -165,7 +165,7 @@ int colibri_expert_cache_stage(colibri_cache *c, int layer, const int32_t *ids, 
         if (ids[i] < 0 || ids[i] >= c->n_exp)
             return COLIBRI_E_INVAL;
         const int64_t key = (int64_t)layer * c->n_exp + ids[i];
-        const LruCore::Result r = c->lru.access(key, false);
+        const LruCore::Result r = c->lru.access(key, false, false);  // a prefetch is not a use
         if (r.result == 2) {
             ++c->st.prefetch_skipped;
             continue;
@@ -241,6 +241,14 @@ const colibri_expert *colibri_expert_cache_table(colibri_cache *c, int layer)
     return c->dtables + (size_t)layer * c->n_exp;
 }
 
+int colibri_expert_cache_set_hot(colibri_cache *c, int n_hot)
+{
+    if (!c || n_hot < 0 || n_hot > c->n_slots - c->top_k)
+        return COLIBRI_E_INVAL;
+    c->lru.set_hot(n_hot);
+    return COLIBRI_OK;
+}
+
 int colibri_expert_cache_set_strict(colibri_cache *c, int strict)
 {
     if (!c)
@@ -306,15 +314,21 @@ int colibri_expert_cache_inject_stage_failure(colibri_cache *c, int count)
 
 int colibri_lru_trace(int capacity, int64_t n_ops, const int32_t *kind, const int64_t *key, int8_t *result)
 {
-    if (capacity <= 0 || n_ops < 0 || (n_ops > 0 && (!kind || !key || !result)))
+    return colibri_lru_trace_hot(capacity, 0, n_ops, kind, key, result);
+}
+
+int colibri_lru_trace_hot(int capacity, int n_hot, int64_t n_ops, const int32_t *kind, const int64_t *key,
+                          int8_t *result)
+{
+    if (capacity <= 0 || n_hot < 0 || n_hot > capacity || n_ops < 0 || (n_ops > 0 && (!kind || !key || !result)))
         return COLIBRI_E_INVAL;
-    LruCore lru(capacity);
+    LruCore lru(capacity, n_hot);
     for (int64_t i = 0; i < n_ops; ++i) {
         if (kind[i] == 0) {
             lru.unpin_all();
             result[i] = 0;
         } else if (kind[i] == 1 || kind[i] == 2) {
-            result[i] = (int8_t)lru.access(key[i], kind[i] == 1).result;
+            result[i] = (int8_t)lru.access(key[i], kind[i] == 1, kind[i] == 1).result;
         } else {
             return COLIBRI_E_INVAL;
         }

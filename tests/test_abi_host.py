@@ -90,3 +90,15 @@ def test_cache_policy_thrash_and_reuse(lib):
     keys = np.repeat(np.arange(20 * C_) % C_, 2).astype(np.int64)
     kinds = np.tile([0, 1], 20 * C_).astype(np.int32)
     assert C.colibri_lru_trace(C_, kinds, keys)[1::2].sum() == 19 * C_
+
+
+def test_cache_hot_policy_matches_oracle(lib, orc):
+    rng = np.random.default_rng(12)
+    for cap in (3, 8):
+        for n_hot in (1, 2, cap // 2, cap):
+            kinds = rng.choice([0, 1, 1, 1, 2], size=3000).astype(np.int32)
+            # skewed keys, so that use counts differ and the hot set changes hands
+            keys = np.minimum(rng.zipf(1.3, 3000), 4 * cap).astype(np.int64)
+            assert np.array_equal(C.colibri_lru_trace_hot(cap, n_hot, kinds, keys),
+                                  orc.lru_hot_trace(cap, n_hot, kinds, keys)), (cap, n_hot)
+    assert lib.colibri_lru_trace_hot(2, 3, 0, None, None, None) == C.E_INVAL

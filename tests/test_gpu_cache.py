@@ -169,3 +169,31 @@ def test_strict_miss_and_injected_stage_failure(torch_cuda, C, host):
     cache.sync(5000)
     torch.cuda.synchronize()
     cache.close()
+
+
+def test_hot_slots_follow_the_policy(torch_cuda, C, orc, host):
+    """With usage-pinned slots the cache's hits are those of the oracle's policy, and a
+    hot-set size that would leave no room for a lookup batch is rejected."""
+    torch = torch_cuda
+    _, pinned, _ = host
+    copy = torch.cuda.Stream()
+    n_slots = 6
+    cache, _ = make_cache(torch, C, pinned, n_slots, copy)
+    with pytest.raises(C.ColibriError) as e:
+        cache.set_hot(n_slots - SPEC.top_k + 1)
+    assert e.value.status == C.E_INVAL
+    cache.set_hot(2)
+    batches = [[0, 1, 2, 3]] * 3 + [[4, 5, 6, 7], [8, 9, 10, 11], [12, 13, 14, 15], [0, 1, 2, 3]]
+    stream = torch.cuda.current_stream()
+    kinds, keys = [], []
+    before = cache.stats()["hits"]
+    for b in batches:
+        cache.lookup(0, np.array(b, np.int32), wait_on=stream)
+        kinds += [0] + [1] * len(b)
+        keys += [0] + list(b)
+    torch.cuda.synchronize()
+    res = orc.lru_hot_trace(n_slots, 2, np.array(kinds, np.int32), np.array(keys, np.int64))
+    assert cache.stats()["hits"] - before == int((res == 1).sum())
+    assert res[-4:].tolist() == [1, 1, 0, 0]      # the two hot experts survived the scan
+    cache.sync(5000)
+    cache.close()

@@ -417,3 +417,41 @@ def test_lru_random_against_ordered_dict(orc):
             pinned.add(k)
         want.append(0)
     assert got.tolist() == want
+
+
+# ---- usage-pinned hot set of the cache policy -----------------------------------------
+def _batches(keys):
+    """One lookup batch per key: a batch start, then the lookup."""
+    kinds = np.tile([0, 1], len(keys)).astype(np.int32)
+    ks = np.repeat(np.asarray(keys, np.int64), 2)
+    return kinds, ks
+
+
+def test_hot_set_zero_is_plain_lru(orc):
+    rng = np.random.default_rng(5)
+    for cap in (1, 3, 8):
+        kinds = rng.choice([0, 1, 1, 2], size=3000).astype(np.int32)
+        keys = rng.integers(0, 3 * cap + 2, 3000).astype(np.int64)
+        assert np.array_equal(orc.lru_hot_trace(cap, 0, kinds, keys), orc.lru_trace(cap, kinds, keys))
+
+
+def test_hot_key_survives_a_cyclic_scan(orc):
+    # capacity 3, one hot slot: A (three uses) stays through the B, C, D cycle that evicts it
+    # under plain LRU; worked by hand
+    A, B, Cc, D = 1, 2, 3, 4
+    kinds, keys = _batches([A, A, A, B, Cc, D, B, Cc, D, A])
+    assert orc.lru_hot_trace(3, 1, kinds, keys)[1::2].tolist() == [0, 1, 1, 0, 0, 0, 0, 0, 0, 1]
+    assert orc.lru_hot_trace(3, 0, kinds, keys)[1::2].tolist() == [0, 1, 1, 0, 0, 0, 1, 1, 1, 0]
+
+
+def test_hot_set_follows_use_counts(orc):
+    # capacity 4, one hot slot: B (three uses) takes the slot from A (two uses); the scan
+    # C, D, E, F then evicts A but not B; worked by hand
+    A, B, Cc, D, E, F = 1, 2, 3, 4, 5, 6
+    kinds, keys = _batches([A, A, B, B, B, Cc, D, E, F, A, B])
+    assert orc.lru_hot_trace(4, 1, kinds, keys)[1::2].tolist() == [0, 1, 0, 1, 1, 0, 0, 0, 0, 0, 1]
+
+
+def test_hot_set_rejects_bad_sizes(orc):
+    with pytest.raises(ValueError):
+        orc.lru_hot_trace(2, 3, [1], [0])
