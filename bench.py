@@ -607,15 +607,21 @@ def run_colibri(args):
             # algorithmic bytes of the roofline kernel: gate/up weights for the prefill
             # GEMM, all expert weights for the fused decode kernel
             prof_bytes.append(u * gu_b + sh[1] if prefill else u * nb + sh[0])
-    kern_ms = {k: float(np.mean(v)) for k, v in prof.items()}
+    mean = {k: float(np.mean(v)) for k, v in prof.items()}
     if prefill:
+        kern_ms = {"k_q8 + k_route_logits_tiled": mean["router_logits"], "k_router_select": mean["router_select"],
+                   "k_bucket": mean["bucket"], "k_gemm<0>": mean["gateup"], "k_gemm<1>": mean["down"],
+                   "k_combine": mean["combine"]}
         roof_ms = np.array(prof["gateup"])
         gu_kernel = "k_gemm<0> (tcgen05 gate/up + SwiGLU + q8)"
         traffic = None
     else:
-        # one kernel runs gate/up, down and combine; its profiling marks are back to back
-        roof_ms = np.array(prof["gateup"]) + np.array(prof["down"]) + np.array(prof["combine"])
-        gu_kernel = "k_decode (gate/up + down + combine)"
+        # two kernels; the other slots hold only the time of an event record
+        kern_ms = {"k_route_logits": mean["router_logits"], "k_decode": mean["gateup"],
+                   "event_records": mean["q8"] + mean["router_select"] + mean["bucket"] + mean["down"]
+                   + mean["combine"]}
+        roof_ms = np.array(prof["gateup"])
+        gu_kernel = "k_decode (selection, bucketing, gate/up, down, combine)"
         traffic = traffic_from_profiles("k_decode_glm52_decode_t1", "kernels_decode.cu", args.workload)
     gu_gbs = float(np.mean(np.array(prof_bytes) / (roof_ms / 1e3)) / 1e9)
     roof_tensor = None

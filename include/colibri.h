@@ -139,7 +139,11 @@ size_t colibri_moe_workspace_bytes(const colibri_layer_cfg *cfg, int T_max);
  *   per expert: gate = W1 q8(x), up = W3 q8(x) as int32 group dots times the two
  *   groups' scales; h = silu(gate) * up; down y = W2 q8(h) likewise ->
  *   out[t] = y_shared[t] + sum_i w[t][i] * y_{ids[t][i]}[t] in slot order.
- *   T <= 32 runs the decode GEMV kernels; larger T runs the grouped GEMM on tcgen05.
+ *   T <= 32 (decode) runs two kernels: router logits and scores with q8(x) on the side
+ *   (q8 alone when ids_given), then one persistent kernel that selects and buckets in every
+ *   CTA and runs gate/up, down and the combine, started as a programmatic dependent of the
+ *   first. Larger T (prefill) runs q8, router logits, selection, bucketing, the two
+ *   grouped GEMMs on tcgen05 and the combine.
  *   x        device fp32 [T][d]
  *   Wr, bias as for colibri_router_topk (unused when ids_given)
  *   experts  device array of E colibri_expert (only the selected ids are read)
@@ -205,17 +209,20 @@ typedef struct {
 int colibri_moe_workspace_view(const colibri_layer_cfg *cfg, int T_max, colibri_workspace_view *out);
 
 /* Profiling hook (process-wide, not thread-safe, off by default). While enabled,
- * colibri_moe_layer records a timing event on its stream before its first kernel and
- * after each of its seven kernels (also under CUDA-graph capture, as external
- * event-record nodes), on the device that was current when profiling was enabled. */
+ * colibri_moe_layer records timing events on its stream around its kernels (seven slots;
+ * also under CUDA-graph capture, as external event-record nodes), on the device that
+ * was current when profiling was enabled. */
 #define COLIBRI_PROFILE_KERNELS 7
 int colibri_moe_profile_enable(int on);
 
 /* Milliseconds of each step of the most recent profiled call, after waiting for it:
  * ms[0] q8 of x, [1] router logits, [2] router selection, [3] bucketing, [4] gate/up,
  * [5] down, [6] combine. Steps fused into one kernel report their time in the first of
- * their slots (with the router, q8 rides in the logits kernel; for T <= 32 bucketing
- * rides in the selection kernel); skipped and fused-away slots read about 0.
+ * their slots; skipped and fused-away slots read about 0 (the time of an event record).
+ * Decode (T <= 32): [1] the routing kernel (router logits and scores with q8, or q8 alone
+ * when ids_given), [4] the expert kernel (selection, bucketing, gate/up, down, combine).
+ * Prefill: [1] q8 and the router logits, [2] selection, [3] bucketing, [4] and [5] the two
+ * GEMMs, [6] combine. The events serialise the kernels (no programmatic overlap).
  * n must be >= COLIBRI_PROFILE_KERNELS. */
 int colibri_moe_profile_read(float *ms, int n);
 
