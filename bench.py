@@ -283,15 +283,16 @@ DECODE_T_MAX = 32   # largest T on the decode (GEMV) path; larger T takes the tc
 
 
 def launches_per_step(T: int, n_exp: int, ids_given: bool) -> int:
-    """Kernels one colibri_moe_layer call launches. Decode (T <= 32): routing, then one
-    kernel for gate/up, down and combine; routing is one fused kernel (T x E <= 8192),
-    q8 + bucketing with the ids given, else router logits + selection + bucketing.
-    Prefill: q8, router logits, selection, bucketing (the first three replaced by q8 when
-    the ids are given), the two tcgen05 GEMMs and the combine."""
+    """Kernels one colibri_moe_layer call launches. Decode (T <= 32): one routing kernel
+    (router logits and scores with q8 of x, or q8 alone with the ids given), a selection
+    kernel when T x E > 4096 (else every CTA of the next kernel selects), then one kernel
+    for selection or bucketing, gate/up, down and combine. Prefill: q8, router logits,
+    selection, bucketing (q8 and bucketing alone with the ids given), the two tcgen05 GEMMs
+    and the combine."""
     if T <= DECODE_T_MAX:
         if ids_given:
-            return 3
-        return 2 if T * n_exp <= 8192 else 4
+            return 2
+        return 2 if T * n_exp <= 4096 else 3
     return 5 if ids_given else 7
 
 
@@ -466,7 +467,7 @@ def run_stream(args):
                       "bytes_staged": d["bytes_staged"],
                       "pcie_gbs": d["bytes_staged"] / (ms / 1e3) / 1e9},
             "wall_s": wall, "generate_s": gen_s,
-            # per layer call (ids given) + one table-entry write per staged blob
+            # two per layer call (ids given) + one table-entry write per staged blob
             "gpu_launches": K * L_ * launches_per_step(T, E, True) + d["misses"] + d["prefetch_staged"],
             "clocks": sampler.summary(),
         }

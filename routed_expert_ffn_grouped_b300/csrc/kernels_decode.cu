@@ -1185,18 +1185,19 @@ __global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs
 
 namespace {
 
+// Ring stages (and h and partial-sum buffers) for chunks of TCH tokens; 0 if fewer than
+// two 40 KB stages fit.
 template <int TCH>
-cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
+int ring_for(DecodeArgs &a)
 {
-    auto fn = k_decode<TCH>;
     // partial-sum buffers (= epilogue warps): 4 for chunks of at most 2 tokens, else 2;
-    // then the most 40 KB ring stages beside the rest, with 3 h buffers if that still
-    // leaves 4 stages, else 2 (measured: more buffers beat a fifth stage)
-    const int best_nb = TCH <= 2 ? 4 : 2;
+    // then the most ring stages beside the rest, with 3 h buffers if that still leaves 4
+    // stages, else 2 (measured: more buffers beat a fifth stage)
+    const int nb = TCH <= 2 ? 4 : 2;
     int best_ns = 0, best_nh = 2;
     for (int nh = NH_MAX; nh >= 2; --nh) {
         int ns = MAX_RING;
-        while (ns >= 2 && ring_layout(a, ns, nh, best_nb, TCH).total > SMEM_BUDGET)
+        while (ns >= 2 && ring_layout(a, ns, nh, nb, TCH).total > SMEM_BUDGET)
             --ns;
         if (ns > best_ns) {
             best_ns = ns;
@@ -1206,19 +1207,44 @@ cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
             break;
     }
     if (best_ns < 2)
-        return cudaErrorInvalidValue;
+        return 0;
     a.ring = best_ns;
     a.nh = best_nh;
-    a.nbuf = best_nb;
+    a.nbuf = nb;
+    a.tch = TCH;
+    return best_ns;
+}
+
+template <int TCH>
+cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
+{
+    auto fn = k_decode<TCH>;
     const size_t smem = ring_layout(a, a.ring, a.nh, a.nbuf, TCH).total;
-    int dev = 0, n_sm = 0;
+    // per device: the SM count and the largest dynamic shared memory set so far (the
+    // attribute belongs to the device's context), so that a call costs no queries
+    constexpr int MAX_DEV = 64;
+    static int sm_count[MAX_DEV] = {};
+    static size_t smem_set[MAX_DEV] = {};
+    int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
+    if (dev < 0 || dev >= MAX_DEV)
+        return cudaErrorInvalidDevice;
+    if (sm_count[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        sm_count[dev] = n;
+    }
+    if (smem > smem_set[dev]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        smem_set[dev] = smem;
+    }
+    const int n_sm = sm_count[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_sm);
     cfg.blockDim = dim3((NC + 1 + NE_MAX) * 32);
@@ -1248,7 +1274,8 @@ int decode_hgs(int fmax)
 
 bool decode_selects_in_kernel(int T, int E)
 {
-    return T * E <= 8192;
+    // the selection scratch (c and s of every token) shares shared memory with the ring
+    return T * E <= 4096;
 }
 
 cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
@@ -1257,13 +1284,20 @@ cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
         return cudaSuccess;
     a.hgs = decode_hgs(a.fmax);
     // tokens per chunk: up to 4 (a slot with more tokens streams its weights once per
-    // chunk, but the smaller x, h and partial-sum areas leave room for a deeper ring)
-    a.tch = a.T <= 1 ? 1 : a.T <= 2 ? 2 : 4;
-    switch (a.tch) {
-    case 1: return launch_tch<1>(a, s);
-    case 2: return launch_tch<2>(a, s);
-    default: return launch_tch<4>(a, s);
-    }
+    // chunk, but the smaller x, h and partial-sum areas leave room for a deeper ring);
+    // fewer when a large shape leaves no room for three ring stages
+    const int want = a.T <= 1 ? 1 : a.T <= 2 ? 2 : 4;
+    DecodeArgs c4 = a, c2 = a, c1 = a;
+    const int n4 = want >= 4 ? ring_for<4>(c4) : 0;
+    const int n2 = want >= 2 ? ring_for<2>(c2) : 0;
+    const int n1 = ring_for<1>(c1);
+    if (n4 >= 3 || (n4 >= 2 && n2 < 3 && n1 < 3))
+        return launch_tch<4>(c4, s);
+    if (n2 >= 3 || (n2 >= 2 && n1 < 3))
+        return launch_tch<2>(c2, s);
+    if (n1 >= 2)
+        return launch_tch<1>(c1, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace clb

@@ -166,7 +166,7 @@ def ws_slice(ws, off, nbytes, dtype):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 1), ("tiny", 13), ("olmoe", 1), ("olmoe", 16),
-                                    ("glm52", 1), ("glm52", 4)])
+                                    ("glm52", 1), ("glm52", 4), ("glm52", 32)])
 def test_moe_layer_parity(torch_cuda, C, orc, name, T):
     torch = torch_cuda
     spec = synth.SPECS[name]
@@ -275,3 +275,22 @@ def test_glm_prefill_sampled(torch_cuda, C, orc):
     for t in (0, 1, 777, 2047):
         ref, _, _ = orc.moe_layer(spec, x[t:t + 1], host.Wr, host.bias, host.expert, host.shared())
         assert_rms_close(out[t:t + 1], ref)
+
+
+# d = 96: three 32-row blocks of d, so the down items' last pair has one block; ffn = 64:
+# rows of q8(h) scales padded to 16 bytes; T * d not a multiple of 128: x staged by loads
+ODD = synth.TINY.replace(name="odd96", d=96, ffn=64, n_exp=8, top_k=2, n_group=2, topk_group=1,
+                         shared_ffn=64)
+
+
+@pytest.mark.parametrize("T", [1, 3, 7])
+def test_moe_layer_parity_odd_shape(torch_cuda, C, orc, T):
+    torch = torch_cuda
+    host, dl = dev_layer(C, ODD)
+    x = synth.activations(ODD, 0, T, step=3)
+    out, ids, w, ws = run_layer(torch, C, dl, x)
+    assert C.colibri_workspace_status(dl.cfg, T, ws) == C.OK
+    ref, ids_o, w_o = orc.moe_layer(ODD, x, host.Wr, host.bias, host.expert, host.shared())
+    assert np.array_equal(ids, ids_o)
+    np.testing.assert_allclose(w, w_o, rtol=1e-6)
+    assert_rms_close(out, ref)
