@@ -51,7 +51,7 @@ struct BucketArgs {
 
 // Decode GEMVs (kernels_decode.cu).
 enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
-constexpr int DN_ITEM_ROWS = 32;  // rows of d per down item
+constexpr int DN_ITEM_ROWS = 32;  // rows of d per down work unit in the bucketing counters
 
 struct DecodeArgs {
     const colibri_expert *experts;
