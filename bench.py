@@ -636,9 +636,11 @@ def run_colibri(args):
                        "frac": tf / tpeak, "algorithmic_flops_per_launch": flops,
                        "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({peak_kind})"}
 
-    # end to end through the public API: pinned host x in, out back to pinned host, per step
+    # end to end through the public API: one blocking colibri_moe_layer_host call per step,
+    # x from pinned host memory in, out (and the device error flag) back to pinned host
     x_pin = torch.from_numpy(xs_host).pin_memory()
     out_pin = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
+    ws_host = torch.empty(C.colibri_moe_host_workspace_bytes(dl.cfg, T), dtype=torch.uint8, device="cuda")
     KE = min(K, 500)
     e2e_s = 0.0
     with torch.cuda.stream(stream):
@@ -648,11 +650,8 @@ def run_colibri(args):
             graph_prev.replay()
             stream.synchronize()
             t0 = time.perf_counter()
-            x.copy_(x_pin[i % N_X], non_blocking=True)
-            C.colibri_moe_layer(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws,
-                                stream=stream)
-            out_pin.copy_(out, non_blocking=True)
-            stream.synchronize()
+            C.colibri_moe_layer_host(dl.cfg, x_pin[i % N_X], dl.Wr, dl.bias, dl.table, dl.shared, None, None,
+                                     False, out_pin, ws_host, stream=stream)
             e2e_s += time.perf_counter() - t0
     e2e_s = allreduce_max(torch, world, e2e_s)
     e2e_value = world * T * KE / e2e_s
@@ -686,8 +685,9 @@ def run_colibri(args):
                             "note": "informational; the headline value flushes L2 between steps"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * spec.d * 4,
-                    "d2h_bytes_per_step": T * spec.d * 4, "steps": KE,
-                    "path": "colibri_moe_layer via the Python binding, eager launches"},
+                    "d2h_bytes_per_step": T * spec.d * 4 + 4, "steps": KE,
+                    "path": "colibri_moe_layer_host (pinned host x and out, the error flag read back) "
+                            "via the Python binding, eager launches"},
             "gpu_launches": launches_per_step(T, spec.n_exp, False) * K,
             "clocks": sampler.summary(),
         }

@@ -14,7 +14,8 @@
  *     host memory. The caller allocates and owns every buffer passed in (device
  *     memory, pinned host memory, streams); the library never frees caller memory.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
- *     Compute entry points only enqueue work on it and return without synchronising.
+ *     Compute entry points only enqueue work on it and return without synchronising,
+ *     except colibri_moe_layer_host, which waits for its stream.
  *   - Activations are row-major. A packed int4 weight matrix W [R][K] (R = out, K = in,
  *     both multiples of 32) is stored in row blocks of 32 rows, group-major inside a
  *     block: the 16 bytes of group g (columns 32g..32g+31) of row r are at byte
@@ -187,6 +188,36 @@ int colibri_moe_layer_noalloc(const colibri_layer_cfg *cfg, const float *x, int 
                               const float *bias, const colibri_expert *experts,
                               const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
                               float *out, void *stream);
+
+/* colibri_moe_layer on HOST buffers, as one blocking call: the layer computed on the
+ * host side of the hybrid CPU/GPU engine of the pages ("Streaming d'experts", "Guide
+ * Complet de Colibri") hands one step's activations to the GPU and takes the output back.
+ * On `stream` it copies x (and ids, w when ids_given) from host memory into a region at
+ * the end of the workspace, runs colibri_moe_layer on those device copies, copies out
+ * (and ids, w when routed here and the pointers are non-NULL) and the device error flag
+ * back, and waits for the stream. Host buffers may be pinned (cudaHostAlloc or
+ * cudaHostRegister: the copies then run at PCIe speed without staging) or pageable
+ * (correct, slower).
+ *   x         host fp32 [T][d]
+ *   Wr, bias, experts, shared   device, as for colibri_moe_layer
+ *   ids, w    host [T][top_k]: inputs when ids_given (both required), else outputs,
+ *             each optional (NULL: not copied back)
+ *   out       host fp32 [T][d]
+ *   workspace device, >= colibri_moe_host_workspace_bytes(cfg, T) bytes, 256-byte
+ *             aligned; owned by the caller; its first colibri_moe_workspace_bytes(cfg, T)
+ *             bytes are the layer's workspace
+ * Returns COLIBRI_OK when out holds the result; COLIBRI_E_DEVICE when the kernels set
+ * the device error flag (an id out of range or repeated; out is then undefined);
+ * COLIBRI_E_INVAL / COLIBRI_E_NOMEM for bad arguments or a short workspace (nothing is
+ * enqueued); COLIBRI_E_CUDA when a copy or launch fails. On every return the stream has
+ * finished reading the host buffers. T == 0 is a no-op.
+ * colibri_moe_host_workspace_bytes: the device workspace the call needs for up to T_max
+ * tokens (0 on a bad configuration). */
+size_t colibri_moe_host_workspace_bytes(const colibri_layer_cfg *cfg, int T_max);
+int colibri_moe_layer_host(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                           const float *bias, const colibri_expert *experts,
+                           const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
+                           float *out, void *workspace, size_t ws_bytes, void *stream);
 
 /* Reads the device error flag of a workspace after synchronising `stream`, and clears
  * it. *status_out = COLIBRI_OK or COLIBRI_E_DEVICE. */

@@ -68,6 +68,9 @@ SIGNATURES = {
     "colibri_moe_workspace_bytes": (_SZ, [_PCFG, _I]),
     "colibri_moe_layer": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
                                _SZ, _P]),
+    "colibri_moe_host_workspace_bytes": (_SZ, [_PCFG, _I]),
+    "colibri_moe_layer_host": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
+                                    _SZ, _P]),
     "colibri_moe_layer_noalloc": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I,
                                        _P, _P]),
     "colibri_workspace_status": (_I, [_PCFG, _I, _P, ctypes.POINTER(_I), _P]),
@@ -183,6 +186,26 @@ def colibri_moe_layer(cfg: LayerCfg, x, Wr, bias, experts, shared: Expert | None
                                    ctypes.byref(shared) if shared is not None else None, _ptr(ids), _ptr(w),
                                    int(bool(ids_given)), _ptr(out), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))
+
+
+def colibri_moe_host_workspace_bytes(cfg: LayerCfg, T_max: int) -> int:
+    n = lib().colibri_moe_host_workspace_bytes(ctypes.byref(cfg), T_max)
+    if n == 0:
+        raise ColibriError("colibri_moe_host_workspace_bytes", E_INVAL, "invalid configuration")
+    return n
+
+
+def colibri_moe_layer_host(cfg: LayerCfg, x, Wr, bias, experts, shared: Expert | None, ids, w,
+                           ids_given: bool, out, workspace, stream=None):
+    """colibri_moe_layer on host buffers (numpy arrays or CPU tensors, pinned or not): x,
+    out, and ids, w (inputs when ids_given, else optional outputs) live in host memory;
+    Wr, bias, experts and workspace on the device. Returns when out holds the result."""
+    T = x.shape[0]
+    _check("colibri_moe_layer_host",
+           lib().colibri_moe_layer_host(ctypes.byref(cfg), _ptr(x), T, _ptr(Wr), _ptr(bias), _ptr(experts),
+                                        ctypes.byref(shared) if shared is not None else None, _ptr(ids),
+                                        _ptr(w), int(bool(ids_given)), _ptr(out), _ptr(workspace),
+                                        workspace.numel(), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20

@@ -54,8 +54,14 @@ def test_workspace_bytes_and_config_checks(lib):
         cfg = C.layer_cfg(spec)
         assert C.colibri_moe_workspace_bytes(cfg, 4) > 0
         assert C.colibri_moe_workspace_bytes(cfg, 2048) > C.colibri_moe_workspace_bytes(cfg, 4)
+        for T in (1, 4, 32, 33, 2048):
+            # the host entry's workspace: the layer's, then room for x, out, ids and w
+            extra = C.colibri_moe_host_workspace_bytes(cfg, T) - C.colibri_moe_workspace_bytes(cfg, T)
+            assert extra >= 2 * 4 * T * spec.d + 2 * 4 * T * spec.top_k
+            assert extra < 2 * 4 * T * spec.d + 2 * 4 * T * spec.top_k + 4 * 256
     bad = C.layer_cfg(synth.TINY.replace(n_group=3))
     assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0
+    assert lib.colibri_moe_host_workspace_bytes(ctypes.byref(bad), 4) == 0
     bad = C.layer_cfg(synth.TINY)
     bad.group = 64
     assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0
@@ -71,6 +77,22 @@ def test_argument_errors_detected_on_host(lib):
     assert lib.colibri_moe_layer(ctypes.byref(cfg), None, 4, None, None, None, None, None, None, 0,
                                  None, None, 0, None) == C.E_INVAL
     assert lib.colibri_debug_group_dots(None, None, 1, 31, None, None) == C.E_INVAL
+    # the host-buffer entry: T == 0 is a no-op; missing buffers, missing given ids and a
+    # short workspace are refused before any copy (the workspace address is never used)
+    host = lib.colibri_moe_layer_host
+    x = np.zeros((4, synth.TINY.d), np.float32)
+    out = np.zeros_like(x)
+    fake_ws = 1 << 20
+    assert host(ctypes.byref(cfg), None, 0, None, None, None, None, None, None, 0, None, None, 0, None) == C.OK
+    assert host(ctypes.byref(cfg), None, 4, None, None, None, None, None, None, 0, out.ctypes.data,
+                fake_ws, 1 << 40, None) == C.E_INVAL
+    assert host(ctypes.byref(cfg), x.ctypes.data, 4, None, None, None, None, None, None, 1, out.ctypes.data,
+                fake_ws, 1 << 40, None) == C.E_INVAL
+    assert host(ctypes.byref(cfg), x.ctypes.data, 4, None, None, None, None, None, None, 0, out.ctypes.data,
+                fake_ws + 16, 1 << 40, None) == C.E_INVAL
+    need = C.colibri_moe_host_workspace_bytes(cfg, 4)
+    assert host(ctypes.byref(cfg), x.ctypes.data, 4, None, None, None, None, None, None, 0, out.ctypes.data,
+                fake_ws, need - 1, None) == C.E_NOMEM
     assert lib.colibri_lru_trace(0, 0, None, None, None) == C.E_INVAL
 
 

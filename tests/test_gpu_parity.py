@@ -294,3 +294,62 @@ def test_moe_layer_parity_odd_shape(torch_cuda, C, orc, T):
     assert np.array_equal(ids, ids_o)
     np.testing.assert_allclose(w, w_o, rtol=1e-6)
     assert_rms_close(out, ref)
+
+
+# ------------------------------------------------------------------ host-buffer entry point
+@pytest.mark.parametrize("name,T,pinned", [("glm52", 1, True), ("tiny", 13, False), ("olmoe", 16, True),
+                                           ("tiny", 33, False)])
+def test_moe_layer_host_entry(torch_cuda, C, orc, name, T, pinned):
+    """colibri_moe_layer_host on host buffers: the same bits as colibri_moe_layer on device
+    buffers (decode and prefill), so the same parity with the oracle."""
+    torch = torch_cuda
+    spec = synth.SPECS[name]
+    host, dl = dev_layer(C, spec)
+    x = synth.activations(spec, 0, T, step=13)
+    out_dev, ids_dev, w_dev, _ = run_layer(torch, C, dl, x)
+    ws = torch.empty(C.colibri_moe_host_workspace_bytes(dl.cfg, T), dtype=torch.uint8, device="cuda")
+    if pinned:
+        xh = torch.from_numpy(x).pin_memory()
+        out = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
+        ids = torch.empty((T, spec.top_k), dtype=torch.int32).pin_memory()
+        w = torch.empty((T, spec.top_k), dtype=torch.float32).pin_memory()
+    else:
+        xh = np.ascontiguousarray(x)
+        out = np.empty((T, spec.d), np.float32)
+        ids = np.empty((T, spec.top_k), np.int32)
+        w = np.empty((T, spec.top_k), np.float32)
+    C.colibri_moe_layer_host(dl.cfg, xh, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws)
+    out, ids, w = (np.asarray(a) for a in (out, ids, w))
+    assert np.array_equal(out.view(np.uint32), out_dev.view(np.uint32))
+    assert np.array_equal(ids, ids_dev) and np.array_equal(w.view(np.uint32), w_dev.view(np.uint32))
+    ref, ids_o, _ = orc.moe_layer(spec, x, host.Wr, host.bias, host.expert, host.shared())
+    assert np.array_equal(ids, ids_o)
+    assert_rms_close(out, ref)
+
+
+def test_moe_layer_host_entry_ids_given_and_errors(torch_cuda, C, orc):
+    torch = torch_cuda
+    spec = synth.TINY
+    host, dl = dev_layer(C, spec)
+    ids = np.array([[0, 1, 2, 3], [5, 6, 4, 7]], np.int32)
+    w = np.full((2, 4), 0.25, np.float32)
+    x = synth.activations(spec, 2, 2)
+    ws = torch.empty(C.colibri_moe_host_workspace_bytes(dl.cfg, 2), dtype=torch.uint8, device="cuda")
+    out = np.empty((2, spec.d), np.float32)
+    C.colibri_moe_layer_host(dl.cfg, x, None, None, dl.table, dl.shared, ids, w, True, out, ws)
+    ref, _, _ = orc.moe_layer(spec, x, None, None, host.expert, host.shared(), ids=ids, w=w)
+    assert_rms_close(out, ref)
+    # an id out of range: the kernels skip it and the call returns the device status
+    bad = ids.copy()
+    bad[1, 2] = spec.n_exp
+    with pytest.raises(C.ColibriError) as e:
+        C.colibri_moe_layer_host(dl.cfg, x, None, None, dl.table, dl.shared, bad, w, True, out, ws)
+    assert e.value.status == C.E_DEVICE
+    # the next good call starts clean
+    C.colibri_moe_layer_host(dl.cfg, x, None, None, dl.table, dl.shared, ids, w, True, out, ws)
+    assert_rms_close(out, ref)
+    # a workspace sized for the device entry alone is too short
+    short = torch.empty(C.colibri_moe_workspace_bytes(dl.cfg, 2), dtype=torch.uint8, device="cuda")
+    with pytest.raises(C.ColibriError) as e:
+        C.colibri_moe_layer_host(dl.cfg, x, None, None, dl.table, dl.shared, ids, w, True, out, short)
+    assert e.value.status == C.E_NOMEM
