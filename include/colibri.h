@@ -232,10 +232,14 @@ typedef struct {
     size_t sx;      /* fp32 [T][d/32]       their scales */
     size_t offsets; /* int32 [E+1]          bucket offsets (exclusive scan of counts) */
     size_t pairs;   /* int32 [T*k]          pairs p = t*k+i sorted by (expert, p) */
-    size_t hq;      /* int8 [T*k+T][fmax]   q8 codes of h per pair (routed, then shared) */
-    size_t hs;      /* fp32 [T*k+T][fmax/32] */
+    size_t hq;      /* int8 [T*k+T][fmax]   q8 codes of h per pair (routed, then shared;
+                       decode, T <= 32) */
+    size_t hs;      /* fp32 [T*k+T][hs_stride] their scales */
     size_t y;       /* fp32 [T*k+T][d]      per-pair expert outputs */
     size_t fmax;    /* row stride of hq: max(ffn, shared_ffn) */
+    size_t hs_stride; /* floats per row of hs: fmax/32, rounded up to 4 for decode */
+    size_t hbf;     /* prefill (T > 32): uint16 [T*k+T][fmax], the q8 codes of h as bf16;
+                       inside each run of 8, element k of the run sits at 2*(k%4) + k/4 */
 } colibri_workspace_view;
 int colibri_moe_workspace_view(const colibri_layer_cfg *cfg, int T_max, colibri_workspace_view *out);
 

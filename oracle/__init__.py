@@ -79,7 +79,7 @@ def lib() -> ctypes.CDLL:
                 "orc_router_topk": (_I, [ctypes.POINTER(Cfg), _P, _I64, _P, _P, _P, _P]),
                 "orc_bucket": (_I, [_P, _I64, _I, _I, _P, _P]),
                 "orc_group_dots": (None, [_P, _P, _I64, _I64, _P]),
-                "orc_expert_token": (_I, [_I, _I, ctypes.POINTER(Expert), _P, _P, _P, _P, _P]),
+                "orc_expert_token": (_I, [_I, _I, ctypes.POINTER(Expert), _P, _P, _P, _P, _P, _P]),
                 "orc_moe_layer": (_I, [ctypes.POINTER(Cfg), _P, _I64, _P, _P,
                                        ctypes.POINTER(Expert), ctypes.POINTER(Expert),
                                        _P, _P, _P, _P, _P]),
@@ -191,8 +191,9 @@ def group_dots(w_packed: np.ndarray, qa: np.ndarray) -> np.ndarray:
     return out
 
 
-def expert_token(views: dict, qx: np.ndarray, sx: np.ndarray):
-    """One token through one expert; returns (y, qh, sh)."""
+def expert_token(views: dict, qx: np.ndarray, sx: np.ndarray, want_h: bool = False):
+    """One token through one expert; returns (y, qh, sh), and the fp32 h that (qh, sh)
+    quantise as a fourth item when want_h."""
     ex, keep = make_expert(views)
     f = keep[0].shape[0]
     d = 2 * keep[0].shape[1]
@@ -200,10 +201,12 @@ def expert_token(views: dict, qx: np.ndarray, sx: np.ndarray):
     y = np.empty(d, np.float32)
     qh = np.empty(f, np.int8)
     sh = np.empty(f // 32, np.float32)
-    rc = lib().orc_expert_token(d, f, ctypes.byref(ex), _ptr(qx), _ptr(sx), _ptr(y), _ptr(qh), _ptr(sh))
+    h = np.empty(f, np.float32) if want_h else None
+    rc = lib().orc_expert_token(d, f, ctypes.byref(ex), _ptr(qx), _ptr(sx), _ptr(y), _ptr(qh), _ptr(sh),
+                                _ptr(h) if want_h else None)
     if rc:
         raise MemoryError("orc_expert_token")
-    return y, qh, sh
+    return (y, qh, sh, h) if want_h else (y, qh, sh)
 
 
 def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None):

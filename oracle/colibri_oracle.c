@@ -307,7 +307,7 @@ void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t co
  * h_n = silu(gate_n) * up_n with silu(z) = z / (1 + exp(-z)), rounded to fp32;
  * (qh, sh) = q8(h); y_m = sum_g s2[m][g] * sh[g] * D2[m][g] (fp64), rounded to fp32. */
 int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const float *sx,
-                     float *y, int8_t *qh_out, float *sh_out)
+                     float *y, int8_t *qh_out, float *sh_out, float *h_out)
 {
     const int ngd = d / ORC_GROUP, ngf = f / ORC_GROUP;
     int32_t *dots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(ngd > ngf ? ngd : ngf));
@@ -341,6 +341,8 @@ int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const
         memcpy(qh_out, qh, (size_t)f);
     if (sh_out)
         memcpy(sh_out, sh, sizeof(float) * (size_t)ngf);
+    if (h_out)
+        memcpy(h_out, h, sizeof(float) * (size_t)f);
     free(dots); free(h); free(qh); free(sh);
     return 0;
 }
@@ -389,14 +391,14 @@ int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr
         for (int m = 0; m < d; ++m)
             acc[m] = 0.0;
         if (cfg->has_shared) {
-            rc = orc_expert_token(d, cfg->shared_ffn, shared, qx, sx, y, NULL, NULL);
+            rc = orc_expert_token(d, cfg->shared_ffn, shared, qx, sx, y, NULL, NULL, NULL);
             if (rc)
                 goto done;
             for (int m = 0; m < d; ++m)
                 acc[m] = (double)y[m];
         }
         for (int i = 0; i < K; ++i) {
-            rc = orc_expert_token(d, cfg->ffn, &experts[ids[t * K + i]], qx, sx, y, NULL, NULL);
+            rc = orc_expert_token(d, cfg->ffn, &experts[ids[t * K + i]], qx, sx, y, NULL, NULL, NULL);
             if (rc)
                 goto done;
             for (int m = 0; m < d; ++m)

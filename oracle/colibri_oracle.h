@@ -97,10 +97,11 @@ int orc_bucket(const int32_t *ids, int64_t T, int k, int E, int32_t *offsets, in
 void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int32_t *dots);
 
 /* One token through one expert of intermediate size f: gate/up group dots, SwiGLU,
- * q8 of h, down group dots. y [d] fp32; qh [f] and sh [f/32] receive h's codes
- * (may be NULL). Returns 0, or -1 on allocation failure. */
+ * q8 of h, down group dots. y [d] fp32; qh [f] and sh [f/32] receive h's codes and h_out
+ * [f] the fp32 h they quantise (each may be NULL). Returns 0, or -1 on allocation
+ * failure. */
 int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const float *sx,
-                     float *y, int8_t *qh, float *sh);
+                     float *y, int8_t *qh, float *sh, float *h_out);
 
 /* The whole layer for T tokens. experts [E] (routed), shared (NULL when !has_shared).
  * ids_in/w_in: when ids_in != NULL the router is skipped and ids_in/w_in [T][k] are used.

@@ -44,7 +44,8 @@ class BlobLayout(ctypes.Structure):
 
 
 class WorkspaceView(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_size_t) for n in ("qx", "sx", "offsets", "pairs", "hq", "hs", "y", "fmax")]
+    _fields_ = [(n, ctypes.c_size_t) for n in ("qx", "sx", "offsets", "pairs", "hq", "hs", "y", "fmax",
+                                               "hs_stride", "hbf")]
 
 
 class CacheStats(ctypes.Structure):

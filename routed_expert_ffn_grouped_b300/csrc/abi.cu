@@ -297,6 +297,8 @@ int colibri_moe_workspace_view(const colibri_layer_cfg *cfg, int T_max, colibri_
     out->hs = L.hs;
     out->y = L.y;
     out->fmax = L.fmax;
+    out->hs_stride = uses_gemm(cfg, T_max) ? L.fmax / G : (size_t)decode_hgs((int)L.fmax);
+    out->hbf = L.hbf;
     return COLIBRI_OK;
 }
 

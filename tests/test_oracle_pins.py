@@ -188,6 +188,53 @@ def test_router_single_group_is_plain_topk(orc):
     assert np.array_equal(ids, want)
 
 
+def test_router_group_size_one_is_plain_topk(orc):
+    """One expert per group: a group's score is its one biased score, so keeping the
+    topk_group best groups and then the top_k best experts in them is the plain top_k."""
+    spec = _cfg(n_exp=32, top_k=4, n_group=32, topk_group=8)
+    rng = np.random.default_rng(15)
+    logits = rng.standard_normal((20, 32)).astype(np.float32)
+    bias = (rng.standard_normal(32) * 0.05).astype(np.float32)
+    ids, w = orc.router_select(spec, logits, bias)
+    s, c = _c_scores(logits, bias)
+    assert np.array_equal(ids, np.argsort(-c, axis=1, kind="stable")[:, :4])
+    sel = np.take_along_axis(s, ids, 1).astype(np.float64)
+    assert np.allclose(w, sel / sel.sum(1, keepdims=True) * 2.5, rtol=1e-6)
+
+
+def test_router_maximum_shape_bruteforce(orc):
+    """The largest router the layer accepts (E = 1024 in 32 groups, top_k = 32): the
+    picks equal a brute force over the group choice followed by a plain sort."""
+    spec = _cfg(n_exp=1024, top_k=32, n_group=32, topk_group=4)
+    rng = np.random.default_rng(16)
+    logits = rng.standard_normal((3, 1024)).astype(np.float32)
+    bias = (rng.standard_normal(1024) * 0.01).astype(np.float32)
+    ids, _ = orc.router_select(spec, logits, bias)
+    _, c = _c_scores(logits, bias)
+    for t in range(3):
+        cg = c[t].astype(np.float64).reshape(32, 32)
+        top2 = np.sort(cg, axis=1)[:, -2:].sum(1)
+        # the best 4 of 32 groups by score (ties: lower index), by exhaustive comparison
+        groups = sorted(range(32), key=lambda g: (-top2[g], g))[:4]
+        assert all(sum(top2[h] > top2[g] for h in range(32)) < 4 for g in groups)
+        allowed = np.array([e for g in sorted(groups) for e in range(32 * g, 32 * g + 32)])
+        order = allowed[np.argsort(-c[t][allowed], kind="stable")][:32]
+        assert ids[t].tolist() == order.tolist()
+
+
+def test_router_softmax_top1_normalised_weight_is_the_scale(orc):
+    """Top-1 softmax routing renormalised over its one pick: the weight is exactly the
+    scale and the id is the argmax of the logits (lowest index on ties)."""
+    spec = _cfg(n_exp=16, top_k=1, router="softmax", norm_topk=True, routed_scale=1.0)
+    rng = np.random.default_rng(17)
+    logits = rng.standard_normal((12, 16)).astype(np.float32)
+    logits[0, 3] = logits[0, 9] = logits[0].max() + 1.0
+    ids, w = orc.router_select(spec, logits, None)
+    assert ids[:, 0].tolist() == np.argmax(logits, axis=1).tolist()
+    assert ids[0, 0] == 3
+    assert np.all(w == 1.0)
+
+
 def test_router_grouped_bruteforce_subsets(orc):
     """Exhaustive search over group subsets and expert subsets (E=16, no ties)."""
     spec = _cfg(n_exp=16, top_k=4, n_group=4, topk_group=2)
@@ -271,11 +318,14 @@ def test_expert_matches_dequantised_fp64_matmul(orc):
     v = synth.expert_views(blob, spec.d, spec.ffn)
     x = synth.activations(spec, 0, 1)[0]
     qx, sx = orc.q8_quantize(x)
-    y, qh, sh = orc.expert_token(v, qx, sx)
+    y, qh, sh, h32 = orc.expert_token(v, qx, sx, want_h=True)
     xh = qx.astype(np.float64) * np.repeat(sx.astype(np.float64), 32)
     gate = _dequant(v["w1"], v["s1"]) @ xh
     up = _dequant(v["w3"], v["s3"]) @ xh
     h = gate / (1 + np.exp(-gate)) * up
+    # the oracle's h is this h rounded once to fp32
+    assert np.all(np.abs(h32.astype(np.float64) - h) <= 2.0 ** -24 * np.abs(h) * (1 + 1e-9) + 1e-30)
+    assert np.array_equal(orc.q8_quantize(h32)[0], qh)
     # h codes from the oracle's own q8 of h: check they quantise this h
     hh = qh.astype(np.float64) * np.repeat(sh.astype(np.float64), 32)
     assert np.max(np.abs(hh - h)) <= np.max(sh) * 0.5 * (1 + 1e-5)
