@@ -3,6 +3,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kernels.cuh"
 #include "workspace.h"
@@ -181,9 +182,11 @@ int colibri_q8_quantize(const float *x, int rows, int cols, int8_t *q, float *sc
 // than the largest limit set so far (the limits only grow). The default limit covers
 // 48 KB of static plus dynamic shared memory together, so even a launch just under it
 // sets the attribute.
-// Tracked per device: the attribute belongs to the device's context.
+// Tracked per device: the attribute belongs to the device's context. Host threads that
+// launch at the same time take the lock, so the attribute and the record of it agree.
 constexpr int kMaxDev = 64;
 struct SmemLimits {
+    std::mutex mu;
     size_t have[kMaxDev] = {};
 };
 
@@ -192,6 +195,7 @@ static bool smem_attr(const void *fn, size_t bytes, SmemLimits &lim)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
         return false;
+    std::lock_guard<std::mutex> lock(lim.mu);
     if (bytes <= lim.have[dev])
         return true;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
