@@ -83,6 +83,10 @@ def lib() -> ctypes.CDLL:
                 "orc_moe_layer": (_I, [ctypes.POINTER(Cfg), _P, _I64, _P, _P,
                                        ctypes.POINTER(Expert), ctypes.POINTER(Expert),
                                        _P, _P, _P, _P, _P]),
+                "orc_expert_token_f32": (_I, [_I, _I, ctypes.POINTER(Expert), _P, _P, _P]),
+                "orc_moe_layer_f32": (_I, [ctypes.POINTER(Cfg), _P, _I64, _P, _P,
+                                           ctypes.POINTER(Expert), ctypes.POINTER(Expert),
+                                           _P, _P, _P, _P, _P]),
                 "orc_lru_trace": (_I, [_I, _I64, _P, _P, _P]),
                 "orc_lru_hot_trace": (_I, [_I, _I, _I64, _P, _P, _P]),
             }
@@ -209,9 +213,25 @@ def expert_token(views: dict, qx: np.ndarray, sx: np.ndarray, want_h: bool = Fal
     return (y, qh, sh, h) if want_h else (y, qh, sh)
 
 
-def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None):
+def expert_token_f32(views: dict, x: np.ndarray):
+    """One token through one expert on fp32 activations; returns (y, h)."""
+    ex, keep = make_expert(views)
+    f = keep[0].shape[0]
+    d = 2 * keep[0].shape[1]
+    x = _c(x, np.float32)
+    y = np.empty(d, np.float32)
+    h = np.empty(f, np.float32)
+    if lib().orc_expert_token_f32(d, f, ctypes.byref(ex), _ptr(x), _ptr(y), _ptr(h)):
+        raise MemoryError("orc_expert_token_f32")
+    return y, h
+
+
+def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None, act="q8"):
     """The whole layer; ``experts`` is a list of E view dicts (or a callable e -> view dict,
-    used only for the selected ids). Returns (out, ids, w)."""
+    used only for the selected ids). act = "q8" (int8 activations, the layer's main form)
+    or "f32" (fp32 activations). Returns (out, ids, w)."""
+    if act not in ("q8", "f32"):
+        raise ValueError(act)
     cfg = spec_or_cfg if isinstance(spec_or_cfg, Cfg) else make_cfg(spec_or_cfg)
     x = _c(x, np.float32)
     T = x.shape[0]
@@ -239,7 +259,8 @@ def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None):
         sh_ex, k = make_expert(shared)
         keep.append(k)
     out = np.empty((T, cfg.d), np.float32)
-    rc = lib().orc_moe_layer(ctypes.byref(cfg), _ptr(x), T, None if Wr is None else _ptr(_c(Wr, np.float32)),
+    fn = lib().orc_moe_layer if act == "q8" else lib().orc_moe_layer_f32
+    rc = fn(ctypes.byref(cfg), _ptr(x), T, None if Wr is None else _ptr(_c(Wr, np.float32)),
                              None if bias is None else _ptr(_c(bias, np.float32)), table,
                              ctypes.byref(sh_ex) if sh_ex is not None else None,
                              _ptr(ids_r), _ptr(w_r), None, None, _ptr(out))

@@ -347,15 +347,52 @@ int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const
     return 0;
 }
 
+/* ---- one token through one SwiGLU expert, activations kept in fp32 ------------------
+ * The decode variant of the dashen-tech guide ("Analyse approfondie", step 3: one-token
+ * decode runs on f32 activations) with the same int4 group-scaled weights:
+ * gate_n = sum_k s1[n][k/32] * q1[n][k] * x[k] and up_n likewise (fp64, k ascending);
+ * h_n = silu(gate_n) * up_n rounded to fp32; y_m = sum_j s2[m][j/32] * q2[m][j] * h_j
+ * (fp64, j ascending) rounded to fp32. Nothing is quantised but the weights. */
+static double dot_row_f32(const uint8_t *wrow, const float *srow, const float *v, int K, int8_t *q)
+{
+    orc_unpack_int4(wrow, K / 2, q);
+    double acc = 0.0;
+    for (int k = 0; k < K; ++k)
+        acc += (double)srow[k / ORC_GROUP] * (double)q[k] * (double)v[k];
+    return acc;
+}
+
+int orc_expert_token_f32(int d, int f, const orc_expert *ex, const float *x, float *y, float *h_out)
+{
+    const int ngd = d / ORC_GROUP, ngf = f / ORC_GROUP;
+    int8_t *q = (int8_t *)malloc((size_t)(d > f ? d : f));
+    float *h = (float *)malloc(sizeof(float) * (size_t)f);
+    if (!q || !h) {
+        free(q); free(h);
+        return -1;
+    }
+    for (int n = 0; n < f; ++n) {
+        const double gate = dot_row_f32(ex->w1 + (int64_t)n * (d / 2), ex->s1 + (int64_t)n * ngd, x, d, q);
+        const double up = dot_row_f32(ex->w3 + (int64_t)n * (d / 2), ex->s3 + (int64_t)n * ngd, x, d, q);
+        h[n] = (float)(gate / (1.0 + exp(-gate)) * up);
+    }
+    for (int m = 0; m < d; ++m)
+        y[m] = (float)dot_row_f32(ex->w2 + (int64_t)m * (f / 2), ex->s2 + (int64_t)m * ngf, h, f, q);
+    if (h_out)
+        memcpy(h_out, h, sizeof(float) * (size_t)f);
+    free(q); free(h);
+    return 0;
+}
+
 /* ---- the layer --------------------------------------------------------------------
  * Per token t: route (or take the given ids and weights), q8 the token, run the
  * shared expert (weight 1, not scaled) and each selected expert, and combine
  * out[t] = y_shared + sum_i w[t][i] * y_i in fp64 in selection order, rounded to fp32.
  * Tokens are independent of one another. */
-int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr,
-                  const float *bias, const orc_expert *experts, const orc_expert *shared,
-                  const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
-                  float *out)
+static int moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr,
+                     const float *bias, const orc_expert *experts, const orc_expert *shared,
+                     const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
+                     float *out, int act_f32)
 {
     if (!cfg_ok(cfg) || T < 0 || (cfg->has_shared && !shared))
         return -1;
@@ -387,18 +424,23 @@ int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr
             goto done;
     }
     for (int64_t t = 0; t < T; ++t) {
-        orc_q8_quantize(x + t * d, 1, d, qx, sx);
+        const float *xt = x + t * d;
+        if (!act_f32)
+            orc_q8_quantize(xt, 1, d, qx, sx);
         for (int m = 0; m < d; ++m)
             acc[m] = 0.0;
         if (cfg->has_shared) {
-            rc = orc_expert_token(d, cfg->shared_ffn, shared, qx, sx, y, NULL, NULL, NULL);
+            rc = act_f32 ? orc_expert_token_f32(d, cfg->shared_ffn, shared, xt, y, NULL)
+                         : orc_expert_token(d, cfg->shared_ffn, shared, qx, sx, y, NULL, NULL, NULL);
             if (rc)
                 goto done;
             for (int m = 0; m < d; ++m)
                 acc[m] = (double)y[m];
         }
         for (int i = 0; i < K; ++i) {
-            rc = orc_expert_token(d, cfg->ffn, &experts[ids[t * K + i]], qx, sx, y, NULL, NULL, NULL);
+            const orc_expert *ex = &experts[ids[t * K + i]];
+            rc = act_f32 ? orc_expert_token_f32(d, cfg->ffn, ex, xt, y, NULL)
+                         : orc_expert_token(d, cfg->ffn, ex, qx, sx, y, NULL, NULL, NULL);
             if (rc)
                 goto done;
             for (int m = 0; m < d; ++m)
@@ -414,6 +456,23 @@ int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr
 done:
     free(ids); free(w); free(qx); free(sx); free(y); free(acc);
     return rc;
+}
+
+int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr,
+                  const float *bias, const orc_expert *experts, const orc_expert *shared,
+                  const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
+                  float *out)
+{
+    return moe_layer(cfg, x, T, Wr, bias, experts, shared, ids_in, w_in, ids_out, w_out, out, 0);
+}
+
+/* The same layer with every expert on fp32 activations (orc_expert_token_f32). */
+int orc_moe_layer_f32(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr,
+                      const float *bias, const orc_expert *experts, const orc_expert *shared,
+                      const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
+                      float *out)
+{
+    return moe_layer(cfg, x, T, Wr, bias, experts, shared, ids_in, w_in, ids_out, w_out, out, 1);
 }
 
 /* ---- LRU cache trace -----------------------------------------------------------

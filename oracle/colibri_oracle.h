@@ -103,6 +103,12 @@ void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t co
 int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const float *sx,
                      float *y, int8_t *qh, float *sh, float *h_out);
 
+/* One token through one expert on fp32 activations (the f32 decode variant): gate and
+ * up are fp64 sums over k of scale * int4 code * x[k], h = silu(gate) * up rounded to
+ * fp32, y = the same sums of W2 against h. x [d], y [d]; h_out [f] may be NULL.
+ * Returns 0, or -1 on allocation failure. */
+int orc_expert_token_f32(int d, int f, const orc_expert *ex, const float *x, float *y, float *h_out);
+
 /* The whole layer for T tokens. experts [E] (routed), shared (NULL when !has_shared).
  * ids_in/w_in: when ids_in != NULL the router is skipped and ids_in/w_in [T][k] are used.
  * ids_out/w_out (may be NULL) receive the ids and weights used. out [T][d].
@@ -111,6 +117,11 @@ int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr
                   const float *bias, const orc_expert *experts, const orc_expert *shared,
                   const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
                   float *out);
+/* orc_moe_layer with every expert on fp32 activations (orc_expert_token_f32). */
+int orc_moe_layer_f32(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr,
+                      const float *bias, const orc_expert *experts, const orc_expert *shared,
+                      const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
+                      float *out);
 
 /* LRU cache trace. ops: kind 0 = start of a lookup batch (unpins every key),
  * kind 1 = lookup key (demand), kind 2 = stage key (prefetch). result per op:

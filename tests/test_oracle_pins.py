@@ -353,6 +353,60 @@ def test_single_expert_layer_is_dense_swiglu(orc):
         assert np.max(np.abs(out[t] - ref)) <= 1e-6 * np.max(np.abs(ref))
 
 
+def test_f32_expert_equals_q8_expert_when_x_is_exactly_q8(orc):
+    """When every group of x is exactly a q8 grid (integer codes with |q| = 127 at the
+    group's maximum, a power-of-two step), q8 of x changes nothing, so the fp32-activation
+    expert and the int8 one compute the same h: equal up to the last bit of fp32."""
+    spec = synth.TINY
+    blob = synth.expert_blob(spec, 0, 0, 5)
+    v = synth.expert_views(blob, spec.d, spec.ffn)
+    rng = np.random.default_rng(21)
+    codes = rng.integers(-126, 127, spec.d)
+    codes[::32] = 127 * rng.choice([-1, 1], spec.d // 32)      # each group's amax code
+    step = 2.0 ** rng.integers(-9, -3, spec.d // 32)
+    x = (codes * np.repeat(step, 32)).astype(np.float32)
+    qx, sx = orc.q8_quantize(x)
+    assert np.array_equal(qx, codes) and np.array_equal(sx, step.astype(np.float32))
+    _, _, _, h_q8 = orc.expert_token(v, qx, sx, want_h=True)
+    y32, h_f32 = orc.expert_token_f32(v, x)
+    ulp = np.abs(h_q8.view(np.int32).astype(np.int64) - h_f32.view(np.int32).astype(np.int64))
+    assert ulp.max() <= 1 and (ulp == 0).mean() > 0.99
+    # and y is W2 applied to that fp32 h (fp64 dequantised matmul)
+    ref = _dequant(v["w2"], v["s2"]) @ h_f32.astype(np.float64)
+    assert np.max(np.abs(y32 - ref)) <= 1e-6 * np.max(np.abs(ref))
+
+
+def test_f32_single_expert_layer_is_dense_swiglu(orc):
+    """E = k = 1, scale 1, no shared expert, fp32 activations: one dense SwiGLU FFN of
+    the dequantised weights applied to x itself."""
+    spec = synth.TINY.replace(n_exp=1, top_k=1, n_group=1, topk_group=1, routed_scale=1.0,
+                              has_shared=False, shared_ffn=0, bias="none")
+    layer = synth.make_layer(spec, 2)
+    x = synth.activations(spec, 2, 3)
+    out, ids, w = orc.moe_layer(spec, x, layer.Wr, None, [layer.expert(0)], act="f32")
+    assert ids.tolist() == [[0]] * 3 and np.all(w == 1.0)
+    v = layer.expert(0)
+    g = _dequant(v["w1"], v["s1"]) @ x.T.astype(np.float64)
+    u = _dequant(v["w3"], v["s3"]) @ x.T.astype(np.float64)
+    h = (g / (1 + np.exp(-g)) * u).astype(np.float32).astype(np.float64)
+    ref = (_dequant(v["w2"], v["s2"]) @ h).T
+    assert np.max(np.abs(out - ref)) <= 1e-6 * np.max(np.abs(ref))
+
+
+def test_f32_layer_combine(orc):
+    """The fp32-activation layer combines its experts' outputs like the int8 one."""
+    spec = synth.TINY
+    layer = synth.make_layer(spec, 0)
+    x = synth.activations(spec, 0, 3)
+    out, ids, w = orc.moe_layer(spec, x, layer.Wr, layer.bias, layer.expert, layer.shared(), act="f32")
+    for t in range(3):
+        acc = orc.expert_token_f32(layer.shared(), x[t])[0].astype(np.float64)
+        for i in range(spec.top_k):
+            y = orc.expert_token_f32(layer.expert(int(ids[t, i])), x[t])[0].astype(np.float64)
+            acc += np.float64(w[t, i]) * y
+        assert np.array_equal(out[t], acc.astype(np.float32))
+
+
 def test_layer_combine_and_linearity(orc):
     spec = synth.TINY
     layer = synth.make_layer(spec, 0)
