@@ -48,6 +48,9 @@ WORKLOADS = {
     "olmoe_decode_t16": ("olmoe", 16, False),
     "glm52_prefill_t2048": ("glm52", 2048, True),
     "glm52_stream_8l": ("glm52", 1, False),
+    # the decode variant on fp32 activations (colibri_moe_layer_f32)
+    "glm52_decode_t1_f32": ("glm52", 1, False),
+    "glm52_decode_t4_f32": ("glm52", 4, False),
 }
 DEFAULT_WORKLOAD = "glm52_decode_t1"
 N_X = 64                 # distinct activation batches cycled through
@@ -218,13 +221,17 @@ def blob_bytes(spec, f):
 
 
 # ---------------------------------------------------------------- oracle timing
-def oracle_tokens_per_s(spec, host, xs, budget_s: float, max_tokens: int):
+def is_f32(workload: str) -> bool:
+    return workload.endswith("_f32")
+
+
+def oracle_tokens_per_s(spec, host, xs, budget_s: float, max_tokens: int, act: str = "q8"):
     import oracle
     oracle.lib()
     t0 = time.perf_counter()
     n = 0
     while n < max_tokens:
-        oracle.moe_layer(spec, xs[n % len(xs)], host.Wr, host.bias, host.expert, host.shared())
+        oracle.moe_layer(spec, xs[n % len(xs)], host.Wr, host.bias, host.expert, host.shared(), act=act)
         n += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -246,6 +253,12 @@ def run_reference(args):
     xs = [synth.activations(spec, args.seed, 1, step=i, row_scale=row_scale)[0] for i in range(N_X)]
     per_tok = spec.top_k + (1 if spec.has_shared else 0)
     state = {"tok": -1}
+    f32 = is_f32(args.workload)
+
+    def expert(views):
+        if f32:
+            return oracle.expert_token_f32(views, state["x"])[0]
+        return oracle.expert_token(views, state["q"], state["s"])[0]
 
     def step(i):
         t, slot = divmod(i, per_tok)
@@ -253,13 +266,11 @@ def run_reference(args):
         if slot == 0 or state["tok"] != t:
             q, s = oracle.q8_quantize(x)
             ids, w = oracle.router_topk(spec, x[None], host.Wr, host.bias)
-            state.update(tok=t, q=q, s=s, ids=ids[0], w=w[0], acc=np.zeros(spec.d))
+            state.update(tok=t, x=x, q=q, s=s, ids=ids[0], w=w[0], acc=np.zeros(spec.d))
         if spec.has_shared and slot == per_tok - 1:
-            y, _, _ = oracle.expert_token(host.shared(), state["q"], state["s"])
-            state["acc"] += y
+            state["acc"] += expert(host.shared())
         elif slot < spec.top_k:
-            y, _, _ = oracle.expert_token(host.expert(int(state["ids"][slot])), state["q"], state["s"])
-            state["acc"] += float(state["w"][slot]) * y
+            state["acc"] += float(state["w"][slot]) * expert(host.expert(int(state["ids"][slot])))
 
     for i in range(args.warmup):
         step(i)
@@ -272,7 +283,8 @@ def run_reference(args):
               f"one expert pass of one token per step, single-threaded C oracle")
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8xi4->i32, f64",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "i4 x f32 -> f64" if f32 else "i8xi4->i32, f64",
             "data": "synthetic", "config": workload_config(spec, args.workload, T),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -282,13 +294,16 @@ def run_reference(args):
 DECODE_T_MAX = 32   # largest T on the decode (GEMV) path; larger T takes the tcgen05 GEMMs
 
 
-def launches_per_step(T: int, n_exp: int, ids_given: bool) -> int:
+def launches_per_step(T: int, n_exp: int, ids_given: bool, f32: bool = False) -> int:
     """Kernels one colibri_moe_layer call launches. Decode (T <= 32): one routing kernel
     (router logits and scores with q8 of x, or q8 alone with the ids given), a selection
     kernel when T x E > 4096 (else every CTA of the next kernel selects), then one kernel
     for selection or bucketing, gate/up, down and combine. Prefill: q8, router logits,
     selection, bucketing (q8 and bucketing alone with the ids given), the two tcgen05 GEMMs
-    and the combine."""
+    and the combine. The fp32-activation decode: router logits and selection (unless the
+    ids are given), gate/up, down and the combine."""
+    if f32:
+        return 3 if ids_given else 5
     if T <= DECODE_T_MAX:
         if ids_given:
             return 2
@@ -303,7 +318,8 @@ def workload_config(spec, workload, T):
             "l2": ("between timed steps a 256 MB buffer is written and another 256 MB buffer read, then "
                    "one call of the layer before (same shape, its own weights at other addresses): "
                    "code and small tables warm, none of this layer's weights, router or shared expert in L2"),
-            "timing": "CUDA events per step around one CUDA-graph replay"}
+            "timing": "CUDA events per step around one CUDA-graph replay",
+            "activations": "fp32" if is_f32(workload) else "int8 (per-32-group absmax)"}
 
 
 # ---------------------------------------------------------------- expert streaming
@@ -496,7 +512,10 @@ def run_colibri(args):
     out = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
     ids = torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
     w = torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
-    ws = torch.empty(C.colibri_moe_workspace_bytes(dl.cfg, T), dtype=torch.uint8, device="cuda")
+    f32 = is_f32(args.workload)
+    layer_fn = C.colibri_moe_layer_f32 if f32 else C.colibri_moe_layer
+    ws_bytes = (C.colibri_moe_f32_workspace_bytes if f32 else C.colibri_moe_workspace_bytes)(dl.cfg, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     scrub = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     # the layer before: same shape, its own weights (as in a model, where the previous
@@ -510,8 +529,8 @@ def run_colibri(args):
     ids_log = torch.empty((W + K, T, spec.top_k), dtype=torch.int32, device="cuda")
 
     def layer():
-        C.colibri_moe_layer(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws,
-                            stream=torch.cuda.current_stream())
+        layer_fn(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws,
+                 stream=torch.cuda.current_stream())
 
     with torch.cuda.stream(stream):
         x.copy_(xs[0])
@@ -521,8 +540,8 @@ def run_colibri(args):
         if st != C.OK:
             raise RuntimeError(f"layer reported device error {st}")
     def layer_prev():
-        C.colibri_moe_layer(prev.cfg, x_prev, prev.Wr, prev.bias, prev.table, prev.shared, ids_prev, w_prev, False,
-                            out_prev, ws_prev, stream=torch.cuda.current_stream())
+        layer_fn(prev.cfg, x_prev, prev.Wr, prev.bias, prev.table, prev.shared, ids_prev, w_prev, False,
+                 out_prev, ws_prev, stream=torch.cuda.current_stream())
 
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
@@ -609,7 +628,14 @@ def run_colibri(args):
             # GEMM, all expert weights for the fused decode kernel
             prof_bytes.append(u * gu_b + sh[1] if prefill else u * nb + sh[0])
     mean = {k: float(np.mean(v)) for k, v in prof.items()}
-    if prefill:
+    if f32:
+        kern_ms = {"k_route_logits": mean["router_logits"], "k_router_select": mean["router_select"],
+                   "k_f32_gateup": mean["gateup"], "k_f32_down": mean["down"], "k_combine": mean["combine"],
+                   "event_records": mean["q8"] + mean["bucket"]}
+        roof_ms = np.array(prof["gateup"]) + np.array(prof["down"])
+        gu_kernel = "k_f32_gateup + k_f32_down (fp32 activations; weights read once per pair)"
+        traffic = None
+    elif prefill:
         kern_ms = {"k_q8 + k_route_logits_tiled": mean["router_logits"], "k_router_select": mean["router_select"],
                    "k_bucket": mean["bucket"], "k_gemm<0>": mean["gateup"], "k_gemm<1>": mean["down"],
                    "k_combine": mean["combine"]}
@@ -640,7 +666,8 @@ def run_colibri(args):
     # x from pinned host memory in, out (and the device error flag) back to pinned host
     x_pin = torch.from_numpy(xs_host).pin_memory()
     out_pin = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
-    ws_host = torch.empty(C.colibri_moe_host_workspace_bytes(dl.cfg, T), dtype=torch.uint8, device="cuda")
+    ws_host = None if f32 else torch.empty(C.colibri_moe_host_workspace_bytes(dl.cfg, T), dtype=torch.uint8,
+                                           device="cuda")
     KE = min(K, 500)
     e2e_s = 0.0
     with torch.cuda.stream(stream):
@@ -650,8 +677,14 @@ def run_colibri(args):
             graph_prev.replay()
             stream.synchronize()
             t0 = time.perf_counter()
-            C.colibri_moe_layer_host(dl.cfg, x_pin[i % N_X], dl.Wr, dl.bias, dl.table, dl.shared, None, None,
-                                     False, out_pin, ws_host, stream=stream)
+            if f32:
+                x.copy_(x_pin[i % N_X], non_blocking=True)
+                layer_fn(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws, stream=stream)
+                out_pin.copy_(out, non_blocking=True)
+                stream.synchronize()
+            else:
+                C.colibri_moe_layer_host(dl.cfg, x_pin[i % N_X], dl.Wr, dl.bias, dl.table, dl.shared, None, None,
+                                         False, out_pin, ws_host, stream=stream)
             e2e_s += time.perf_counter() - t0
     e2e_s = allreduce_max(torch, world, e2e_s)
     e2e_value = world * T * KE / e2e_s
@@ -661,7 +694,8 @@ def run_colibri(args):
         # batches of at most 8 of the workload's tokens: the oracle's work per token does
         # not depend on the batch, and a 2048-token batch would run for minutes
         tb = min(T, 8)
-        rate, n, dt = oracle_tokens_per_s(spec, host, [xs_host[i][:tb] for i in range(N_X)], 15.0, 64)
+        rate, n, dt = oracle_tokens_per_s(spec, host, [xs_host[i][:tb] for i in range(N_X)], 15.0, 64,
+                                          act="f32" if f32 else "q8")
         cpu = {"value": rate * tb, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} batches of {tb} tokens of {args.workload} through the C oracle "
                          f"({dt:.1f} s, single-threaded)"}
@@ -670,7 +704,8 @@ def run_colibri(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": ("bf16xbf16->f32 (int4 and q8 codes, exact in bf16)" if prefill else "i8xi4->i32, f32"),
+            "dtype": ("i4 x f32 -> f32" if f32 else "bf16xbf16->f32 (int4 and q8 codes, exact in bf16)" if prefill
+                      else "i8xi4->i32, f32"),
             "data": "synthetic",
             "config": workload_config(spec, args.workload, T),
             "expert_hbm_gbs": layer_gbs, "expert_hbm_frac": layer_gbs / hbm_peak,
@@ -685,10 +720,11 @@ def run_colibri(args):
                             "note": "informational; the headline value flushes L2 between steps"},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * spec.d * 4,
-                    "d2h_bytes_per_step": T * spec.d * 4 + 4, "steps": KE,
-                    "path": "colibri_moe_layer_host (pinned host x and out, the error flag read back) "
-                            "via the Python binding, eager launches"},
-            "gpu_launches": launches_per_step(T, spec.n_exp, False) * K,
+                    "d2h_bytes_per_step": T * spec.d * 4 + (0 if f32 else 4), "steps": KE,
+                    "path": ("colibri_moe_layer_f32 between pinned-host copies of x and out, eager launches"
+                             if f32 else "colibri_moe_layer_host (pinned host x and out, the error flag read "
+                             "back) via the Python binding, eager launches")},
+            "gpu_launches": launches_per_step(T, spec.n_exp, False, f32) * K,
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)

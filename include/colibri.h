@@ -189,6 +189,23 @@ int colibri_moe_layer_noalloc(const colibri_layer_cfg *cfg, const float *x, int 
                               const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
                               float *out, void *stream);
 
+/* The layer on fp32 activations, for decode (T <= 32): the token is not quantised, as in
+ * the pages' one-token decode ("Analyse approfondie", step 3 of the dashen-tech guide),
+ * against the same int4 group-scaled weights. For each pair (token, selected or shared
+ * expert): gate_n = sum_g s1[n][g] * sum_k q1[n][k] x[k] and up_n likewise in fp32, h =
+ * silu(gate) * up in fp32, y_m = sum_g s2[m][g] * sum_j q2[m][j] h[j]; out as in
+ * colibri_moe_layer. Routing is colibri_router_topk's. Weights are read once per pair.
+ *   Arguments, layouts and ownership as for colibri_moe_layer, except the workspace:
+ *   >= colibri_moe_f32_workspace_bytes(cfg, T) bytes, 256-byte aligned (0 from that
+ *   function for a bad configuration or T_max > 32). colibri_workspace_status reads its
+ *   error flag. A given id outside [0, E) sets the flag and its pair contributes nothing;
+ *   a repeated id is computed twice. Returns COLIBRI_E_INVAL for T > 32. T == 0 is a no-op. */
+size_t colibri_moe_f32_workspace_bytes(const colibri_layer_cfg *cfg, int T_max);
+int colibri_moe_layer_f32(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                          const float *bias, const colibri_expert *experts,
+                          const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
+                          float *out, void *workspace, size_t ws_bytes, void *stream);
+
 /* colibri_moe_layer on HOST buffers, as one blocking call: the layer computed on the
  * host side of the hybrid CPU/GPU engine of the pages ("Streaming d'experts", "Guide
  * Complet de Colibri") hands one step's activations to the GPU and takes the output back.

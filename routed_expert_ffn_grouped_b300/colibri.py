@@ -69,6 +69,9 @@ SIGNATURES = {
     "colibri_moe_workspace_bytes": (_SZ, [_PCFG, _I]),
     "colibri_moe_layer": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
                                _SZ, _P]),
+    "colibri_moe_f32_workspace_bytes": (_SZ, [_PCFG, _I]),
+    "colibri_moe_layer_f32": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
+                                   _SZ, _P]),
     "colibri_moe_host_workspace_bytes": (_SZ, [_PCFG, _I]),
     "colibri_moe_layer_host": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
                                     _SZ, _P]),
@@ -187,6 +190,24 @@ def colibri_moe_layer(cfg: LayerCfg, x, Wr, bias, experts, shared: Expert | None
                                    ctypes.byref(shared) if shared is not None else None, _ptr(ids), _ptr(w),
                                    int(bool(ids_given)), _ptr(out), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))
+
+
+def colibri_moe_f32_workspace_bytes(cfg: LayerCfg, T_max: int) -> int:
+    n = lib().colibri_moe_f32_workspace_bytes(ctypes.byref(cfg), T_max)
+    if n == 0:
+        raise ColibriError("colibri_moe_f32_workspace_bytes", E_INVAL, "invalid configuration or T_max > 32")
+    return n
+
+
+def colibri_moe_layer_f32(cfg: LayerCfg, x, Wr, bias, experts, shared: Expert | None, ids, w, ids_given: bool,
+                          out, workspace, stream=None):
+    """The layer on fp32 activations (decode, T <= 32); arguments as colibri_moe_layer."""
+    T = x.shape[0]
+    _check("colibri_moe_layer_f32",
+           lib().colibri_moe_layer_f32(ctypes.byref(cfg), _ptr(x), T, _ptr(Wr), _ptr(bias), _ptr(experts),
+                                       ctypes.byref(shared) if shared is not None else None, _ptr(ids), _ptr(w),
+                                       int(bool(ids_given)), _ptr(out), _ptr(workspace), workspace.numel(),
+                                       _stream(stream)))
 
 
 def colibri_moe_host_workspace_bytes(cfg: LayerCfg, T_max: int) -> int:

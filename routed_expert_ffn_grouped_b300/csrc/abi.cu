@@ -511,6 +511,110 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     return COLIBRI_OK;
 }
 
+// Workspace of colibri_moe_layer_f32: error flag | logits [T][E] | h [PT][fmax] |
+// y [PT][d], PT = T*K (+ T with a shared expert), each part 256-byte aligned. The error
+// flag sits at offset 0, as in colibri_moe_layer's workspace.
+struct F32Layout {
+    size_t err, logits, h, y, fmax, pt, total;
+};
+
+static F32Layout f32_layout(const colibri_layer_cfg *c, int T)
+{
+    F32Layout L{};
+    L.fmax = c->has_shared && c->shared_ffn > c->ffn ? c->shared_ffn : c->ffn;
+    L.pt = (size_t)T * c->top_k + (c->has_shared ? (size_t)T : 0);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = (o + bytes + 255) & ~size_t(255);
+        return at;
+    };
+    L.err = take(256);
+    L.logits = take(4 * (size_t)T * c->n_exp);
+    L.h = take(4 * L.pt * L.fmax);
+    L.y = take(4 * L.pt * c->d);
+    L.total = o;
+    return L;
+}
+
+size_t colibri_moe_f32_workspace_bytes(const colibri_layer_cfg *cfg, int T_max)
+{
+    if (!cfg_valid(cfg) || T_max < 0 || T_max > DECODE_T_MAX)
+        return 0;
+    return f32_layout(cfg, T_max).total;
+}
+
+int colibri_moe_layer_f32(const colibri_layer_cfg *cfg, const float *x, int T, const float *Wr,
+                          const float *bias, const colibri_expert *experts,
+                          const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
+                          float *out, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!cfg_valid(cfg) || T < 0 || T > DECODE_T_MAX)
+        return COLIBRI_E_INVAL;
+    if (T == 0)
+        return COLIBRI_OK;
+    if (!x || !experts || !ids || !w || !out || !workspace)
+        return COLIBRI_E_INVAL;
+    if (cfg->has_shared && !shared)
+        return COLIBRI_E_INVAL;
+    if (!ids_given && (!Wr || !aligned(Wr, 16)))
+        return COLIBRI_E_INVAL;
+    if (!aligned(workspace, 256) || !aligned(out, 16) || !aligned(x, 16))
+        return COLIBRI_E_INVAL;
+    const F32Layout L = f32_layout(cfg, T);
+    if (ws_bytes < L.total)
+        return COLIBRI_E_NOMEM;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *ws = static_cast<char *>(workspace);
+    int *err = reinterpret_cast<int *>(ws + L.err);
+    float *lg = reinterpret_cast<float *>(ws + L.logits);
+    if (cudaMemsetAsync(ws + L.err, 0, 256, s) != cudaSuccess)
+        return COLIBRI_E_CUDA;
+    // profiling slots: as colibri_moe_layer's prefill path (no q8, no bucketing)
+    if (prof_mark(0, s) || prof_mark(1, s))
+        return COLIBRI_E_CUDA;
+    if (!ids_given) {
+        const Q8Args none{};
+        if (launch_route_logits(cfg, x, T, Wr, bias, lg, nullptr, nullptr, none, err, s) || prof_mark(2, s))
+            return COLIBRI_E_CUDA;
+        if (launch_select(select_args(cfg, T, lg, nullptr, nullptr, bias, ids, w), s) || prof_mark(3, s))
+            return COLIBRI_E_CUDA;
+    } else if (prof_mark(2, s) || prof_mark(3, s)) {
+        return COLIBRI_E_CUDA;
+    }
+    if (prof_mark(4, s))
+        return COLIBRI_E_CUDA;
+    F32Args fa{};
+    fa.experts = experts;
+    if (cfg->has_shared)
+        fa.shared = *shared;
+    fa.ids = ids;
+    fa.x = x;
+    fa.h = reinterpret_cast<float *>(ws + L.h);
+    fa.y = reinterpret_cast<float *>(ws + L.y);
+    fa.T = T;
+    fa.K = cfg->top_k;
+    fa.E = cfg->n_exp;
+    fa.d = cfg->d;
+    fa.ffn = cfg->ffn;
+    fa.shared_ffn = cfg->shared_ffn;
+    fa.has_shared = cfg->has_shared;
+    fa.fmax = (int)L.fmax;
+    fa.err = err;
+    const unsigned pt = (unsigned)L.pt;
+    k_f32_gateup<<<dim3((unsigned)(L.fmax / G), pt), 256, f32_smem_gateup(cfg->d), s>>>(fa);
+    if (cudaGetLastError() != cudaSuccess || prof_mark(5, s))
+        return COLIBRI_E_CUDA;
+    k_f32_down<<<dim3((unsigned)(cfg->d / G), pt), 256, f32_smem_down((int)L.fmax), s>>>(fa);
+    if (cudaGetLastError() != cudaSuccess || prof_mark(6, s))
+        return COLIBRI_E_CUDA;
+    CombineArgs ca{fa.y, w, T, cfg->top_k, cfg->d, cfg->has_shared, out};
+    k_combine<<<dim3((unsigned)((cfg->d / 4 + 255) / 256), (unsigned)T), 256, 0, s>>>(ca);
+    if (cudaGetLastError() != cudaSuccess || prof_mark(7, s))
+        return COLIBRI_E_CUDA;
+    return COLIBRI_OK;
+}
+
 int colibri_moe_profile_enable(int on)
 {
     if (on && !g_prof.ev[0]) {

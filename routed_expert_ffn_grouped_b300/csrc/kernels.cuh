@@ -126,6 +126,22 @@ cudaError_t launch_gemm(int mode, const GemmArgs &a, cudaStream_t s);
 __global__ void k_debug_umma(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, int *err);
 size_t debug_umma_smem(int n, int k);
 
+// Decode on fp32 activations (kernels_f32act.cu).
+struct F32Args {
+    const colibri_expert *experts;  // device table [E]
+    colibri_expert shared;          // members are device pointers (unused when !has_shared)
+    const int32_t *ids;             // [T][K]
+    const float *x;                 // [T][d]
+    float *h;                       // [T*K + T][fmax]: pairs, then the shared expert's rows
+    float *y;                       // [T*K + T][d]
+    int T, K, E, d, ffn, shared_ffn, has_shared, fmax;
+    int *err;
+};
+__global__ void k_f32_gateup(F32Args a);
+__global__ void k_f32_down(F32Args a);
+size_t f32_smem_gateup(int d);
+size_t f32_smem_down(int fmax);
+
 struct CombineArgs {
     const float *y;
     const float *w;

@@ -54,6 +54,8 @@ def test_workspace_bytes_and_config_checks(lib):
         cfg = C.layer_cfg(spec)
         assert C.colibri_moe_workspace_bytes(cfg, 4) > 0
         assert C.colibri_moe_workspace_bytes(cfg, 2048) > C.colibri_moe_workspace_bytes(cfg, 4)
+        assert C.colibri_moe_f32_workspace_bytes(cfg, 32) > C.colibri_moe_f32_workspace_bytes(cfg, 1) > 0
+        assert lib.colibri_moe_f32_workspace_bytes(ctypes.byref(cfg), 33) == 0   # decode sizes only
         for T in (1, 4, 32, 33, 2048):
             # the host entry's workspace: the layer's, then room for x, out, ids and w
             extra = C.colibri_moe_host_workspace_bytes(cfg, T) - C.colibri_moe_workspace_bytes(cfg, T)
@@ -77,6 +79,10 @@ def test_argument_errors_detected_on_host(lib):
     assert lib.colibri_moe_layer(ctypes.byref(cfg), None, 4, None, None, None, None, None, None, 0,
                                  None, None, 0, None) == C.E_INVAL
     assert lib.colibri_debug_group_dots(None, None, 1, 31, None, None) == C.E_INVAL
+    f32 = lib.colibri_moe_layer_f32
+    assert f32(ctypes.byref(cfg), None, 0, None, None, None, None, None, None, 0, None, None, 0, None) == C.OK
+    assert f32(ctypes.byref(cfg), None, 33, None, None, None, None, None, None, 0, None, None, 0, None) == C.E_INVAL
+    assert f32(ctypes.byref(cfg), None, 4, None, None, None, None, None, None, 0, None, None, 0, None) == C.E_INVAL
     # the host-buffer entry: T == 0 is a no-op; missing buffers, missing given ids and a
     # short workspace are refused before any copy (the workspace address is never used)
     host = lib.colibri_moe_layer_host

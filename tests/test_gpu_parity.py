@@ -401,3 +401,53 @@ def test_moe_layer_host_entry_ids_given_and_errors(torch_cuda, C, orc):
     with pytest.raises(C.ColibriError) as e:
         C.colibri_moe_layer_host(dl.cfg, x, None, None, dl.table, dl.shared, ids, w, True, out, short)
     assert e.value.status == C.E_NOMEM
+
+
+# ------------------------------------------------------------------ fp32-activation decode
+def run_layer_f32(torch, C, dl, x, ids=None, w=None):
+    spec = dl.spec
+    T = x.shape[0]
+    ws = torch.empty(C.colibri_moe_f32_workspace_bytes(dl.cfg, max(T, 1)), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
+    given = ids is not None
+    ids_d = to_dev(torch, ids) if given else torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda")
+    w_d = to_dev(torch, w) if given else torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda")
+    C.colibri_moe_layer_f32(dl.cfg, to_dev(torch, x), dl.Wr, dl.bias, dl.table, dl.shared, ids_d, w_d, given,
+                            out, ws)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), ids_d.cpu().numpy(), w_d.cpu().numpy(), ws
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1), ("tiny", 13), ("olmoe", 1), ("olmoe", 16), ("glm52", 1),
+                                    ("glm52", 4), ("odd96", 3)])
+def test_moe_layer_f32_parity(torch_cuda, C, orc, name, T):
+    """Decode on fp32 activations against the oracle's fp32-activation layer: the same
+    routing bit for bit, outputs within the layer's tolerance (nothing is quantised but
+    the weights, so no code can round either way)."""
+    torch = torch_cuda
+    spec = ODD if name == "odd96" else synth.SPECS[name]
+    host, dl = dev_layer(C, spec)
+    x = synth.activations(spec, 0, T, step=17)
+    out, ids, w, ws = run_layer_f32(torch, C, dl, x)
+    assert C.colibri_workspace_status(dl.cfg, T, ws) == C.OK
+    ref, ids_o, w_o = orc.moe_layer(spec, x, host.Wr, host.bias, host.expert, host.shared(), act="f32")
+    assert np.array_equal(ids, ids_o)
+    np.testing.assert_allclose(w, w_o, rtol=1e-6)
+    assert_rms_close(out, ref)
+
+
+def test_moe_layer_f32_ids_given_and_bad_id(torch_cuda, C, orc):
+    torch = torch_cuda
+    spec = synth.TINY
+    host, dl = dev_layer(C, spec)
+    ids = np.array([[0, 1, 2, 3], [5, 6, 5, 7]], np.int32)   # a repeated id is computed twice
+    w = np.full((2, 4), 0.25, np.float32)
+    x = synth.activations(spec, 4, 2)
+    out, _, _, ws = run_layer_f32(torch, C, dl, x, ids, w)
+    assert C.colibri_workspace_status(dl.cfg, 2, ws) == C.OK
+    ref, _, _ = orc.moe_layer(spec, x, None, None, host.expert, host.shared(), ids=ids, w=w, act="f32")
+    assert_rms_close(out, ref)
+    bad = ids.copy()
+    bad[0, 1] = spec.n_exp
+    _, _, _, ws = run_layer_f32(torch, C, dl, x, bad, w)
+    assert C.colibri_workspace_status(dl.cfg, 2, ws) == C.E_DEVICE
