@@ -67,3 +67,25 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     class Args:  # what run_reference would read after its rank check
         workload, steps, warmup, seed = "glm52_decode_t1", 1, 0, 0
     assert bench.run_reference(Args()) is None
+
+
+def test_launch_counts_and_workload_tags():
+    """The kernel launches the bench claims per layer call, by path, match the entry points'
+    documented launch sequences; every workload names its activation type."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.launches_per_step(1, 256, False) == 2          # routing kernel + expert kernel
+    assert bench.launches_per_step(32, 256, False) == 3         # + selection kernel above T x E = 4096
+    assert bench.launches_per_step(4, 256, True) == 2           # q8 + expert kernel
+    assert bench.launches_per_step(2048, 256, False) == 7
+    assert bench.launches_per_step(2048, 256, True) == 5
+    assert bench.launches_per_step(1, 256, False, f32=True) == 5   # logits, select, gate/up, down, combine
+    assert bench.launches_per_step(1, 256, True, f32=True) == 3
+    for name in bench.WORKLOADS:
+        spec_name, T, _ = bench.WORKLOADS[name]
+        from routed_expert_ffn_grouped_b300 import synth
+        cfg = bench.workload_config(synth.SPECS[spec_name], name, T)
+        assert cfg["workload"] == name
+        assert cfg["activations"] == ("fp32" if name.endswith("_f32") else "int8 (per-32-group absmax)")
+        if name.endswith("_f32"):
+            assert T <= bench.DECODE_T_MAX     # the fp32-activation variant is decode only
