@@ -84,6 +84,13 @@ def lib() -> ctypes.CDLL:
                                        ctypes.POINTER(Expert), ctypes.POINTER(Expert),
                                        _P, _P, _P, _P, _P]),
                 "orc_expert_token_f32": (_I, [_I, _I, ctypes.POINTER(Expert), _P, _P, _P]),
+                "orc_q8_quantize_g": (_I, [_P, _I64, _I64, _I, _P, _P]),
+                "orc_group_dots_g": (None, [_P, _P, _I64, _I64, _I, _P]),
+                "orc_expert_token_g": (_I, [_I, _I, _I, ctypes.POINTER(Expert), _P, _P, _P, _P, _P, _P]),
+                "orc_expert_token_f32_g": (_I, [_I, _I, _I, ctypes.POINTER(Expert), _P, _P, _P]),
+                "orc_moe_layer_g": (_I, [ctypes.POINTER(Cfg), _I, _I, _P, _I64, _P, _P,
+                                         ctypes.POINTER(Expert), ctypes.POINTER(Expert),
+                                         _P, _P, _P, _P, _P]),
                 "orc_moe_layer_f32": (_I, [ctypes.POINTER(Cfg), _P, _I64, _P, _P,
                                            ctypes.POINTER(Expert), ctypes.POINTER(Expert),
                                            _P, _P, _P, _P, _P]),
@@ -130,12 +137,16 @@ def unpack_int4(packed: np.ndarray) -> np.ndarray:
     return q
 
 
-def q8_quantize(x: np.ndarray):
+def q8_quantize(x: np.ndarray, group: int = 32):
+    """q8 codes and scales per `group` (32 or 64) elements of each row."""
     x = _c(x, np.float32)
     rows, cols = (1, x.shape[0]) if x.ndim == 1 else x.shape
     q = np.empty(x.shape, np.int8)
-    s = np.empty(x.shape[:-1] + (cols // 32,), np.float32)
-    rc = lib().orc_q8_quantize(_ptr(x), rows, cols, _ptr(q), _ptr(s))
+    s = np.empty(x.shape[:-1] + (cols // group,), np.float32)
+    if group == 32:
+        rc = lib().orc_q8_quantize(_ptr(x), rows, cols, _ptr(q), _ptr(s))
+    else:
+        rc = lib().orc_q8_quantize_g(_ptr(x), rows, cols, group, _ptr(q), _ptr(s))
     if rc:
         raise ValueError("orc_q8_quantize: bad sizes")
     return q, s
@@ -187,33 +198,43 @@ def bucket(ids: np.ndarray, E: int):
     return offsets, pairs
 
 
-def group_dots(w_packed: np.ndarray, qa: np.ndarray) -> np.ndarray:
+def group_dots(w_packed: np.ndarray, qa: np.ndarray, group: int = 32) -> np.ndarray:
     w, qa = _c(w_packed, np.uint8), _c(qa, np.int8)
     rows, cols = w.shape[0], 2 * w.shape[1]
-    out = np.empty((rows, cols // 32), np.int32)
-    lib().orc_group_dots(_ptr(w), _ptr(qa), rows, cols, _ptr(out))
+    if group not in (32, 64) or cols % group:
+        raise ValueError("group_dots: bad group")
+    out = np.empty((rows, cols // group), np.int32)
+    if group == 32:
+        lib().orc_group_dots(_ptr(w), _ptr(qa), rows, cols, _ptr(out))
+    else:
+        lib().orc_group_dots_g(_ptr(w), _ptr(qa), rows, cols, group, _ptr(out))
     return out
 
 
-def expert_token(views: dict, qx: np.ndarray, sx: np.ndarray, want_h: bool = False):
+def expert_token(views: dict, qx: np.ndarray, sx: np.ndarray, want_h: bool = False, group: int = 32):
     """One token through one expert; returns (y, qh, sh), and the fp32 h that (qh, sh)
-    quantise as a fourth item when want_h."""
+    quantise as a fourth item when want_h. group: the quantisation group (32 or 64) of the
+    expert's scales and of the activations."""
     ex, keep = make_expert(views)
     f = keep[0].shape[0]
     d = 2 * keep[0].shape[1]
     qx, sx = _c(qx, np.int8), _c(sx, np.float32)
     y = np.empty(d, np.float32)
     qh = np.empty(f, np.int8)
-    sh = np.empty(f // 32, np.float32)
+    sh = np.empty(f // group, np.float32)
     h = np.empty(f, np.float32) if want_h else None
-    rc = lib().orc_expert_token(d, f, ctypes.byref(ex), _ptr(qx), _ptr(sx), _ptr(y), _ptr(qh), _ptr(sh),
-                                _ptr(h) if want_h else None)
+    if group == 32:
+        rc = lib().orc_expert_token(d, f, ctypes.byref(ex), _ptr(qx), _ptr(sx), _ptr(y), _ptr(qh), _ptr(sh),
+                                    _ptr(h) if want_h else None)
+    else:
+        rc = lib().orc_expert_token_g(d, f, group, ctypes.byref(ex), _ptr(qx), _ptr(sx), _ptr(y), _ptr(qh),
+                                      _ptr(sh), _ptr(h) if want_h else None)
     if rc:
         raise MemoryError("orc_expert_token")
     return (y, qh, sh, h) if want_h else (y, qh, sh)
 
 
-def expert_token_f32(views: dict, x: np.ndarray):
+def expert_token_f32(views: dict, x: np.ndarray, group: int = 32):
     """One token through one expert on fp32 activations; returns (y, h)."""
     ex, keep = make_expert(views)
     f = keep[0].shape[0]
@@ -221,17 +242,22 @@ def expert_token_f32(views: dict, x: np.ndarray):
     x = _c(x, np.float32)
     y = np.empty(d, np.float32)
     h = np.empty(f, np.float32)
-    if lib().orc_expert_token_f32(d, f, ctypes.byref(ex), _ptr(x), _ptr(y), _ptr(h)):
-        raise MemoryError("orc_expert_token_f32")
+    if group == 32:
+        rc = lib().orc_expert_token_f32(d, f, ctypes.byref(ex), _ptr(x), _ptr(y), _ptr(h))
+    else:
+        rc = lib().orc_expert_token_f32_g(d, f, group, ctypes.byref(ex), _ptr(x), _ptr(y), _ptr(h))
+    if rc:
+        raise ValueError("orc_expert_token_f32: bad sizes")
     return y, h
 
 
-def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None, act="q8"):
+def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None, act="q8", group=32):
     """The whole layer; ``experts`` is a list of E view dicts (or a callable e -> view dict,
     used only for the selected ids). act = "q8" (int8 activations, the layer's main form)
-    or "f32" (fp32 activations). Returns (out, ids, w)."""
-    if act not in ("q8", "f32"):
-        raise ValueError(act)
+    or "f32" (fp32 activations); group = 32 or 64 (the quantisation group of the experts'
+    scales and of the activations). Returns (out, ids, w)."""
+    if act not in ("q8", "f32") or group not in (32, 64):
+        raise ValueError((act, group))
     cfg = spec_or_cfg if isinstance(spec_or_cfg, Cfg) else make_cfg(spec_or_cfg)
     x = _c(x, np.float32)
     T = x.shape[0]
@@ -259,7 +285,11 @@ def moe_layer(spec_or_cfg, x, Wr, bias, experts, shared=None, ids=None, w=None, 
         sh_ex, k = make_expert(shared)
         keep.append(k)
     out = np.empty((T, cfg.d), np.float32)
-    fn = lib().orc_moe_layer if act == "q8" else lib().orc_moe_layer_f32
+    if group == 32:
+        fn = lib().orc_moe_layer if act == "q8" else lib().orc_moe_layer_f32
+    else:
+        def fn(cfg_p, *rest):
+            return lib().orc_moe_layer_g(cfg_p, group, int(act == "f32"), *rest)
     rc = fn(ctypes.byref(cfg), _ptr(x), T, None if Wr is None else _ptr(_c(Wr, np.float32)),
                              None if bias is None else _ptr(_c(bias, np.float32)), table,
                              ctypes.byref(sh_ex) if sh_ex is not None else None,

@@ -27,27 +27,33 @@ void orc_unpack_int4(const uint8_t *packed, int64_t nbytes, int8_t *q)
 }
 
 /* ---- q8 activation quantiser ------------------------------------------------
- * Symmetric absmax int8 per 32 consecutive elements of a row, in fp32:
- * d = amax / 127, q = clamp(roundf(x / d), -127, 127), roundf rounding halves
- * away from zero; an all-zero group gets d = 0 and zero codes. */
-int orc_q8_quantize(const float *x, int64_t rows, int64_t cols, int8_t *q, float *scale)
+ * Symmetric absmax int8 per `group` (32, or 64 for the pages' gs64 container)
+ * consecutive elements of a row, in fp32: d = amax / 127, q = clamp(roundf(x / d),
+ * -127, 127), roundf rounding halves away from zero; an all-zero group gets d = 0
+ * and zero codes. */
+static int group_ok(int group)
 {
-    if (rows < 0 || cols < 0 || cols % ORC_GROUP != 0)
+    return group == 32 || group == 64;
+}
+
+int orc_q8_quantize_g(const float *x, int64_t rows, int64_t cols, int group, int8_t *q, float *scale)
+{
+    if (!group_ok(group) || rows < 0 || cols < 0 || cols % group != 0)
         return -1;
-    const int64_t ng = cols / ORC_GROUP;
+    const int64_t ng = cols / group;
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t g = 0; g < ng; ++g) {
-            const float *xg = x + r * cols + g * ORC_GROUP;
-            int8_t *qg = q + r * cols + g * ORC_GROUP;
+            const float *xg = x + r * cols + g * group;
+            int8_t *qg = q + r * cols + g * group;
             float amax = 0.0f;
-            for (int k = 0; k < ORC_GROUP; ++k) {
+            for (int k = 0; k < group; ++k) {
                 float a = fabsf(xg[k]);
                 if (a > amax)
                     amax = a;
             }
             float d = amax / 127.0f;
             scale[r * ng + g] = d;
-            for (int k = 0; k < ORC_GROUP; ++k) {
+            for (int k = 0; k < group; ++k) {
                 if (d == 0.0f) {
                     qg[k] = 0;
                     continue;
@@ -62,6 +68,11 @@ int orc_q8_quantize(const float *x, int64_t rows, int64_t cols, int8_t *q, float
         }
     }
     return 0;
+}
+
+int orc_q8_quantize(const float *x, int64_t rows, int64_t cols, int8_t *q, float *scale)
+{
+    return orc_q8_quantize_g(x, rows, cols, ORC_GROUP, q, scale);
 }
 
 /* ---- router logits ----------------------------------------------------------
@@ -286,30 +297,38 @@ int orc_bucket(const int32_t *ids, int64_t T, int k, int E, int32_t *offsets, in
 }
 
 /* ---- integer group dots ---------------------------------------------------------
- * The int8 x int4 dot of the pages' integer kernel, one int32 per 32-group. */
-void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int32_t *dots)
+ * The int8 x int4 dot of the pages' integer kernel, one int32 per group of `group`
+ * columns (|dot| <= 64 * 8 * 127 = 65,024). */
+void orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots)
 {
-    const int64_t ng = cols / ORC_GROUP;
-    int8_t q[ORC_GROUP];
+    const int64_t ng = cols / group;
+    int8_t q[64];
     for (int64_t r = 0; r < rows; ++r) {
         for (int64_t g = 0; g < ng; ++g) {
-            orc_unpack_int4(w + r * (cols / 2) + g * (ORC_GROUP / 2), ORC_GROUP / 2, q);
+            orc_unpack_int4(w + r * (cols / 2) + g * (group / 2), group / 2, q);
             int32_t acc = 0;
-            for (int k = 0; k < ORC_GROUP; ++k)
-                acc += (int32_t)q[k] * (int32_t)qa[g * ORC_GROUP + k];
+            for (int k = 0; k < group; ++k)
+                acc += (int32_t)q[k] * (int32_t)qa[g * group + k];
             dots[r * ng + g] = acc;
         }
     }
+}
+
+void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int32_t *dots)
+{
+    orc_group_dots_g(w, qa, rows, cols, ORC_GROUP, dots);
 }
 
 /* ---- one token through one SwiGLU expert ---------------------------------------
  * gate_n = sum_g s1[n][g] * sx[g] * D1[n][g], up_n likewise with W3 (fp64);
  * h_n = silu(gate_n) * up_n with silu(z) = z / (1 + exp(-z)), rounded to fp32;
  * (qh, sh) = q8(h); y_m = sum_g s2[m][g] * sh[g] * D2[m][g] (fp64), rounded to fp32. */
-int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const float *sx,
-                     float *y, int8_t *qh_out, float *sh_out, float *h_out)
+int orc_expert_token_g(int d, int f, int group, const orc_expert *ex, const int8_t *qx, const float *sx,
+                       float *y, int8_t *qh_out, float *sh_out, float *h_out)
 {
-    const int ngd = d / ORC_GROUP, ngf = f / ORC_GROUP;
+    if (!group_ok(group) || d % group || f % group)
+        return -1;
+    const int ngd = d / group, ngf = f / group;
     int32_t *dots = (int32_t *)malloc(sizeof(int32_t) * (size_t)(ngd > ngf ? ngd : ngf));
     float *h = (float *)malloc(sizeof(float) * (size_t)f);
     int8_t *qh = (int8_t *)malloc((size_t)f);
@@ -319,19 +338,19 @@ int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const
         return -1;
     }
     for (int n = 0; n < f; ++n) {
-        orc_group_dots(ex->w1 + (int64_t)n * (d / 2), qx, 1, d, dots);
+        orc_group_dots_g(ex->w1 + (int64_t)n * (d / 2), qx, 1, d, group, dots);
         double gate = 0.0;
         for (int g = 0; g < ngd; ++g)
             gate += (double)ex->s1[(int64_t)n * ngd + g] * (double)sx[g] * (double)dots[g];
-        orc_group_dots(ex->w3 + (int64_t)n * (d / 2), qx, 1, d, dots);
+        orc_group_dots_g(ex->w3 + (int64_t)n * (d / 2), qx, 1, d, group, dots);
         double up = 0.0;
         for (int g = 0; g < ngd; ++g)
             up += (double)ex->s3[(int64_t)n * ngd + g] * (double)sx[g] * (double)dots[g];
         h[n] = (float)(gate / (1.0 + exp(-gate)) * up);
     }
-    orc_q8_quantize(h, 1, f, qh, sh);
+    orc_q8_quantize_g(h, 1, f, group, qh, sh);
     for (int m = 0; m < d; ++m) {
-        orc_group_dots(ex->w2 + (int64_t)m * (f / 2), qh, 1, f, dots);
+        orc_group_dots_g(ex->w2 + (int64_t)m * (f / 2), qh, 1, f, group, dots);
         double acc = 0.0;
         for (int g = 0; g < ngf; ++g)
             acc += (double)ex->s2[(int64_t)m * ngf + g] * (double)sh[g] * (double)dots[g];
@@ -347,24 +366,33 @@ int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const
     return 0;
 }
 
+int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const float *sx,
+                     float *y, int8_t *qh_out, float *sh_out, float *h_out)
+{
+    return orc_expert_token_g(d, f, ORC_GROUP, ex, qx, sx, y, qh_out, sh_out, h_out);
+}
+
 /* ---- one token through one SwiGLU expert, activations kept in fp32 ------------------
  * The decode variant of the dashen-tech guide ("Analyse approfondie", step 3: one-token
  * decode runs on f32 activations) with the same int4 group-scaled weights:
  * gate_n = sum_k s1[n][k/32] * q1[n][k] * x[k] and up_n likewise (fp64, k ascending);
  * h_n = silu(gate_n) * up_n rounded to fp32; y_m = sum_j s2[m][j/32] * q2[m][j] * h_j
  * (fp64, j ascending) rounded to fp32. Nothing is quantised but the weights. */
-static double dot_row_f32(const uint8_t *wrow, const float *srow, const float *v, int K, int8_t *q)
+static double dot_row_f32(const uint8_t *wrow, const float *srow, const float *v, int K, int group, int8_t *q)
 {
     orc_unpack_int4(wrow, K / 2, q);
     double acc = 0.0;
     for (int k = 0; k < K; ++k)
-        acc += (double)srow[k / ORC_GROUP] * (double)q[k] * (double)v[k];
+        acc += (double)srow[k / group] * (double)q[k] * (double)v[k];
     return acc;
 }
 
-int orc_expert_token_f32(int d, int f, const orc_expert *ex, const float *x, float *y, float *h_out)
+int orc_expert_token_f32_g(int d, int f, int group, const orc_expert *ex, const float *x, float *y,
+                           float *h_out)
 {
-    const int ngd = d / ORC_GROUP, ngf = f / ORC_GROUP;
+    if (!group_ok(group) || d % group || f % group)
+        return -1;
+    const int ngd = d / group, ngf = f / group;
     int8_t *q = (int8_t *)malloc((size_t)(d > f ? d : f));
     float *h = (float *)malloc(sizeof(float) * (size_t)f);
     if (!q || !h) {
@@ -372,16 +400,21 @@ int orc_expert_token_f32(int d, int f, const orc_expert *ex, const float *x, flo
         return -1;
     }
     for (int n = 0; n < f; ++n) {
-        const double gate = dot_row_f32(ex->w1 + (int64_t)n * (d / 2), ex->s1 + (int64_t)n * ngd, x, d, q);
-        const double up = dot_row_f32(ex->w3 + (int64_t)n * (d / 2), ex->s3 + (int64_t)n * ngd, x, d, q);
+        const double gate = dot_row_f32(ex->w1 + (int64_t)n * (d / 2), ex->s1 + (int64_t)n * ngd, x, d, group, q);
+        const double up = dot_row_f32(ex->w3 + (int64_t)n * (d / 2), ex->s3 + (int64_t)n * ngd, x, d, group, q);
         h[n] = (float)(gate / (1.0 + exp(-gate)) * up);
     }
     for (int m = 0; m < d; ++m)
-        y[m] = (float)dot_row_f32(ex->w2 + (int64_t)m * (f / 2), ex->s2 + (int64_t)m * ngf, h, f, q);
+        y[m] = (float)dot_row_f32(ex->w2 + (int64_t)m * (f / 2), ex->s2 + (int64_t)m * ngf, h, f, group, q);
     if (h_out)
         memcpy(h_out, h, sizeof(float) * (size_t)f);
     free(q); free(h);
     return 0;
+}
+
+int orc_expert_token_f32(int d, int f, const orc_expert *ex, const float *x, float *y, float *h_out)
+{
+    return orc_expert_token_f32_g(d, f, ORC_GROUP, ex, x, y, h_out);
 }
 
 /* ---- the layer --------------------------------------------------------------------
@@ -389,15 +422,16 @@ int orc_expert_token_f32(int d, int f, const orc_expert *ex, const float *x, flo
  * shared expert (weight 1, not scaled) and each selected expert, and combine
  * out[t] = y_shared + sum_i w[t][i] * y_i in fp64 in selection order, rounded to fp32.
  * Tokens are independent of one another. */
-static int moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr,
-                     const float *bias, const orc_expert *experts, const orc_expert *shared,
-                     const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
-                     float *out, int act_f32)
+int orc_moe_layer_g(const orc_cfg *cfg, int group, int act_f32, const float *x, int64_t T, const float *Wr,
+                    const float *bias, const orc_expert *experts, const orc_expert *shared,
+                    const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out, float *out)
 {
-    if (!cfg_ok(cfg) || T < 0 || (cfg->has_shared && !shared))
+    if (!cfg_ok(cfg) || !group_ok(group) || T < 0 || (cfg->has_shared && !shared))
+        return -1;
+    if (cfg->d % group || cfg->ffn % group || (cfg->has_shared && cfg->shared_ffn % group))
         return -1;
     const int d = cfg->d, K = cfg->top_k, E = cfg->n_exp;
-    const int ngd = d / ORC_GROUP;
+    const int ngd = d / group;
     int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T * K + 1));
     float *w = (float *)malloc(sizeof(float) * (size_t)(T * K + 1));
     int8_t *qx = (int8_t *)malloc((size_t)d);
@@ -426,12 +460,12 @@ static int moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float 
     for (int64_t t = 0; t < T; ++t) {
         const float *xt = x + t * d;
         if (!act_f32)
-            orc_q8_quantize(xt, 1, d, qx, sx);
+            orc_q8_quantize_g(xt, 1, d, group, qx, sx);
         for (int m = 0; m < d; ++m)
             acc[m] = 0.0;
         if (cfg->has_shared) {
-            rc = act_f32 ? orc_expert_token_f32(d, cfg->shared_ffn, shared, xt, y, NULL)
-                         : orc_expert_token(d, cfg->shared_ffn, shared, qx, sx, y, NULL, NULL, NULL);
+            rc = act_f32 ? orc_expert_token_f32_g(d, cfg->shared_ffn, group, shared, xt, y, NULL)
+                         : orc_expert_token_g(d, cfg->shared_ffn, group, shared, qx, sx, y, NULL, NULL, NULL);
             if (rc)
                 goto done;
             for (int m = 0; m < d; ++m)
@@ -439,8 +473,8 @@ static int moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float 
         }
         for (int i = 0; i < K; ++i) {
             const orc_expert *ex = &experts[ids[t * K + i]];
-            rc = act_f32 ? orc_expert_token_f32(d, cfg->ffn, ex, xt, y, NULL)
-                         : orc_expert_token(d, cfg->ffn, ex, qx, sx, y, NULL, NULL, NULL);
+            rc = act_f32 ? orc_expert_token_f32_g(d, cfg->ffn, group, ex, xt, y, NULL)
+                         : orc_expert_token_g(d, cfg->ffn, group, ex, qx, sx, y, NULL, NULL, NULL);
             if (rc)
                 goto done;
             for (int m = 0; m < d; ++m)
@@ -463,7 +497,7 @@ int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr
                   const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
                   float *out)
 {
-    return moe_layer(cfg, x, T, Wr, bias, experts, shared, ids_in, w_in, ids_out, w_out, out, 0);
+    return orc_moe_layer_g(cfg, ORC_GROUP, 0, x, T, Wr, bias, experts, shared, ids_in, w_in, ids_out, w_out, out);
 }
 
 /* The same layer with every expert on fp32 activations (orc_expert_token_f32). */
@@ -472,7 +506,7 @@ int orc_moe_layer_f32(const orc_cfg *cfg, const float *x, int64_t T, const float
                       const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
                       float *out)
 {
-    return moe_layer(cfg, x, T, Wr, bias, experts, shared, ids_in, w_in, ids_out, w_out, out, 1);
+    return orc_moe_layer_g(cfg, ORC_GROUP, 1, x, T, Wr, bias, experts, shared, ids_in, w_in, ids_out, w_out, out);
 }
 
 /* ---- LRU cache trace -----------------------------------------------------------

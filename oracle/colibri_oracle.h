@@ -73,6 +73,8 @@ void orc_unpack_int4(const uint8_t *packed, int64_t nbytes, int8_t *q);
 /* Per row, per 32-group: amax = max|x|, d = amax/127 (fp32), q = clamp(roundf(x/d), -127, 127);
  * amax == 0 gives d = 0 and all-zero codes. cols % 32 == 0. Returns 0, or -1 on bad sizes. */
 int orc_q8_quantize(const float *x, int64_t rows, int64_t cols, int8_t *q, float *scale);
+/* The same per `group` (32 or 64) elements; scale [rows][cols/group]. */
+int orc_q8_quantize_g(const float *x, int64_t rows, int64_t cols, int group, int8_t *q, float *scale);
 
 /* Router logits l[t][e] = x[t] . Wr[e] in fp32 in one fixed order: partial sum j in [0,32)
  * accumulates x[k]*Wr[e][k] with fmaf over k = j, j+32, ... ascending; then, for
@@ -95,6 +97,8 @@ int orc_bucket(const int32_t *ids, int64_t T, int k, int E, int32_t *offsets, in
 
 /* dots[r][g] = sum over the 32 k in group g of unpack(w)[r][k] * qa[k] (int32). */
 void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int32_t *dots);
+/* The same per `group` (32 or 64) columns; dots [rows][cols/group]. */
+void orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots);
 
 /* One token through one expert of intermediate size f: gate/up group dots, SwiGLU,
  * q8 of h, down group dots. y [d] fp32; qh [f] and sh [f/32] receive h's codes and h_out
@@ -102,12 +106,19 @@ void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t co
  * failure. */
 int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const float *sx,
                      float *y, int8_t *qh, float *sh, float *h_out);
+/* The same with quantisation groups of `group` (32 or 64) elements, for weights and
+ * activations alike: the expert's scales are [f][d/group], [f][d/group], [d][f/group],
+ * sx [d/group], sh [f/group]. Returns -1 also for a group size that does not divide d, f. */
+int orc_expert_token_g(int d, int f, int group, const orc_expert *ex, const int8_t *qx, const float *sx,
+                       float *y, int8_t *qh, float *sh, float *h_out);
 
 /* One token through one expert on fp32 activations (the f32 decode variant): gate and
  * up are fp64 sums over k of scale * int4 code * x[k], h = silu(gate) * up rounded to
  * fp32, y = the same sums of W2 against h. x [d], y [d]; h_out [f] may be NULL.
  * Returns 0, or -1 on allocation failure. */
 int orc_expert_token_f32(int d, int f, const orc_expert *ex, const float *x, float *y, float *h_out);
+int orc_expert_token_f32_g(int d, int f, int group, const orc_expert *ex, const float *x, float *y,
+                           float *h_out);
 
 /* The whole layer for T tokens. experts [E] (routed), shared (NULL when !has_shared).
  * ids_in/w_in: when ids_in != NULL the router is skipped and ids_in/w_in [T][k] are used.
@@ -117,6 +128,12 @@ int orc_moe_layer(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr
                   const float *bias, const orc_expert *experts, const orc_expert *shared,
                   const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out,
                   float *out);
+/* The layer with quantisation groups of `group` (32 or 64) elements, on int8 (act_f32 = 0)
+ * or fp32 (act_f32 = 1) activations. orc_moe_layer is (group 32, int8). */
+int orc_moe_layer_g(const orc_cfg *cfg, int group, int act_f32, const float *x, int64_t T, const float *Wr,
+                    const float *bias, const orc_expert *experts, const orc_expert *shared,
+                    const int32_t *ids_in, const float *w_in, int32_t *ids_out, float *w_out, float *out);
+
 /* orc_moe_layer with every expert on fp32 activations (orc_expert_token_f32). */
 int orc_moe_layer_f32(const orc_cfg *cfg, const float *x, int64_t T, const float *Wr,
                       const float *bias, const orc_expert *experts, const orc_expert *shared,

@@ -407,6 +407,143 @@ def test_f32_layer_combine(orc):
         assert np.array_equal(out[t], acc.astype(np.float32))
 
 
+# ---------------------------------------------------------------- 64-element groups
+# The pages' own container has 64-element groups ("Run a 744B-parameter model on your own
+# machine", "Step 3"). The oracle takes the group size as a parameter; these pins fix its
+# 64-element form.
+def _views_g(rng, d, f, group):
+    return {"w1": rng.integers(0, 256, (f, d // 2), dtype=np.uint8),
+            "w3": rng.integers(0, 256, (f, d // 2), dtype=np.uint8),
+            "w2": rng.integers(0, 256, (d, f // 2), dtype=np.uint8),
+            "s1": np.abs(rng.normal(0, 0.02, (f, d // group))).astype(np.float32),
+            "s3": np.abs(rng.normal(0, 0.02, (f, d // group))).astype(np.float32),
+            "s2": np.abs(rng.normal(0, 0.02, (d, f // group))).astype(np.float32)}
+
+
+def _dequant_g(wp, s, group):
+    lo = (wp & 15).astype(np.float64) - 8
+    hi = (wp >> 4).astype(np.float64) - 8
+    q = np.stack([lo, hi], -1).reshape(wp.shape[0], -1)
+    return q * np.repeat(s.astype(np.float64), group, axis=1)
+
+
+def test_q8_g64_hand_cases_and_bound(orc):
+    x = np.zeros(192, np.float32)
+    x[:64] = np.arange(64, dtype=np.float32) - 31.5    # |x| <= 31.5 ...
+    x[63], x[3] = 32.0, -32.0                           # ... but for amax 32 twice: d = 32/127
+    # group 1 all zero; group 2: codes exactly representable with a power-of-two step
+    codes = np.arange(-63, 65) % 255 - 127
+    x[128:] = (codes[:64] * 0.25).astype(np.float32)
+    x[128] = 127 * 0.25
+    q, d = orc.q8_quantize(x, group=64)
+    assert d.shape == (3,) and d[1] == 0.0 and np.all(q[64:128] == 0)
+    assert d[0] == np.float32(32.0) / np.float32(127.0) and q[63] == 127 and q[3] == -127
+    assert d[2] == np.float32(0.25) and np.array_equal(q[128:], np.clip(np.rint(x[128:] / 0.25), -127, 127))
+    rng = np.random.default_rng(31)
+    y = (rng.standard_normal((50, 256)) * rng.uniform(0.01, 10, (50, 1))).astype(np.float32)
+    qy, dy = orc.q8_quantize(y, group=64)
+    err = np.abs(y.astype(np.float64) - qy * np.repeat(dy.astype(np.float64), 64, axis=1))
+    assert np.all(err <= np.repeat(dy.astype(np.float64), 64, axis=1) * 0.5 * (1 + 1e-6))
+    assert np.all(np.abs(qy).reshape(50, 4, 64).max(-1) == 127)
+    with pytest.raises(ValueError):
+        orc.q8_quantize(np.zeros(96, np.float32), group=64)
+
+
+def test_group_dots_g64_closed_forms_and_bruteforce(orc):
+    qa = np.full(128, -127, np.int8)
+    w = np.zeros((2, 64), np.uint8)          # all nibbles 0: q = -8
+    w[1] = 0xFF                              # all nibbles 15: q = +7
+    dots = orc.group_dots(w, qa, group=64)
+    assert dots.tolist() == [[64 * 8 * 127] * 2, [-64 * 7 * 127] * 2]
+    rng = np.random.default_rng(32)
+    w = rng.integers(0, 256, (24, 192), dtype=np.uint8)
+    qa = rng.integers(-127, 128, 384).astype(np.int8)
+    lo = (w & 15).astype(np.int64) - 8
+    hi = (w >> 4).astype(np.int64) - 8
+    qw = np.stack([lo, hi], -1).reshape(24, 384)
+    want = (qw * qa.astype(np.int64)).reshape(24, 6, 64).sum(-1)
+    assert np.array_equal(orc.group_dots(w, qa, group=64), want)
+    # a 64-group dot is the sum of its two 32-group dots
+    d32 = orc.group_dots(w, qa)
+    assert np.array_equal(d32.reshape(24, 6, 2).sum(-1), want)
+
+
+def test_g64_gate_up_reduces_to_g32_when_halves_agree(orc):
+    """Scales shared by the two 32-halves of each 64-group, and an x whose two halves of
+    every 64-group have the same amax: the 64-group expert forms the same h as the pinned
+    32-group one (to the last bit of fp32)."""
+    rng = np.random.default_rng(33)
+    d, f = 256, 128
+    v64 = _views_g(rng, d, f, 64)
+    v32 = dict(v64)
+    for k in ("s1", "s3", "s2"):
+        v32[k] = np.repeat(v64[k], 2, axis=1)
+    x = rng.uniform(-1, 1, d).astype(np.float32)
+    x[0::32] = np.float32(1.5) * np.where(rng.integers(0, 2, d // 32) == 0, 1, -1)
+    q32, s32 = orc.q8_quantize(x)
+    q64, s64 = orc.q8_quantize(x, group=64)
+    assert np.array_equal(q32, q64) and np.array_equal(np.repeat(s64, 2), s32)
+    _, _, _, h32 = orc.expert_token(v32, q32, s32, want_h=True)
+    _, _, _, h64 = orc.expert_token(v64, q64, s64, want_h=True, group=64)
+    ulp = np.abs(h32.view(np.int32).astype(np.int64) - h64.view(np.int32).astype(np.int64))
+    assert ulp.max() <= 1 and (ulp == 0).mean() > 0.99
+
+
+def test_g64_expert_matches_dequantised_fp64_matmul(orc):
+    rng = np.random.default_rng(34)
+    d, f = 256, 192
+    v = _views_g(rng, d, f, 64)
+    x = rng.standard_normal(d).astype(np.float32)
+    qx, sx = orc.q8_quantize(x, group=64)
+    y, qh, sh, h = orc.expert_token(v, qx, sx, want_h=True, group=64)
+    assert sh.shape == (f // 64,)
+    xh = qx.astype(np.float64) * np.repeat(sx.astype(np.float64), 64)
+    g = _dequant_g(v["w1"], v["s1"], 64) @ xh
+    u = _dequant_g(v["w3"], v["s3"], 64) @ xh
+    hd = g / (1 + np.exp(-g)) * u
+    assert np.all(np.abs(h.astype(np.float64) - hd) <= 2.0 ** -24 * np.abs(hd) * (1 + 1e-9) + 1e-30)
+    assert np.array_equal(orc.q8_quantize(h, group=64)[0], qh)
+    yref = _dequant_g(v["w2"], v["s2"], 64) @ (qh.astype(np.float64) * np.repeat(sh.astype(np.float64), 64))
+    assert np.max(np.abs(y - yref)) <= 1e-6 * np.max(np.abs(yref))
+    # fp32 activations with 64-element groups: the dense SwiGLU of x itself
+    y32, h32 = orc.expert_token_f32(v, x, group=64)
+    g = _dequant_g(v["w1"], v["s1"], 64) @ x.astype(np.float64)
+    u = _dequant_g(v["w3"], v["s3"], 64) @ x.astype(np.float64)
+    hf = (g / (1 + np.exp(-g)) * u).astype(np.float32)
+    assert np.array_equal(h32, hf) or np.max(np.abs(h32 - hf) / np.abs(hf).max()) < 1e-6
+    yref = _dequant_g(v["w2"], v["s2"], 64) @ h32.astype(np.float64)
+    assert np.max(np.abs(y32 - yref)) <= 1e-6 * np.max(np.abs(yref))
+    with pytest.raises(ValueError):
+        orc.expert_token_f32(_views_g(rng, 96, 64, 32), np.zeros(96, np.float32), group=64)
+
+
+def test_g64_layer_combines_its_experts(orc):
+    """The layer with 64-element groups: routing unchanged, out = shared + sum w * y of
+    the 64-group experts, for int8 and fp32 activations."""
+    rng = np.random.default_rng(35)
+    spec = _cfg(d=256, ffn=128, n_exp=4, top_k=2, n_group=2, topk_group=1, has_shared=True, shared_ffn=128)
+    experts = [_views_g(rng, 256, 128, 64) for _ in range(4)]
+    shared = _views_g(rng, 256, 128, 64)
+    Wr = rng.normal(0, 0.05, (4, 256)).astype(np.float32)
+    x = rng.standard_normal((3, 256)).astype(np.float32)
+    for act in ("q8", "f32"):
+        out, ids, w = orc.moe_layer(spec, x, Wr, None, experts, shared, act=act, group=64)
+        ids32, w32 = orc.router_topk(spec, x, Wr, None)
+        assert np.array_equal(ids, ids32) and np.array_equal(w, w32)
+        for t in range(3):
+            if act == "q8":
+                qx, sx = orc.q8_quantize(x[t], group=64)
+                run = lambda v: orc.expert_token(v, qx, sx, group=64)[0]
+            else:
+                run = lambda v: orc.expert_token_f32(v, x[t], group=64)[0]
+            acc = run(shared).astype(np.float64)
+            for i in range(2):
+                acc += np.float64(w[t, i]) * run(experts[int(ids[t, i])]).astype(np.float64)
+            assert np.array_equal(out[t], acc.astype(np.float32))
+    with pytest.raises(ValueError):
+        orc.moe_layer(spec, x, Wr, None, experts, shared, group=48)
+
+
 def test_layer_combine_and_linearity(orc):
     spec = synth.TINY
     layer = synth.make_layer(spec, 0)
