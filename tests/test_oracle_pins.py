@@ -257,6 +257,22 @@ def test_router_grouped_bruteforce_subsets(orc):
         assert list(c[t][ids[t]]) == sorted(c[t][ids[t]], reverse=True)
 
 
+def test_router_sigmoid_without_renormalisation(orc):
+    """norm_topk = 0: each weight is its own unbiased sigmoid score times the scale (no
+    division by the sum); the ids do not depend on the flag."""
+    spec = _cfg(n_exp=16, top_k=4, n_group=4, topk_group=2, norm_topk=False, routed_scale=2.5)
+    rng = np.random.default_rng(36)
+    logits = rng.standard_normal((12, 16)).astype(np.float32)
+    bias = (rng.standard_normal(16) * 0.05).astype(np.float32)
+    ids, w = orc.router_select(spec, logits, bias)
+    ids_n, w_n = orc.router_select(spec.replace(norm_topk=True), logits, bias)
+    assert np.array_equal(ids, ids_n)
+    s, _ = _c_scores(logits, bias)
+    want = (np.take_along_axis(s, ids, 1).astype(np.float64) * 2.5).astype(np.float32)
+    assert np.array_equal(w, want)
+    assert np.allclose(w_n.sum(1), 2.5, rtol=1e-6) and not np.allclose(w.sum(1), 2.5, rtol=1e-3)
+
+
 def test_router_softmax_matches_textbook(orc):
     spec = _cfg(n_exp=64, top_k=8, router="softmax", norm_topk=False, routed_scale=1.0)
     rng = np.random.default_rng(7)
