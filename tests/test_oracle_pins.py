@@ -288,6 +288,19 @@ def test_router_softmax_matches_textbook(orc):
     assert np.allclose(wn.sum(1), 1.0, rtol=1e-6)
 
 
+def test_router_softmax_ignores_bias_and_scales_linearly(orc):
+    """Softmax mode takes no selection bias (the sigmoid router's steering term), and its
+    weights are the probabilities times routed_scale."""
+    spec = _cfg(n_exp=32, top_k=4, router="softmax", norm_topk=False, routed_scale=1.0)
+    rng = np.random.default_rng(37)
+    logits = rng.standard_normal((6, 32)).astype(np.float32)
+    ids, w = orc.router_select(spec, logits, None)
+    ids_b, w_b = orc.router_select(spec, logits, (rng.standard_normal(32) * 5).astype(np.float32))
+    assert np.array_equal(ids, ids_b) and np.array_equal(w, w_b)
+    _, w3 = orc.router_select(spec.replace(routed_scale=3.0), logits, None)
+    assert np.allclose(w3, 3.0 * w, rtol=1e-6)
+
+
 def test_router_bad_config_rejected(orc):
     with pytest.raises(ValueError):
         orc.router_select(_cfg(n_exp=8, n_group=3), np.zeros((1, 8), np.float32), None)
