@@ -299,7 +299,8 @@ int orc_bucket(const int32_t *ids, int64_t T, int k, int E, int32_t *offsets, in
 /* ---- integer group dots ---------------------------------------------------------
  * The int8 x int4 dot of the pages' integer kernel, one int32 per group of `group`
  * columns (|dot| <= 64 * 8 * 127 = 65,024). */
-void orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots)
+static inline void group_dots_n(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group,
+                                int32_t *dots)
 {
     const int64_t ng = cols / group;
     int8_t q[64];
@@ -312,6 +313,15 @@ void orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t 
             dots[r * ng + g] = acc;
         }
     }
+}
+
+void orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots)
+{
+    /* the same loop with the group size as a constant of each call */
+    if (group == 64)
+        group_dots_n(w, qa, rows, cols, 64, dots);
+    else
+        group_dots_n(w, qa, rows, cols, 32, dots);
 }
 
 void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int32_t *dots)
@@ -381,9 +391,10 @@ int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const
 static double dot_row_f32(const uint8_t *wrow, const float *srow, const float *v, int K, int group, int8_t *q)
 {
     orc_unpack_int4(wrow, K / 2, q);
+    const int shift = group == 64 ? 6 : 5;  /* k / group */
     double acc = 0.0;
     for (int k = 0; k < K; ++k)
-        acc += (double)srow[k / group] * (double)q[k] * (double)v[k];
+        acc += (double)srow[k >> shift] * (double)q[k] * (double)v[k];
     return acc;
 }
 
