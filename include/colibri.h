@@ -261,7 +261,8 @@ typedef struct {
 int colibri_moe_workspace_view(const colibri_layer_cfg *cfg, int T_max, colibri_workspace_view *out);
 
 /* Profiling hook (process-wide, not thread-safe, off by default). While enabled,
- * colibri_moe_layer records timing events on its stream around its kernels (seven slots;
+ * colibri_moe_layer and colibri_moe_layer_f32 record timing events on their stream around
+ * their kernels (seven slots;
  * also under CUDA-graph capture, as external event-record nodes), on the device that
  * was current when profiling was enabled. */
 #define COLIBRI_PROFILE_KERNELS 7
@@ -274,7 +275,8 @@ int colibri_moe_profile_enable(int on);
  * Decode (T <= 32): [1] the routing kernel (router logits and scores with q8, or q8 alone
  * when ids_given), [4] the expert kernel (selection, bucketing, gate/up, down, combine).
  * Prefill: [1] q8 and the router logits, [2] selection, [3] bucketing, [4] and [5] the two
- * GEMMs, [6] combine. The events serialise the kernels (no programmatic overlap).
+ * GEMMs, [6] combine. colibri_moe_layer_f32: [1] router logits, [2] selection, [4] gate/up,
+ * [5] down, [6] combine. The events serialise the kernels (no programmatic overlap).
  * n must be >= COLIBRI_PROFILE_KERNELS. */
 int colibri_moe_profile_read(float *ms, int n);
 
