@@ -221,6 +221,44 @@ def blob_bytes(spec, f):
 
 
 # ---------------------------------------------------------------- oracle timing
+def expert_load(ids_steps: np.ndarray, n_exp: int) -> dict:
+    """How the routed pairs of each timed step's batch spread over the experts, averaged
+    over the steps: distinct experts, the busiest expert's tokens, that over the mean per
+    expert, and percentiles of tokens per expert (all E experts, zeros included).
+    ids_steps: [steps][T][top_k]."""
+    steps = ids_steps.shape[0]
+    counts = np.stack([np.bincount(ids_steps[i].ravel(), minlength=n_exp) for i in range(steps)])
+    pairs = counts.sum(1)
+    mean = pairs / n_exp
+    return {"steps": int(steps), "pairs_per_step": float(pairs.mean()),
+            "distinct_experts": float((counts > 0).sum(1).mean()),
+            "max_tokens_per_expert": float(counts.max(1).mean()),
+            "max_over_mean": float((counts.max(1) / mean).mean()),
+            "tokens_per_expert_p50_p90_p99": [float(np.percentile(counts, q)) for q in (50, 90, 99)]}
+
+
+def host_info() -> dict:
+    """The bench host's CPU: logical cores and model name."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+def informational(fn, *args) -> dict:
+    """fn(*args), or the error it raised: an informational field never stops the bench."""
+    try:
+        return fn(*args)
+    except Exception as e:  # noqa: BLE001
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
 def is_f32(workload: str) -> bool:
     return workload.endswith("_f32")
 
@@ -725,6 +763,8 @@ def run_colibri(args):
                              if f32 else "colibri_moe_layer_host (pinned host x and out, the error flag read "
                              "back) via the Python binding, eager launches")},
             "gpu_launches": launches_per_step(T, spec.n_exp, False, f32) * K,
+            "expert_load": informational(expert_load, ids_np, spec.n_exp),
+            "host": informational(host_info),
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -89,3 +89,21 @@ def test_launch_counts_and_workload_tags():
         assert cfg["activations"] == ("fp32" if name.endswith("_f32") else "int8 (per-32-group absmax)")
         if name.endswith("_f32"):
             assert T <= bench.DECODE_T_MAX     # the fp32-activation variant is decode only
+
+
+def test_expert_load_and_host_fields():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    # two steps of 2 tokens x top-2 over 4 experts
+    ids = np.array([[[0, 1], [0, 2]],
+                    [[3, 3], [3, 3]]], np.int32)
+    ld = bench.expert_load(ids, 4)
+    assert ld["steps"] == 2 and ld["pairs_per_step"] == 4.0
+    assert ld["distinct_experts"] == (3 + 1) / 2
+    assert ld["max_tokens_per_expert"] == (2 + 4) / 2
+    assert ld["max_over_mean"] == (2 / 1 + 4 / 1) / 2           # mean per expert = 4 pairs / 4
+    assert ld["tokens_per_expert_p50_p90_p99"][0] == float(np.percentile([2, 1, 1, 0, 0, 0, 0, 4], 50))
+    h = bench.host_info()
+    assert h["nproc"] and h["nproc"] >= 1
+    assert bench.informational(lambda: 1 / 0)["error"].startswith("ZeroDivisionError")
