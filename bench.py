@@ -708,21 +708,28 @@ def run_colibri(args):
                                            device="cuda")
     KE = min(K, 500)
     e2e_s = 0.0
+
+    def e2e_call(i):
+        if f32:
+            x.copy_(x_pin[i % N_X], non_blocking=True)
+            layer_fn(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws, stream=stream)
+            out_pin.copy_(out, non_blocking=True)
+            stream.synchronize()
+        else:
+            C.colibri_moe_layer_host(dl.cfg, x_pin[i % N_X], dl.Wr, dl.bias, dl.table, dl.shared, None, None,
+                                     False, out_pin, ws_host, stream=stream)
+
     with torch.cuda.stream(stream):
+        for i in range(max(W, 3)):               # untimed warm-up calls of the same entry point
+            e2e_call(i)
+        stream.synchronize()
         for i in range(KE):
             flush.fill_(float(i))
             scrub.sum()
             graph_prev.replay()
             stream.synchronize()
             t0 = time.perf_counter()
-            if f32:
-                x.copy_(x_pin[i % N_X], non_blocking=True)
-                layer_fn(dl.cfg, x, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws, stream=stream)
-                out_pin.copy_(out, non_blocking=True)
-                stream.synchronize()
-            else:
-                C.colibri_moe_layer_host(dl.cfg, x_pin[i % N_X], dl.Wr, dl.bias, dl.table, dl.shared, None, None,
-                                         False, out_pin, ws_host, stream=stream)
+            e2e_call(i)
             e2e_s += time.perf_counter() - t0
     e2e_s = allreduce_max(torch, world, e2e_s)
     e2e_value = world * T * KE / e2e_s

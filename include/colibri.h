@@ -171,15 +171,18 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
  *   The workspace is a fixed array of COLIBRI_NOALLOC_SCRATCH_BYTES (16 MiB) that the
  *   library holds in the memory of every device it is loaded on, until the process
  *   exits. The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
- *   library routine. The first call made with a device current looks up the array's
- *   device address on that device (cudaGetSymbolAddress); make that first call before
- *   any stream capture.
+ *   library routine. The first call made in a device's context looks up the array's
+ *   device address there (cudaGetSymbolAddress, which may load the library's module);
+ *   make that first call before any stream capture. The address is kept per device
+ *   with the id of the context it belongs to: after a cudaDeviceReset (or the primary
+ *   context released and created again) the next call looks it up afresh, so a call
+ *   never uses an address of a destroyed context.
  *   Arguments, layouts and results are those of colibri_moe_layer. Returns
  *   COLIBRI_E_NOMEM when colibri_moe_workspace_bytes(cfg, T) exceeds the array (the
  *   GLM-5.2-shaped layer fits up to T = 32), COLIBRI_E_INVAL on a bad configuration.
  *   Every call on a device shares the one array and leaves its contents behind for
- *   the next call; each call rewrites what it reads (its first kernel clears the
- *   error flag). Calls whose work overlaps on the GPU (other streams, other host
+ *   the next call; each call rewrites what it reads (the layer's host code clears the
+ *   error flag and the kernels' sync counters with a memset before its first kernel). Calls whose work overlaps on the GPU (other streams, other host
  *   threads) race on the array and corrupt each other's results: serialise them.
  *   Device-side errors (an id out of range) are skipped by the kernels as in
  *   colibri_moe_layer; this variant offers no reader for the flag. */
@@ -288,11 +291,14 @@ int colibri_debug_group_dots(const uint8_t *w, const int8_t *qa, int rows, int c
                              int32_t *dots, void *stream);
 
 /* Test export: D = A B^T for one tile of integer codes on the tcgen05 tensor core, as the
- * prefill grouped GEMM computes its per-group dots (codes as bf16, fp32 accumulation in
- * tensor memory, exact for these ranges).
+ * prefill grouped GEMM computes its per-group dots: the codes enter a kind::f16 MMA as
+ * bf16 (every integer in [-128, 127] is exact in bf16) and accumulate in fp32 in tensor
+ * memory, which is exact for these ranges. (The integer MMA, tcgen05.mma kind::i8, does
+ * not exist on sm_103a: ptxas answers "Feature '.kind::i8' not supported on .target
+ * 'sm_103a'".)
  *   a device int8 [128][k] (values in [-128, 127]), b device int8 [n][k], row-major;
  *   d device int32 [128][n] (out). n % 16 == 0, n <= 256; k % 16 == 0, k <= 256. */
-int colibri_debug_umma_i8(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, void *stream);
+int colibri_debug_umma_codes(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, void *stream);
 
 /* ---- HBM expert cache -------------------------------------------------------------
  * Experts stream from a larger, slower tier into a small LRU cache of HBM slots

@@ -85,7 +85,7 @@ def lib() -> ctypes.CDLL:
                                        _P, _P, _P, _P, _P]),
                 "orc_expert_token_f32": (_I, [_I, _I, ctypes.POINTER(Expert), _P, _P, _P]),
                 "orc_q8_quantize_g": (_I, [_P, _I64, _I64, _I, _P, _P]),
-                "orc_group_dots_g": (None, [_P, _P, _I64, _I64, _I, _P]),
+                "orc_group_dots_g": (_I, [_P, _P, _I64, _I64, _I, _P]),
                 "orc_expert_token_g": (_I, [_I, _I, _I, ctypes.POINTER(Expert), _P, _P, _P, _P, _P, _P]),
                 "orc_expert_token_f32_g": (_I, [_I, _I, _I, ctypes.POINTER(Expert), _P, _P, _P]),
                 "orc_moe_layer_g": (_I, [ctypes.POINTER(Cfg), _I, _I, _P, _I64, _P, _P,
@@ -206,8 +206,8 @@ def group_dots(w_packed: np.ndarray, qa: np.ndarray, group: int = 32) -> np.ndar
     out = np.empty((rows, cols // group), np.int32)
     if group == 32:
         lib().orc_group_dots(_ptr(w), _ptr(qa), rows, cols, _ptr(out))
-    else:
-        lib().orc_group_dots_g(_ptr(w), _ptr(qa), rows, cols, group, _ptr(out))
+    elif lib().orc_group_dots_g(_ptr(w), _ptr(qa), rows, cols, group, _ptr(out)) != 0:
+        raise ValueError("group_dots: the oracle rejected the group size")
     return out
 
 

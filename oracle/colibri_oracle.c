@@ -315,13 +315,16 @@ static inline void group_dots_n(const uint8_t *w, const int8_t *qa, int64_t rows
     }
 }
 
-void orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots)
+int orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots)
 {
+    if (!group_ok(group) || rows < 0 || cols < 0 || cols % group != 0)
+        return -1;
     /* the same loop with the group size as a constant of each call */
     if (group == 64)
         group_dots_n(w, qa, rows, cols, 64, dots);
     else
         group_dots_n(w, qa, rows, cols, 32, dots);
+    return 0;
 }
 
 void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int32_t *dots)
@@ -388,6 +391,7 @@ int orc_expert_token(int d, int f, const orc_expert *ex, const int8_t *qx, const
  * gate_n = sum_k s1[n][k/32] * q1[n][k] * x[k] and up_n likewise (fp64, k ascending);
  * h_n = silu(gate_n) * up_n rounded to fp32; y_m = sum_j s2[m][j/32] * q2[m][j] * h_j
  * (fp64, j ascending) rounded to fp32. Nothing is quantised but the weights. */
+/* group is 32 or 64: its only caller, orc_expert_token_f32_g, rejects any other size */
 static double dot_row_f32(const uint8_t *wrow, const float *srow, const float *v, int K, int group, int8_t *q)
 {
     orc_unpack_int4(wrow, K / 2, q);

@@ -97,8 +97,9 @@ int orc_bucket(const int32_t *ids, int64_t T, int k, int E, int32_t *offsets, in
 
 /* dots[r][g] = sum over the 32 k in group g of unpack(w)[r][k] * qa[k] (int32). */
 void orc_group_dots(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int32_t *dots);
-/* The same per `group` (32 or 64) columns; dots [rows][cols/group]. */
-void orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots);
+/* The same per `group` (32 or 64) columns; dots [rows][cols/group]. Returns 0, or -1
+ * (dots untouched) for another group size or cols not a multiple of it. */
+int orc_group_dots_g(const uint8_t *w, const int8_t *qa, int64_t rows, int64_t cols, int group, int32_t *dots);
 
 /* One token through one expert of intermediate size f: gate/up group dots, SwiGLU,
  * q8 of h, down group dots. y [d] fp32; qh [f] and sh [f/32] receive h's codes and h_out

@@ -80,7 +80,7 @@ SIGNATURES = {
     "colibri_workspace_status": (_I, [_PCFG, _I, _P, ctypes.POINTER(_I), _P]),
     "colibri_moe_workspace_view": (_I, [_PCFG, _I, ctypes.POINTER(WorkspaceView)]),
     "colibri_debug_group_dots": (_I, [_P, _P, _I, _I, _P, _P]),
-    "colibri_debug_umma_i8": (_I, [_P, _P, _I, _I, _P, _P]),
+    "colibri_debug_umma_codes": (_I, [_P, _P, _I, _I, _P, _P]),
     "colibri_moe_profile_enable": (_I, [_I]),
     "colibri_moe_profile_read": (_I, [ctypes.POINTER(ctypes.c_float), _I]),
     "colibri_expert_cache_init": (_I, [ctypes.POINTER(_P), _P, _SZ, _P, _I, _I, _I, _I, _I, _P]),
@@ -263,11 +263,11 @@ def colibri_debug_group_dots(w, qa, dots, rows: int, cols: int, stream=None):
            lib().colibri_debug_group_dots(_ptr(w), _ptr(qa), rows, cols, _ptr(dots), _stream(stream)))
 
 
-def colibri_debug_umma_i8(a, b, d, stream=None):
+def colibri_debug_umma_codes(a, b, d, stream=None):
     """d[128][n] = a[128][k] . b[n][k]^T on the tensor core (int8 codes as bf16)."""
     n, k = b.shape
-    _check("colibri_debug_umma_i8",
-           lib().colibri_debug_umma_i8(_ptr(a), _ptr(b), n, k, _ptr(d), _stream(stream)))
+    _check("colibri_debug_umma_codes",
+           lib().colibri_debug_umma_codes(_ptr(a), _ptr(b), n, k, _ptr(d), _stream(stream)))
 
 
 PROFILE_KERNELS = ("q8", "router_logits", "router_select", "bucket", "gateup", "down", "combine")

@@ -640,7 +640,7 @@ int colibri_moe_profile_read(float *ms, int n)
     return COLIBRI_OK;
 }
 
-int colibri_debug_umma_i8(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, void *stream)
+int colibri_debug_umma_codes(const int8_t *a, const int8_t *b, int n, int k, int32_t *d, void *stream)
 {
     if (!a || !b || !d || n <= 0 || n % 16 || n > 256 || k <= 0 || k % 16 || k > 256)
         return COLIBRI_E_INVAL;

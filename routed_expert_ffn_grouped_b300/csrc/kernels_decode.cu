@@ -36,6 +36,8 @@
 // (router logits and scores, q8 of x): before waiting for that kernel, each CTA sends its
 // share of the shared expert's weights towards L2 and the producer streams the shared
 // expert's gate/up items, which need no routing.
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace clb {
@@ -1221,8 +1223,11 @@ cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
     auto fn = k_decode<TCH>;
     const size_t smem = ring_layout(a, a.ring, a.nh, a.nbuf, TCH).total;
     // per device: the SM count and the largest dynamic shared memory set so far (the
-    // attribute belongs to the device's context), so that a call costs no queries
+    // attribute belongs to the device's context), so that a call costs no queries; host
+    // threads that launch at the same time take the lock, so the attribute and its record
+    // agree
     constexpr int MAX_DEV = 64;
+    static std::mutex mu;
     static int sm_count[MAX_DEV] = {};
     static size_t smem_set[MAX_DEV] = {};
     int dev = 0;
@@ -1231,20 +1236,24 @@ cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
         return e;
     if (dev < 0 || dev >= MAX_DEV)
         return cudaErrorInvalidDevice;
-    if (sm_count[dev] == 0) {
-        int n = 0;
-        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess)
-            return e;
-        sm_count[dev] = n;
+    int n_sm = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (sm_count[dev] == 0) {
+            int n = 0;
+            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess)
+                return e;
+            sm_count[dev] = n;
+        }
+        if (smem > smem_set[dev]) {
+            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess)
+                return e;
+            smem_set[dev] = smem;
+        }
+        n_sm = sm_count[dev];
     }
-    if (smem > smem_set[dev]) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        smem_set[dev] = smem;
-    }
-    const int n_sm = sm_count[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_sm);
     cfg.blockDim = dim3((NC + 1 + NE_MAX) * 32);

@@ -69,6 +69,8 @@ __device__ __forceinline__ bool pair_expert(const F32Args &a, int p, colibri_exp
     t = p / a.K;
     f = a.ffn;
     if (e < 0 || e >= a.E) {
+        // row block 0 exists for every pair (f >= 32), so this block always runs and the
+        // flag is raised once per bad id
         if (blockIdx.x == 0 && threadIdx.x == 0)
             atomicOr(a.err, ERR_BAD_ID);
         return false;

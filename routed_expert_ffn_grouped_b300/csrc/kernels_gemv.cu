@@ -1,5 +1,6 @@
 // Combine (out = y_shared + sum_i w_i * y_i in slot order) and the group-dot test export.
-// The decode GEMVs live in kernels_stream.cu.
+// The decode GEMVs live in kernels_decode.cu (int8 activations) and kernels_f32act.cu
+// (fp32 activations).
 #include "kernels.cuh"
 
 namespace clb {

@@ -42,9 +42,14 @@ def bf16_codes(raw):
     return (raw[:, pos].astype(np.uint32) << 16).view(np.float32).astype(np.int64)
 
 
-def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TOL):
+def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TOL, tokens=None, threads=1):
     """q8(h) codes and scales of every (token, expert) pair against the oracle's, then
     the layer output. Returns the number of codes that differ.
+
+    x, ids, w: the whole batch the layer ran on (T tokens). tokens: the token indices to
+    check (default all T); out and ref then hold those tokens' rows, in that order (ref
+    from the oracle on those tokens). threads > 1 checks tokens in parallel (the oracle's
+    C calls release the GIL).
 
     Codes and scales must be equal, except where the oracle's h lies within the kernel's
     fp32 error (h_error_bound) of a rounding boundary of q8: there either code is a
@@ -54,6 +59,7 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
     |W2| (dequantised) applied to |h_kernel - h_oracle| (dequantised). Where every code
     agrees that extra term is zero."""
     T, K, d = x.shape[0], spec.top_k, spec.d
+    tokens = list(range(T)) if tokens is None else [int(t) for t in tokens]
     v = C.colibri_moe_workspace_view(C.layer_cfg(spec), T)
     rows = T * K + (T if spec.has_shared else 0)
     if T > 32:
@@ -61,22 +67,24 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
     else:
         codes = ws_slice(ws, v.hq, rows * v.fmax, np.int8).reshape(rows, v.fmax).astype(np.int64)
     scales = ws_slice(ws, v.hs, 4 * rows * v.hs_stride, np.float32).reshape(rows, v.hs_stride)
-    qx, sx = orc.q8_quantize(x)
-    allow = np.zeros((T, d))
-    n_diff = 0
-    for t in range(T):
+    qx, sx = orc.q8_quantize(x[tokens])
+
+    def one(j):
+        t = tokens[j]
+        allow = np.zeros(d)
+        n_diff = 0
         pairs = [(t * K + i, host.expert(int(ids[t, i])), float(w[t, i]), spec.ffn) for i in range(K)]
         if spec.has_shared:
             pairs.append((T * K + t, host.shared(), 1.0, spec.shared_ffn))
         for pr, view, wt, f in pairs:
-            _, qh, sh, h = orc.expert_token(view, qx[t], sx[t], want_h=True)
+            _, qh, sh, h = orc.expert_token(view, qx[j], sx[j], want_h=True)
             c, gsc = codes[pr, :f], scales[pr, :f // 32]
             dq = c - qh
             dsc = gsc.view(np.uint32) != sh.view(np.uint32)
             if not (dq.any() or dsc.any()):
                 continue
             assert np.abs(dq).max() <= 1, (t, pr)
-            relg = h_error_bound(orc, view, qx[t], sx[t]).reshape(-1, 32)
+            relg = h_error_bound(orc, view, qx[j], sx[j]).reshape(-1, 32)
             sh64 = sh.astype(np.float64)
             assert np.all(sh64 > 0), (t, pr)
             r = np.abs(h.astype(np.float64)).reshape(-1, 32) / sh64[:, None]
@@ -90,7 +98,17 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
             dh = np.abs(c * np.repeat(gsc.astype(np.float64), 32) - qh * np.repeat(sh64, 32))
             w2 = np.abs(orc.unpack_int4(view["w2"]).astype(np.float64))
             w2 *= np.repeat(view["s2"].astype(np.float64), 32, axis=1)
-            allow[t] += wt * (w2 @ dh)
+            allow += wt * (w2 @ dh)
+        return allow, n_diff
+
+    if threads > 1 and len(tokens) > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(threads) as ex:
+            res = list(ex.map(one, range(len(tokens))))
+    else:
+        res = [one(j) for j in range(len(tokens))]
+    allow = np.stack([a for a, _ in res]) if res else np.zeros((0, d))
+    n_diff = sum(n for _, n in res)
     want = np.asarray(ref, np.float64)
     rms = np.sqrt(np.mean(want ** 2))
     err = np.abs(np.asarray(out, np.float64) - want)
@@ -98,3 +116,8 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
     assert not bad.any(), (f"{int(bad.sum())} outputs off; worst excess "
                            f"{float((err - tol * rms - allow).max()):.3e} (rms {rms:.3e})")
     return n_diff
+
+
+def h_codes_checked(spec, n_tokens):
+    """Codes of q8(h) that check_h_codes_and_output compares for n_tokens tokens."""
+    return n_tokens * (spec.top_k * spec.ffn + (spec.shared_ffn if spec.has_shared else 0))

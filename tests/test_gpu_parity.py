@@ -9,7 +9,7 @@ import pytest
 
 from routed_expert_ffn_grouped_b300 import synth
 
-from h_codes import check_h_codes_and_output
+from h_codes import check_h_codes_and_output, h_codes_checked
 
 pytestmark = pytest.mark.gpu
 
@@ -141,7 +141,7 @@ def test_umma_tile_integer_dots_exact(torch_cuda, C, n, k):
     a[0, :32 if k >= 32 else k] = -8                  # the extreme group: -8 x -127 per element
     b[0, :32 if k >= 32 else k] = -127
     d = torch.empty((128, n), dtype=torch.int32, device="cuda")
-    C.colibri_debug_umma_i8(to_dev(torch, a), to_dev(torch, b), d)
+    C.colibri_debug_umma_codes(to_dev(torch, a), to_dev(torch, b), d)
     torch.cuda.synchronize()
     want = a.astype(np.int64) @ b.astype(np.int64).T
     assert want[0, 0] == 1016 * min(k, 32) + (int(a[0, 32:].astype(np.int64) @ b[0, 32:].astype(np.int64)) if k > 32 else 0)
@@ -167,9 +167,28 @@ def ws_slice(ws, off, nbytes, dtype):
     return ws[off:off + nbytes].cpu().numpy().view(dtype)
 
 
+def assert_buckets_exact(C, dl, ws, T, ids_o):
+    """Bucket offsets and the pair list the layer left in its workspace: bit-exact against
+    the oracle's stable counting sort of the oracle's ids (a non-stable scatter, or a wrong
+    scan, fails here even where the outputs would agree)."""
+    spec = dl.spec
+    v = C.colibri_moe_workspace_view(dl.cfg, T)
+    off = ws_slice(ws, v.offsets, 4 * (spec.n_exp + 1), np.int32)
+    pairs = ws_slice(ws, v.pairs, 4 * T * spec.top_k, np.int32)
+    off_o, pairs_o = orc_bucket(ids_o, spec.n_exp)
+    assert np.array_equal(off, off_o), "bucket offsets differ"
+    assert np.array_equal(pairs, pairs_o), "pair list differs"
+    return off_o, pairs_o
+
+
+def orc_bucket(ids, E):
+    import oracle
+    return oracle.bucket(ids, E)
+
+
 @pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 1), ("tiny", 13), ("olmoe", 1), ("olmoe", 16),
                                     ("glm52", 1), ("glm52", 4), ("glm52", 32)])
-def test_moe_layer_parity(torch_cuda, C, orc, name, T):
+def test_moe_layer_parity(torch_cuda, C, orc, flip_report, name, T):
     torch = torch_cuda
     spec = synth.SPECS[name]
     host, dl = dev_layer(C, spec)
@@ -182,7 +201,8 @@ def test_moe_layer_parity(torch_cuda, C, orc, name, T):
     assert_rms_close(out, ref)
     if T * spec.top_k <= 64:
         # every pair's q8(h) codes and scales (larger batches: the sample below)
-        check_h_codes_and_output(orc, C, spec, host, x, ids_o, w_o, ws, out, ref)
+        n = check_h_codes_and_output(orc, C, spec, host, x, ids_o, w_o, ws, out, ref)
+        flip_report(n, h_codes_checked(spec, T))
     # intermediates inside the workspace: q8 codes of x and the bucket lists, bit-exact
     v = C.colibri_moe_workspace_view(dl.cfg, T)
     qx = ws_slice(ws, v.qx, T * spec.d, np.int8).reshape(T, spec.d)
@@ -249,9 +269,10 @@ def test_moe_layer_empty_and_deterministic(torch_cuda, C):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", 33), ("tiny", 100), ("olmoe", 48)])
-def test_prefill_gemm_parity(torch_cuda, C, orc, name, T):
+def test_prefill_gemm_parity(torch_cuda, C, orc, flip_report, name, T):
     """Batches above 32 tokens run the tcgen05 grouped GEMMs: every token against the
-    oracle, ragged token tiles (counts not multiples of the 64-token tile) included."""
+    oracle, ragged token tiles (counts not multiples of the 64-token tile) included; the
+    prefill bucketing kernel's offsets and pair list bit-exact."""
     torch = torch_cuda
     spec = synth.SPECS[name]
     host, dl = dev_layer(C, spec)
@@ -262,25 +283,79 @@ def test_prefill_gemm_parity(torch_cuda, C, orc, name, T):
     assert np.array_equal(ids, ids_o)
     np.testing.assert_allclose(w, w_o, rtol=1e-6)
     assert_rms_close(out, ref)
-    check_h_codes_and_output(orc, C, spec, host, x, ids_o, w_o, ws, out, ref)
+    assert_buckets_exact(C, dl, ws, T, ids_o)
+    n = check_h_codes_and_output(orc, C, spec, host, x, ids_o, w_o, ws, out, ref)
+    flip_report(n, h_codes_checked(spec, T))
 
 
-def test_glm_prefill_sampled(torch_cuda, C, orc):
-    """T = 2048 prefill; the oracle recomputes a sample of tokens (tokens are independent)."""
+def glm_prefill_check_tokens(counts, off_o, pairs_o, K, T, rng):
+    """Tokens of the GLM-shaped T = 2048 batch whose outputs and q8(h) codes are compared
+    with the oracle: the tokens of the last (ragged) 64-token tile and of the tile
+    boundary of the three busiest experts, every token of four experts that fit one
+    ragged tile (the fewest, a quarter, half and the most tokens below 64), and 64 more
+    drawn at random."""
+    picked = set()
+    busiest = np.argsort(-counts, kind="stable")[:3]
+    for e in busiest:
+        b, c = int(off_o[e]), int(counts[e])
+        last = ((c - 1) // 64) * 64
+        for j in list(range(last, c)) + [j for j in (63, 64) if j < c]:
+            picked.add(int(pairs_o[b + j]) // K)
+    small = [int(e) for e in np.argsort(counts, kind="stable") if 0 < counts[e] < 64]
+    if small:
+        for q in (0, len(small) // 4, len(small) // 2, len(small) - 1):
+            e = small[q]
+            for j in range(int(counts[e])):
+                picked.add(int(pairs_o[int(off_o[e]) + j]) // K)
+    picked.update(int(t) for t in rng.choice(T, 64, replace=False))
+    return sorted(picked)
+
+
+def test_glm_prefill_t2048(torch_cuda, C, orc, flip_report):
+    """The GLM-shaped prefill at its full size (T = 2048, Zipf-skewed expert loads):
+    ids, weights, q8 codes of x and the bucket lists of all 16,384 pairs bit-exact or
+    within 1e-6; outputs and every q8(h) code of a few hundred tokens chosen to cover the
+    busiest experts' ragged and boundary tiles and whole lightly loaded experts (tokens
+    are independent, so the oracle recomputes them alone)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
     torch = torch_cuda
     spec = synth.GLM52
     host, dl = dev_layer(C, spec)
-    T = 2048
+    T, K = 2048, spec.top_k
     x = synth.activations(spec, 0, T, step=21, row_scale=True)
     out, ids, w, ws = run_layer(torch, C, dl, x)
     assert C.colibri_workspace_status(dl.cfg, T, ws) == C.OK
-    io_all, _ = orc.router_topk(spec, x, host.Wr, host.bias)
+    io_all, wo_all = orc.router_topk(spec, x, host.Wr, host.bias)
     assert np.array_equal(ids, io_all)
-    counts = np.bincount(ids.ravel(), minlength=spec.n_exp)
-    assert counts.sum() == T * spec.top_k
-    for t in (0, 1, 777, 2047):
-        ref, _, _ = orc.moe_layer(spec, x[t:t + 1], host.Wr, host.bias, host.expert, host.shared())
-        assert_rms_close(out[t:t + 1], ref)
+    np.testing.assert_allclose(w, wo_all, rtol=1e-6)
+    v = C.colibri_moe_workspace_view(dl.cfg, T)
+    qx = ws_slice(ws, v.qx, T * spec.d, np.int8).reshape(T, spec.d)
+    sx = ws_slice(ws, v.sx, 4 * T * spec.d // 32, np.float32).reshape(T, -1)
+    qo, so = orc.q8_quantize(x)
+    assert np.array_equal(qx, qo) and np.array_equal(sx.view(np.uint32), so.view(np.uint32))
+    off_o, pairs_o = assert_buckets_exact(C, dl, ws, T, io_all)
+    counts = np.bincount(io_all.ravel(), minlength=spec.n_exp)
+    assert counts.sum() == T * K and counts.max() > 64      # skewed: the busiest expert spans tiles
+    toks = glm_prefill_check_tokens(counts, off_o, pairs_o, K, T, np.random.default_rng(7))
+    assert len(toks) >= 100
+    threads = max(1, min(16, os.cpu_count() or 1))
+    chunks = [toks[i::threads] for i in range(threads) if toks[i::threads]]
+
+    def ref_of(ch):
+        r, _, _ = orc.moe_layer(spec, x[ch], host.Wr, host.bias, host.expert, host.shared())
+        return ch, r
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(ref_of, chunks))
+    ref = np.empty((len(toks), spec.d), np.float32)
+    pos = {t: j for j, t in enumerate(toks)}
+    for ch, r in parts:
+        for t, row in zip(ch, r):
+            ref[pos[t]] = row
+    n = check_h_codes_and_output(orc, C, spec, host, x, io_all, wo_all, ws, out[toks], ref,
+                                 tokens=toks, threads=threads)
+    flip_report(n, h_codes_checked(spec, len(toks)))
 
 
 # d = 96: three 32-row blocks of d, so the down items' last pair has one block; ffn = 64:
@@ -290,7 +365,7 @@ ODD = synth.TINY.replace(name="odd96", d=96, ffn=64, n_exp=8, top_k=2, n_group=2
 
 
 @pytest.mark.parametrize("T", [1, 3, 7])
-def test_moe_layer_parity_odd_shape(torch_cuda, C, orc, T):
+def test_moe_layer_parity_odd_shape(torch_cuda, C, orc, flip_report, T):
     torch = torch_cuda
     host, dl = dev_layer(C, ODD)
     x = synth.activations(ODD, 0, T, step=3)
@@ -300,7 +375,9 @@ def test_moe_layer_parity_odd_shape(torch_cuda, C, orc, T):
     assert np.array_equal(ids, ids_o)
     np.testing.assert_allclose(w, w_o, rtol=1e-6)
     assert_rms_close(out, ref)
-    check_h_codes_and_output(orc, C, ODD, host, x, ids_o, w_o, ws, out, ref)
+    n = check_h_codes_and_output(orc, C, ODD, host, x, ids_o, w_o, ws, out, ref)
+    flip_report(n, h_codes_checked(ODD, T))
+    assert_buckets_exact(C, dl, ws, T, ids_o)
 
 
 
@@ -322,7 +399,7 @@ TOP1 = synth.TINY.replace(name="top1", n_exp=16, top_k=1, n_group=1, topk_group=
                                     (ALLK, 1), (ALLK, 3), (ALLK, 40), (GS1, 1), (GS1, 2), (GS1, 33),
                                     (TOP1, 1), (TOP1, 7), (TOP1, 33)],
                          ids=lambda v: v.name if hasattr(v, "name") else str(v))
-def test_moe_layer_parity_extreme_shapes(torch_cuda, C, orc, spec, T):
+def test_moe_layer_parity_extreme_shapes(torch_cuda, C, orc, flip_report, spec, T):
     torch = torch_cuda
     host, dl = dev_layer(C, spec)
     x = synth.activations(spec, 0, T, step=5)
@@ -331,18 +408,15 @@ def test_moe_layer_parity_extreme_shapes(torch_cuda, C, orc, spec, T):
     ref, ids_o, w_o = orc.moe_layer(spec, x, host.Wr, host.bias, host.expert, host.shared())
     assert np.array_equal(ids, ids_o)
     np.testing.assert_allclose(w, w_o, rtol=1e-6)
-    check_h_codes_and_output(orc, C, spec, host, x, ids_o, w_o, ws, out, ref)
+    n = check_h_codes_and_output(orc, C, spec, host, x, ids_o, w_o, ws, out, ref)
+    flip_report(n, h_codes_checked(spec, T))
     if spec is ALLK:
         assert all(sorted(r) == list(range(8)) for r in ids.tolist())
     if spec is TOP1:
         assert np.all(w == 1.0)
-    if T <= 32:
-        # bucket lists in the workspace: bit-exact
-        v = C.colibri_moe_workspace_view(dl.cfg, T)
-        off = ws_slice(ws, v.offsets, 4 * (spec.n_exp + 1), np.int32)
-        pairs = ws_slice(ws, v.pairs, 4 * T * spec.top_k, np.int32)
-        off_o, pairs_o = orc.bucket(ids_o, spec.n_exp)
-        assert np.array_equal(off, off_o) and np.array_equal(pairs, pairs_o)
+    # bucket lists in the workspace, bit-exact: the decode kernel's (T <= 32) and the
+    # prefill bucketing kernel's (T > 32)
+    assert_buckets_exact(C, dl, ws, T, ids_o)
 
 # ------------------------------------------------------------------ host-buffer entry point
 @pytest.mark.parametrize("name,T,pinned", [("glm52", 1, True), ("tiny", 13, False), ("olmoe", 16, True),

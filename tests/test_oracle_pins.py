@@ -497,6 +497,20 @@ def test_group_dots_g64_closed_forms_and_bruteforce(orc):
     assert np.array_equal(d32.reshape(24, 6, 2).sum(-1), want)
 
 
+def test_group_dots_rejects_other_group_sizes(orc):
+    """The C entry refuses a group size other than 32 or 64 (and cols not a multiple of
+    it) instead of computing some other grouping; the output stays untouched."""
+    import ctypes
+    L = orc.lib()
+    w = np.zeros((1, 64), np.uint8)
+    qa = np.ones(128, np.int8)
+    for group, cols in ((16, 128), (128, 128), (0, 128), (64, 96)):
+        out = np.full(8, 12345, np.int32)
+        rc = L.orc_group_dots_g(w.ctypes.data_as(ctypes.c_void_p), qa.ctypes.data_as(ctypes.c_void_p),
+                                1, cols, group, out.ctypes.data_as(ctypes.c_void_p))
+        assert rc == -1 and np.all(out == 12345), group
+
+
 def test_g64_gate_up_reduces_to_g32_when_halves_agree(orc):
     """Scales shared by the two 32-halves of each 64-group, and an x whose two halves of
     every 64-group have the same amax: the 64-group expert forms the same h as the pinned

@@ -46,12 +46,24 @@ def _rms_err(got, want):
     return err, rms
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 4), ("olmoe", 16)])
+_layers = {}
+
+
+def _device_layer(C, spec):
+    if spec.name not in _layers:
+        _layers[spec.name] = C.DeviceLayer(synth.make_layer(spec, 0))
+    return _layers[spec.name]
+
+
+# GLM-5.2-shaped at T = 32: the largest batch of that layer whose workspace fits the
+# fixed scratch array
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("olmoe", 16), ("glm52", 32)])
 def test_noalloc_matches_workspace_entry_point(torch_cuda, C, name, T):
     torch = torch_cuda
     spec = synth.SPECS[name]
-    dl = C.DeviceLayer(synth.make_layer(spec, 0))
+    dl = _device_layer(C, spec)
     cfg = dl.cfg
+    assert C.colibri_moe_workspace_bytes(cfg, T) <= C.NOALLOC_SCRATCH_BYTES
 
     def buffers():
         return (torch.empty((T, spec.d), dtype=torch.float32, device="cuda"),
