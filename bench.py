@@ -333,19 +333,15 @@ DECODE_T_MAX = 32   # largest T on the decode (GEMV) path; larger T takes the tc
 
 
 def launches_per_step(T: int, n_exp: int, ids_given: bool, f32: bool = False) -> int:
-    """Kernels one colibri_moe_layer call launches. Decode (T <= 32): one routing kernel
-    (router logits and scores with q8 of x, or q8 alone with the ids given), a selection
-    kernel when T x E > 4096 (else every CTA of the next kernel selects), then one kernel
-    for selection or bucketing, gate/up, down and combine. Prefill: q8, router logits,
-    selection, bucketing (q8 and bucketing alone with the ids given), the two tcgen05 GEMMs
-    and the combine. The fp32-activation decode: router logits and selection (unless the
-    ids are given), gate/up, down and the combine."""
+    """Kernels one colibri_moe_layer call launches. Decode (T <= 32): one kernel for q8 of
+    x, router logits, selection (or the given ids), bucketing, gate/up, down and combine.
+    Prefill: q8, router logits, selection, bucketing (q8 and bucketing alone with the ids
+    given), the two tcgen05 GEMMs and the combine. The fp32-activation decode: router
+    logits and selection (unless the ids are given), gate/up, down and the combine."""
     if f32:
         return 3 if ids_given else 5
     if T <= DECODE_T_MAX:
-        if ids_given:
-            return 2
-        return 2 if T * n_exp <= 4096 else 3
+        return 1
     return 5 if ids_given else 7
 
 
@@ -681,12 +677,12 @@ def run_colibri(args):
         gu_kernel = "k_gemm<0> (tcgen05 gate/up + SwiGLU + q8)"
         traffic = None
     else:
-        # two kernels; the other slots hold only the time of an event record
-        kern_ms = {"k_route_logits": mean["router_logits"], "k_decode": mean["gateup"],
-                   "event_records": mean["q8"] + mean["router_select"] + mean["bucket"] + mean["down"]
-                   + mean["combine"]}
+        # one kernel; the other slots hold only the time of an event record
+        kern_ms = {"k_decode": mean["gateup"],
+                   "event_records": mean["q8"] + mean["router_logits"] + mean["router_select"] + mean["bucket"]
+                   + mean["down"] + mean["combine"]}
         roof_ms = np.array(prof["gateup"])
-        gu_kernel = "k_decode (selection, bucketing, gate/up, down, combine)"
+        gu_kernel = "k_decode (q8 of x, router logits, selection, bucketing, gate/up, down, combine)"
         traffic = traffic_from_profiles("k_decode_glm52_decode_t1", "kernels_decode.cu", args.workload)
     gu_gbs = float(np.mean(np.array(prof_bytes) / (roof_ms / 1e3)) / 1e9)
     roof_tensor = None

@@ -358,12 +358,10 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     if (prof_mark(0, s))
         return COLIBRI_E_CUDA;
     const bool prefill = uses_gemm(cfg, T);
-    // q8 of x: plain codes and scales; decode also wants the even/odd codes and their
-    // corrections, prefill the bf16 codes in the tensor-core order
-    Q8Args qa{x, T, d, reinterpret_cast<int8_t *>(ws + L.qx), reinterpret_cast<float *>(ws + L.sx),
-              prefill ? nullptr : reinterpret_cast<int8_t *>(ws + L.qx_eo),
-              prefill ? nullptr : reinterpret_cast<int *>(ws + L.xc),
-              prefill ? reinterpret_cast<uint16_t *>(ws + L.xbf) : nullptr};
+    // q8 of x for prefill: plain codes and scales, and the bf16 codes in the tensor-core
+    // order (decode quantises x inside its kernel)
+    Q8Args qa{x, T, d, reinterpret_cast<int8_t *>(ws + L.qx), reinterpret_cast<float *>(ws + L.sx), nullptr,
+              nullptr, reinterpret_cast<uint16_t *>(ws + L.xbf)};
     const int down_blocks = (d + DN_ITEM_ROWS - 1) / DN_ITEM_ROWS;
     BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks, 0,
                   reinterpret_cast<int32_t *>(ws + L.offsets), reinterpret_cast<int32_t *>(ws + L.pairs),
@@ -376,24 +374,9 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     if (cfg->has_shared)
         sh = *shared;
     if (!prefill) {
-        // decode: routing inputs (router logits and scores with q8 of x on the side, or q8
-        // of x alone for given ids), then one kernel that selects, buckets and runs a6-a9
-        const bool select = !ids_given && decode_selects_in_kernel(T, E);
-        if (prof_mark(1, s))
-            return COLIBRI_E_CUDA;
-        if (ids_given) {
-            const long groups = (long)T * (d / G);
-            k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
-            if (cudaGetLastError() != cudaSuccess)
-                return COLIBRI_E_CUDA;
-        } else if (launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, qa, err, s)) {
-            return COLIBRI_E_CUDA;
-        }
-        if (prof_mark(2, s))
-            return COLIBRI_E_CUDA;
-        if (!ids_given && !select && launch_select(sa, s))  // many experts: selection kernel
-            return COLIBRI_E_CUDA;
-        if (prof_mark(3, s) || prof_mark(4, s))
+        // decode: one kernel for q8 of x, router logits, selection (unless ids_given),
+        // bucketing, gate/up, down and the combine
+        if (prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s) || prof_mark(4, s))
             return COLIBRI_E_CUDA;
         DecodeArgs da{};
         da.experts = experts;
@@ -405,7 +388,10 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
         da.K = K;
         da.has_shared = cfg->has_shared;
         da.fmax = (int)L.fmax;
-        da.ids_given = !select;
+        da.x = x;
+        da.Wr = ids_given ? nullptr : Wr;
+        da.bias = cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : bias;
+        da.ids_given = ids_given ? 1 : 0;
         da.E = E;
         da.n_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->n_group;
         da.topk_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->topk_group;
@@ -422,9 +408,10 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
         da.pairs = reinterpret_cast<int32_t *>(ws + L.pairs);
         da.slots = reinterpret_cast<Slot *>(ws + L.slots);
         da.counters = reinterpret_cast<Counters *>(ws + L.counters);
-        da.xq_eo = reinterpret_cast<const int8_t *>(ws + L.qx_eo);
-        da.xs = reinterpret_cast<const float *>(ws + L.sx);
-        da.xc = reinterpret_cast<const int *>(ws + L.xc);
+        da.qx = reinterpret_cast<int8_t *>(ws + L.qx);
+        da.xq_eo = reinterpret_cast<int8_t *>(ws + L.qx_eo);
+        da.sx = reinterpret_cast<float *>(ws + L.sx);
+        da.xc = reinterpret_cast<int *>(ws + L.xc);
         da.hq = reinterpret_cast<int8_t *>(ws + L.hq);
         da.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
         da.hs = reinterpret_cast<float *>(ws + L.hs);
@@ -433,6 +420,7 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
         da.out = out;
         int *sync = reinterpret_cast<int *>(ws + L.sync);
         da.claim = sync;
+        da.route_done = sync + 1;
         da.done_gu = sync + 4;
         da.done_rb = sync + 4 + L.nslots;
         da.err = err;

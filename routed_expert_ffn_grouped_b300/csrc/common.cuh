@@ -145,6 +145,26 @@ __device__ __forceinline__ int q8_code(float x, float d)
     return (int)v;
 }
 
+// q8_code(x, d) given r = fp32(1/d) (__frcp_rn), the same code with one multiplication in
+// place of the division, except next to a rounding boundary. With f = fp32(x/d) and
+// y = fp32(x * r), |y - f| <= |x/d| * (2^-23 + 2^-24 + 2^-48) <= 2.3e-5 while |x/d| <= 128,
+// so roundf(y) == roundf(f) whenever y is more than 1e-4 away from every half-integer;
+// nearer (and for any y that is not a finite value below 128 in magnitude) the exact
+// division decides.
+__device__ __forceinline__ int q8_code_r(float x, float d, float r)
+{
+    if (d == 0.0f)
+        return 0;
+    const float y = x * r;
+    float v;
+    if (fabsf(y) <= 128.0f && fabsf(y - floorf(y) - 0.5f) > 1e-4f)
+        v = roundf(y);
+    else
+        v = roundf(__fdiv_rn(x, d));
+    v = fminf(fmaxf(v, -127.0f), 127.0f);
+    return (int)v;
+}
+
 // ---- mbarrier + 1-D bulk copy (cp.async.bulk) ---------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {

@@ -49,30 +49,35 @@ struct BucketArgs {
     int *err;
 };
 
-// Decode GEMVs (kernels_decode.cu).
-enum { MODE_GATEUP = 0, MODE_DOWN = 1 };
+// Decode (kernels_decode.cu).
+enum { MODE_GATEUP = 0, MODE_DOWN = 1, MODE_LOGIT = 2 };
 constexpr int DN_ITEM_ROWS = 32;  // rows of d per down work unit in the bucketing counters
 
 struct DecodeArgs {
     const colibri_expert *experts;
     colibri_expert shared;
     int d, ffn, shared_ffn, T, K, has_shared, fmax;
-    // routing, done by every CTA: selection from the router scores (sigmoid: s, c;
-    // softmax: logits; [T][E]) unless ids_given, then bucketing
+    // routing inputs: activations [T][d], router matrix [E][d] and bias [E] (sigmoid mode;
+    // may be null); unused when ids_given
+    const float *x, *Wr, *bias;
     int ids_given, E, n_group, topk_group, router, norm_topk;
     float routed_scale;
-    const float *logits, *rs, *rc;
+    // router logits, sigmoid scores s and biased scores c [T][E], written by the logit items
+    float *logits, *rs, *rc;
     int32_t *ids;       // [T][K]: given, or the selection (written by CTA 0)
     const float *w_in;  // [T][K] given weights
     float *w_out;       // [T][K] selected weights (CTA 0)
-    // bucketing results, written to the workspace by CTA 0
+    // bucketing results (every CTA keeps its own copy in shared memory; CTA 0 writes them
+    // here for inspection): bucket offsets, pair list, slots, counters
     int32_t *offsets, *pairs;
     Slot *slots;
     Counters *counters;
-    // q8 of x in even/odd order, its scales and +8 corrections (row = token)
-    const int8_t *xq_eo;
-    const float *xs;
-    const int *xc;
+    // q8 of x, each CTA's share quantised by its epilogue warps: plain codes (for
+    // inspection), codes in even/odd word order, scales, corrections 8 * sum(codes) per
+    // 32-group (read by every CTA once the routing counter is complete)
+    int8_t *qx, *xq_eo;
+    float *sx;
+    int *xc;
     // q8(h) (row = pair; the shared expert's rows follow the T*K routed pairs; scales and
     // corrections hgs to a row), written by the gate/up items and read by the down items
     int8_t *hq, *hq_eo;
@@ -80,25 +85,26 @@ struct DecodeArgs {
     int *hc;
     float *y;    // down outputs [pairs][d]
     float *out;  // layer output [T][d]
-    // zeroed per call: the work-claim counter, finished rows of h per slot, finished rows
-    // of y per row block of d
-    int *claim, *done_gu, *done_rb;
+    // zeroed per call: the work-claim counter, the routing counter (logit tasks (expert,
+    // token) and q8 groups of x done), finished rows of h per slot, finished rows of y per
+    // row block of d
+    int *claim, *route_done, *done_gu, *done_rb;
     int *err;
     int max_slots;  // the shared expert + min(E, T*K) routed slots
     // set by launch_decode: ring stages, h buffers, partial-sum buffers (= epilogue warps),
-    // tokens per chunk, groups per h row
+    // tokens per chunk, groups per h row; logit items: experts and tokens per item, K
+    // columns per stage, stages per item, items (0 with the ids given); warps that select
+    // at once
     int ring, nh, nbuf, tch, hgs;
+    int lg_ne, lg_tb, lg_kc, lg_nck, n_logit, sel_warps;
 };
 
-// One persistent launch for a decode step's routing (selection unless ids_given, and
-// bucketing) and experts (gate/up, down, combine), started as a programmatic dependent of
-// the kernel before it.
+// One persistent launch for a decode step: router logits, expert selection (unless
+// ids_given) and bucketing, then gate/up, down and the combine.
 cudaError_t launch_decode(DecodeArgs a, cudaStream_t s);
 // Scales (and corrections) a row of q8(h) holds on the decode path: fmax/32 rounded up to
 // 16 bytes.
 int decode_hgs(int fmax);
-// Whether the decode kernel selects the experts itself (else a selection kernel does).
-bool decode_selects_in_kernel(int T, int E);
 
 // Prefill grouped GEMMs on tcgen05 (kernels_gemm.cu).
 struct GemmArgs {

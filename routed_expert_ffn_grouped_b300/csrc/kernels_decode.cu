@@ -1,6 +1,5 @@
-// Decode (T <= 32 tokens): the experts of a layer in one persistent kernel. Each CTA
-// routes (expert selection from the router scores, or the given ids, and bucketing into
-// slots) in shared memory, then runs fused gate/up + SwiGLU + q8(h), down, and the
+// Decode (T <= 32 tokens): a whole routed MoE layer in one persistent kernel: router
+// logits, expert selection and bucketing, fused gate/up + SwiGLU + q8(h), down, and the
 // weighted combine with the shared expert.
 //
 // Expert matrices are stored in row blocks of 32 rows, group-major inside a block: the 16
@@ -10,11 +9,16 @@
 // W2 for down (64 rows of y); either way a stage holds the same group range of two 32-row
 // blocks, so one code path computes both.
 //
-// Items are claimed from a device counter, in the order: the shared expert's gate/up
-// items, the routed slots' gate/up items, then the down items slot by slot. A CTA
-// processes its items in claim order, so no down item precedes a gate/up item in any CTA
-// and every wait below ends (a down item waits for the gate/up items of its slot, all of
-// which were claimed earlier by running CTAs).
+// Items are claimed from a device counter, in the order: the logit items (a block of
+// router rows against a block of tokens, streamed in K-chunks), the shared expert's
+// gate/up items, the routed slots' gate/up items, then the down items slot by slot. The
+// CTA that completes the last logit item selects the experts of every token (one warp per
+// token, from the scores the logit items left in the workspace), buckets the pairs and
+// publishes the routing table with a flag; every other CTA streams the shared expert
+// meanwhile and copies the table into its shared memory when it reaches a routed item. A
+// CTA processes its items in claim order, so every wait below is for work claimed earlier
+// by a running CTA and ends: the table waits for the logit items, a down item for the
+// gate/up items of its slot.
 //
 // One CTA per SM, three roles. The producer warp claims items (two ahead, so a claim's
 // latency hides behind the copies of the items before) and streams each item through a
@@ -25,17 +29,13 @@
 // items of its slot are done, ahead of the consumers. The consumer warps split each
 // stage's groups; lane l owns row l of the block and reads its 16 bytes of a group tile
 // from shared memory, so a lane accumulates whole row dots over its groups in registers.
-// At the end of a chunk the consumers leave their partial sums in one of several buffers
-// and go on; an epilogue warp per buffer adds them in a fixed order, writes h (SwiGLU +
-// q8) or y, and publishes the result with a device-scope fence and a counter: rows of h
-// finished per slot, rows of y finished per row block of d. The epilogue warp that
-// completes a row block of d adds the slots' outputs for it in slot order:
+// Each CTA quantises the activations itself (q8 of x, into shared memory). At the end of
+// a chunk the consumers leave their partial sums in one of several buffers and go on; an
+// epilogue warp per buffer adds them in a fixed order, writes h (SwiGLU + q8) or y, and
+// publishes the result with a device-scope fence and a counter: rows of h finished per
+// slot, rows of y finished per row block of d. The epilogue warp that completes a row
+// block of d adds the slots' outputs for it in slot order:
 // out = y_shared + sum_i w_i * y_i.
-//
-// The kernel is launched as a programmatic dependent of the routing kernel before it
-// (router logits and scores, q8 of x): before waiting for that kernel, each CTA sends its
-// share of the shared expert's weights towards L2 and the producer streams the shared
-// expert's gate/up items, which need no routing.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -54,6 +54,9 @@ constexpr size_t SMEM_BUDGET = 227 * 1024;  // the largest opt-in dynamic shared
 constexpr int NE_MAX = 4;                    // epilogue warps launched
 constexpr int NH_MAX = 3;                    // h buffers at most
 constexpr int TAG_NEW_H = 1 << 20;           // stage tag: this chunk starts a new h buffer
+constexpr int TAG_END = -1, TAG_ROUTE = -2;  // stage tags (item field): end of work, routing
+constexpr int LT = 8;                        // logit tasks (expert, token) per consumer warp and item
+constexpr int SEL_SCRATCH = 32 * 1024;       // selection scratch of the routing CTA (bytes, at most)
 
 
 __host__ __device__ constexpr int round_up(int v, int m)
@@ -62,7 +65,6 @@ __host__ __device__ constexpr int round_up(int v, int m)
 }
 
 struct DecItem {
-    colibri_expert ex;
     int mode, slot, is_shared, rb, begin, count, kdim;
 };
 
@@ -72,6 +74,23 @@ struct SlotInfo {
     colibri_expert ex;
     int begin, count, pad[2];
 };
+
+// A logit item: router rows [e0, e0 + ne) against tokens [t0, t0 + ntok).
+struct LogitItem {
+    int e0, ne, t0, ntok;
+};
+
+__device__ __forceinline__ LogitItem logit_item(const DecodeArgs &a, int idx)
+{
+    const int neb = (a.E + a.lg_ne - 1) / a.lg_ne;
+    const int eb = idx % neb, tb = idx / neb;
+    LogitItem li;
+    li.e0 = eb * a.lg_ne;
+    li.ne = min(a.lg_ne, a.E - li.e0);
+    li.t0 = tb * a.lg_tb;
+    li.ntok = min(a.lg_tb, a.T - li.t0);
+    return li;
+}
 
 // What an epilogue warp needs about a finished chunk.
 struct ChunkDesc {
@@ -86,13 +105,25 @@ struct RingLayout {
     size_t hb;  // bytes of one h buffer
 };
 
-// Bytes of the routing scratch (selection and bucketing), laid over the x staging area.
-__host__ __device__ __forceinline__ size_t route_scratch_bytes(int T, int E, int K, bool select)
+// Bytes of the routing scratch (selection and bucketing), laid over the partial-sum
+// buffers (which no chunk uses before routing; the logit items keep their chains there
+// too): picked ids and first-occurrence flags of the T*K pairs, then per selecting warp
+// two score rows (c or logits, and s) of E floats and 32 picks.
+// The selection of all T tokens at once by the whole CTA (select_cta) keeps every token's
+// scores in shared memory: up to T * E = 4096.
+__host__ __device__ __forceinline__ bool select_all_at_once(int T, int E)
 {
-    const size_t P = (size_t)T * K;
-    size_t b = 8 * P + 16;  // picked ids, first-occurrence flags (+ alignment)
-    if (select)
-        b += 2 * (size_t)T * ((E + 3) & ~3) * 4 + (size_t)T * 32 * 16;
+    return T * E <= 4096;
+}
+
+__host__ __device__ __forceinline__ size_t route_scratch_bytes(int T, int E, int K, int sel_warps, bool select)
+{
+    size_t b = (8 * (size_t)T * K + 16 + 15) & ~size_t(15);
+    const size_t Ep = (E + 3) & ~3;
+    if (select && select_all_at_once(T, E))
+        b += 2 * (size_t)T * Ep * 4 + (size_t)T * 32 * 16;  // c and s rows, group scores, kept, picks
+    else if (select)
+        b += (size_t)sel_warps * (8 * Ep + 128);
     return b;
 }
 
@@ -112,11 +143,11 @@ __host__ __device__ __forceinline__ size_t x_area_bytes(int d, int tch)
 }
 
 // ring [ns][STAGE_BYTES] | full [ns] | empty [ns] | hfull [NH_MAX] | hempty [NH_MAX] |
-// consumer barrier | table barrier | x barrier | pfull [NE_MAX] | pempty [NE_MAX] | stage
-// tags [ns] (int2) | flags (16 B) | counters | chunk descriptors [NE_MAX] | slot table
-// [max_slots] | pair list [T*K] | weights [T*K] | x staging area | h buffers [nh] (codes
-// [TCH][fmax] | scales [TCH][hgs] | corrections [TCH][hgs]) | partial sums
-// [NBUF][NC][2][TCH][32] (before the first chunk: the routing scratch).
+// consumer barrier | table barrier | x barrier | pfull [NE_MAX] | pempty [NE_MAX] | stage tags [ns]
+// (int2) | flags (16 B) | counters | chunk descriptors [NE_MAX] | slot table [max_slots] |
+// pair list [T*K] | weights [T*K] | x staging area | h buffers [nh] (codes [TCH][fmax] |
+// scales [TCH][hgs] | corrections [TCH][hgs]) | partial sums [NBUF][NC][2][TCH][32]
+// (before the first chunk: the routing scratch).
 __host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, int ns, int nh, int nbuf, int tch)
 {
     RingLayout L;
@@ -142,13 +173,15 @@ __host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, 
     L.ctab = take(sizeof(Counters), 16);
     L.desc = take(sizeof(ChunkDesc) * NE_MAX, 16);
     L.stab = take(sizeof(SlotInfo) * (size_t)a.max_slots, 16);
-    L.ptab = take(4 * (size_t)P, 16);
-    L.wtab = take(4 * (size_t)P, 16);
+    L.ptab = take(round_up(4 * P, 16), 16);
+    L.wtab = take(round_up(4 * P, 16), 16);
     L.act = take(x_area_bytes(a.d, tch), 16);
     L.hb = round_up(tch * a.fmax + 8 * tch * a.hgs, 16);
     L.hbuf = take(L.hb * nh, 16);
     const size_t pbytes = 4 * (size_t)nbuf * NC * 2 * tch * 32;
-    const size_t rbytes = route_scratch_bytes(a.T, a.E, a.K, !a.ids_given);
+    size_t rbytes = route_scratch_bytes(a.T, a.E, a.K, a.sel_warps, !a.ids_given);
+    const size_t lbytes = 4 * (size_t)NC * LT * 32;  // logit chains
+    rbytes = rbytes > lbytes ? rbytes : lbytes;
     L.part = take(pbytes > rbytes ? pbytes : rbytes, 16);  // routing scratch before the first chunk
     L.total = o;
     return L;
@@ -158,7 +191,7 @@ struct RingSmem {
     unsigned char *ring;
     uint64_t *full, *empty, *hfull, *hempty, *cbar, *tbar, *xbar, *pfull, *pempty;
     int2 *tag;
-    int *flags;  // [0] abort, [1] valid pairs, [2] distinct experts
+    int *flags;  // [0] abort, [1] valid pairs, [2] distinct experts, [3] this CTA routes
     Counters *ctab;
     ChunkDesc *desc;
     SlotInfo *stab;
@@ -225,19 +258,41 @@ __device__ __forceinline__ void fence_proxy_async_global()
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Work item idx of the claim order, given n_gu gate/up items. The shared expert's items
-// (slot 0) need nothing written by routing; the routed slots come from the table.
+// Items of the shared expert's gate/up phase.
+__device__ __forceinline__ int shared_gu_items(const DecodeArgs &a)
+{
+    return a.has_shared ? a.shared_ffn / G : 0;
+}
+
+// One past the last gate/up item, as far as item idx needs it: the shared expert's
+// gate/up items need no routing; past them the routing table (s.ctab) must be loaded.
+__device__ __forceinline__ int gu_end(const DecodeArgs &a, const Counters *ctab, int idx)
+{
+    const int pre = a.n_logit + shared_gu_items(a);
+    return idx < pre ? pre : a.n_logit + ctab->n_items_gateup;
+}
+
+// Work item idx of the claim order, given n_gu (gu_end). The logit items and the shared
+// expert's items (slot 0) need nothing written by routing; the routed slots come from the
+// table.
 __device__ __forceinline__ DecItem work_item(const DecodeArgs &a, const SlotInfo *stab, int n_gu, int idx)
 {
-    DecItem it;
-    const int sh_items = a.has_shared ? a.shared_ffn / G : 0;
+    DecItem it{};
+    if (idx < a.n_logit) {
+        it.mode = MODE_LOGIT;
+        it.slot = -1;
+        it.kdim = a.d;
+        return it;
+    }
+    const int sh_items = shared_gu_items(a);
     if (idx < n_gu) {
+        const int r0 = idx - a.n_logit;
         it.mode = MODE_GATEUP;
-        if (idx < sh_items) {
+        if (r0 < sh_items) {
             it.slot = 0;
-            it.rb = idx;
+            it.rb = r0;
         } else {
-            const int r = idx - sh_items, nrb = a.ffn / G;
+            const int r = r0 - sh_items, nrb = a.ffn / G;
             it.slot = (a.has_shared ? 1 : 0) + r / nrb;
             it.rb = r % nrb;
         }
@@ -249,15 +304,13 @@ __device__ __forceinline__ DecItem work_item(const DecodeArgs &a, const SlotInfo
     }
     if (a.has_shared && it.slot == 0) {
         it.is_shared = 1;
-        it.ex = a.shared;
         it.begin = 0;
         it.count = a.T;
     } else {
-        const SlotInfo &si = stab[it.slot];
+        const SlotInfo &sl = stab[it.slot];
         it.is_shared = 0;
-        it.ex = si.ex;
-        it.begin = si.begin;
-        it.count = si.count;
+        it.begin = sl.begin;
+        it.count = sl.count;
     }
     it.kdim = it.mode == MODE_GATEUP ? a.d : (it.is_shared ? a.shared_ffn : a.ffn);
     return it;
@@ -304,6 +357,236 @@ __device__ __forceinline__ void top2_merge(float &m1, float &m2, float o1, float
     }
 }
 
+// The q8 of the tokens rows[0..nrow) of x from the workspace into the staging area, row r
+// at row r: codes in even/odd word order, scales, corrections.
+template <int TCH>
+__device__ void stage_x_rows(const DecodeArgs &a, int8_t *codes, float *sc, int *cr, const int (&rows)[TCH], int nrow,
+                             int tid)
+{
+    const int v16 = a.d / 16, gx = a.d / G;
+    for (int i = tid; i < nrow * v16; i += NT) {
+        const int r = i / v16, o = i - r * v16;
+        int xr = 0;
+#pragma unroll
+        for (int t = 0; t < TCH; ++t)
+            xr = t == r ? rows[t] : xr;
+        reinterpret_cast<uint4 *>(codes + (size_t)r * a.d)[o] =
+            __ldcg(reinterpret_cast<const uint4 *>(a.xq_eo + (long)xr * a.d) + o);
+    }
+    for (int i = tid; i < nrow * gx; i += NT) {
+        const int r = i / gx, g = i - r * gx;
+        int xr = 0;
+#pragma unroll
+        for (int t = 0; t < TCH; ++t)
+            xr = t == r ? rows[t] : xr;
+        sc[i] = __ldcg(a.sx + (long)xr * gx + g);
+        cr[i] = __ldcg(a.xc + (long)xr * gx + g);
+    }
+}
+
+// One K-chunk of logit item idx: consumer warp w owns the item's (expert, token) tasks w,
+// w + NC, ...; lane j continues the fmaf chain of its tasks over k = j, j + 32, ...
+// ascending. The stage holds the chunk of the item's token rows of x ([lg_tb][lg_kc]) and
+// then of its router rows ([ne][lg_kc]). The chains live in the partial-sum area (no
+// chunk uses it before routing): lacc[i * 32 + lane] for task w + NC * i.
+__device__ __forceinline__ void logit_chunk(const unsigned char *stg, const DecodeArgs &a, int idx, int c, float *lacc,
+                                            int warp, int lane)
+{
+    const LogitItem li = logit_item(a, idx);
+    const int kc = a.lg_kc, kcl = min(kc, a.d - c * kc);
+    const float *xs = reinterpret_cast<const float *>(stg);
+    const float *ws = xs + (size_t)a.lg_tb * kc;
+    const int ntask = li.ne * li.ntok;
+    for (int i = 0; i < LT; ++i) {
+        const int task = warp + NC * i;
+        if (task >= ntask)
+            break;
+        const int te = task / li.ntok, tt = task - te * li.ntok;
+        const float *xr = xs + (size_t)tt * kc, *wr = ws + (size_t)te * kc;
+        float acc = c == 0 ? 0.0f : lacc[i * 32 + lane];
+        // sixteen operand pairs at a time into registers, then the sixteen fmaf of the
+        // chain (the chain's order is unchanged; only the loads run ahead)
+        constexpr int PF = 16;
+        int k = lane;
+        for (; k + 32 * (PF - 1) < kcl; k += 32 * PF) {
+            float xv[PF], wv[PF];
+#pragma unroll
+            for (int u = 0; u < PF; ++u) {
+                xv[u] = xr[k + 32 * u];
+                wv[u] = wr[k + 32 * u];
+            }
+#pragma unroll
+            for (int u = 0; u < PF; ++u)
+                acc = fmaf(xv[u], wv[u], acc);
+        }
+        for (; k < kcl; k += 32)
+            acc = fmaf(xr[k], wr[k], acc);
+        lacc[i * 32 + lane] = acc;
+    }
+}
+
+// The end of logit item idx: each task's 32 chains joined by a butterfly (offsets 16, 8,
+// 4, 2, 1: every lane then holds the halving tree's sum); lane i writes task w + NC * i:
+// the logit and, in sigmoid mode, s = fp32(sigmoid(l)) evaluated in fp64 and c = s + bias.
+// Returns the tasks written by this warp.
+__device__ __forceinline__ int logit_finish(const DecodeArgs &a, int idx, const float *lacc, int warp, int lane)
+{
+    const LogitItem li = logit_item(a, idx);
+    const int ntask = li.ne * li.ntok;
+    float mine = 0.0f;
+    int nw = 0;
+    for (int i = 0; i < LT; ++i) {
+        const int task = warp + NC * i;
+        if (task >= ntask)
+            break;
+        float v = lacc[i * 32 + lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            v = v + __shfl_xor_sync(FULL, v, o);
+        mine = lane == i ? v : mine;
+        ++nw;
+    }
+    if (lane < nw) {
+        const int task = warp + NC * lane;
+        const int te = task / li.ntok, tt = task - te * li.ntok;
+        const int e = li.e0 + te;
+        const long o = (long)(li.t0 + tt) * a.E + e;
+        a.logits[o] = mine;
+        if (a.router != COLIBRI_ROUTER_SOFTMAX) {
+            const float sv = (float)(1.0 / (1.0 + exp(-(double)mine)));
+            a.rs[o] = sv;
+            a.rc[o] = sv + (a.bias ? a.bias[e] : 0.0f);
+        }
+    }
+    return nw;
+}
+
+// Expert selection of token t by one warp, from the router scores in the workspace (cs,
+// ss: this warp's scratch of E floats each; pick: 32 ints). Sigmoid mode: lane g takes
+// the two largest biased scores c of group g, their sum is the group score, and the
+// topk_group best groups are kept (ties: lower group index); then every allowed expert
+// counts the allowed experts that beat it by (c, lower index), and the one that exactly
+// k others beat is the k-th pick: the same ids, in the same order, as a sequential
+// selection. w = s / sum(s) * routed_scale with a compensated fp32 sum in selection order.
+// Softmax mode: top_k by logit, w = softmax over all experts in fp64. Writes the ids and
+// weights to sids and wtab (shared memory); the writer CTA also to the caller's ids and w.
+__device__ void select_warp(const DecodeArgs &a, int t, float *cs, float *ss, int *pick, int *sids, float *wtab,
+                            bool writer, int lane)
+{
+    const int E = a.E, K = a.K;
+    const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
+    const int NG = sig ? a.n_group : 1, gs = E / NG;
+    const long base = (long)t * E;
+    __syncwarp();
+    for (int e0 = 0; e0 < E; e0 += 32 * 8) {
+        // eight loads of each row in flight at once
+        float cv[8], sv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + 32 * u + lane;
+            cv[u] = e < E ? __ldcg((sig ? a.rc : a.logits) + base + e) : 0.0f;
+            sv[u] = sig && e < E ? __ldcg(a.rs + base + e) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + 32 * u + lane;
+            if (e < E) {
+                cs[e] = cv[u];
+                ss[e] = sv[u];
+            }
+        }
+    }
+    __syncwarp();
+    unsigned kept = 1u;
+    if (sig) {
+        float gsc = -INFINITY;  // lane g: the score of group g
+        if (lane < NG) {
+            float m1 = -INFINITY, m2 = -INFINITY;
+            for (int j = lane * gs; j < (lane + 1) * gs; ++j)
+                top2_merge(m1, m2, cs[j], -INFINITY);
+            gsc = gs == 1 ? m1 : m1 + m2;
+        }
+        int rank = 0;
+        for (int h = 0; h < NG; ++h)
+            rank += beats(__shfl_sync(FULL, gsc, h), h, gsc, lane);
+        kept = __ballot_sync(FULL, lane < NG && rank < a.topk_group);
+    }
+    const bool vec = (gs & 3) == 0;
+    for (int e = lane; e < E; e += 32) {
+        if (!((kept >> (e / gs)) & 1u))
+            continue;
+        const float v = cs[e];
+        int r = 0;
+        for (int g = 0; g < NG; ++g) {
+            if (!((kept >> g) & 1u))
+                continue;
+            if (vec) {
+                const float4 *q4 = reinterpret_cast<const float4 *>(cs + g * gs);
+                int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+                for (int j = 0; j < gs / 4; ++j) {
+                    const float4 x = q4[j];
+                    const int f = g * gs + 4 * j;
+                    r0 += beats(x.x, f, v, e);
+                    r1 += beats(x.y, f + 1, v, e);
+                    r2 += beats(x.z, f + 2, v, e);
+                    r3 += beats(x.w, f + 3, v, e);
+                }
+                r += r0 + r1 + r2 + r3;
+            } else {
+                for (int f = g * gs; f < (g + 1) * gs; ++f)
+                    r += beats(cs[f], f, v, e);
+            }
+        }
+        if (r < K)
+            pick[r] = e;
+    }
+    __syncwarp();
+    const bool have = lane < K;
+    const int my_id = have ? pick[lane] : 0;
+    float wt = 0.0f;
+    if (sig) {
+        // compensated (TwoSum) sum of the k scores in selection order, one division
+        const float sv = have ? ss[my_id] : 0.0f;
+        float hi = 0.0f, lo = 0.0f;
+        for (int i = 0; i < K; ++i) {
+            const float x = __shfl_sync(FULL, sv, i);
+            const float u = hi + x, bb = u - hi;
+            lo += (hi - (u - bb)) + (x - bb);
+            hi = u;
+        }
+        const float sum = hi + lo;
+        wt = (a.norm_topk ? __fdiv_rn(sv, sum) : sv) * a.routed_scale;
+    } else {
+        double m = -INFINITY;
+        for (int i = lane; i < E; i += 32)
+            m = fmax(m, (double)cs[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            m = fmax(m, __shfl_xor_sync(FULL, m, o));
+        double z = 0.0;
+        for (int i = lane; i < E; i += 32)
+            z += exp((double)cs[i] - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            z += __shfl_xor_sync(FULL, z, o);
+        double p = have ? exp((double)cs[my_id] - m) / z : 0.0;
+        double sum = 0.0;
+        for (int i = 0; i < K; ++i)
+            sum += __shfl_sync(FULL, p, i);
+        if (a.norm_topk)
+            p = p / sum;
+        wt = (float)(p * (double)a.routed_scale);
+    }
+    if (have) {
+        sids[t * K + lane] = my_id;
+        wtab[t * K + lane] = wt;
+        if (writer) {
+            a.ids[(long)t * K + lane] = my_id;
+            a.w_out[(long)t * K + lane] = wt;
+        }
+    }
+}
+
 // Expert selection for the T tokens by the consumer warps, in shared memory (every CTA
 // the same way). The k-th pick of the sequential selection (repeatedly take the best
 // remaining candidate) is the candidate that exactly k others beat, so each candidate
@@ -312,9 +595,10 @@ __device__ __forceinline__ void top2_merge(float &m1, float &m2, float o1, float
 // group's two largest biased scores c, top topk_group groups, top_k by c inside them,
 // w = s / sum(s) * routed_scale with a compensated fp32 sum in selection order. Softmax
 // mode: top_k by logit, w = softmax over all experts in fp64. Writes the ids and weights
-// to sids and s.wtab; CTA 0 also to the caller's ids and w.
-__device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, int *sids, uint32_t &cph, int tid,
-                           int warp, int lane)
+// to sids and s.wtab; the writer CTA also to the caller's ids and w. Used when the scores of
+// all T tokens fit the scratch (T * E <= 4096); select_warp otherwise.
+__device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, int *sids, bool writer, uint32_t &cph,
+                           int tid, int warp, int lane)
 {
     const int E = a.E, K = a.K, T = a.T;
     const bool sig = a.router != COLIBRI_ROUTER_SOFTMAX;
@@ -332,8 +616,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
         if (sig)
             ss[t * Ep + e] = __ldcg(a.rs + i);
     }
-    if (!consumers_sync(s, cph, lane))
-        return false;
+    named_sync(1, NT);
     if (sig) {
         for (int i = warp; i < T * NG; i += NC) {
             const int t = i / NG, g = i - t * NG;
@@ -349,8 +632,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             if (lane == 0)
                 gsc[t * 32 + g] = gs == 1 ? m1 : m1 + m2;
         }
-        if (!consumers_sync(s, cph, lane))
-            return false;
+        named_sync(1, NT);
         for (int i = tid; i < T * NG; i += NT) {
             const int t = i / NG, g = i - t * NG;
             const float v = gsc[t * 32 + g];
@@ -359,8 +641,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
                 rank += beats(gsc[t * 32 + h], h, v, g);
             kept[t * 32 + g] = rank < a.topk_group;
         }
-        if (!consumers_sync(s, cph, lane))
-            return false;
+        named_sync(1, NT);
     }
     // rank of each allowed candidate, two adjacent threads a candidate (each counts over
     // every other allowed group), added with one shuffle
@@ -401,8 +682,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             ps[t * 32 + rank] = sig ? ss[t * Ep + e] : cs[t * Ep + e];
         }
     }
-    if (!consumers_sync(s, cph, lane))
-        return false;
+    named_sync(1, NT);
     for (int t = warp; t < T; t += NC) {
         double m = 0.0, z = 1.0;
         if (!sig) {
@@ -448,19 +728,54 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             const int id = pick[t * 32 + lane];
             sids[t * K + lane] = id;
             s.wtab[t * K + lane] = wt;
-            if (blockIdx.x == 0) {
+            if (writer) {
                 a.ids[(long)t * K + lane] = id;
                 a.w_out[(long)t * K + lane] = wt;
             }
         }
     }
-    // one token: warp 0 wrote every pick and goes on to bucket them itself
-    return (T == 1 && T * K <= 32) || consumers_sync(s, cph, lane);
+    return true;
 }
 
-// Slot table, counters and (CTA 0) the workspace copies from the pair ids, for at most 32
-// pairs, by one warp: lane p holds pair p. Same results as the general bucketing below.
-__device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *sids, int lane)
+// The shared expert's slot (0) and the counters, from the valid pairs and the distinct
+// routed experts, into shared memory (and the workspace, by the writer CTA).
+__device__ __forceinline__ void write_counters(const DecodeArgs &a, const RingSmem &s, bool writer, int n_valid,
+                                               int n_routed)
+{
+    const int sbase = a.has_shared ? 1 : 0;
+    if (a.has_shared) {
+        SlotInfo si;
+        si.ex = a.shared;
+        si.begin = 0;
+        si.count = a.T;
+        si.pad[0] = si.pad[1] = 0;
+        s.stab[0] = si;
+        if (writer) {
+            Slot sl;
+            sl.expert = -1;
+            sl.begin = 0;
+            sl.count = a.T;
+            sl.pad = 0;
+            a.slots[0] = sl;
+        }
+    }
+    Counters ct;
+    ct.n_slots = sbase + n_routed;
+    ct.n_routed = n_routed;
+    ct.n_items_gateup = shared_gu_items(a) + n_routed * (a.ffn / G);
+    ct.n_items_down = ct.n_slots * ((a.d / G + 1) / 2);
+    ct.n_rows = n_valid + (a.has_shared ? a.T : 0);
+    ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
+    *s.ctab = ct;
+    if (writer)
+        *a.counters = ct;
+}
+
+// Bucketing of at most 32 pairs by one warp (lane p holds pair p): pair list stable by
+// expert, slots = the shared expert then the distinct valid experts in ascending id,
+// counters, into shared memory; the writer CTA also writes them, with the bucket
+// offsets, to the workspace and flags bad ids (outside [0, E), or twice in a token).
+__device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *sids, bool writer, int lane)
 {
     const int T = a.T, K = a.K, E = a.E, P = T * K;
     const int sbase = a.has_shared ? 1 : 0;
@@ -475,7 +790,7 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
     const unsigned in_tok = below & ~((1u << tok0) - 1u);
     const bool dup = live && (same & in_tok) != 0;
     const bool fst = valid && (same & below) == 0;
-    if (blockIdx.x == 0 && live && (!valid || dup))
+    if (writer && live && (!valid || dup))
         atomicOr(a.err, ERR_BAD_ID);
     const unsigned fmask = __ballot_sync(FULL, fst);
     const int n_valid = __popc(__ballot_sync(FULL, valid)), n_routed = __popc(fmask);
@@ -489,7 +804,7 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
     if (valid) {
         const int pos = __popc(same & below);
         s.ptab[less + pos] = lane;
-        if (blockIdx.x == 0)
+        if (writer)
             a.pairs[less + pos] = lane;
         if (fst) {
             SlotInfo si;
@@ -498,7 +813,7 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
             si.count = __popc(same);
             si.pad[0] = si.pad[1] = 0;
             s.stab[sbase + dless] = si;
-            if (blockIdx.x == 0) {
+            if (writer) {
                 Slot sl;
                 sl.expert = e;
                 sl.begin = less;
@@ -508,7 +823,7 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
             }
         }
     }
-    if (blockIdx.x == 0) {
+    if (writer) {
         for (int x = lane; x <= E; x += 32) {
             int c = 0;
             for (int q = 0; q < P; ++q)
@@ -516,65 +831,16 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
             a.offsets[x] = c;
         }
     }
-    if (lane == 0) {
-        if (a.has_shared) {
-            SlotInfo si;
-            si.ex = a.shared;
-            si.begin = 0;
-            si.count = T;
-            si.pad[0] = si.pad[1] = 0;
-            s.stab[0] = si;
-        }
-        Counters ct;
-        ct.n_slots = sbase + n_routed;
-        ct.n_routed = n_routed;
-        ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
-        ct.n_items_down = ct.n_slots * ((a.d / G + 1) / 2);
-        ct.n_rows = n_valid + (a.has_shared ? T : 0);
-        ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
-        *s.ctab = ct;
-        if (blockIdx.x == 0) {
-            if (a.has_shared) {
-                Slot sl;
-                sl.expert = -1;
-                sl.begin = 0;
-                sl.count = T;
-                sl.pad = 0;
-                a.slots[0] = sl;
-            }
-            *a.counters = ct;
-        }
-    }
+    if (lane == 0)
+        write_counters(a, s, writer, n_valid, n_routed);
 }
 
-// Routing of this CTA: ids and weights (selected, or given), then bucketing in shared
-// memory: pair list stable by expert, slots = the shared expert then the distinct valid
-// experts in ascending id, counters. CTA 0 also writes the pair offsets, pair list, slots
-// and counters to the workspace and flags bad ids (outside [0, E), or twice in a token).
-__device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph, int tid, int warp, int lane)
+// The same for more than 32 pairs, by all consumer threads (O(P^2) comparisons, P <=
+// 1024), with first-occurrence flags in shared memory.
+__device__ bool bucket_cta(const DecodeArgs &a, const RingSmem &s, const int *sids, int *first, bool writer,
+                           uint32_t &cph, int tid, int lane)
 {
     const int T = a.T, K = a.K, E = a.E, P = T * K;
-    int *sids = reinterpret_cast<int *>(s.part);
-    int *first = sids + P;
-    float *scr = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(s.part) +
-                                           ((8 * (size_t)P + 15) & ~size_t(15)));
-    if (tid == 0)
-        s.flags[1] = s.flags[2] = 0;
-    if (a.ids_given) {
-        for (int i = tid; i < P; i += NT) {
-            sids[i] = __ldcg(a.ids + i);
-            s.wtab[i] = __ldcg(a.w_in + i);
-        }
-        if (P > 32 && !consumers_sync(s, cph, lane))
-            return false;
-    } else if (!select_cta(a, s, scr, sids, cph, tid, warp, lane)) {
-        return false;
-    }
-    if (P <= 32) {
-        if (warp == 0)
-            bucket_warp(a, s, sids, lane);
-        return consumers_sync(s, cph, lane);
-    }
     for (int p = tid; p < P; p += NT) {
         const int e = sids[p];
         const bool valid = e >= 0 && e < E;
@@ -584,7 +850,7 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
             dup |= same && q >= p - p % K;
             fst &= !same;
         }
-        if (blockIdx.x == 0 && (!valid || dup))
+        if (writer && (!valid || dup))
             atomicOr(a.err, ERR_BAD_ID);
         first[p] = fst;
         if (valid)
@@ -592,8 +858,7 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
         if (fst)
             atomicAdd(&s.flags[2], 1);
     }
-    if (!consumers_sync(s, cph, lane))
-        return false;
+    named_sync(1, NT);
     const int sbase = a.has_shared ? 1 : 0;
     for (int p = tid; p < P; p += NT) {
         const int e = sids[p];
@@ -609,7 +874,7 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
             dless += first[q] && eq < e;
         }
         s.ptab[less + pos] = p;
-        if (blockIdx.x == 0)
+        if (writer)
             a.pairs[less + pos] = p;
         if (first[p]) {
             SlotInfo si;
@@ -618,7 +883,7 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
             si.count = cnt;
             si.pad[0] = si.pad[1] = 0;
             s.stab[sbase + dless] = si;
-            if (blockIdx.x == 0) {
+            if (writer) {
                 Slot sl;
                 sl.expert = e;
                 sl.begin = less;
@@ -628,7 +893,7 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
             }
         }
     }
-    if (blockIdx.x == 0) {
+    if (writer) {
         for (int e = tid; e <= E; e += NT) {
             int less = 0;
             for (int q = 0; q < P; ++q)
@@ -636,37 +901,97 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
             a.offsets[e] = less;
         }
     }
+    if (tid == 0)
+        write_counters(a, s, writer, s.flags[1], s.flags[2]);
+    return true;
+}
+
+// Routing of this CTA, at its routing stage: once every logit task of the layer is in
+// (a device counter), every token's selection (or the given ids and weights), then
+// bucketing, into shared memory; CTA 0 also writes the results to the workspace and the
+// caller's ids and w. Then the producer may read the table (tbar). The consumer warps
+// meet on hardware barrier 1 here: every one of them runs this code to its end (the only
+// wait, for the counter, is bounded and taken by one thread before the first barrier).
+__device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph, int tid, int warp, int lane)
+{
+    const int T = a.T, K = a.K, P = T * K;
+    const bool writer = blockIdx.x == 0;
+    // all T tokens' x codes staged at once, by bulk copies when the parts are whole 16-byte
+    // runs
+    const bool x_all = T <= a.tch, x_bulk = x_all && ((long)T * a.d) % 128 == 0;
+    int *sids = reinterpret_cast<int *>(s.part);
+    int *first = sids + P;
+    unsigned char *scr0 = reinterpret_cast<unsigned char *>(s.part) + ((8 * (size_t)P + 16 + 15) & ~size_t(15));
+    const int Ep = (a.E + 3) & ~3;
     if (tid == 0) {
-        if (a.has_shared) {
-            SlotInfo si;
-            si.ex = a.shared;
-            si.begin = 0;
-            si.count = T;
-            si.pad[0] = si.pad[1] = 0;
-            s.stab[0] = si;
+        s.flags[1] = s.flags[2] = 0;
+        int ok = 1;
+        // every logit task and every q8 group of x of the layer
+        ok = wait_count_geq(a.route_done, (a.ids_given ? 0 : a.E * a.T) + a.T * (a.d / G));
+        __threadfence();
+        if (ok && x_bulk) {
+            // the q8 of all T tokens into the x staging area (codes in even/odd order,
+            // scales, corrections)
+            fence_proxy_async_global();
+            const uint32_t nc = (uint32_t)(a.T * a.d), ns = (uint32_t)(4 * a.T * (a.d / G));
+            unsigned char *act = reinterpret_cast<unsigned char *>(s.act);
+            mbar_arrive_expect_tx(s.xbar, nc + 2 * ns);
+            bulk_g2s(act, a.xq_eo, nc, s.xbar);
+            bulk_g2s(act + x_sc_off(a.d, a.tch), a.sx, ns, s.xbar);
+            bulk_g2s(act + x_cr_off(a.d, a.tch), a.xc, ns, s.xbar);
         }
-        const int n_routed = s.flags[2];
-        Counters ct;
-        ct.n_slots = sbase + n_routed;
-        ct.n_routed = n_routed;
-        ct.n_items_gateup = (a.has_shared ? a.shared_ffn / G : 0) + n_routed * (a.ffn / G);
-        ct.n_items_down = ct.n_slots * ((a.d / G + 1) / 2);
-        ct.n_rows = s.flags[1] + (a.has_shared ? T : 0);
-        ct.pad[0] = ct.pad[1] = ct.pad[2] = 0;
-        *s.ctab = ct;
-        if (blockIdx.x == 0) {
-            if (a.has_shared) {
-                Slot sl;
-                sl.expert = -1;
-                sl.begin = 0;
-                sl.count = T;
-                sl.pad = 0;
-                a.slots[0] = sl;
-            }
-            *a.counters = ct;
-        }
+        s.flags[3] = ok;
     }
-    return consumers_sync(s, cph, lane);
+    named_sync(1, NT);
+    if (!s.flags[3]) {
+        if (lane == 0)
+            set_abort(a, s);
+        return false;
+    }
+    if (a.ids_given) {
+        for (int i = tid; i < P; i += NT) {
+            sids[i] = __ldcg(a.ids + i);
+            s.wtab[i] = __ldcg(a.w_in + i);
+        }
+    } else if (select_all_at_once(T, a.E)) {
+        if (!select_cta(a, s, reinterpret_cast<float *>(scr0), sids, writer, cph, tid, warp, lane))
+            return false;
+    } else if (warp < a.sel_warps) {
+        float *cs = reinterpret_cast<float *>(scr0 + (size_t)warp * (8 * Ep + 128));
+        int *pick = reinterpret_cast<int *>(cs + 2 * Ep);
+        for (int t = warp; t < T; t += a.sel_warps)
+            select_warp(a, t, cs, cs + Ep, pick, sids, s.wtab, writer, lane);
+    }
+    named_sync(1, NT);
+    if (P <= 32) {
+        if (warp == 0)
+            bucket_warp(a, s, sids, writer, lane);
+    } else if (!bucket_cta(a, s, sids, first, writer, cph, tid, lane)) {
+        return false;
+    }
+    named_sync(1, NT);
+    if (tid == 0)
+        mbar_arrive(s.tbar);  // the producer may read the table
+    // the staged q8 of x before the first gate/up stage
+    if (x_bulk && !mbar_wait(s.xbar, 0)) {
+        if (lane == 0)
+            set_abort(a, s);
+        return false;
+    }
+    if (x_all && !x_bulk) {
+        const int v16 = a.d / 16, gx = a.d / G;
+        int8_t *codes = reinterpret_cast<int8_t *>(s.act);
+        float *sc = reinterpret_cast<float *>(s.act + x_sc_off(a.d, a.tch));
+        int *cr = reinterpret_cast<int *>(s.act + x_cr_off(a.d, a.tch));
+        for (int i = tid; i < T * v16; i += NT)
+            reinterpret_cast<uint4 *>(codes)[i] = __ldcg(reinterpret_cast<const uint4 *>(a.xq_eo) + i);
+        for (int i = tid; i < T * gx; i += NT) {
+            sc[i] = __ldcg(a.sx + i);
+            cr[i] = __ldcg(a.xc + i);
+        }
+        named_sync(1, NT);
+    }
+    return true;
 }
 
 // Partial dots of one stage: consumer warp w takes groups w, w + NC, ... of the stage.
@@ -716,52 +1041,111 @@ template <int TCH>
 __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
 {
     const int NS = a.ring, NH = a.nh;
-    const int sh_items = a.has_shared ? a.shared_ffn / G : 0;
+    const int P = a.T * a.K;
     if (a.has_shared)
         prefetch_shared(a);
     if (blockIdx.x == 0)
         prefetch_l2(a.experts, (uint32_t)(((size_t)a.E * sizeof(colibri_expert) + 15) & ~size_t(15)));
+    grid_dep_wait();  // inputs and the zeroed counters are in
     const uint64_t pol = policy_evict_first();
-    int n_gu = sh_items + 1, total = 0x7fffffff;  // until the table is in
-    bool have_table = false;
+    const int pre = a.n_logit + shared_gu_items(a);  // items that need no routing table
+    int n_gu = pre, total = 0x7fffffff;              // until the table is in
+    bool have_table = false, route_posted = false;
     uint32_t st = 0, hsw = 0;  // stages posted, h buffers filled
     int hslot = -1, hch = -1;  // rows in the newest h buffer
     uint64_t h_ready = 0;      // slots (below 64) whose rows of h are all published
-    // the ring slot of stage st, once the consumers have released it
+    // the ring slot of stage st, once the consumers have released it; the slot and the
+    // lap parity are kept incrementally (no division on this path)
+    uint32_t pslot = 0, plap = 0;
     auto acquire = [&](uint32_t &slot) -> bool {
-        slot = st % NS;
-        if (st >= (uint32_t)NS && !mbar_wait(&s.empty[slot], ((st / NS) - 1) & 1)) {
+        slot = pslot;
+        if (st >= (uint32_t)NS && !mbar_wait(&s.empty[slot], plap ^ 1u)) {
             set_abort(a, s);
             return false;
         }
+        if (++pslot == (uint32_t)NS) {
+            pslot = 0;
+            plap ^= 1u;
+        }
         return !aborted(s);
     };
-    // claims run two items ahead of the item being streamed
-    int idx = atomicAdd(a.claim, 1), ahead = atomicAdd(a.claim, 1);
+    // claims run two items ahead of the item being streamed, except behind a logit item:
+    // the next claim waits until the logit item's bytes have landed, so that the logit
+    // items (claimed first) spread over all CTAs instead of pairing up
+    int idx = atomicAdd(a.claim, 1), ahead = idx < a.n_logit ? -1 : atomicAdd(a.claim, 1);
     for (bool run = true; run;) {
-        if (!have_table && idx >= sh_items) {
-            // past the shared expert: wait for the consumers' routing (slot table)
+        if (!route_posted && idx >= a.n_logit) {
+            // past this CTA's logit items: the consumers route next (an empty stage)
+            uint32_t slot;
+            if (!acquire(slot))
+                break;
+            s.tag[slot] = make_int2(TAG_ROUTE, 0);
+            mbar_arrive(&s.full[slot]);
+            ++st;
+            route_posted = true;
+        }
+        if (!have_table && idx >= pre) {
+            // the consumers' routing table (slots, pairs, counters) in shared memory
             if (!mbar_wait(s.tbar, 0)) {
                 set_abort(a, s);
                 break;
             }
             have_table = true;
-            n_gu = s.ctab->n_items_gateup;
+            n_gu = a.n_logit + s.ctab->n_items_gateup;
             total = n_gu + s.ctab->n_items_down;
         }
         if (idx >= total) {
             uint32_t slot;
             if (acquire(slot)) {
-                s.tag[slot] = make_int2(-1, 0);  // end of work
+                s.tag[slot] = make_int2(TAG_END, 0);  // end of work
                 mbar_arrive(&s.full[slot]);
                 ++st;
             }
             break;
         }
-        const int next = ahead;
-        ahead = atomicAdd(a.claim, 1);  // used two items from now
+        int next = ahead;
+        if (next >= 0)
+            ahead = atomicAdd(a.claim, 1);  // used two items from now
         const DecItem it = work_item(a, s.stab, n_gu, idx);
+        if (it.mode == MODE_LOGIT) {
+            // chunk c: the item's token rows of x and its router rows over columns
+            // [c * kc, c * kc + kcl)
+            for (int c = 0; c < a.lg_nck; ++c) {
+                uint32_t slot;
+                if (!acquire(slot)) {
+                    run = false;
+                    break;
+                }
+                s.tag[slot] = make_int2(idx, c);
+                {
+                    const LogitItem li = logit_item(a, idx);
+                    const int kc = a.lg_kc, k0 = c * kc, kcl = min(kc, a.d - k0);
+                    const uint32_t rb = 4u * (uint32_t)kcl;
+                    unsigned char *dst = s.ring + (size_t)slot * STAGE_BYTES;
+                    mbar_arrive_expect_tx(&s.full[slot], (uint32_t)(li.ntok + li.ne) * rb);
+                    for (int t = 0; t < li.ntok; ++t)
+                        bulk_g2s(dst + (size_t)t * kc * 4, a.x + (long)(li.t0 + t) * a.d + k0, rb, &s.full[slot]);
+                    for (int i = 0; i < li.ne; ++i)
+                        bulk_g2s_hint(dst + (size_t)(a.lg_tb + i) * kc * 4, a.Wr + (long)(li.e0 + i) * a.d + k0, rb,
+                                      &s.full[slot], pol);
+                }
+                ++st;
+            }
+            if (run && next < 0) {
+                // the item's last stage has landed: claim the next item (and one ahead of
+                // it unless it is a logit item too)
+                if (!mbar_wait(&s.full[(st - 1) % NS], ((st - 1) / NS) & 1)) {
+                    set_abort(a, s);
+                    break;
+                }
+                next = atomicAdd(a.claim, 1);
+                ahead = next < a.n_logit ? -1 : atomicAdd(a.claim, 1);
+            }
+            idx = next;
+            continue;
+        }
         const bool gu = it.mode == MODE_GATEUP;
+        const colibri_expert ex = it.is_shared ? a.shared : s.stab[it.slot].ex;
         const int ng = it.kdim / G, spi = (ng + SG - 1) / SG;
         const int nq = spi * ((it.count + TCH - 1) / TCH);
         // the two row blocks: W1 and W3 at rb (gate/up), or W2 at rb and rb + 1 (down; the
@@ -770,19 +1154,18 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
         const float *sa_, *sb_;
         bool two = true;
         if (gu) {
-            wa = it.ex.w1 + (size_t)it.rb * ng * 512;
-            wb = it.ex.w3 + (size_t)it.rb * ng * 512;
-            sa_ = it.ex.s1 + (size_t)it.rb * ng * 32;
-            sb_ = it.ex.s3 + (size_t)it.rb * ng * 32;
+            wa = ex.w1 + (size_t)it.rb * ng * 512;
+            wb = ex.w3 + (size_t)it.rb * ng * 512;
+            sa_ = ex.s1 + (size_t)it.rb * ng * 32;
+            sb_ = ex.s3 + (size_t)it.rb * ng * 32;
         } else {
             two = it.rb + 1 < a.d / G;
-            wa = it.ex.w2 + (size_t)it.rb * ng * 512;
+            wa = ex.w2 + (size_t)it.rb * ng * 512;
             wb = wa + (size_t)ng * 512;
-            sa_ = it.ex.s2 + (size_t)it.rb * ng * 32;
+            sa_ = ex.s2 + (size_t)it.rb * ng * 32;
             sb_ = sa_ + (size_t)ng * 32;
         }
-        for (int q = 0; q < nq && run; ++q) {
-            const int ch = q / spi, k = q % spi;
+        for (int q = 0, ch = 0, k = 0; q < nq && run; ++q) {
             int flag = 0;
             if (!gu && k == 0 && (it.slot != hslot || ch != hch)) {
                 // the chunk's rows of q8(h) into the next h buffer, once all rows of h of
@@ -828,7 +1211,7 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
             }
             const int g0 = k * SG, n = min(SG, ng - g0);
             unsigned char *dst = s.ring + (size_t)slot * STAGE_BYTES;
-            s.tag[slot] = make_int2(idx, q | flag);
+            s.tag[slot] = make_int2(idx, k | (ch << 8) | flag);
             mbar_arrive_expect_tx(&s.full[slot], (uint32_t)((two ? 2 : 1) * n * 640));
             bulk_g2s_hint(dst, wa + (size_t)g0 * 512, n * 512, &s.full[slot], pol);
             bulk_g2s_hint(dst + 2 * SG * 512, sa_ + (size_t)g0 * 32, n * 128, &s.full[slot], pol);
@@ -837,6 +1220,10 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
                 bulk_g2s_hint(dst + 2 * SG * 512 + SG * 128, sb_ + (size_t)g0 * 32, n * 128, &s.full[slot], pol);
             }
             ++st;
+            if (++k == spi) {
+                k = 0;
+                ++ch;
+            }
         }
         idx = next;
     }
@@ -851,6 +1238,40 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
 }
 
 // ---------------- epilogue warp e: the chunks that used partial-sum buffer e ----------------
+// The epilogue warps' first job, while the consumers stream the logit items: this CTA's
+// share of the q8 of x (one warp per 32-group, lane k holding element k, groups
+// blockIdx.x * NE_MAX + e, ...), written to the workspace as plain codes and scales and as
+// the codes in even/odd word order with their corrections 8 * sum(codes); each group is
+// counted with the logit tasks on the routing counter.
+__device__ void quantise_x(const DecodeArgs &a, int e, int lane)
+{
+    const int gx = a.d / G;
+    const long n = (long)a.T * gx;
+    int done = 0;
+    for (long gw = (long)blockIdx.x * NE_MAX + e; gw < n; gw += (long)gridDim.x * NE_MAX) {
+        const long t = gw / gx, g = gw - t * gx;
+        const long base = t * a.d + g * G;
+        const float x = __ldg(a.x + base + lane);
+        const float amax = warp_max(fabsf(x));
+        const float dd = __fdiv_rn(amax, 127.0f);
+        const int q = q8_code_r(x, dd, __frcp_rn(dd));
+        a.qx[base + lane] = (int8_t)q;
+        a.xq_eo[base + eo_pos(lane)] = (int8_t)q;
+        const int sq = warp_sum_i(q);
+        if (lane == 0) {
+            a.sx[gw] = dd;
+            a.xc[gw] = 8 * sq;
+        }
+        ++done;
+    }
+    if (done) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+            atomicAdd(a.route_done, done);
+    }
+}
+
 template <int TCH>
 __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int lane)
 {
@@ -878,7 +1299,7 @@ __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int 
                 const float h = gt / (1.0f + expf(-gt)) * up;
                 const float amax = warp_max(fabsf(h));
                 const float dd = __fdiv_rn(amax, 127.0f);
-                const int q = q8_code(h, dd);
+                const int q = q8_code_r(h, dd, __frcp_rn(dd));
                 const long hb = r * a.fmax + (long)rb * G;
                 a.hq[hb + lane] = (int8_t)q;
                 a.hq_eo[hb + eo_pos(lane)] = (int8_t)q;
@@ -938,33 +1359,19 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
     const int NS = a.ring, NH = a.nh;
     const int tid = threadIdx.x;
     uint32_t cph = 0;  // consumer barrier phase
-    grid_dep_wait();   // router scores and q8 of x (or the given ids) are in
-    // x codes of all T tokens, when one chunk holds them, come in with bulk copies while
-    // the CTA routes
-    const bool x_all = a.T <= TCH;
-    const bool x_bulk = x_all && ((long)a.T * a.d) % 128 == 0;
+    grid_dep_wait();   // the activations are in
     int8_t *xcodes = reinterpret_cast<int8_t *>(s.act);
     float *xsc = reinterpret_cast<float *>(s.act + x_sc_off(a.d, TCH));
     int *xcr = reinterpret_cast<int *>(s.act + x_cr_off(a.d, TCH));
-    if (x_bulk && tid == 0) {
-        fence_proxy_async_global();
-        const uint32_t nc = (uint32_t)(a.T * a.d), ns = (uint32_t)(4 * a.T * (a.d / G));
-        mbar_arrive_expect_tx(s.xbar, nc + 2 * ns);
-        bulk_g2s(xcodes, a.xq_eo, nc, s.xbar);
-        bulk_g2s(xsc, a.xs, ns, s.xbar);
-        bulk_g2s(xcr, a.xc, ns, s.xbar);
-    }
-    if (!route_cta(a, s, cph, tid, warp, lane))
-        return;
-    if (tid == 0)
-        mbar_arrive(s.tbar);  // the producer may read the table now
-    const int n_gu = s.ctab->n_items_gateup;
-    // the x staging area: all T tokens at once when they fit a chunk, else the chunk's
-    bool x_staged = false;
+    // q8 of x: all T tokens in the staging area when one chunk holds them, quantised by the
+    // epilogue warps at the start (xbar; waited for at the routing stage), else each
+    // chunk's tokens when it starts
+    const bool x_all = a.T <= TCH;
     int xrows[TCH];  // token of each staged x row
 #pragma unroll
     for (int t = 0; t < TCH; ++t)
-        xrows[t] = -1;
+        xrows[t] = x_all && t < a.T ? t : -1;
+    bool x_staged = x_all;
     uint32_t chunk = 0;  // chunks handed to the epilogue (buffer chunk % NBUF)
     uint32_t hsw = 0;    // h buffers entered
     int cur_h = 0;
@@ -973,27 +1380,45 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
     int rows[TCH];
     int orow = -1;  // lane t < nt: pair row of the chunk's t-th token
     float acc[2][TCH];
+    float *lacc = s.part + (size_t)warp * LT * 32;  // this warp's logit chains
     // a buffer's previous chunk must have been read before it is written again
+    const int nb_shift = NBUF == 4 ? 2 : 1;  // NBUF is 2 or 4
     auto buffer_free = [&](int b) -> bool {
-        if (chunk >= (uint32_t)NBUF && !mbar_wait(&s.pempty[b], ((chunk / NBUF) - 1) & 1)) {
+        if (chunk >= (uint32_t)NBUF && !mbar_wait(&s.pempty[b], ((chunk >> nb_shift) - 1) & 1)) {
             if (lane == 0)
                 set_abort(a, s);
             return false;
         }
         return true;
     };
-    for (uint32_t st = 0;; ++st) {
-        const int slot = st % NS;
-        if (!mbar_wait(&s.full[slot], (st / NS) & 1)) {
+    // the ring position of the next stage, kept incrementally (no division on this path)
+    int nslot = 0;
+    uint32_t nphase = 0;
+    for (;;) {
+        const int slot = nslot;
+        const uint32_t phase = nphase;
+        if (++nslot == NS) {
+            nslot = 0;
+            nphase ^= 1u;
+        }
+        if (!mbar_wait(&s.full[slot], phase)) {
             if (lane == 0)
                 set_abort(a, s);
             return;
         }
         const int2 tag = s.tag[slot];
+        if (tag.x == TAG_ROUTE) {
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s.empty[slot]);
+            if (!route_cta(a, s, cph, tid, warp, lane))
+                return;
+            continue;
+        }
         if (tag.x < 0) {
             // end of work: one end descriptor into every buffer, in buffer order
             for (int j = 0; j < NBUF; ++j, ++chunk) {
-                const int b = chunk % NBUF;
+                const int b = chunk & (NBUF - 1);
                 if (!buffer_free(b))
                     return;
                 if (tid == 0)
@@ -1006,12 +1431,29 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
         }
         if (tag.x != cur) {
             cur = tag.x;
-            it = work_item(a, s.stab, n_gu, cur);
+            it = work_item(a, s.stab, gu_end(a, s.ctab, cur), cur);
             ng = it.kdim / G;
             spi = (ng + SG - 1) / SG;
         }
-        const int q = tag.y & (TAG_NEW_H - 1);
-        const int ch = q / spi, k = q % spi;
+        const unsigned char *stg = s.ring + (size_t)slot * STAGE_BYTES;
+        if (it.mode == MODE_LOGIT) {
+            const int c = tag.y;
+            logit_chunk(stg, a, cur, c, lacc, warp, lane);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s.empty[slot]);
+            if (c != a.lg_nck - 1)
+                continue;
+            // end of the item: write its scores and count its tasks (the routing stages of
+            // all CTAs wait for every task of the layer)
+            const int nw = logit_finish(a, cur, lacc, warp, lane);
+            __threadfence();
+            __syncwarp();
+            if (lane == 0 && nw > 0)
+                atomicAdd(a.route_done, nw);
+            continue;
+        }
+        const int k = tag.y & 255, ch = (tag.y >> 8) & 255;  // stage in the chunk, chunk
         const int c0 = ch * TCH, nt = min(TCH, it.count - c0);
         if (k == 0) {
             orow = lane < nt ? item_row(a, s, it, c0 + lane) : -1;
@@ -1022,17 +1464,6 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
                     const int p = __shfl_sync(FULL, orow, t);
                     tok[t] = t < nt ? (it.is_shared ? c0 + t : p / a.K) : -1;
                 }
-                if (x_bulk && !x_staged) {
-                    if (!mbar_wait(s.xbar, 0)) {
-                        if (lane == 0)
-                            set_abort(a, s);
-                        return;
-                    }
-                    x_staged = true;
-#pragma unroll
-                    for (int t = 0; t < TCH; ++t)
-                        xrows[t] = t < a.T ? t : -1;
-                }
                 bool same = x_staged;
                 if (!x_all) {
 #pragma unroll
@@ -1040,32 +1471,13 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
                         same &= xrows[t] == tok[t];
                 }
                 if (!same) {
-                    // stage the x rows (all T tokens, or this chunk's), every warp alike
+                    // q8 of this chunk's tokens into the staging area, every warp alike
                     if (!consumers_sync(s, cph, lane))
                         return;
-                    const int nrow = x_all ? a.T : nt;
 #pragma unroll
                     for (int t = 0; t < TCH; ++t)
-                        xrows[t] = x_all ? (t < a.T ? t : -1) : tok[t];
-                    const int v16 = a.d / 16, gx = a.d / G;
-                    for (int i = tid; i < nrow * v16; i += NT) {
-                        const int tt = i / v16, o = i % v16;
-                        int xr = 0;
-#pragma unroll
-                        for (int t = 0; t < TCH; ++t)
-                            xr = t == tt ? xrows[t] : xr;
-                        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(a.xq_eo + (long)xr * a.d) + o);
-                        reinterpret_cast<uint4 *>(xcodes + (size_t)tt * a.d)[o] = v;
-                    }
-                    for (int i = tid; i < nrow * gx; i += NT) {
-                        const int tt = i / gx, g = i % gx;
-                        int xr = 0;
-#pragma unroll
-                        for (int t = 0; t < TCH; ++t)
-                            xr = t == tt ? xrows[t] : xr;
-                        xsc[i] = __ldcg(a.xs + (long)xr * gx + g);
-                        xcr[i] = __ldcg(a.xc + (long)xr * gx + g);
-                    }
+                        xrows[t] = tok[t];
+                    stage_x_rows<TCH>(a, xcodes, xsc, xcr, xrows, nt, tid);
                     if (!consumers_sync(s, cph, lane))
                         return;
                     x_staged = true;
@@ -1097,7 +1509,6 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
                 for (int t = 0; t < TCH; ++t)
                     acc[m][t] = 0.0f;
         }
-        const unsigned char *stg = s.ring + (size_t)slot * STAGE_BYTES;
         if (it.mode == MODE_GATEUP) {
             consume<TCH>(stg, xcodes, xsc, xcr, a.d, a.d / G, rows, ng, k * SG, nt, warp, lane, acc);
         } else {
@@ -1114,7 +1525,7 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
             continue;
 
         // ---- end of a chunk: hand the partial sums to the epilogue warp of the buffer ----
-        const int b = chunk % NBUF;
+        const int b = chunk & (NBUF - 1);
         if (!buffer_free(b))
             return;
         float *pb = s.part + (size_t)b * PART;
@@ -1176,6 +1587,8 @@ __global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs
         if (lane == 0)
             run_producer<TCH>(a, s);
     } else if (warp > NC) {
+        grid_dep_wait();  // the activations are in
+        quantise_x(a, warp - NC - 1, lane);
         if (warp - NC - 1 < NBUF)
             run_epilogue<TCH>(a, s, warp - NC - 1, lane);
     } else {
@@ -1217,18 +1630,40 @@ int ring_for(DecodeArgs &a)
     return best_ns;
 }
 
-template <int TCH>
-cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
+// The SM count of the current device (cached per device, under a lock).
+cudaError_t sm_count_of_current(int &n_sm)
 {
-    auto fn = k_decode<TCH>;
-    const size_t smem = ring_layout(a, a.ring, a.nh, a.nbuf, TCH).total;
-    // per device: the SM count and the largest dynamic shared memory set so far (the
-    // attribute belongs to the device's context), so that a call costs no queries; host
-    // threads that launch at the same time take the lock, so the attribute and its record
-    // agree
     constexpr int MAX_DEV = 64;
     static std::mutex mu;
     static int sm_count[MAX_DEV] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= MAX_DEV)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (sm_count[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        sm_count[dev] = n;
+    }
+    n_sm = sm_count[dev];
+    return cudaSuccess;
+}
+
+template <int TCH>
+cudaError_t launch_tch(DecodeArgs a, int n_sm, cudaStream_t s)
+{
+    auto fn = k_decode<TCH>;
+    const size_t smem = ring_layout(a, a.ring, a.nh, a.nbuf, TCH).total;
+    // per device: the largest dynamic shared memory set so far (the attribute belongs to
+    // the device's context), so that a call costs no query; host threads that launch at
+    // the same time take the lock, so the attribute and its record agree
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
     static size_t smem_set[MAX_DEV] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1236,23 +1671,14 @@ cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
         return e;
     if (dev < 0 || dev >= MAX_DEV)
         return cudaErrorInvalidDevice;
-    int n_sm = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (sm_count[dev] == 0) {
-            int n = 0;
-            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess)
-                return e;
-            sm_count[dev] = n;
-        }
         if (smem > smem_set[dev]) {
             e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess)
                 return e;
             smem_set[dev] = smem;
         }
-        n_sm = sm_count[dev];
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_sm);
@@ -1274,6 +1700,44 @@ cudaError_t launch_tch(DecodeArgs a, cudaStream_t s)
     return e;
 }
 
+// The logit items: ne router rows against tb tokens, streamed in K-chunks of kc columns
+// ((tb + ne) rows of kc floats fill at most one stage). The choice minimises the rows a
+// CTA streams before routing can start, (tb + ne) times the items per CTA, with at most
+// LT tasks (expert, token) per consumer warp; ties go to fewer items.
+void logit_geometry(DecodeArgs &a, int n_sm)
+{
+    int best = 0x7fffffff, best_items = 0, bne = 1, btb = 1;
+    for (int ne = 1; ne <= 8 && ne <= a.E; ++ne) {
+        for (int tb = 1; tb <= a.T; ++tb) {
+            if (ne * tb > NC * LT || 4 * (tb + ne) * 32 > STAGE_BYTES)
+                continue;
+            const int items = ((a.E + ne - 1) / ne) * ((a.T + tb - 1) / tb);
+            const int cost = ((items + n_sm - 1) / n_sm) * (tb + ne);
+            if (cost < best || (cost == best && items < best_items)) {
+                best = cost;
+                best_items = items;
+                bne = ne;
+                btb = tb;
+            }
+        }
+    }
+    int kc = STAGE_BYTES / (4 * (btb + bne)) / 32 * 32;
+    kc = kc > a.d ? a.d : kc;
+    const int nck = (a.d + kc - 1) / kc;
+    a.lg_ne = bne;
+    a.lg_tb = btb;
+    a.lg_kc = round_up((a.d + nck - 1) / nck, 32);  // the same chunk count, balanced
+    a.lg_nck = (a.d + a.lg_kc - 1) / a.lg_kc;
+    a.n_logit = a.ids_given ? 0 : best_items;
+    // warps that select at once: two score rows of E floats and 32 picks each in
+    // SEL_SCRATCH bytes
+    const int per = 8 * ((a.E + 3) & ~3) + 128;
+    int sw = SEL_SCRATCH / per;
+    sw = sw < 1 ? 1 : sw;
+    sw = sw > NC ? NC : sw;
+    a.sel_warps = sw > a.T ? a.T : sw;
+}
+
 }  // namespace
 
 int decode_hgs(int fmax)
@@ -1281,17 +1745,16 @@ int decode_hgs(int fmax)
     return round_up(fmax / G, 4);
 }
 
-bool decode_selects_in_kernel(int T, int E)
-{
-    // the selection scratch (c and s of every token) shares shared memory with the ring
-    return T * E <= 4096;
-}
-
 cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
 {
     if (a.T <= 0)
         return cudaSuccess;
     a.hgs = decode_hgs(a.fmax);
+    int n_sm = 0;
+    cudaError_t e = sm_count_of_current(n_sm);
+    if (e != cudaSuccess)
+        return e;
+    logit_geometry(a, n_sm);
     // tokens per chunk: up to 4 (a slot with more tokens streams its weights once per
     // chunk, but the smaller x, h and partial-sum areas leave room for a deeper ring);
     // fewer when a large shape leaves no room for three ring stages
@@ -1301,11 +1764,11 @@ cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
     const int n2 = want >= 2 ? ring_for<2>(c2) : 0;
     const int n1 = ring_for<1>(c1);
     if (n4 >= 3 || (n4 >= 2 && n2 < 3 && n1 < 3))
-        return launch_tch<4>(c4, s);
+        return launch_tch<4>(c4, n_sm, s);
     if (n2 >= 3 || (n2 >= 2 && n1 < 3))
-        return launch_tch<2>(c2, s);
+        return launch_tch<2>(c2, n_sm, s);
     if (n1 >= 2)
-        return launch_tch<1>(c1, s);
+        return launch_tch<1>(c1, n_sm, s);
     return cudaErrorInvalidValue;
 }
 

@@ -13,7 +13,8 @@ struct WsLayout {
     size_t hq, hq_eo, hs, hc, y;
     size_t xbf, hbf;  // prefill (T > DECODE_T_MAX): bf16 codes of x and of q8(h)
     size_t nslots;      // slots at most: the shared expert + min(E, T*K) routed experts
-    size_t sync_bytes;  // decode kernel's claim counter | done_gu [nslots] | done_rb [d/32]
+    size_t sync_bytes;  // decode kernel's claim counter, routing counter, (two spare words) |
+                        // done_gu [nslots] | done_rb [d/32]
     size_t fmax, total;
 };
 

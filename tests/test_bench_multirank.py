@@ -74,9 +74,9 @@ def test_launch_counts_and_workload_tags():
     documented launch sequences; every workload names its activation type."""
     sys.path.insert(0, ROOT)
     import bench
-    assert bench.launches_per_step(1, 256, False) == 2          # routing kernel + expert kernel
-    assert bench.launches_per_step(32, 256, False) == 3         # + selection kernel above T x E = 4096
-    assert bench.launches_per_step(4, 256, True) == 2           # q8 + expert kernel
+    assert bench.launches_per_step(1, 256, False) == 1          # one kernel routes and runs the experts
+    assert bench.launches_per_step(32, 256, False) == 1
+    assert bench.launches_per_step(4, 256, True) == 1
     assert bench.launches_per_step(2048, 256, False) == 7
     assert bench.launches_per_step(2048, 256, True) == 5
     assert bench.launches_per_step(1, 256, False, f32=True) == 5   # logits, select, gate/up, down, combine
