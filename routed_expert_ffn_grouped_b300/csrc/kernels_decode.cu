@@ -44,9 +44,9 @@ namespace clb {
 
 namespace {
 
-constexpr int NC = 16;                       // consumer warps
+constexpr int NC = 8;                        // consumer warps
 constexpr int NT = NC * 32;                  // consumer threads
-constexpr int GPW = 2;                       // groups per consumer warp and stage
+constexpr int GPW = 4;                       // groups per consumer warp and stage
 constexpr int SG = NC * GPW;                 // group tiles per matrix and stage
 constexpr int STAGE_BYTES = 2 * SG * 640;    // 2 matrices x 32 groups x (512 + 128) bytes
 constexpr int MAX_RING = 16;
