@@ -51,7 +51,8 @@ extern "C" {
 #define COLIBRI_E_STAGE (-6)   /* staging an expert into the cache failed */
 #define COLIBRI_E_DEVICE (-7)  /* a kernel reported bad input through the error flag */
 
-#define COLIBRI_GROUP 32 /* quantisation group: elements per scale */
+#define COLIBRI_GROUP 32   /* the default quantisation group: elements per scale */
+#define COLIBRI_GROUP64 64 /* the 64-element groups of the pages' int4 containers */
 
 enum { COLIBRI_ROUTER_SIGMOID_GROUPED = 0, COLIBRI_ROUTER_SOFTMAX = 1 };
 
@@ -65,7 +66,11 @@ enum { COLIBRI_ROUTER_SIGMOID_GROUPED = 0, COLIBRI_ROUTER_SOFTMAX = 1 };
  *   router       COLIBRI_ROUTER_*
  *   norm_topk    1: the k selected weights are renormalised to sum 1 before scaling
  *   routed_scale multiplies the routed weights
- *   group        must be COLIBRI_GROUP */
+ *   group        elements per scale, COLIBRI_GROUP (32) or COLIBRI_GROUP64 (64): of the
+ *                expert weights (one fp32 scale per row and group of columns) and of the
+ *                q8 activations x and h (one scale per row and group); d, ffn and
+ *                shared_ffn must be multiples of it. The int4 container of the
+ *                aifrontierpost tutorial ("Step 3 -- Get a model") uses 64. */
 typedef struct {
     int d, ffn, n_exp, top_k, n_group, topk_group, has_shared, shared_ffn, router, norm_topk;
     float routed_scale;
@@ -73,9 +78,11 @@ typedef struct {
 } colibri_layer_cfg;
 
 /* One expert's tensors (device pointers, 16-byte aligned), in the stored layout above:
- * gate w1 [f][d], up w3 [f][d], down w2 [d][f] packed int4; scales s1 [f][d/32],
- * s3 [f][d/32], s2 [d][f/32] fp32. Group-scaled int4 container: aifrontierpost tutorial,
- * "Step 3 -- Get a model"; the layer uses 32-element groups. */
+ * gate w1 [f][d], up w3 [f][d], down w2 [d][f] packed int4; scales s1 [f][d/g],
+ * s3 [f][d/g], s2 [d][f/g] fp32 for the layer's group g. Group-scaled int4 container:
+ * aifrontierpost tutorial, "Step 3 -- Get a model". With g = 64 the nibbles are stored
+ * exactly as for 32 (a 64-group is two consecutive 32-column tiles of a row block) and the
+ * scales S[r][g] at float ((r / 32) * (K / 64) + g) * 32 + r % 32. */
 typedef struct {
     const uint8_t *w1, *w3, *w2;
     const float *s1, *s3, *s2;
@@ -93,6 +100,9 @@ typedef struct {
  * 23,592,960 bytes with its scales. Returns COLIBRI_E_INVAL unless d, f are positive
  * multiples of 32. */
 int colibri_blob_layout_for(int d, int f, colibri_blob_layout *out);
+/* The same for experts with `group`-element scale groups (32 or 64; d, f multiples of
+ * it): the nibbles are the same, the scale parts are d*f/group floats each. */
+int colibri_blob_layout_for_g(int d, int f, int group, colibri_blob_layout *out);
 
 /* Host only. A static string naming a status code. */
 const char *colibri_strerror(int status);
@@ -107,6 +117,10 @@ const char *colibri_strerror(int status);
  *   scale  device fp32 [rows][cols/32] (out)
  * rows == 0 is a no-op. */
 int colibri_q8_quantize(const float *x, int rows, int cols, int8_t *q, float *scale, void *stream);
+/* The same quantiser per `group` (32 or 64) consecutive columns: scale [rows][cols/group],
+ * cols % group == 0 (64: the 64-element groups of the aifrontierpost tutorial, "Step 3"). */
+int colibri_q8_quantize_g(const float *x, int rows, int cols, int group, int8_t *q, float *scale,
+                          void *stream);
 
 /* Router: logits, selection and weights for T tokens (DeepSeek-V3-style sigmoid router
  * with a selection bias: dashen-tech guide, table "Points techniques cles", row "Router

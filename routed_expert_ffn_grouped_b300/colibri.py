@@ -63,8 +63,10 @@ _PCFG = ctypes.POINTER(LayerCfg)
 # name -> (restype, argtypes); every symbol include/colibri.h declares.
 SIGNATURES = {
     "colibri_blob_layout_for": (_I, [_I, _I, ctypes.POINTER(BlobLayout)]),
+    "colibri_blob_layout_for_g": (_I, [_I, _I, _I, ctypes.POINTER(BlobLayout)]),
     "colibri_strerror": (ctypes.c_char_p, [_I]),
     "colibri_q8_quantize": (_I, [_P, _I, _I, _P, _P, _P]),
+    "colibri_q8_quantize_g": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "colibri_router_topk": (_I, [_PCFG, _P, _I, _P, _P, _P, _P, _P, _P]),
     "colibri_moe_workspace_bytes": (_SZ, [_PCFG, _I]),
     "colibri_moe_layer": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
@@ -152,19 +154,27 @@ def layer_cfg(spec) -> LayerCfg:
                     n_group=spec.n_group, topk_group=spec.topk_group,
                     has_shared=int(spec.has_shared), shared_ffn=spec.shared_ffn,
                     router=ROUTER_SOFTMAX if spec.router == "softmax" else ROUTER_SIGMOID_GROUPED,
-                    norm_topk=int(spec.norm_topk), routed_scale=spec.routed_scale, group=GROUP)
+                    norm_topk=int(spec.norm_topk), routed_scale=spec.routed_scale,
+                    group=getattr(spec, "group", GROUP))
 
 
-def colibri_blob_layout_for(d: int, f: int) -> BlobLayout:
+def colibri_blob_layout_for(d: int, f: int, group: int = GROUP) -> BlobLayout:
     out = BlobLayout()
-    _check("colibri_blob_layout_for", lib().colibri_blob_layout_for(d, f, ctypes.byref(out)))
+    if group == GROUP:
+        _check("colibri_blob_layout_for", lib().colibri_blob_layout_for(d, f, ctypes.byref(out)))
+    else:
+        _check("colibri_blob_layout_for_g", lib().colibri_blob_layout_for_g(d, f, group, ctypes.byref(out)))
     return out
 
 
-def colibri_q8_quantize(x, q, scale, stream=None):
+def colibri_q8_quantize(x, q, scale, stream=None, group: int = GROUP):
     rows, cols = x.shape
-    _check("colibri_q8_quantize",
-           lib().colibri_q8_quantize(_ptr(x), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+    if group == GROUP:
+        _check("colibri_q8_quantize",
+               lib().colibri_q8_quantize(_ptr(x), rows, cols, _ptr(q), _ptr(scale), _stream(stream)))
+    else:
+        _check("colibri_q8_quantize_g",
+               lib().colibri_q8_quantize_g(_ptr(x), rows, cols, group, _ptr(q), _ptr(scale), _stream(stream)))
 
 
 def colibri_router_topk(cfg: LayerCfg, x, Wr, bias, logits, ids, w, stream=None):
@@ -367,7 +377,7 @@ class DeviceLayer:
         spec = layer.spec
         self.spec = spec
         self.cfg = layer_cfg(spec)
-        self.lay = colibri_blob_layout_for(spec.d, spec.ffn)
+        self.lay = colibri_blob_layout_for(spec.d, spec.ffn, getattr(spec, "group", GROUP))
         nb = self.lay.nbytes
         assert layer.blobs.shape[1] == nb
         self.blobs = torch.from_numpy(layer.blobs).to(device)
@@ -382,7 +392,7 @@ class DeviceLayer:
         self.shared_blob = None
         if spec.has_shared:
             self.shared_blob = torch.from_numpy(layer.shared_blob).to(device)
-            sl = colibri_blob_layout_for(spec.d, spec.shared_ffn)
+            sl = colibri_blob_layout_for(spec.d, spec.shared_ffn, getattr(spec, "group", GROUP))
             self.shared = self._expert_at(self.shared_blob.data_ptr(), sl)
 
     @classmethod
@@ -406,7 +416,7 @@ class DeviceLayer:
         t.shared_blob = None
         if t.spec.has_shared:
             t.shared_blob = other.shared_blob.clone()
-            sl = colibri_blob_layout_for(t.spec.d, t.spec.shared_ffn)
+            sl = colibri_blob_layout_for(t.spec.d, t.spec.shared_ffn, getattr(t.spec, "group", GROUP))
             t.shared = cls._expert_at(t.shared_blob.data_ptr(), sl)
         return t
 

@@ -43,13 +43,14 @@ namespace clb {
 
 bool cfg_valid(const colibri_layer_cfg *c)
 {
-    if (!c || c->group != G)
+    if (!c || (c->group != 32 && c->group != 64))
         return false;
-    if (c->d <= 0 || c->d % G || c->d > 8192 || c->ffn <= 0 || c->ffn % G || c->ffn > 4096)
+    const int gq = c->group;
+    if (c->d <= 0 || c->d % gq || c->d > 8192 || c->ffn <= 0 || c->ffn % gq || c->ffn > 4096)
         return false;
     if (c->n_exp <= 0 || c->n_exp > 1024 || c->top_k <= 0 || c->top_k > 32 || c->top_k > c->n_exp)
         return false;
-    if (c->has_shared && (c->shared_ffn <= 0 || c->shared_ffn % G || c->shared_ffn > 4096))
+    if (c->has_shared && (c->shared_ffn <= 0 || c->shared_ffn % gq || c->shared_ffn > 4096))
         return false;
     if (c->router == COLIBRI_ROUTER_SIGMOID_GROUPED) {
         if (c->n_group <= 0 || c->n_group > 32 || c->n_exp % c->n_group)
@@ -93,7 +94,10 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     L.err = take(256);
     L.counters = take(sizeof(Counters));
     L.nslots = nslots;
-    L.sync_bytes = 4 * (4 + nslots + d / G);
+    // 64-element groups: one pair counter per (row of h, 64-group) for the decode kernel's
+    // q8 of h across two gate/up items
+    L.hpair_count = c->group == 64 ? PT * (fmax / 64) : 0;
+    L.sync_bytes = 4 * (4 + nslots + d / G + L.hpair_count);
     L.sync = take(L.sync_bytes);
     L.qx = take((size_t)T * d);
     L.qx_eo = take((size_t)T * d);
@@ -112,6 +116,7 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     L.hc = take(4 * PT * hgs);
     L.y = take(4 * PT * d);
     const bool prefill = uses_gemm(c, T);
+    L.hf = take(c->group == 64 && !prefill ? 4 * PT * fmax : 0);  // fp32 h before its q8 per 64
     L.xbf = take(prefill ? 2 * (size_t)T * d : 0);
     L.hbf = take(prefill ? 2 * PT * fmax : 0);
     L.fmax = fmax;
@@ -125,10 +130,15 @@ extern "C" {
 
 int colibri_blob_layout_for(int d, int f, colibri_blob_layout *out)
 {
-    if (!out || d <= 0 || f <= 0 || d % G || f % G)
+    return colibri_blob_layout_for_g(d, f, COLIBRI_GROUP, out);
+}
+
+int colibri_blob_layout_for_g(int d, int f, int group, colibri_blob_layout *out)
+{
+    if (!out || (group != 32 && group != 64) || d <= 0 || f <= 0 || d % group || f % group)
         return COLIBRI_E_INVAL;
-    const size_t nib = (size_t)f * d / 2, sc = 4 * (size_t)f * (d / G);
-    const size_t nib2 = (size_t)d * f / 2, sc2 = 4 * (size_t)d * (f / G);
+    const size_t nib = (size_t)f * d / 2, sc = 4 * (size_t)f * (d / group);
+    const size_t nib2 = (size_t)d * f / 2, sc2 = 4 * (size_t)d * (f / group);
     size_t o = 0;
     out->w1 = o;
     o = up256(o + nib);
@@ -163,14 +173,19 @@ const char *colibri_strerror(int status)
 
 int colibri_q8_quantize(const float *x, int rows, int cols, int8_t *q, float *scale, void *stream)
 {
-    if (rows < 0 || cols <= 0 || cols % G)
+    return colibri_q8_quantize_g(x, rows, cols, COLIBRI_GROUP, q, scale, stream);
+}
+
+int colibri_q8_quantize_g(const float *x, int rows, int cols, int group, int8_t *q, float *scale, void *stream)
+{
+    if (rows < 0 || cols <= 0 || (group != 32 && group != 64) || cols % group)
         return COLIBRI_E_INVAL;
     if (rows == 0)
         return COLIBRI_OK;
     if (!x || !q || !scale)
         return COLIBRI_E_INVAL;
-    Q8Args a{x, rows, cols, q, scale, nullptr, nullptr, nullptr};  // codes and scales only
-    const long groups = (long)rows * (cols / G);
+    Q8Args a{x, rows, cols, q, scale, nullptr, nullptr, nullptr, group};  // codes and scales only
+    const long groups = (long)rows * (cols / group);
     const long blocks = (groups + 7) / 8;
     if (blocks > 0x7fffffffL)
         return COLIBRI_E_INVAL;
@@ -227,7 +242,7 @@ static int launch_route_logits(const colibri_layer_cfg *cfg, const float *x, int
     if (T > DECODE_T_MAX) {
         // many tokens: (token x expert) tiles; q8 of x runs as its own kernel
         if (q8.x) {
-            const long groups = (long)T * (cfg->d / G);
+            const long groups = (long)T * (cfg->d / cfg->group);
             k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(q8);
             if (cudaGetLastError() != cudaSuccess)
                 return COLIBRI_E_CUDA;
@@ -301,7 +316,7 @@ int colibri_moe_workspace_view(const colibri_layer_cfg *cfg, int T_max, colibri_
     out->hs = L.hs;
     out->y = L.y;
     out->fmax = L.fmax;
-    out->hs_stride = uses_gemm(cfg, T_max) ? L.fmax / G : (size_t)decode_hgs((int)L.fmax);
+    out->hs_stride = uses_gemm(cfg, T_max) ? L.fmax / cfg->group : (size_t)decode_hgs((int)L.fmax);
     out->hbf = L.hbf;
     return COLIBRI_OK;
 }
@@ -361,7 +376,7 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     // q8 of x for prefill: plain codes and scales, and the bf16 codes in the tensor-core
     // order (decode quantises x inside its kernel)
     Q8Args qa{x, T, d, reinterpret_cast<int8_t *>(ws + L.qx), reinterpret_cast<float *>(ws + L.sx), nullptr,
-              nullptr, reinterpret_cast<uint16_t *>(ws + L.xbf)};
+              nullptr, reinterpret_cast<uint16_t *>(ws + L.xbf), cfg->group};
     const int down_blocks = (d + DN_ITEM_ROWS - 1) / DN_ITEM_ROWS;
     BucketArgs ba{ids, T, K, E, cfg->has_shared, cfg->shared_ffn, cfg->ffn, down_blocks, 0,
                   reinterpret_cast<int32_t *>(ws + L.offsets), reinterpret_cast<int32_t *>(ws + L.pairs),
@@ -425,13 +440,16 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
         da.done_rb = sync + 4 + L.nslots;
         da.err = err;
         da.max_slots = (int)L.nslots;
+        da.group = cfg->group;
+        da.hf = reinterpret_cast<float *>(ws + L.hf);
+        da.hpair = sync + 4 + L.nslots + d / G;
         if (launch_decode(da, s) != cudaSuccess || prof_mark(5, s) || prof_mark(6, s) || prof_mark(7, s))
             return COLIBRI_E_CUDA;
         return COLIBRI_OK;
     }
     if (ids_given) {
         // a1: q8 of x
-        const long groups = (long)T * (d / G);
+        const long groups = (long)T * (d / cfg->group);
         k_q8<<<(unsigned)((groups + 7) / 8), 256, 0, s>>>(qa);
         if (cudaGetLastError() != cudaSuccess || prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s))
             return COLIBRI_E_CUDA;
@@ -471,12 +489,13 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     gm.slots = reinterpret_cast<const Slot *>(ws + L.slots);
     gm.counters = reinterpret_cast<const Counters *>(ws + L.counters);
     gm.pairs = reinterpret_cast<const int32_t *>(ws + L.pairs);
+    gm.group = cfg->group;
     gm.err = err;
     GemmArgs gg = gm;
     gg.abf = reinterpret_cast<const uint16_t *>(ws + L.xbf);
     gg.as = reinterpret_cast<const float *>(ws + L.sx);
     gg.act_stride = d;
-    gg.act_groups = d / G;
+    gg.act_groups = d / cfg->group;
     gg.hbf = reinterpret_cast<uint16_t *>(ws + L.hbf);
     gg.hs = reinterpret_cast<float *>(ws + L.hs);
     if (launch_gemm(MODE_GATEUP, gg, s) != cudaSuccess || prof_mark(5, s))
@@ -485,7 +504,7 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     gd.abf = reinterpret_cast<const uint16_t *>(ws + L.hbf);
     gd.as = reinterpret_cast<const float *>(ws + L.hs);
     gd.act_stride = (long)L.fmax;
-    gd.act_groups = (int)L.fmax / G;
+    gd.act_groups = (int)L.fmax / cfg->group;
     gd.y = reinterpret_cast<float *>(ws + L.y);
     if (launch_gemm(MODE_DOWN, gd, s) != cudaSuccess || prof_mark(6, s))
         return COLIBRI_E_CUDA;
@@ -588,6 +607,7 @@ int colibri_moe_layer_f32(const colibri_layer_cfg *cfg, const float *x, int T, c
     fa.shared_ffn = cfg->shared_ffn;
     fa.has_shared = cfg->has_shared;
     fa.fmax = (int)L.fmax;
+    fa.gsh = cfg->group == 64 ? 1 : 0;
     fa.err = err;
     const unsigned pt = (unsigned)L.pt;
     k_f32_gateup<<<dim3((unsigned)(L.fmax / G), pt), 256, f32_smem_gateup(cfg->d), s>>>(fa);

@@ -14,6 +14,7 @@ struct Q8Args {
     int8_t *q_eo;  // optional: codes in even/odd word order
     int *corr;     // optional: 8 * sum(codes) per group
     uint16_t *q_bf;  // optional: codes as bf16 in the tensor-core k order (bf16_pos)
+    int group;       // elements per scale: 32 or 64 (corrections stay per 32 elements)
 };
 
 struct RouterArgs {
@@ -97,6 +98,11 @@ struct DecodeArgs {
     // at once
     int ring, nh, nbuf, tch, hgs;
     int lg_ne, lg_tb, lg_kc, lg_nck, n_logit, sel_warps;
+    // quantisation group (32 or 64); with 64, the gate/up items' fp32 h rows and one
+    // counter per (row of h, 64-group): the item that completes a pair quantises it
+    int group;
+    float *hf;
+    int *hpair;
 };
 
 // One persistent launch for a decode step: router logits, expert selection (unless
@@ -123,6 +129,7 @@ struct GemmArgs {
     uint16_t *hbf;     // gate/up output: q8(h) codes as bf16 [pairs_total][fmax]
     float *hs;         // gate/up output: their scales [pairs_total][fmax/32]
     float *y;          // down output [pairs_total][d]
+    int group;         // quantisation group: 32 or 64 (one scale per group of 32-column tiles)
     int *err;
 };
 
@@ -141,6 +148,7 @@ struct F32Args {
     float *h;                       // [T*K + T][fmax]: pairs, then the shared expert's rows
     float *y;                       // [T*K + T][d]
     int T, K, E, d, ffn, shared_ffn, has_shared, fmax;
+    int gsh;  // 1 for 64-element groups (the scale of 32-column tile g is group g >> gsh)
     int *err;
 };
 __global__ void k_f32_gateup(F32Args a);

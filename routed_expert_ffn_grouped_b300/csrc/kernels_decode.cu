@@ -379,8 +379,16 @@ __device__ void stage_x_rows(const DecodeArgs &a, int8_t *codes, float *sc, int 
 #pragma unroll
         for (int t = 0; t < TCH; ++t)
             xr = t == r ? rows[t] : xr;
-        sc[i] = __ldcg(a.sx + (long)xr * gx + g);
         cr[i] = __ldcg(a.xc + (long)xr * gx + g);
+    }
+    const int gs = a.d / a.group;  // scales a row
+    for (int i = tid; i < nrow * gs; i += NT) {
+        const int r = i / gs, g = i - r * gs;
+        int xr = 0;
+#pragma unroll
+        for (int t = 0; t < TCH; ++t)
+            xr = t == r ? rows[t] : xr;
+        sc[i] = __ldcg(a.sx + (long)xr * gs + g);
     }
 }
 
@@ -918,7 +926,7 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
     const bool writer = blockIdx.x == 0;
     // all T tokens' x codes staged at once, by bulk copies when the parts are whole 16-byte
     // runs
-    const bool x_all = T <= a.tch, x_bulk = x_all && ((long)T * a.d) % 128 == 0;
+    const bool x_all = T <= a.tch, x_bulk = x_all && ((long)T * a.d) % (4 * a.group) == 0;
     int *sids = reinterpret_cast<int *>(s.part);
     int *first = sids + P;
     unsigned char *scr0 = reinterpret_cast<unsigned char *>(s.part) + ((8 * (size_t)P + 16 + 15) & ~size_t(15));
@@ -927,18 +935,19 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
         s.flags[1] = s.flags[2] = 0;
         int ok = 1;
         // every logit task and every q8 group of x of the layer
-        ok = wait_count_geq(a.route_done, (a.ids_given ? 0 : a.E * a.T) + a.T * (a.d / G));
+        ok = wait_count_geq(a.route_done, (a.ids_given ? 0 : a.E * a.T) + a.T * (a.d / a.group));
         __threadfence();
         if (ok && x_bulk) {
             // the q8 of all T tokens into the x staging area (codes in even/odd order,
             // scales, corrections)
             fence_proxy_async_global();
-            const uint32_t nc = (uint32_t)(a.T * a.d), ns = (uint32_t)(4 * a.T * (a.d / G));
+            const uint32_t nc = (uint32_t)(a.T * a.d), ns = (uint32_t)(4 * a.T * (a.d / a.group)),
+                           nr = (uint32_t)(4 * a.T * (a.d / G));
             unsigned char *act = reinterpret_cast<unsigned char *>(s.act);
-            mbar_arrive_expect_tx(s.xbar, nc + 2 * ns);
+            mbar_arrive_expect_tx(s.xbar, nc + ns + nr);
             bulk_g2s(act, a.xq_eo, nc, s.xbar);
             bulk_g2s(act + x_sc_off(a.d, a.tch), a.sx, ns, s.xbar);
-            bulk_g2s(act + x_cr_off(a.d, a.tch), a.xc, ns, s.xbar);
+            bulk_g2s(act + x_cr_off(a.d, a.tch), a.xc, nr, s.xbar);
         }
         s.flags[3] = ok;
     }
@@ -985,22 +994,25 @@ __device__ bool route_cta(const DecodeArgs &a, const RingSmem &s, uint32_t &cph,
         int *cr = reinterpret_cast<int *>(s.act + x_cr_off(a.d, a.tch));
         for (int i = tid; i < T * v16; i += NT)
             reinterpret_cast<uint4 *>(codes)[i] = __ldcg(reinterpret_cast<const uint4 *>(a.xq_eo) + i);
-        for (int i = tid; i < T * gx; i += NT) {
-            sc[i] = __ldcg(a.sx + i);
+        for (int i = tid; i < T * gx; i += NT)
             cr[i] = __ldcg(a.xc + i);
-        }
+        for (int i = tid; i < T * (a.d / a.group); i += NT)
+            sc[i] = __ldcg(a.sx + i);
         named_sync(1, NT);
     }
     return true;
 }
 
-// Partial dots of one stage: consumer warp w takes groups w, w + NC, ... of the stage.
-// Activation row t of the chunk sits at row rows[t] of the staged codes (row stride
-// cstride bytes), scales and corrections (gstride groups a row).
+// Partial dots of one stage: consumer warp w takes 32-column tiles w, w + NC, ... of the
+// stage. Activation row t of the chunk sits at row rows[t] of the staged codes (row stride
+// cstride bytes), corrections (gstride a row, one per 32 columns) and scales (sstride a
+// row, one per group: tile g >> gsh, gsh = 1 for 64-element groups). The stage holds one
+// weight scale tile per group.
 template <int TCH>
 __device__ __forceinline__ void consume(const unsigned char *stg, const int8_t *codes, const float *sc,
-                                        const int *corr, int cstride, int gstride, const int (&rows)[TCH], int ng,
-                                        int g0, int nt, int warp, int lane, float (&acc)[2][TCH])
+                                        const int *corr, int cstride, int gstride, int sstride, int gsh,
+                                        const int (&rows)[TCH], int ng, int g0, int nt, int warp, int lane,
+                                        float (&acc)[2][TCH])
 {
     constexpr int M = 2;
     constexpr int scale_off = M * SG * 512;
@@ -1015,7 +1027,7 @@ __device__ __forceinline__ void consume(const unsigned char *stg, const int8_t *
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 nsp[m] = split_nibbles(*reinterpret_cast<const uint4 *>(stg + (m * SG + j) * 512 + lane * 16));
-                sw[m] = *reinterpret_cast<const float *>(stg + scale_off + (m * SG + j) * 128 + lane * 4);
+                sw[m] = *reinterpret_cast<const float *>(stg + scale_off + (m * SG + (j >> gsh)) * 128 + lane * 4);
             }
 #pragma unroll
             for (int t = 0; t < TCH; ++t) {
@@ -1024,7 +1036,7 @@ __device__ __forceinline__ void consume(const unsigned char *stg, const int8_t *
                     const uint4 *xa = reinterpret_cast<const uint4 *>(codes + (size_t)r * cstride + g * G);
                     const uint4 A0 = xa[0], A1 = xa[1];
                     const int cr = corr[r * gstride + g];
-                    const float sa = sc[r * gstride + g];
+                    const float sa = sc[r * sstride + (g >> gsh)];
 #pragma unroll
                     for (int m = 0; m < M; ++m) {
                         const int D = dot_split(nsp[m], A0, A1, cr);
@@ -1048,6 +1060,7 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
         prefetch_l2(a.experts, (uint32_t)(((size_t)a.E * sizeof(colibri_expert) + 15) & ~size_t(15)));
     grid_dep_wait();  // inputs and the zeroed counters are in
     const uint64_t pol = policy_evict_first();
+    const int gsh = a.group == 64 ? 1 : 0;           // 32-column tile -> group
     const int pre = a.n_logit + shared_gu_items(a);  // items that need no routing table
     int n_gu = pre, total = 0x7fffffff;              // until the table is in
     bool have_table = false, route_posted = false;
@@ -1153,17 +1166,18 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
         const unsigned char *wa, *wb;
         const float *sa_, *sb_;
         bool two = true;
+        const int nsg = ng >> gsh;  // scale tiles a row block
         if (gu) {
             wa = ex.w1 + (size_t)it.rb * ng * 512;
             wb = ex.w3 + (size_t)it.rb * ng * 512;
-            sa_ = ex.s1 + (size_t)it.rb * ng * 32;
-            sb_ = ex.s3 + (size_t)it.rb * ng * 32;
+            sa_ = ex.s1 + (size_t)it.rb * nsg * 32;
+            sb_ = ex.s3 + (size_t)it.rb * nsg * 32;
         } else {
             two = it.rb + 1 < a.d / G;
             wa = ex.w2 + (size_t)it.rb * ng * 512;
             wb = wa + (size_t)ng * 512;
-            sa_ = ex.s2 + (size_t)it.rb * ng * 32;
-            sb_ = sa_ + (size_t)ng * 32;
+            sa_ = ex.s2 + (size_t)it.rb * nsg * 32;
+            sb_ = sa_ + (size_t)nsg * 32;
         }
         for (int q = 0, ch = 0, k = 0; q < nq && run; ++q) {
             int flag = 0;
@@ -1212,12 +1226,13 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
             const int g0 = k * SG, n = min(SG, ng - g0);
             unsigned char *dst = s.ring + (size_t)slot * STAGE_BYTES;
             s.tag[slot] = make_int2(idx, k | (ch << 8) | flag);
-            mbar_arrive_expect_tx(&s.full[slot], (uint32_t)((two ? 2 : 1) * n * 640));
+            const int ns = n >> gsh, s0 = g0 >> gsh;  // the stage's scale tiles
+            mbar_arrive_expect_tx(&s.full[slot], (uint32_t)((two ? 2 : 1) * (n * 512 + ns * 128)));
             bulk_g2s_hint(dst, wa + (size_t)g0 * 512, n * 512, &s.full[slot], pol);
-            bulk_g2s_hint(dst + 2 * SG * 512, sa_ + (size_t)g0 * 32, n * 128, &s.full[slot], pol);
+            bulk_g2s_hint(dst + 2 * SG * 512, sa_ + (size_t)s0 * 32, ns * 128, &s.full[slot], pol);
             if (two) {
                 bulk_g2s_hint(dst + SG * 512, wb + (size_t)g0 * 512, n * 512, &s.full[slot], pol);
-                bulk_g2s_hint(dst + 2 * SG * 512 + SG * 128, sb_ + (size_t)g0 * 32, n * 128, &s.full[slot], pol);
+                bulk_g2s_hint(dst + 2 * SG * 512 + SG * 128, sb_ + (size_t)s0 * 32, ns * 128, &s.full[slot], pol);
             }
             ++st;
             if (++k == spi) {
@@ -1239,29 +1254,37 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
 
 // ---------------- epilogue warp e: the chunks that used partial-sum buffer e ----------------
 // The epilogue warps' first job, while the consumers stream the logit items: this CTA's
-// share of the q8 of x (one warp per 32-group, lane k holding element k, groups
-// blockIdx.x * NE_MAX + e, ...), written to the workspace as plain codes and scales and as
-// the codes in even/odd word order with their corrections 8 * sum(codes); each group is
-// counted with the logit tasks on the routing counter.
+// share of the q8 of x (one warp per group of 32 or 64 elements, lane k holding element k
+// and k + 32, groups blockIdx.x * NE_MAX + e, ...), written to the workspace as plain
+// codes and scales and as the codes in even/odd word order with their corrections
+// 8 * sum(codes) per 32 elements; each group is counted with the logit tasks on the
+// routing counter.
 __device__ void quantise_x(const DecodeArgs &a, int e, int lane)
 {
-    const int gx = a.d / G;
+    const int gq = a.group, halves = gq / G, gx = a.d / gq;
     const long n = (long)a.T * gx;
     int done = 0;
     for (long gw = (long)blockIdx.x * NE_MAX + e; gw < n; gw += (long)gridDim.x * NE_MAX) {
         const long t = gw / gx, g = gw - t * gx;
-        const long base = t * a.d + g * G;
-        const float x = __ldg(a.x + base + lane);
-        const float amax = warp_max(fabsf(x));
-        const float dd = __fdiv_rn(amax, 127.0f);
-        const int q = q8_code_r(x, dd, __frcp_rn(dd));
-        a.qx[base + lane] = (int8_t)q;
-        a.xq_eo[base + eo_pos(lane)] = (int8_t)q;
-        const int sq = warp_sum_i(q);
-        if (lane == 0) {
-            a.sx[gw] = dd;
-            a.xc[gw] = 8 * sq;
+        const long base = t * a.d + g * gq;
+        float x[2];
+        float m = 0.0f;
+        for (int h = 0; h < halves; ++h) {
+            x[h] = __ldg(a.x + base + h * G + lane);
+            m = fmaxf(m, fabsf(x[h]));
         }
+        const float amax = warp_max(m);
+        const float dd = __fdiv_rn(amax, 127.0f), rd = __frcp_rn(dd);
+        for (int h = 0; h < halves; ++h) {
+            const int q = q8_code_r(x[h], dd, rd);
+            a.qx[base + h * G + lane] = (int8_t)q;
+            a.xq_eo[base + h * G + eo_pos(lane)] = (int8_t)q;
+            const int sq = warp_sum_i(q);
+            if (lane == 0)
+                a.xc[t * (a.d / G) + g * halves + h] = 8 * sq;
+        }
+        if (lane == 0)
+            a.sx[gw] = dd;
         ++done;
     }
     if (done) {
@@ -1288,6 +1311,7 @@ __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int 
         if (mode < 0)
             return;  // end of work
         const int slot = dp->slot, rb = dp->rb, nt = dp->nt;
+        int published = 0;  // rows of h (32-row blocks x tokens) whose q8 this chunk completed
         for (int t = 0; t < nt; ++t) {
             const long r = dp->orow[t];
             if (mode == MODE_GATEUP) {
@@ -1297,16 +1321,48 @@ __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int 
                     up += pb[((w * 2 + 1) * TCH + t) * 32 + lane];
                 }
                 const float h = gt / (1.0f + expf(-gt)) * up;
-                const float amax = warp_max(fabsf(h));
-                const float dd = __fdiv_rn(amax, 127.0f);
-                const int q = q8_code_r(h, dd, __frcp_rn(dd));
-                const long hb = r * a.fmax + (long)rb * G;
-                a.hq[hb + lane] = (int8_t)q;
-                a.hq_eo[hb + eo_pos(lane)] = (int8_t)q;
-                const int sq = warp_sum_i(q);
-                if (lane == 0) {
-                    a.hs[r * a.hgs + rb] = dd;
-                    a.hc[r * a.hgs + rb] = 8 * sq;
+                if (a.group == 64) {
+                    // the 64-group of h spans row blocks rb & ~1 and rb | 1: the item that
+                    // finishes second quantises both halves
+                    a.hf[r * a.fmax + (long)rb * G + lane] = h;
+                    __threadfence();
+                    __syncwarp();
+                    int second = 0;
+                    if (lane == 0)
+                        second = atomicAdd(a.hpair + r * (a.fmax / 64) + (rb >> 1), 1) == 1;
+                    if (__shfl_sync(FULL, second, 0)) {
+                        __threadfence();
+                        const float hp = __ldcg(a.hf + r * a.fmax + (long)(rb ^ 1) * G + lane);
+                        const float h0 = (rb & 1) ? hp : h, h1 = (rb & 1) ? h : hp;
+                        const float amax = warp_max(fmaxf(fabsf(h0), fabsf(h1)));
+                        const float dd = __fdiv_rn(amax, 127.0f), rd = __frcp_rn(dd);
+                        const int q0 = q8_code_r(h0, dd, rd), q1 = q8_code_r(h1, dd, rd);
+                        const long hb = r * a.fmax + (long)(rb >> 1) * 64;
+                        a.hq[hb + lane] = (int8_t)q0;
+                        a.hq[hb + G + lane] = (int8_t)q1;
+                        a.hq_eo[hb + eo_pos(lane)] = (int8_t)q0;
+                        a.hq_eo[hb + G + eo_pos(lane)] = (int8_t)q1;
+                        const int s0 = warp_sum_i(q0), s1 = warp_sum_i(q1);
+                        if (lane == 0) {
+                            a.hs[r * a.hgs + (rb >> 1)] = dd;
+                            a.hc[r * a.hgs + (rb & ~1)] = 8 * s0;
+                            a.hc[r * a.hgs + (rb | 1)] = 8 * s1;
+                        }
+                        published += 2;
+                    }
+                } else {
+                    const float amax = warp_max(fabsf(h));
+                    const float dd = __fdiv_rn(amax, 127.0f);
+                    const int q = q8_code_r(h, dd, __frcp_rn(dd));
+                    const long hb = r * a.fmax + (long)rb * G;
+                    a.hq[hb + lane] = (int8_t)q;
+                    a.hq_eo[hb + eo_pos(lane)] = (int8_t)q;
+                    const int sq = warp_sum_i(q);
+                    if (lane == 0) {
+                        a.hs[r * a.hgs + rb] = dd;
+                        a.hc[r * a.hgs + rb] = 8 * sq;
+                    }
+                    published += 1;
                 }
             } else {
                 float y0 = 0.0f, y1 = 0.0f;
@@ -1325,8 +1381,8 @@ __device__ void run_epilogue(const DecodeArgs &a, const RingSmem &s, int e, int 
         __threadfence();                // this chunk's rows are visible device-wide
         __syncwarp();
         if (mode == MODE_GATEUP) {
-            if (lane == 0)
-                atomicAdd(a.done_gu + slot, nt);
+            if (lane == 0 && published)
+                atomicAdd(a.done_gu + slot, published);
             continue;
         }
         // each of the item's row blocks of d: the epilogue that completes it combines it
@@ -1381,6 +1437,7 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
     int orow = -1;  // lane t < nt: pair row of the chunk's t-th token
     float acc[2][TCH];
     float *lacc = s.part + (size_t)warp * LT * 32;  // this warp's logit chains
+    const int gsh = a.group == 64 ? 1 : 0;          // 32-column tile -> group
     // a buffer's previous chunk must have been read before it is written again
     const int nb_shift = NBUF == 4 ? 2 : 1;  // NBUF is 2 or 4
     auto buffer_free = [&](int b) -> bool {
@@ -1510,13 +1567,14 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
                     acc[m][t] = 0.0f;
         }
         if (it.mode == MODE_GATEUP) {
-            consume<TCH>(stg, xcodes, xsc, xcr, a.d, a.d / G, rows, ng, k * SG, nt, warp, lane, acc);
+            consume<TCH>(stg, xcodes, xsc, xcr, a.d, a.d / G, a.d / a.group, gsh, rows, ng, k * SG, nt, warp, lane,
+                         acc);
         } else {
             const unsigned char *hb = s.hbuf + (size_t)cur_h * s.hb;
             const int8_t *hcodes = reinterpret_cast<const int8_t *>(hb);
             const float *hsc = reinterpret_cast<const float *>(hb + (size_t)TCH * a.fmax);
             const int *hcr = reinterpret_cast<const int *>(hsc + (size_t)TCH * a.hgs);
-            consume<TCH>(stg, hcodes, hsc, hcr, a.fmax, a.hgs, rows, ng, k * SG, nt, warp, lane, acc);
+            consume<TCH>(stg, hcodes, hsc, hcr, a.fmax, a.hgs, a.hgs, gsh, rows, ng, k * SG, nt, warp, lane, acc);
         }
         __syncwarp();
         if (lane == 0)

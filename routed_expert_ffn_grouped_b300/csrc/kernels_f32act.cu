@@ -80,9 +80,10 @@ __device__ __forceinline__ bool pair_expert(const F32Args &a, int p, colibri_exp
 }
 
 // Row block rb of two matrices (or one: wb == nullptr) against v: lane's row dots, summed
-// over the groups the warp takes (g = warp, warp + FW, ...), four groups in flight.
+// over the 32-column tiles the warp takes (g = warp, warp + FW, ...), four in flight. The
+// scale of tile g is the one of its group, g >> gsh (gsh = 1 for 64-element groups).
 __device__ __forceinline__ void rows_dot(const unsigned char *wa, const float *sa, const unsigned char *wb,
-                                         const float *sb, const float *v, int ng, int warp, int lane,
+                                         const float *sb, const float *v, int ng, int gsh, int warp, int lane,
                                          float &acc_a, float &acc_b)
 {
     wa += lane * 16;
@@ -99,10 +100,10 @@ __device__ __forceinline__ void rows_dot(const unsigned char *wa, const float *s
         for (int u = 0; u < 4; ++u) {
             const size_t gg = (size_t)(g + u * FW);
             qa[u] = ld_stream(wa + gg * 512);
-            ca[u] = __ldg(sa + gg * 32);
+            ca[u] = __ldg(sa + (gg >> gsh) * 32);
             if (wb) {
                 qb[u] = ld_stream(wb + gg * 512);
-                cb[u] = __ldg(sb + gg * 32);
+                cb[u] = __ldg(sb + (gg >> gsh) * 32);
             }
         }
 #pragma unroll
@@ -116,9 +117,9 @@ __device__ __forceinline__ void rows_dot(const unsigned char *wa, const float *s
     for (; g < ng; g += FW) {
         const size_t gg = (size_t)g;
         const float *vg = v + g * G;
-        acc_a = fmaf(__ldg(sa + gg * 32), dot_group(ld_stream(wa + gg * 512), vg), acc_a);
+        acc_a = fmaf(__ldg(sa + (gg >> gsh) * 32), dot_group(ld_stream(wa + gg * 512), vg), acc_a);
         if (wb)
-            acc_b = fmaf(__ldg(sb + gg * 32), dot_group(ld_stream(wb + gg * 512), vg), acc_b);
+            acc_b = fmaf(__ldg(sb + (gg >> gsh) * 32), dot_group(ld_stream(wb + gg * 512), vg), acc_b);
     }
 }
 
@@ -154,9 +155,9 @@ __global__ void __launch_bounds__(FW * 32) k_f32_gateup(F32Args a)
     stage_row(xs, a.x + (size_t)t * a.d, a.d);
     __syncthreads();
     const int ng = a.d / G;
-    const size_t tile0 = (size_t)rb * ng;
+    const size_t tile0 = (size_t)rb * ng, stile0 = (size_t)rb * (ng >> a.gsh);
     float gt = 0.0f, up = 0.0f;
-    rows_dot(ex.w1 + tile0 * 512, ex.s1 + tile0 * 32, ex.w3 + tile0 * 512, ex.s3 + tile0 * 32, xs, ng, warp,
+    rows_dot(ex.w1 + tile0 * 512, ex.s1 + stile0 * 32, ex.w3 + tile0 * 512, ex.s3 + stile0 * 32, xs, ng, a.gsh, warp,
              lane, gt, up);
     part[0][warp][lane] = gt;
     part[1][warp][lane] = up;
@@ -191,9 +192,9 @@ __global__ void __launch_bounds__(FW * 32) k_f32_down(F32Args a)
     stage_row(hsm, a.h + (size_t)p * a.fmax, f);
     __syncthreads();
     const int ng = f / G;
-    const size_t tile0 = (size_t)rb * ng;
+    const size_t tile0 = (size_t)rb * ng, stile0 = (size_t)rb * (ng >> a.gsh);
     float acc = 0.0f, unused = 0.0f;
-    rows_dot(ex.w2 + tile0 * 512, ex.s2 + tile0 * 32, nullptr, nullptr, hsm, ng, warp, lane, acc, unused);
+    rows_dot(ex.w2 + tile0 * 512, ex.s2 + stile0 * 32, nullptr, nullptr, hsm, ng, a.gsh, warp, lane, acc, unused);
     part[warp][lane] = acc;
     __syncthreads();
     if (warp == 0) {

@@ -160,7 +160,11 @@ struct GemmSmem {
     static constexpr int CONV = M * CA + CB + M * UMMA_M * 4 + GT_N * 4;
     static constexpr int BARS = 8 * (2 * GT_RR + 2 * GT_CQ + 2 * GT_TB) + 16;
     static constexpr int PRE = 4 * 1040;  // item prefix over at most 1025 slots
-    static constexpr int TOTAL = GT_RR * RAW + GT_CQ * CONV + BARS + PRE;
+    // 64-element groups: per item parity, epilogue warp and column, the |h| max of the
+    // warp's 32 rows; one mbarrier per pair of warps that share a 64-row group
+    static constexpr int XCH = 2 * 4 * GT_NEPI * 32;
+    static constexpr int XBARS = 8 * GT_NEPI / 2;
+    static constexpr int TOTAL = GT_RR * RAW + GT_CQ * CONV + BARS + PRE + XCH + XBARS;
 };
 
 template <int MODE>
@@ -178,6 +182,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + GT_TB);
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
     int *pre = reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(bars) + L::BARS);
+    float *xch = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(pre) + L::PRE);
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(reinterpret_cast<unsigned char *>(xch) + L::XCH);
+    const int gsh = a.group == 64 ? 1 : 0;  // 32-column tile -> group
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Counters ct = *a.counters;
     const int n_slots = ct.n_slots;
@@ -197,6 +204,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 mbar_init(&tm_full[i], 1);
                 mbar_init(&tm_empty[i], GT_NEPI);
             }
+            for (int i = 0; i < GT_NEPI / 2; ++i)
+                mbar_init(&xbar[i], 2);
             *abort_flag = 0;
             fence_mbar_init();
         }
@@ -254,16 +263,18 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                         break;
                     }
                     const int n = min(GT_GS, ng - g0);
+                    const int ns = n >> gsh;  // scale tiles (one per group)
                     unsigned char *dst = raw + (size_t)slot * L::RAW;
-                    mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)(M * 4 * n * (512 + 128)));
+                    mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)(M * 4 * (n * 512 + ns * 128)));
 #pragma unroll
                     for (int m = 0; m < M; ++m) {
                         const uint8_t *W = m == 0 ? (MODE == MODE_GATEUP ? it.ex.w1 : it.ex.w2) : it.ex.w3;
                         const float *S = m == 0 ? (MODE == MODE_GATEUP ? it.ex.s1 : it.ex.s2) : it.ex.s3;
                         for (int b = 0; b < 4; ++b) {
-                            const size_t tile = (size_t)(it.mt * 4 + b) * ng + g0;  // group tile index
+                            const size_t tile = (size_t)(it.mt * 4 + b) * ng + g0;  // 32-column tile index
+                            const size_t stile = (size_t)(it.mt * 4 + b) * (ng >> gsh) + (g0 >> gsh);
                             bulk_g2s(dst + m * L::RAW_W + b * GT_GS * 512, W + tile * 512, n * 512, &raw_full[slot]);
-                            bulk_g2s(dst + M * L::RAW_W + m * L::RAW_S + b * GT_GS * 128, S + tile * 32, n * 128,
+                            bulk_g2s(dst + M * L::RAW_W + m * L::RAW_S + b * GT_GS * 128, S + stile * 32, ns * 128,
                                      &raw_full[slot]);
                         }
                     }
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         v[h][q] = ld_nc(src + 8 * q);
-                    sv[h] = a.as[ck.arow[h] * a.act_groups + g];
+                    sv[h] = a.as[ck.arow[h] * a.act_groups + (g >> gsh)];
                 }
             }
         };
@@ -432,7 +443,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                             }
                             reinterpret_cast<float *>(cb + M * L::CA + L::CB)[m * UMMA_M + r] =
                                 *reinterpret_cast<const float *>(rb + M * L::RAW_W + m * L::RAW_S +
-                                                                 (blk * GT_GS + cw) * 128 + lane * 4);
+                                                                 (blk * GT_GS + (cw >> gsh)) * 128 + lane * 4);
                         }
                     }
                     // the token tile (zeros past the tile's tokens) and the tokens' scales
@@ -472,7 +483,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
         const int e = warp - GT_EPI0;
         const int q = warp & 3, chalf = e >> 2;  // TMEM lane quarter (rows), token half
         const int row = q * 32 + lane;             // row within the 128-row tile
-        uint32_t cs = 0, gcount = 0;
+        uint32_t cs = 0, gcount = 0, xitems = 0;
         bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             GemmItem it;
@@ -534,6 +545,41 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 break;
             // item output: columns chalf*32 + j < nt are tokens n0 + that of the slot
             const int orow = it.mt * UMMA_M + row;  // output row (h row or d row)
+            if (MODE == MODE_GATEUP) {
+                // h, then |h| max per column over the 32 rows of this warp; with 64-element
+                // groups the two warps holding rows 64p..64p+63 (TMEM lane quarters 2p and
+                // 2p + 1, same column half) exchange theirs (hardware barrier 2 + pair)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float gt = acc[0][j], up = acc[M - 1][j];
+                    acc[0][j] = gt / (1.0f + expf(-gt)) * up;
+                    const float m = warp_max(fabsf(acc[0][j]));
+                    if (gsh && lane == 0)
+                        xch[((int)(xitems & 1) * GT_NEPI + e) * 32 + j] = m;
+                    acc[M - 1][j] = m;
+                }
+                if (gsh) {
+                    // warps 6 + e pair up as (e, e ^ 1): TMEM lane quarters (2, 3) and (0, 1);
+                    // one bounded mbarrier phase per item, the exchange area double-buffered
+                    // by item parity (a warp writes buffer p again only after the partner
+                    // has arrived for the item in between, so after it read buffer p)
+                    const int partner = e ^ 1, buf = (int)(xitems & 1);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&xbar[e >> 1]);
+                    if (!mbar_wait(&xbar[e >> 1], xitems & 1)) {
+                        if (lane == 0)
+                            fail();
+                        ok = false;
+                        break;
+                    }
+                    ++xitems;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        acc[M - 1][j] = fmaxf(acc[M - 1][j], xch[(buf * GT_NEPI + partner) * 32 + j]);
+                }
+            }
+            const int gq = a.group;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const int col = chalf * 32 + j;
@@ -544,16 +590,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                     pr = it.is_shared ? (long)a.T * a.K + cidx : a.pairs[it.begin + cidx];
                 }
                 if (MODE == MODE_GATEUP) {
-                    const float gt = acc[0][j], up = acc[M - 1][j];
-                    const float h = gt / (1.0f + expf(-gt)) * up;
-                    const float amax = warp_max(fabsf(h));  // the 32 rows of one h group
+                    const float h = acc[0][j], amax = acc[M - 1][j];  // |h| max of the h group
                     const float dd = __fdiv_rn(amax, 127.0f);
-                    const int qv = q8_code(h, dd);
+                    const int qv = q8_code_r(h, dd, __frcp_rn(dd));
                     if (valid) {
                         const long hb = pr * a.fmax + (long)(orow & ~31);
                         a.hbf[hb + bf16_pos(lane)] = bf16_of_int(qv);
-                        if (lane == 0)
-                            a.hs[pr * (a.fmax / G) + orow / G] = dd;
+                        if (lane == 0 && (orow % gq) < 32)
+                            a.hs[pr * (a.fmax / gq) + orow / gq] = dd;
                     }
                 } else if (valid) {
                     a.y[pr * a.d + orow] = acc[0][j];

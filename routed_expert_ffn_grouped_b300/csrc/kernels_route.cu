@@ -4,9 +4,10 @@
 namespace clb {
 
 // ---- q8 ---------------------------------------------------------------------------
-// One warp per 32-element group, lane k holds element k. Writes the plain codes and
-// scales; optionally also the even/odd-ordered codes and the offset correction
-// 8 * sum(codes) the decode GEMV consumes.
+// One warp per group of a.group (32 or 64) elements, lane k holding element k (and
+// k + 32). Writes the plain codes and scales; optionally also the even/odd-ordered codes
+// and the offset correction 8 * sum(codes) per 32 elements that the decode GEMV consumes,
+// and the bf16 codes.
 __device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane);
 
 __global__ void __launch_bounds__(256) k_q8(Q8Args a)
@@ -14,7 +15,7 @@ __global__ void __launch_bounds__(256) k_q8(Q8Args a)
     grid_dep_launch();  // a decode expert kernel after this one may be scheduled now
     const int lane = threadIdx.x & 31;
     const long gw = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (gw >= a.rows * (a.cols / G))
+    if (gw >= a.rows * (a.cols / a.group))
         return;
     q8_group(a, gw, lane);
 }
@@ -30,24 +31,32 @@ __global__ void __launch_bounds__(256) k_q8(Q8Args a)
 // asks for it.
 __device__ __forceinline__ void q8_group(const Q8Args &a, long gw, int lane)
 {
-    const int ng = a.cols / G;
+    const int gq = a.group, ng = a.cols / gq, halves = gq / G;
     const long row = gw / ng;
     const int g = (int)(gw % ng);
-    const long base = row * a.cols + (long)g * G;
-    const float x = a.x[base + lane];
-    const float amax = warp_max(fabsf(x));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const int q = q8_code(x, d);
-    a.q[base + lane] = (int8_t)q;
+    const long base = row * a.cols + (long)g * gq;
+    float x[2];
+    float m = 0.0f;
+    for (int h = 0; h < halves; ++h) {
+        x[h] = a.x[base + h * G + lane];
+        m = fmaxf(m, fabsf(x[h]));
+    }
+    const float amax = warp_max(m);
+    const float d = __fdiv_rn(amax, 127.0f), rd = __frcp_rn(d);
     if (lane == 0)
         a.scale[row * ng + g] = d;
-    if (a.q_bf)
-        a.q_bf[base + bf16_pos(lane)] = bf16_of_int(q);
-    if (a.q_eo) {
-        a.q_eo[base + eo_pos(lane)] = (int8_t)q;
-        const int s = warp_sum_i(q);
-        if (lane == 0)
-            a.corr[row * ng + g] = 8 * s;
+    for (int h = 0; h < halves; ++h) {
+        const long b = base + h * G;
+        const int q = q8_code_r(x[h], d, rd);
+        a.q[b + lane] = (int8_t)q;
+        if (a.q_bf)
+            a.q_bf[b + bf16_pos(lane)] = bf16_of_int(q);
+        if (a.q_eo) {
+            a.q_eo[b + eo_pos(lane)] = (int8_t)q;
+            const int s = warp_sum_i(q);
+            if (lane == 0)
+                a.corr[row * (a.cols / G) + (long)g * halves + h] = 8 * s;
+        }
     }
 }
 
@@ -65,7 +74,7 @@ __device__ bool route_logits_part(const RouterArgs &a, unsigned char *smem_raw, 
     __syncthreads();
     // q8 side job: warp-granular, grid-strided over the T*d/32 groups of x
     if (a.q8.x) {
-        const long n = (long)a.T * (d / G);
+        const long n = (long)a.T * (d / a.q8.group);
         for (long gw = (long)blockIdx.x * nw + warp; gw < n; gw += (long)gridDim.x * nw)
             q8_group(a.q8, gw, lane);
     }

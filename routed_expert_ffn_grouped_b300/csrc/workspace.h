@@ -12,9 +12,11 @@ struct WsLayout {
     size_t err, counters, sync, qx, qx_eo, sx, xc, logits, s, c, offsets, pairs, slots;
     size_t hq, hq_eo, hs, hc, y;
     size_t xbf, hbf;  // prefill (T > DECODE_T_MAX): bf16 codes of x and of q8(h)
+    size_t hf;        // decode with 64-element groups: fp32 h rows before their q8
+    size_t hpair_count;  // decode with 64-element groups: pair counters in the sync region
     size_t nslots;      // slots at most: the shared expert + min(E, T*K) routed experts
     size_t sync_bytes;  // decode kernel's claim counter, routing counter, (two spare words) |
-                        // done_gu [nslots] | done_rb [d/32]
+                        // done_gu [nslots] | done_rb [d/32] | hpair [hpair_count]
     size_t fmax, total;
 };
 

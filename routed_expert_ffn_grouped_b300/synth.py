@@ -49,6 +49,7 @@ class LayerSpec:
     bias: str = "none"               # "none" | "normal" | "zipf"
     zipf_s: float = 1.1
     zipf_b0: float = 1.0
+    group: int = 32                  # quantisation group: 32 or 64 elements per scale
 
     def replace(self, **kw) -> "LayerSpec":
         return dataclasses.replace(self, **kw)
@@ -65,14 +66,20 @@ GLM52 = LayerSpec("glm52", d=6144, ffn=2048, n_exp=256, top_k=8, n_group=8, topk
 
 SPECS = {s.name: s for s in (TINY, OLMOE, GLM52)}
 
+# The same layers with the 64-element groups of the pages' int4 containers.
+TINY64 = TINY.replace(name="tiny_g64", group=64)
+OLMOE64 = OLMOE.replace(name="olmoe_g64", group=64)
+GLM52_64 = GLM52.replace(name="glm52_g64", group=64)
+SPECS.update({s.name: s for s in (TINY64, OLMOE64, GLM52_64)})
+
 
 @dataclass(frozen=True)
 class BlobLayout:
     """Byte offsets of one expert inside its blob: w1 | w3 | w2 | s1 | s3 | s2.
 
     Logical tensors: w1, w3 [f][d/2] packed nibbles (gate, up); w2 [d][f/2] (down);
-    s1, s3 [f][d/32] fp32; s2 [d][f/32] fp32. Each part starts on a 256-byte boundary and
-    is stored in row blocks (see ``pack_nibbles`` / ``pack_scales``).
+    s1, s3 [f][d/group] fp32; s2 [d][f/group] fp32. Each part starts on a 256-byte boundary
+    and is stored in row blocks (see ``pack_nibbles`` / ``pack_scales``).
     """
     d: int
     f: int
@@ -93,11 +100,11 @@ def _up(n: int) -> int:
     return (n + ALIGN - 1) // ALIGN * ALIGN
 
 
-def blob_layout(d: int, f: int) -> BlobLayout:
-    if d % GROUP or f % GROUP:
-        raise ValueError("d and f must be multiples of 32")
+def blob_layout(d: int, f: int, group: int = GROUP) -> BlobLayout:
+    if group not in (32, 64) or d % group or f % group:
+        raise ValueError("d and f must be multiples of the group (32 or 64)")
     sizes = [f * d // 2, f * d // 2, d * f // 2,
-             4 * f * (d // GROUP), 4 * f * (d // GROUP), 4 * d * (f // GROUP)]
+             4 * f * (d // group), 4 * f * (d // group), 4 * d * (f // group)]
     offs, o = [], 0
     for s in sizes:
         offs.append(o)
@@ -111,6 +118,9 @@ def blob_layout(d: int, f: int) -> BlobLayout:
 #     ((r // 32) * (K // 32) + g) * 512 + (r % 32) * 16 + j,
 # and byte j of a group holds column 32g+2j in its low nibble, 32g+2j+1 in its high nibble.
 # Scales S [R][K/32] follow the same order: S[r][g] at ((r // 32) * (K // 32) + g) * 32 + r % 32.
+# With 64-element groups the nibbles are stored the same way (a 64-group is two
+# consecutive 32-column tiles) and the scales S [R][K/64] at ((r // 32) * (K // 64) + g) * 32
+# + r % 32.
 ROW_BLOCK = 32
 
 
@@ -129,30 +139,30 @@ def unpack_nibbles(flat: np.ndarray, R: int, K: int) -> np.ndarray:
 
 
 def pack_scales(s: np.ndarray) -> np.ndarray:
-    """Logical scales [R][K/32] (fp32) -> stored order (flat fp32)."""
+    """Logical scales [R][K/group] (fp32) -> stored order (flat fp32)."""
     R, NG = s.shape
     assert R % ROW_BLOCK == 0
     return np.ascontiguousarray(s.reshape(R // ROW_BLOCK, ROW_BLOCK, NG).transpose(0, 2, 1)).reshape(-1)
 
 
-def unpack_scales(flat: np.ndarray, R: int, K: int) -> np.ndarray:
-    """Stored scales (flat fp32) -> logical [R][K/32]."""
-    NG = K // GROUP
+def unpack_scales(flat: np.ndarray, R: int, K: int, group: int = GROUP) -> np.ndarray:
+    """Stored scales (flat fp32) -> logical [R][K/group]."""
+    NG = K // group
     b = flat[:R * NG].reshape(R // ROW_BLOCK, NG, ROW_BLOCK)
     return np.ascontiguousarray(b.transpose(0, 2, 1)).reshape(R, NG)
 
 
-def _parts(d: int, f: int):
+def _parts(d: int, f: int, group: int = GROUP):
     """(name, offset, rows R, columns K) of the six parts of a blob."""
-    L = blob_layout(d, f)
+    L = blob_layout(d, f, group)
     return L, (("w1", L.w1, f, d), ("w3", L.w3, f, d), ("w2", L.w2, d, f),
                ("s1", L.s1, f, d), ("s3", L.s3, f, d), ("s2", L.s2, d, f))
 
 
-def expert_views(blob: np.ndarray, d: int, f: int) -> dict:
-    """The logical tensors of one expert blob (uint8, length blob_layout(d, f).nbytes):
-    w1, w3 [f][d/2], w2 [d][f/2] uint8 and s1, s3 [f][d/32], s2 [d][f/32] fp32 (copies)."""
-    L, parts = _parts(d, f)
+def expert_views(blob: np.ndarray, d: int, f: int, group: int = GROUP) -> dict:
+    """The logical tensors of one expert blob (uint8, length blob_layout(d, f, group).nbytes):
+    w1, w3 [f][d/2], w2 [d][f/2] uint8 and s1, s3 [f][d/group], s2 [d][f/group] fp32 (copies)."""
+    L, parts = _parts(d, f, group)
     b = blob.reshape(-1)
     assert b.dtype == np.uint8 and b.size >= L.nbytes
     out = {}
@@ -160,28 +170,28 @@ def expert_views(blob: np.ndarray, d: int, f: int) -> dict:
         if name[0] == "w":
             out[name] = unpack_nibbles(b[off:off + R * K // 2], R, K)
         else:
-            out[name] = unpack_scales(b[off:off + 4 * R * (K // GROUP)].view(np.float32), R, K)
+            out[name] = unpack_scales(b[off:off + 4 * R * (K // group)].view(np.float32), R, K, group)
     return out
 
 
-def write_expert(out: np.ndarray, d: int, f: int, tensors: dict) -> np.ndarray:
+def write_expert(out: np.ndarray, d: int, f: int, tensors: dict, group: int = GROUP) -> np.ndarray:
     """Store logical tensors (the keys of ``expert_views``) into a blob."""
-    L, parts = _parts(d, f)
+    L, parts = _parts(d, f, group)
     b = out.reshape(-1)
     b[:L.nbytes] = 0
     for name, off, R, K in parts:
         if name[0] == "w":
             b[off:off + R * K // 2] = pack_nibbles(np.asarray(tensors[name], np.uint8))
         else:
-            b[off:off + 4 * R * (K // GROUP)] = pack_scales(np.asarray(tensors[name], np.float32)).view(np.uint8)
+            b[off:off + 4 * R * (K // group)] = pack_scales(np.asarray(tensors[name], np.float32)).view(np.uint8)
     return out
 
 
 def fill_expert_blob(out: np.ndarray, d: int, f: int, seed: int, layer: int, expert: int,
-                     shared: bool = False) -> np.ndarray:
+                     shared: bool = False, group: int = GROUP) -> np.ndarray:
     """Draw one expert (uniform int4 codes, |N(0, 0.02)| scales) into ``out`` (uint8 blob).
     Codes and scales are i.i.d., so they are drawn straight into storage order."""
-    L, parts = _parts(d, f)
+    L, parts = _parts(d, f, group)
     rng = np.random.default_rng([seed, layer, expert, _TAG_SHARED if shared else _TAG_EXPERT])
     b = out.reshape(-1)
     b[:L.nbytes] = 0
@@ -190,7 +200,7 @@ def fill_expert_blob(out: np.ndarray, d: int, f: int, seed: int, layer: int, exp
             n = R * K // 2
             b[off:off + n] = np.frombuffer(rng.bytes(n), np.uint8)
         else:
-            n = R * (K // GROUP)
+            n = R * (K // group)
             s = np.abs(rng.standard_normal(n, dtype=np.float32)) * np.float32(0.02)
             b[off:off + 4 * n] = s.view(np.uint8)
     return out
@@ -198,8 +208,8 @@ def fill_expert_blob(out: np.ndarray, d: int, f: int, seed: int, layer: int, exp
 
 def expert_blob(spec: LayerSpec, seed: int, layer: int, expert: int, shared: bool = False) -> np.ndarray:
     f = spec.shared_ffn if shared else spec.ffn
-    blob = np.empty(blob_layout(spec.d, f).nbytes, np.uint8)
-    return fill_expert_blob(blob, spec.d, f, seed, layer, expert, shared)
+    blob = np.empty(blob_layout(spec.d, f, spec.group).nbytes, np.uint8)
+    return fill_expert_blob(blob, spec.d, f, seed, layer, expert, shared, spec.group)
 
 
 def router_weights(spec: LayerSpec, seed: int, layer: int = 0):
@@ -243,7 +253,7 @@ class Layer:
         """Logical tensors of routed expert e (unpacked once, then kept)."""
         memo = self.__dict__.setdefault("_views", {})
         if e not in memo:
-            memo[e] = expert_views(self.blobs[e], self.spec.d, self.spec.ffn)
+            memo[e] = expert_views(self.blobs[e], self.spec.d, self.spec.ffn, self.spec.group)
         return memo[e]
 
     def shared(self) -> dict | None:
@@ -251,17 +261,17 @@ class Layer:
             return None
         memo = self.__dict__.setdefault("_views", {})
         if "shared" not in memo:
-            memo["shared"] = expert_views(self.shared_blob, self.spec.d, self.spec.shared_ffn)
+            memo["shared"] = expert_views(self.shared_blob, self.spec.d, self.spec.shared_ffn, self.spec.group)
         return memo["shared"]
 
 
 def make_layer(spec: LayerSpec, seed: int, layer: int = 0, experts=None) -> Layer:
     """Draw a whole layer. ``experts`` limits which routed experts are drawn (others stay zero)."""
     Wr, bias = router_weights(spec, seed, layer)
-    nb = blob_layout(spec.d, spec.ffn).nbytes
+    nb = blob_layout(spec.d, spec.ffn, spec.group).nbytes
     blobs = np.zeros((spec.n_exp, nb), np.uint8)
     for e in (range(spec.n_exp) if experts is None else experts):
-        fill_expert_blob(blobs[e], spec.d, spec.ffn, seed, layer, e)
+        fill_expert_blob(blobs[e], spec.d, spec.ffn, seed, layer, e, group=spec.group)
     sh = expert_blob(spec, seed, layer, 0, shared=True) if spec.has_shared else None
     return Layer(spec, seed, Wr, bias, blobs, sh)
 

@@ -15,18 +15,20 @@ def ws_slice(ws, off, nbytes, dtype):
 U32 = 2.0 ** -24  # unit roundoff of fp32
 
 
-def h_error_bound(orc, v, qx, sx):
+def h_error_bound(orc, v, qx, sx, group=32):
     """[f]: a bound on the relative error of the kernel's fp32 h against the oracle's.
 
-    The kernel adds the d/32 exact group dots times their fp32 scale products in fp32 (in
-    any order), so its gate and up are within (d/32 + 8) u sum|terms| of the exact sums
-    (the oracle's fp64 sums are exact to far below that); relative to h that is the
-    sums' condition kappa = sum|terms| / |sum|, the gate's times the condition of silu
-    (1 + |z| sigmoid(-z)), plus a few u for expf, the division and the products."""
+    The kernel adds the d/32 exact 32-column dots times their fp32 scale products (the
+    scales of their group of 32 or 64) in fp32 (in any order), so its gate and up are
+    within (d/32 + 8) u sum|terms| of the exact sums (the oracle's fp64 sums are exact to
+    far below that); relative to h that is the sums' condition kappa = sum|terms| / |sum|,
+    the gate's times the condition of silu (1 + |z| sigmoid(-z)), plus a few u for expf,
+    the division and the products."""
     ng = qx.shape[0] // 32
-    sxg = sx.astype(np.float64)[None, :]
-    tg = v["s1"].astype(np.float64) * sxg * orc.group_dots(v["w1"], qx)
-    tu = v["s3"].astype(np.float64) * sxg * orc.group_dots(v["w3"], qx)
+    rep = group // 32
+    sxg = np.repeat(sx.astype(np.float64), rep)[None, :]
+    tg = np.repeat(v["s1"].astype(np.float64), rep, axis=1) * sxg * orc.group_dots(v["w1"], qx)
+    tu = np.repeat(v["s3"].astype(np.float64), rep, axis=1) * sxg * orc.group_dots(v["w3"], qx)
     gate, up = tg.sum(1), tu.sum(1)
     kg = np.abs(tg).sum(1) / np.maximum(np.abs(gate), 1e-300)
     ku = np.abs(tu).sum(1) / np.maximum(np.abs(up), 1e-300)
@@ -59,6 +61,7 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
     |W2| (dequantised) applied to |h_kernel - h_oracle| (dequantised). Where every code
     agrees that extra term is zero."""
     T, K, d = x.shape[0], spec.top_k, spec.d
+    gq = getattr(spec, "group", 32)
     tokens = list(range(T)) if tokens is None else [int(t) for t in tokens]
     v = C.colibri_moe_workspace_view(C.layer_cfg(spec), T)
     rows = T * K + (T if spec.has_shared else 0)
@@ -67,7 +70,7 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
     else:
         codes = ws_slice(ws, v.hq, rows * v.fmax, np.int8).reshape(rows, v.fmax).astype(np.int64)
     scales = ws_slice(ws, v.hs, 4 * rows * v.hs_stride, np.float32).reshape(rows, v.hs_stride)
-    qx, sx = orc.q8_quantize(x[tokens])
+    qx, sx = orc.q8_quantize(x[tokens], group=gq)
 
     def one(j):
         t = tokens[j]
@@ -77,17 +80,17 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
         if spec.has_shared:
             pairs.append((T * K + t, host.shared(), 1.0, spec.shared_ffn))
         for pr, view, wt, f in pairs:
-            _, qh, sh, h = orc.expert_token(view, qx[j], sx[j], want_h=True)
-            c, gsc = codes[pr, :f], scales[pr, :f // 32]
+            _, qh, sh, h = orc.expert_token(view, qx[j], sx[j], want_h=True, group=gq)
+            c, gsc = codes[pr, :f], scales[pr, :f // gq]
             dq = c - qh
             dsc = gsc.view(np.uint32) != sh.view(np.uint32)
             if not (dq.any() or dsc.any()):
                 continue
             assert np.abs(dq).max() <= 1, (t, pr)
-            relg = h_error_bound(orc, view, qx[j], sx[j]).reshape(-1, 32)
+            relg = h_error_bound(orc, view, qx[j], sx[j], gq).reshape(-1, gq)
             sh64 = sh.astype(np.float64)
             assert np.all(sh64 > 0), (t, pr)
-            r = np.abs(h.astype(np.float64)).reshape(-1, 32) / sh64[:, None]
+            r = np.abs(h.astype(np.float64)).reshape(-1, gq) / sh64[:, None]
             # the scale amax / 127 moves by at most the largest error of a |h| of the group
             rel_scale = (relg * r).max(1) / 127.0 + 2 * U32
             assert np.all(np.abs(gsc / sh64 - 1.0) <= rel_scale), (t, pr)
@@ -95,9 +98,9 @@ def check_h_codes_and_output(orc, C, spec, host, x, ids, w, ws, out, ref, tol=TO
             ambiguous = (np.abs(r - np.floor(r) - 0.5) <= window).ravel()
             assert np.all(ambiguous[dq != 0]), (t, pr, np.flatnonzero(dq)[:4])
             n_diff += int(np.count_nonzero(dq))
-            dh = np.abs(c * np.repeat(gsc.astype(np.float64), 32) - qh * np.repeat(sh64, 32))
+            dh = np.abs(c * np.repeat(gsc.astype(np.float64), gq) - qh * np.repeat(sh64, gq))
             w2 = np.abs(orc.unpack_int4(view["w2"]).astype(np.float64))
-            w2 *= np.repeat(view["s2"].astype(np.float64), 32, axis=1)
+            w2 *= np.repeat(view["s2"].astype(np.float64), gq, axis=1)
             allow += wt * (w2 @ dh)
         return allow, n_diff
 

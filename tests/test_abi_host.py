@@ -64,15 +64,35 @@ def test_workspace_bytes_and_config_checks(lib):
     bad = C.layer_cfg(synth.TINY.replace(n_group=3))
     assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0
     assert lib.colibri_moe_host_workspace_bytes(ctypes.byref(bad), 4) == 0
-    bad = C.layer_cfg(synth.TINY)
+    # 64-element groups are accepted; other group sizes, or shapes that are not multiples
+    # of the group, are not
+    g64 = C.layer_cfg(synth.TINY)
+    g64.group = 64
+    assert lib.colibri_moe_workspace_bytes(ctypes.byref(g64), 4) > 0
+    for group in (16, 48, 128, 0):
+        bad = C.layer_cfg(synth.TINY)
+        bad.group = group
+        assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0, group
+    bad = C.layer_cfg(synth.TINY.replace(d=96, ffn=64, shared_ffn=64))
+    assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) > 0          # fine at 32
     bad.group = 64
-    assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0
+    assert lib.colibri_moe_workspace_bytes(ctypes.byref(bad), 4) == 0         # d = 96 is not a multiple of 64
+    # the blob layout per group: same nibbles, half the scale bytes at 64
+    l32, l64 = C.colibri_blob_layout_for(512, 256), C.colibri_blob_layout_for(512, 256, 64)
+    assert (l64.w1, l64.w3, l64.w2, l64.s1) == (l32.w1, l32.w3, l32.w2, l32.s1)
+    assert l64.nbytes - l64.s1 == (l32.nbytes - l32.s1) // 2
+    lay = C.BlobLayout()
+    assert lib.colibri_blob_layout_for_g(96, 64, 64, ctypes.byref(lay)) == C.E_INVAL
+    assert lib.colibri_blob_layout_for_g(512, 256, 48, ctypes.byref(lay)) == C.E_INVAL
 
 
 def test_argument_errors_detected_on_host(lib):
     # Rejected before anything is enqueued: no device is touched.
     assert lib.colibri_q8_quantize(None, 1, 33, None, None, None) == C.E_INVAL
     assert lib.colibri_q8_quantize(None, 0, 64, None, None, None) == C.OK   # empty is a no-op
+    assert lib.colibri_q8_quantize_g(None, 1, 96, 64, None, None, None) == C.E_INVAL
+    assert lib.colibri_q8_quantize_g(None, 1, 128, 48, None, None, None) == C.E_INVAL
+    assert lib.colibri_q8_quantize_g(None, 0, 128, 64, None, None, None) == C.OK
     cfg = C.layer_cfg(synth.TINY)
     assert lib.colibri_moe_layer(ctypes.byref(cfg), None, 0, None, None, None, None, None, None, 0,
                                  None, None, 0, None) == C.OK
