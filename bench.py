@@ -51,6 +51,10 @@ WORKLOADS = {
     # the decode variant on fp32 activations (colibri_moe_layer_f32)
     "glm52_decode_t1_f32": ("glm52", 1, False),
     "glm52_decode_t4_f32": ("glm52", 4, False),
+    # the same GLM-shaped layer with the 64-element groups of the pages' int4 containers
+    "glm52_decode_t1_g64": ("glm52_g64", 1, False),
+    "glm52_decode_t4_g64": ("glm52_g64", 4, False),
+    "glm52_prefill_t2048_g64": ("glm52_g64", 2048, True),
 }
 DEFAULT_WORKLOAD = "glm52_decode_t1"
 N_X = 64                 # distinct activation batches cycled through
@@ -214,9 +218,10 @@ def weak_scaling_value(world: int, tokens_per_rank: int, steps: int, max_ms: flo
 
 
 def blob_bytes(spec, f):
-    L = synth.blob_layout(spec.d, f)
-    gate_up = 2 * (f * spec.d // 2) + 2 * 4 * f * (spec.d // 32)
-    down = spec.d * f // 2 + 4 * spec.d * (f // 32)
+    gq = getattr(spec, "group", 32)
+    L = synth.blob_layout(spec.d, f, gq)
+    gate_up = 2 * (f * spec.d // 2) + 2 * 4 * f * (spec.d // gq)
+    down = spec.d * f // 2 + 4 * spec.d * (f // gq)
     return L.nbytes, gate_up, down
 
 
@@ -269,7 +274,8 @@ def oracle_tokens_per_s(spec, host, xs, budget_s: float, max_tokens: int, act: s
     t0 = time.perf_counter()
     n = 0
     while n < max_tokens:
-        oracle.moe_layer(spec, xs[n % len(xs)], host.Wr, host.bias, host.expert, host.shared(), act=act)
+        oracle.moe_layer(spec, xs[n % len(xs)], host.Wr, host.bias, host.expert, host.shared(), act=act,
+                         group=getattr(spec, "group", 32))
         n += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -292,17 +298,18 @@ def run_reference(args):
     per_tok = spec.top_k + (1 if spec.has_shared else 0)
     state = {"tok": -1}
     f32 = is_f32(args.workload)
+    gq = getattr(spec, "group", 32)
 
     def expert(views):
         if f32:
             return oracle.expert_token_f32(views, state["x"])[0]
-        return oracle.expert_token(views, state["q"], state["s"])[0]
+        return oracle.expert_token(views, state["q"], state["s"], group=gq)[0]
 
     def step(i):
         t, slot = divmod(i, per_tok)
         x = xs[t % N_X]
         if slot == 0 or state["tok"] != t:
-            q, s = oracle.q8_quantize(x)
+            q, s = oracle.q8_quantize(x, group=gq)
             ids, w = oracle.router_topk(spec, x[None], host.Wr, host.bias)
             state.update(tok=t, x=x, q=q, s=s, ids=ids[0], w=w[0], acc=np.zeros(spec.d))
         if spec.has_shared and slot == per_tok - 1:
@@ -353,7 +360,8 @@ def workload_config(spec, workload, T):
                    "one call of the layer before (same shape, its own weights at other addresses): "
                    "code and small tables warm, none of this layer's weights, router or shared expert in L2"),
             "timing": "CUDA events per step around one CUDA-graph replay",
-            "activations": "fp32" if is_f32(workload) else "int8 (per-32-group absmax)"}
+            "group": getattr(spec, "group", 32),
+            "activations": "fp32" if is_f32(workload) else f"int8 (per-{getattr(spec, 'group', 32)}-group absmax)"}
 
 
 # ---------------------------------------------------------------- expert streaming

@@ -86,7 +86,9 @@ def test_launch_counts_and_workload_tags():
         from routed_expert_ffn_grouped_b300 import synth
         cfg = bench.workload_config(synth.SPECS[spec_name], name, T)
         assert cfg["workload"] == name
-        assert cfg["activations"] == ("fp32" if name.endswith("_f32") else "int8 (per-32-group absmax)")
+        gq = 64 if name.endswith("_g64") else 32
+        assert cfg["group"] == gq
+        assert cfg["activations"] == ("fp32" if name.endswith("_f32") else f"int8 (per-{gq}-group absmax)")
         if name.endswith("_f32"):
             assert T <= bench.DECODE_T_MAX     # the fp32-activation variant is decode only
 
