@@ -710,7 +710,9 @@ def run_colibri(args):
     out_pin = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
     ws_host = None if f32 else torch.empty(C.colibri_moe_host_workspace_bytes(dl.cfg, T), dtype=torch.uint8,
                                            device="cuda")
-    KE = min(K, 500)
+    # at least 200 timed calls (whatever --steps is) after 50 warm-up calls: a host-side
+    # figure needs more samples than the device-timed steps to be stable
+    KE = min(max(K, 200), 500)
     e2e_s = 0.0
 
     def e2e_call(i):
@@ -724,7 +726,7 @@ def run_colibri(args):
                                      False, out_pin, ws_host, stream=stream)
 
     with torch.cuda.stream(stream):
-        for i in range(max(W, 3)):               # untimed warm-up calls of the same entry point
+        for i in range(max(W, 50)):              # untimed warm-up calls of the same entry point
             e2e_call(i)
         stream.synchronize()
         for i in range(KE):

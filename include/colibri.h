@@ -229,7 +229,8 @@ int colibri_moe_layer_f32(const colibri_layer_cfg *cfg, const float *x, int T, c
  * On `stream` it copies x (and ids, w when ids_given) from host memory into a region at
  * the end of the workspace, runs colibri_moe_layer on those device copies, copies out
  * (and ids, w when routed here and the pointers are non-NULL) and the device error flag
- * back, and waits for the stream. Host buffers may be pinned (cudaHostAlloc or
+ * (into a page-locked word of the calling thread, allocated on its first call) back, and
+ * waits for the stream. Host buffers may be pinned (cudaHostAlloc or
  * cudaHostRegister: the copies then run at PCIe speed without staging) or pageable
  * (correct, slower).
  *   x         host fp32 [T][d]

@@ -12,6 +12,19 @@
 
 namespace {
 
+// A page-locked word per host thread for the device error flag, so that its copy back is
+// an ordinary asynchronous copy on the stream (allocated on the thread's first call, kept
+// until the thread exits).
+struct PinnedFlag {
+    int *p = nullptr;
+    ~PinnedFlag()
+    {
+        if (p)
+            cudaFreeHost(p);
+    }
+};
+thread_local PinnedFlag t_flag;
+
 size_t up256(size_t n)
 {
     return (n + 255) & ~size_t(255);
@@ -89,7 +102,12 @@ extern "C" int colibri_moe_layer_host(const colibri_layer_cfg *cfg, const float 
         cudaStreamSynchronize(s);
         return st;
     }
-    int flag = 0;
+    int stack_flag = 0;
+    if (!t_flag.p && cudaHostAlloc(reinterpret_cast<void **>(&t_flag.p), sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+        (void)cudaGetLastError();
+        t_flag.p = nullptr;
+    }
+    int *flag = t_flag.p ? t_flag.p : &stack_flag;
     const size_t err_off = clb::ws_layout(cfg, T).err;
     if (cudaMemcpyAsync(out, dout, xb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         st = COLIBRI_E_CUDA;
@@ -99,11 +117,11 @@ extern "C" int colibri_moe_layer_host(const colibri_layer_cfg *cfg, const float 
     if (st == COLIBRI_OK && !ids_given && w && cudaMemcpyAsync(w, dw, kb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         st = COLIBRI_E_CUDA;
     if (st == COLIBRI_OK &&
-        cudaMemcpyAsync(&flag, ws + err_off, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        cudaMemcpyAsync(flag, ws + err_off, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
         st = COLIBRI_E_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess)
         return COLIBRI_E_CUDA;
     if (st != COLIBRI_OK)
         return st;
-    return flag ? COLIBRI_E_DEVICE : COLIBRI_OK;
+    return *flag ? COLIBRI_E_DEVICE : COLIBRI_OK;
 }

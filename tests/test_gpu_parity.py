@@ -449,6 +449,39 @@ def test_moe_layer_host_entry(torch_cuda, C, orc, name, T, pinned):
     assert_rms_close(out, ref)
 
 
+def test_moe_layer_host_entry_repeated_pinned_calls(torch_cuda, C, orc):
+    """Back-to-back calls on fresh page-locked buffers give the device entry's bits each
+    time; a bad id reports the device status through the page-locked flag word, and the
+    next good call is clean."""
+    torch = torch_cuda
+    spec = synth.TINY
+    host, dl = dev_layer(C, spec)
+    T = 3
+    ws = torch.empty(C.colibri_moe_host_workspace_bytes(dl.cfg, T), dtype=torch.uint8, device="cuda")
+    for step in range(4):
+        x = synth.activations(spec, 1, T, step=50 + step)
+        out_dev, ids_dev, w_dev, _ = run_layer(torch, C, dl, x)
+        xh = torch.from_numpy(x).pin_memory()                   # a fresh buffer every call
+        out = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
+        ids = torch.empty((T, spec.top_k), dtype=torch.int32).pin_memory()
+        w = torch.empty((T, spec.top_k), dtype=torch.float32).pin_memory()
+        C.colibri_moe_layer_host(dl.cfg, xh, dl.Wr, dl.bias, dl.table, dl.shared, ids, w, False, out, ws)
+        assert np.array_equal(out.numpy().view(np.uint32), out_dev.view(np.uint32)), step
+        assert np.array_equal(ids.numpy(), ids_dev) and np.array_equal(w.numpy().view(np.uint32), w_dev.view(np.uint32))
+    # ids given, pinned, one id out of range: the status comes back through the graph
+    gid = torch.from_numpy(np.array([[0, 1, 2, 3], [4, 5, 6, 7], [8, 9, 10, spec.n_exp]], np.int32)).pin_memory()
+    gw = torch.full((T, spec.top_k), 0.25, dtype=torch.float32).pin_memory()
+    xh = torch.from_numpy(synth.activations(spec, 2, T)).pin_memory()
+    out = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
+    with pytest.raises(C.ColibriError) as e:
+        C.colibri_moe_layer_host(dl.cfg, xh, None, None, dl.table, dl.shared, gid, gw, True, out, ws)
+    assert e.value.status == C.E_DEVICE
+    gid[2, 3] = 11
+    C.colibri_moe_layer_host(dl.cfg, xh, None, None, dl.table, dl.shared, gid, gw, True, out, ws)
+    ref, _, _ = orc.moe_layer(spec, xh.numpy(), None, None, host.expert, host.shared(), ids=gid.numpy(), w=gw.numpy())
+    assert_rms_close(out.numpy(), ref)
+
+
 def test_moe_layer_host_entry_ids_given_and_errors(torch_cuda, C, orc):
     torch = torch_cuda
     spec = synth.TINY
