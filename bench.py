@@ -283,6 +283,34 @@ def oracle_tokens_per_s(spec, host, xs, budget_s: float, max_tokens: int, act: s
     return n / dt, n, dt
 
 
+def oracle_tokens_per_s_all_cores(spec, host, xs, budget_s: float, act: str = "q8"):
+    """The oracle as it stands on every host core: one token per call, as many calls in
+    flight as the host has logical cores (host threads; the oracle's C calls release the
+    GIL, and tokens are independent). Returns (tokens/s, tokens, seconds, threads)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    oracle.lib()
+    threads = max(1, os.cpu_count() or 1)
+    gq = getattr(spec, "group", 32)
+    stop = time.perf_counter() + budget_s
+    counts = [0] * threads
+
+    def worker(k):
+        i = k
+        while time.perf_counter() < stop:
+            x = xs[i % len(xs)]
+            oracle.moe_layer(spec, x[None] if x.ndim == 1 else x[:1], host.Wr, host.bias, host.expert,
+                             host.shared(), act=act, group=gq)
+            counts[k] += 1
+            i += threads
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(worker, range(threads)))
+    dt = time.perf_counter() - t0
+    n = sum(counts)
+    return n / dt, n, dt, threads
+
+
 def run_reference(args):
     """The oracle on the host cores, step = one expert pass of one token."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -741,6 +769,7 @@ def run_colibri(args):
     e2e_value = world * T * KE / e2e_s
 
     cpu = None
+    cpu_all = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # batches of at most 8 of the workload's tokens: the oracle's work per token does
         # not depend on the batch, and a 2048-token batch would run for minutes
@@ -750,6 +779,14 @@ def run_colibri(args):
         cpu = {"value": rate * tb, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{n} batches of {tb} tokens of {args.workload} through the C oracle "
                          f"({dt:.1f} s, single-threaded)"}
+        if prefill:
+            # prefill is minutes of oracle work per batch single-threaded: also the oracle
+            # on every host core (informational, beside the single-core baseline)
+            rate_a, n_a, dt_a, thr = oracle_tokens_per_s_all_cores(
+                spec, host, [xs_host[i][:1] for i in range(N_X)], 15.0, act="f32" if f32 else "q8")
+            cpu_all = {"value": rate_a, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                       "sample": f"{n_a} tokens of {args.workload}, one token per oracle call, {thr} host "
+                                 f"threads ({dt_a:.1f} s)"}
 
     if rank == 0:
         line = {
@@ -770,6 +807,7 @@ def run_colibri(args):
             "no_l2_flush": {"value": world * T / (nf_ms / 1e3), "ms_per_step": nf_ms, "steps": KB,
                             "note": "informational; the headline value flushes L2 between steps"},
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * spec.d * 4,
                     "d2h_bytes_per_step": T * spec.d * 4 + (0 if f32 else 4), "steps": KE,
                     "path": ("colibri_moe_layer_f32 between pinned-host copies of x and out, eager launches"

@@ -518,11 +518,12 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     return COLIBRI_OK;
 }
 
-// Workspace of colibri_moe_layer_f32: error flag | logits [T][E] | h [PT][fmax] |
-// y [PT][d], PT = T*K (+ T with a shared expert), each part 256-byte aligned. The error
-// flag sits at offset 0, as in colibri_moe_layer's workspace.
+// Workspace of colibri_moe_layer_f32: error flag | logits [T][E] | sigmoid scores s and
+// biased scores c [T][E] | h [PT][fmax] | y [PT][d], PT = T*K (+ T with a shared expert),
+// each part 256-byte aligned. The error flag sits at offset 0, as in colibri_moe_layer's
+// workspace.
 struct F32Layout {
-    size_t err, logits, h, y, fmax, pt, total;
+    size_t err, logits, s, c, h, y, fmax, pt, total;
 };
 
 static F32Layout f32_layout(const colibri_layer_cfg *c, int T)
@@ -538,6 +539,8 @@ static F32Layout f32_layout(const colibri_layer_cfg *c, int T)
     };
     L.err = take(256);
     L.logits = take(4 * (size_t)T * c->n_exp);
+    L.s = take(4 * (size_t)T * c->n_exp);
+    L.c = take(4 * (size_t)T * c->n_exp);
     L.h = take(4 * L.pt * L.fmax);
     L.y = take(4 * L.pt * c->d);
     L.total = o;
@@ -581,10 +584,13 @@ int colibri_moe_layer_f32(const colibri_layer_cfg *cfg, const float *x, int T, c
     if (prof_mark(0, s) || prof_mark(1, s))
         return COLIBRI_E_CUDA;
     if (!ids_given) {
+        // the logits kernel evaluates the sigmoid scores (spread over its CTAs) and hands
+        // them to the selection, as on the int8 path
         const Q8Args none{};
-        if (launch_route_logits(cfg, x, T, Wr, bias, lg, nullptr, nullptr, none, err, s) || prof_mark(2, s))
+        float *sv = reinterpret_cast<float *>(ws + L.s), *cv = reinterpret_cast<float *>(ws + L.c);
+        if (launch_route_logits(cfg, x, T, Wr, bias, lg, sv, cv, none, err, s) || prof_mark(2, s))
             return COLIBRI_E_CUDA;
-        if (launch_select(select_args(cfg, T, lg, nullptr, nullptr, bias, ids, w), s) || prof_mark(3, s))
+        if (launch_select(select_args(cfg, T, lg, sv, cv, bias, ids, w), s) || prof_mark(3, s))
             return COLIBRI_E_CUDA;
     } else if (prof_mark(2, s) || prof_mark(3, s)) {
         return COLIBRI_E_CUDA;
