@@ -55,7 +55,11 @@ WORKLOADS = {
     "glm52_decode_t1_g64": ("glm52_g64", 1, False),
     "glm52_decode_t4_g64": ("glm52_g64", 4, False),
     "glm52_prefill_t2048_g64": ("glm52_g64", 2048, True),
+    # eight resident GLM-shaped layers in one launch (colibri_moe_stack_decode)
+    "glm52_decode_t1_stack8": ("glm52", 1, False),
+    "glm52_decode_t4_stack8": ("glm52", 4, False),
 }
+STACK_LAYERS = 8
 DEFAULT_WORKLOAD = "glm52_decode_t1"
 N_X = 64                 # distinct activation batches cycled through
 L2_FLUSH_BYTES = 256 << 20
@@ -80,6 +84,14 @@ def parse():
     p.add_argument("--predictor", default="previous", choices=["previous", "lookahead"],
                    help="expert streaming: next-layer prefetch from an emulated router lookahead "
                         "that names each true id with probability 0.716, or the previous step's ids")
+    p.add_argument("--prefetch-chunk-mb", type=float, default=1.0,
+                   help="expert streaming: prefetch chunk size (queued, cancellable prefetch); "
+                        "0: whole-blob prefetch copies enqueued at once")
+    p.add_argument("--prefetch-inflight", type=int, default=2,
+                   help="expert streaming: prefetch chunks (or whole blobs) in flight at most")
+    p.add_argument("--ids-ahead", action="store_true",
+                   help="expert streaming: the host knows every layer's ids before the step starts "
+                        "(no wait for the previous layer before a lookup)")
     return p.parse_args()
 
 
@@ -447,13 +459,55 @@ def run_cache_sim(args):
     print(json.dumps(line), flush=True)
 
 
+def interval_union(iv) -> float:
+    """Total length of the union of intervals [a, b)."""
+    tot, end = 0.0, float("-inf")
+    for a, b in sorted(iv):
+        if b <= end:
+            continue
+        tot += b - max(a, end)
+        end = b
+    return tot
+
+
+def overlap_stats(copy_iv, compute_iv, window: float) -> dict:
+    """Busy fractions of a window from the copy and compute intervals, and the share of
+    copy time that ran beside compute (|A and B| = |A| + |B| - |A or B|)."""
+    cu, pu = interval_union(copy_iv), interval_union(compute_iv)
+    au = interval_union(list(copy_iv) + list(compute_iv))
+    both = cu + pu - au
+    return {"copy_busy_frac": cu / window, "compute_busy_frac": pu / window,
+            "overlap_frac_of_copy": both / cu if cu > 0 else None, "idle_frac": 1.0 - au / window}
+
+
+def h2d_peak_gbs(torch, src, dst, reps: int = 4) -> float:
+    """Pinned host -> HBM copy rate of one large cudaMemcpyAsync, timed with CUDA events
+    on its own stream (src pinned, dst on the device, both flat uint8)."""
+    n = min(src.numel(), dst.numel())
+    s = torch.cuda.Stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        dst[:n].copy_(src[:n], non_blocking=True)
+        e0.record(s)
+        for _ in range(reps):
+            dst[:n].copy_(src[:n], non_blocking=True)
+        e1.record(s)
+    s.synchronize()
+    return n * reps / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+
 def run_stream(args):
     """Decode T=1 through a stack of GLM-5.2-shaped layers whose routed experts live in
     pinned host memory (2048 blobs, ~48 GB) behind an HBM LRU cache of 512 slots
-    (~12 GB); routing keeps each id from the previous step with probability 0.7; before
-    each layer the next layer's experts are prefetched as predicted by the previous
-    step's ids. The shared experts stay resident. A step is one token through all
-    layers; the timed region includes the host's cache decisions."""
+    (~12 GB); routing keeps each id from the previous step with probability 0.7. A layer's
+    ids reach the host only once the previous layer has finished (the host waits on the
+    compute stream, as a host-side cache must), unless --ids-ahead. Before each layer the
+    next layer's experts are prefetched as predicted (previous step's ids, or an emulated
+    router lookahead), as a queue of chunks that the host enqueues while it waits and that
+    the next lookup finishes or cancels. The shared experts stay resident. A step is one
+    token through all layers; the timed region includes the host's cache decisions. An
+    instrumented pass after the timed one records CUDA events on the demand copy stream,
+    the prefetch stream and the compute stream for the overlap figures."""
     import ctypes
     import torch
     from routed_expert_ffn_grouped_b300 import build as cbuild
@@ -484,12 +538,18 @@ def run_stream(args):
                        b.data_ptr() + sl.s1, b.data_ptr() + sl.s3, b.data_ptr() + sl.s2) for b in shared_dev]
     tables = (L_ * E * ctypes.sizeof(C.Expert) + 255) // 256 * 256
     pool = torch.empty(tables + STREAM_SLOTS * nb, dtype=torch.uint8, device="cuda")
+    peak_n = min(2 << 30, STREAM_SLOTS * nb)
+    h2d_peak = h2d_peak_gbs(torch, pinned.view(-1)[:peak_n], pool[tables:tables + peak_n])
     copy = torch.cuda.Stream()
+    pcopy = torch.cuda.Stream()
     stream = torch.cuda.Stream()
     cache = C.ExpertCache(pool, pinned, L_, E, spec.d, spec.ffn, spec.top_k, copy)
+    chunk = int(args.prefetch_chunk_mb * (1 << 20)) // 256 * 256
+    cache.set_prefetch(pcopy, args.prefetch_inflight, chunk)
     if args.hot_slots:
         cache.set_hot(args.hot_slots)
-    ids_np, w_np = synth.streaming_ids(spec, args.seed, L_, W + K + 1)
+    K2 = min(K, 24)                                 # instrumented steps after the timed ones
+    ids_np, w_np = synth.streaming_ids(spec, args.seed, L_, W + K + K2 + 1)
     # emulated router lookahead: each id of the next layer is named correctly with the
     # pages' stated predictability (71.6%), else replaced by a popular-looking wrong id
     prng = np.random.default_rng([args.seed, 99])
@@ -503,16 +563,36 @@ def run_stream(args):
     out = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
     ws = torch.empty(C.colibri_moe_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
 
-    def step(s):
+    def ev(q):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(q)
+        return e
+
+    def step(s, rec=None):
         for l in range(L_):
+            if not args.ids_ahead:
+                # layer l's ids exist once layer l-1 has run; prefetch chunks go out meanwhile
+                p0 = ev(pcopy) if rec is not None else None
+                cache.wait(stream, 60000)
+                if rec is not None:
+                    rec["copy"].append((p0, ev(pcopy)))
+            d0 = ev(copy) if rec is not None else None
             cache.lookup(l, ids_np[s, l], wait_on=stream)
+            if rec is not None:
+                rec["copy"].append((d0, ev(copy)))
             nl, ns = (l + 1, s) if l + 1 < L_ else (0, s + 1)
+            s0 = ev(pcopy) if rec is not None else None
             if args.predictor == "lookahead":
                 cache.stage(nl, np.unique(guess[ns, nl]))   # next-layer prefetch, predicted
             elif ns - 1 >= 0:
                 cache.stage(nl, ids_np[ns - 1, nl])         # the previous step's ids
+            if rec is not None:
+                rec["copy"].append((s0, ev(pcopy)))         # whole-blob prefetches, if any
+            c0 = ev(stream) if rec is not None else None
             C.colibri_moe_layer(cfg, xs[(s * L_ + l) % 16], None, None, cache.table(l), shared[l],
                                 ids[s, l].view(1, -1), w[s, l].view(1, -1), True, out, ws, stream=stream)
+            if rec is not None:
+                rec["compute"].append((c0, ev(stream)))
 
     for s in range(W):
         step(s)
@@ -535,6 +615,22 @@ def run_stream(args):
     st1 = cache.stats()
     d = {k: st1[k] - st0[k] for k in st1 if k != "n_slots"}
     value = world * T * K / (ms / 1e3)
+    # instrumented pass: events on the three streams (not part of the timed value)
+    rec = {"copy": [], "compute": []}
+    cache.sync(60000)
+    torch.cuda.synchronize()
+    base = ev(stream)
+    for s in range(W + K, W + K + K2):
+        step(s, rec)
+    end = ev(stream)
+    torch.cuda.synchronize()
+    cache.sync(60000)
+    rel = lambda pairs: [(base.elapsed_time(a), base.elapsed_time(b)) for a, b in pairs]
+    overlap = overlap_stats(rel(rec["copy"]), rel(rec["compute"]), base.elapsed_time(end))
+    overlap["steps"] = K2
+    overlap["how"] = ("CUDA events on the demand copy stream around each lookup, on the prefetch stream "
+                      "around each host wait and each prefetch call, on the compute stream around each "
+                      "layer call")
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
@@ -545,16 +641,22 @@ def run_stream(args):
                        "hbm_slots": STREAM_SLOTS, "hot_slots": args.hot_slots, "reuse": 0.7,
                        "prefetch": ("next layer's ids from an emulated lookahead, 71.6% correct"
                                     if args.predictor == "lookahead" else "previous step's ids of the next layer"),
+                       "prefetch_chunk_bytes": chunk, "prefetch_inflight": args.prefetch_inflight,
+                       "host_waits_for_previous_layer": not args.ids_ahead,
                        "timing": "CUDA events around K steps on the compute stream; host cache decisions inside"},
             "cache": {"hit_rate": d["hits"] / max(1, d["lookups"]), "lookups": d["lookups"],
                       "misses": d["misses"], "prefetch_staged": d["prefetch_staged"],
-                      "prefetch_used": d["prefetch_used"],
+                      "prefetch_used": d["prefetch_used"], "prefetch_cancelled": d["prefetch_cancelled"],
                       "prefetch_accuracy": d["prefetch_used"] / max(1, d["prefetch_staged"]),
-                      "bytes_staged": d["bytes_staged"],
-                      "pcie_gbs": d["bytes_staged"] / (ms / 1e3) / 1e9},
+                      "bytes_staged": d["bytes_staged"], "prefetch_bytes": d["prefetch_bytes"],
+                      "pcie_gbs": d["bytes_staged"] / (ms / 1e3) / 1e9,
+                      "h2d_peak_gbs": h2d_peak,
+                      "staging_frac_of_peak": d["bytes_staged"] / (ms / 1e3) / 1e9 / h2d_peak},
+            "overlap": overlap,
             "wall_s": wall, "generate_s": gen_s,
-            # two per layer call (ids given) + one table-entry write per staged blob
-            "gpu_launches": K * L_ * launches_per_step(T, E, True) + d["misses"] + d["prefetch_staged"],
+            # one per layer call (ids given) + one table-entry write per blob staged to the end
+            "gpu_launches": K * L_ * launches_per_step(T, E, True) + d["misses"]
+                            + d["prefetch_staged"] - d["prefetch_cancelled"],
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -824,12 +926,135 @@ def run_colibri(args):
         dist.destroy_process_group()
 
 
+def run_stack_decode(args):
+    """Eight resident GLM-shaped layers per step, each with activations of its own (as when
+    attention sits between a model's MoE layers; a bare chain of SwiGLU layers, out into x,
+    overflows within a few layers): one colibri_moe_stack_decode launch, timed with CUDA
+    events around a graph replay, beside the same eight layers as eight colibri_moe_layer
+    calls in one graph. The layers are one drawn layer and device copies of it whose
+    router rows are rolled (each routes elsewhere, and their weights sit at other
+    addresses); 8 x 6 GB of weights keep every step's bytes far above the L2."""
+    import torch
+    from routed_expert_ffn_grouped_b300 import build as cbuild
+    from routed_expert_ffn_grouped_b300 import colibri as C
+
+    world, rank, local = dist_setup(torch)
+    if rank == 0 or not os.path.exists(C.LIB_PATH):
+        cbuild.build()
+    barrier(torch, world)
+    name, T, _ = WORKLOADS[args.workload]
+    spec = synth.SPECS[name]
+    L_ = STACK_LAYERS
+    base = C.DeviceLayer(synth.make_layer(spec, args.seed))
+    layers = [base] + [C.DeviceLayer.twin(base, shift=(spec.n_exp // L_) * l + 1) for l in range(1, L_)]
+    stream = torch.cuda.Stream()
+    xs = torch.from_numpy(np.stack([synth.activations(spec, args.seed, T, step=i) for i in range(N_X)])).cuda()
+    xl = [torch.empty((T, spec.d), dtype=torch.float32, device="cuda") for _ in range(L_)]
+    x = xl[0]
+    outs = [torch.empty((T, spec.d), dtype=torch.float32, device="cuda") for _ in range(L_)]
+    ids = [torch.empty((T, spec.top_k), dtype=torch.int32, device="cuda") for _ in range(L_)]
+    w = [torch.empty((T, spec.top_k), dtype=torch.float32, device="cuda") for _ in range(L_)]
+    cfg = base.cfg
+    ws_stack = torch.empty(C.colibri_moe_stack_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(C.colibri_moe_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+    st = [dict(x=xl[l], Wr=dl.Wr, bias=dl.bias, experts=dl.table, shared=dl.shared, ids=ids[l], w=w[l],
+               out=outs[l]) for l, dl in enumerate(layers)]
+
+    def stacked():
+        C.colibri_moe_stack_decode(cfg, x, st, False, ws_stack, stream=torch.cuda.current_stream())
+
+    def sequential():
+        for l, dl in enumerate(layers):
+            C.colibri_moe_layer(cfg, xl[l], dl.Wr, dl.bias, dl.table, dl.shared, ids[l], w[l], False, outs[l], ws,
+                                stream=torch.cuda.current_stream())
+
+    def fill(i):
+        for l in range(L_):
+            xl[l].copy_(xs[(i + l) % N_X])
+
+    with torch.cuda.stream(stream):
+        fill(0)
+        stacked()
+        stream.synchronize()
+        if C.colibri_workspace_status(cfg, T, ws_stack, stream=stream) != C.OK:
+            raise RuntimeError("layer stack reported a device error")
+    graphs = {}
+    for key, fn in (("stack", stacked), ("sequential", sequential)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs[key] = g
+    K, W = args.steps, args.warmup
+    ids_log = torch.empty((K, L_, T, spec.top_k), dtype=torch.int32, device="cuda")
+
+    def timed(g, log):
+        with torch.cuda.stream(stream):
+            for i in range(W):
+                fill(i)
+                g.replay()
+        torch.cuda.synchronize()
+        s_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                fill(W + i)
+                s_ev[i].record(stream)
+                g.replay()
+                e_ev[i].record(stream)
+                if log:
+                    for l in range(L_):
+                        ids_log[i, l].copy_(ids[l])
+            torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in zip(s_ev, e_ev)]
+
+    barrier(torch, world)
+    sampler = ClockSampler(torch, local)
+    with sampler:
+        step_ms = timed(graphs["stack"], True)
+    total_ms = allreduce_max(torch, world, float(sum(step_ms)))
+    seq_ms = timed(graphs["sequential"], False)
+    if (C.colibri_workspace_status(cfg, T, ws_stack, stream=stream) != C.OK or
+            C.colibri_workspace_status(cfg, T, ws, stream=stream) != C.OK):
+        raise RuntimeError("a layer reported a device error")
+    value = weak_scaling_value(world, T * L_, K, total_ms)
+    nb, _, _ = blob_bytes(spec, spec.ffn)
+    sh = blob_bytes(spec, spec.shared_ffn)[0] if spec.has_shared else 0
+    ids_np = ids_log.cpu().numpy()
+    step_bytes = np.array([sum(len(np.unique(ids_np[i, l])) * nb + sh for l in range(L_)) for i in range(K)])
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved = float(np.sum(step_bytes) / (sum(step_ms) / 1e3) / 1e9)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s (layer-tokens: tokens x layers)",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "i8xi4->i32, f32", "data": "synthetic",
+            "config": dict(workload_config(spec, args.workload, T), layers=L_, inputs="each layer its own activations (no chaining)",
+                           l2="no flush: each step streams 8 layers' weights (far above L2)",
+                           timing="CUDA events per step around one CUDA-graph replay of the 8-layer launch"),
+            "us_per_layer": total_ms / K / L_ * 1e3,
+            "sequential_us_per_layer": float(np.mean(seq_ms)) / L_ * 1e3,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "kernel": "k_decode_stack (all 8 layers)",
+                         "bytes": "per layer: distinct routed experts x blob bytes + the shared expert",
+                         "peak_kind": peak_kind},
+            "gpu_launches": K,
+            "e2e": None,
+            "cpu_baseline": None,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "glm52_stream_8l":
         run_cache_sim(args) if args.cache_sim else run_stream(args)
+    elif args.workload.endswith("_stack8"):
+        run_stack_decode(args)
     else:
         run_colibri(args)
 

@@ -154,11 +154,10 @@ size_t colibri_moe_workspace_bytes(const colibri_layer_cfg *cfg, int T_max);
  *   per expert: gate = W1 q8(x), up = W3 q8(x) as int32 group dots times the two
  *   groups' scales; h = silu(gate) * up; down y = W2 q8(h) likewise ->
  *   out[t] = y_shared[t] + sum_i w[t][i] * y_{ids[t][i]}[t] in slot order.
- *   T <= 32 (decode) runs two kernels: router logits and scores with q8(x) on the side
- *   (q8 alone when ids_given), then one persistent kernel that selects and buckets in every
- *   CTA and runs gate/up, down and the combine, started as a programmatic dependent of the
- *   first. Larger T (prefill) runs q8, router logits, selection, bucketing, the two
- *   grouped GEMMs on tcgen05 and the combine.
+ *   T <= 32 (decode) runs one persistent kernel: q8(x) and the router logits spread over
+ *   every CTA, then each CTA selects and buckets for itself and runs its share of
+ *   gate/up, down and the combine. Larger T (prefill) runs q8, router logits, selection,
+ *   bucketing, the two grouped GEMMs on tcgen05 and the combine.
  *   x        device fp32 [T][d]
  *   Wr, bias as for colibri_router_topk (unused when ids_given)
  *   experts  device array of E colibri_expert (only the selected ids are read)
@@ -175,6 +174,48 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
                       const float *bias, const colibri_expert *experts,
                       const colibri_expert *shared, int32_t *ids, float *w, int ids_given,
                       float *out, void *workspace, size_t ws_bytes, void *stream);
+
+/* Several decode layers in one launch (the next layer's router and shared expert are
+ * sent towards L2 while the current layer drains, in the spirit of the dashen-tech
+ * guide's section "Router-Lookahead prefetch"). Layer l computes colibri_moe_layer on
+ * its own weights and activations: layers[l].x when given, else the previous layer's
+ * out (the call's x for layer 0). The results equal n_layers sequential
+ * colibri_moe_layer calls bit for bit. The CTAs meet on a grid barrier between layers.
+ * Every layer shares cfg, T and ids_given. (A chain of these layers alone, out into x,
+ * is not a model: each SwiGLU layer about squares the activations' magnitude, so long
+ * chains overflow; a model normalises between layers, outside this library.)
+ *   1 <= n_layers <= COLIBRI_STACK_MAX, 0 <= T <= 32 (decode only)
+ *   layers[l]  per layer: x (device fp32 [T][d], 16-byte aligned, or NULL), Wr, bias (as
+ *              colibri_moe_layer; unused when ids_given), experts, shared (host pointer,
+ *              as colibri_moe_layer), ids and w (device [T][top_k], outputs or inputs as
+ *              in colibri_moe_layer), out (device fp32 [T][d], 16-byte aligned). layers[]
+ *              itself is host memory, read during the call. out of layer l must differ
+ *              from its input; a chained layer may write the buffer of layer l - 2 (two
+ *              buffers in turn suffice).
+ *   workspace  device, >= colibri_moe_stack_workspace_bytes(cfg, T) bytes, 256-byte
+ *              aligned, owned by the caller; the error flag is read as for
+ *              colibri_moe_layer (colibri_workspace_status).
+ * COLIBRI_E_INVAL for a bad argument, COLIBRI_E_NOMEM for a short workspace; T == 0 is a
+ * no-op. */
+#define COLIBRI_STACK_MAX 16
+typedef struct {
+    const float *x;
+    const float *Wr;
+    const float *bias;
+    const colibri_expert *experts;
+    const colibri_expert *shared;
+    int32_t *ids;
+    float *w;
+    float *out;
+} colibri_stack_layer;
+
+/* Bytes of device workspace colibri_moe_stack_decode needs for up to T_max tokens (0 on
+ * a bad configuration or T_max > 32). */
+size_t colibri_moe_stack_workspace_bytes(const colibri_layer_cfg *cfg, int T_max);
+
+int colibri_moe_stack_decode(const colibri_layer_cfg *cfg, const float *x, int T, int n_layers,
+                             const colibri_stack_layer *layers, int ids_given, void *workspace,
+                             size_t ws_bytes, void *stream);
 
 /* colibri_moe_layer without a caller-supplied workspace. The pages have no counterpart
  * to this entry point: it exists for callers that cannot allocate device memory when
@@ -196,8 +237,9 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
  *   GLM-5.2-shaped layer fits up to T = 32), COLIBRI_E_INVAL on a bad configuration.
  *   Every call on a device shares the one array and leaves its contents behind for
  *   the next call; each call rewrites what it reads (the layer's host code clears the
- *   error flag and the kernels' sync counters with a memset before its first kernel). Calls whose work overlaps on the GPU (other streams, other host
- *   threads) race on the array and corrupt each other's results: serialise them.
+ *   error flag and the kernels' sync counters with a memset before its first kernel).
+ *   Calls whose work overlaps on the GPU (other streams, other host threads) race on
+ *   the array and corrupt each other's results: serialise them.
  *   Device-side errors (an id out of range) are skipped by the kernels as in
  *   colibri_moe_layer; this variant offers no reader for the flag. */
 #define COLIBRI_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -333,6 +375,9 @@ typedef struct {
     int64_t prefetch_skipped;/* prefetches dropped: every slot pinned */
     int64_t evictions;
     int64_t bytes_staged;    /* host -> HBM bytes enqueued */
+    int64_t prefetch_throttled; /* prefetches dropped: the cap on prefetch copies in flight */
+    int64_t prefetch_cancelled; /* queued prefetches dropped unfinished (wrong guess or evicted) */
+    int64_t prefetch_bytes;  /* host -> HBM bytes enqueued by prefetches (chunks included) */
     int n_slots;
 } colibri_cache_stats;
 
@@ -350,12 +395,16 @@ int colibri_expert_cache_init(colibri_cache **out, void *hbm_pool, size_t pool_b
 
 /* Prefetch: stage the blobs of layer `layer` named by host ids [n] that are not
  * resident (the router-lookahead prefetch of the dashen-tech guide). Resident ones
- * become most recently used. Returns at once; the copies run on the copy stream. */
+ * become most recently used. Returns at once. By default the copies are enqueued now on
+ * the copy stream; colibri_expert_cache_set_prefetch moves them to a prefetch stream, or
+ * queues them as chunks that colibri_expert_cache_wait enqueues. */
 int colibri_expert_cache_stage(colibri_cache *c, int layer, const int32_t *ids, int n);
 
 /* Makes the blobs of layer `layer` named by host ids [n] usable by work enqueued on
- * `wait_on` after this call: misses are staged now (or COLIBRI_E_MISS in strict mode),
- * and `wait_on` waits for each slot's ready event. The slots stay pinned until the
+ * `wait_on` after this call: misses are staged now on the copy stream (or
+ * COLIBRI_E_MISS in strict mode), and `wait_on` waits for each slot's ready event.
+ * Queued prefetches of `layer` are settled first: a named id's blob is finished on the
+ * copy stream (its remaining chunks), the others are cancelled and their slots freed. The slots stay pinned until the
  * next lookup, which also records when the previous batch's compute has finished
  * using them. Afterwards colibri_expert_cache_table(c, layer)[id] holds the expert. */
 int colibri_expert_cache_lookup(colibri_cache *c, int layer, const int32_t *ids, int n,
@@ -373,12 +422,42 @@ const colibri_expert *colibri_expert_cache_table(colibri_cache *c, int layer);
  * COLIBRI_E_INVAL unless 0 <= n_hot <= slots - top_k (a lookup batch must always fit). */
 int colibri_expert_cache_set_hot(colibri_cache *c, int n_hot);
 
+/* How prefetches (colibri_expert_cache_stage) are copied. They go on `prefetch_stream`
+ * (a cudaStream_t owned by the caller; NULL: the copy stream, as by default), so that a
+ * demand miss of colibri_expert_cache_lookup, on the copy stream, never waits behind a
+ * speculative copy.
+ *   chunk_bytes 0: each prefetch is one whole-blob copy enqueued by stage();
+ *     max_in_flight > 0 caps the prefetch copies still running: a prefetch of a
+ *     non-resident id beyond the cap is dropped (counted in prefetch_throttled);
+ *     0: no cap.
+ *   chunk_bytes > 0: stage() only reserves a slot and queues the blob;
+ *     colibri_expert_cache_wait enqueues it in chunks of chunk_bytes, at most
+ *     max_in_flight (1..64) chunks running, and only while no demand copy runs; a lookup
+ *     of the blob's layer finishes it or cancels it. A wrong guess then costs the chunks
+ *     already copied, which ran while the copy link was otherwise idle.
+ * COLIBRI_E_INVAL for a bad argument, or while queued prefetches or chunks are pending. */
+int colibri_expert_cache_set_prefetch(colibri_cache *c, void *prefetch_stream, int max_in_flight,
+                                      size_t chunk_bytes);
+
+/* Waits, polling on the calling thread, at most timeout_ms, for the work enqueued so far
+ * on `stream` (a cudaStream_t; typically the compute stream, whose current layer decides
+ * the next lookup's ids). Meanwhile it enqueues queued prefetch chunks whenever no demand
+ * copy is running (the pages' lookahead thread, run while the host waits anyway).
+ * COLIBRI_E_TIMEOUT if the work is still running. */
+int colibri_expert_cache_wait(colibri_cache *c, void *stream, int timeout_ms);
+
+/* One step of that wait's work, for callers with a wait loop of their own: enqueues up to
+ * max_chunks queued prefetch chunks now, if no demand copy is running and fewer than the
+ * cap are in flight; *enqueued counts them (0 with chunk_bytes 0 or an empty queue). */
+int colibri_expert_cache_pump(colibri_cache *c, int max_chunks, int *enqueued);
+
 /* 1: lookups of non-resident ids fail with COLIBRI_E_MISS instead of staging. */
 int colibri_expert_cache_set_strict(colibri_cache *c, int strict);
 
 int colibri_expert_cache_stats(colibri_cache *c, colibri_cache_stats *out);
 
-/* Waits (polling, at most timeout_ms) for every staging copy issued so far.
+/* Waits (polling, at most timeout_ms) for every staging copy issued so far, on the copy
+ * stream and on the prefetch stream.
  * COLIBRI_E_TIMEOUT if they are still running. */
 int colibri_expert_cache_sync(colibri_cache *c, int timeout_ms);
 

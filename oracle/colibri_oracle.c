@@ -136,6 +136,8 @@ static int select_sigmoid(const orc_cfg *cfg, const float *l, const float *bias,
     for (int e = 0; e < E; ++e) {
         s[e] = (float)(1.0 / (1.0 + exp(-(double)l[e])));
         c[e] = s[e] + (bias ? bias[e] : 0.0f);
+        if (isnan(c[e]))
+            c[e] = -INFINITY;  /* a NaN score ranks below every number */
     }
     for (int g = 0; g < G; ++g) {
         const float *cg = c + g * gs;
@@ -191,11 +193,16 @@ static int select_softmax(const orc_cfg *cfg, const float *l, int32_t *ids, floa
 {
     const int E = cfg->n_exp, K = cfg->top_k;
     unsigned char *allowed = (unsigned char *)malloc(E);
-    if (!allowed)
+    float *key = (float *)malloc(sizeof(float) * E);
+    if (!allowed || !key) {
+        free(allowed); free(key);
         return -1;
+    }
+    for (int e = 0; e < E; ++e)
+        key[e] = isnan(l[e]) ? -INFINITY : l[e];  /* a NaN logit ranks below every number */
     memset(allowed, 1, E);
     for (int i = 0; i < K; ++i) {
-        int e = argmax_allowed(l, allowed, E);
+        int e = argmax_allowed(key, allowed, E);
         ids[i] = e;
         if (e >= 0)
             allowed[e] = 0;
@@ -217,6 +224,7 @@ static int select_softmax(const orc_cfg *cfg, const float *l, int32_t *ids, floa
         w[i] = (float)(p * (double)cfg->routed_scale);
     }
     free(allowed);
+    free(key);
     return 0;
 }
 

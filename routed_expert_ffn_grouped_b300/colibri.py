@@ -39,6 +39,17 @@ class Expert(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w1", "w3", "w2", "s1", "s3", "s2")]
 
 
+class StackLayer(ctypes.Structure):
+    """colibri_stack_layer: one layer's device pointers for colibri_moe_stack_decode
+    (`shared` is a host pointer to an Expert)."""
+    _fields_ = [("x", ctypes.c_void_p), ("Wr", ctypes.c_void_p), ("bias", ctypes.c_void_p),
+                ("experts", ctypes.c_void_p),
+                ("shared", ctypes.c_void_p), ("ids", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("out", ctypes.c_void_p)]
+
+STACK_MAX = 16
+
+
 class BlobLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("w1", "w3", "w2", "s1", "s3", "s2", "nbytes")]
 
@@ -51,7 +62,8 @@ class WorkspaceView(ctypes.Structure):
 class CacheStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("lookups", "hits", "misses", "prefetch_staged",
                                               "prefetch_used", "prefetch_skipped", "evictions",
-                                              "bytes_staged")] + [("n_slots", ctypes.c_int)]
+                                              "bytes_staged", "prefetch_throttled", "prefetch_cancelled",
+                                              "prefetch_bytes")] + [("n_slots", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -69,6 +81,8 @@ SIGNATURES = {
     "colibri_q8_quantize_g": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "colibri_router_topk": (_I, [_PCFG, _P, _I, _P, _P, _P, _P, _P, _P]),
     "colibri_moe_workspace_bytes": (_SZ, [_PCFG, _I]),
+    "colibri_moe_stack_workspace_bytes": (_SZ, [_PCFG, _I]),
+    "colibri_moe_stack_decode": (_I, [_PCFG, _P, _I, _I, ctypes.POINTER(StackLayer), _I, _P, _SZ, _P]),
     "colibri_moe_layer": (_I, [_PCFG, _P, _I, _P, _P, _P, ctypes.POINTER(Expert), _P, _P, _I, _P, _P,
                                _SZ, _P]),
     "colibri_moe_f32_workspace_bytes": (_SZ, [_PCFG, _I]),
@@ -90,6 +104,9 @@ SIGNATURES = {
     "colibri_expert_cache_lookup": (_I, [_P, _I, _P, _I, _P]),
     "colibri_expert_cache_table": (_P, [_P, _I]),
     "colibri_expert_cache_set_strict": (_I, [_P, _I]),
+    "colibri_expert_cache_set_prefetch": (_I, [_P, _P, _I, ctypes.c_size_t]),
+    "colibri_expert_cache_wait": (_I, [_P, _P, _I]),
+    "colibri_expert_cache_pump": (_I, [_P, _I, _P]),
     "colibri_expert_cache_stats": (_I, [_P, ctypes.POINTER(CacheStats)]),
     "colibri_expert_cache_sync": (_I, [_P, _I]),
     "colibri_expert_cache_destroy": (None, [_P]),
@@ -200,6 +217,33 @@ def colibri_moe_layer(cfg: LayerCfg, x, Wr, bias, experts, shared: Expert | None
                                    ctypes.byref(shared) if shared is not None else None, _ptr(ids), _ptr(w),
                                    int(bool(ids_given)), _ptr(out), _ptr(workspace), workspace.numel(),
                                    _stream(stream)))
+
+
+def colibri_moe_stack_workspace_bytes(cfg: LayerCfg, T_max: int) -> int:
+    n = lib().colibri_moe_stack_workspace_bytes(ctypes.byref(cfg), T_max)
+    if n == 0:
+        raise ColibriError("colibri_moe_stack_workspace_bytes", E_INVAL, "invalid configuration or T_max > 32")
+    return n
+
+
+def colibri_moe_stack_decode(cfg: LayerCfg, x, layers, ids_given: bool, workspace, stream=None):
+    """Several decode layers in one launch. layers: per layer a dict with x (optional:
+    the layer's own activations), Wr, bias, experts (device tensors or None), shared
+    (Expert or None), ids, w, out (device tensors); a layer without x reads the previous
+    layer's out (layer 0: x)."""
+    T = x.shape[0]
+    arr = (StackLayer * len(layers))()
+    keep = []
+    for i, y in enumerate(layers):
+        sh = y.get("shared")
+        if sh is not None:
+            keep.append(sh)
+        arr[i] = StackLayer(_ptr(y.get("x")), _ptr(y.get("Wr")), _ptr(y.get("bias")), _ptr(y["experts"]),
+                            ctypes.addressof(sh) if sh is not None else None, _ptr(y["ids"]), _ptr(y["w"]),
+                            _ptr(y["out"]))
+    _check("colibri_moe_stack_decode",
+           lib().colibri_moe_stack_decode(ctypes.byref(cfg), _ptr(x), T, len(layers), arr, int(bool(ids_given)),
+                                          _ptr(workspace), workspace.numel(), _stream(stream)))
 
 
 def colibri_moe_f32_workspace_bytes(cfg: LayerCfg, T_max: int) -> int:
@@ -340,6 +384,26 @@ class ExpertCache:
 
     def set_hot(self, n_hot: int):
         _check("colibri_expert_cache_set_hot", lib().colibri_expert_cache_set_hot(self.handle, int(n_hot)))
+
+    def set_prefetch(self, prefetch_stream=None, max_in_flight: int = 0, chunk_bytes: int = 0):
+        """Prefetches on their own stream (kept alive here): whole-blob copies, at most
+        max_in_flight running (chunk_bytes 0), or queued chunks that wait() enqueues."""
+        self._pcopy = prefetch_stream
+        _check("colibri_expert_cache_set_prefetch",
+               lib().colibri_expert_cache_set_prefetch(
+                   self.handle, None if prefetch_stream is None else _stream(prefetch_stream), int(max_in_flight),
+                   int(chunk_bytes)))
+
+    def wait(self, stream=None, timeout_ms: int = 10000):
+        """Waits for `stream`'s work so far, enqueuing queued prefetch chunks meanwhile."""
+        _check("colibri_expert_cache_wait", lib().colibri_expert_cache_wait(self.handle, _stream(stream), timeout_ms))
+
+    def pump(self, max_chunks: int) -> int:
+        """Enqueues up to max_chunks queued prefetch chunks now; returns how many."""
+        n = ctypes.c_int(0)
+        _check("colibri_expert_cache_pump", lib().colibri_expert_cache_pump(self.handle, int(max_chunks),
+                                                                             ctypes.byref(n)))
+        return n.value
 
     def set_strict(self, strict: bool):
         _check("colibri_expert_cache_set_strict", lib().colibri_expert_cache_set_strict(self.handle, int(strict)))

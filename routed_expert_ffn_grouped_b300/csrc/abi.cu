@@ -78,7 +78,7 @@ static size_t up256(size_t n)
     return (n + 255) & ~size_t(255);
 }
 
-WsLayout ws_layout(const colibri_layer_cfg *c, int T)
+WsLayout ws_layout(const colibri_layer_cfg *c, int T, bool stack)
 {
     WsLayout L{};
     const size_t d = c->d, E = c->n_exp, K = c->top_k;
@@ -98,7 +98,10 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     // q8 of h across two gate/up items
     L.hpair_count = c->group == 64 ? PT * (fmax / 64) : 0;
     L.sync_bytes = 4 * (4 + nslots + d / G + L.hpair_count);
-    L.sync = take(L.sync_bytes);
+    L.sync_stride = (L.sync_bytes + 15) & ~size_t(15);
+    L.sync = take(stack ? 2 * L.sync_stride + 16 : L.sync_bytes);
+    L.bar = stack ? L.sync + 2 * L.sync_stride : 0;
+    L.sync_end = stack ? L.bar + 16 : L.sync + L.sync_bytes;
     L.qx = take((size_t)T * d);
     L.qx_eo = take((size_t)T * d);
     L.sx = take(4 * (size_t)T * (d / G));
@@ -122,6 +125,72 @@ WsLayout ws_layout(const colibri_layer_cfg *c, int T)
     L.fmax = fmax;
     L.total = o;
     return L;
+}
+
+}  // namespace clb
+
+namespace clb {
+
+// The decode kernel's arguments for one layer; `sync` is its control-word area.
+DecodeArgs decode_args(const colibri_layer_cfg *cfg, int T, const WsLayout &L, char *ws, const float *x,
+                       const float *Wr, const float *bias, const colibri_expert *experts, const colibri_expert &sh,
+                       int32_t *ids, float *w, int ids_given, float *out, int *sync)
+{
+    const int d = cfg->d;
+    int *err = reinterpret_cast<int *>(ws + L.err);
+    float *lg = reinterpret_cast<float *>(ws + L.logits);
+    float *sv = reinterpret_cast<float *>(ws + L.s);
+    float *cv = reinterpret_cast<float *>(ws + L.c);
+    DecodeArgs da{};
+    da.experts = experts;
+    da.shared = sh;
+    da.d = d;
+    da.ffn = cfg->ffn;
+    da.shared_ffn = cfg->shared_ffn;
+    da.T = T;
+    da.K = cfg->top_k;
+    da.has_shared = cfg->has_shared;
+    da.fmax = (int)L.fmax;
+    da.x = x;
+    da.Wr = ids_given ? nullptr : Wr;
+    da.bias = cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : bias;
+    da.ids_given = ids_given ? 1 : 0;
+    da.E = cfg->n_exp;
+    da.n_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->n_group;
+    da.topk_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->topk_group;
+    da.router = cfg->router;
+    da.norm_topk = cfg->norm_topk;
+    da.routed_scale = cfg->routed_scale;
+    da.logits = lg;
+    da.rs = sv;
+    da.rc = cv;
+    da.ids = ids;
+    da.w_in = w;
+    da.w_out = w;
+    da.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
+    da.pairs = reinterpret_cast<int32_t *>(ws + L.pairs);
+    da.slots = reinterpret_cast<Slot *>(ws + L.slots);
+    da.counters = reinterpret_cast<Counters *>(ws + L.counters);
+    da.qx = reinterpret_cast<int8_t *>(ws + L.qx);
+    da.xq_eo = reinterpret_cast<int8_t *>(ws + L.qx_eo);
+    da.sx = reinterpret_cast<float *>(ws + L.sx);
+    da.xc = reinterpret_cast<int *>(ws + L.xc);
+    da.hq = reinterpret_cast<int8_t *>(ws + L.hq);
+    da.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
+    da.hs = reinterpret_cast<float *>(ws + L.hs);
+    da.hc = reinterpret_cast<int *>(ws + L.hc);
+    da.y = reinterpret_cast<float *>(ws + L.y);
+    da.out = out;
+    da.claim = sync;
+    da.route_done = sync + 1;
+    da.done_gu = sync + 4;
+    da.done_rb = sync + 4 + L.nslots;
+    da.err = err;
+    da.max_slots = (int)L.nslots;
+    da.group = cfg->group;
+    da.hf = reinterpret_cast<float *>(ws + L.hf);
+    da.hpair = sync + 4 + L.nslots + d / G;
+    return da;
 }
 
 }  // namespace clb
@@ -368,7 +437,7 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     // the control words (error flag, routing counter), the work counters and the decode
     // kernel's claim and completion counters start every call at zero: if routing fails,
     // the expert kernels find no work
-    if (cudaMemsetAsync(ws + L.err, 0, L.sync + L.sync_bytes - L.err, s) != cudaSuccess)
+    if (cudaMemsetAsync(ws + L.err, 0, L.sync_end - L.err, s) != cudaSuccess)
         return COLIBRI_E_CUDA;
     if (prof_mark(0, s))
         return COLIBRI_E_CUDA;
@@ -393,56 +462,8 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
         // bucketing, gate/up, down and the combine
         if (prof_mark(1, s) || prof_mark(2, s) || prof_mark(3, s) || prof_mark(4, s))
             return COLIBRI_E_CUDA;
-        DecodeArgs da{};
-        da.experts = experts;
-        da.shared = sh;
-        da.d = d;
-        da.ffn = cfg->ffn;
-        da.shared_ffn = cfg->shared_ffn;
-        da.T = T;
-        da.K = K;
-        da.has_shared = cfg->has_shared;
-        da.fmax = (int)L.fmax;
-        da.x = x;
-        da.Wr = ids_given ? nullptr : Wr;
-        da.bias = cfg->router == COLIBRI_ROUTER_SOFTMAX ? nullptr : bias;
-        da.ids_given = ids_given ? 1 : 0;
-        da.E = E;
-        da.n_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->n_group;
-        da.topk_group = cfg->router == COLIBRI_ROUTER_SOFTMAX ? 1 : cfg->topk_group;
-        da.router = cfg->router;
-        da.norm_topk = cfg->norm_topk;
-        da.routed_scale = cfg->routed_scale;
-        da.logits = lg;
-        da.rs = sv;
-        da.rc = cv;
-        da.ids = ids;
-        da.w_in = w;
-        da.w_out = w;
-        da.offsets = reinterpret_cast<int32_t *>(ws + L.offsets);
-        da.pairs = reinterpret_cast<int32_t *>(ws + L.pairs);
-        da.slots = reinterpret_cast<Slot *>(ws + L.slots);
-        da.counters = reinterpret_cast<Counters *>(ws + L.counters);
-        da.qx = reinterpret_cast<int8_t *>(ws + L.qx);
-        da.xq_eo = reinterpret_cast<int8_t *>(ws + L.qx_eo);
-        da.sx = reinterpret_cast<float *>(ws + L.sx);
-        da.xc = reinterpret_cast<int *>(ws + L.xc);
-        da.hq = reinterpret_cast<int8_t *>(ws + L.hq);
-        da.hq_eo = reinterpret_cast<int8_t *>(ws + L.hq_eo);
-        da.hs = reinterpret_cast<float *>(ws + L.hs);
-        da.hc = reinterpret_cast<int *>(ws + L.hc);
-        da.y = reinterpret_cast<float *>(ws + L.y);
-        da.out = out;
-        int *sync = reinterpret_cast<int *>(ws + L.sync);
-        da.claim = sync;
-        da.route_done = sync + 1;
-        da.done_gu = sync + 4;
-        da.done_rb = sync + 4 + L.nslots;
-        da.err = err;
-        da.max_slots = (int)L.nslots;
-        da.group = cfg->group;
-        da.hf = reinterpret_cast<float *>(ws + L.hf);
-        da.hpair = sync + 4 + L.nslots + d / G;
+        const DecodeArgs da = decode_args(cfg, T, L, ws, x, Wr, bias, experts, sh, ids, w, ids_given, out,
+                                          reinterpret_cast<int *>(ws + L.sync));
         if (launch_decode(da, s) != cudaSuccess || prof_mark(5, s) || prof_mark(6, s) || prof_mark(7, s))
             return COLIBRI_E_CUDA;
         return COLIBRI_OK;
@@ -516,6 +537,67 @@ int colibri_moe_layer(const colibri_layer_cfg *cfg, const float *x, int T, const
     if (cudaGetLastError() != cudaSuccess || prof_mark(7, s))
         return COLIBRI_E_CUDA;
     return COLIBRI_OK;
+}
+
+size_t colibri_moe_stack_workspace_bytes(const colibri_layer_cfg *cfg, int T_max)
+{
+    if (!cfg_valid(cfg) || T_max < 0 || T_max > DECODE_T_MAX)
+        return 0;
+    return ws_layout(cfg, T_max, true).total;
+}
+
+int colibri_moe_stack_decode(const colibri_layer_cfg *cfg, const float *x, int T, int n_layers,
+                             const colibri_stack_layer *layers, int ids_given, void *workspace,
+                             size_t ws_bytes, void *stream)
+{
+    if (!cfg_valid(cfg) || T < 0 || T > DECODE_T_MAX || n_layers < 1 || n_layers > COLIBRI_STACK_MAX ||
+        !layers)
+        return COLIBRI_E_INVAL;
+    if (T == 0)
+        return COLIBRI_OK;
+    if (!workspace || !aligned(workspace, 256))
+        return COLIBRI_E_INVAL;
+    // layer l's activations: its own x, else the previous layer's out (x for layer 0)
+    auto input_of = [&](int l) -> const float * {
+        return layers[l].x ? layers[l].x : l ? layers[l - 1].out : x;
+    };
+    for (int l = 0; l < n_layers; ++l) {
+        const colibri_stack_layer &y = layers[l];
+        if (!input_of(l) || !aligned(input_of(l), 16))
+            return COLIBRI_E_INVAL;
+        if (!y.experts || !y.ids || !y.w || !y.out || !aligned(y.out, 16))
+            return COLIBRI_E_INVAL;
+        if (cfg->has_shared && !y.shared)
+            return COLIBRI_E_INVAL;
+        if (!ids_given && (!y.Wr || !aligned(y.Wr, 16)))
+            return COLIBRI_E_INVAL;
+        // layer l reads its input while it writes its output
+        if (y.out == input_of(l))
+            return COLIBRI_E_INVAL;
+    }
+    const WsLayout L = ws_layout(cfg, T, true);
+    if (ws_bytes < L.total)
+        return COLIBRI_E_NOMEM;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *ws = static_cast<char *>(workspace);
+    // the error word, both control-word areas and the barrier start at zero
+    if (cudaMemsetAsync(ws + L.err, 0, L.sync_end - L.err, s) != cudaSuccess)
+        return COLIBRI_E_CUDA;
+    DecodeStack p{};
+    p.L = n_layers;
+    p.bar = reinterpret_cast<int *>(ws + L.bar);
+    p.sync_area[0] = reinterpret_cast<int *>(ws + L.sync);
+    p.sync_area[1] = reinterpret_cast<int *>(ws + L.sync + L.sync_stride);
+    p.sync_words = (int)(L.sync_stride / 4);
+    for (int l = 0; l < n_layers; ++l) {
+        const colibri_stack_layer &y = layers[l];
+        colibri_expert sh{};
+        if (cfg->has_shared)
+            sh = *y.shared;
+        p.layer[l] = decode_args(cfg, T, L, ws, input_of(l), y.Wr, y.bias, y.experts, sh, y.ids, y.w, ids_given,
+                                 y.out, p.sync_area[l & 1]);
+    }
+    return launch_decode_stack(p, s) == cudaSuccess ? COLIBRI_OK : COLIBRI_E_CUDA;
 }
 
 // Workspace of colibri_moe_layer_f32: error flag | logits [T][E] | sigmoid scores s and

@@ -176,6 +176,12 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
 
+// Ends an mbarrier's life, so that its word may be initialised again.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -272,6 +278,14 @@ __device__ __forceinline__ void grid_dep_wait()
 __device__ __forceinline__ void grid_dep_launch()
 {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// The key a router score is ranked by: the score, or -inf for NaN, so that the order
+// (larger first, then lower index) is total and a selection always yields distinct,
+// valid ids.
+__device__ __forceinline__ float rank_score(float v)
+{
+    return v != v ? -INFINITY : v;
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *p)

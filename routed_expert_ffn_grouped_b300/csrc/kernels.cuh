@@ -108,6 +108,21 @@ struct DecodeArgs {
 // One persistent launch for a decode step: router logits, expert selection (unless
 // ids_given) and bucketing, then gate/up, down and the combine.
 cudaError_t launch_decode(DecodeArgs a, cudaStream_t s);
+
+// Several layers in one persistent launch: layer l + 1 reads layer l's output as its
+// activations. The layers share shapes, workspace and launch geometry; their control
+// words alternate between two areas (CTA 0 clears the one the next layer takes), and
+// the CTAs meet on a grid barrier (a counter) between layers.
+constexpr int STACK_MAX = 16;
+struct DecodeStack {
+    DecodeArgs layer[STACK_MAX];
+    int L;
+    int *bar;         // grid barrier: CTAs arrived, over all layer boundaries
+    int *sync_area[2];
+    int sync_words;   // ints of one control-word area
+};
+cudaError_t launch_decode_stack(DecodeStack &p, cudaStream_t s);
+
 // Scales (and corrections) a row of q8(h) holds on the decode path: fmax/32 rounded up to
 // 16 bytes.
 int decode_hgs(int fmax);

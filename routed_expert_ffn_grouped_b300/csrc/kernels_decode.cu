@@ -492,7 +492,7 @@ __device__ void select_warp(const DecodeArgs &a, int t, float *cs, float *ss, in
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int e = e0 + 32 * u + lane;
-            cv[u] = e < E ? __ldcg((sig ? a.rc : a.logits) + base + e) : 0.0f;
+            cv[u] = e < E ? rank_score(__ldcg((sig ? a.rc : a.logits) + base + e)) : 0.0f;
             sv[u] = sig && e < E ? __ldcg(a.rs + base + e) : 0.0f;
         }
 #pragma unroll
@@ -620,7 +620,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
     float *ps = reinterpret_cast<float *>(pick + (size_t)T * 32);
     for (int i = tid; i < T * E; i += NT) {
         const int t = i / E, e = i - t * E;
-        cs[t * Ep + e] = sig ? __ldcg(a.rc + i) : __ldcg(a.logits + i);
+        cs[t * Ep + e] = rank_score(sig ? __ldcg(a.rc + i) : __ldcg(a.logits + i));
         if (sig)
             ss[t * Ep + e] = __ldcg(a.rs + i);
     }
@@ -1270,7 +1270,7 @@ __device__ void quantise_x(const DecodeArgs &a, int e, int lane)
         float x[2];
         float m = 0.0f;
         for (int h = 0; h < halves; ++h) {
-            x[h] = __ldg(a.x + base + h * G + lane);
+            x[h] = __ldcg(a.x + base + h * G + lane);  // in a layer stack, written in this launch
             m = fmaxf(m, fabsf(x[h]));
         }
         const float amax = warp_max(m);
@@ -1613,44 +1613,120 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
 
 }  // namespace
 
-template <int TCH>
-__global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs a)
+// The CTA's mbarriers for one layer (thread 0); `again` ends the previous layer's first.
+__device__ void init_barriers(const DecodeArgs &a, const RingSmem &s, bool again)
 {
-    const int NBUF = a.nbuf;
-    static_assert(TCH <= 8, "chunk descriptors hold 8 rows");  // launched with 1, 2 or 4
-    extern __shared__ __align__(128) unsigned char sm[];
-    const RingSmem s = carve(sm, a, TCH);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < a.ring; ++i) {
-            mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], NC);
-        }
-        for (int i = 0; i < a.nh; ++i) {
-            mbar_init(&s.hfull[i], 1);
-            mbar_init(&s.hempty[i], NC);
-        }
-        mbar_init(s.cbar, NC);
-        mbar_init(s.tbar, 1);
-        mbar_init(s.xbar, 1);
-        for (int i = 0; i < NBUF; ++i) {
-            mbar_init(&s.pfull[i], NC);
-            mbar_init(&s.pempty[i], 1);
-        }
-        s.flags[0] = 0;
-        fence_mbar_init();
+    auto init = [&](uint64_t *b, uint32_t count) {
+        if (again)
+            mbar_inval(b);
+        mbar_init(b, count);
+    };
+    for (int i = 0; i < a.ring; ++i) {
+        init(&s.full[i], 1);
+        init(&s.empty[i], NC);
     }
-    __syncthreads();
+    for (int i = 0; i < a.nh; ++i) {
+        init(&s.hfull[i], 1);
+        init(&s.hempty[i], NC);
+    }
+    init(s.cbar, NC);
+    init(s.tbar, 1);
+    init(s.xbar, 1);
+    for (int i = 0; i < a.nbuf; ++i) {
+        init(&s.pfull[i], NC);
+        init(&s.pempty[i], 1);
+    }
+    s.flags[0] = 0;
+    fence_mbar_init();
+}
+
+// One layer on this CTA: the three roles.
+template <int TCH>
+__device__ __forceinline__ void run_layer(const DecodeArgs &a, const RingSmem &s, int warp, int lane)
+{
     if (warp == NC) {
         if (lane == 0)
             run_producer<TCH>(a, s);
     } else if (warp > NC) {
         grid_dep_wait();  // the activations are in
         quantise_x(a, warp - NC - 1, lane);
-        if (warp - NC - 1 < NBUF)
+        if (warp - NC - 1 < a.nbuf)
             run_epilogue<TCH>(a, s, warp - NC - 1, lane);
     } else {
         run_consumers<TCH>(a, s, warp, lane);
+    }
+}
+
+template <int TCH>
+__global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode(DecodeArgs a)
+{
+    static_assert(TCH <= 8, "chunk descriptors hold 8 rows");  // launched with 1, 2 or 4
+    extern __shared__ __align__(128) unsigned char sm[];
+    const RingSmem s = carve(sm, a, TCH);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0)
+        init_barriers(a, s, false);
+    __syncthreads();
+    run_layer<TCH>(a, s, warp, lane);
+}
+
+// This CTA's share of the next layer's router matrix and shared expert, sent towards L2
+// while the current layer drains.
+__device__ void prefetch_next_layer(const DecodeArgs &n)
+{
+    if (n.has_shared)
+        prefetch_shared(n);
+    if (n.Wr && !n.ids_given) {
+        const size_t bytes = 4 * (size_t)n.E * n.d;
+        const size_t share = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~size_t(15);
+        const size_t b0 = share * blockIdx.x;
+        if (b0 < bytes)
+            prefetch_l2(reinterpret_cast<const char *>(n.Wr) + b0, (uint32_t)min(share, bytes - b0));
+    }
+}
+
+// Layers 0..L-1 in one launch. Between layers every CTA arrives on a grid barrier (a
+// device counter, bounded wait): layer l + 1 starts only when layer l's output, its
+// activations, is complete everywhere. Layer l uses control-word area l % 2; CTA 0 clears
+// the other area at the start of layer l >= 1 for layer l + 1 (the launch's memset cleared
+// both for layers 0 and 1). A CTA that gave up on a wait still arrives; after the
+// barrier every CTA stops if the error word is set.
+template <int TCH>
+__global__ void __launch_bounds__((NC + 1 + NE_MAX) * 32, 1) k_decode_stack(const __grid_constant__ DecodeStack p)
+{
+    extern __shared__ __align__(128) unsigned char sm[];
+    const RingSmem s = carve(sm, p.layer[0], TCH);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int l = 0; l < p.L; ++l) {
+        const DecodeArgs &a = p.layer[l];
+        if (blockIdx.x == 0 && l >= 1 && l + 1 < p.L) {
+            int *z = p.sync_area[(l + 1) & 1];
+            for (int i = threadIdx.x; i < p.sync_words; i += blockDim.x)
+                z[i] = 0;
+        }
+        if (threadIdx.x == 0)
+            init_barriers(a, s, l > 0);
+        if (l > 0 && warp == NC && lane == 0)
+            fence_proxy_async_global();  // the previous layer's output is read by bulk copies
+        __syncthreads();
+        run_layer<TCH>(a, s, warp, lane);
+        if (l + 1 == p.L)
+            break;
+        if (warp == NC && lane == 0)
+            prefetch_next_layer(p.layer[l + 1]);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(p.bar, 1);
+            const bool ok = wait_count_geq(p.bar, (int)gridDim.x * (l + 1));
+            if (!ok)
+                atomicOr(a.err, ERR_WAIT_TIMEOUT);
+            __threadfence();
+            s.flags[1] = ok && ld_acquire_gpu(a.err) == 0;
+        }
+        __syncthreads();
+        if (!s.flags[1])
+            break;
     }
 }
 
@@ -1712,32 +1788,73 @@ cudaError_t sm_count_of_current(int &n_sm)
     return cudaSuccess;
 }
 
+// Raises kernel fn's dynamic shared memory limit to `smem` if needed. Per device and
+// kernel (slot), the largest size set so far is kept (the attribute belongs to the
+// device's context), so that a call costs no query; host threads that launch at the same
+// time take the lock, so the attribute and its record agree.
+template <typename F>
+cudaError_t ensure_smem(F fn, int slot, size_t smem)
+{
+    constexpr int MAX_DEV = 64, SLOTS = 8;
+    static std::mutex mu;
+    static size_t smem_set[MAX_DEV][SLOTS] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= MAX_DEV || slot < 0 || slot >= SLOTS)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (smem > smem_set[dev][slot]) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        smem_set[dev][slot] = smem;
+    }
+    return cudaSuccess;
+}
+
+template <int TCH>
+cudaError_t launch_stack_tch(const DecodeStack &p, int n_sm, cudaStream_t s)
+{
+    auto fn = k_decode_stack<TCH>;
+    const DecodeArgs &a = p.layer[0];
+    const size_t smem = ring_layout(a, a.ring, a.nh, a.nbuf, TCH).total;
+    cudaError_t e = ensure_smem(fn, 4 + TCH / 2, smem);
+    if (e != cudaSuccess)
+        return e;
+    // a cooperative launch: the grid barrier between layers needs every CTA resident
+    // (one per SM), which the launch then guarantees or refuses
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_sm);
+    cfg.blockDim = dim3((NC + 1 + NE_MAX) * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, fn, p);
+    if (e != cudaSuccess) {
+        // a stream that cannot take a programmatic dependency: plain stream order
+        (void)cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, fn, p);
+    }
+    return e;
+}
+
 template <int TCH>
 cudaError_t launch_tch(DecodeArgs a, int n_sm, cudaStream_t s)
 {
     auto fn = k_decode<TCH>;
     const size_t smem = ring_layout(a, a.ring, a.nh, a.nbuf, TCH).total;
-    // per device: the largest dynamic shared memory set so far (the attribute belongs to
-    // the device's context), so that a call costs no query; host threads that launch at
-    // the same time take the lock, so the attribute and its record agree
-    constexpr int MAX_DEV = 64;
-    static std::mutex mu;
-    static size_t smem_set[MAX_DEV] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = ensure_smem(fn, TCH / 2, smem);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= MAX_DEV)
-        return cudaErrorInvalidDevice;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (smem > smem_set[dev]) {
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess)
-                return e;
-            smem_set[dev] = smem;
-        }
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)n_sm);
     cfg.blockDim = dim3((NC + 1 + NE_MAX) * 32);
@@ -1803,15 +1920,11 @@ int decode_hgs(int fmax)
     return round_up(fmax / G, 4);
 }
 
-cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
+// The launch geometry of a decode call (logit items, tokens per chunk, ring); returns the
+// tokens per chunk, or 0 if no ring fits.
+int decode_geometry(DecodeArgs &a, int n_sm)
 {
-    if (a.T <= 0)
-        return cudaSuccess;
     a.hgs = decode_hgs(a.fmax);
-    int n_sm = 0;
-    cudaError_t e = sm_count_of_current(n_sm);
-    if (e != cudaSuccess)
-        return e;
     logit_geometry(a, n_sm);
     // tokens per chunk: up to 4 (a slot with more tokens streams its weights once per
     // chunk, but the smaller x, h and partial-sum areas leave room for a deeper ring);
@@ -1821,13 +1934,77 @@ cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
     const int n4 = want >= 4 ? ring_for<4>(c4) : 0;
     const int n2 = want >= 2 ? ring_for<2>(c2) : 0;
     const int n1 = ring_for<1>(c1);
-    if (n4 >= 3 || (n4 >= 2 && n2 < 3 && n1 < 3))
-        return launch_tch<4>(c4, n_sm, s);
-    if (n2 >= 3 || (n2 >= 2 && n1 < 3))
-        return launch_tch<2>(c2, n_sm, s);
-    if (n1 >= 2)
-        return launch_tch<1>(c1, n_sm, s);
-    return cudaErrorInvalidValue;
+    if (n4 >= 3 || (n4 >= 2 && n2 < 3 && n1 < 3)) {
+        a = c4;
+        return 4;
+    }
+    if (n2 >= 3 || (n2 >= 2 && n1 < 3)) {
+        a = c2;
+        return 2;
+    }
+    if (n1 >= 2) {
+        a = c1;
+        return 1;
+    }
+    return 0;
+}
+
+cudaError_t launch_decode(DecodeArgs a, cudaStream_t s)
+{
+    if (a.T <= 0)
+        return cudaSuccess;
+    int n_sm = 0;
+    cudaError_t e = sm_count_of_current(n_sm);
+    if (e != cudaSuccess)
+        return e;
+    switch (decode_geometry(a, n_sm)) {
+    case 4:
+        return launch_tch<4>(a, n_sm, s);
+    case 2:
+        return launch_tch<2>(a, n_sm, s);
+    case 1:
+        return launch_tch<1>(a, n_sm, s);
+    default:
+        return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode_stack(DecodeStack &p, cudaStream_t s)
+{
+    if (p.L < 1 || p.L > STACK_MAX)
+        return cudaErrorInvalidValue;
+    if (p.layer[0].T <= 0)
+        return cudaSuccess;
+    int n_sm = 0;
+    cudaError_t e = sm_count_of_current(n_sm);
+    if (e != cudaSuccess)
+        return e;
+    DecodeArgs g = p.layer[0];
+    const int tch = decode_geometry(g, n_sm);
+    for (int l = 0; l < p.L; ++l) {
+        DecodeArgs &a = p.layer[l];
+        a.ring = g.ring;
+        a.nh = g.nh;
+        a.nbuf = g.nbuf;
+        a.tch = g.tch;
+        a.hgs = g.hgs;
+        a.lg_ne = g.lg_ne;
+        a.lg_tb = g.lg_tb;
+        a.lg_kc = g.lg_kc;
+        a.lg_nck = g.lg_nck;
+        a.n_logit = g.n_logit;
+        a.sel_warps = g.sel_warps;
+    }
+    switch (tch) {
+    case 4:
+        return launch_stack_tch<4>(p, n_sm, s);
+    case 2:
+        return launch_stack_tch<2>(p, n_sm, s);
+    case 1:
+        return launch_stack_tch<1>(p, n_sm, s);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace clb

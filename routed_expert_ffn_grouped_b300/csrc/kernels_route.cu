@@ -269,13 +269,14 @@ __device__ void select_token(const SelectArgs &a, int t, int lane, float *sc)
         const int e = lane + 32 * r;
         if (r < R && e < E) {
             if (a.router == COLIBRI_ROUTER_SOFTMAX) {
-                sv[r] = cv[r] = a.logits[row + e];
+                sv[r] = a.logits[row + e];
+                cv[r] = rank_score(sv[r]);
             } else if (a.s) {
                 sv[r] = a.s[row + e];
-                cv[r] = a.c[row + e];
+                cv[r] = rank_score(a.c[row + e]);
             } else {
                 sv[r] = (float)(1.0 / (1.0 + exp(-(double)a.logits[row + e])));
-                cv[r] = sv[r] + (a.bias ? a.bias[e] : 0.0f);
+                cv[r] = rank_score(sv[r] + (a.bias ? a.bias[e] : 0.0f));
             }
             avail[r] = true;
             sc[e] = cv[r];

@@ -17,6 +17,9 @@ struct WsLayout {
     size_t nslots;      // slots at most: the shared expert + min(E, T*K) routed experts
     size_t sync_bytes;  // decode kernel's claim counter, routing counter, (two spare words) |
                         // done_gu [nslots] | done_rb [d/32] | hpair [hpair_count]
+    size_t sync_stride; // a layer stack: two such areas sync_stride apart, then the grid
+    size_t bar;         // barrier's counter at bar
+    size_t sync_end;    // the end of the words zeroed per call (from err)
     size_t fmax, total;
 };
 
@@ -24,6 +27,7 @@ constexpr int DECODE_T_MAX = 32;  // larger batches take the tensor-core prefill
 
 bool cfg_valid(const colibri_layer_cfg *c);
 bool uses_gemm(const colibri_layer_cfg *c, int T);
-WsLayout ws_layout(const colibri_layer_cfg *c, int T);
+// stack: the workspace of colibri_moe_stack_decode (two control-word areas and a barrier)
+WsLayout ws_layout(const colibri_layer_cfg *c, int T, bool stack = false);
 
 }  // namespace clb

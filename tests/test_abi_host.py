@@ -119,6 +119,29 @@ def test_argument_errors_detected_on_host(lib):
     need = C.colibri_moe_host_workspace_bytes(cfg, 4)
     assert host(ctypes.byref(cfg), x.ctypes.data, 4, None, None, None, None, None, None, 0, out.ctypes.data,
                 fake_ws, need - 1, None) == C.E_NOMEM
+    # the layer stack: sizes are decode only; n_layers, aliasing and the workspace size are
+    # checked before anything is enqueued (fake addresses are never dereferenced)
+    assert C.colibri_moe_stack_workspace_bytes(cfg, 32) > C.colibri_moe_workspace_bytes(cfg, 32)
+    assert lib.colibri_moe_stack_workspace_bytes(ctypes.byref(cfg), 33) == 0
+    stack = lib.colibri_moe_stack_decode
+    fx, fo1, fo2 = 1 << 24, 1 << 25, 1 << 26
+    lay = (C.StackLayer * 2)(C.StackLayer(None, fx, None, fx, None, fx, fx, fo1),
+                             C.StackLayer(None, fx, None, fx, None, fx, fx, fo2))
+    no_shared = C.layer_cfg(synth.TINY.replace(has_shared=False))
+    ok_args = (fx, 4, 2, lay, 0, fake_ws)
+    assert stack(ctypes.byref(no_shared), fx, 0, 2, lay, 0, None, 0, None) == C.OK           # T == 0
+    assert stack(ctypes.byref(no_shared), fx, 4, 0, lay, 0, fake_ws, 1 << 40, None) == C.E_INVAL
+    assert stack(ctypes.byref(no_shared), fx, 4, C.STACK_MAX + 1, lay, 0, fake_ws, 1 << 40, None) == C.E_INVAL
+    assert stack(ctypes.byref(no_shared), fx, 33, 2, lay, 0, fake_ws, 1 << 40, None) == C.E_INVAL
+    assert stack(ctypes.byref(cfg), *ok_args, 1 << 40, None) == C.E_INVAL                   # no shared expert
+    alias = (C.StackLayer * 2)(C.StackLayer(None, fx, None, fx, None, fx, fx, fo1),
+                               C.StackLayer(None, fx, None, fx, None, fx, fx, fo1))
+    assert stack(ctypes.byref(no_shared), fx, 4, 2, alias, 0, fake_ws, 1 << 40, None) == C.E_INVAL
+    own = (C.StackLayer * 2)(C.StackLayer(None, fx, None, fx, None, fx, fx, fo1),
+                             C.StackLayer(fo2, fx, None, fx, None, fx, fx, fo2))    # writes its own input
+    assert stack(ctypes.byref(no_shared), fx, 4, 2, own, 0, fake_ws, 1 << 40, None) == C.E_INVAL
+    need = C.colibri_moe_stack_workspace_bytes(no_shared, 4)
+    assert stack(ctypes.byref(no_shared), *ok_args, need - 1, None) == C.E_NOMEM
     assert lib.colibri_lru_trace(0, 0, None, None, None) == C.E_INVAL
 
 

@@ -109,3 +109,19 @@ def test_expert_load_and_host_fields():
     h = bench.host_info()
     assert h["nproc"] and h["nproc"] >= 1
     assert bench.informational(lambda: 1 / 0)["error"].startswith("ZeroDivisionError")
+
+
+def test_interval_overlap_arithmetic():
+    """The streaming overlap figures: union lengths and the copy time that ran beside
+    compute, on hand-made intervals."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.interval_union([]) == 0.0
+    assert bench.interval_union([(0, 2), (1, 3), (5, 6)]) == 4.0
+    assert bench.interval_union([(0, 10), (2, 3)]) == 10.0
+    o = bench.overlap_stats([(0, 4), (6, 8)], [(3, 7)], 10.0)
+    assert o["copy_busy_frac"] == pytest.approx(0.6)
+    assert o["compute_busy_frac"] == pytest.approx(0.4)
+    assert o["overlap_frac_of_copy"] == pytest.approx(2 / 6)      # [3,4) and [6,7)
+    assert o["idle_frac"] == pytest.approx(0.2)                   # [8,10)
+    assert bench.overlap_stats([], [(0, 1)], 2.0)["overlap_frac_of_copy"] is None

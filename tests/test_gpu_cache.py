@@ -89,14 +89,22 @@ def test_staged_blobs_land_byte_for_byte(torch_cuda, C, host):
     cache.close()
 
 
-def test_layer_through_cache_equals_resident_layer(torch_cuda, C, host):
+@pytest.mark.parametrize("mode", ["copy_stream", "prefetch_stream", "queued"])
+def test_layer_through_cache_equals_resident_layer(torch_cuda, C, host, mode):
     """Decode steps with correlated routing over a cache smaller than the expert set:
     the layer reads its experts through the cache's table and must give the same bits
-    as the same layer on fully resident experts."""
+    as the same layer on fully resident experts. Prefetches go on the copy stream, on a
+    stream of their own, or as queued chunks that the host enqueues while it waits for
+    the previous layer."""
     torch = torch_cuda
     layers, pinned, nb = host
     copy = torch.cuda.Stream()
     cache, _ = make_cache(torch, C, pinned, 6, copy)        # 6 slots for 3 x 16 experts
+    pcopy = torch.cuda.Stream()
+    if mode == "prefetch_stream":
+        cache.set_prefetch(pcopy, 1)
+    elif mode == "queued":
+        cache.set_prefetch(pcopy, 2, 16384)
     resident = [C.DeviceLayer(lay) for lay in layers]
     T, steps = 1, 6
     ids_all, w_all = synth.streaming_ids(SPEC.replace(n_exp=SPEC.n_exp), 3, N_LAYERS, steps)
@@ -108,6 +116,9 @@ def test_layer_through_cache_equals_resident_layer(torch_cuda, C, host):
             x = torch.from_numpy(synth.activations(SPEC, s, T, step=l)).cuda()
             ids = torch.from_numpy(ids_all[s, l][None].copy()).cuda()
             w = torch.from_numpy(w_all[s, l][None].copy()).cuda()
+            if mode == "queued":
+                torch.cuda._sleep(2_000_000)                    # a busy stream to wait on
+                cache.wait(stream, 10000)
             cache.lookup(l, ids_all[s, l], wait_on=stream)
             if l + 1 < N_LAYERS and s > 0:
                 cache.stage(l + 1, ids_all[s - 1, l + 1])       # next-layer prefetch
@@ -122,8 +133,105 @@ def test_layer_through_cache_equals_resident_layer(torch_cuda, C, host):
     cache.sync()
     st = cache.stats()
     assert st["hits"] + st["misses"] == st["lookups"] == steps * N_LAYERS * SPEC.top_k
-    assert st["bytes_staged"] == (st["misses"] + st["prefetch_staged"]) * nb
+    if mode == "queued":
+        assert st["misses"] * nb <= st["bytes_staged"] <= (st["misses"] + st["prefetch_staged"]) * nb
+        assert st["prefetch_bytes"] > 0
+    else:
+        assert st["bytes_staged"] == (st["misses"] + st["prefetch_staged"]) * nb
+        assert st["prefetch_bytes"] == st["prefetch_staged"] * nb
     assert st["evictions"] > 0
+    cache.close()
+
+
+def test_queued_prefetch_finishes_named_and_cancels_the_rest(torch_cuda, C, host):
+    """Queued, chunked prefetches: the next lookup of their layer finishes the named blobs
+    on the demand stream, from where their chunks stopped, and cancels the others (their
+    slots freed); blobs that finished before the lookup stay resident. The named blobs
+    land byte for byte."""
+    torch = torch_cuda
+    layers, pinned, nb = host
+    copy, pcopy = torch.cuda.Stream(), torch.cuda.Stream()
+    cache, _ = make_cache(torch, C, pinned, 12, copy)
+    chunk = 16384
+    cache.set_prefetch(pcopy, 8, chunk)
+    stream = torch.cuda.current_stream()
+    lay = synth.blob_layout(SPEC.d, SPEC.ffn)
+    per_blob = -(-nb // chunk)
+    # layer 1: guesses 1, 2 right and 3, 9, 10 wrong; blob 1 finishes, blob 2 gets 3 chunks
+    cache.stage(1, np.array([1, 2, 3, 9, 10], np.int32))
+    st = cache.stats()
+    assert st["prefetch_staged"] == 5 and st["prefetch_bytes"] == 0 and st["bytes_staged"] == 0
+    sent = 0
+    while sent < per_blob + 3:
+        sent += cache.pump(per_blob + 3 - sent)
+        pcopy.synchronize()
+    assert cache.stats()["prefetch_bytes"] == nb + 3 * chunk
+    named = np.array([1, 2, 5, 6], np.int32)
+    cache.lookup(1, named, wait_on=stream)
+    torch.cuda.synchronize()
+    cache.sync(5000)
+    st = cache.stats()
+    assert st["prefetch_cancelled"] == 3 and st["prefetch_used"] == 2
+    assert st["misses"] == 2 and st["hits"] == 2
+    assert st["bytes_staged"] == 4 * nb                     # 1 + 2 (finished) + 5 + 6
+    tab = table_entries(torch, C, cache, 1)
+    for e in named:
+        assert np.array_equal(raw_bytes(tab[e].w1 - lay.w1, nb), layers[1].blobs[e]), f"expert {e}"
+    # the cancelled guesses left the cache: looking them up misses
+    before = cache.stats()["misses"]
+    cache.lookup(1, np.array([3, 9, 10, 1], np.int32), wait_on=stream)
+    assert cache.stats()["misses"] - before == 3
+    # a wait on a busy stream sends the queue out; a blob that finished stays resident
+    cache.stage(2, np.array([4, 7], np.int32))
+    torch.cuda._sleep(80_000_000)                           # tens of ms of a busy stream
+    cache.wait(stream, 10000)
+    pcopy.synchronize()
+    st = cache.stats()
+    assert st["prefetch_bytes"] == nb + 3 * chunk + 2 * nb
+    cache.lookup(2, np.array([4, 0, 1, 2], np.int32), wait_on=stream)
+    st2 = cache.stats()
+    assert st2["prefetch_cancelled"] == 3 and st2["prefetch_used"] == 3
+    torch.cuda.synchronize()
+    tab = table_entries(torch, C, cache, 2)
+    assert np.array_equal(raw_bytes(tab[4].w1 - lay.w1, nb), layers[2].blobs[4])
+    cache.close()
+
+
+def test_queued_prefetch_evicted_before_use(torch_cuda, C, host):
+    """A queued prefetch whose slot a demand miss takes is cancelled; copies into the slot
+    stay ordered after the chunks already sent, so both layers' blobs land intact."""
+    torch = torch_cuda
+    layers, pinned, nb = host
+    copy, pcopy = torch.cuda.Stream(), torch.cuda.Stream()
+    cache, _ = make_cache(torch, C, pinned, SPEC.top_k + 1, copy)
+    chunk = 8192
+    cache.set_prefetch(pcopy, 4, chunk)
+    stream = torch.cuda.current_stream()
+    lay = synth.blob_layout(SPEC.d, SPEC.ffn)
+    cache.stage(2, np.arange(SPEC.top_k + 1, dtype=np.int32))   # fills every slot
+    assert cache.pump(4) == 4                                   # part of the first blob
+    first = np.array([0, 1, 2, 3], np.int32)
+    with torch.cuda.stream(copy):
+        torch.cuda._sleep(20_000_000)                           # holds the demand copies back a while
+    cache.lookup(0, first, wait_on=stream)                      # four misses evict four pending prefetches
+    assert cache.pump(4) == 0                                   # demand copies pending: no chunk goes out
+    torch.cuda.synchronize()
+    cache.sync(5000)
+    st = cache.stats()
+    assert st["prefetch_cancelled"] == SPEC.top_k and st["misses"] == SPEC.top_k
+    assert st["prefetch_bytes"] == 4 * chunk
+    tab = table_entries(torch, C, cache, 0)
+    for e in first:
+        assert np.array_equal(raw_bytes(tab[e].w1 - lay.w1, nb), layers[0].blobs[e]), f"layer 0 expert {e}"
+    second = np.array([SPEC.top_k, 5, 6, 7], np.int32)          # the surviving guess is named
+    cache.lookup(2, second, wait_on=stream)
+    torch.cuda.synchronize()
+    cache.sync(5000)
+    st = cache.stats()
+    assert st["prefetch_used"] == 1
+    tab = table_entries(torch, C, cache, 2)
+    for e in second:
+        assert np.array_equal(raw_bytes(tab[e].w1 - lay.w1, nb), layers[2].blobs[e]), f"layer 2 expert {e}"
     cache.close()
 
 

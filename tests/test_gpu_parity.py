@@ -245,6 +245,23 @@ def test_moe_layer_bad_id_reports(torch_cuda, C):
     assert C.colibri_workspace_status(dl.cfg, 1, ws) == C.OK    # read clears it
 
 
+@pytest.mark.parametrize("name,T,f32", [("tiny", 3, False), ("olmoe", 2, False), ("glm52", 1, False),
+                                        ("glm52", 4, False), ("tiny", 40, False), ("glm52", 2, True)])
+def test_router_nan_activation_ranks_lowest(torch_cuda, C, orc, name, T, f32):
+    """A token with a NaN activation has NaN logits. Every selection (decode kernel,
+    prefill and fp32-activation selection kernels) ranks a NaN score as -inf, so the layer
+    still picks the oracle's ids (distinct and valid), reports no error and returns."""
+    torch = torch_cuda
+    spec = synth.SPECS[name]
+    host, dl = dev_layer(C, spec)
+    x = synth.activations(spec, 6, T)
+    x[0, 5] = np.nan
+    _, ids_d, _, ws = (run_layer_f32 if f32 else run_layer)(torch, C, dl, x)
+    ids_o, _ = orc.router_topk(spec, x, host.Wr, host.bias)
+    assert np.array_equal(ids_d, ids_o)
+    assert C.colibri_workspace_status(dl.cfg, T, ws) == C.OK
+
+
 def test_moe_layer_duplicate_id_reports(torch_cuda, C):
     """A token listing the same expert twice is bad input: the device flag reports it."""
     torch = torch_cuda

@@ -202,6 +202,32 @@ def test_router_group_size_one_is_plain_topk(orc):
     assert np.allclose(w, sel / sel.sum(1, keepdims=True) * 2.5, rtol=1e-6)
 
 
+def test_router_nan_scores_rank_lowest(orc):
+    """A NaN score ranks below every number (as -inf, ties by lower index): the ids are
+    those of a stable sort of the scores with NaN replaced by -inf, in both router modes,
+    and a token whose scores are all NaN takes the lowest ids."""
+    rng = np.random.default_rng(21)
+    logits = rng.standard_normal((6, 32)).astype(np.float32)
+    logits[0, [3, 7, 30]] = np.nan
+    logits[1, :] = np.nan
+    logits[2, ::2] = np.nan
+    key = np.where(np.isnan(logits), -np.inf, logits)
+    sig = _cfg(n_exp=32, top_k=5, n_group=1, topk_group=1)
+    ids, _ = orc.router_select(sig, logits, None)
+    assert np.array_equal(ids, np.argsort(-key, axis=1, kind="stable")[:, :5])
+    assert ids[1].tolist() == [0, 1, 2, 3, 4]
+    soft = _cfg(n_exp=32, top_k=5, router="softmax", norm_topk=False, routed_scale=1.0)
+    ids, _ = orc.router_select(soft, logits, None)
+    assert np.array_equal(ids, np.argsort(-key, axis=1, kind="stable")[:, :5])
+    # grouped: a group of NaNs scores -inf and is kept only when nothing else is left
+    grp = _cfg(n_exp=32, top_k=4, n_group=4, topk_group=2)
+    lg = np.zeros((1, 32), np.float32)
+    lg[0, :8] = np.nan
+    lg[0, 8:16] = 1.0
+    ids, _ = orc.router_select(grp, lg, None)
+    assert ids.tolist() == [[8, 9, 10, 11]]
+
+
 def test_router_maximum_shape_bruteforce(orc):
     """The largest router the layer accepts (E = 1024 in 32 groups, top_k = 32): the
     picks equal a brute force over the group choice followed by a plain sort."""
