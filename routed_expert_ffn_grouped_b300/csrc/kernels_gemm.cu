@@ -167,6 +167,40 @@ struct GemmSmem {
     static constexpr int TOTAL = GT_RR * RAW + GT_CQ * CONV + BARS + PRE + XCH + XBARS;
 };
 
+// One group of the epilogue for one warp: per matrix m, NH x 16 TMEM columns of D (at
+// ta + m * 64), then acc += D * (s_w * s_a), two columns per packed instruction. sw: the
+// group's row scales [M][128]; sa: this warp's token scales.
+template <int M, int NH>
+__device__ __forceinline__ void epi_accumulate(float (&acc)[M][32], uint32_t ta, const float *sw, const float *sa,
+                                               int row)
+{
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const float swm = sw[m * UMMA_M + row];
+        uint32_t dv[NH][16];
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+            tmem_ld16_async(ta + m * 64 + 16 * h, dv[h]);
+        tmem_wait_ld();
+        const float2 sw2 = make_float2(swm, swm);
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(sa + 16 * h + j);
+                const float2 q0 = ffma2(sw2, make_float2(v.x, v.y), make_float2(0.f, 0.f));
+                const float2 q1 = ffma2(sw2, make_float2(v.z, v.w), make_float2(0.f, 0.f));
+                float *ac = &acc[m][16 * h + j];
+                const float2 r0 = ffma2(make_float2(__uint_as_float(dv[h][j]), __uint_as_float(dv[h][j + 1])), q0,
+                                        make_float2(ac[0], ac[1]));
+                const float2 r1 = ffma2(make_float2(__uint_as_float(dv[h][j + 2]), __uint_as_float(dv[h][j + 3])), q1,
+                                        make_float2(ac[2], ac[3]));
+                ac[0] = r0.x, ac[1] = r0.y, ac[2] = r1.x, ac[3] = r1.y;
+            }
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
 {
@@ -288,7 +322,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            uint32_t cs = 0, gcount = 0;
+            // one accumulator per quantisation group: a 32-column tile, or with 64-element
+            // groups the two tiles of a group (four K = 16 MMAs into one buffer; the dots
+            // of 64 codes, |sum| <= 65,024, stay exact in fp32)
+            uint32_t cs = 0, acount = 0;  // conversion stages, accumulators
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 GemmItem it;
@@ -296,10 +333,11 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 const int ng = it.kdim / G;
                 const int nn = max(16, (it.nt + 15) & ~15);
                 const uint32_t idesc = umma_idesc_bf16(UMMA_M, nn);
-                for (int g = 0; g < ng; ++g, ++cs, ++gcount) {
-                    const int slot = cs % GT_CQ, tb = gcount % GT_TB;
+                for (int g = 0; g < ng; ++g, ++cs) {
+                    const bool first = (g & gsh) == 0, last = (g & gsh) == gsh;
+                    const int slot = cs % GT_CQ, tb = acount % GT_TB;
                     if (!mbar_wait(&conv_full[slot], (cs / GT_CQ) & 1) ||
-                        (gcount >= GT_TB && !mbar_wait(&tm_empty[tb], ((gcount / GT_TB) - 1) & 1))) {
+                        (first && acount >= GT_TB && !mbar_wait(&tm_empty[tb], ((acount / GT_TB) - 1) & 1))) {
                         fail();
                         ok = false;
                         break;
@@ -316,11 +354,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                         for (int ks = 0; ks < 2; ++ks) {
                             const uint64_t ad = umma_desc(cb + m * L::CA + ks * 256, 128, 32 * 16);
                             const uint64_t bd = umma_desc(cb + M * L::CA + ks * 256, 128, 32 * 16);
-                            umma_bf16(tmem + tb * 128 + m * 64, ad, bd, idesc, ks);
+                            umma_bf16(tmem + tb * 128 + m * 64, ad, bd, idesc, first ? ks : 1);
                         }
                     }
                     umma_commit(&conv_empty[slot]);
-                    umma_commit(&tm_full[tb]);
+                    if (last) {
+                        umma_commit(&tm_full[tb]);
+                        ++acount;
+                    }
                 }
             }
         }
@@ -483,62 +524,45 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
         const int e = warp - GT_EPI0;
         const int q = warp & 3, chalf = e >> 2;  // TMEM lane quarter (rows), token half
         const int row = q * 32 + lane;             // row within the 128-row tile
-        uint32_t cs = 0, gcount = 0, xitems = 0;
+        uint32_t cs = 0, acount = 0, xitems = 0;  // conversion stages, accumulators, items
         bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             GemmItem it;
             gemm_item<MODE>(a, pre, n_slots, item, it);
             const int ng = it.kdim / G;
+            // this warp's token columns in the item's tile; a warp with none (a tile of at
+            // most 32 tokens, second half) skips the arithmetic but keeps the barrier phases
+            const int ncol = min(32, max(0, it.nt - chalf * 32));
             float acc[M][32];
 #pragma unroll
             for (int m = 0; m < M; ++m)
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     acc[m][j] = 0.0f;
-            for (int g = 0; g < ng; ++g, ++cs, ++gcount) {
-                const int slot = cs % GT_CQ, tb = gcount % GT_TB;
-                if (!mbar_wait(&tm_full[tb], (gcount / GT_TB) & 1)) {
+            // one accumulator per quantisation group (one or two conversion stages); its
+            // scales are in the group's last stage
+            for (int g = 0; g < ng; g += 1 + gsh, cs += 1 + gsh, ++acount) {
+                const int slot = (cs + gsh) % GT_CQ, tb = acount % GT_TB;
+                if (!mbar_wait(&tm_full[tb], (acount / GT_TB) & 1)) {
                     if (lane == 0)
                         fail();
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const unsigned char *cb = conv + (size_t)slot * L::CONV;
-                const float *sw = reinterpret_cast<const float *>(cb + M * L::CA + L::CB);
-                const float *sa = sw + M * UMMA_M + chalf * 32;
-                // 16 columns at a time: TMEM -> registers -> fma into the accumulators
-#pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    const float swm = sw[m * UMMA_M + row];
-                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * 128 + m * 64 + chalf * 32;
-                    uint32_t dv[2][16];
-                    tmem_ld16_async(ta, dv[0]);
-                    tmem_ld16_async(ta + 16, dv[1]);
-                    tmem_wait_ld();
-                    const float2 sw2 = make_float2(swm, swm);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 v = *reinterpret_cast<const float4 *>(sa + 16 * h + j);
-                            // acc += D * (s_w * s_a), two columns per packed instruction
-                            const float2 q0 = ffma2(sw2, make_float2(v.x, v.y), make_float2(0.f, 0.f));
-                            const float2 q1 = ffma2(sw2, make_float2(v.z, v.w), make_float2(0.f, 0.f));
-                            float *ac = &acc[m][16 * h + j];
-                            const float2 r0 = ffma2(make_float2(__uint_as_float(dv[h][j]), __uint_as_float(dv[h][j + 1])),
-                                                    q0, make_float2(ac[0], ac[1]));
-                            const float2 r1 = ffma2(make_float2(__uint_as_float(dv[h][j + 2]), __uint_as_float(dv[h][j + 3])),
-                                                    q1, make_float2(ac[2], ac[3]));
-                            ac[0] = r0.x, ac[1] = r0.y, ac[2] = r1.x, ac[3] = r1.y;
-                        }
-                    }
+                if (ncol > 0) {
+                    const unsigned char *cb = conv + (size_t)slot * L::CONV;
+                    const float *sw = reinterpret_cast<const float *>(cb + M * L::CA + L::CB);
+                    const float *sa = sw + M * UMMA_M + chalf * 32;
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * 128 + chalf * 32;
+                    epi_accumulate<M, 2>(acc, ta, sw, sa, row);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&tm_empty[tb]);
-                    mbar_arrive(&conv_empty[slot]);
+                    for (int u = 0; u <= gsh; ++u)
+                        mbar_arrive(&conv_empty[(cs + u) % GT_CQ]);
                 }
             }
             if (!ok)

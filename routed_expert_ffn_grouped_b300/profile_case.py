@@ -1,6 +1,6 @@
 """A GLM-5.2-shaped layer with only the experts it routes to resident, for profiling.
 
-    python -m routed_expert_ffn_grouped_b300.profile_case decode  [--T 1] [--iters 5]
+    python -m routed_expert_ffn_grouped_b300.profile_case decode  [--T 1] [--iters 5] [--f32]
     python -m routed_expert_ffn_grouped_b300.profile_case prefill [--T 512] [--experts 32] [--iters 3]
 
 Each token is given 8 distinct experts out of a fixed set (ids passed in, the router
@@ -8,6 +8,7 @@ skipped), so the device holds only those experts (plus the shared one): the deco
 streams exactly the bytes of one decode step of the full layer (8 routed experts per
 token and the shared expert), with a few hundred MB on the device instead of 6 GB. Runs
 `--iters` layer calls, printing each call's time (CUDA events) and the device status.
+`--f32` runs the decode layer on fp32 activations (colibri_moe_layer_f32) instead.
 """
 from __future__ import annotations
 
@@ -27,6 +28,7 @@ def main():
     p.add_argument("--T", type=int, default=None)
     p.add_argument("--experts", type=int, default=None, help="resident routed experts (prefill)")
     p.add_argument("--iters", type=int, default=5)
+    p.add_argument("--f32", action="store_true", help="decode on fp32 activations")
     a = p.parse_args()
     build.build()
     spec = synth.GLM52
@@ -55,11 +57,14 @@ def main():
     w = torch.full((T, 8), 0.3, dtype=torch.float32, device="cuda")
     x = torch.from_numpy(synth.activations(spec, 0, T)).cuda()
     out = torch.empty((T, spec.d), dtype=torch.float32, device="cuda")
-    ws = torch.empty(C.colibri_moe_workspace_bytes(cfg, T), dtype=torch.uint8, device="cuda")
+    f32 = a.f32 and a.mode == "decode"
+    ws_bytes = (C.colibri_moe_f32_workspace_bytes if f32 else C.colibri_moe_workspace_bytes)(cfg, T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    layer = C.colibri_moe_layer_f32 if f32 else C.colibri_moe_layer
     st, en = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(a.iters):
         st.record()
-        C.colibri_moe_layer(cfg, x, None, None, tdev, shared, idsd, w, True, out, ws)
+        layer(cfg, x, None, None, tdev, shared, idsd, w, True, out, ws)
         en.record()
         torch.cuda.synchronize()
         print(f"call {i}: {st.elapsed_time(en) * 1e3:.1f} us")
