@@ -45,6 +45,7 @@ __device__ __forceinline__ uint4 ld_nc(const void *p)
     return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+
 // sum of four unsigned bytes of a times four signed bytes of b, plus c
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
 {
@@ -169,6 +170,27 @@ __device__ __forceinline__ int q8_code_r(float x, float d, float r)
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Asynchronous global -> shared copies (no registers held while in flight): 16 or 4 bytes
+// to dst, of which src_bytes (0 or the full size) come from src and the rest are zeros;
+// src must be 16- (4-) byte aligned. Complete after cp_async_wait_all() by the issuing
+// thread.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *dst, const void *src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)

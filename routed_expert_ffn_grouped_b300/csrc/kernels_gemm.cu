@@ -92,16 +92,17 @@ size_t debug_umma_smem(int n, int k)
 //   warps 2-5   converters, one group each: nibbles -> bf16 A tiles (magic-number
 //               trick, k in the tensor-core order), the token tile's bf16 codes -> B
 //               tile, and the group's weight and activation scales, into a converted ring;
-//   warps 6-13  epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
-//               32*((w-6)/4).. (its tokens) of each group's D and accumulates
+//   warps 6-21  epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
+//               16*((w-6)/4).. (its tokens) of each group's D and accumulates
 //               D * s_w * s_a in registers; at the end of an item it forms the output.
 constexpr int GT_N = 64;       // tokens per item
 constexpr int GT_GS = 4;       // groups per raw (bulk-copied) stage
 constexpr int GT_RR = 4;       // raw ring stages
 constexpr int GT_CQ = 6;       // converted ring stages
-constexpr int GT_THREADS = 14 * 32;
 constexpr int GT_EPI0 = 6;     // first epilogue warp
-constexpr int GT_NEPI = 8;
+constexpr int GT_NEPI = 16;    // epilogue warps: TMEM lane quarter x 16-column quarter
+constexpr int GT_ECOL = 16;    // token columns per epilogue warp
+constexpr int GT_THREADS = (GT_EPI0 + GT_NEPI) * 32;
 constexpr int GT_TB = 4;       // TMEM accumulator buffers (128 columns each)
 
 struct GemmItem {
@@ -162,41 +163,36 @@ struct GemmSmem {
     static constexpr int PRE = 4 * 1040;  // item prefix over at most 1025 slots
     // 64-element groups: per item parity, epilogue warp and column, the |h| max of the
     // warp's 32 rows; one mbarrier per pair of warps that share a 64-row group
-    static constexpr int XCH = 2 * 4 * GT_NEPI * 32;
+    static constexpr int XCH = 2 * 4 * GT_NEPI * GT_ECOL;
     static constexpr int XBARS = 8 * GT_NEPI / 2;
     static constexpr int TOTAL = GT_RR * RAW + GT_CQ * CONV + BARS + PRE + XCH + XBARS;
 };
 
-// One group of the epilogue for one warp: per matrix m, NH x 16 TMEM columns of D (at
+// One group of the epilogue for one warp: per matrix m, the 16 TMEM columns of D (at
 // ta + m * 64), then acc += D * (s_w * s_a), two columns per packed instruction. sw: the
-// group's row scales [M][128]; sa: this warp's token scales.
-template <int M, int NH>
-__device__ __forceinline__ void epi_accumulate(float (&acc)[M][32], uint32_t ta, const float *sw, const float *sa,
-                                               int row)
+// group's row scales [M][128]; sa: this warp's 16 token scales.
+template <int M>
+__device__ __forceinline__ void epi_accumulate(float (&acc)[M][GT_ECOL], uint32_t ta, const float *sw,
+                                               const float *sa, int row)
 {
 #pragma unroll
     for (int m = 0; m < M; ++m) {
+        uint32_t dv[16];
+        tmem_ld16_async(ta + m * 64, dv);
         const float swm = sw[m * UMMA_M + row];
-        uint32_t dv[NH][16];
-#pragma unroll
-        for (int h = 0; h < NH; ++h)
-            tmem_ld16_async(ta + m * 64 + 16 * h, dv[h]);
         tmem_wait_ld();
         const float2 sw2 = make_float2(swm, swm);
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(sa + 16 * h + j);
-                const float2 q0 = ffma2(sw2, make_float2(v.x, v.y), make_float2(0.f, 0.f));
-                const float2 q1 = ffma2(sw2, make_float2(v.z, v.w), make_float2(0.f, 0.f));
-                float *ac = &acc[m][16 * h + j];
-                const float2 r0 = ffma2(make_float2(__uint_as_float(dv[h][j]), __uint_as_float(dv[h][j + 1])), q0,
-                                        make_float2(ac[0], ac[1]));
-                const float2 r1 = ffma2(make_float2(__uint_as_float(dv[h][j + 2]), __uint_as_float(dv[h][j + 3])), q1,
-                                        make_float2(ac[2], ac[3]));
-                ac[0] = r0.x, ac[1] = r0.y, ac[2] = r1.x, ac[3] = r1.y;
-            }
+        for (int j = 0; j < 16; j += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(sa + j);
+            const float2 q0 = ffma2(sw2, make_float2(v.x, v.y), make_float2(0.f, 0.f));
+            const float2 q1 = ffma2(sw2, make_float2(v.z, v.w), make_float2(0.f, 0.f));
+            float *ac = &acc[m][j];
+            const float2 r0 = ffma2(make_float2(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1])), q0,
+                                    make_float2(ac[0], ac[1]));
+            const float2 r1 = ffma2(make_float2(__uint_as_float(dv[j + 2]), __uint_as_float(dv[j + 3])), q1,
+                                    make_float2(ac[2], ac[3]));
+            ac[0] = r0.x, ac[1] = r0.y, ac[2] = r1.x, ac[3] = r1.y;
         }
     }
 }
@@ -371,74 +367,35 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
         // groups convert at once. Lane l handles rows l, l+32, l+64, l+96 of the 128-row
         // weight tile (512 contiguous bytes per row block and group) and tokens l, l+32
         // of the token tile. Nibbles become bf16 by a mask and the magic exponent 0x4300
-        // (128 + nibble) minus 136, in the tensor-core k order. The activations of the
-        // warp's next group are loaded one chunk ahead, so their L2 latency hides behind
-        // the current chunk.
+        // (128 + nibble) minus 136, in the tensor-core k order. The token tile (bf16 codes,
+        // zeros past the item's tokens) and the tokens' scales go straight from global to
+        // shared memory by asynchronous copies issued first, so their L2 latency hides
+        // behind the weight conversion and they hold no registers.
         const int cw = warp - 2;
         uint32_t rs = 0, cb0 = 0;  // raw chunks seen, conversion stages of earlier chunks
         bool ok = true;
-        struct Chunk {
-            int item, g0, ng;
-            long arow[2];
-            GemmItem it;
-        };
-        auto chunk_at = [&](int item, int g0, Chunk &ck) -> bool {
-            if (item >= n_items)
-                return false;
-            ck.item = item;
-            ck.g0 = g0;
-            gemm_item<MODE>(a, pre, n_slots, item, ck.it);
-            ck.ng = ck.it.kdim / G;
+        int item = blockIdx.x, g0 = 0;
+        GemmItem it;
+        long arow[2] = {-1, -1};
+        auto item_rows = [&]() {
+            gemm_item<MODE>(a, pre, n_slots, item, it);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int tn = lane + 32 * h;
-                ck.arow[h] = -1;
-                if (tn < ck.it.nt) {
-                    const int cidx = ck.it.n0 + tn;
+                arow[h] = -1;
+                if (tn < it.nt) {
+                    const int cidx = it.n0 + tn;
                     if (MODE == MODE_GATEUP)
-                        ck.arow[h] = ck.it.is_shared ? cidx : a.pairs[ck.it.begin + cidx] / a.K;
+                        arow[h] = it.is_shared ? cidx : a.pairs[it.begin + cidx] / a.K;
                     else
-                        ck.arow[h] = ck.it.is_shared ? (long)a.T * a.K + cidx : a.pairs[ck.it.begin + cidx];
-                }
-            }
-            return true;
-        };
-        auto next_of = [&](const Chunk &ck, Chunk &nx) -> bool {
-            if (ck.g0 + GT_GS < ck.ng) {
-                nx = ck;
-                nx.g0 = ck.g0 + GT_GS;
-                return true;
-            }
-            return chunk_at(ck.item + gridDim.x, 0, nx);
-        };
-        // this warp's group of a chunk: tokens lane, lane+32, four 16-byte chunks each
-        uint4 vc[2][4], vn[2][4];
-        float sc[2], sn[2];
-        auto load_acts = [&](const Chunk &ck, uint4 (&v)[2][4], float (&sv)[2]) {
-            const int g = ck.g0 + cw;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                sv[h] = 0.0f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    v[h][q] = make_uint4(0, 0, 0, 0);
-                if (ck.arow[h] >= 0 && g < ck.ng) {
-                    const uint16_t *src = a.abf + ck.arow[h] * a.act_stride + (long)g * G;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        v[h][q] = ld_nc(src + 8 * q);
-                    sv[h] = a.as[ck.arow[h] * a.act_groups + (g >> gsh)];
+                        arow[h] = it.is_shared ? (long)a.T * a.K + cidx : a.pairs[it.begin + cidx];
                 }
             }
         };
-        Chunk cur, nxt;
-        bool have = chunk_at(blockIdx.x, 0, cur);
-        if (have)
-            load_acts(cur, vc, sc);
-        while (ok && have) {
-            const bool more = next_of(cur, nxt);
-            if (more)
-                load_acts(nxt, vn, sn);
+        if (item < n_items)
+            item_rows();
+        while (ok && item < n_items) {
+            const int ng = it.kdim / G;
             const int rslot = rs % GT_RR;
             if (!mbar_wait(&raw_full[rslot], (rs / GT_RR) & 1)) {
                 if (lane == 0)
@@ -447,7 +404,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 break;
             }
             const unsigned char *rb = raw + (size_t)rslot * L::RAW;
-            const int n = min(GT_GS, cur.ng - cur.g0);
+            const int n = min(GT_GS, ng - g0);
             if (cw < n) {
                 const uint32_t cs = cb0 + cw;
                 const int slot = cs % GT_CQ;
@@ -458,6 +415,19 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 }
                 if (ok) {
                     unsigned char *cb = conv + (size_t)slot * L::CONV;
+                    const int g = g0 + cw;
+                    float *sa_dst = reinterpret_cast<float *>(cb + M * L::CA + L::CB + M * UMMA_M * 4);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int tn = lane + 32 * h;
+                        const bool valid = arow[h] >= 0;
+                        const uint16_t *src = valid ? a.abf + arow[h] * a.act_stride + (long)g * G : a.abf;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            cp_async16(cb + M * L::CA + umma_off(tn, 8 * q, 32), src + 8 * q, valid ? 16 : 0);
+                        cp_async4(sa_dst + tn, valid ? a.as + arow[h] * a.act_groups + (g >> gsh) : a.as,
+                                  valid ? 4 : 0);
+                    }
                     const __nv_bfloat162 off136 = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
                     for (int m = 0; m < M; ++m) {
@@ -475,9 +445,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
 #pragma unroll
                                 for (int s2 = 0; s2 < 4; ++s2) {
                                     const uint32_t u = ((wv[j] >> (4 * s2)) & 0x000F000Fu) | 0x43004300u;
-                                    const __nv_bfloat162 h =
+                                    const __nv_bfloat162 hv =
                                         __hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&u), off136);
-                                    o[s2] = *reinterpret_cast<const uint32_t *>(&h);
+                                    o[s2] = *reinterpret_cast<const uint32_t *>(&hv);
                                 }
                                 *reinterpret_cast<uint4 *>(cb + m * L::CA + umma_off(r, 8 * j, 32)) =
                                     make_uint4(o[0], o[1], o[2], o[3]);
@@ -487,15 +457,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                                                                  (blk * GT_GS + (cw >> gsh)) * 128 + lane * 4);
                         }
                     }
-                    // the token tile (zeros past the tile's tokens) and the tokens' scales
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int tn = lane + 32 * h;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            *reinterpret_cast<uint4 *>(cb + M * L::CA + umma_off(tn, 8 * q, 32)) = vc[h][q];
-                        reinterpret_cast<float *>(cb + M * L::CA + L::CB + M * UMMA_M * 4)[tn] = sc[h];
-                    }
+                    cp_async_wait_all();
                     fence_async_smem();
                     __syncwarp();
                     if (lane == 0)
@@ -509,20 +471,18 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 mbar_arrive(&raw_empty[rslot]);
             ++rs;
             cb0 += n;
-            cur = nxt;
-            have = more;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                sc[h] = sn[h];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    vc[h][q] = vn[h][q];
+            g0 += GT_GS;
+            if (g0 >= ng) {
+                g0 = 0;
+                item += gridDim.x;
+                if (item < n_items)
+                    item_rows();
             }
         }
     } else {
-        // ---------------- epilogue (256 threads) ----------------
+        // ---------------- epilogue (512 threads) ----------------
         const int e = warp - GT_EPI0;
-        const int q = warp & 3, chalf = e >> 2;  // TMEM lane quarter (rows), token half
+        const int q = warp & 3, cq = e >> 2;  // TMEM lane quarter (rows), token quarter
         const int row = q * 32 + lane;             // row within the 128-row tile
         uint32_t cs = 0, acount = 0, xitems = 0;  // conversion stages, accumulators, items
         bool ok = true;
@@ -530,14 +490,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
             GemmItem it;
             gemm_item<MODE>(a, pre, n_slots, item, it);
             const int ng = it.kdim / G;
-            // this warp's token columns in the item's tile; a warp with none (a tile of at
-            // most 32 tokens, second half) skips the arithmetic but keeps the barrier phases
-            const int ncol = min(32, max(0, it.nt - chalf * 32));
-            float acc[M][32];
+            // a warp whose token quarter of the item's tile is empty skips the arithmetic
+            // but keeps the barrier phases
+            const bool has_cols = it.nt > cq * GT_ECOL;
+            float acc[M][GT_ECOL];
 #pragma unroll
             for (int m = 0; m < M; ++m)
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < GT_ECOL; ++j)
                     acc[m][j] = 0.0f;
             // one accumulator per quantisation group (one or two conversion stages); its
             // scales are in the group's last stage
@@ -550,12 +510,12 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                     break;
                 }
                 tc_fence_after();
-                if (ncol > 0) {
+                if (has_cols) {
                     const unsigned char *cb = conv + (size_t)slot * L::CONV;
                     const float *sw = reinterpret_cast<const float *>(cb + M * L::CA + L::CB);
-                    const float *sa = sw + M * UMMA_M + chalf * 32;
-                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * 128 + chalf * 32;
-                    epi_accumulate<M, 2>(acc, ta, sw, sa, row);
+                    const float *sa = sw + M * UMMA_M + cq * GT_ECOL;
+                    const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + tb * 128 + cq * GT_ECOL;
+                    epi_accumulate<M>(acc, ta, sw, sa, row);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -567,19 +527,19 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
             }
             if (!ok)
                 break;
-            // item output: columns chalf*32 + j < nt are tokens n0 + that of the slot
+            // item output: columns cq * GT_ECOL + j < nt are tokens n0 + that of the slot
             const int orow = it.mt * UMMA_M + row;  // output row (h row or d row)
             if (MODE == MODE_GATEUP) {
                 // h, then |h| max per column over the 32 rows of this warp; with 64-element
                 // groups the two warps holding rows 64p..64p+63 (TMEM lane quarters 2p and
-                // 2p + 1, same column half) exchange theirs (hardware barrier 2 + pair)
+                // 2p + 1, same token quarter) exchange theirs through shared memory
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < GT_ECOL; ++j) {
                     const float gt = acc[0][j], up = acc[M - 1][j];
                     acc[0][j] = gt / (1.0f + expf(-gt)) * up;
                     const float m = warp_max(fabsf(acc[0][j]));
                     if (gsh && lane == 0)
-                        xch[((int)(xitems & 1) * GT_NEPI + e) * 32 + j] = m;
+                        xch[((int)(xitems & 1) * GT_NEPI + e) * GT_ECOL + j] = m;
                     acc[M - 1][j] = m;
                 }
                 if (gsh) {
@@ -599,14 +559,14 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                     }
                     ++xitems;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        acc[M - 1][j] = fmaxf(acc[M - 1][j], xch[(buf * GT_NEPI + partner) * 32 + j]);
+                    for (int j = 0; j < GT_ECOL; ++j)
+                        acc[M - 1][j] = fmaxf(acc[M - 1][j], xch[(buf * GT_NEPI + partner) * GT_ECOL + j]);
                 }
             }
             const int gq = a.group;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int col = chalf * 32 + j;
+            for (int j = 0; j < GT_ECOL; ++j) {
+                const int col = cq * GT_ECOL + j;
                 const bool valid = col < it.nt;
                 long pr = 0;
                 if (valid) {
