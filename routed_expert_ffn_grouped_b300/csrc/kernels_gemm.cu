@@ -89,19 +89,21 @@ size_t debug_umma_smem(int n, int k)
 //               (four 32-row blocks per matrix, contiguous runs) into a raw ring;
 //   warp 1      MMA issuer (one thread): per group, two K = 16 MMAs per matrix into a
 //               fresh TMEM accumulator (GT_TB buffers), then commits;
-//   warps 2-5   converters, one group each: nibbles -> bf16 A tiles (magic-number
-//               trick, k in the tensor-core order), the token tile's bf16 codes -> B
-//               tile, and the group's weight and activation scales, into a converted ring;
-//   warps 6-21  epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
-//               16*((w-6)/4).. (its tokens) of each group's D and accumulates
+//   warps 2-7   converters, two per 32-column tile (64 weight rows and 32 tokens each):
+//               nibbles -> bf16 A tiles (magic-number trick, k in the tensor-core order),
+//               the token tile's bf16 codes -> B tile, and the tile's weight and
+//               activation scales, into a converted ring;
+//   warps 8-15  epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
+//               32*((w-8)/4).. (its tokens) of each group's D and accumulates
 //               D * s_w * s_a in registers; at the end of an item it forms the output.
 constexpr int GT_N = 64;       // tokens per item
-constexpr int GT_GS = 4;       // groups per raw (bulk-copied) stage
+constexpr int GT_GS = 3;       // 32-column tiles per raw (bulk-copied) stage
 constexpr int GT_RR = 4;       // raw ring stages
 constexpr int GT_CQ = 6;       // converted ring stages
-constexpr int GT_EPI0 = 6;     // first epilogue warp
-constexpr int GT_NEPI = 16;    // epilogue warps: TMEM lane quarter x 16-column quarter
-constexpr int GT_ECOL = 16;    // token columns per epilogue warp
+constexpr int GT_NCONV = 2 * GT_GS;  // converter warps: two per tile of a raw chunk
+constexpr int GT_EPI0 = 2 + GT_NCONV;  // first epilogue warp
+constexpr int GT_NEPI = 8;     // epilogue warps: TMEM lane quarter x 32-column half
+constexpr int GT_ECOL = 32;    // token columns per epilogue warp
 constexpr int GT_THREADS = (GT_EPI0 + GT_NEPI) * 32;
 constexpr int GT_TB = 4;       // TMEM accumulator buffers (128 columns each)
 
@@ -168,31 +170,36 @@ struct GemmSmem {
     static constexpr int TOTAL = GT_RR * RAW + GT_CQ * CONV + BARS + PRE + XCH + XBARS;
 };
 
-// One group of the epilogue for one warp: per matrix m, the 16 TMEM columns of D (at
+// One group of the epilogue for one warp: per matrix m, the GT_ECOL TMEM columns of D (at
 // ta + m * 64), then acc += D * (s_w * s_a), two columns per packed instruction. sw: the
-// group's row scales [M][128]; sa: this warp's 16 token scales.
+// group's row scales [M][128]; sa: this warp's GT_ECOL token scales.
 template <int M>
 __device__ __forceinline__ void epi_accumulate(float (&acc)[M][GT_ECOL], uint32_t ta, const float *sw,
                                                const float *sa, int row)
 {
+    constexpr int NH = GT_ECOL / 16;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-        uint32_t dv[16];
-        tmem_ld16_async(ta + m * 64, dv);
         const float swm = sw[m * UMMA_M + row];
-        tmem_wait_ld();
         const float2 sw2 = make_float2(swm, swm);
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(sa + j);
-            const float2 q0 = ffma2(sw2, make_float2(v.x, v.y), make_float2(0.f, 0.f));
-            const float2 q1 = ffma2(sw2, make_float2(v.z, v.w), make_float2(0.f, 0.f));
-            float *ac = &acc[m][j];
-            const float2 r0 = ffma2(make_float2(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1])), q0,
-                                    make_float2(ac[0], ac[1]));
-            const float2 r1 = ffma2(make_float2(__uint_as_float(dv[j + 2]), __uint_as_float(dv[j + 3])), q1,
-                                    make_float2(ac[2], ac[3]));
-            ac[0] = r0.x, ac[1] = r0.y, ac[2] = r1.x, ac[3] = r1.y;
+        for (int h = 0; h < NH; ++h) {
+            // 16 columns at a time: the registers of one load beside the accumulators
+            uint32_t dv[16];
+            tmem_ld16_async(ta + m * 64 + 16 * h, dv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(sa + 16 * h + j);
+                const float2 q0 = ffma2(sw2, make_float2(v.x, v.y), make_float2(0.f, 0.f));
+                const float2 q1 = ffma2(sw2, make_float2(v.z, v.w), make_float2(0.f, 0.f));
+                float *ac = &acc[m][16 * h + j];
+                const float2 r0 = ffma2(make_float2(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1])), q0,
+                                        make_float2(ac[0], ac[1]));
+                const float2 r1 = ffma2(make_float2(__uint_as_float(dv[j + 2]), __uint_as_float(dv[j + 3])), q1,
+                                        make_float2(ac[2], ac[3]));
+                ac[0] = r0.x, ac[1] = r0.y, ac[2] = r1.x, ac[3] = r1.y;
+            }
         }
     }
 }
@@ -224,10 +231,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
         if (lane == 0) {
             for (int i = 0; i < GT_RR; ++i) {
                 mbar_init(&raw_full[i], 1);
-                mbar_init(&raw_empty[i], 4);
+                mbar_init(&raw_empty[i], GT_NCONV);
             }
             for (int i = 0; i < GT_CQ; ++i) {
-                mbar_init(&conv_full[i], 1);
+                mbar_init(&conv_full[i], 2);
                 mbar_init(&conv_empty[i], 1 + GT_NEPI);
             }
             for (int i = 0; i < GT_TB; ++i) {
@@ -293,7 +300,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                         break;
                     }
                     const int n = min(GT_GS, ng - g0);
-                    const int ns = n >> gsh;  // scale tiles (one per group)
+                    // scale tiles (one per group) of the groups the chunk's tiles belong to;
+                    // with 64-element groups a chunk may start or end inside a group
+                    const int ns = ((g0 + n - 1) >> gsh) - (g0 >> gsh) + 1;
                     unsigned char *dst = raw + (size_t)slot * L::RAW;
                     mbar_arrive_expect_tx(&raw_full[slot], (uint32_t)(M * 4 * (n * 512 + ns * 128)));
 #pragma unroll
@@ -362,34 +371,33 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
             }
         }
     } else if (warp < GT_EPI0) {
-        // ---------------- converters (4 warps) ----------------
-        // Converter warp cw takes group cw of each raw chunk (GS = 4 groups), so four
-        // groups convert at once. Lane l handles rows l, l+32, l+64, l+96 of the 128-row
-        // weight tile (512 contiguous bytes per row block and group) and tokens l, l+32
-        // of the token tile. Nibbles become bf16 by a mask and the magic exponent 0x4300
+        // ---------------- converters (6 warps) ----------------
+        // Converter warps cw and cw + 3 take tile cw of each raw chunk (GS = 3 tiles), half
+        // the work each, so three tiles convert at once (a single warp's conversion is
+        // latency-bound: two warps halve a tile's latency). Half hf handles row blocks
+        // 2hf, 2hf + 1 of the 128-row weight tile (lane l: rows 64hf + l and 64hf + 32 + l;
+        // 512 contiguous bytes per row block and group) and token 32hf + l of the token
+        // tile. Nibbles become bf16 by a mask and the magic exponent 0x4300
         // (128 + nibble) minus 136, in the tensor-core k order. The token tile (bf16 codes,
         // zeros past the item's tokens) and the tokens' scales go straight from global to
         // shared memory by asynchronous copies issued first, so their L2 latency hides
         // behind the weight conversion and they hold no registers.
-        const int cw = warp - 2;
+        const int cw = (warp - 2) % GT_GS, hf = (warp - 2) / GT_GS;
         uint32_t rs = 0, cb0 = 0;  // raw chunks seen, conversion stages of earlier chunks
         bool ok = true;
         int item = blockIdx.x, g0 = 0;
         GemmItem it;
-        long arow[2] = {-1, -1};
+        long arow = -1;  // activation row of this lane's token
+        const int tn = lane + 32 * hf;
         auto item_rows = [&]() {
             gemm_item<MODE>(a, pre, n_slots, item, it);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int tn = lane + 32 * h;
-                arow[h] = -1;
-                if (tn < it.nt) {
-                    const int cidx = it.n0 + tn;
-                    if (MODE == MODE_GATEUP)
-                        arow[h] = it.is_shared ? cidx : a.pairs[it.begin + cidx] / a.K;
-                    else
-                        arow[h] = it.is_shared ? (long)a.T * a.K + cidx : a.pairs[it.begin + cidx];
-                }
+            arow = -1;
+            if (tn < it.nt) {
+                const int cidx = it.n0 + tn;
+                if (MODE == MODE_GATEUP)
+                    arow = it.is_shared ? cidx : a.pairs[it.begin + cidx] / a.K;
+                else
+                    arow = it.is_shared ? (long)a.T * a.K + cidx : a.pairs[it.begin + cidx];
             }
         };
         if (item < n_items)
@@ -416,23 +424,23 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                 if (ok) {
                     unsigned char *cb = conv + (size_t)slot * L::CONV;
                     const int g = g0 + cw;
-                    float *sa_dst = reinterpret_cast<float *>(cb + M * L::CA + L::CB + M * UMMA_M * 4);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int tn = lane + 32 * h;
-                        const bool valid = arow[h] >= 0;
-                        const uint16_t *src = valid ? a.abf + arow[h] * a.act_stride + (long)g * G : a.abf;
+                    float *sw_dst = reinterpret_cast<float *>(cb + M * L::CA + L::CB);
+                    float *sa_dst = sw_dst + M * UMMA_M;
+                    {
+                        const bool valid = arow >= 0;
+                        const uint16_t *src = valid ? a.abf + arow * a.act_stride + (long)g * G : a.abf;
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             cp_async16(cb + M * L::CA + umma_off(tn, 8 * q, 32), src + 8 * q, valid ? 16 : 0);
-                        cp_async4(sa_dst + tn, valid ? a.as + arow[h] * a.act_groups + (g >> gsh) : a.as,
+                        cp_async4(sa_dst + tn, valid ? a.as + arow * a.act_groups + (g >> gsh) : a.as,
                                   valid ? 4 : 0);
                     }
                     const __nv_bfloat162 off136 = __floats2bfloat162_rn(136.0f, 136.0f);
 #pragma unroll
                     for (int m = 0; m < M; ++m) {
 #pragma unroll
-                        for (int blk = 0; blk < 4; ++blk) {
+                        for (int bb = 0; bb < 2; ++bb) {
+                            const int blk = 2 * hf + bb;
                             const int r = blk * 32 + lane;
                             const uint4 w =
                                 *reinterpret_cast<const uint4 *>(rb + m * L::RAW_W + (blk * GT_GS + cw) * 512 + lane * 16);
@@ -452,9 +460,10 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                                 *reinterpret_cast<uint4 *>(cb + m * L::CA + umma_off(r, 8 * j, 32)) =
                                     make_uint4(o[0], o[1], o[2], o[3]);
                             }
-                            reinterpret_cast<float *>(cb + M * L::CA + L::CB)[m * UMMA_M + r] =
+                            sw_dst[m * UMMA_M + r] =
                                 *reinterpret_cast<const float *>(rb + M * L::RAW_W + m * L::RAW_S +
-                                                                 (blk * GT_GS + (cw >> gsh)) * 128 + lane * 4);
+                                                                 (blk * GT_GS + (((g0 + cw) >> gsh) - (g0 >> gsh))) * 128 +
+                                                                 lane * 4);
                         }
                     }
                     cp_async_wait_all();
@@ -480,9 +489,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
             }
         }
     } else {
-        // ---------------- epilogue (512 threads) ----------------
+        // ---------------- epilogue (256 threads) ----------------
         const int e = warp - GT_EPI0;
-        const int q = warp & 3, cq = e >> 2;  // TMEM lane quarter (rows), token quarter
+        const int q = warp & 3, cq = e >> 2;  // TMEM lane quarter (rows), token half
         const int row = q * 32 + lane;             // row within the 128-row tile
         uint32_t cs = 0, acount = 0, xitems = 0;  // conversion stages, accumulators, items
         bool ok = true;
@@ -490,7 +499,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
             GemmItem it;
             gemm_item<MODE>(a, pre, n_slots, item, it);
             const int ng = it.kdim / G;
-            // a warp whose token quarter of the item's tile is empty skips the arithmetic
+            // a warp whose token half of the item's tile is empty skips the arithmetic
             // but keeps the barrier phases
             const bool has_cols = it.nt > cq * GT_ECOL;
             float acc[M][GT_ECOL];
@@ -532,7 +541,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
             if (MODE == MODE_GATEUP) {
                 // h, then |h| max per column over the 32 rows of this warp; with 64-element
                 // groups the two warps holding rows 64p..64p+63 (TMEM lane quarters 2p and
-                // 2p + 1, same token quarter) exchange theirs through shared memory
+                // 2p + 1, same token half) exchange theirs through shared memory
 #pragma unroll
                 for (int j = 0; j < GT_ECOL; ++j) {
                     const float gt = acc[0][j], up = acc[M - 1][j];
@@ -543,7 +552,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) k_gemm(GemmArgs a)
                     acc[M - 1][j] = m;
                 }
                 if (gsh) {
-                    // warps 6 + e pair up as (e, e ^ 1): TMEM lane quarters (2, 3) and (0, 1);
+                    // warps GT_EPI0 + e pair up as (e, e ^ 1): TMEM lane quarters (2, 3) and (0, 1);
                     // one bounded mbarrier phase per item, the exchange area double-buffered
                     // by item parity (a warp writes buffer p again only after the partner
                     // has arrived for the item in between, so after it read buffer p)
