@@ -58,6 +58,7 @@ WORKLOADS = {
     # eight resident GLM-shaped layers in one launch (colibri_moe_stack_decode)
     "glm52_decode_t1_stack8": ("glm52", 1, False),
     "glm52_decode_t4_stack8": ("glm52", 4, False),
+    "olmoe_decode_t1_stack8": ("olmoe", 1, False),
 }
 STACK_LAYERS = 8
 DEFAULT_WORKLOAD = "glm52_decode_t1"
@@ -927,13 +928,14 @@ def run_colibri(args):
 
 
 def run_stack_decode(args):
-    """Eight resident GLM-shaped layers per step, each with activations of its own (as when
+    """Eight resident layers of one shape per step, each with activations of its own (as when
     attention sits between a model's MoE layers; a bare chain of SwiGLU layers, out into x,
     overflows within a few layers): one colibri_moe_stack_decode launch, timed with CUDA
     events around a graph replay, beside the same eight layers as eight colibri_moe_layer
     calls in one graph. The layers are one drawn layer and device copies of it whose
     router rows are rolled (each routes elsewhere, and their weights sit at other
-    addresses); 8 x 6 GB of weights keep every step's bytes far above the L2."""
+    addresses); 8 x 6 GB of GLM-shaped weights keep every step's bytes far above the L2
+    (the OLMoE-shaped stack, 8 x 0.25 GB, streams its 8 x 31.5 MB per step through it)."""
     import torch
     from routed_expert_ffn_grouped_b300 import build as cbuild
     from routed_expert_ffn_grouped_b300 import colibri as C
@@ -1030,7 +1032,7 @@ def run_stack_decode(args):
             "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": total_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "i8xi4->i32, f32", "data": "synthetic",
             "config": dict(workload_config(spec, args.workload, T), layers=L_, inputs="each layer its own activations (no chaining)",
-                           l2="no flush: each step streams 8 layers' weights (far above L2)",
+                           l2="no flush between steps: each step reads 8 layers' weights once",
                            timing="CUDA events per step around one CUDA-graph replay of the 8-layer launch"),
             "us_per_layer": total_ms / K / L_ * 1e3,
             "sequential_us_per_layer": float(np.mean(seq_ms)) / L_ * 1e3,
