@@ -11,14 +11,14 @@
 //
 // Items are claimed from a device counter, in the order: the logit items (a block of
 // router rows against a block of tokens, streamed in K-chunks), the shared expert's
-// gate/up items, the routed slots' gate/up items, then the down items slot by slot. The
-// CTA that completes the last logit item selects the experts of every token (one warp per
-// token, from the scores the logit items left in the workspace), buckets the pairs and
-// publishes the routing table with a flag; every other CTA streams the shared expert
-// meanwhile and copies the table into its shared memory when it reaches a routed item. A
-// CTA processes its items in claim order, so every wait below is for work claimed earlier
-// by a running CTA and ends: the table waits for the logit items, a down item for the
-// gate/up items of its slot.
+// gate/up items, the routed slots' gate/up items, then the down items slot by slot. Once
+// a device counter holds every logit task and every q8 group of x, each CTA selects the
+// experts of every token itself (the whole CTA by rank counting, or a warp per token when
+// the scores of all tokens do not fit), from the scores the logit items left in the
+// workspace, buckets the pairs into its shared memory and goes on to the routed items;
+// CTA 0 also writes the routing results out. A CTA processes its items in claim order, so
+// every wait below is for work claimed earlier by a running CTA and ends: routing waits
+// for the logit items, a down item for the gate/up items of its slot.
 //
 // One CTA per SM, three roles. The producer warp claims items (two ahead, so a claim's
 // latency hides behind the copies of the items before) and streams each item through a
@@ -1053,7 +1053,6 @@ template <int TCH>
 __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
 {
     const int NS = a.ring, NH = a.nh;
-    const int P = a.T * a.K;
     if (a.has_shared)
         prefetch_shared(a);
     if (blockIdx.x == 0)
