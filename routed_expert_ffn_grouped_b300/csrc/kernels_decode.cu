@@ -121,7 +121,7 @@ __host__ __device__ __forceinline__ size_t route_scratch_bytes(int T, int E, int
     size_t b = (8 * (size_t)T * K + 16 + 15) & ~size_t(15);
     const size_t Ep = (E + 3) & ~3;
     if (select && select_all_at_once(T, E))
-        b += 2 * (size_t)T * Ep * 4 + (size_t)T * 32 * 16;  // c and s rows, group scores, kept, picks
+        b += 2 * (size_t)T * Ep * 4 + (size_t)T * 32 * 20;  // c and s rows, group scores, kept, picks, kept list
     else if (select)
         b += (size_t)sel_warps * (8 * Ep + 128);
     return b;
@@ -651,41 +651,49 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
         }
         named_sync(1, NT);
     }
-    // rank of each allowed candidate, two adjacent threads a candidate (each counts over
-    // every other allowed group), added with one shuffle
-    const bool vec = (gs & 3) == 0;
-    const int half = tid & 1;
-    for (int base = 0; base < T * E; base += NT / 2) {
-        const int i = base + (tid >> 1);
-        const bool live = i < T * E;
-        const int t = live ? i / E : 0, e = live ? i - t * E : 0;
-        const bool allowed = live && (!sig || kept[t * 32 + e / gs]);
-        int rank = 0;
-        if (allowed) {
-            const float *row = cs + (size_t)t * Ep;
-            const float v = row[e];
-            for (int g = half; g < NG; g += 2) {
-                if (sig && !kept[t * 32 + g])
-                    continue;
-                if (vec) {
-                    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-                    const float4 *q4 = reinterpret_cast<const float4 *>(row);
-                    for (int j = g * gs; j < (g + 1) * gs; j += 4) {
-                        const float4 x = q4[j >> 2];
-                        r0 += beats(x.x, j, v, e);
-                        r1 += beats(x.y, j + 1, v, e);
-                        r2 += beats(x.z, j + 2, v, e);
-                        r3 += beats(x.w, j + 3, v, e);
-                    }
-                    rank += r0 + r1 + r2 + r3;
-                } else {
-                    for (int j = g * gs; j < (g + 1) * gs; ++j)
-                        rank += beats(row[j], j, v, e);
+    // rank of each allowed candidate, one thread a candidate: the allowed candidates of its
+    // token that beat it, counted as those with a larger c plus those with an equal c and a
+    // lower index, over the kept groups listed in shared memory
+    int *klist = reinterpret_cast<int *>(ps + (size_t)T * 32);  // [T][32] kept group ids
+    if (sig) {
+        for (int t = warp; t < T; t += NC) {
+            const bool k = lane < NG && kept[t * 32 + lane];
+            const unsigned m = __ballot_sync(FULL, k);
+            if (k)
+                klist[t * 32 + __popc(m & ((1u << lane) - 1))] = lane;
+        }
+        named_sync(1, NT);
+    }
+    const int nk = sig ? a.topk_group : 1;
+    for (int i = tid; i < T * E; i += NT) {
+        const int t = i / E, e = i - t * E;
+        if (sig && !kept[t * 32 + e / gs])
+            continue;
+        const float *row = cs + (size_t)t * Ep;
+        const float v = row[e];
+        int gt = 0, eq = 0;
+        for (int kk = 0; kk < nk; ++kk) {
+            const int j0 = (sig ? klist[t * 32 + kk] : 0) * gs, j1 = j0 + gs;
+            int j = j0;
+            if ((gs & 7) == 0) {
+                for (; j < j1; j += 8) {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(row + j);
+                    const float4 x1 = *reinterpret_cast<const float4 *>(row + j + 4);
+                    gt += (x0.x > v) + (x0.y > v) + (x0.z > v) + (x0.w > v) + (x1.x > v) + (x1.y > v) + (x1.z > v) +
+                          (x1.w > v);
+                    eq += (x0.x == v && j < e) + (x0.y == v && j + 1 < e) + (x0.z == v && j + 2 < e) +
+                          (x0.w == v && j + 3 < e) + (x1.x == v && j + 4 < e) + (x1.y == v && j + 5 < e) +
+                          (x1.z == v && j + 6 < e) + (x1.w == v && j + 7 < e);
                 }
             }
+            for (; j < j1; ++j) {
+                const float x = row[j];
+                gt += x > v;
+                eq += x == v && j < e;
+            }
         }
-        rank += __shfl_xor_sync(FULL, rank, 1);
-        if (allowed && half == 0 && rank < K) {
+        const int rank = gt + eq;
+        if (rank < K) {
             pick[t * 32 + rank] = e;
             ps[t * 32 + rank] = sig ? ss[t * Ep + e] : cs[t * Ep + e];
         }
