@@ -700,22 +700,6 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
     }
     named_sync(1, NT);
     for (int t = warp; t < T; t += NC) {
-        double m = 0.0, z = 1.0;
-        if (!sig) {
-            const float *l = cs + (size_t)t * Ep;
-            m = -INFINITY;
-            for (int i = lane; i < E; i += 32)
-                m = fmax(m, (double)l[i]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                m = fmax(m, __shfl_xor_sync(FULL, m, o));
-            z = 0.0;
-            for (int i = lane; i < E; i += 32)
-                z += exp((double)l[i] - m);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                z += __shfl_xor_sync(FULL, z, o);
-        }
         float wt = 0.0f;
         if (sig) {
             // compensated (TwoSum) sum of the k scores in selection order, one division
@@ -730,15 +714,47 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             const float sum = hi + lo;
             wt = (a.norm_topk ? __fdiv_rn(sv, sum) : sv) * a.routed_scale;
         } else {
-            double p = 0.0;
-            if (lane < K)
-                p = exp((double)ps[t * 32 + lane] - m) / z;
-            double sum = 0.0;
-            for (int i = 0; i < K; ++i)
-                sum += __shfl_sync(FULL, p, i);
-            if (a.norm_topk)
-                p = p / sum;
-            wt = (float)(p * (double)a.routed_scale);
+            // softmax weights in fp32, within a few 1e-7 of the fp64 definition: each
+            // exp(l - m) takes the argument's rounding error back to first order (the error
+            // of l - m is exact by TwoSum), expf errs by at most 2 ulp, and the sums over
+            // the experts and the picks are compensated (fp64 exp on this part's small fp64
+            // rate took several microseconds per token)
+            const float *l = cs + (size_t)t * Ep;
+            float m = -INFINITY;
+            for (int i = lane; i < E; i += 32)
+                m = fmaxf(m, l[i]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+            auto ex = [&](float x) {
+                const float d = x - m, bb = d - x;
+                const float err = (x - (d - bb)) + (-m - bb);  // d + err == x - m exactly
+                const float e = expf(d);
+                return fmaf(e, err, e);
+            };
+            auto add2 = [](float &hi, float &lo, float x) {  // TwoSum accumulate
+                const float u = hi + x, bb = u - hi;
+                lo += (hi - (u - bb)) + (x - bb);
+                hi = u;
+            };
+            float zh = 0.0f, zl = 0.0f;
+            for (int i = lane; i < E; i += 32)
+                add2(zh, zl, ex(l[i]));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float oh = __shfl_xor_sync(FULL, zh, o), ol = __shfl_xor_sync(FULL, zl, o);
+                add2(zh, zl, oh);
+                zl += ol;
+            }
+            const float z = zh + zl;
+            float p = lane < K ? __fdiv_rn(ex(ps[t * 32 + lane]), z) : 0.0f;
+            if (a.norm_topk) {
+                float sh = 0.0f, sl = 0.0f;
+                for (int i = 0; i < K; ++i)
+                    add2(sh, sl, __shfl_sync(FULL, p, i));
+                p = __fdiv_rn(p, sh + sl);
+            }
+            wt = p * a.routed_scale;
         }
         if (lane < K) {
             const int id = pick[t * 32 + lane];
@@ -861,9 +877,19 @@ __device__ bool bucket_cta(const DecodeArgs &a, const RingSmem &s, const int *si
         const int e = sids[p];
         const bool valid = e >= 0 && e < E;
         bool dup = false, fst = valid;
-        for (int q = 0; q < p; ++q) {
+        const int tok0 = p - p % K;
+        int q = 0;
+        if ((P & 3) == 0) {
+            for (; q + 4 <= p; q += 4) {
+                const int4 e4 = *reinterpret_cast<const int4 *>(sids + q);
+                const bool s0 = e4.x == e, s1 = e4.y == e, s2 = e4.z == e, s3 = e4.w == e;
+                dup |= (s0 && q >= tok0) || (s1 && q + 1 >= tok0) || (s2 && q + 2 >= tok0) || (s3 && q + 3 >= tok0);
+                fst &= !(s0 || s1 || s2 || s3);
+            }
+        }
+        for (; q < p; ++q) {
             const bool same = sids[q] == e;
-            dup |= same && q >= p - p % K;
+            dup |= same && q >= tok0;
             fst &= !same;
         }
         if (writer && (!valid || dup))
@@ -876,19 +902,30 @@ __device__ bool bucket_cta(const DecodeArgs &a, const RingSmem &s, const int *si
     }
     named_sync(1, NT);
     const int sbase = a.has_shared ? 1 : 0;
+    // four pairs a 16-byte load when the two arrays allow it (P a multiple of 4)
+    const int P4 = (P & 3) == 0 ? P : 0;
     for (int p = tid; p < P; p += NT) {
         const int e = sids[p];
         if (e < 0 || e >= E)
             continue;
         int less = 0, pos = 0, cnt = 0, dless = 0;
-        for (int q = 0; q < P; ++q) {
-            const int eq = sids[q];
+        auto count = [&](int q, int eq, int fq) {
             const bool v = eq >= 0 && eq < E;
             less += v && eq < e;
             pos += q < p && eq == e;
             cnt += eq == e;
-            dless += first[q] && eq < e;
+            dless += fq && eq < e;
+        };
+        for (int q = 0; q < P4; q += 4) {
+            const int4 e4 = *reinterpret_cast<const int4 *>(sids + q);
+            const int4 f4 = *reinterpret_cast<const int4 *>(first + q);
+            count(q, e4.x, f4.x);
+            count(q + 1, e4.y, f4.y);
+            count(q + 2, e4.z, f4.z);
+            count(q + 3, e4.w, f4.w);
         }
+        for (int q = P4; q < P; ++q)
+            count(q, sids[q], first[q]);
         s.ptab[less + pos] = p;
         if (writer)
             a.pairs[less + pos] = p;
