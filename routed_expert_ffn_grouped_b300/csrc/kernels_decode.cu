@@ -1098,8 +1098,6 @@ template <int TCH>
 __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
 {
     const int NS = a.ring, NH = a.nh;
-    if (a.has_shared)
-        prefetch_shared(a);
     if (blockIdx.x == 0)
         prefetch_l2(a.experts, (uint32_t)(((size_t)a.E * sizeof(colibri_expert) + 15) & ~size_t(15)));
     grid_dep_wait();  // inputs and the zeroed counters are in
@@ -1140,6 +1138,10 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
             mbar_arrive(&s.full[slot]);
             ++st;
             route_posted = true;
+            // the shared expert towards L2 only now: the router rows of the logit items,
+            // on the routing critical path, go first
+            if (a.has_shared)
+                prefetch_shared(a);
         }
         if (!have_table && idx >= pre) {
             // the consumers' routing table (slots, pairs, counters) in shared memory
