@@ -145,6 +145,16 @@ def test_argument_errors_detected_on_host(lib):
     assert lib.colibri_lru_trace(0, 0, None, None, None) == C.E_INVAL
 
 
+def test_cache_prefetch_entry_points_check_arguments(lib):
+    """The prefetch-queue entry points refuse a missing cache or bad counts before touching
+    a device."""
+    import ctypes as ct
+    n = ct.c_int(7)
+    assert lib.colibri_expert_cache_set_prefetch(None, None, 2, 1 << 20) == C.E_INVAL
+    assert lib.colibri_expert_cache_wait(None, None, 100) == C.E_INVAL
+    assert lib.colibri_expert_cache_pump(None, 4, ct.byref(n)) == C.E_INVAL
+
+
 def test_cache_policy_matches_oracle(lib, orc):
     rng = np.random.default_rng(11)
     for cap in (1, 3, 8):
