@@ -602,9 +602,18 @@ __device__ void select_warp(const DecodeArgs &a, int t, float *cs, float *ss, in
 // position rank; groups are kept the same way. Sigmoid mode: group score = sum of the
 // group's two largest biased scores c, top topk_group groups, top_k by c inside them,
 // w = s / sum(s) * routed_scale with a compensated fp32 sum in selection order. Softmax
-// mode: top_k by logit, w = softmax over all experts in fp64. Writes the ids and weights
-// to sids and s.wtab; the writer CTA also to the caller's ids and w. Used when the scores of
-// all T tokens fit the scratch (T * E <= 4096); select_warp otherwise.
+// mode: top_k by logit, w = softmax over all experts (fp32, compensated). Writes the ids
+// and weights to sids and s.wtab; the writer CTA also to the caller's ids and w. Used when
+// the scores of all T tokens fit the scratch (T * E <= 4096); select_warp otherwise.
+//
+// Chunked form (groups of at most 32 experts in sigmoid mode, runs of 32 experts in softmax
+// mode, when the kept chunks' best kk = min(top_k, chunk) fit one warp): one warp a (token,
+// chunk) ranks the chunk's experts among themselves, one lane an expert, and lists its kk
+// best in order (the two best give the group score); then one warp a token ranks the
+// listed experts of its kept chunks among themselves. Every expert of the overall top_k is
+// among the kk best of its own chunk under the same order, so the picks are the same as
+// ranking every allowed expert against every other, at a quarter of the comparisons or
+// less.
 __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, int *sids, bool writer, uint32_t &cph,
                            int tid, int warp, int lane)
 {
@@ -625,7 +634,45 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             ss[t * Ep + e] = __ldcg(a.rs + i);
     }
     named_sync(1, NT);
-    if (sig) {
+    // chunks: the groups (sigmoid) or runs of 32 experts (softmax); kk best listed a chunk
+    const int cl = sig ? gs : min(E, 32), nch = (E + cl - 1) / cl, kk = min(K, cl);
+    const int nkept = sig ? a.topk_group : nch;
+    const bool chunked = cl <= 32 && nch <= 32 && nch * kk <= 64 && nkept * kk <= 32;
+    int16_t *ctop = reinterpret_cast<int16_t *>(ps + (size_t)T * 32);  // [T][64]: chunk ch at ch * kk
+    if (chunked) {
+        for (int i = warp; i < T * nch; i += NC) {
+            const int t = i / nch, ch = i - t * nch;
+            const int base = ch * cl, len = min(cl, E - base);
+            const float *row = cs + (size_t)t * Ep + base;
+            const bool live = lane < len;
+            const float v = live ? row[lane] : -INFINITY;
+            int r = 0;  // the chunk's experts that beat this lane's
+            if (len == 32) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(row + j);
+                    r += (x.x > v || (x.x == v && j < lane)) + (x.y > v || (x.y == v && j + 1 < lane)) +
+                         (x.z > v || (x.z == v && j + 2 < lane)) + (x.w > v || (x.w == v && j + 3 < lane));
+                }
+            } else {
+                for (int j = 0; j < len; ++j) {
+                    const float x = row[j];
+                    r += x > v || (x == v && j < lane);
+                }
+            }
+            if (live && r < kk)
+                ctop[t * 64 + ch * kk + r] = (int16_t)(base + lane);
+            if (sig) {
+                const unsigned m0 = __ballot_sync(FULL, live && r == 0), m1 = __ballot_sync(FULL, live && r == 1);
+                const float v0 = __shfl_sync(FULL, v, __ffs(m0) - 1);
+                const float v1 = __shfl_sync(FULL, v, m1 ? __ffs(m1) - 1 : 0);
+                if (lane == 0)
+                    gsc[t * 32 + ch] = len == 1 ? v0 : v0 + v1;
+            }
+        }
+        named_sync(1, NT);
+    }
+    if (!chunked && sig) {
         for (int i = warp; i < T * NG; i += NC) {
             const int t = i / NG, g = i - t * NG;
             const float *row = cs + (size_t)t * Ep + g * gs;
@@ -655,7 +702,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
     // token that beat it, counted as those with a larger c plus those with an equal c and a
     // lower index, over the kept groups listed in shared memory
     int *klist = reinterpret_cast<int *>(ps + (size_t)T * 32);  // [T][32] kept group ids
-    if (sig) {
+    if (!chunked && sig) {
         for (int t = warp; t < T; t += NC) {
             const bool k = lane < NG && kept[t * 32 + lane];
             const unsigned m = __ballot_sync(FULL, k);
@@ -665,7 +712,7 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
         named_sync(1, NT);
     }
     const int nk = sig ? a.topk_group : 1;
-    for (int i = tid; i < T * E; i += NT) {
+    for (int i = chunked ? T * E : tid; i < T * E; i += NT) {
         const int t = i / E, e = i - t * E;
         if (sig && !kept[t * 32 + e / gs])
             continue;
@@ -698,8 +745,47 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             ps[t * 32 + rank] = sig ? ss[t * Ep + e] : cs[t * Ep + e];
         }
     }
-    named_sync(1, NT);
+    if (!chunked)
+        named_sync(1, NT);
     for (int t = warp; t < T; t += NC) {
+        if (chunked) {
+            // the kept chunks (ascending), then lane q * kk + r holds the r-th best of the
+            // q-th kept chunk and counts the listed experts that beat it
+            unsigned kmask;
+            if (sig) {
+                const float gv = lane < nch ? gsc[t * 32 + lane] : 0.0f;
+                int rk = 0;
+                for (int h = 0; h < nch; ++h)
+                    rk += beats(gsc[t * 32 + h], h, gv, lane);
+                kmask = __ballot_sync(FULL, lane < nch && rk < a.topk_group);
+            } else {
+                kmask = nch == 32 ? FULL : (1u << nch) - 1u;
+            }
+            const int q = lane / kk, r = lane - q * kk;
+            unsigned mm = kmask;
+            for (int z = 0; z < q && mm; ++z)
+                mm &= mm - 1u;
+            int e = -1;
+            if (lane < nkept * kk && mm) {
+                const int ch = __ffs(mm) - 1;
+                if (r < min(kk, E - ch * cl))
+                    e = ctop[t * 64 + ch * kk + r];
+            }
+            const bool valid = e >= 0;
+            const float v = valid ? cs[(size_t)t * Ep + e] : -INFINITY;
+            const unsigned vm = __ballot_sync(FULL, valid);
+            int rank = 0;
+            for (int c = 0; c < nkept * kk; ++c) {
+                const float xv = __shfl_sync(FULL, v, c);
+                const int xe = __shfl_sync(FULL, e, c);
+                rank += ((vm >> c) & 1u) && beats(xv, xe, v, e);
+            }
+            if (valid && rank < K) {
+                pick[t * 32 + rank] = e;
+                ps[t * 32 + rank] = sig ? ss[(size_t)t * Ep + e] : v;
+            }
+            __syncwarp();
+        }
         float wt = 0.0f;
         if (sig) {
             // compensated (TwoSum) sum of the k scores in selection order, one division
@@ -1062,6 +1148,43 @@ __device__ __forceinline__ void consume(const unsigned char *stg, const int8_t *
     constexpr int M = 2;
     constexpr int scale_off = M * SG * 512;
     const int n = min(SG, ng - g0);
+    if (n == SG) {
+        // a full stage (every stage but an item's ragged last one): the warp's weight words
+        // and scales of all its tiles are loaded up front, so that the dot chains of the
+        // tiles overlap instead of running one tile after the other; the sums per (m, t)
+        // still run over the tiles in ascending order
+        uint4 wv[GPW][M];
+        float sw[GPW][M];
+#pragma unroll
+        for (int u = 0; u < GPW; ++u) {
+            const int j = warp + u * NC;
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                wv[u][m] = *reinterpret_cast<const uint4 *>(stg + (m * SG + j) * 512 + lane * 16);
+                sw[u][m] = *reinterpret_cast<const float *>(stg + scale_off + (m * SG + (j >> gsh)) * 128 + lane * 4);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TCH; ++t) {
+            if (t < nt) {
+                const int r = rows[t];
+#pragma unroll
+                for (int u = 0; u < GPW; ++u) {
+                    const int g = g0 + warp + u * NC;
+                    const uint4 *xa = reinterpret_cast<const uint4 *>(codes + (size_t)r * cstride + g * G);
+                    const uint4 A0 = xa[0], A1 = xa[1];
+                    const int cr = corr[r * gstride + g];
+                    const float sa = sc[r * sstride + (g >> gsh)];
+#pragma unroll
+                    for (int m = 0; m < M; ++m) {
+                        const int D = dot_split(split_nibbles(wv[u][m]), A0, A1, cr);
+                        acc[m][t] = fmaf((float)D, sw[u][m] * sa, acc[m][t]);
+                    }
+                }
+            }
+        }
+        return;
+    }
 #pragma unroll
     for (int u = 0; u < GPW; ++u) {
         const int j = warp + u * NC;
