@@ -64,8 +64,8 @@ __host__ __device__ constexpr int round_up(int v, int m)
     return (v + m - 1) / m * m;
 }
 
-struct DecItem {
-    int mode, slot, is_shared, rb, begin, count, kdim;
+struct __align__(16) DecItem {
+    int mode, slot, is_shared, rb, begin, count, kdim, pad;
 };
 
 // One slot as the kernel keeps it in shared memory: its expert's matrices and its run of
@@ -101,7 +101,7 @@ struct ChunkDesc {
 // Shared memory beside the ring: see ring_layout().
 struct RingLayout {
     size_t full, empty, hfull, hempty, cbar, tbar, xbar, pfull, pempty, tag, flags, ctab, desc, stab, ptab, wtab,
-        act, hbuf, part, total;
+        act, hbuf, part, sitem, total;
     size_t hb;  // bytes of one h buffer
 };
 
@@ -144,7 +144,7 @@ __host__ __device__ __forceinline__ size_t x_area_bytes(int d, int tch)
 
 // ring [ns][STAGE_BYTES] | full [ns] | empty [ns] | hfull [NH_MAX] | hempty [NH_MAX] |
 // consumer barrier | table barrier | x barrier | pfull [NE_MAX] | pempty [NE_MAX] | stage tags [ns]
-// (int2) | flags (16 B) | counters | chunk descriptors [NE_MAX] | slot table [max_slots] |
+// (int2) | stage items [ns] (the producer's work item of each stage) | flags (16 B) | counters | chunk descriptors [NE_MAX] | slot table [max_slots] |
 // pair list [T*K] | weights [T*K] | x staging area | h buffers [nh] (codes [TCH][fmax] |
 // scales [TCH][hgs] | corrections [TCH][hgs]) | partial sums [NBUF][NC][2][TCH][32]
 // (before the first chunk: the routing scratch).
@@ -169,6 +169,7 @@ __host__ __device__ __forceinline__ RingLayout ring_layout(const DecodeArgs &a, 
     L.pfull = take(8 * NE_MAX, 8);
     L.pempty = take(8 * NE_MAX, 8);
     L.tag = take(8 * (size_t)ns, 8);
+    L.sitem = take(sizeof(DecItem) * (size_t)ns, 16);
     L.flags = take(16, 16);
     L.ctab = take(sizeof(Counters), 16);
     L.desc = take(sizeof(ChunkDesc) * NE_MAX, 16);
@@ -191,6 +192,7 @@ struct RingSmem {
     unsigned char *ring;
     uint64_t *full, *empty, *hfull, *hempty, *cbar, *tbar, *xbar, *pfull, *pempty;
     int2 *tag;
+    DecItem *sitem;  // the work item of the stage in each ring slot, as the producer decoded it
     int *flags;  // [0] abort, [1] valid pairs, [2] distinct experts, [3] this CTA routes
     Counters *ctab;
     ChunkDesc *desc;
@@ -217,6 +219,7 @@ __device__ __forceinline__ RingSmem carve(unsigned char *sm, const DecodeArgs &a
     s.pfull = reinterpret_cast<uint64_t *>(sm + L.pfull);
     s.pempty = reinterpret_cast<uint64_t *>(sm + L.pempty);
     s.tag = reinterpret_cast<int2 *>(sm + L.tag);
+    s.sitem = reinterpret_cast<DecItem *>(sm + L.sitem);
     s.flags = reinterpret_cast<int *>(sm + L.flags);
     s.ctab = reinterpret_cast<Counters *>(sm + L.ctab);
     s.desc = reinterpret_cast<ChunkDesc *>(sm + L.desc);
@@ -264,17 +267,11 @@ __device__ __forceinline__ int shared_gu_items(const DecodeArgs &a)
     return a.has_shared ? a.shared_ffn / G : 0;
 }
 
-// One past the last gate/up item, as far as item idx needs it: the shared expert's
-// gate/up items need no routing; past them the routing table (s.ctab) must be loaded.
-__device__ __forceinline__ int gu_end(const DecodeArgs &a, const Counters *ctab, int idx)
-{
-    const int pre = a.n_logit + shared_gu_items(a);
-    return idx < pre ? pre : a.n_logit + ctab->n_items_gateup;
-}
-
-// Work item idx of the claim order, given n_gu (gu_end). The logit items and the shared
-// expert's items (slot 0) need nothing written by routing; the routed slots come from the
-// table.
+// Work item idx of the claim order, given n_gu (one past the last gate/up item: before the
+// routing table is in, the end of the shared expert's items). The logit items and the
+// shared expert's items (slot 0) need nothing written by routing; the routed slots come
+// from the table. The producer decodes each item once and leaves it beside each of its
+// stages for the consumer warps.
 __device__ __forceinline__ DecItem work_item(const DecodeArgs &a, const SlotInfo *stab, int n_gu, int idx)
 {
     DecItem it{};
@@ -755,8 +752,11 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             if (sig) {
                 const float gv = lane < nch ? gsc[t * 32 + lane] : 0.0f;
                 int rk = 0;
-                for (int h = 0; h < nch; ++h)
-                    rk += beats(gsc[t * 32 + h], h, gv, lane);
+#pragma unroll
+                for (int h = 0; h < 32; ++h) {
+                    const float x = __shfl_sync(FULL, gv, h);
+                    rk += h < nch && beats(x, h, gv, lane);
+                }
                 kmask = __ballot_sync(FULL, lane < nch && rk < a.topk_group);
             } else {
                 kmask = nch == 32 ? FULL : (1u << nch) - 1u;
@@ -774,8 +774,9 @@ __device__ bool select_cta(const DecodeArgs &a, const RingSmem &s, float *scr, i
             const bool valid = e >= 0;
             const float v = valid ? cs[(size_t)t * Ep + e] : -INFINITY;
             const unsigned vm = __ballot_sync(FULL, valid);
-            int rank = 0;
-            for (int c = 0; c < nkept * kk; ++c) {
+            int rank = 0;  // lanes without a candidate are outside vm
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
                 const float xv = __shfl_sync(FULL, v, c);
                 const int xe = __shfl_sync(FULL, e, c);
                 rank += ((vm >> c) & 1u) && beats(xv, xe, v, e);
@@ -1299,6 +1300,7 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
                     break;
                 }
                 s.tag[slot] = make_int2(idx, c);
+                s.sitem[slot] = it;
                 {
                     const LogitItem li = logit_item(a, idx);
                     const int kc = a.lg_kc, k0 = c * kc, kcl = min(kc, a.d - k0);
@@ -1395,6 +1397,7 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
             const int g0 = k * SG, n = min(SG, ng - g0);
             unsigned char *dst = s.ring + (size_t)slot * STAGE_BYTES;
             s.tag[slot] = make_int2(idx, k | (ch << 8) | flag);
+            s.sitem[slot] = it;
             const int ns = n >> gsh, s0 = g0 >> gsh;  // the stage's scale tiles
             mbar_arrive_expect_tx(&s.full[slot], (uint32_t)((two ? 2 : 1) * (n * 512 + ns * 128)));
             bulk_g2s_hint(dst, wa + (size_t)g0 * 512, n * 512, &s.full[slot], pol);
@@ -1657,7 +1660,7 @@ __device__ void run_consumers(const DecodeArgs &a, const RingSmem &s, int warp, 
         }
         if (tag.x != cur) {
             cur = tag.x;
-            it = work_item(a, s.stab, gu_end(a, s.ctab, cur), cur);
+            it = s.sitem[slot];  // decoded once, by the producer
             ng = it.kdim / G;
             spi = (ng + SG - 1) / SG;
         }
