@@ -16,9 +16,11 @@
 // experts of every token itself (the whole CTA by rank counting, or a warp per token when
 // the scores of all tokens do not fit), from the scores the logit items left in the
 // workspace, buckets the pairs into its shared memory and goes on to the routed items;
-// CTA 0 also writes the routing results out. A CTA processes its items in claim order, so
-// every wait below is for work claimed earlier by a running CTA and ends: routing waits
-// for the logit items, a down item for the gate/up items of its slot.
+// CTA 0 also writes the routing results out. CTA b's first item is item b; the counter
+// hands out the rest in order. A CTA processes its items in claim order and an item waits
+// only for items of lower index, each held by a running CTA (the first items all at once,
+// the rest claimed earlier), so every wait below ends: routing waits for the logit items,
+// a down item for the gate/up items of its slot.
 //
 // One CTA per SM, three roles. The producer warp claims items (two ahead, so a claim's
 // latency hides behind the copies of the items before) and streams each item through a
@@ -911,6 +913,9 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
     const bool fst = valid && (same & below) == 0;
     if (writer && live && (!valid || dup))
         atomicOr(a.err, ERR_BAD_ID);
+    colibri_expert ex{};
+    if (fst)
+        ex = a.experts[e];  // in flight during the counting below
     const unsigned fmask = __ballot_sync(FULL, fst);
     const int n_valid = __popc(__ballot_sync(FULL, valid)), n_routed = __popc(fmask);
     int less = 0, dless = 0;
@@ -927,7 +932,7 @@ __device__ void bucket_warp(const DecodeArgs &a, const RingSmem &s, const int *s
             a.pairs[less + pos] = lane;
         if (fst) {
             SlotInfo si;
-            si.ex = a.experts[e];
+            si.ex = ex;
             si.begin = less;
             si.count = __popc(same);
             si.pad[0] = si.pad[1] = 0;
@@ -960,32 +965,42 @@ __device__ bool bucket_cta(const DecodeArgs &a, const RingSmem &s, const int *si
                            uint32_t &cph, int tid, int lane)
 {
     const int T = a.T, K = a.K, E = a.E, P = T * K;
-    for (int p = tid; p < P; p += NT) {
-        const int e = sids[p];
-        const bool valid = e >= 0 && e < E;
+    // whole warps take the pairs (lane l pair p0 + l), so the two counts go in with one
+    // shared-memory atomic per warp
+    for (int p0 = tid & ~31; p0 < P; p0 += NT) {
+        const int p = p0 + lane;
+        const bool live = p < P;
+        const int e = live ? sids[p] : -1;
+        const bool valid = live && e >= 0 && e < E;
         bool dup = false, fst = valid;
-        const int tok0 = p - p % K;
-        int q = 0;
-        if ((P & 3) == 0) {
-            for (; q + 4 <= p; q += 4) {
-                const int4 e4 = *reinterpret_cast<const int4 *>(sids + q);
-                const bool s0 = e4.x == e, s1 = e4.y == e, s2 = e4.z == e, s3 = e4.w == e;
-                dup |= (s0 && q >= tok0) || (s1 && q + 1 >= tok0) || (s2 && q + 2 >= tok0) || (s3 && q + 3 >= tok0);
-                fst &= !(s0 || s1 || s2 || s3);
+        if (live) {
+            const int tok0 = p - p % K;
+            int q = 0;
+            if ((P & 3) == 0) {
+                for (; q + 4 <= p; q += 4) {
+                    const int4 e4 = *reinterpret_cast<const int4 *>(sids + q);
+                    const bool s0 = e4.x == e, s1 = e4.y == e, s2 = e4.z == e, s3 = e4.w == e;
+                    dup |= (s0 && q >= tok0) || (s1 && q + 1 >= tok0) || (s2 && q + 2 >= tok0) ||
+                           (s3 && q + 3 >= tok0);
+                    fst &= !(s0 || s1 || s2 || s3);
+                }
             }
+            for (; q < p; ++q) {
+                const bool same = sids[q] == e;
+                dup |= same && q >= tok0;
+                fst &= !same;
+            }
+            if (writer && (!valid || dup))
+                atomicOr(a.err, ERR_BAD_ID);
+            first[p] = fst;
         }
-        for (; q < p; ++q) {
-            const bool same = sids[q] == e;
-            dup |= same && q >= tok0;
-            fst &= !same;
+        const int nv = __popc(__ballot_sync(FULL, valid)), nf = __popc(__ballot_sync(FULL, fst));
+        if (lane == 0) {
+            if (nv)
+                atomicAdd(&s.flags[1], nv);
+            if (nf)
+                atomicAdd(&s.flags[2], nf);
         }
-        if (writer && (!valid || dup))
-            atomicOr(a.err, ERR_BAD_ID);
-        first[p] = fst;
-        if (valid)
-            atomicAdd(&s.flags[1], 1);
-        if (fst)
-            atomicAdd(&s.flags[2], 1);
     }
     named_sync(1, NT);
     const int sbase = a.has_shared ? 1 : 0;
@@ -995,6 +1010,10 @@ __device__ bool bucket_cta(const DecodeArgs &a, const RingSmem &s, const int *si
         const int e = sids[p];
         if (e < 0 || e >= E)
             continue;
+        const bool fst = first[p];
+        colibri_expert ex{};
+        if (fst)
+            ex = a.experts[e];  // in flight during the counting below
         int less = 0, pos = 0, cnt = 0, dless = 0;
         auto count = [&](int q, int eq, int fq) {
             const bool v = eq >= 0 && eq < E;
@@ -1016,9 +1035,9 @@ __device__ bool bucket_cta(const DecodeArgs &a, const RingSmem &s, const int *si
         s.ptab[less + pos] = p;
         if (writer)
             a.pairs[less + pos] = p;
-        if (first[p]) {
+        if (fst) {
             SlotInfo si;
-            si.ex = a.experts[e];
+            si.ex = ex;
             si.begin = less;
             si.count = cnt;
             si.pad[0] = si.pad[1] = 0;
@@ -1250,8 +1269,11 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
     };
     // claims run two items ahead of the item being streamed, except behind a logit item:
     // the next claim waits until the logit item's bytes have landed, so that the logit
-    // items (claimed first) spread over all CTAs instead of pairing up
-    int idx = atomicAdd(a.claim, 1), ahead = idx < a.n_logit ? -1 : atomicAdd(a.claim, 1);
+    // items (claimed first) spread over all CTAs instead of pairing up. Each CTA's first
+    // item is its own index (no counter round trip before the first copy); the counter
+    // hands out the items from gridDim.x on, in order
+    auto claim = [&]() { return (int)gridDim.x + atomicAdd(a.claim, 1); };
+    int idx = blockIdx.x, ahead = idx < a.n_logit ? -1 : claim();
     for (bool run = true; run;) {
         if (!route_posted && idx >= a.n_logit) {
             // past this CTA's logit items: the consumers route next (an empty stage)
@@ -1288,7 +1310,7 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
         }
         int next = ahead;
         if (next >= 0)
-            ahead = atomicAdd(a.claim, 1);  // used two items from now
+            ahead = claim();  // used two items from now
         const DecItem it = work_item(a, s.stab, n_gu, idx);
         if (it.mode == MODE_LOGIT) {
             // chunk c: the item's token rows of x and its router rows over columns
@@ -1322,8 +1344,8 @@ __device__ void run_producer(const DecodeArgs &a, const RingSmem &s)
                     set_abort(a, s);
                     break;
                 }
-                next = atomicAdd(a.claim, 1);
-                ahead = next < a.n_logit ? -1 : atomicAdd(a.claim, 1);
+                next = claim();
+                ahead = next < a.n_logit ? -1 : claim();
             }
             idx = next;
             continue;
