@@ -317,8 +317,11 @@ static int launch_route_logits(const colibri_layer_cfg *cfg, const float *x, int
                 return COLIBRI_E_CUDA;
         }
         ra.q8.x = nullptr;
+        static SmemLimits have_tiled;
+        if (!smem_attr((const void *)k_route_logits_tiled, ROUTE_TILED_SMEM, have_tiled))
+            return COLIBRI_E_CUDA;
         dim3 grid((T + 15) / 16, (cfg->n_exp + 31) / 32);
-        k_route_logits_tiled<<<grid, 256, 0, s>>>(ra);
+        k_route_logits_tiled<<<grid, 256, ROUTE_TILED_SMEM, s>>>(ra);
         return cuda_status(cudaGetLastError());
     }
     if (!smem_attr((const void *)k_route_logits, smem, have))

@@ -182,6 +182,7 @@ struct CombineArgs {
 __global__ void k_q8(Q8Args a);
 __global__ void k_route_logits(RouterArgs a);
 __global__ void k_route_logits_tiled(RouterArgs a);
+constexpr size_t ROUTE_TILED_SMEM = 2 * (16 + 32) * 256 * 4;  // two stages of a 16-token x 32-expert tile, 256 columns
 size_t bucket_smem_bytes(int E, int nthreads);
 __global__ void k_router_select(SelectArgs a);
 __global__ void k_bucket(BucketArgs a);

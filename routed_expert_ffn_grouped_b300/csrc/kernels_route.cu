@@ -127,14 +127,16 @@ __device__ bool route_logits_part(const RouterArgs &a, unsigned char *smem_raw, 
 
 // ---- router logits for many tokens: (16 tokens x 32 experts) tiles --------------------
 // The same fixed summation order as route_logits_part: lane j of a warp keeps chain j
-// (k = j, j+32, ... ascending, fmaf) for each of its (token, expert) pairs; a K-chunk of x
-// and of Wr is staged in shared memory for the whole CTA. Warp w owns experts 4w..4w+3
+// (k = j, j+32, ... ascending, fmaf) for each of its (token, expert) pairs; K-chunks of x
+// and of Wr are staged in shared memory for the whole CTA by cp.async, two stages deep, so
+// that the next chunk's copies run while the current one is summed. Warp w owns experts 4w..4w+3
 // of the tile and all 16 tokens: 64 chains a lane. The chains of each pair are then
 // added in the halving-tree pairs (16, 8, 4, 2, 1) by a transpose reduction: each step
 // adds the same two partial sums as the tree, only in another lane, so the result is the
 // tree's bit for bit; lane l ends with pair l and pair 32 + l, and evaluates their
 // sigmoid scores (fp64) in parallel.
 constexpr int RT_T = 16, RT_E = 32, RT_KC = 256;
+static_assert(ROUTE_TILED_SMEM == 2 * (RT_T + RT_E) * RT_KC * sizeof(float), "launch size of the tiled router");
 
 template <int N>
 __device__ __forceinline__ float tree_reduce_lanes(float (&v)[N], int lane)
@@ -156,33 +158,46 @@ __device__ __forceinline__ float tree_reduce_lanes(float (&v)[N], int lane)
 
 __global__ void __launch_bounds__(256, 2) k_route_logits_tiled(RouterArgs a)
 {
-    __shared__ __align__(16) float xs[RT_T][RT_KC];
-    __shared__ __align__(16) float ws[RT_E][RT_KC];
+    extern __shared__ __align__(16) float rt_smem[];  // [2] x (xs [RT_T][RT_KC], ws [RT_E][RT_KC])
+    constexpr int STAGE = (RT_T + RT_E) * RT_KC;
     const int d = a.d, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
     const int nt = min(RT_T, a.T - t0), ne = min(RT_E, a.E - e0);
+    const int nck = (d + RT_KC - 1) / RT_KC;
+    // K-chunk c of the tile's rows of x and Wr into stage c & 1; rows past the tile are
+    // zero-filled (a copy of 0 source bytes from the tile's first row)
+    auto stage_chunk = [&](int c) {
+        float *xs = rt_smem + (c & 1) * STAGE, *ws = xs + RT_T * RT_KC;
+        const int k0 = c * RT_KC, q = min(RT_KC, d - k0) / 4;
+        for (int i = threadIdx.x; i < (RT_T + RT_E) * q; i += blockDim.x) {
+            const int r = i / q, col = (i - r * q) * 4;
+            if (r < RT_T) {
+                const bool live = r < nt;
+                cp_async16(xs + r * RT_KC + col, a.x + (long)(t0 + (live ? r : 0)) * d + k0 + col, live ? 16u : 0u);
+            } else {
+                const int e = r - RT_T;
+                const bool live = e < ne;
+                cp_async16(ws + e * RT_KC + col, a.Wr + (long)(e0 + (live ? e : 0)) * d + k0 + col, live ? 16u : 0u);
+            }
+        }
+        cp_async_commit();
+    };
     float acc[RT_T * 4];  // [expert 4w+i][token t]: index i * 16 + t
 #pragma unroll
     for (int i = 0; i < RT_T * 4; ++i)
         acc[i] = 0.0f;
-    for (int k0 = 0; k0 < d; k0 += RT_KC) {
-        const int kc = min(RT_KC, d - k0);  // a multiple of 32
-        __syncthreads();
-        for (int i = threadIdx.x; i < RT_T * (kc / 4); i += blockDim.x) {
-            const int t = i / (kc / 4), c = (i % (kc / 4)) * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < nt)
-                v = *reinterpret_cast<const float4 *>(a.x + (long)(t0 + t) * d + k0 + c);
-            *reinterpret_cast<float4 *>(&xs[t][c]) = v;
-        }
-        for (int i = threadIdx.x; i < RT_E * (kc / 4); i += blockDim.x) {
-            const int e = i / (kc / 4), c = (i % (kc / 4)) * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e < ne)
-                v = *reinterpret_cast<const float4 *>(a.Wr + (long)(e0 + e) * d + k0 + c);
-            *reinterpret_cast<float4 *>(&ws[e][c]) = v;
+    stage_chunk(0);
+    for (int c = 0; c < nck; ++c) {
+        if (c + 1 < nck) {
+            stage_chunk(c + 1);  // into the stage chunk c - 1 used (freed by the barrier below)
+            cp_async_wait_group<1>();
+        } else {
+            cp_async_wait_group<0>();
         }
         __syncthreads();
+        const float(*xs)[RT_KC] = reinterpret_cast<const float(*)[RT_KC]>(rt_smem + (c & 1) * STAGE);
+        const float(*ws)[RT_KC] = reinterpret_cast<const float(*)[RT_KC]>(rt_smem + (c & 1) * STAGE + RT_T * RT_KC);
+        const int kc = min(RT_KC, d - c * RT_KC);  // a multiple of 32
         for (int k = lane; k < kc; k += 32) {
             float xv[RT_T];
 #pragma unroll
@@ -196,6 +211,7 @@ __global__ void __launch_bounds__(256, 2) k_route_logits_tiled(RouterArgs a)
                     acc[i * RT_T + t] = fmaf(xv[t], wv, acc[i * RT_T + t]);
             }
         }
+        __syncthreads();  // every warp is done with stage c & 1 before chunk c + 2 refills it
     }
     float lo[32], hi[32];
 #pragma unroll
