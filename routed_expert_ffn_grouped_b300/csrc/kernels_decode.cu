@@ -13,8 +13,9 @@
 // router rows against a block of tokens, streamed in K-chunks), the shared expert's
 // gate/up items, the routed slots' gate/up items, then the down items slot by slot. Once
 // a device counter holds every logit task and every q8 group of x, each CTA selects the
-// experts of every token itself (the whole CTA by rank counting, or a warp per token when
-// the scores of all tokens do not fit), from the scores the logit items left in the
+// experts of every token itself (the whole CTA by rank counting, each group first ranked
+// within itself, or a warp per token when the scores of all tokens do not fit), from the
+// scores the logit items left in the
 // workspace, buckets the pairs into its shared memory and goes on to the routed items;
 // CTA 0 also writes the routing results out. CTA b's first item is item b; the counter
 // hands out the rest in order. A CTA processes its items in claim order and an item waits
@@ -26,7 +27,8 @@
 // latency hides behind the copies of the items before) and streams each item through a
 // ring of shared-memory stages with 1-D bulk copies (a stage holds 32 group tiles of each
 // of the two row blocks, with their scales: 40 KB), tagging each stage with the item and its
-// position; completion is counted on a "full" mbarrier per stage. For a down item it
+// position and leaving the decoded item beside it; completion is counted on a "full"
+// mbarrier per stage. For a down item it
 // also copies the item's rows of q8(h) into one of a few h buffers, once the gate/up
 // items of its slot are done, ahead of the consumers. The consumer warps split each
 // stage's groups; lane l owns row l of the block and reads its 16 bytes of a group tile
